@@ -1,0 +1,274 @@
+/*
+ * CPU oracle for the routed-expert Q4_K MoE FFN layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, fp64 statement of
+ * what the layer computes.  Only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg load it; the product path never does.  It
+ * shares no code, header or table with the CUDA library.
+ *
+ * What it follows (page title, then the item on the page):
+ *  - forward_qwen3_moe.rs (aprender-serve 0.35.0), step 2h of
+ *    forward_single_qwen3_moe_with_cache: the MoE FFN output is the gate x up
+ *    SwiGLU of each selected expert, weighted by the softmax-normalised top-k
+ *    router weights;
+ *  - same page, doc of forward_qwen3_moe ("Arguments", `data`): each
+ *    selected expert is a dequant+matvec over the Q4_K bytes in place;
+ *  - same page, step 2g of forward_qwen3_moe: every position goes through
+ *    the layer on its own (tokens are independent);
+ *  - forward_qwen3_moe_cuda_traced.rs (aprender-serve 0.34.0), doc of
+ *    forward_qwen3_moe_cuda_traced_with_plan: the router stage is the k
+ *    post-softmax, renormalised top-k weights, the output stage is [H];
+ *  - qwen3_moe_dispatch.rs (aprender-serve 0.70.2), doc of cpu_reference:
+ *    activations enter as exact fp32 values (no Q8_K quantisation).
+ * The Q4_K block layout is the GGUF format named by those pages ("Q4_K_M");
+ * the pages do not spell it out, so the field placement below is the format's
+ * public definition, restated.
+ *
+ * Readings where the pages leave a step open:
+ *  - softmax over all E logits, then the k largest probabilities in
+ *    descending order, equal values by lowest expert index; the k weights are
+ *    the selected probabilities divided by their sum;
+ *  - SiLU applies to the gate projection, SiLU(z) = z / (1 + exp(-z));
+ *    the up projection is linear; h = SiLU(g) * u; o = W_down h;
+ *  - y = sum over slots j = 0..k-1, in slot order, of w_j * o_j;
+ *  - a slot whose expert index is outside [0, E) contributes nothing and is
+ *    reported through the status count.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define QK 256
+#define BLK 144
+
+/* IEEE binary16 -> double, exactly, subnormals included. */
+static double half_bits_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 31;
+    int mant = h & 1023;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)mant, -24);            /* subnormal or zero */
+    else if (expo == 31)
+        v = mant ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + mant), expo - 25);
+    return sign ? -v : v;
+}
+
+/* The 6-bit scale and min of sub-block j (0..7) from the 12 packed bytes. */
+static void scale_min(const uint8_t *scales, int j, int *sc, int *m)
+{
+    if (j < 4) {
+        *sc = scales[j] & 63;
+        *m = scales[j + 4] & 63;
+    } else {
+        *sc = (scales[j + 4] & 15) | ((scales[j - 4] >> 6) << 4);
+        *m = (scales[j + 4] >> 4) | ((scales[j] >> 6) << 4);
+    }
+}
+
+/* Decode one 144-byte block into its 256 weights, in weight order. */
+void moq_decode_block(const uint8_t *blk, double *out)
+{
+    uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
+    uint16_t mbits = (uint16_t)(blk[2] | (blk[3] << 8));
+    double d = half_bits_to_double(dbits);
+    double dmin = half_bits_to_double(mbits);
+    const uint8_t *scales = blk + 4;
+    const uint8_t *qs = blk + 16;
+    for (int i = 0; i < QK; i++) {
+        int j = i / 32;               /* sub-block */
+        int c = i / 64;               /* 32-byte chunk of qs */
+        int l = i % 32;               /* position inside the sub-block */
+        int hi = (i % 64) >= 32;      /* second sub-block of the chunk -> high nibble */
+        uint8_t byte = qs[32 * c + l];
+        int q = hi ? (byte >> 4) : (byte & 15);
+        int sc, m;
+        scale_min(scales, j, &sc, &m);
+        out[i] = d * (double)sc * (double)q - dmin * (double)m;
+    }
+}
+
+/* Decode `nrows` rows of `ncols` weights (ncols a multiple of 256). */
+void moq_decode_rows(const uint8_t *blob, long nrows, int ncols, double *out)
+{
+    int nsb = ncols / QK;
+    for (long r = 0; r < nrows; r++)
+        for (int s = 0; s < nsb; s++)
+            moq_decode_block(blob + (r * nsb + s) * BLK, out + r * ncols + (long)s * QK);
+}
+
+/* Dot product of one Q4_K row (ncols weights) with a double vector. */
+static double row_dot(const uint8_t *row, int ncols, const double *v, double *tmp)
+{
+    int nsb = ncols / QK;
+    double acc = 0.0;
+    for (int s = 0; s < nsb; s++) {
+        moq_decode_block(row + (long)s * BLK, tmp);
+        for (int i = 0; i < QK; i++)
+            acc += tmp[i] * v[s * QK + i];
+    }
+    return acc;
+}
+
+/*
+ * Router: logits l = x Wr^T (+ bias), p = softmax over all E, the k largest
+ * p (ties -> lowest index) in descending order, w = p_sel / sum(p_sel).
+ * x [T,H], Wr [E,H] fp32, bias [E] fp32 or NULL.
+ * Outputs: logits [T,E] (biased, fp64), p [T,E], idx [T,k], w [T,k].
+ */
+void moq_router(const float *x, const float *Wr, const float *bias,
+                int T, int H, int E, int k,
+                double *logits, double *p, int32_t *idx, double *w)
+{
+#pragma omp parallel for schedule(dynamic)
+    for (int t = 0; t < T; t++) {
+        double *l = logits + (long)t * E;
+        double *pt = p + (long)t * E;
+        for (int e = 0; e < E; e++) {
+            double acc = 0.0;
+            for (int h = 0; h < H; h++)
+                acc += (double)x[(long)t * H + h] * (double)Wr[(long)e * H + h];
+            l[e] = acc + (bias ? (double)bias[e] : 0.0);
+        }
+        double mx = l[0];
+        for (int e = 1; e < E; e++)
+            if (l[e] > mx) mx = l[e];
+        double z = 0.0;
+        for (int e = 0; e < E; e++) {
+            pt[e] = exp(l[e] - mx);
+            z += pt[e];
+        }
+        for (int e = 0; e < E; e++)
+            pt[e] /= z;
+        /* selection by repeated maximum: strict '>' keeps the lowest index on ties */
+        char *taken = calloc((size_t)E, 1);
+        double sel_sum = 0.0;
+        for (int j = 0; j < k; j++) {
+            int best = -1;
+            for (int e = 0; e < E; e++)
+                if (!taken[e] && (best < 0 || pt[e] > pt[best]))
+                    best = e;
+            taken[best] = 1;
+            idx[(long)t * k + j] = best;
+            sel_sum += pt[best];
+        }
+        for (int j = 0; j < k; j++)
+            w[(long)t * k + j] = pt[idx[(long)t * k + j]] / sel_sum;
+        free(taken);
+    }
+}
+
+/*
+ * One expert applied to one activation row: g = W_gate x, u = W_up x,
+ * h = SiLU(g) * u, o = W_down h.  gate/up: [I rows x H], down: [H rows x I].
+ */
+void moq_expert(const double *xv, const uint8_t *gate_e, const uint8_t *up_e,
+                const uint8_t *down_e, int H, int I, double *h, double *o)
+{
+    int nsb_h = H / QK, nsb_i = I / QK;
+    double tmp[QK];
+    for (int r = 0; r < I; r++) {
+        double g = row_dot(gate_e + (long)r * nsb_h * BLK, H, xv, tmp);
+        double u = row_dot(up_e + (long)r * nsb_h * BLK, H, xv, tmp);
+        h[r] = g / (1.0 + exp(-g)) * u;
+    }
+    for (int r = 0; r < H; r++)
+        o[r] = row_dot(down_e + (long)r * nsb_i * BLK, I, h, tmp);
+}
+
+/*
+ * The FFN for the listed tokens (all T when `tokens` is NULL, else
+ * `ntok` entries of `tokens`): y[t] = sum_j w[t,j] * expert_{idx[t,j]}(x[t]).
+ * y is [T,H] (only the listed rows are written).  Returns the number of
+ * slots skipped for an out-of-range expert index.
+ */
+long moq_ffn(const float *x, const int32_t *idx, const double *w,
+             const uint8_t *gate, const uint8_t *up, const uint8_t *down,
+             int T, int H, int E, int k, int I,
+             const int32_t *tokens, int ntok, double *y)
+{
+    long gate_bytes = (long)I * (H / QK) * BLK;
+    long down_bytes = (long)H * (I / QK) * BLK;
+    int n = tokens ? ntok : T;
+    long skipped = 0;
+#pragma omp parallel for schedule(dynamic) reduction(+ : skipped)
+    for (int a = 0; a < n; a++) {
+        int t = tokens ? tokens[a] : a;
+        double *xv = malloc(sizeof(double) * (size_t)H);
+        double *h = malloc(sizeof(double) * (size_t)I);
+        double *o = malloc(sizeof(double) * (size_t)H);
+        double *yt = y + (long)t * H;
+        for (int i = 0; i < H; i++) {
+            xv[i] = (double)x[(long)t * H + i];
+            yt[i] = 0.0;
+        }
+        for (int j = 0; j < k; j++) {
+            int e = idx[(long)t * k + j];
+            if (e < 0 || e >= E) {
+                skipped++;
+                continue;
+            }
+            moq_expert(xv, gate + e * gate_bytes, up + e * gate_bytes, down + e * down_bytes,
+                       H, I, h, o);
+            double wj = w[(long)t * k + j];
+            for (int i = 0; i < H; i++)
+                yt[i] += wj * o[i];
+        }
+        free(xv);
+        free(h);
+        free(o);
+    }
+    return skipped;
+}
+
+/*
+ * Token->expert permutation: counts[e] = number of (t,j) slots routed to e,
+ * offs = exclusive prefix sum of counts (E+1 entries), perm = slot ids
+ * p = t*k + j ordered by (expert, p).  Out-of-range slots are left out.
+ */
+void moq_permutation(const int32_t *idx, int T, int k, int E,
+                     int32_t *counts, int32_t *offs, int32_t *perm)
+{
+    long n = (long)T * k;
+    for (int e = 0; e < E; e++)
+        counts[e] = 0;
+    for (long p = 0; p < n; p++)
+        if (idx[p] >= 0 && idx[p] < E)
+            counts[idx[p]]++;
+    offs[0] = 0;
+    for (int e = 0; e < E; e++)
+        offs[e + 1] = offs[e] + counts[e];
+    int32_t *cursor = malloc(sizeof(int32_t) * (size_t)E);
+    for (int e = 0; e < E; e++)
+        cursor[e] = offs[e];
+    for (long p = 0; p < n; p++)
+        if (idx[p] >= 0 && idx[p] < E)
+            perm[cursor[idx[p]]++] = (int32_t)p;
+    free(cursor);
+}
+
+void moq_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int moq_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

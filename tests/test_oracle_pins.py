@@ -1,0 +1,318 @@
+"""Pins of the fp64 oracle against facts fixed outside it.
+
+Each test checks the oracle against something it does not compute itself:
+hand-built Q4_K blocks, closed forms, special cases that reduce to a dense
+NumPy computation, brute force on tiny inputs, and NumPy's stable sort.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from quantized_routed_expert_02_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "q4k_blocks.json")
+
+
+def _silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+# ---------------------------------------------------------------- Q4_K decode
+
+def _golden_blocks():
+    with open(GOLDEN) as f:
+        return json.load(f)["blocks"]
+
+
+@pytest.mark.parametrize("blk", _golden_blocks(), ids=lambda b: b["name"])
+def test_hand_built_block(oracle, blk):
+    raw = np.frombuffer(bytes.fromhex(blk["hex"]), dtype=np.uint8)
+    assert raw.size == 144
+    got = oracle.decode_block(raw)
+    if "expect_runs16" in blk:
+        want = np.repeat(np.array(blk["expect_runs16"], dtype=np.float64), 16)
+    else:
+        want = np.tile(np.array(blk["expect_pattern64"], dtype=np.float64), 4)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_pack_decode_round_trip(oracle):
+    """Random fields -> synth's byte placement -> oracle decode recovers
+    d*sc*q - dmin*m exactly for every weight (pins the packer to the decoder)."""
+    rng = np.random.default_rng(7)
+    n = 64
+    d = rng.normal(0, 1e-2, n).astype(np.float16)
+    dmin = np.abs(rng.normal(0, 1e-2, n)).astype(np.float16)
+    sc = rng.integers(0, 64, (n, 8))
+    m = rng.integers(0, 64, (n, 8))
+    q = rng.integers(0, 16, (n, 256))
+    blocks = synth.pack_blocks(d, dmin, sc, m, synth.pack_nibbles(q))
+    for b in range(n):
+        got = oracle.decode_block(blocks[b])
+        j = np.arange(256) // 32
+        want = (float(d[b]) * sc[b][j].astype(np.float64) * q[b]
+                - float(dmin[b]) * m[b][j].astype(np.float64))
+        np.testing.assert_array_equal(got, want)
+
+
+def test_decode_rows_matches_blockwise(oracle):
+    rng = np.random.default_rng(3)
+    rows, ncols = 3, 512
+    blob = synth.random_blocks(rng, rows * 2).reshape(-1)
+    dense = oracle.decode_rows(blob, rows, ncols)
+    for r in range(rows):
+        for s in range(2):
+            np.testing.assert_array_equal(
+                dense[r, 256 * s:256 * (s + 1)],
+                oracle.decode_block(blob[(r * 2 + s) * 144:(r * 2 + s + 1) * 144]))
+
+
+def test_generated_fields_in_range(oracle):
+    """Generated blocks have sc in 1..63 (never 0): every weight of a block
+    with all codes forced to 0 must be -dmin*m, and with codes 15 the spread
+    d*sc*15 must be positive."""
+    rng = np.random.default_rng(11)
+    blk = synth.random_blocks(rng, 32).copy()
+    blk[:, 16:] = 0xFF
+    for b in range(32):
+        w15 = oracle.decode_block(blk[b])
+        blk0 = blk[b].copy()
+        blk0[16:] = 0
+        w0 = oracle.decode_block(blk0)
+        spread = (w15 - w0).reshape(8, 32)
+        assert np.all(spread > 0)
+        assert np.all(w0 <= 0)
+
+
+# ---------------------------------------------------------------- router
+
+def test_router_closed_form(oracle):
+    # logits 0, ln2, ln3 -> p = 1/6, 2/6, 3/6; top-2 = [2, 1]; w = [3/5, 2/5]
+    x = np.ones((1, 1), np.float32)
+    Wr = np.array([[0.0], [math.log(2)], [math.log(3)]], np.float32)
+    r = oracle.router(x, Wr, None, 2)
+    assert r["idx"].tolist() == [[2, 1]]
+    np.testing.assert_allclose(r["w"], [[0.6, 0.4]], atol=1e-7)
+    np.testing.assert_allclose(r["p"], [[1 / 6, 2 / 6, 3 / 6]], atol=1e-7)
+
+
+def test_router_ties_lowest_index(oracle):
+    x = np.ones((1, 4), np.float32)
+    Wr = np.zeros((6, 4), np.float32)
+    Wr[3] = 1.0
+    r = oracle.router(x, Wr, None, 3)
+    # expert 3 first, then the tied zeros by lowest index
+    assert r["idx"].tolist() == [[3, 0, 1]]
+    e4 = math.exp(4.0)
+    np.testing.assert_allclose(r["w"], [[e4 / (e4 + 2), 1 / (e4 + 2), 1 / (e4 + 2)]], rtol=1e-12)
+
+
+def test_router_weights_sum_to_one_and_sorted(oracle):
+    rng = np.random.default_rng(5)
+    T, H, E, k = 33, 256, 16, 4
+    x = rng.normal(0, 1, (T, H)).astype(np.float32)
+    Wr = rng.normal(0, 0.05, (E, H)).astype(np.float32)
+    r = oracle.router(x, Wr, None, k)
+    np.testing.assert_allclose(r["w"].sum(1), 1.0, atol=1e-12)
+    assert np.all(np.diff(r["w"], axis=1) <= 0)
+
+
+def test_router_topk_matches_brute_force(oracle):
+    rng = np.random.default_rng(9)
+    T, H, E, k = 40, 512, 32, 6
+    x = rng.normal(0, 1, (T, H)).astype(np.float32)
+    Wr = rng.normal(0, 0.05, (E, H)).astype(np.float32)
+    b = rng.normal(0, 0.5, E).astype(np.float32)
+    r = oracle.router(x, Wr, b, k)
+    logits = x.astype(np.float64) @ Wr.astype(np.float64).T + b.astype(np.float64)
+    np.testing.assert_allclose(r["logits"], logits, rtol=1e-12, atol=1e-12)
+    for t in range(T):
+        order = np.lexsort((np.arange(E), -logits[t]))   # value desc, index asc
+        assert r["idx"][t].tolist() == order[:k].tolist()
+        p = np.exp(logits[t] - logits[t].max())
+        p /= p.sum()
+        sel = p[order[:k]]
+        np.testing.assert_allclose(r["w"][t], sel / sel.sum(), rtol=1e-12)
+
+
+def test_router_k_equals_E_is_dense_softmax(oracle):
+    rng = np.random.default_rng(12)
+    x = rng.normal(0, 1, (5, 256)).astype(np.float32)
+    Wr = rng.normal(0, 0.1, (8, 256)).astype(np.float32)
+    r = oracle.router(x, Wr, None, 8)
+    logits = x.astype(np.float64) @ Wr.astype(np.float64).T
+    sm = np.exp(logits - logits.max(1, keepdims=True))
+    sm /= sm.sum(1, keepdims=True)
+    for t in range(5):
+        np.testing.assert_allclose(r["w"][t], sm[t][r["idx"][t]], rtol=1e-12)
+        assert sorted(r["idx"][t].tolist()) == list(range(8))
+
+
+# ---------------------------------------------------------------- FFN
+
+def _tiny_layer(H=256, I=256, E=8, seed=21):
+    shape = synth.custom_shape(1, H, E, 2, I, cfg_id=90 + seed % 7)
+    blobs = synth.expert_blobs(shape, 0)
+    return shape, blobs
+
+
+def _dense(oracle, shape, blobs, e):
+    H, I = shape.H, shape.I
+    g = oracle.decode_rows(blobs["gate"][e * shape.gate_bytes:(e + 1) * shape.gate_bytes], I, H)
+    u = oracle.decode_rows(blobs["up"][e * shape.gate_bytes:(e + 1) * shape.gate_bytes], I, H)
+    d = oracle.decode_rows(blobs["down"][e * shape.down_bytes:(e + 1) * shape.down_bytes], H, I)
+    return g, u, d
+
+
+def _dense_ffn(gud, xv):
+    g, u, d = gud
+    return d @ (_silu(g @ xv) * (u @ xv))
+
+
+def test_ffn_brute_force_tiny(oracle):
+    shape, blobs = _tiny_layer()
+    rng = np.random.default_rng(1)
+    T, k = 3, 2
+    x = rng.normal(0, 1, (T, shape.H)).astype(np.float32)
+    idx = np.array([[1, 6], [3, 3], [7, 0]], np.int32)
+    w = np.array([[0.7, 0.3], [0.25, 0.75], [0.5, 0.5]])
+    y, skipped = oracle.ffn(x, idx, w, blobs["gate"], blobs["up"], blobs["down"], shape.E, shape.I)
+    assert skipped == 0
+    dense = {e: _dense(oracle, shape, blobs, e) for e in set(idx.ravel().tolist())}
+    for t in range(T):
+        want = sum(w[t, j] * _dense_ffn(dense[idx[t, j]], x[t].astype(np.float64)) for j in range(k))
+        np.testing.assert_allclose(y[t], want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
+
+
+def test_ffn_k_equals_E_is_dense_mixture(oracle):
+    shape, blobs = _tiny_layer(E=4, seed=2)
+    rng = np.random.default_rng(2)
+    x = rng.normal(0, 1, (2, shape.H)).astype(np.float32)
+    Wr = rng.normal(0, 0.05, (4, shape.H)).astype(np.float32)
+    r = oracle.layer(x, Wr, None, 4, blobs["gate"], blobs["up"], blobs["down"], 4, shape.I)
+    logits = x.astype(np.float64) @ Wr.astype(np.float64).T
+    for t in range(2):
+        p = np.exp(logits[t] - logits[t].max())
+        p /= p.sum()
+        want = sum(p[e] * _dense_ffn(_dense(oracle, shape, blobs, e), x[t].astype(np.float64))
+                   for e in range(4))
+        np.testing.assert_allclose(r["y"][t], want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
+
+
+def test_ffn_k1_is_single_expert(oracle):
+    shape, blobs = _tiny_layer(seed=3)
+    rng = np.random.default_rng(3)
+    x = rng.normal(0, 1, (2, shape.H)).astype(np.float32)
+    Wr = rng.normal(0, 0.05, (shape.E, shape.H)).astype(np.float32)
+    r = oracle.layer(x, Wr, None, 1, blobs["gate"], blobs["up"], blobs["down"], shape.E, shape.I)
+    assert np.all(r["w"] == 1.0)
+    logits = x.astype(np.float64) @ Wr.astype(np.float64).T
+    for t in range(2):
+        e = int(np.argmax(logits[t]))
+        assert r["idx"][t, 0] == e
+        want = _dense_ffn(_dense(oracle, shape, blobs, e), x[t].astype(np.float64))
+        np.testing.assert_allclose(r["y"][t], want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
+
+
+def test_ffn_one_hot_router(oracle):
+    """A logit gap of 1000 makes every other probability underflow to 0, so
+    k=2 reduces to one dense SwiGLU FFN of the favoured expert."""
+    shape, blobs = _tiny_layer(seed=4)
+    rng = np.random.default_rng(4)
+    x = rng.normal(0, 1, (1, shape.H)).astype(np.float32)
+    Wr = rng.normal(0, 0.05, (shape.E, shape.H)).astype(np.float32)
+    bias = np.zeros(shape.E, np.float32)
+    bias[5] = 1000.0
+    r = oracle.layer(x, Wr, bias, 2, blobs["gate"], blobs["up"], blobs["down"], shape.E, shape.I)
+    assert r["idx"][0, 0] == 5
+    assert r["w"][0, 0] == 1.0 and r["w"][0, 1] == 0.0
+    want = _dense_ffn(_dense(oracle, shape, blobs, 5), x[0].astype(np.float64))
+    np.testing.assert_allclose(r["y"][0], want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
+
+
+def test_ffn_out_of_range_slot_contributes_nothing(oracle):
+    shape, blobs = _tiny_layer(seed=5)
+    rng = np.random.default_rng(5)
+    x = rng.normal(0, 1, (1, shape.H)).astype(np.float32)
+    idx = np.array([[2, 99]], np.int32)
+    y, skipped = oracle.ffn(x, idx, np.array([[0.5, 0.5]]), blobs["gate"], blobs["up"],
+                            blobs["down"], shape.E, shape.I)
+    assert skipped == 1
+    want = 0.5 * _dense_ffn(_dense(oracle, shape, blobs, 2), x[0].astype(np.float64))
+    np.testing.assert_allclose(y[0], want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
+
+
+def test_ffn_token_subset_matches_full(oracle):
+    shape, blobs = _tiny_layer(seed=6)
+    rng = np.random.default_rng(6)
+    x = rng.normal(0, 1, (5, shape.H)).astype(np.float32)
+    idx = rng.integers(0, shape.E, (5, 2)).astype(np.int32)
+    w = rng.random((5, 2))
+    full, _ = oracle.ffn(x, idx, w, blobs["gate"], blobs["up"], blobs["down"], shape.E, shape.I)
+    part, _ = oracle.ffn(x, idx, w, blobs["gate"], blobs["up"], blobs["down"], shape.E, shape.I,
+                         tokens=np.array([4, 1]))
+    np.testing.assert_array_equal(part[[4, 1]], full[[4, 1]])
+    assert np.isnan(part[0]).all()
+
+
+def test_silu_closed_form(oracle):
+    """One weight row per matrix: with H = I = 256 and an expert whose gate,
+    up and down rows are known, h = SiLU(g)*u and y = w * down . h."""
+    H = I = 256
+    # every gate/up weight = 1/128 (d=2^-7, sc=1, q=1, dmin=0); down weight = 2 (d=2, sc=1, q=1)
+    def block(d_bits):
+        b = np.zeros(144, np.uint8)
+        b[0], b[1] = d_bits & 0xFF, d_bits >> 8
+        b[4:8] = 1
+        b[12:16] = 1
+        b[16:] = 0x11
+        return b
+    g_blk = block(0x2000)   # 2^-7
+    d_blk = block(0x4000)   # 2.0
+    gate = np.tile(g_blk, I)
+    down = np.tile(d_blk, H)
+    xv = np.full(H, 0.5, np.float32)
+    h, o = oracle.expert(xv, gate, gate, down, H, I)
+    g = 256 * 0.5 / 128.0     # = 1.0
+    want_h = g / (1 + math.exp(-g)) * g
+    np.testing.assert_allclose(h, want_h, rtol=1e-15)
+    np.testing.assert_allclose(o, 2.0 * 256 * want_h, rtol=1e-14)
+
+
+# ---------------------------------------------------------------- permutation
+
+def test_permutation_invariants(oracle):
+    rng = np.random.default_rng(8)
+    T, k, E = 300, 4, 16
+    idx = rng.integers(0, E, (T, k)).astype(np.int32)
+    counts, offs, perm = oracle.permutation(idx, E)
+    flat = idx.ravel()
+    np.testing.assert_array_equal(counts, np.bincount(flat, minlength=E))
+    assert offs[0] == 0 and np.all(np.diff(offs) == counts) and offs[-1] == T * k
+    np.testing.assert_array_equal(perm, np.argsort(flat, kind="stable"))
+    assert sorted(perm.tolist()) == list(range(T * k))
+
+
+def test_permutation_skips_out_of_range(oracle):
+    idx = np.array([[0, 5], [9, 0], [-1, 2]], np.int32)
+    counts, offs, perm = oracle.permutation(idx, 6)
+    assert counts.tolist() == [2, 0, 1, 0, 0, 1]
+    assert perm.tolist() == [0, 3, 5, 1]
+
+
+@pytest.mark.parametrize("H,I", [(512, 256), (256, 512)])
+def test_ffn_brute_force_rectangular(oracle, H, I):
+    shape = synth.custom_shape(1, H, 4, 2, I, cfg_id=97)
+    blobs = synth.expert_blobs(shape, 0)
+    rng = np.random.default_rng(H + I)
+    x = rng.normal(0, 1, (2, H)).astype(np.float32)
+    idx = np.array([[3, 1], [0, 2]], np.int32)
+    w = np.array([[0.9, 0.1], [0.4, 0.6]])
+    y, _ = oracle.ffn(x, idx, w, blobs["gate"], blobs["up"], blobs["down"], 4, I)
+    for t in range(2):
+        want = sum(w[t, j] * _dense_ffn(_dense(oracle, shape, blobs, idx[t, j]),
+                                        x[t].astype(np.float64)) for j in range(2))
+        np.testing.assert_allclose(y[t], want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
