@@ -1,0 +1,400 @@
+#!/usr/bin/env python
+"""Throughput of the routed-expert Q4_K MoE FFN layer on GB300.
+
+One step is one pass of the layer (router -> permutation -> gate/up+SwiGLU
+-> down -> slot-ordered combine) over every layer of a rotation of
+independently seeded layers, i.e. `layers` calls of moe_layer with T tokens
+each.  The rotation's weights (48 x 340 MB for the Qwen3-30B-A3B shape) are
+far larger than L2, and consecutive uses of one layer are separated by every
+other layer's traffic, so no L2 flush is needed.
+
+Prints one JSON line (rank 0).  `value` is MoE-FFN tokens per second through
+one layer (T * layers_per_step * steps / time, summed over ranks); the
+roofline object compares the achieved algorithmic bytes per call (unique
+selected experts' Q4_K bytes + x + y + idx + w) with the measured HBM copy
+bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from quantized_routed_expert_02_gb300 import synth  # noqa: E402
+
+DEFAULT_CONFIG = "a3b_decode"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.SHAPES))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=0, help="override the rotation length")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="bound on the oracle's CPU-baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- inputs
+
+def _gen_layer(job):
+    name, layer, rank = job
+    shape = synth.SHAPES[name]
+    blobs = synth.expert_blobs(shape, layer)
+    Wr = synth.router_weights(shape, layer)
+    x = synth.activations_fast(shape, layer + 7919 * rank)
+    return layer, x, Wr, blobs
+
+
+def generate(name, n_layers, rank, workers):
+    import multiprocessing as mp
+    jobs = [(name, layer, rank) for layer in range(n_layers)]
+    if workers <= 1 or n_layers == 1:
+        for j in jobs:
+            yield _gen_layer(j)
+        return
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers) as pool:
+        for r in pool.imap(_gen_layer, jobs):
+            yield r
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(",") for ln in self.file.read().splitlines() if ln.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                smax = float(r[1])
+                for nm, v in zip(names, r[4:8]):
+                    if v.strip().lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- oracle (CPU) timing
+
+def oracle_sample(name, seconds, layers_available, rank=0):
+    """Time the fp64 oracle on whole layer calls of the workload until
+    `seconds` of CPU time have been spent (at least one call)."""
+    from oracle.oracle import Oracle
+    shape = synth.SHAPES[name]
+    o = Oracle()
+    calls, t_total, layer = 0, 0.0, 0
+    T = shape.T
+    tokens = None
+    if T > 64:
+        # prefill: a bounded token subset of one layer per call
+        tokens = np.arange(0, T, max(1, T // 64), dtype=np.int32)[:64]
+    while True:
+        _, x, Wr, blobs = _gen_layer((name, layer % max(1, layers_available), rank))
+        bias = synth.router_bias(shape)
+        t0 = time.perf_counter()
+        r = o.router(x, Wr, bias, shape.k)
+        o.ffn(x, r["idx"], r["w"], blobs["gate"], blobs["up"], blobs["down"], shape.E, shape.I,
+              tokens=tokens)
+        t_total += time.perf_counter() - t0
+        calls += 1
+        layer += 1
+        if t_total >= seconds:
+            break
+    ntok = T if tokens is None else len(tokens)
+    threads = min(o.max_threads(), ntok)
+    return {
+        "value": ntok * calls / t_total,
+        "unit": "tokens/s",
+        "cores": threads,
+        "kind": "oracle",
+        "sample": (f"{calls} layer call(s) of {name} (T={T}"
+                   + (f", FFN on {ntok} of {T} tokens, router on all" if tokens is not None else "")
+                   + f"), fp64 C oracle, {t_total:.1f} s"),
+    }
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    shape = synth.SHAPES[args.config]
+    times = []
+    last = None
+    for step in range(args.warmup + args.steps):
+        last = oracle_sample(args.config, 0.0, 1, 0)
+        if step >= args.warmup:
+            times.append(last["value"])
+    value = statistics.median(times)
+    line = {
+        "impl": "reference", "metric": "MoE FFN tokens/s (one layer)", "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.config, "T": shape.T, "H": shape.H, "E": shape.E,
+                   "k": shape.k, "I": shape.I},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": last["cores"],
+                         "kind": "oracle", "sample": "each step: " + last["sample"]},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    shape = synth.SHAPES[args.config]
+    n_layers = args.layers or shape.layers
+    workers = max(1, min(16, (os.cpu_count() or 2) // max(1, world)))
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    from quantized_routed_expert_02_gb300 import moeq4k as m
+
+    T, H, E, k, I = shape.T, shape.H, shape.E, shape.k, shape.I
+    layers = []
+    t_gen = time.perf_counter()
+    for layer, x, Wr, blobs in generate(args.config, n_layers, rank, workers):
+        L = dict(
+            x=torch.from_numpy(x).to(dev),
+            x_host=torch.from_numpy(x).pin_memory(),
+            Wr=torch.from_numpy(Wr).to(dev),
+            gate=torch.from_numpy(blobs["gate"]).to(dev),
+            up=torch.from_numpy(blobs["up"]).to(dev),
+            down=torch.from_numpy(blobs["down"]).to(dev),
+            idx=torch.empty(T, k, dtype=torch.int32, device=dev),
+            w=torch.empty(T, k, dtype=torch.float32, device=dev),
+            y=torch.empty(T, H, dtype=torch.float32, device=dev),
+        )
+        layers.append(L)
+        del blobs
+    t_gen = time.perf_counter() - t_gen
+    b = synth.router_bias(shape)
+    bias = None if b is None else torch.from_numpy(b).to(dev)
+    ws = m.alloc_workspace(T, H, E, k, I, device=dev)
+    ws_host = m.alloc_workspace(T, H, E, k, I, device=dev, host_staging=True)
+    y_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def one_step(s):
+        for L in layers:
+            m.moe_layer(L["x"], L["Wr"], bias, L["gate"], L["up"], L["down"], k, I,
+                        L["idx"], L["w"], L["y"], ws, stream=s)
+
+    # eager warm-up, then capture one step (the whole rotation) as a CUDA graph
+    with torch.cuda.stream(stream):
+        one_step(stream)
+    stream.synchronize()
+    code, detail = m.moe_read_device_status(ws, stream)
+    if code != 0:
+        raise RuntimeError(f"device status {m.status_str(code)} ({detail})")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        one_step(stream)
+
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # algorithmic bytes of one step, from the routing each call made
+    per_expert = 2 * shape.gate_bytes + shape.down_bytes
+    act_bytes = T * H * 4 * 2 + T * k * 8
+    step_bytes = 0
+    uniques = []
+    for L in layers:
+        u = int(torch.unique(L["idx"]).numel())
+        uniques.append(u)
+        step_bytes += u * per_expert + act_bytes
+    wr_bytes = n_layers * E * H * 4
+
+    gpu_id = 0
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        gpu_id = str(props.uuid)
+        if not gpu_id.startswith("GPU-"):
+            gpu_id = "GPU-" + gpu_id
+    except Exception:
+        gpu_id = str(local_rank)
+    clocks = ClockSampler(gpu_id)
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    tokens_per_step = T * n_layers
+    value = tokens_per_step * args.steps * world / (ms / 1e3)
+
+    # end to end through the host-buffer entry point (copies inside the timed region)
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(1, min(args.steps, 10))
+        for L in layers[:2]:
+            m.moe_layer_host(L["x_host"], L["Wr"], bias, L["gate"], L["up"], L["down"], k, I,
+                             L["idx"], L["w"], y_host, ws_host, stream=stream)
+        if dist is not None:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            for L in layers:
+                m.moe_layer_host(L["x_host"], L["Wr"], bias, L["gate"], L["up"], L["down"], k, I,
+                                 L["idx"], L["w"], y_host, ws_host, stream=stream)
+        dt = time.perf_counter() - t0
+        if dist is not None:
+            t = torch.tensor([dt], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": T * n_layers * e2e_steps * world / dt, "unit": "tokens/s",
+               "h2d_bytes_per_step": n_layers * T * H * 4,
+               "d2h_bytes_per_step": n_layers * T * H * 4}
+
+    peak, peak_kind = measured_peaks()
+    call_us = ms_per_step * 1e3 / n_layers
+    achieved = (step_bytes / n_layers) / (call_us * 1e-6) / 1e9
+    roofline = {
+        "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+        "frac": round(achieved / peak, 4), "traffic": None,
+        "kernel": "moe_layer call (all launches of one call)",
+        "peak_kind": peak_kind,
+        "algorithmic_bytes_per_call": step_bytes / n_layers,
+        "achieved_incl_router_weight": round(
+            ((step_bytes + wr_bytes) / n_layers) / (call_us * 1e-6) / 1e9, 1),
+    }
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = oracle_sample(args.config, args.cpu_seconds, n_layers, rank)
+
+    launches = m.moe_layer_launch_count(T, H, E, k, I) * n_layers * args.steps
+    if rank == 0:
+        line = {
+            "metric": "MoE FFN tokens/s (one layer)",
+            "value": round(value, 1),
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5),
+            "us_per_layer_call": round(call_us, 3),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": {
+                "workload": args.config, "T": T, "H": H, "E": E, "k": k, "I": I,
+                "layers_per_step": n_layers, "weights": "Q4_K",
+                "unique_experts_per_call": round(sum(uniques) / len(uniques), 2),
+                "l2": "inputs larger than L2 (layer rotation, no flush)",
+                "parallelism": f"replicas x{world}",
+                "graph": "one CUDA graph per step",
+                "input_gen_s": round(t_gen, 1),
+            },
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+/*
+ * moeq4k — routed-expert MoE FFN over GGUF Q4_K expert weights, for one GB300
+ * (sm_103a).  C ABI.
+ *
+ * The operation is one Qwen3-MoE routed-expert FFN layer
+ * (forward_qwen3_moe.rs, aprender-serve 0.35.0, step 2h of
+ * forward_single_qwen3_moe_with_cache and step 2g of forward_qwen3_moe):
+ *
+ *   router:   l[t,e] = sum_h x[t,h] Wr[e,h] (+ bias[e])
+ *             p[t,:] = softmax over all E experts of l[t,:]
+ *             idx[t,0..k) = the k largest p, descending, ties -> lowest index
+ *             w[t,j] = p[t,idx[t,j]] / sum_j' p[t,idx[t,j']]
+ *             (forward_qwen3_moe_cuda_traced.rs, aprender-serve 0.34.0, doc of
+ *             forward_qwen3_moe_cuda_traced_with_plan: the router stage is the
+ *             k post-softmax, renormalised top-k weights)
+ *   expert e: g = Wg[e] x, u = Wu[e] x, h = SiLU(g) * u, o = Wd[e] h,
+ *             SiLU(z) = z / (1 + exp(-z))
+ *   output:   y[t] = sum over slots j = 0..k-1, in slot order, of w[t,j] o_{t,j}
+ *             (the output stage is [H] per token)
+ *
+ * Each expert matrix is consumed in place in the Q4_K block format (fused
+ * dequant + matvec; forward_qwen3_moe.rs, doc of forward_qwen3_moe, argument
+ * `data`).  Activations are fp32 and are not quantised
+ * (qwen3_moe_dispatch.rs, aprender-serve 0.70.2, doc of cpu_reference).
+ *
+ * Q4_K block: 144 bytes per 256 weights — fp16 d, fp16 dmin, 12 bytes of
+ * packed 6-bit scales sc[8] and mins m[8], 128 bytes of 4-bit codes q;
+ * weight = d * sc[j] * q - dmin * m[j] for sub-block j (32 weights).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_dev are device pointers, owned by the caller, never
+ *    freed or retained by the library.  Expert blobs are borrowed in place.
+ *  - Every device pointer must be 16-byte aligned; the workspace 256-byte
+ *    aligned.
+ *  - Row-major layouts: x [T,H] fp32, Wr [E,H] fp32, bias [E] fp32,
+ *    idx [T,k] int32, w [T,k] fp32, y [T,H] fp32.
+ *    gate/up blobs: [E][I rows][H/256 blocks] x 144 B; down blob:
+ *    [E][H rows][I/256 blocks] x 144 B (blocks contiguous along the
+ *    reduction dimension, rows contiguous, experts contiguous).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *    Calls only enqueue work on it: they never allocate, free or
+ *    synchronise, except moe_read_device_status (which synchronises the
+ *    stream) and moe_layer_host (which synchronises before returning).
+ *  - Argument errors are returned before anything is enqueued.  Problems
+ *    only the device can see (an expert index outside [0,E) in a
+ *    caller-given idx) are recorded in a sticky status word inside the
+ *    workspace; the offending slot contributes nothing to y.  Read the word
+ *    with moe_read_device_status, reset it with moe_workspace_init.
+ *  - Limits: 1 <= T, 1 <= k <= E <= 256, k <= 32, H and I multiples of 256,
+ *    H <= 8192, I <= 8192, T*k <= 2^22.  Shapes outside them return
+ *    MOE_ERR_INVALID_SHAPE (forward_qwen3_moe.rs, forward_qwen3_moe: an
+ *    incomplete or mismatched MoE shape is an InvalidShape error).
+ */
+#ifndef MOEQ4K_H
+#define MOEQ4K_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_SHAPE = 1,  /* a dimension is out of range or inconsistent */
+    MOE_ERR_NULL = 2,           /* a required pointer is NULL */
+    MOE_ERR_MISALIGNED = 3,     /* a pointer breaks the alignment rule */
+    MOE_ERR_WORKSPACE = 4,      /* workspace smaller than moe_workspace_bytes() */
+    MOE_ERR_EXPERT_RANGE = 5,   /* device saw an expert index outside [0,E) */
+    MOE_ERR_TIMEOUT = 6,        /* a bounded device-side wait expired */
+    MOE_ERR_CUDA = 7            /* the CUDA runtime reported an error */
+} moe_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+MOE_API const char *moe_status_str(moe_status s);
+
+/* Library version as major*10000 + minor*100 + patch. */
+MOE_API int moe_version(void);
+
+/*
+ * Bytes of device workspace that moe_router / moe_permute / moe_ffn /
+ * moe_layer need for this shape (0 when the shape is invalid).  The
+ * workspace holds the sticky status word, the permutation, the expert
+ * activations h [T*k, I] and the per-slot outputs [T*k, H].
+ */
+MOE_API size_t moe_workspace_bytes(int T, int H, int E, int k, int I);
+
+/*
+ * Number of kernel launches one moe_layer call enqueues for this shape
+ * (0 when the shape is invalid); moe_ffn enqueues all but the router's.
+ */
+MOE_API int moe_layer_launch_count(int T, int H, int E, int k, int I);
+
+/*
+ * Zero the workspace header (status word and counters).  Call once after
+ * allocating a workspace and whenever the sticky status should be cleared.
+ * Enqueued on `stream`.
+ */
+MOE_API moe_status moe_workspace_init(void *ws_dev, size_t ws_bytes, void *stream);
+
+/*
+ * Router (logits, softmax, top-k, renormalise) for T tokens.
+ *  x_dev [T,H] fp32, Wr_dev [E,H] fp32, bias_dev [E] fp32 or NULL.
+ *  Writes idx_dev [T,k] int32 (descending logit, ties -> lowest index) and
+ *  w_dev [T,k] fp32 (sums to 1 per token).
+ */
+MOE_API moe_status moe_router(const float *x_dev, const float *Wr_dev, const float *bias_dev,
+                      int T, int H, int E, int k,
+                      int32_t *idx_dev, float *w_dev,
+                      void *ws_dev, size_t ws_bytes, void *stream);
+
+/*
+ * Token->expert permutation of a routing: counts_dev [E], offs_dev [E+1]
+ * (exclusive prefix sum of counts) and perm_dev [T*k] = slot ids p = t*k+j
+ * grouped by expert, ascending p within an expert (stable).  Slots whose
+ * expert index is outside [0,E) are left out (perm has offs[E] valid
+ * entries) and set the sticky status.
+ */
+MOE_API moe_status moe_permute(const int32_t *idx_dev, int T, int k, int E,
+                       int32_t *counts_dev, int32_t *offs_dev, int32_t *perm_dev,
+                       void *ws_dev, size_t ws_bytes, void *stream);
+
+/*
+ * Expert FFN and combine for a given routing.
+ *  x_dev [T,H] fp32; idx_dev [T,k] int32; w_dev [T,k] fp32 (any values;
+ *  they need not sum to 1); gate/up/down: Q4_K blobs as above.
+ *  Writes y_dev [T,H] fp32: y[t] = sum_j w[t,j] * expert_{idx[t,j]}(x[t]),
+ *  summed in slot order j = 0..k-1.  Duplicate experts in a row are legal.
+ */
+MOE_API moe_status moe_ffn(const float *x_dev, const int32_t *idx_dev, const float *w_dev,
+                   const void *gate_dev, const void *up_dev, const void *down_dev,
+                   int T, int H, int E, int k, int I, float *y_dev,
+                   void *ws_dev, size_t ws_bytes, void *stream);
+
+/*
+ * The whole layer: moe_router then moe_ffn.  idx_dev / w_dev receive the
+ * routing (the router stage), y_dev the output stage.
+ */
+MOE_API moe_status moe_layer(const float *x_dev, const float *Wr_dev, const float *bias_dev,
+                     const void *gate_dev, const void *up_dev, const void *down_dev,
+                     int T, int H, int E, int k, int I,
+                     int32_t *idx_dev, float *w_dev, float *y_dev,
+                     void *ws_dev, size_t ws_bytes, void *stream);
+
+/*
+ * The whole layer for a caller whose activations live in host memory:
+ * copies x_host [T,H] fp32 to the device, runs moe_layer, copies y back to
+ * y_host [T,H] fp32, and synchronises `stream` before returning.  Page-locked
+ * host buffers make the copies asynchronous DMA; pageable ones work too.
+ * Device staging for x and y lives in the workspace: size it with
+ * moe_workspace_bytes_host().  idx_dev / w_dev are device outputs as in
+ * moe_layer.
+ */
+MOE_API size_t moe_workspace_bytes_host(int T, int H, int E, int k, int I);
+MOE_API moe_status moe_layer_host(const float *x_host, const float *Wr_dev, const float *bias_dev,
+                          const void *gate_dev, const void *up_dev, const void *down_dev,
+                          int T, int H, int E, int k, int I,
+                          int32_t *idx_dev, float *w_dev, float *y_host,
+                          void *ws_dev, size_t ws_bytes, void *stream);
+
+/*
+ * Synchronise `stream`, then return the first device-side error recorded in
+ * the workspace since the last moe_workspace_init (MOE_OK if none).  If
+ * `detail` is not NULL it receives the offending value (e.g. the expert
+ * index seen).
+ */
+MOE_API moe_status moe_read_device_status(const void *ws_dev, void *stream, int32_t *detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEQ4K_H */

@@ -1,0 +1,239 @@
+// C ABI of the moeq4k library: argument checks, workspace carving and launch
+// order.  Every entry point checks its arguments before anything is enqueued
+// and returns a moe_status; nothing here allocates device memory.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+using namespace moeq4k;
+
+namespace {
+
+struct DevInfo {
+    bool ready = false;
+    int sms = 0;
+};
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+// Per-device one-time set-up (kernel attributes, SM count) for the current device.
+moe_status device_info(int *sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_dev[dev].ready) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (init_expert_ffn() != cudaSuccess) return MOE_ERR_CUDA;
+        g_dev[dev].sms = n;
+        g_dev[dev].ready = true;
+    }
+    *sms = g_dev[dev].sms;
+    return MOE_OK;
+}
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status check_shape(int T, int H, int E, int k, int I) {
+    if (T < 1 || H < 1 || E < 1 || k < 1 || I < 1) return MOE_ERR_INVALID_SHAPE;
+    if (k > E || E > kMaxE || k > kMaxK) return MOE_ERR_INVALID_SHAPE;
+    if (H % kQK != 0 || I % kQK != 0 || H > kMaxHI || I > kMaxHI) return MOE_ERR_INVALID_SHAPE;
+    if (int64_t(T) * k > (int64_t(1) << 22)) return MOE_ERR_INVALID_SHAPE;
+    return MOE_OK;
+}
+
+moe_status check_ptr(const void *p, size_t align) {
+    if (p == nullptr) return MOE_ERR_NULL;
+    if (!aligned(p, align)) return MOE_ERR_MISALIGNED;
+    return MOE_OK;
+}
+
+#define MOE_TRY(expr)                        \
+    do {                                     \
+        moe_status _s = (expr);              \
+        if (_s != MOE_OK) return _s;         \
+    } while (0)
+
+struct Ws {
+    uint8_t *base;
+    WsLayout L;
+    WsHeader *hdr() const { return reinterpret_cast<WsHeader *>(base); }
+    int32_t *i32(size_t off) const { return reinterpret_cast<int32_t *>(base + off); }
+    float *f32(size_t off) const { return reinterpret_cast<float *>(base + off); }
+};
+
+moe_status check_ws(void *ws, size_t ws_bytes, const WsLayout &L) {
+    MOE_TRY(check_ptr(ws, 256));
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status ffn_enqueue(const float *x, const int32_t *idx, const float *w, const void *gate,
+                       const void *up, const void *down, int T, int H, int E, int k, int I,
+                       float *y, const Ws &ws, int sms, cudaStream_t s) {
+    const WsLayout &L = ws.L;
+    MOE_TRY(cuda_status(launch_permute(idx, T, k, E, ws.i32(L.counts), ws.i32(L.offs),
+                                       ws.i32(L.perm), ws.i32(L.active), ws.i32(L.nactive),
+                                       ws.hdr(), s)));
+    return cuda_status(launch_expert_ffn(
+        x, idx, w, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
+        static_cast<const uint8_t *>(down), T, H, E, k, I, y, ws.i32(L.offs), ws.i32(L.perm),
+        ws.i32(L.active), ws.i32(L.nactive), ws.f32(L.h), ws.f32(L.o), sms, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_str(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_SHAPE: return "MOE_ERR_INVALID_SHAPE";
+        case MOE_ERR_NULL: return "MOE_ERR_NULL";
+        case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+        case MOE_ERR_EXPERT_RANGE: return "MOE_ERR_EXPERT_RANGE";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+int moe_version(void) { return 100; }
+
+size_t moe_workspace_bytes(int T, int H, int E, int k, int I) {
+    if (check_shape(T, H, E, k, I) != MOE_OK) return 0;
+    return ws_layout(T, H, E, k, I, false).total;
+}
+
+size_t moe_workspace_bytes_host(int T, int H, int E, int k, int I) {
+    if (check_shape(T, H, E, k, I) != MOE_OK) return 0;
+    return ws_layout(T, H, E, k, I, true).total;
+}
+
+int moe_layer_launch_count(int T, int H, int E, int k, int I) {
+    if (check_shape(T, H, E, k, I) != MOE_OK) return 0;
+    return 2 /* router */ + 1 /* permutation */ + 3 /* gate/up, down, combine */;
+}
+
+moe_status moe_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+    MOE_TRY(check_ptr(ws, 256));
+    if (ws_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+    return cuda_status(cudaMemsetAsync(ws, 0, sizeof(WsHeader), static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
+                      int k, int32_t *idx, float *w, void *ws, size_t ws_bytes, void *stream) {
+    MOE_TRY(check_shape(T, H, E, k, 256));
+    MOE_TRY(check_ptr(x, 16));
+    MOE_TRY(check_ptr(Wr, 16));
+    if (bias && !aligned(bias, 16)) return MOE_ERR_MISALIGNED;
+    MOE_TRY(check_ptr(idx, 16));
+    MOE_TRY(check_ptr(w, 16));
+    WsLayout L = ws_layout(T, H, E, k, 256, false);
+    // the router only needs the header and the logits region
+    MOE_TRY(check_ptr(ws, 256));
+    if (ws_bytes < L.logits + sizeof(float) * size_t(T) * E) return MOE_ERR_WORKSPACE;
+    int sms = 0;
+    MOE_TRY(device_info(&sms));
+    Ws W{static_cast<uint8_t *>(ws), L};
+    return cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits),
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_permute(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offs,
+                       int32_t *perm, void *ws, size_t ws_bytes, void *stream) {
+    MOE_TRY(check_shape(T, 256, E, k, 256));
+    MOE_TRY(check_ptr(idx, 16));
+    MOE_TRY(check_ptr(counts, 16));
+    MOE_TRY(check_ptr(offs, 16));
+    MOE_TRY(check_ptr(perm, 16));
+    MOE_TRY(check_ptr(ws, 256));
+    WsLayout L = ws_layout(T, 256, E, k, 256, false);
+    if (ws_bytes < L.perm) return MOE_ERR_WORKSPACE;
+    int sms = 0;
+    MOE_TRY(device_info(&sms));
+    Ws W{static_cast<uint8_t *>(ws), L};
+    return cuda_status(launch_permute(idx, T, k, E, counts, offs, perm, W.i32(L.active),
+                                      W.i32(L.nactive), W.hdr(),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_ffn(const float *x, const int32_t *idx, const float *w, const void *gate,
+                   const void *up, const void *down, int T, int H, int E, int k, int I, float *y,
+                   void *ws, size_t ws_bytes, void *stream) {
+    MOE_TRY(check_shape(T, H, E, k, I));
+    MOE_TRY(check_ptr(x, 16));
+    MOE_TRY(check_ptr(idx, 16));
+    MOE_TRY(check_ptr(w, 16));
+    MOE_TRY(check_ptr(gate, 16));
+    MOE_TRY(check_ptr(up, 16));
+    MOE_TRY(check_ptr(down, 16));
+    MOE_TRY(check_ptr(y, 16));
+    WsLayout L = ws_layout(T, H, E, k, I, false);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    int sms = 0;
+    MOE_TRY(device_info(&sms));
+    Ws W{static_cast<uint8_t *>(ws), L};
+    return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms,
+                       static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer(const float *x, const float *Wr, const float *bias, const void *gate,
+                     const void *up, const void *down, int T, int H, int E, int k, int I,
+                     int32_t *idx, float *w, float *y, void *ws, size_t ws_bytes, void *stream) {
+    MOE_TRY(check_shape(T, H, E, k, I));
+    MOE_TRY(check_ptr(x, 16));
+    MOE_TRY(check_ptr(Wr, 16));
+    if (bias && !aligned(bias, 16)) return MOE_ERR_MISALIGNED;
+    MOE_TRY(check_ptr(gate, 16));
+    MOE_TRY(check_ptr(up, 16));
+    MOE_TRY(check_ptr(down, 16));
+    MOE_TRY(check_ptr(idx, 16));
+    MOE_TRY(check_ptr(w, 16));
+    MOE_TRY(check_ptr(y, 16));
+    WsLayout L = ws_layout(T, H, E, k, I, false);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    int sms = 0;
+    MOE_TRY(device_info(&sms));
+    Ws W{static_cast<uint8_t *>(ws), L};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), s)));
+    return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, s);
+}
+
+moe_status moe_layer_host(const float *x_host, const float *Wr, const float *bias,
+                          const void *gate, const void *up, const void *down, int T, int H, int E,
+                          int k, int I, int32_t *idx, float *w, float *y_host, void *ws,
+                          size_t ws_bytes, void *stream) {
+    MOE_TRY(check_shape(T, H, E, k, I));
+    if (x_host == nullptr || y_host == nullptr) return MOE_ERR_NULL;
+    WsLayout L = ws_layout(T, H, E, k, I, true);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    Ws W{static_cast<uint8_t *>(ws), L};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = sizeof(float) * size_t(T) * H;
+    float *xd = W.f32(L.xstage), *yd = W.f32(L.ystage);
+    MOE_TRY(cuda_status(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s)));
+    MOE_TRY(moe_layer(xd, Wr, bias, gate, up, down, T, H, E, k, I, idx, w, yd, ws, ws_bytes,
+                      stream));
+    MOE_TRY(cuda_status(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s)));
+    return cuda_status(cudaStreamSynchronize(s));
+}
+
+moe_status moe_read_device_status(const void *ws, void *stream, int32_t *detail) {
+    MOE_TRY(check_ptr(ws, 256));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsHeader h;
+    MOE_TRY(cuda_status(cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, s)));
+    MOE_TRY(cuda_status(cudaStreamSynchronize(s)));
+    if (detail) *detail = h.detail;
+    return static_cast<moe_status>(h.status);
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+// Shared device helpers and the workspace layout of the moeq4k library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "moeq4k.h"
+
+namespace moeq4k {
+
+constexpr int kQK = 256;          // weights per Q4_K block
+constexpr int kBlockBytes = 144;  // bytes per Q4_K block
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 32;
+constexpr int kMaxHI = 8192;
+
+// ---------------------------------------------------------------------------
+// Workspace layout (all regions 256-byte aligned).  The header is zeroed by
+// moe_workspace_init; everything else is scratch rewritten by every call.
+// ---------------------------------------------------------------------------
+struct WsHeader {
+    uint32_t status;     // first device-side moe_status recorded (sticky)
+    int32_t detail;      // value that caused it
+    uint32_t pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+struct WsLayout {
+    size_t counts, offs, active, nactive, perm, h, o, logits, xstage, ystage, total;
+};
+
+__host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(int T, int H, int E, int k, int I, bool host_staging) {
+    WsLayout L;
+    size_t off = sizeof(WsHeader);
+    size_t pairs = size_t(T) * k;
+    L.counts = off;  off = align256(off + sizeof(int32_t) * E);
+    L.offs = off;    off = align256(off + sizeof(int32_t) * (E + 1));
+    L.active = off;  off = align256(off + sizeof(int32_t) * E);
+    L.nactive = off; off = align256(off + sizeof(int32_t) * 4);
+    L.logits = off;  off = align256(off + sizeof(float) * size_t(T) * E);
+    L.perm = off;    off = align256(off + sizeof(int32_t) * pairs);
+    L.h = off;       off = align256(off + sizeof(float) * pairs * I);
+    L.o = off;       off = align256(off + sizeof(float) * pairs * H);
+    L.xstage = off;
+    L.ystage = off;
+    if (host_staging) {
+        L.xstage = off; off = align256(off + sizeof(float) * size_t(T) * H);
+        L.ystage = off; off = align256(off + sizeof(float) * size_t(T) * H);
+    }
+    L.total = off;
+    return L;
+}
+
+// Record the first device-side error (later ones are dropped).
+__device__ inline void record_status(WsHeader *hdr, moe_status s, int32_t detail) {
+    if (atomicCAS(&hdr->status, 0u, uint32_t(s)) == 0u) {
+        hdr->detail = detail;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Q4_K block pieces.  The 16-byte block head holds d, dmin and scales[12]:
+//   head.x = d | dmin << 16, head.y = scales[0..3], head.z = scales[4..7],
+//   head.w = scales[8..11] (little-endian bytes).
+// Sub-block j < 4:  sc = scales[j] & 63,  m = scales[j+4] & 63
+// Sub-block j >= 4: sc = (scales[j+4] & 15) | (scales[j-4] >> 6) << 4
+//                   m  = (scales[j+4] >> 4) | (scales[j]   >> 6) << 4
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void q4k_scale_min(const uint4 &head, int j, float &sc, float &m) {
+    uint32_t s, mm;
+    if (j < 4) {
+        s = (head.y >> (8 * j)) & 63u;
+        mm = (head.z >> (8 * j)) & 63u;
+    } else {
+        int jj = j - 4;
+        s = ((head.w >> (8 * jj)) & 15u) | (((head.y >> (8 * jj + 6)) & 3u) << 4);
+        mm = ((head.w >> (8 * jj + 4)) & 15u) | (((head.z >> (8 * jj + 6)) & 3u) << 4);
+    }
+    sc = float(s);
+    m = float(mm);
+}
+
+__device__ __forceinline__ float2 q4k_d_dmin(const uint4 &head) {
+    __half2 hd = *reinterpret_cast<const __half2 *>(&head.x);
+    return __half22float2(hd);
+}
+
+// Code byte i (0..3) of a 32-bit word as an exact fp32 value: the byte lands
+// in the low mantissa bits of 2^23, then 2^23 is subtracted.
+__device__ __forceinline__ float nib_to_float(uint32_t nibbles4, int i) {
+    uint32_t bits = __byte_perm(nibbles4, 0x4B000000u, 0x7540u | uint32_t(i));
+    return __uint_as_float(bits) - 8388608.0f;
+}
+
+// Dot products of one 16-byte code chunk (qs bytes b = 0..15 of a 32-byte
+// group c) with the matching activations: `lo` = sum_b q_lo[b] * xlo[b]
+// (sub-block 2c), `hi` = sum_b q_hi[b] * xhi[b] (sub-block 2c+1).
+__device__ __forceinline__ void chunk_dot(const uint4 &q, const float *xlo, const float *xhi,
+                                          float &lo, float &hi) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+        uint32_t l4 = w[wi] & 0x0F0F0F0Fu;
+        uint32_t h4 = (w[wi] >> 4) & 0x0F0F0F0Fu;
+        float4 xl = *reinterpret_cast<const float4 *>(xlo + 4 * wi);
+        float4 xh = *reinterpret_cast<const float4 *>(xhi + 4 * wi);
+        a = fmaf(nib_to_float(l4, 0), xl.x, a);
+        a = fmaf(nib_to_float(l4, 1), xl.y, a);
+        a = fmaf(nib_to_float(l4, 2), xl.z, a);
+        a = fmaf(nib_to_float(l4, 3), xl.w, a);
+        b = fmaf(nib_to_float(h4, 0), xh.x, b);
+        b = fmaf(nib_to_float(h4, 1), xh.y, b);
+        b = fmaf(nib_to_float(h4, 2), xh.z, b);
+        b = fmaf(nib_to_float(h4, 3), xh.w, b);
+    }
+    lo = a;
+    hi = b;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return g / (1.0f + expf(-g)) * u;
+}
+
+}  // namespace moeq4k

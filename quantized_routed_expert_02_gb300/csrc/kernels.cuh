@@ -1,0 +1,22 @@
+// Launch wrappers of the moeq4k kernels (host side).
+#pragma once
+
+#include "common.cuh"
+
+namespace moeq4k {
+
+cudaError_t launch_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
+                          int k, int32_t *idx, float *w, float *logits, cudaStream_t s);
+
+cudaError_t launch_permute(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offs,
+                           int32_t *perm, int32_t *active, int32_t *nactive, WsHeader *hdr,
+                           cudaStream_t s);
+
+cudaError_t init_expert_ffn();
+cudaError_t launch_expert_ffn(const float *x, const int32_t *idx, const float *w,
+                              const uint8_t *gate, const uint8_t *up, const uint8_t *down, int T,
+                              int H, int E, int k, int I, float *y, const int32_t *offs,
+                              const int32_t *perm, const int32_t *active, const int32_t *nactive,
+                              float *hbuf, float *obuf, int num_sms, cudaStream_t s);
+
+}  // namespace moeq4k

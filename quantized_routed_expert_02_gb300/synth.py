@@ -153,14 +153,18 @@ def random_blocks(rng: np.random.Generator, n: int) -> np.ndarray:
 
     Nibbles uniform 0..15 (uniform random bytes), sc uniform 1..63, m uniform
     0..63, d = fp16(|N(0,1e-3)|), dmin = fp16(|N(0,5e-4)|); fp16 rounding is
-    NumPy's round-to-nearest-even.
+    NumPy's round-to-nearest-even.  The qs bytes come straight from the raw
+    64-bit output of the generator; the 16 header bytes are then written over.
     """
+    out = rng.bit_generator.random_raw(n * (BLOCK_BYTES // 8)).view(np.uint8).reshape(n, BLOCK_BYTES)
     d = np.abs(rng.normal(0.0, 1e-3, n)).astype(np.float16)
     dmin = np.abs(rng.normal(0.0, 5e-4, n)).astype(np.float16)
     sc = rng.integers(1, 64, size=(n, 8), dtype=np.uint8)
     m = rng.integers(0, 64, size=(n, 8), dtype=np.uint8)
-    qs = np.frombuffer(rng.bytes(n * 128), dtype=np.uint8).reshape(n, 128)
-    return pack_blocks(d, dmin, sc, m, qs)
+    out[:, 0:2] = d.view(np.uint8).reshape(n, 2)
+    out[:, 2:4] = dmin.view(np.uint8).reshape(n, 2)
+    out[:, 4:16] = pack_scales(sc, m)
+    return out
 
 
 # ---------------------------------------------------------------------------
