@@ -121,12 +121,10 @@ __device__ __forceinline__ void chunk_dot(const uint4 &q, const float *xlo, cons
     hi = b;
 }
 
+// Read-only 16-byte load of weight bytes.  An intrinsic, not inline asm: the
+// compiler must never move a load above the bounds check that guards it.
 __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
+    return __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
