@@ -75,7 +75,8 @@ typedef enum {
     MOE_ERR_WORKSPACE = 4,      /* workspace smaller than moe_workspace_bytes() */
     MOE_ERR_EXPERT_RANGE = 5,   /* device saw an expert index outside [0,E) */
     MOE_ERR_TIMEOUT = 6,        /* a bounded device-side wait expired */
-    MOE_ERR_CUDA = 7            /* the CUDA runtime reported an error */
+    MOE_ERR_CUDA = 7,           /* the CUDA runtime reported an error */
+    MOE_ERR_INTERNAL = 8        /* a device-side consistency check failed (a library fault) */
 } moe_status;
 
 /* Human-readable name of a status code (static string, never NULL). */

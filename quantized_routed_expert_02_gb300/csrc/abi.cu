@@ -83,7 +83,7 @@ moe_status ffn_enqueue(const float *x, const int32_t *idx, const float *w, const
     return cuda_status(launch_expert_ffn(
         x, idx, w, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
         static_cast<const uint8_t *>(down), T, H, E, k, I, y, ws.i32(L.offs), ws.i32(L.perm),
-        ws.i32(L.active), ws.i32(L.nactive), ws.f32(L.h), ws.f32(L.o), sms, s));
+        ws.i32(L.active), ws.i32(L.nactive), ws.f32(L.h), ws.f32(L.o), ws.hdr(), sms, s));
 }
 
 }  // namespace
@@ -100,6 +100,7 @@ const char *moe_status_str(moe_status s) {
         case MOE_ERR_EXPERT_RANGE: return "MOE_ERR_EXPERT_RANGE";
         case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
         case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_INTERNAL: return "MOE_ERR_INTERNAL";
     }
     return "MOE_ERR_UNKNOWN";
 }

@@ -46,6 +46,17 @@ __device__ __forceinline__ void stage_rows(float *vs, float *vsum, int n, int le
     __syncthreads();
 }
 
+// A slot id read back from the permutation, checked against [0, npairs):
+// an id outside it is recorded and replaced by 0 so no access leaves the
+// buffers (the write of its result is skipped by the caller).
+__device__ __forceinline__ int checked_pair(int p, int npairs, WsHeader *hdr, int site) {
+    if (p < 0 || p >= npairs) {
+        record_status(hdr, MOE_ERR_INTERNAL, site + (p & 0xffffff));
+        return 0;
+    }
+    return p;
+}
+
 // Partial dot product of one lane's share of a Q4_K row with staged vector
 // `v` (length len = nsb*256, with 16-element partial sums `vsum`).
 __device__ __forceinline__ float row_part(const uint8_t *row, int nsb, int lane, const float *v,
@@ -80,30 +91,46 @@ __global__ void __launch_bounds__(256) gateup_kernel(const float *__restrict__ x
                                                      const int32_t *__restrict__ perm,
                                                      const int32_t *__restrict__ active,
                                                      const int32_t *__restrict__ nactive,
-                                                     int H, int I, int k,
-                                                     float *__restrict__ h) {
+                                                     int H, int I, int k, int E, int npairs,
+                                                     float *__restrict__ h, WsHeader *hdr) {
     extern __shared__ float smem[];
     float *xs = smem;                         // [kTokGroup][H]
     float *xsum = smem + kTokGroup * H;       // [kTokGroup][H/16]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsb = H / kQK;
     const int nrb = I / kRowsPerItem;
-    const int items = (*nactive) * nrb;
+    int na = *nactive;
+    if (na < 0 || na > E) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) record_status(hdr, MOE_ERR_INTERNAL, 500000000 + (na & 0xffffff));
+        na = 0;
+    }
+    const int items = na * nrb;
     const size_t mat_bytes = size_t(I) * nsb * kBlockBytes;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
         const int e = active[it / nrb];
+        if (e < 0 || e >= E) {
+            if (threadIdx.x == 0) record_status(hdr, MOE_ERR_INTERNAL, 100000000 + (e & 0xffffff));
+            continue;
+        }
         const int r = (it % nrb) * kRowsPerItem + warp;
         const int p0 = offs[e], n_e = offs[e + 1] - p0;
+        if (p0 < 0 || n_e < 0 || p0 + n_e > npairs) {
+            if (threadIdx.x == 0) record_status(hdr, MOE_ERR_INTERNAL, 200000000 + (p0 & 0xffffff));
+            continue;
+        }
         const uint8_t *grow = gate + e * mat_bytes + size_t(r) * nsb * kBlockBytes;
         const uint8_t *urow = up + e * mat_bytes + size_t(r) * nsb * kBlockBytes;
         for (int g0 = 0; g0 < n_e; g0 += kTokGroup) {
             const int ng = min(kTokGroup, n_e - g0);
             __syncthreads();
-            stage_rows(xs, xsum, ng, H, [&](int i) { return x + size_t(perm[p0 + g0 + i] / k) * H; });
+            stage_rows(xs, xsum, ng, H, [&](int i) {
+                return x + size_t(checked_pair(perm[p0 + g0 + i], npairs, hdr, 300000000) / k) * H;
+            });
             for (int i = 0; i < ng; ++i) {
                 float g = warp_sum(row_part(grow, nsb, lane, xs + i * H, xsum + i * (H >> 4)));
                 float u = warp_sum(row_part(urow, nsb, lane, xs + i * H, xsum + i * (H >> 4)));
-                if (lane == 0) h[size_t(perm[p0 + g0 + i]) * I + r] = silu_mul(g, u);
+                const int p = perm[p0 + g0 + i];
+                if (lane == 0 && p >= 0 && p < npairs) h[size_t(p) * I + r] = silu_mul(g, u);
             }
         }
     }
@@ -116,27 +143,44 @@ __global__ void __launch_bounds__(256) down_kernel(const float *__restrict__ h,
                                                    const int32_t *__restrict__ perm,
                                                    const int32_t *__restrict__ active,
                                                    const int32_t *__restrict__ nactive,
-                                                   int H, int I, float *__restrict__ o) {
+                                                   int H, int I, int E, int npairs,
+                                                   float *__restrict__ o, WsHeader *hdr) {
     extern __shared__ float smem[];
     float *hs = smem;                         // [kTokGroup][I]
     float *hsum = smem + kTokGroup * I;       // [kTokGroup][I/16]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsb = I / kQK;
     const int nrb = H / kRowsPerItem;
-    const int items = (*nactive) * nrb;
+    int na = *nactive;
+    if (na < 0 || na > E) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) record_status(hdr, MOE_ERR_INTERNAL, 510000000 + (na & 0xffffff));
+        na = 0;
+    }
+    const int items = na * nrb;
     const size_t mat_bytes = size_t(H) * nsb * kBlockBytes;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
         const int e = active[it / nrb];
+        if (e < 0 || e >= E) {
+            if (threadIdx.x == 0) record_status(hdr, MOE_ERR_INTERNAL, 110000000 + (e & 0xffffff));
+            continue;
+        }
         const int r = (it % nrb) * kRowsPerItem + warp;
         const int p0 = offs[e], n_e = offs[e + 1] - p0;
+        if (p0 < 0 || n_e < 0 || p0 + n_e > npairs) {
+            if (threadIdx.x == 0) record_status(hdr, MOE_ERR_INTERNAL, 210000000 + (p0 & 0xffffff));
+            continue;
+        }
         const uint8_t *drow = down + e * mat_bytes + size_t(r) * nsb * kBlockBytes;
         for (int g0 = 0; g0 < n_e; g0 += kTokGroup) {
             const int ng = min(kTokGroup, n_e - g0);
             __syncthreads();
-            stage_rows(hs, hsum, ng, I, [&](int i) { return h + size_t(perm[p0 + g0 + i]) * I; });
+            stage_rows(hs, hsum, ng, I, [&](int i) {
+                return h + size_t(checked_pair(perm[p0 + g0 + i], npairs, hdr, 310000000)) * I;
+            });
             for (int i = 0; i < ng; ++i) {
                 float v = warp_sum(row_part(drow, nsb, lane, hs + i * I, hsum + i * (I >> 4)));
-                if (lane == 0) o[size_t(perm[p0 + g0 + i]) * H + r] = v;
+                const int p = perm[p0 + g0 + i];
+                if (lane == 0 && p >= 0 && p < npairs) o[size_t(p) * H + r] = v;
             }
         }
     }
@@ -179,15 +223,18 @@ cudaError_t launch_expert_ffn(const float *x, const int32_t *idx, const float *w
                               const uint8_t *gate, const uint8_t *up, const uint8_t *down, int T,
                               int H, int E, int k, int I, float *y, const int32_t *offs,
                               const int32_t *perm, const int32_t *active, const int32_t *nactive,
-                              float *hbuf, float *obuf, int num_sms, cudaStream_t s) {
+                              float *hbuf, float *obuf, WsHeader *hdr, int num_sms,
+                              cudaStream_t s) {
     const int max_active = min(E, T * k);
     const size_t smem_gu = sizeof(float) * kTokGroup * (H + H / 16);
     const size_t smem_dn = sizeof(float) * kTokGroup * (I + I / 16);
     const int cap = num_sms * 8;
     int g1 = min(max_active * (I / kRowsPerItem), cap);
-    gateup_kernel<<<g1, 256, smem_gu, s>>>(x, gate, up, offs, perm, active, nactive, H, I, k, hbuf);
+    gateup_kernel<<<g1, 256, smem_gu, s>>>(x, gate, up, offs, perm, active, nactive, H, I, k, E,
+                                           T * k, hbuf, hdr);
     int g2 = min(max_active * (H / kRowsPerItem), cap);
-    down_kernel<<<g2, 256, smem_dn, s>>>(hbuf, down, offs, perm, active, nactive, H, I, obuf);
+    down_kernel<<<g2, 256, smem_dn, s>>>(hbuf, down, offs, perm, active, nactive, H, I, E, T * k,
+                                         obuf, hdr);
     const size_t total = size_t(T) * (H / 4);
     const size_t g3s = (total + 255) / 256, g3cap = size_t(num_sms) * 16;
     int g3 = int(g3s < g3cap ? g3s : g3cap);

@@ -17,6 +17,7 @@ cudaError_t launch_expert_ffn(const float *x, const int32_t *idx, const float *w
                               const uint8_t *gate, const uint8_t *up, const uint8_t *down, int T,
                               int H, int E, int k, int I, float *y, const int32_t *offs,
                               const int32_t *perm, const int32_t *active, const int32_t *nactive,
-                              float *hbuf, float *obuf, int num_sms, cudaStream_t s);
+                              float *hbuf, float *obuf, WsHeader *hdr, int num_sms,
+                              cudaStream_t s);
 
 }  // namespace moeq4k

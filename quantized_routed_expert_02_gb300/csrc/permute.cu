@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t *__restrict
         unsigned peers = __match_any_sync(0xffffffffu, key);
         int rank = __popc(peers & ((1u << lane) - 1u));
         bool leader = ok && (rank == 0);
-        for (int i = tid; i < 32 * E; i += blockDim.x) (&table[0][0])[i] = 0;
+        for (int i = tid; i < 32 * E; i += blockDim.x) table[i / E][i % E] = 0;
         __syncthreads();
         if (leader) table[warp][e] = __popc(peers);
         __syncthreads();
@@ -96,7 +96,14 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t *__restrict
             cnt[ee] = run;
         }
         __syncthreads();
-        if (ok) perm[cursor[e] + table[warp][e] + rank] = p;
+        if (ok) {
+            const int pos = cursor[e] + table[warp][e] + rank;
+            if (pos >= 0 && pos < n) {
+                perm[pos] = p;
+            } else {
+                record_status(hdr, MOE_ERR_INTERNAL, 400000000 + (pos & 0xffffff));
+            }
+        }
         __syncthreads();
         for (int ee = tid; ee < E; ee += blockDim.x) cursor[ee] += cnt[ee];
         __syncthreads();

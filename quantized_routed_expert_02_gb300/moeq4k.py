@@ -51,7 +51,7 @@ for _name, (_args, _res) in _SIGS.items():
 EXPORTS = tuple(_SIGS)
 
 MOE_OK = 0
-STATUS_NAMES = {i: _lib.moe_status_str(i).decode() for i in range(8)}
+STATUS_NAMES = {i: _lib.moe_status_str(i).decode() for i in range(9)}
 
 
 class MoeError(RuntimeError):
