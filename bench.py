@@ -270,8 +270,10 @@ def main():
     with torch.cuda.graph(graph, stream=stream):
         one_step(stream)
 
-    for _ in range(max(3, args.warmup)):
-        graph.replay()
+    # CUDAGraph.replay() launches on the current stream: make it `stream`
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
     torch.cuda.synchronize()
 
     # algorithmic bytes of one step, from the routing each call made
@@ -302,10 +304,11 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    start.record(stream)
-    for _ in range(args.steps):
-        graph.replay()
-    end.record(stream)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        end.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
