@@ -174,6 +174,18 @@ MOE_API moe_status moe_layer_host(const float *x_host, const float *Wr_dev, cons
  */
 MOE_API moe_status moe_read_device_status(const void *ws_dev, void *stream, int32_t *detail);
 
+/*
+ * Test hooks for the bounded device-side waits (not for production use).
+ * moe_debug_set_wait_limit: upper bound, in ns, of every device-side wait
+ * of later calls (0 restores the default of 1 s).  moe_debug_withhold_arrivals:
+ * make the grid barrier of later single-token calls wait for n CTAs that
+ * never arrive, so the wait runs out; such a call records MOE_ERR_TIMEOUT in
+ * the workspace status, writes no output, and leaves the barrier counters
+ * dirty: re-initialise the workspace (moe_workspace_init) afterwards.
+ */
+MOE_API void moe_debug_set_wait_limit(unsigned long long ns);
+MOE_API void moe_debug_withhold_arrivals(int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,13 +13,18 @@ namespace {
 struct DevInfo {
     bool ready = false;
     int sms = 0;
+    int id = 0;
 };
 constexpr int kMaxDevices = 64;
 DevInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
 // Per-device one-time set-up (kernel attributes, SM count) for the current device.
-moe_status device_info(int *sms) {
+// Test hooks (see moe_debug_set_wait_limit / moe_debug_withhold_arrivals).
+unsigned long long g_wait_ns = 1000000000ull;  // 1 s: far above any healthy wait
+int g_withhold = 0;
+
+moe_status device_info(int *sms, int *dev_out = nullptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
@@ -28,10 +33,13 @@ moe_status device_info(int *sms) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return MOE_ERR_CUDA;
         if (init_expert_ffn() != cudaSuccess) return MOE_ERR_CUDA;
+        if (init_decode_fused(dev, n) != cudaSuccess) return MOE_ERR_CUDA;
         g_dev[dev].sms = n;
+        g_dev[dev].id = dev;
         g_dev[dev].ready = true;
     }
     *sms = g_dev[dev].sms;
+    if (dev_out) *dev_out = dev;
     return MOE_OK;
 }
 
@@ -119,8 +127,15 @@ size_t moe_workspace_bytes_host(int T, int H, int E, int k, int I) {
 
 int moe_layer_launch_count(int T, int H, int E, int k, int I) {
     if (check_shape(T, H, E, k, I) != MOE_OK) return 0;
+    int sms = 0, dev = 0;
+    if (device_info(&sms, &dev) != MOE_OK) return 0;
+    if (decode_fused_supported(dev, T, H, E, k, I)) return 1;
     return 2 /* router */ + 1 /* permutation */ + 3 /* gate/up, down, combine */;
 }
+
+void moe_debug_set_wait_limit(unsigned long long ns) { g_wait_ns = ns ? ns : 1000000000ull; }
+
+void moe_debug_withhold_arrivals(int n) { g_withhold = n < 0 ? 0 : n; }
 
 moe_status moe_workspace_init(void *ws, size_t ws_bytes, void *stream) {
     MOE_TRY(check_ptr(ws, 256));
@@ -178,9 +193,16 @@ moe_status moe_ffn(const float *x, const int32_t *idx, const float *w, const voi
     MOE_TRY(check_ptr(y, 16));
     WsLayout L = ws_layout(T, H, E, k, I, false);
     MOE_TRY(check_ws(ws, ws_bytes, L));
-    int sms = 0;
-    MOE_TRY(device_info(&sms));
+    int sms = 0, dev = 0;
+    MOE_TRY(device_info(&sms, &dev));
     Ws W{static_cast<uint8_t *>(ws), L};
+    if (decode_fused_supported(dev, T, H, E, k, I)) {
+        return cuda_status(launch_decode_fused(
+            dev, x, nullptr, nullptr, idx, w, nullptr, nullptr, static_cast<const uint8_t *>(gate),
+            static_cast<const uint8_t *>(up), static_cast<const uint8_t *>(down), H, E, k, I, y,
+            W.f32(L.logits), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns,
+            static_cast<cudaStream_t>(stream)));
+    }
     return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms,
                        static_cast<cudaStream_t>(stream));
 }
@@ -200,10 +222,16 @@ moe_status moe_layer(const float *x, const float *Wr, const float *bias, const v
     MOE_TRY(check_ptr(y, 16));
     WsLayout L = ws_layout(T, H, E, k, I, false);
     MOE_TRY(check_ws(ws, ws_bytes, L));
-    int sms = 0;
-    MOE_TRY(device_info(&sms));
+    int sms = 0, dev = 0;
+    MOE_TRY(device_info(&sms, &dev));
     Ws W{static_cast<uint8_t *>(ws), L};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (decode_fused_supported(dev, T, H, E, k, I)) {
+        return cuda_status(launch_decode_fused(
+            dev, x, Wr, bias, nullptr, nullptr, idx, w, static_cast<const uint8_t *>(gate),
+            static_cast<const uint8_t *>(up), static_cast<const uint8_t *>(down), H, E, k, I, y,
+            W.f32(L.logits), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns, s));
+    }
     MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), s)));
     return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, s);
 }

@@ -20,4 +20,15 @@ cudaError_t launch_expert_ffn(const float *x, const int32_t *idx, const float *w
                               float *hbuf, float *obuf, WsHeader *hdr, int num_sms,
                               cudaStream_t s);
 
+cudaError_t init_decode_fused(int dev, int num_sms);
+bool decode_fused_supported(int dev, int T, int H, int E, int k, int I);
+// Wr == nullptr: routing comes from idx_in / w_in (moe_ffn); otherwise the
+// kernel routes and writes idx_out / w_out (moe_layer).
+cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const float *bias,
+                                const int32_t *idx_in, const float *w_in, int32_t *idx_out,
+                                float *w_out, const uint8_t *gate, const uint8_t *up,
+                                const uint8_t *down, int H, int E, int k, int I, float *y,
+                                float *logits, float *hbuf, WsHeader *hdr, int withhold,
+                                unsigned long long wait_ns, cudaStream_t s);
+
 }  // namespace moeq4k

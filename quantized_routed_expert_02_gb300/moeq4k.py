@@ -42,6 +42,8 @@ _SIGS = {
     "moe_layer_host": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P],
                        ctypes.c_int),
     "moe_read_device_status": ([_P, _P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+    "moe_debug_set_wait_limit": ([ctypes.c_ulonglong], None),
+    "moe_debug_withhold_arrivals": ([_I], None),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -159,3 +161,11 @@ def moe_read_device_status(ws, stream=None):
     detail = ctypes.c_int32(0)
     code = _lib.moe_read_device_status(_ptr(ws), _stream(stream), ctypes.byref(detail))
     return int(code), int(detail.value)
+
+
+def moe_debug_set_wait_limit(ns: int) -> None:
+    _lib.moe_debug_set_wait_limit(int(ns))
+
+
+def moe_debug_withhold_arrivals(n: int) -> None:
+    _lib.moe_debug_withhold_arrivals(int(n))
