@@ -81,27 +81,37 @@ def generate(name, n_layers, rank, workers):
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every 20 ms, each tagged with the host clock when
+    read, so the ones inside the timed region can be picked out."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_id):
         self.gpu_id = gpu_id
         self.proc = None
-        self.file = None
+        self.rows = []
+        self.thread = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.perf_counter(), line.strip().split(",")))
 
     def start(self):
+        import threading
         try:
-            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=self.file, stderr=subprocess.DEVNULL)
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
 
-    def stop(self):
+    def stop(self, t0, t1):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -109,24 +119,24 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        self.file.flush()
-        self.file.seek(0)
-        rows = [ln.strip().split(",") for ln in self.file.read().splitlines() if ln.strip()]
-        self.file.close()
-        os.unlink(self.file.name)
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        inside = [r for t, r in self.rows if t0 <= t <= t1]
+        # a region shorter than the sampling period: take the samples nearest to it
+        near = inside or [r for t, r in self.rows if t0 - 0.1 <= t <= t1 + 0.1]
         sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        for r in near:
             try:
                 sm.append(float(r[0]))
                 smax = float(r[1])
-                for nm, v in zip(names, r[4:8]):
+                for nm, v in zip(self.NAMES, r[4:8]):
                     if v.strip().lower() == "active":
                         reasons.add(nm)
             except (ValueError, IndexError):
                 continue
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "samples_inside_timed_region": len(inside)}
 
 
 def measured_peaks():
@@ -304,15 +314,17 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    t_region0 = time.perf_counter()
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(args.steps):
             graph.replay()
         end.record(stream)
     torch.cuda.synchronize()
+    t_region1 = time.perf_counter()
     if dist is not None:
         dist.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop(t_region0, t_region1)
     ms = start.elapsed_time(end)
     if dist is not None:
         t = torch.tensor([ms], device=dev)
