@@ -20,10 +20,9 @@ constexpr int kMaxHI = 8192;
 // moe_workspace_init; everything else is scratch rewritten by every call.
 // ---------------------------------------------------------------------------
 struct WsHeader {
-    uint32_t status;     // first device-side moe_status recorded (sticky)
-    int32_t detail;      // value that caused it
-    uint32_t bar_count;  // grid barrier: CTAs arrived in the current round
-    uint32_t bar_gen;    // grid barrier: completed rounds (wraps)
+    uint32_t status;                 // first device-side moe_status recorded (sticky)
+    int32_t detail;                  // value that caused it
+    unsigned long long bar_arrivals; // grid barrier: CTA arrivals since initialisation
     uint32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");

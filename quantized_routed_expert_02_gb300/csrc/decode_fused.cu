@@ -8,29 +8,30 @@
 // doc of forward_qwen3_moe_cuda_traced_with_plan: the router stage is the k
 // post-softmax, renormalised weights and the output stage is [H].
 //
-// Design (one CTA per SM, cooperative launch so every CTA is resident):
+// Design (one CTA of 16 warps per SM, cooperative launch so every CTA is
+// resident):
 //  1. Every CTA stages x in shared memory and computes a share of the E
 //     router logits (Wr read with an L2 evict-last policy: it is re-read by
-//     every token, unlike the expert bytes).
+//     every token, unlike the expert bytes, which are read evict-first).
 //  2. Grid barrier; every CTA reads the E logits and runs the same top-k and
 //     renormalisation, so all CTAs know the k experts without a broadcast.
-//  3. A producer warp streams this CTA's share of the selected experts' Q4_K
-//     rows into a ring of shared-memory slots with 1-D bulk copies (TMA
-//     engine, mbarrier completion, L2 evict-first policy): first the
-//     gate/up row pairs (slot j, row r), then the down rows of the CTA's
-//     output rows for all k experts.  At T=1 the share of the Qwen3-30B-A3B
-//     shape (~140 KB) fits in the ring entirely, so every byte is requested
-//     up front and HBM sees the whole 21 MB at once.
-//  4. Consumer warps decode rows as they land (nibbles and 6-bit scales in
-//     registers, fp32 FMA against x in shared memory) and write
-//     h = SiLU(g) * u to the workspace.
-//  5. Grid barrier; each CTA stages h of all k slots, then for each of its
+//  3. The k*I gate/up row pairs are split evenly over the CTAs and, inside a
+//     CTA, over its warps.  Each warp streams its own rows into a private
+//     ring of shared-memory slots with 16-byte cp.async copies (every lane
+//     issues, so hundreds of requests per SM are in flight; completion is
+//     tracked by one mbarrier per slot), decodes nibbles and 6-bit scales
+//     in registers, does fp32 FMAs against x in shared memory, and writes
+//     h = SiLU(g) * u to the workspace.  When the CTA's down rows (its share
+//     of the H output rows, for all k experts) fit beside the rings, all
+//     threads prefetch them right after the first gate/up rows.
+//  4. Grid barrier; each CTA stages h of all k slots, then for each of its
 //     output rows computes o_j = Wd[e_j][row] . h_j for j = 0..k-1 and
-//     y = sum_j w_j o_j in slot order, so the combine is deterministic and
-//     needs no atomics.
-// Every wait (mbarrier, grid barrier) is bounded by a global-timer deadline;
-// on expiry the kernel records MOE_ERR_TIMEOUT and returns after draining
-// its own copies.
+//     y = sum_j w_j o_j in slot order: deterministic, no atomics.
+// The grid barrier is a monotonic 64-bit arrival counter (release add,
+// acquire polling), so it needs no reset between calls or graph replays.
+// Every wait is bounded by a global-timer deadline; on expiry the kernel
+// records MOE_ERR_TIMEOUT, stops computing and lets its copies land before
+// returning.
 #include <algorithm>
 
 #include "async_copy.cuh"
@@ -40,11 +41,19 @@
 namespace moeq4k {
 namespace fused {
 
-constexpr int kConsWarps = 16;
-constexpr int kConsThreads = kConsWarps * 32;
-constexpr int kThreads = kConsThreads + 32;  // + one producer warp
-constexpr int kMaxSlots = 64;
-constexpr int kHeadBytes = 2048;             // barriers + small arrays
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxNbw = 8;         // ring slots per warp
+constexpr int kHeadBytes = 2048;   // mbarriers + small arrays
+
+// Optional phase timeline for profiling builds (-DMOEQ4K_TIMELINE): thread 0
+// of each CTA stamps the global timer at phase boundaries into the
+// workspace's per-slot output region, which this path does not otherwise use.
+#ifdef MOEQ4K_TIMELINE
+#define TL_STAMP(p, i) ((p).timeline[blockIdx.x * 16 + (i)] = global_timer_ns())
+#else
+#define TL_STAMP(p, i) ((void)0)
+#endif
 
 struct Params {
     const float *x, *Wr, *bias;
@@ -57,9 +66,11 @@ struct Params {
     WsHeader *hdr;
     int H, E, k, I;
     int router_on;
-    int nslots, slot_bytes, ring_off;
+    int nbw, slot_bytes, ring_off;
+    int down_resident, down_off;  // CTA's down rows prefetched into [down_off, ...)
     int withhold;                 // test hook: extra arrivals the grid barrier waits for
     unsigned long long wait_ns;   // bound of every wait
+    unsigned long long *timeline; // profiling builds only
 };
 
 // Padded shared-memory vector: 4 floats of padding after every 64, so the
@@ -99,15 +110,14 @@ __device__ __forceinline__ float u6_to_float(uint32_t v) {
 }
 
 // One lane's share of a Q4_K row (nsb blocks in shared memory at `row`)
-// dotted with the padded vector `vec` (run sums in `vsum`).  Lane L takes
-// code chunk L%8 of blocks L/8, L/8+4, ...
+// dotted with the padded vector `vec` (16-element run sums in `vsum`).  Lane
+// L takes code chunk L%8 of blocks L/8, L/8+4, ...
 template <int NSB>
 __device__ __forceinline__ float row_lane_dot(const uint8_t *row, int nsb_rt, const float *vec,
                                               const float *vsum, int lane) {
     const int nsb = NSB > 0 ? NSB : nsb_rt;
     const int cq = lane & 7, c = cq >> 1, hf = cq & 1;
-    // sub-blocks 2c and 2c+1: shifts into the packed scale words
-    const bool upper = c >= 2;
+    const bool upper = c >= 2;  // sub-blocks 4..7 keep their high scale bits elsewhere
     const int j0 = 2 * c, j1 = 2 * c + 1;
     float acc = 0.f;
 #pragma unroll(NSB > 8 ? 2 : 4)
@@ -146,55 +156,40 @@ __device__ __forceinline__ float row_lane_dot(const uint8_t *row, int nsb_rt, co
     return acc;
 }
 
-// Stage `n` floats from global `src` (row-major, 16-byte aligned) into the
-// padded shared vector and its 16-element run sums; consumer threads only.
-__device__ __forceinline__ void stage_vector(const float *src, int n, bool coherent, float *vec,
-                                             float *vsum) {
-    for (int i = threadIdx.x; i < (n >> 2); i += kConsThreads) {
-        const float4 v = coherent ? __ldcg(reinterpret_cast<const float4 *>(src) + i)
-                                  : __ldg(reinterpret_cast<const float4 *>(src) + i);
-        *reinterpret_cast<float4 *>(vec + padded(4 * i)) = v;
-    }
-    named_bar_sync(1, kConsThreads);
-    for (int r = threadIdx.x; r < (n >> 4); r += kConsThreads) {
-        const float *v = vec + padded(16 * r);
+// Sum each 16-float run of `count` runs of the padded vector(s) into vsum.
+// Run q starts at logical element 16*(q % runs_per_vec) of vector q / runs_per_vec.
+__device__ __forceinline__ void run_sums(const float *vec, float *vsum, int count, int runs_per_vec,
+                                         int vec_stride) {
+    for (int q = threadIdx.x; q < count; q += kThreads) {
+        const int j = q / runs_per_vec, c = 16 * (q % runs_per_vec);
+        const float *v = vec + j * vec_stride + padded(c);
         float s = 0.f;
 #pragma unroll
         for (int b = 0; b < 16; ++b) s += v[b];
-        vsum[r] = s;
+        vsum[q] = s;
     }
-    named_bar_sync(1, kConsThreads);
 }
 
-// Grid barrier over the consumer threads of every CTA (sense by generation
-// counter, self-resetting so it works across graph replays).  Returns false
-// if the wait ran past the deadline.
-__device__ __forceinline__ bool grid_barrier(WsHeader *hdr, unsigned expected, uint64_t deadline,
-                                             int *flag) {
-    named_bar_sync(1, kConsThreads);
+// Grid barrier on a monotonic arrival counter: arrive (release), then wait
+// (acquire) until the counter reaches `target`.  All threads of the CTA call
+// it; returns false on time-out.
+__device__ __forceinline__ bool grid_sync(WsHeader *hdr, unsigned long long target,
+                                          uint64_t deadline, int *flag) {
+    __syncthreads();
     if (threadIdx.x == 0) {
-        volatile unsigned *genp = &hdr->bar_gen;
-        const unsigned g = *genp;
         __threadfence();
-        const unsigned prev = atomicAdd(&hdr->bar_count, 1u);
+        red_release_add_u64(&hdr->bar_arrivals, 1ull);
         bool ok = true;
-        if (prev == expected - 1) {
-            atomicExch(&hdr->bar_count, 0u);
-            __threadfence();
-            atomicAdd(&hdr->bar_gen, 1u);
-        } else {
-            while (*genp == g) {
-                if (global_timer_ns() > deadline) {
-                    ok = false;
-                    break;
-                }
-                __nanosleep(32);
+        while (ld_acquire_u64(&hdr->bar_arrivals) < target) {
+            if (global_timer_ns() > deadline) {
+                ok = false;
+                break;
             }
+            __nanosleep(20);
         }
-        __threadfence();
         *flag = ok ? 0 : 1;
     }
-    named_bar_sync(1, kConsThreads);
+    __syncthreads();
     return *flag == 0;
 }
 
@@ -203,163 +198,82 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 }
 
 template <int NSB_H, int NSB_I>
-__device__ __forceinline__ void consumer_phases(const Params &p, uint64_t *full, uint64_t *empty,
-                                                const int *sel_e, const float *sel_w, int *flags,
-                                                float *vec, float *vsum, uint8_t *ring,
-                                                uint64_t deadline, int u0, int n_gu, int r0,
-                                                int F) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int E = p.E, k = p.k, I = p.I, NS = p.nslots;
-    const unsigned nblk = gridDim.x;
-    const int nsb_h = p.H / kQK, nsb_i = I / kQK;
-    const int row_gu = nsb_h * kBlockBytes, row_dn = nsb_i * kBlockBytes;
-    // consumers: gate/up row pairs
-    bool alive = true;
-    for (int f = warp; f < n_gu; f += kConsWarps) {
-        const int slot = f % NS;
-        if (!mbar_wait(full + slot, (f / NS) & 1, deadline)) {
-            if (lane == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 3);
-            alive = false;
-            break;
-        }
-        const int u = u0 + f, j = u / I, r = u % I;
-        const int e = sel_e[j];
-        if (e >= 0 && e < E) {
-            const uint8_t *src = ring + size_t(slot) * p.slot_bytes;
-            const float g = warp_sum(row_lane_dot<NSB_H>(src, nsb_h, vec, vsum, lane));
-            const float uu = warp_sum(row_lane_dot<NSB_H>(src + row_gu, nsb_h, vec, vsum, lane));
-            if (lane == 0) p.hbuf[size_t(j) * I + r] = silu_mul(g, uu);
-        }
-        __syncwarp();
-        fence_proxy_async_smem();
-        if (lane == 0) mbar_arrive(empty + slot);
-    }
-    if (!alive) flags[1] = 1;
-
-    // h of every slot must be complete before the down rows
-    if (!grid_barrier(p.hdr, nblk + p.withhold, deadline, flags)) {
-        if (threadIdx.x == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 4);
-        flags[1] = 1;
-    }
-    const bool run = flags[1] == 0;
-    if (run) {
-        // h for all k slots -> padded vector (slot j at j * padded_len(I))
-        const int ip = padded_len(I);
-        for (int i = threadIdx.x; i < (k * I) >> 2; i += kConsThreads) {
-            const int j = (4 * i) / I, c = (4 * i) % I;
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.hbuf) + i);
-            *reinterpret_cast<float4 *>(vec + j * ip + padded(c)) = v;
-        }
-        named_bar_sync(1, kConsThreads);
-        for (int q = threadIdx.x; q < (k * I) >> 4; q += kConsThreads) {
-            const int j = (16 * q) / I, c = (16 * q) % I;
-            const float *v = vec + j * ip + padded(c);
-            float s = 0.f;
-#pragma unroll
-            for (int b = 0; b < 16; ++b) s += v[b];
-            vsum[q] = s;
-        }
-        named_bar_sync(1, kConsThreads);
-    }
-
-    // down rows + slot-ordered combine
-    for (int f = n_gu + warp; f < F; f += kConsWarps) {
-        const int slot = f % NS;
-        if (!mbar_wait(full + slot, (f / NS) & 1, deadline)) {
-            if (lane == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 5);
-            break;
-        }
-        if (run) {
-            const int r = r0 + (f - n_gu);
-            const uint8_t *src = ring + size_t(slot) * p.slot_bytes;
-            const int ip = padded_len(I);
-            float yacc = 0.f;
-            for (int j = 0; j < k; ++j) {
-                const int e = sel_e[j];
-                if (e < 0 || e >= E) continue;
-                const float o = warp_sum(row_lane_dot<NSB_I>(src + j * row_dn, nsb_i,
-                                                              vec + j * ip, vsum + j * (I >> 4),
-                                                              lane));
-                yacc = fmaf(sel_w[j], o, yacc);
-            }
-            if (lane == 0) p.y[r] = yacc;
-        }
-        __syncwarp();
-        fence_proxy_async_smem();
-        if (lane == 0) mbar_arrive(empty + slot);
-    }
-}
-
-template <int NSB_H, int NSB_I>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *empty = full + kMaxSlots;
-    int *sel_e = reinterpret_cast<int *>(empty + kMaxSlots);
+    uint64_t *slot_bar = reinterpret_cast<uint64_t *>(smem);          // [kWarps][kMaxNbw]
+    uint64_t *down_bar = slot_bar + kWarps * kMaxNbw;
+    unsigned long long *base_sh = reinterpret_cast<unsigned long long *>(down_bar + 1);
+    int *sel_e = reinterpret_cast<int *>(base_sh + 1);
     float *sel_w = reinterpret_cast<float *>(sel_e + 32);
     float *red = sel_w + 32;
-    int *flags = reinterpret_cast<int *>(red + 32);  // [0] barrier result, [1] abort, [2] fills issued
+    int *flags = reinterpret_cast<int *>(red + 32);  // [0] barrier result, [1] abort
     float *vec = reinterpret_cast<float *>(smem + kHeadBytes);
     const int H = p.H, E = p.E, k = p.k, I = p.I;
     const int vec_pad = max(padded_len(H), k * padded_len(I));
     float *vsum = vec + vec_pad;
-    uint8_t *ring = smem + p.ring_off;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool producer = warp == kConsWarps;
     const uint64_t deadline = global_timer_ns() + p.wait_ns;
     const unsigned nblk = gridDim.x;
     const int nsb_h = H / kQK, nsb_i = I / kQK;
     const int row_gu = nsb_h * kBlockBytes, row_dn = nsb_i * kBlockBytes;
     const size_t mat_gu = size_t(I) * row_gu, mat_dn = size_t(H) * row_dn;
+    const int nbw = p.nbw;
+    uint8_t *ring = smem + p.ring_off + size_t(warp) * nbw * p.slot_bytes;
+    uint64_t *my_bar = slot_bar + warp * kMaxNbw;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < p.nslots; ++s) {
-            mbar_init(full + s, 1);
-            mbar_init(empty + s, 1);
-        }
-        flags[1] = 0;
-        flags[2] = 0;
+        TL_STAMP(p, 0);
+        for (int s = 0; s < kWarps * kMaxNbw; ++s) mbar_init(slot_bar + s, 32);
+        mbar_init(down_bar, kThreads);
         fence_mbar_init();
+        // this call's barrier rounds: every call adds 2 arrivals per CTA, and
+        // fewer than 2*nblk arrivals of this call can precede this read
+        const unsigned long long c0 = ld_acquire_u64(&p.hdr->bar_arrivals);
+        *base_sh = c0 - c0 % (2ull * nblk);
+        flags[1] = 0;
     }
-    // x -> padded shared vector (consumers); the producer waits below
-    if (!producer) stage_vector(p.x, H, false, vec, vsum);
+    // x -> padded shared vector and its run sums
+    for (int i = threadIdx.x; i < (H >> 2); i += kThreads)
+        *reinterpret_cast<float4 *>(vec + padded(4 * i)) = __ldg(reinterpret_cast<const float4 *>(p.x) + i);
     __syncthreads();
+    run_sums(vec, vsum, H >> 4, H >> 4, 0);
+    __syncthreads();
+    const unsigned long long base = *base_sh;
+    if (threadIdx.x == 0) TL_STAMP(p, 1);
 
     // ---------------- 1. router logits (a share per CTA), grid barrier
     if (p.router_on) {
-        if (!producer) {
-            const uint64_t pol = l2_policy_evict_last();
-            for (int e = blockIdx.x; e < E; e += nblk) {
-                const float *wr = p.Wr + size_t(e) * H;
-                float a = 0.f;
-                for (int i = threadIdx.x; i < (H >> 2); i += kConsThreads) {
-                    const float4 w4 = ldg_f4_policy(wr + 4 * i, pol);
-                    const float4 x4 = *reinterpret_cast<const float4 *>(vec + padded(4 * i));
-                    a = fmaf(w4.x, x4.x, a);
-                    a = fmaf(w4.y, x4.y, a);
-                    a = fmaf(w4.z, x4.z, a);
-                    a = fmaf(w4.w, x4.w, a);
-                }
-                a = warp_sum(a);
-                if (lane == 0) red[warp] = a;
-                named_bar_sync(1, kConsThreads);
-                if (threadIdx.x == 0) {
-                    float s = 0.f;
-                    for (int w = 0; w < kConsWarps; ++w) s += red[w];
-                    p.logits[e] = s + (p.bias ? p.bias[e] : 0.f);
-                }
-                named_bar_sync(1, kConsThreads);
+        const uint64_t pol = l2_policy_evict_last();
+        for (int e = blockIdx.x; e < E; e += nblk) {
+            const float *wr = p.Wr + size_t(e) * H;
+            float a = 0.f;
+            for (int i = threadIdx.x; i < (H >> 2); i += kThreads) {
+                const float4 w4 = ldg_f4_policy(wr + 4 * i, pol);
+                const float4 x4 = *reinterpret_cast<const float4 *>(vec + padded(4 * i));
+                a = fmaf(w4.x, x4.x, a);
+                a = fmaf(w4.y, x4.y, a);
+                a = fmaf(w4.z, x4.z, a);
+                a = fmaf(w4.w, x4.w, a);
             }
-            if (!grid_barrier(p.hdr, nblk + p.withhold, deadline, flags)) {
-                if (threadIdx.x == 0) {
-                    record_status(p.hdr, MOE_ERR_TIMEOUT, 1);
-                    flags[1] = 1;
-                }
+            a = warp_sum(a);
+            if (lane == 0) red[warp] = a;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                float s = 0.f;
+                for (int w = 0; w < kWarps; ++w) s += red[w];
+                p.logits[e] = s + (p.bias ? p.bias[e] : 0.f);
             }
+            __syncthreads();
         }
-        __syncthreads();
-        if (flags[1]) return;  // nothing issued yet: safe to leave
+        if (threadIdx.x == 0) TL_STAMP(p, 2);
+        if (!grid_sync(p.hdr, base + nblk + p.withhold, deadline, flags)) {
+            if (threadIdx.x == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 1);
+            cp_async_wait_all();
+            return;  // no output written
+        }
+    } else if (threadIdx.x == 0) {
+        red_release_add_u64(&p.hdr->bar_arrivals, 1ull);  // keep 2 arrivals per call
     }
 
     // ---------------- 2. top-k + renormalise (warp 0 of every CTA)
@@ -423,78 +337,142 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         }
     }
     __syncthreads();
+    if (threadIdx.x == 0) TL_STAMP(p, 3);
 
-    // ---------------- 3/4/5. streamed expert rows
-    const int U = k * I;                                   // gate/up row pairs
+    // ---------------- 3. gate/up rows: per-warp cp.async rings
+    const int U = k * I;
     const int u0 = int((long long)U * blockIdx.x / nblk);
     const int u1 = int((long long)U * (blockIdx.x + 1) / nblk);
     const int r0 = int((long long)H * blockIdx.x / nblk);
     const int r1 = int((long long)H * (blockIdx.x + 1) / nblk);
-    const int n_gu = u1 - u0, n_dn = r1 - r0;
-    const int F = n_gu + n_dn;
-    const int NS = p.nslots;
+    const int R = r1 - r0;
+    const int n_gu = u1 - u0;
+    const int n_mine = n_gu > warp ? (n_gu - warp + kWarps - 1) / kWarps : 0;  // rows warp+16i
+    const uint64_t pol = l2_policy_evict_first();
+    const int n16_gu = row_gu >> 4, n16_dn = row_dn >> 4;
 
-    if (producer) {
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            int f = 0;
-            for (; f < F; ++f) {
-                const int slot = f % NS;
-                if (f >= NS) {
-                    if (!mbar_wait(empty + slot, ((f / NS) - 1) & 1, deadline)) {
-                        record_status(p.hdr, MOE_ERR_TIMEOUT, 2);
-                        flags[1] = 1;
-                        break;
-                    }
-                }
-                uint8_t *dst = ring + size_t(slot) * p.slot_bytes;
-                if (f < n_gu) {
-                    const int u = u0 + f, j = u / I, r = u % I;
-                    const int e = sel_e[j];
-                    if (e >= 0 && e < E) {
-                        mbar_arrive_expect_tx(full + slot, 2 * row_gu);
-                        bulk_copy_g2s(dst, p.gate + e * mat_gu + size_t(r) * row_gu, row_gu,
-                                      full + slot, pol);
-                        bulk_copy_g2s(dst + row_gu, p.up + e * mat_gu + size_t(r) * row_gu, row_gu,
-                                      full + slot, pol);
-                    } else {
-                        mbar_arrive(full + slot);
-                    }
-                } else {
-                    const int r = r0 + (f - n_gu);
-                    uint32_t bytes = 0;
-                    for (int j = 0; j < k; ++j) {
-                        const int e = sel_e[j];
-                        if (e >= 0 && e < E) bytes += row_dn;
-                    }
-                    if (bytes) {
-                        mbar_arrive_expect_tx(full + slot, bytes);
-                        for (int j = 0; j < k; ++j) {
-                            const int e = sel_e[j];
-                            if (e >= 0 && e < E)
-                                bulk_copy_g2s(dst + j * row_dn,
-                                              p.down + e * mat_dn + size_t(r) * row_dn, row_dn,
-                                              full + slot, pol);
-                        }
-                    } else {
-                        mbar_arrive(full + slot);
-                    }
-                }
+    // issue the copies of this warp's i-th gate/up row pair into its ring slot
+    auto issue_gu = [&](int i) {
+        const int u = u0 + warp + kWarps * i, j = u / I, r = u % I;
+        const int e = sel_e[j];
+        uint8_t *dst = ring + (i % nbw) * p.slot_bytes;
+        if (e >= 0 && e < E) {
+            const uint8_t *g = p.gate + e * mat_gu + size_t(r) * row_gu;
+            const uint8_t *uu = p.up + e * mat_gu + size_t(r) * row_gu;
+            for (int c = lane; c < 2 * n16_gu; c += 32) {
+                const uint8_t *src = c < n16_gu ? g + 16 * c : uu + 16 * (c - n16_gu);
+                cp_async_16(dst + 16 * c, src, pol);
             }
-            flags[2] = f;
         }
-    } else {
-        consumer_phases<NSB_H, NSB_I>(p, full, empty, sel_e, sel_w, flags, vec, vsum, ring,
-                                      deadline, u0, n_gu, r0, F);
+        cp_async_arrive_noinc(my_bar + (i % nbw));
+    };
+    // issue the copies of this warp's i-th down row (all k experts) into a ring slot
+    auto issue_dn = [&](int i, int slot) {
+        const int r = r0 + warp + kWarps * i;
+        uint8_t *dst = ring + slot * p.slot_bytes;
+        for (int c = lane; c < k * n16_dn; c += 32) {
+            const int j = c / n16_dn, w16 = c % n16_dn;
+            const int e = sel_e[j];
+            if (e >= 0 && e < E)
+                cp_async_16(dst + 16 * c, p.down + e * mat_dn + size_t(r) * row_dn + 16 * w16, pol);
+        }
+        cp_async_arrive_noinc(my_bar + slot);
+    };
+
+    const int first = min(nbw, n_mine);
+    for (int i = 0; i < first; ++i) issue_gu(i);
+    uint8_t *dbuf = smem + p.down_off;
+    if (p.down_resident) {
+        // the CTA's R output rows of all k experts: k contiguous ranges
+        const int per_j = R * n16_dn;
+        for (int c = threadIdx.x; c < k * per_j; c += kThreads) {
+            const int j = c / per_j, w16 = c % per_j;
+            const int e = sel_e[j];
+            if (e >= 0 && e < E)
+                cp_async_16(dbuf + 16 * c, p.down + e * mat_dn + size_t(r0) * row_dn + 16 * w16, pol);
+        }
+        cp_async_arrive_noinc(down_bar);
+    }
+
+    bool alive = true;
+    for (int i = 0; i < n_mine; ++i) {
+        const int slot = i % nbw;
+        if (!mbar_wait(my_bar + slot, (i / nbw) & 1, deadline)) {
+            if (lane == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 3);
+            alive = false;
+            break;
+        }
+        const int u = u0 + warp + kWarps * i, j = u / I, r = u % I;
+        const int e = sel_e[j];
+        if (e >= 0 && e < E) {
+            const uint8_t *src = ring + slot * p.slot_bytes;
+            const float g = warp_sum(row_lane_dot<NSB_H>(src, nsb_h, vec, vsum, lane));
+            const float uu = warp_sum(row_lane_dot<NSB_H>(src + row_gu, nsb_h, vec, vsum, lane));
+            if (lane == 0) p.hbuf[size_t(j) * I + r] = silu_mul(g, uu);
+        }
+        __syncwarp();
+        if (i + nbw < n_mine) issue_gu(i + nbw);
+    }
+    if (!alive) flags[1] = 1;
+    if (threadIdx.x == 0) TL_STAMP(p, 4);
+
+    // ---------------- 4. h complete everywhere -> down rows + combine
+    if (!grid_sync(p.hdr, base + 2ull * nblk + p.withhold, deadline, flags)) {
+        if (threadIdx.x == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 4);
+        flags[1] = 1;
     }
     __syncthreads();
-    // After a time-out some issued fills may never have been waited for:
-    // drain them (bounded) so no bulk copy lands after the CTA has exited.
-    if (threadIdx.x == 0 && flags[1]) {
-        const int issued = flags[2];
-        const uint64_t dl = global_timer_ns() + p.wait_ns;
-        for (int f = max(0, issued - NS); f < issued; ++f) mbar_wait(full + f % NS, (f / NS) & 1, dl);
+    if (threadIdx.x == 0) TL_STAMP(p, 5);
+    if (flags[1] == 0) {
+        const int ip = padded_len(I);
+        for (int i = threadIdx.x; i < (k * I) >> 2; i += kThreads) {
+            const int j = (4 * i) / I, c = (4 * i) % I;
+            *reinterpret_cast<float4 *>(vec + j * ip + padded(c)) =
+                __ldcg(reinterpret_cast<const float4 *>(p.hbuf) + i);
+        }
+        __syncthreads();
+        run_sums(vec, vsum, (k * I) >> 4, I >> 4, ip);
+        __syncthreads();
+        if (threadIdx.x == 0) TL_STAMP(p, 6);
+
+        const int n_rows = R > warp ? (R - warp + kWarps - 1) / kWarps : 0;  // rows warp+16i
+        bool ok = true;
+        if (p.down_resident) ok = mbar_wait(down_bar, 0, deadline);
+        const int first_dn = p.down_resident ? 0 : min(nbw, n_rows);
+        for (int i = 0; i < first_dn; ++i) issue_dn(i, (n_mine + i) % nbw);
+        for (int i = 0; ok && i < n_rows; ++i) {
+            const int rr = warp + kWarps * i;  // row inside the CTA's share
+            const uint8_t *src;
+            size_t jstride;
+            if (p.down_resident) {
+                src = dbuf + size_t(rr) * row_dn;
+                jstride = size_t(R) * row_dn;
+            } else {
+                const int n = n_mine + i, slot = n % nbw;
+                if (!mbar_wait(my_bar + slot, (n / nbw) & 1, deadline)) {
+                    ok = false;
+                    break;
+                }
+                src = ring + slot * p.slot_bytes;
+                jstride = row_dn;
+            }
+            float yacc = 0.f;
+            for (int j = 0; j < k; ++j) {
+                const int e = sel_e[j];
+                if (e < 0 || e >= E) continue;
+                const float o = warp_sum(row_lane_dot<NSB_I>(src + j * jstride, nsb_i, vec + j * ip,
+                                                              vsum + j * (I >> 4), lane));
+                yacc = fmaf(sel_w[j], o, yacc);
+            }
+            if (lane == 0) p.y[r0 + rr] = yacc;
+            __syncwarp();
+            if (!p.down_resident && i + nbw < n_rows) issue_dn(i + nbw, (n_mine + i + nbw) % nbw);
+        }
+        if (!ok && lane == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 5);
     }
+    // every copy this thread issued must land before the CTA's shared memory goes away
+    cp_async_wait_all();
+    if (threadIdx.x == 0) TL_STAMP(p, 7);
 }
 
 }  // namespace fused
@@ -502,20 +480,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
 namespace {
 
 struct FusedConfig {
-    int nslots = 0, slot_bytes = 0, ring_off = 0, smem = 0;
+    int nbw = 0, slot_bytes = 0, ring_off = 0, down_resident = 0, down_off = 0, smem = 0;
 };
 
-bool fused_config(int H, int E, int k, int I, int max_smem, FusedConfig &c) {
+bool fused_config(int H, int E, int k, int I, int nblk, int max_smem, FusedConfig &c) {
     using namespace fused;
+    if (E > kMaxE || k > kMaxK || nblk < 1) return false;
     const int row_gu = (H / kQK) * kBlockBytes, row_dn = (I / kQK) * kBlockBytes;
     const int vec_pad = std::max(padded_len(H), k * padded_len(I));
     const int vec_sum = std::max(H, k * I) / 16;
-    c.ring_off = int(align256(size_t(kHeadBytes) + sizeof(float) * size_t(vec_pad + vec_sum)));
-    c.slot_bytes = int((std::max(2 * row_gu, k * row_dn) + 127) / 128 * 128);
-    const int avail = max_smem - c.ring_off;
-    c.nslots = std::min(kMaxSlots, avail / c.slot_bytes);
-    c.smem = c.ring_off + c.nslots * c.slot_bytes;
-    return c.nslots >= 4 && E <= kMaxE && k <= kMaxK;
+    const int vec_end = int(align256(size_t(kHeadBytes) + sizeof(float) * size_t(vec_pad + vec_sum)));
+    const int rmax = (H + nblk - 1) / nblk;
+    const int down_bytes = int(align256(size_t(k) * rmax * row_dn));
+    // A: the CTA's down rows resident, rings hold gate/up row pairs
+    int slot = (2 * row_gu + 127) / 128 * 128;
+    int nbw = (max_smem - vec_end - down_bytes) / (kWarps * slot);
+    if (nbw >= 2) {
+        c.down_resident = 1;
+        c.down_off = vec_end;
+        c.ring_off = vec_end + down_bytes;
+    } else {
+        // B: rings hold gate/up row pairs, then down rows of all k experts
+        slot = (std::max(2 * row_gu, k * row_dn) + 127) / 128 * 128;
+        nbw = (max_smem - vec_end) / (kWarps * slot);
+        c.down_resident = 0;
+        c.down_off = vec_end;
+        c.ring_off = vec_end;
+    }
+    nbw = std::min(nbw, kMaxNbw);
+    if (nbw < 1) return false;
+    c.nbw = nbw;
+    c.slot_bytes = slot;
+    c.smem = c.ring_off + kWarps * nbw * slot;
+    return c.smem <= max_smem;
 }
 
 template <int A, int B>
@@ -532,11 +529,10 @@ void *pick_kernel(int H, int I) {
     return kernel_ptr<0, 0>();
 }
 
-}  // namespace
+int g_fused_max_smem[64];
+int g_fused_blocks[64];
 
-// Per-device limits for the fused kernel (set by init_decode_fused).
-static int g_fused_max_smem[64];
-static int g_fused_blocks[64];
+}  // namespace
 
 cudaError_t init_decode_fused(int dev, int num_sms) {
     int optin = 0;
@@ -556,7 +552,7 @@ cudaError_t init_decode_fused(int dev, int num_sms) {
 bool decode_fused_supported(int dev, int T, int H, int E, int k, int I) {
     if (T != 1) return false;
     FusedConfig c;
-    return fused_config(H, E, k, I, g_fused_max_smem[dev], c);
+    return fused_config(H, E, k, I, g_fused_blocks[dev], g_fused_max_smem[dev], c);
 }
 
 cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const float *bias,
@@ -566,7 +562,8 @@ cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const 
                                 float *logits, float *hbuf, WsHeader *hdr, int withhold,
                                 unsigned long long wait_ns, cudaStream_t s) {
     FusedConfig c;
-    if (!fused_config(H, E, k, I, g_fused_max_smem[dev], c)) return cudaErrorInvalidValue;
+    if (!fused_config(H, E, k, I, g_fused_blocks[dev], g_fused_max_smem[dev], c))
+        return cudaErrorInvalidValue;
     fused::Params p;
     p.x = x;
     p.Wr = Wr;
@@ -587,11 +584,14 @@ cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const 
     p.k = k;
     p.I = I;
     p.router_on = (Wr != nullptr) ? 1 : 0;
-    p.nslots = c.nslots;
+    p.nbw = c.nbw;
     p.slot_bytes = c.slot_bytes;
     p.ring_off = c.ring_off;
+    p.down_resident = c.down_resident;
+    p.down_off = c.down_off;
     p.withhold = withhold;
     p.wait_ns = wait_ns;
+    p.timeline = reinterpret_cast<unsigned long long *>(hbuf + size_t(k) * I);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(g_fused_blocks[dev]);
