@@ -113,6 +113,25 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most n (0..9) of this thread's committed cp.async groups are
+// still pending; larger n waits for all.
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+    switch (n) {
+        case 9: asm volatile("cp.async.wait_group 9;" ::: "memory"); break;
+        case 8: asm volatile("cp.async.wait_group 8;" ::: "memory"); break;
+        case 7: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+        case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+        case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    }
+}
+
 __device__ __forceinline__ void red_release_add_u64(unsigned long long *p, unsigned long long v) {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }

@@ -18,8 +18,8 @@
 //  3. The k*I gate/up row pairs are split evenly over the CTAs and, inside a
 //     CTA, over its warps.  Each warp streams its own rows into a private
 //     ring of shared-memory slots with 16-byte cp.async copies (every lane
-//     issues, so hundreds of requests per SM are in flight; completion is
-//     tracked by one mbarrier per slot), decodes nibbles and 6-bit scales
+//     issues, so hundreds of requests per SM are in flight; one commit group
+//     per row, waited with cp.async.wait_group), decodes nibbles and 6-bit scales
 //     in registers, does fp32 FMAs against x in shared memory, and writes
 //     h = SiLU(g) * u to the workspace.  When the CTA's down rows (its share
 //     of the H output rows, for all k experts) fit beside the rings, all
@@ -29,9 +29,9 @@
 //     y = sum_j w_j o_j in slot order: deterministic, no atomics.
 // The grid barrier is a monotonic 64-bit arrival counter (release add,
 // acquire polling), so it needs no reset between calls or graph replays.
-// Every wait is bounded by a global-timer deadline; on expiry the kernel
-// records MOE_ERR_TIMEOUT, stops computing and lets its copies land before
-// returning.
+// The grid-barrier wait is bounded by a global-timer deadline; on expiry the
+// kernel records MOE_ERR_TIMEOUT, stops computing and lets its copies land
+// before returning.  (Copy completion needs no bound: loads always finish.)
 #include <algorithm>
 
 #include "async_copy.cuh"
@@ -44,7 +44,7 @@ namespace fused {
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxNbw = 8;         // ring slots per warp
-constexpr int kHeadBytes = 2048;   // mbarriers + small arrays
+constexpr int kHeadBytes = 2048;   // small shared arrays
 
 // Optional phase timeline for profiling builds (-DMOEQ4K_TIMELINE): thread 0
 // of each CTA stamps the global timer at phase boundaries into the
@@ -69,7 +69,7 @@ struct Params {
     int nbw, slot_bytes, ring_off;
     int down_resident, down_off;  // CTA's down rows prefetched into [down_off, ...)
     int withhold;                 // test hook: extra arrivals the grid barrier waits for
-    unsigned long long wait_ns;   // bound of every wait
+    unsigned long long wait_ns;   // bound of the grid-barrier waits
     unsigned long long *timeline; // profiling builds only
 };
 
@@ -200,9 +200,7 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 template <int NSB_H, int NSB_I>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *slot_bar = reinterpret_cast<uint64_t *>(smem);          // [kWarps][kMaxNbw]
-    uint64_t *down_bar = slot_bar + kWarps * kMaxNbw;
-    unsigned long long *base_sh = reinterpret_cast<unsigned long long *>(down_bar + 1);
+    unsigned long long *base_sh = reinterpret_cast<unsigned long long *>(smem);
     int *sel_e = reinterpret_cast<int *>(base_sh + 1);
     float *sel_w = reinterpret_cast<float *>(sel_e + 32);
     float *red = sel_w + 32;
@@ -220,13 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     const size_t mat_gu = size_t(I) * row_gu, mat_dn = size_t(H) * row_dn;
     const int nbw = p.nbw;
     uint8_t *ring = smem + p.ring_off + size_t(warp) * nbw * p.slot_bytes;
-    uint64_t *my_bar = slot_bar + warp * kMaxNbw;
 
     if (threadIdx.x == 0) {
         TL_STAMP(p, 0);
-        for (int s = 0; s < kWarps * kMaxNbw; ++s) mbar_init(slot_bar + s, 32);
-        mbar_init(down_bar, kThreads);
-        fence_mbar_init();
         // this call's barrier rounds: every call adds 2 arrivals per CTA, and
         // fewer than 2*nblk arrivals of this call can precede this read
         const unsigned long long c0 = ld_acquire_u64(&p.hdr->bar_arrivals);
@@ -364,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
                 cp_async_16(dst + 16 * c, src, pol);
             }
         }
-        cp_async_arrive_noinc(my_bar + (i % nbw));
+        cp_async_commit();
     };
     // issue the copies of this warp's i-th down row (all k experts) into a ring slot
     auto issue_dn = [&](int i, int slot) {
@@ -376,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             if (e >= 0 && e < E)
                 cp_async_16(dst + 16 * c, p.down + e * mat_dn + size_t(r) * row_dn + 16 * w16, pol);
         }
-        cp_async_arrive_noinc(my_bar + slot);
+        cp_async_commit();
     };
 
     const int first = min(nbw, n_mine);
@@ -391,17 +385,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             if (e >= 0 && e < E)
                 cp_async_16(dbuf + 16 * c, p.down + e * mat_dn + size_t(r0) * row_dn + 16 * w16, pol);
         }
-        cp_async_arrive_noinc(down_bar);
+        cp_async_commit();  // one group after the first gate/up rows
     }
 
-    bool alive = true;
     for (int i = 0; i < n_mine; ++i) {
         const int slot = i % nbw;
-        if (!mbar_wait(my_bar + slot, (i / nbw) & 1, deadline)) {
-            if (lane == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 3);
-            alive = false;
-            break;
-        }
+        // groups committed after row i: the rows issued beyond it, plus the
+        // down prefetch when it went in after the first rows
+        const int later = min(nbw - 1, n_mine - 1 - i) + ((p.down_resident && i < first) ? 1 : 0);
+        cp_async_wait_pending(later);
+        __syncwarp();
         const int u = u0 + warp + kWarps * i, j = u / I, r = u % I;
         const int e = sel_e[j];
         if (e >= 0 && e < E) {
@@ -413,7 +406,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         __syncwarp();
         if (i + nbw < n_mine) issue_gu(i + nbw);
     }
-    if (!alive) flags[1] = 1;
     if (threadIdx.x == 0) TL_STAMP(p, 4);
 
     // ---------------- 4. h complete everywhere -> down rows + combine
@@ -436,11 +428,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         if (threadIdx.x == 0) TL_STAMP(p, 6);
 
         const int n_rows = R > warp ? (R - warp + kWarps - 1) / kWarps : 0;  // rows warp+16i
-        bool ok = true;
-        if (p.down_resident) ok = mbar_wait(down_bar, 0, deadline);
+        if (p.down_resident) {
+            cp_async_wait_all();  // this thread's share of the prefetch
+            __syncthreads();      // everyone's share
+        }
         const int first_dn = p.down_resident ? 0 : min(nbw, n_rows);
-        for (int i = 0; i < first_dn; ++i) issue_dn(i, (n_mine + i) % nbw);
-        for (int i = 0; ok && i < n_rows; ++i) {
+        for (int i = 0; i < first_dn; ++i) issue_dn(i, i % nbw);
+        for (int i = 0; i < n_rows; ++i) {
             const int rr = warp + kWarps * i;  // row inside the CTA's share
             const uint8_t *src;
             size_t jstride;
@@ -448,12 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
                 src = dbuf + size_t(rr) * row_dn;
                 jstride = size_t(R) * row_dn;
             } else {
-                const int n = n_mine + i, slot = n % nbw;
-                if (!mbar_wait(my_bar + slot, (n / nbw) & 1, deadline)) {
-                    ok = false;
-                    break;
-                }
-                src = ring + slot * p.slot_bytes;
+                cp_async_wait_pending(min(nbw - 1, n_rows - 1 - i));
+                __syncwarp();
+                src = ring + (i % nbw) * p.slot_bytes;
                 jstride = row_dn;
             }
             float yacc = 0.f;
@@ -466,9 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             }
             if (lane == 0) p.y[r0 + rr] = yacc;
             __syncwarp();
-            if (!p.down_resident && i + nbw < n_rows) issue_dn(i + nbw, (n_mine + i + nbw) % nbw);
+            if (!p.down_resident && i + nbw < n_rows) issue_dn(i + nbw, (i + nbw) % nbw);
         }
-        if (!ok && lane == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 5);
     }
     // every copy this thread issued must land before the CTA's shared memory goes away
     cp_async_wait_all();
