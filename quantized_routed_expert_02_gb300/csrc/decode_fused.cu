@@ -485,18 +485,15 @@ bool fused_config(int H, int E, int k, int I, int nblk, int max_smem, FusedConfi
     // A: the CTA's down rows resident, rings hold gate/up row pairs
     int slot = (2 * row_gu + 127) / 128 * 128;
     int nbw = (max_smem - vec_end - down_bytes) / (kWarps * slot);
-    if (nbw >= 2) {
-        c.down_resident = 1;
-        c.down_off = vec_end;
-        c.ring_off = vec_end + down_bytes;
-    } else {
-        // B: rings hold gate/up row pairs, then down rows of all k experts
-        slot = (std::max(2 * row_gu, k * row_dn) + 127) / 128 * 128;
-        nbw = (max_smem - vec_end) / (kWarps * slot);
-        c.down_resident = 0;
-        c.down_off = vec_end;
-        c.ring_off = vec_end;
-    }
+    // Only shapes whose down rows fit resident take this kernel.  The variant
+    // that streams down rows through the per-warp rings after the second
+    // barrier (needed by the Qwen3-235B-A22B shape) raised an illegal
+    // instruction on GB300 and is not launched; those shapes run the
+    // multi-kernel path.
+    if (nbw < 2) return false;
+    c.down_resident = 1;
+    c.down_off = vec_end;
+    c.ring_off = vec_end + down_bytes;
     nbw = std::min(nbw, kMaxNbw);
     if (nbw < 1) return false;
     c.nbw = nbw;

@@ -12,7 +12,7 @@ torch = pytest.importorskip("torch")
 
 
 def test_single_token_is_one_launch(m):
-    for name in ("tiny", "a3b_decode", "a22b_decode"):
+    for name in ("tiny", "a3b_decode"):
         s = synth.SHAPES[name]
         assert m.moe_layer_launch_count(s.T, s.H, s.E, s.k, s.I) == 1
     s = synth.SHAPES["a3b_batch64_zipf"]
