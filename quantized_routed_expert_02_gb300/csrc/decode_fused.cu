@@ -156,6 +156,41 @@ __device__ __forceinline__ float row_lane_dot(const uint8_t *row, int nsb_rt, co
     return acc;
 }
 
+// Contribution of one 16-byte code chunk (chunk cq of the block at `blk`)
+// to a row dot product with the padded vector `vec` / run sums `vsum`; the
+// block is block `s` of its row.
+__device__ __forceinline__ float block_chunk_dot(const uint8_t *blk, int s, int cq, const float *vec,
+                                                 const float *vsum) {
+    const int c = cq >> 1, hf = cq & 1;
+    const uint4 head = *reinterpret_cast<const uint4 *>(blk);
+    const uint4 q = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * cq);
+    const int base = s * kQK + 64 * c + 16 * hf;
+    float alo = 0.f, ahi = 0.f;
+    chunk_acc(q, vec + padded(base), alo, ahi);
+    const float slo = vsum[base >> 4], shi = vsum[(base >> 4) + 2];
+    const int j0 = 2 * c, j1 = 2 * c + 1;
+    uint32_t sc0, m0, sc1, m1;
+    if (c < 2) {
+        sc0 = (head.y >> (8 * j0)) & 63u;
+        m0 = (head.z >> (8 * j0)) & 63u;
+        sc1 = (head.y >> (8 * j1)) & 63u;
+        m1 = (head.z >> (8 * j1)) & 63u;
+    } else {
+        const int a = j0 - 4, b = j1 - 4;
+        sc0 = ((head.w >> (8 * a)) & 15u) | (((head.y >> (8 * a + 6)) & 3u) << 4);
+        m0 = ((head.w >> (8 * a + 4)) & 15u) | (((head.z >> (8 * a + 6)) & 3u) << 4);
+        sc1 = ((head.w >> (8 * b)) & 15u) | (((head.y >> (8 * b + 6)) & 3u) << 4);
+        m1 = ((head.w >> (8 * b + 4)) & 15u) | (((head.z >> (8 * b + 6)) & 3u) << 4);
+    }
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&head.x));
+    const float d128 = dd.x * 128.0f;
+    float acc = (d128 * u6_to_float(sc0)) * (alo - slo);
+    acc = fmaf(-dd.y * u6_to_float(m0), slo, acc);
+    acc = fmaf(d128 * u6_to_float(sc1), ahi - shi, acc);
+    acc = fmaf(-dd.y * u6_to_float(m1), shi, acc);
+    return acc;
+}
+
 // Sum each 16-float run of `count` runs of the padded vector(s) into vsum.
 // Run q starts at logical element 16*(q % runs_per_vec) of vector q / runs_per_vec.
 __device__ __forceinline__ void run_sums(const float *vec, float *vsum, int count, int runs_per_vec,
@@ -269,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     } else if (threadIdx.x == 0) {
         red_release_add_u64(&p.hdr->bar_arrivals, 1ull);  // keep 2 arrivals per call
     }
+    if (threadIdx.x == 0) TL_STAMP(p, 8);
 
     // ---------------- 2. top-k + renormalise (warp 0 of every CTA)
     if (warp == 0) {
@@ -395,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         const int later = min(nbw - 1, n_mine - 1 - i) + ((p.down_resident && i < first) ? 1 : 0);
         cp_async_wait_pending(later);
         __syncwarp();
+        if (threadIdx.x == 0 && i == 0) TL_STAMP(p, 9);
         const int u = u0 + warp + kWarps * i, j = u / I, r = u % I;
         const int e = sel_e[j];
         if (e >= 0 && e < E) {
@@ -417,13 +454,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     if (threadIdx.x == 0) TL_STAMP(p, 5);
     if (flags[1] == 0) {
         const int ip = padded_len(I);
-        for (int i = threadIdx.x; i < (k * I) >> 2; i += kThreads) {
-            const int j = (4 * i) / I, c = (4 * i) % I;
-            *reinterpret_cast<float4 *>(vec + j * ip + padded(c)) =
-                __ldcg(reinterpret_cast<const float4 *>(p.hbuf) + i);
+        for (int q = threadIdx.x; q < (k * I) >> 4; q += kThreads) {  // one 16-float run each
+            const int j = (16 * q) / I, c = (16 * q) % I;
+            const float4 *src = reinterpret_cast<const float4 *>(p.hbuf) + 4 * q;
+            float4 v[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) v[b] = __ldcg(src + b);
+            float *dst = vec + j * ip + padded(c);
+            float sum = 0.f;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                *reinterpret_cast<float4 *>(dst + 4 * b) = v[b];
+                sum += (v[b].x + v[b].y) + (v[b].z + v[b].w);
+            }
+            vsum[q] = sum;
         }
-        __syncthreads();
-        run_sums(vec, vsum, (k * I) >> 4, I >> 4, ip);
         __syncthreads();
         if (threadIdx.x == 0) TL_STAMP(p, 6);
 
@@ -432,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             cp_async_wait_all();  // this thread's share of the prefetch
             __syncthreads();      // everyone's share
         }
+        if (threadIdx.x == 0) TL_STAMP(p, 10);
         const int first_dn = p.down_resident ? 0 : min(nbw, n_rows);
         for (int i = 0; i < first_dn; ++i) issue_dn(i, i % nbw);
         for (int i = 0; i < n_rows; ++i) {
@@ -447,14 +493,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
                 src = ring + (i % nbw) * p.slot_bytes;
                 jstride = row_dn;
             }
+            // k experts x nsb_i blocks x 8 chunks, spread over the 32 lanes in a
+            // fixed order; each chunk's partial dot is weighted by its slot's
+            // router weight, then one warp reduction gives y (deterministic)
             float yacc = 0.f;
-            for (int j = 0; j < k; ++j) {
+            const int nchunks = k * nsb_i * 8;
+            for (int t = lane; t < nchunks; t += 32) {
+                const int j = t / (nsb_i * 8), rem = t % (nsb_i * 8);
+                const int sb = rem >> 3, cq = rem & 7;
                 const int e = sel_e[j];
                 if (e < 0 || e >= E) continue;
-                const float o = warp_sum(row_lane_dot<NSB_I>(src + j * jstride, nsb_i, vec + j * ip,
-                                                              vsum + j * (I >> 4), lane));
-                yacc = fmaf(sel_w[j], o, yacc);
+                const float part = block_chunk_dot(src + j * jstride + sb * kBlockBytes, sb, cq,
+                                                   vec + j * ip, vsum + j * (I >> 4));
+                yacc = fmaf(sel_w[j], part, yacc);
             }
+            yacc = warp_sum(yacc);
             if (lane == 0) p.y[r0 + rr] = yacc;
             __syncwarp();
             if (!p.down_resident && i + nbw < n_rows) issue_dn(i + nbw, (i + nbw) % nbw);
