@@ -76,7 +76,8 @@ typedef enum {
     MOE_ERR_EXPERT_RANGE = 5,   /* device saw an expert index outside [0,E) */
     MOE_ERR_TIMEOUT = 6,        /* a bounded device-side wait expired */
     MOE_ERR_CUDA = 7,           /* the CUDA runtime reported an error */
-    MOE_ERR_INTERNAL = 8        /* a device-side consistency check failed (a library fault) */
+    MOE_ERR_INTERNAL = 8,       /* a device-side consistency check failed (a library fault) */
+    MOE_ERR_SCRATCH_LIMIT = 9   /* the shape needs more than moe_layer_noalloc's fixed scratch */
 } moe_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -173,6 +174,31 @@ MOE_API moe_status moe_layer_host(const float *x_host, const float *Wr_dev, cons
  * index seen).
  */
 MOE_API moe_status moe_read_device_status(const void *ws_dev, void *stream, int32_t *detail);
+
+/*
+ * moe_layer for one token without any workspace, for callers that cannot
+ * allocate device memory (for example a plugin whose host framework owns
+ * every device allocation, or a decode loop that must not reach an
+ * allocator on its hot path).  The paper has no counterpart: it exists for
+ * those callers only.  Same arguments as moe_layer with T = 1 and no
+ * workspace; x, weights, idx, w and y are still the caller's device buffers.
+ *
+ * Scratch: a fixed 256 KB array in device global memory defined by the
+ * library (held on every GPU that loads it until the process exits).  It
+ * fits k*I <= 65216 and E <= 256; larger shapes return
+ * MOE_ERR_SCRATCH_LIMIT.  Shapes the single-token kernel does not take
+ * return MOE_ERR_INVALID_SHAPE.  The call allocates and frees nothing; it
+ * clears the scratch's status word and barrier counter with an async memset
+ * on `stream`, then launches one kernel.  All calls share the array: calls
+ * that overlap on the GPU race and must be serialised by the caller.
+ * The first call on each device looks up the array's device address; make
+ * that first call before any stream capture.  Only argument and launch
+ * errors are returned; device-side errors of this path are not reported.
+ */
+MOE_API moe_status moe_layer_noalloc(const float *x_dev, const float *Wr_dev, const float *bias_dev,
+                                     const void *gate_dev, const void *up_dev, const void *down_dev,
+                                     int T, int H, int E, int k, int I,
+                                     int32_t *idx_dev, float *w_dev, float *y_dev, void *stream);
 
 /*
  * Test hooks for the bounded device-side waits (not for production use).

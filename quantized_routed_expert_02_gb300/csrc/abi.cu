@@ -19,12 +19,14 @@ constexpr int kMaxDevices = 64;
 DevInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
-// Per-device one-time set-up (kernel attributes, SM count) for the current device.
 // Test hooks (see moe_debug_set_wait_limit / moe_debug_withhold_arrivals).
 unsigned long long g_wait_ns = 1000000000ull;  // 1 s: far above any healthy wait
 int g_withhold = 0;
 
-moe_status device_info(int *sms, int *dev_out = nullptr) {
+}  // namespace
+
+// Per-device one-time set-up (kernel attributes, SM count) for the current device.
+moe_status moeq4k::device_info(int *sms, int *dev_out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
@@ -42,6 +44,8 @@ moe_status device_info(int *sms, int *dev_out = nullptr) {
     if (dev_out) *dev_out = dev;
     return MOE_OK;
 }
+
+namespace {
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -96,6 +100,10 @@ moe_status ffn_enqueue(const float *x, const int32_t *idx, const float *w, const
 
 }  // namespace
 
+moe_status moeq4k::validate_shape(int T, int H, int E, int k, int I) {
+    return check_shape(T, H, E, k, I);
+}
+
 extern "C" {
 
 const char *moe_status_str(moe_status s) {
@@ -109,6 +117,7 @@ const char *moe_status_str(moe_status s) {
         case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
         case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
         case MOE_ERR_INTERNAL: return "MOE_ERR_INTERNAL";
+        case MOE_ERR_SCRATCH_LIMIT: return "MOE_ERR_SCRATCH_LIMIT";
     }
     return "MOE_ERR_UNKNOWN";
 }
@@ -156,7 +165,7 @@ moe_status moe_router(const float *x, const float *Wr, const float *bias, int T,
     MOE_TRY(check_ptr(ws, 256));
     if (ws_bytes < L.logits + sizeof(float) * size_t(T) * E) return MOE_ERR_WORKSPACE;
     int sms = 0;
-    MOE_TRY(device_info(&sms));
+    MOE_TRY(device_info(&sms, nullptr));
     Ws W{static_cast<uint8_t *>(ws), L};
     return cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits),
                                      static_cast<cudaStream_t>(stream)));
@@ -173,7 +182,7 @@ moe_status moe_permute(const int32_t *idx, int T, int k, int E, int32_t *counts,
     WsLayout L = ws_layout(T, 256, E, k, 256, false);
     if (ws_bytes < L.perm) return MOE_ERR_WORKSPACE;
     int sms = 0;
-    MOE_TRY(device_info(&sms));
+    MOE_TRY(device_info(&sms, nullptr));
     Ws W{static_cast<uint8_t *>(ws), L};
     return cuda_status(launch_permute(idx, T, k, E, counts, offs, perm, W.i32(L.active),
                                       W.i32(L.nactive), W.hdr(),

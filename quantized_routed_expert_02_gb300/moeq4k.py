@@ -42,6 +42,8 @@ _SIGS = {
     "moe_layer_host": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P],
                        ctypes.c_int),
     "moe_read_device_status": ([_P, _P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+    "moe_layer_noalloc": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P],
+                          ctypes.c_int),
     "moe_debug_set_wait_limit": ([ctypes.c_ulonglong], None),
     "moe_debug_withhold_arrivals": ([_I], None),
 }
@@ -53,7 +55,7 @@ for _name, (_args, _res) in _SIGS.items():
 EXPORTS = tuple(_SIGS)
 
 MOE_OK = 0
-STATUS_NAMES = {i: _lib.moe_status_str(i).decode() for i in range(9)}
+STATUS_NAMES = {i: _lib.moe_status_str(i).decode() for i in range(10)}
 
 
 class MoeError(RuntimeError):
@@ -154,6 +156,15 @@ def moe_layer_host(x_host, Wr, bias, gate, up, down, k, I, idx, w, y_host, ws,
     _check(_lib.moe_layer_host(_ptr(x_host), _ptr(Wr), _ptr(bias), _ptr(gate), _ptr(up),
                                _ptr(down), T, H, E, k, I, _ptr(idx), _ptr(w), _ptr(y_host),
                                _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_host")
+
+
+def moe_layer_noalloc(x, Wr, bias, gate, up, down, k, I, idx, w, y, stream=None) -> None:
+    """Single-token layer without a workspace (the library's fixed scratch)."""
+    T, H = x.shape
+    E = Wr.shape[0]
+    _check(_lib.moe_layer_noalloc(_ptr(x), _ptr(Wr), _ptr(bias), _ptr(gate), _ptr(up), _ptr(down),
+                                  T, H, E, k, I, _ptr(idx), _ptr(w), _ptr(y), _stream(stream)),
+           "moe_layer_noalloc")
 
 
 def moe_read_device_status(ws, stream=None):
