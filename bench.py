@@ -139,6 +139,25 @@ class ClockSampler:
                 "samples_inside_timed_region": len(inside)}
 
 
+def profiled_traffic(kernel_src, profile):
+    """DRAM bytes per launch recorded by the ncu summary in profiles/, if that
+    summary was taken of the kernel source as it is now (hash match)."""
+    import hashlib
+    try:
+        src = open(os.path.join(ROOT, kernel_src), "rb").read()
+        text = open(os.path.join(ROOT, "profiles", profile)).read()
+    except OSError:
+        return None
+    h = hashlib.sha256(src).hexdigest()[:16]
+    fields = dict(ln.split(":", 1) for ln in text.splitlines() if ":" in ln and not ln.startswith(" "))
+    if fields.get("source-sha256-16", "").strip() != h:
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -360,10 +379,14 @@ def main():
     peak, peak_kind = measured_peaks()
     call_us = ms_per_step * 1e3 / n_layers
     achieved = (step_bytes / n_layers) / (call_us * 1e-6) / 1e9
+    single = m.moe_layer_launch_count(T, H, E, k, I) == 1
+    traffic = profiled_traffic("quantized_routed_expert_02_gb300/csrc/decode_fused.cu",
+                               "decode_fused_a3b_decode.md") if (single and args.config == "a3b_decode") else None
     roofline = {
         "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-        "frac": round(achieved / peak, 4), "traffic": None,
-        "kernel": "moe_layer call (all launches of one call)",
+        "frac": round(achieved / peak, 4), "traffic": traffic,
+        "kernel": ("decode_fused_kernel (the only launch of a call; duration = timed region / calls)"
+                   if single else "moe_layer call (all launches of one call)"),
         "peak_kind": peak_kind,
         "algorithmic_bytes_per_call": step_bytes / n_layers,
         "achieved_incl_router_weight": round(
