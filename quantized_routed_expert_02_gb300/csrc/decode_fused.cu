@@ -191,6 +191,102 @@ __device__ __forceinline__ float block_chunk_dot(const uint8_t *blk, int s, int 
     return acc;
 }
 
+// Scale and min of sub-blocks 2c and 2c+1 of a block head, as d*sc*128 and
+// dmin*m (the 128 undoes the 1 + q/128 encoding of the codes).
+__device__ __forceinline__ void pair_scales(const uint4 &head, int c, float &A0, float &B0, float &A1,
+                                            float &B1) {
+    const int j0 = 2 * c, j1 = 2 * c + 1;
+    uint32_t sc0, m0, sc1, m1;
+    if (c < 2) {
+        sc0 = (head.y >> (8 * j0)) & 63u;
+        m0 = (head.z >> (8 * j0)) & 63u;
+        sc1 = (head.y >> (8 * j1)) & 63u;
+        m1 = (head.z >> (8 * j1)) & 63u;
+    } else {
+        const int a = j0 - 4, b = j1 - 4;
+        sc0 = ((head.w >> (8 * a)) & 15u) | (((head.y >> (8 * a + 6)) & 3u) << 4);
+        m0 = ((head.w >> (8 * a + 4)) & 15u) | (((head.z >> (8 * a + 6)) & 3u) << 4);
+        sc1 = ((head.w >> (8 * b)) & 15u) | (((head.y >> (8 * b + 6)) & 3u) << 4);
+        m1 = ((head.w >> (8 * b + 4)) & 15u) | (((head.z >> (8 * b + 6)) & 3u) << 4);
+    }
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&head.x));
+    const float d128 = dd.x * 128.0f;
+    A0 = d128 * u6_to_float(sc0);
+    A1 = d128 * u6_to_float(sc1);
+    B0 = dd.y * u6_to_float(m0);
+    B1 = dd.y * u6_to_float(m1);
+}
+
+// Dot of sub-blocks 2c (low nibbles of qs[32c..32c+31]) and 2c+1 (high
+// nibbles) of one block with the padded vector: `xs` points at the block's
+// element 64c (32 x values for 2c, then 32 for 2c+1), `s2` at the two
+// 32-element sums.  Four independent accumulators keep the FMA chains short.
+__device__ __forceinline__ float pair_dot(const uint8_t *blk, int c, const float *xs,
+                                          const float *s2) {
+    const uint4 head = *reinterpret_cast<const uint4 *>(blk);
+    const uint4 qa = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
+    const uint4 qb = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
+    const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+    for (int wi = 0; wi < 8; ++wi) {
+        const uint32_t lo = (w[wi] & 0x0F0F0F0Fu) | 0x80808080u;
+        const uint32_t hi = ((w[wi] >> 4) & 0x0F0F0F0Fu) | 0x80808080u;
+        const float4 xl = *reinterpret_cast<const float4 *>(xs + 4 * wi);
+        const float4 xh = *reinterpret_cast<const float4 *>(xs + 32 + 4 * wi);
+        a0 = fmaf(one_plus_q(lo, 0), xl.x, a0);
+        a1 = fmaf(one_plus_q(lo, 1), xl.y, a1);
+        a0 = fmaf(one_plus_q(lo, 2), xl.z, a0);
+        a1 = fmaf(one_plus_q(lo, 3), xl.w, a1);
+        b0 = fmaf(one_plus_q(hi, 0), xh.x, b0);
+        b1 = fmaf(one_plus_q(hi, 1), xh.y, b1);
+        b0 = fmaf(one_plus_q(hi, 2), xh.z, b0);
+        b1 = fmaf(one_plus_q(hi, 3), xh.w, b1);
+    }
+    float A0, B0, A1, B1;
+    pair_scales(head, c, A0, B0, A1, B1);
+    const float slo = s2[0], shi = s2[1];
+    // d*sc*sum(q x) - dmin*m*sum(x), with sum(q x) = 128*(acc - sum(x))
+    float acc = A0 * ((a0 + a1) - slo);
+    acc = fmaf(-B0, slo, acc);
+    acc = fmaf(A1, (b0 + b1) - shi, acc);
+    acc = fmaf(-B1, shi, acc);
+    return acc;
+}
+
+// One lane's share of a Q4_K row in shared memory: lane L takes sub-block
+// pair L%4 of blocks L/4, L/4+8, ...  `vec` is the padded vector, `sum32`
+// its 32-element sums.
+template <int NSB>
+__device__ __forceinline__ float row_dot_pairs(const uint8_t *row, int nsb_rt, const float *vec,
+                                               const float *sum32, int lane) {
+    const int nsb = NSB > 0 ? NSB : nsb_rt;
+    const int c = lane & 3;
+    float acc = 0.f;
+#pragma unroll
+    for (int s = lane >> 2; s < nsb; s += 8)
+        acc += pair_dot(row + s * kBlockBytes, c, vec + padded(s * kQK + 64 * c),
+                        sum32 + s * 8 + 2 * c);
+    return acc;
+}
+
+// Sum each 32-float run of the padded vector(s) into sum32; run q starts at
+// logical element 32*(q % runs_per_vec) of vector q / runs_per_vec.
+__device__ __forceinline__ void run_sums32(const float *vec, float *sum32, int count,
+                                           int runs_per_vec, int vec_stride) {
+    for (int q = threadIdx.x; q < count; q += kThreads) {
+        const int j = q / runs_per_vec, c = 32 * (q % runs_per_vec);
+        const float *v = vec + j * vec_stride + padded(c);
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int b = 0; b < 32; b += 2) {
+            s0 += v[b];
+            s1 += v[b + 1];
+        }
+        sum32[q] = s0 + s1;
+    }
+}
+
 // Sum each 16-float run of `count` runs of the padded vector(s) into vsum.
 // Run q starts at logical element 16*(q % runs_per_vec) of vector q / runs_per_vec.
 __device__ __forceinline__ void run_sums(const float *vec, float *vsum, int count, int runs_per_vec,
@@ -262,23 +358,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         *base_sh = c0 - c0 % (2ull * nblk);
         flags[1] = 0;
     }
-    // x -> padded shared vector and its run sums
-    for (int i = threadIdx.x; i < (H >> 2); i += kThreads)
-        *reinterpret_cast<float4 *>(vec + padded(4 * i)) = __ldg(reinterpret_cast<const float4 *>(p.x) + i);
-    __syncthreads();
-    run_sums(vec, vsum, H >> 4, H >> 4, 0);
-    __syncthreads();
+    // ---------------- 1. router logits (a share per CTA), grid barrier.
+    // The CTA's first logit is computed while x is staged: x and the router
+    // row are requested together, so their latencies overlap.
+    const uint64_t pol_last = l2_policy_evict_last();
+    {
+        const int e = blockIdx.x;
+        const bool logit = p.router_on && e < E;
+        const float *wr = p.Wr + size_t(logit ? e : 0) * H;
+        float a = 0.f;
+        for (int i = threadIdx.x; i < (H >> 2); i += kThreads) {
+            const float4 x4 = __ldg(reinterpret_cast<const float4 *>(p.x) + i);
+            if (logit) {
+                const float4 w4 = ldg_f4_policy(wr + 4 * i, pol_last);
+                a = fmaf(w4.x, x4.x, a);
+                a = fmaf(w4.y, x4.y, a);
+                a = fmaf(w4.z, x4.z, a);
+                a = fmaf(w4.w, x4.w, a);
+            }
+            *reinterpret_cast<float4 *>(vec + padded(4 * i)) = x4;
+        }
+        a = warp_sum(a);
+        if (lane == 0) red[warp] = a;
+        __syncthreads();
+        if (logit && threadIdx.x == 0) {
+            float sum = 0.f;
+            for (int w = 0; w < kWarps; ++w) sum += red[w];
+            p.logits[e] = sum + (p.bias ? p.bias[e] : 0.f);
+        }
+        run_sums32(vec, vsum, H >> 5, H >> 5, 0);
+        __syncthreads();
+    }
     const unsigned long long base = *base_sh;
     if (threadIdx.x == 0) TL_STAMP(p, 1);
 
-    // ---------------- 1. router logits (a share per CTA), grid barrier
     if (p.router_on) {
-        const uint64_t pol = l2_policy_evict_last();
-        for (int e = blockIdx.x; e < E; e += nblk) {
+        for (int e = blockIdx.x + nblk; e < E; e += nblk) {
             const float *wr = p.Wr + size_t(e) * H;
             float a = 0.f;
             for (int i = threadIdx.x; i < (H >> 2); i += kThreads) {
-                const float4 w4 = ldg_f4_policy(wr + 4 * i, pol);
+                const float4 w4 = ldg_f4_policy(wr + 4 * i, pol_last);
                 const float4 x4 = *reinterpret_cast<const float4 *>(vec + padded(4 * i));
                 a = fmaf(w4.x, x4.x, a);
                 a = fmaf(w4.y, x4.y, a);
@@ -436,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         const int e = sel_e[j];
         if (e >= 0 && e < E) {
             const uint8_t *src = ring + slot * p.slot_bytes;
-            const float g = warp_sum(row_lane_dot<NSB_H>(src, nsb_h, vec, vsum, lane));
-            const float uu = warp_sum(row_lane_dot<NSB_H>(src + row_gu, nsb_h, vec, vsum, lane));
+            const float g = warp_sum(row_dot_pairs<NSB_H>(src, nsb_h, vec, vsum, lane));
+            const float uu = warp_sum(row_dot_pairs<NSB_H>(src + row_gu, nsb_h, vec, vsum, lane));
             if (lane == 0) p.hbuf[size_t(j) * I + r] = silu_mul(g, uu);
         }
         __syncwarp();
@@ -454,20 +573,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     if (threadIdx.x == 0) TL_STAMP(p, 5);
     if (flags[1] == 0) {
         const int ip = padded_len(I);
-        for (int q = threadIdx.x; q < (k * I) >> 4; q += kThreads) {  // one 16-float run each
-            const int j = (16 * q) / I, c = (16 * q) % I;
-            const float4 *src = reinterpret_cast<const float4 *>(p.hbuf) + 4 * q;
-            float4 v[4];
+        for (int q = threadIdx.x; q < (k * I) >> 5; q += kThreads) {  // one 32-float run each
+            const int j = (32 * q) / I, c = (32 * q) % I;
+            const float4 *src = reinterpret_cast<const float4 *>(p.hbuf) + 8 * q;
+            float4 v[8];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) v[b] = __ldcg(src + b);
+            for (int b = 0; b < 8; ++b) v[b] = __ldcg(src + b);
             float *dst = vec + j * ip + padded(c);
-            float sum = 0.f;
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
+            for (int b = 0; b < 8; b += 2) {
                 *reinterpret_cast<float4 *>(dst + 4 * b) = v[b];
-                sum += (v[b].x + v[b].y) + (v[b].z + v[b].w);
+                *reinterpret_cast<float4 *>(dst + 4 * b + 4) = v[b + 1];
+                s0 += (v[b].x + v[b].y) + (v[b].z + v[b].w);
+                s1 += (v[b + 1].x + v[b + 1].y) + (v[b + 1].z + v[b + 1].w);
             }
-            vsum[q] = sum;
+            vsum[q] = s0 + s1;
         }
         __syncthreads();
         if (threadIdx.x == 0) TL_STAMP(p, 6);
@@ -497,14 +618,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             // fixed order; each chunk's partial dot is weighted by its slot's
             // router weight, then one warp reduction gives y (deterministic)
             float yacc = 0.f;
-            const int nchunks = k * nsb_i * 8;
-            for (int t = lane; t < nchunks; t += 32) {
-                const int j = t / (nsb_i * 8), rem = t % (nsb_i * 8);
-                const int sb = rem >> 3, cq = rem & 7;
+            const int per_j = (NSB_I > 0 ? NSB_I : nsb_i) * 4;   // (block, pair) units per slot
+            const int nunits = k * per_j;
+            for (int t = lane; t < nunits; t += 32) {
+                const int j = t / per_j, rem = t - j * per_j;
+                const int sb = rem >> 2, c = rem & 3;
                 const int e = sel_e[j];
                 if (e < 0 || e >= E) continue;
-                const float part = block_chunk_dot(src + j * jstride + sb * kBlockBytes, sb, cq,
-                                                   vec + j * ip, vsum + j * (I >> 4));
+                const float part = pair_dot(src + j * jstride + sb * kBlockBytes, c,
+                                            vec + j * ip + padded(sb * kQK + 64 * c),
+                                            vsum + j * (I >> 5) + sb * 8 + 2 * c);
                 yacc = fmaf(sel_w[j], part, yacc);
             }
             yacc = warp_sum(yacc);
