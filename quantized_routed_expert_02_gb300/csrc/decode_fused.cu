@@ -44,7 +44,7 @@ namespace fused {
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxNbw = 8;         // ring slots per warp
-constexpr int kHeadBytes = 2048;   // small shared arrays
+constexpr int kHeadBytes = 4096;   // small shared arrays
 
 // Optional phase timeline for profiling builds (-DMOEQ4K_TIMELINE): thread 0
 // of each CTA stamps the global timer at phase boundaries into the
@@ -305,10 +305,12 @@ __device__ __forceinline__ void run_sums(const float *vec, float *vsum, int coun
 // (acquire) until the counter reaches `target`.  All threads of the CTA call
 // it; returns false on time-out.
 __device__ __forceinline__ bool grid_sync(WsHeader *hdr, unsigned long long target,
-                                          uint64_t deadline, int *flag) {
+                                          uint64_t deadline, int *flag, bool publish_cta) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
+        // the release add publishes this thread's writes; other threads'
+        // writes (ordered before it by the CTA barrier) get a full fence
+        if (publish_cta) __threadfence();
         red_release_add_u64(&hdr->bar_arrivals, 1ull);
         bool ok = true;
         while (ld_acquire_u64(&hdr->bar_arrivals) < target) {
@@ -324,9 +326,6 @@ __device__ __forceinline__ bool grid_sync(WsHeader *hdr, unsigned long long targ
     return *flag == 0;
 }
 
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-    return v > bv || (v == bv && i < bi);
-}
 
 template <int NSB_H, int NSB_I>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params p) {
@@ -334,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     unsigned long long *base_sh = reinterpret_cast<unsigned long long *>(smem);
     int *sel_e = reinterpret_cast<int *>(base_sh + 1);
     float *sel_w = reinterpret_cast<float *>(sel_e + 32);
-    float *red = sel_w + 32;
-    int *flags = reinterpret_cast<int *>(red + 32);  // [0] barrier result, [1] abort
+    int *flags = reinterpret_cast<int *>(sel_w + 32);  // [0] barrier result, [1] abort
+    float *red = reinterpret_cast<float *>(flags + 4); // partial sums, then logits + ranks (2*kMaxE)
     float *vec = reinterpret_cast<float *>(smem + kHeadBytes);
     const int H = p.H, E = p.E, k = p.k, I = p.I;
     const int vec_pad = max(padded_len(H), k * padded_len(I));
@@ -415,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             __syncthreads();
         }
         if (threadIdx.x == 0) TL_STAMP(p, 2);
-        if (!grid_sync(p.hdr, base + nblk + p.withhold, deadline, flags)) {
+        if (!grid_sync(p.hdr, base + nblk + p.withhold, deadline, flags, false)) {
             if (threadIdx.x == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 1);
             cp_async_wait_all();
             return;  // no output written
@@ -425,65 +424,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     }
     if (threadIdx.x == 0) TL_STAMP(p, 8);
 
-    // ---------------- 2. top-k + renormalise (warp 0 of every CTA)
-    if (warp == 0) {
-        if (p.router_on) {
-            constexpr int kPer = kMaxE / 32;
-            float v[kPer];
-            bool taken[kPer];
-#pragma unroll
-            for (int s = 0; s < kPer; ++s) {
-                const int e = lane + 32 * s;
-                v[s] = (e < E) ? __ldcg(p.logits + e) : -INFINITY;
-                taken[s] = e >= E;
+    // ---------------- 2. top-k + renormalise, by rank: every CTA ranks the E
+    // logits in the order (value descending, index ascending); the logit of
+    // rank j < k is slot j.  G threads share the comparisons of one logit.
+    if (p.router_on) {
+        float *lsm = red;                     // E logits (red is free again)
+        int *rank = reinterpret_cast<int *>(lsm + kMaxE);
+        for (int e = threadIdx.x; e < E; e += kThreads) {
+            float v = __ldcg(p.logits + e);
+            lsm[e] = (v == v) ? v : -INFINITY;   // a NaN never ranks first
+            rank[e] = 0;
+        }
+        __syncthreads();
+        const int G = max(1, kThreads / E);      // threads per logit
+        const int per = (E + G - 1) / G;         // comparisons per thread
+        for (int t = threadIdx.x; t < E * G; t += kThreads) {
+            const int e = t / G, part = t % G;
+            const float ve = lsm[e];
+            int cnt = 0;
+            const int b0 = part * per, b1 = min(E, b0 + per);
+            for (int o = b0; o < b1; ++o) {
+                const float vo = lsm[o];
+                cnt += (vo > ve || (vo == ve && o < e)) ? 1 : 0;
             }
-            float sel_v = 0.f, vmax = 0.f;
-            int sel_i = 0;
-            for (int j = 0; j < k; ++j) {
-                float bv = -INFINITY;
-                int bi = 0x7fffffff;
-#pragma unroll
-                for (int s = 0; s < kPer; ++s) {
-                    const int e = lane + 32 * s;
-                    if (!taken[s] && better(v[s], e, bv, bi)) {
-                        bv = v[s];
-                        bi = e;
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                    if (better(ov, oi, bv, bi)) {
-                        bv = ov;
-                        bi = oi;
-                    }
-                }
-#pragma unroll
-                for (int s = 0; s < kPer; ++s)
-                    if (bi == lane + 32 * s) taken[s] = true;
-                if (j == 0) vmax = bv;
-                if (lane == j) {
-                    sel_v = bv;
-                    sel_i = bi;
-                }
-            }
-            const float ex = (lane < k) ? expf(sel_v - vmax) : 0.f;
+            if (cnt) atomicAdd(rank + e, cnt);
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += kThreads) {
+            const int r = rank[e];
+            if (r < k) sel_e[r] = e;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const float l = (lane < k) ? lsm[sel_e[lane]] : 0.f;
+            const float l0 = lsm[sel_e[0]];
+            const float ex = (lane < k) ? expf(l - l0) : 0.f;
             const float z = warp_sum(ex);
             if (lane < k) {
-                sel_e[lane] = sel_i;
                 sel_w[lane] = ex / z;
                 if (blockIdx.x == 0) {
-                    p.idx_out[lane] = sel_i;
+                    p.idx_out[lane] = sel_e[lane];
                     p.w_out[lane] = ex / z;
                 }
             }
-        } else if (lane < k) {
-            const int e = p.idx_in[lane];
-            sel_e[lane] = e;
-            sel_w[lane] = p.w_in[lane];
-            if (blockIdx.x == 0 && (e < 0 || e >= E)) record_status(p.hdr, MOE_ERR_EXPERT_RANGE, e);
         }
+    } else if (warp == 0 && lane < k) {
+        const int e = p.idx_in[lane];
+        sel_e[lane] = e;
+        sel_w[lane] = p.w_in[lane];
+        if (blockIdx.x == 0 && (e < 0 || e >= E)) record_status(p.hdr, MOE_ERR_EXPERT_RANGE, e);
     }
     __syncthreads();
     if (threadIdx.x == 0) TL_STAMP(p, 3);
@@ -565,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     if (threadIdx.x == 0) TL_STAMP(p, 4);
 
     // ---------------- 4. h complete everywhere -> down rows + combine
-    if (!grid_sync(p.hdr, base + 2ull * nblk + p.withhold, deadline, flags)) {
+    if (!grid_sync(p.hdr, base + 2ull * nblk + p.withhold, deadline, flags, true)) {
         if (threadIdx.x == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 4);
         flags[1] = 1;
     }
@@ -686,7 +675,6 @@ void *kernel_ptr() {
 void *pick_kernel(int H, int I) {
     const int a = H / kQK, b = I / kQK;
     if (a == 8 && b == 3) return kernel_ptr<8, 3>();
-    if (a == 16 && b == 6) return kernel_ptr<16, 6>();
     if (a == 1 && b == 1) return kernel_ptr<1, 1>();
     if (a == 8 && b == 4) return kernel_ptr<8, 4>();
     return kernel_ptr<0, 0>();
@@ -702,8 +690,7 @@ cudaError_t init_decode_fused(int dev, int num_sms) {
     cudaError_t err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (err != cudaSuccess) return err;
     g_fused_max_smem[dev] = optin;
-    void *ks[] = {kernel_ptr<8, 3>(), kernel_ptr<16, 6>(), kernel_ptr<1, 1>(), kernel_ptr<8, 4>(),
-                  kernel_ptr<0, 0>()};
+    void *ks[] = {kernel_ptr<8, 3>(), kernel_ptr<1, 1>(), kernel_ptr<8, 4>(), kernel_ptr<0, 0>()};
     for (void *kp : ks) {
         err = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (err != cudaSuccess) return err;
