@@ -36,6 +36,7 @@ moe_status moeq4k::device_info(int *sms, int *dev_out) {
             return MOE_ERR_CUDA;
         if (init_expert_ffn() != cudaSuccess) return MOE_ERR_CUDA;
         if (init_decode_fused(dev, n) != cudaSuccess) return MOE_ERR_CUDA;
+        if (init_prefill_tc(dev) != cudaSuccess) return MOE_ERR_CUDA;
         g_dev[dev].sms = n;
         g_dev[dev].id = dev;
         g_dev[dev].ready = true;
@@ -87,11 +88,20 @@ inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK 
 
 moe_status ffn_enqueue(const float *x, const int32_t *idx, const float *w, const void *gate,
                        const void *up, const void *down, int T, int H, int E, int k, int I,
-                       float *y, const Ws &ws, int sms, cudaStream_t s) {
+                       float *y, const Ws &ws, int sms, int dev, cudaStream_t s) {
     const WsLayout &L = ws.L;
     MOE_TRY(cuda_status(launch_permute(idx, T, k, E, ws.i32(L.counts), ws.i32(L.offs),
                                        ws.i32(L.perm), ws.i32(L.active), ws.i32(L.nactive),
                                        ws.hdr(), s)));
+    if (prefill_tc_supported(T, H, E, k, I)) {
+        MOE_TRY(cuda_status(launch_prefill_tc(
+            dev, x, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
+            static_cast<const uint8_t *>(down), T, H, E, k, I, ws.i32(L.offs), ws.i32(L.perm),
+            ws.i32(L.active), ws.i32(L.nactive), reinterpret_cast<__half *>(ws.base + L.x16),
+            reinterpret_cast<__half *>(ws.base + L.h16), ws.f32(L.o),
+            reinterpret_cast<TcChunk *>(ws.base + L.chunks), ws.hdr(), sms, g_wait_ns, s)));
+        return cuda_status(launch_combine(ws.f32(L.o), idx, w, T, H, E, k, y, sms, s));
+    }
     return cuda_status(launch_expert_ffn(
         x, idx, w, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
         static_cast<const uint8_t *>(down), T, H, E, k, I, y, ws.i32(L.offs), ws.i32(L.perm),
@@ -139,6 +149,8 @@ int moe_layer_launch_count(int T, int H, int E, int k, int I) {
     int sms = 0, dev = 0;
     if (device_info(&sms, &dev) != MOE_OK) return 0;
     if (decode_fused_supported(dev, T, H, E, k, I)) return 1;
+    if (prefill_tc_supported(T, H, E, k, I))
+        return 2 /* router */ + 1 /* permutation */ + 2 /* fp16 x, plan */ + 2 /* GEMMs */ + 1;
     return 2 /* router */ + 1 /* permutation */ + 3 /* gate/up, down, combine */;
 }
 
@@ -212,7 +224,7 @@ moe_status moe_ffn(const float *x, const int32_t *idx, const float *w, const voi
             W.f32(L.logits), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns,
             static_cast<cudaStream_t>(stream)));
     }
-    return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms,
+    return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -242,7 +254,7 @@ moe_status moe_layer(const float *x, const float *Wr, const float *bias, const v
             W.f32(L.logits), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns, s));
     }
     MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), s)));
-    return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, s);
+    return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev, s);
 }
 
 moe_status moe_layer_host(const float *x_host, const float *Wr, const float *bias,

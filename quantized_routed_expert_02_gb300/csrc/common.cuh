@@ -23,12 +23,20 @@ struct WsHeader {
     uint32_t status;                 // first device-side moe_status recorded (sticky)
     int32_t detail;                  // value that caused it
     unsigned long long bar_arrivals; // grid barrier: CTA arrivals since initialisation
-    uint32_t pad[60];
+    uint32_t tc_work[2];             // prefill GEMMs: next work item (gate/up, down)
+    int32_t tc_chunks;               // prefill GEMMs: expert chunks of <= 256 slots
+    uint32_t pad[57];
+};
+
+// One expert's chunk of at most 256 routed slots (prefill GEMM column tile).
+struct TcChunk {
+    int32_t e, tok_off, tok_cnt, pad;
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 struct WsLayout {
-    size_t counts, offs, active, nactive, perm, h, o, logits, xstage, ystage, total;
+    size_t counts, offs, active, nactive, perm, h, o, logits, x16, h16, chunks, xstage, ystage,
+        total;
 };
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -45,6 +53,9 @@ inline WsLayout ws_layout(int T, int H, int E, int k, int I, bool host_staging) 
     L.perm = off;    off = align256(off + sizeof(int32_t) * pairs);
     L.h = off;       off = align256(off + sizeof(float) * pairs * I);
     L.o = off;       off = align256(off + sizeof(float) * pairs * H);
+    L.x16 = off;     off = align256(off + 2 * size_t(T) * H);            // fp16 activations
+    L.h16 = off;     off = align256(off + 2 * pairs * I);                // fp16 SwiGLU output
+    L.chunks = off;  off = align256(off + sizeof(TcChunk) * (pairs / 256 + E + 1));
     L.xstage = off;
     L.ystage = off;
     if (host_staging) {

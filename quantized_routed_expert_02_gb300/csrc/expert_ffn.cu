@@ -212,6 +212,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
     }
 }
 
+cudaError_t launch_combine(const float *obuf, const int32_t *idx, const float *w, int T, int H,
+                           int E, int k, float *y, int num_sms, cudaStream_t s) {
+    const size_t total = size_t(T) * (H / 4);
+    const size_t g3s = (total + 255) / 256, g3cap = size_t(num_sms) * 16;
+    combine_kernel<<<int(g3s < g3cap ? g3s : g3cap), 256, 0, s>>>(obuf, idx, w, T, H, E, k, y);
+    return cudaGetLastError();
+}
+
 cudaError_t init_expert_ffn() {
     const int max_smem = int(sizeof(float) * kTokGroup * (kMaxHI + kMaxHI / 16));
     cudaError_t err = cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);

@@ -26,6 +26,18 @@ cudaError_t launch_expert_ffn(const float *x, const int32_t *idx, const float *w
                               float *hbuf, float *obuf, WsHeader *hdr, int num_sms,
                               cudaStream_t s);
 
+cudaError_t launch_combine(const float *obuf, const int32_t *idx, const float *w, int T, int H,
+                           int E, int k, float *y, int num_sms, cudaStream_t s);
+
+cudaError_t init_prefill_tc(int dev);
+bool prefill_tc_supported(int T, int H, int E, int k, int I);
+cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, const uint8_t *up,
+                              const uint8_t *down, int T, int H, int E, int k, int I,
+                              const int32_t *offs, const int32_t *perm, const int32_t *active,
+                              const int32_t *nactive, __half *x16, __half *h16, float *obuf,
+                              TcChunk *chunks, WsHeader *hdr, int num_sms,
+                              unsigned long long wait_ns, cudaStream_t s);
+
 cudaError_t init_decode_fused(int dev, int num_sms);
 bool decode_fused_supported(int dev, int T, int H, int E, int k, int I);
 // Wr == nullptr: routing comes from idx_in / w_in (moe_ffn); otherwise the

@@ -1,0 +1,451 @@
+// Prefill: the expert FFN of a large batch as two grouped GEMMs on the
+// tcgen05 tensor cores, with the Q4_K weights dequantised to fp16 in shared
+// memory on the way in.
+//
+// forward_qwen3_moe.rs (aprender-serve 0.35.0), step 2g of forward_qwen3_moe
+// runs every position through the layer on its own; tokens are independent,
+// so the slots routed to one expert form the columns of one GEMM per expert:
+//   gate/up:  G = Wg[e] X_e^T, U = Wu[e] X_e^T  (M = 128 weight rows per tile,
+//             N = up to 256 tokens, K = H), epilogue h = SiLU(G) * U (fp16);
+//   down:     O = Wd[e] H_e^T (K = I), epilogue o[p, row] in fp32, followed
+//             by the slot-ordered combine kernel.
+//
+// One persistent CTA per SM takes work items (expert chunk of <= 256 slots,
+// 128-row weight tile) from an atomic counter.  12 warps:
+//   warps 4-11  dequantise the Q4_K rows of the tile, 64 K per stage, into
+//               fp16 K-major tiles with the 128-byte swizzle (generic stores,
+//               then a proxy fence), two stages of raw bytes in flight;
+//   warps 1-3   gather the fp16 activation rows of the chunk with 16-byte
+//               cp.async into the same swizzled layout;
+//   thread 0    issues tcgen05.mma (fp16 x fp16 -> fp32 in tensor memory)
+//               when a stage is full and commits its completion to the
+//               stage's "empty" mbarrier;
+//   warps 0-3   read the accumulators back (tcgen05.ld) for the epilogue.
+// Every wait is bounded by a global-timer deadline and records
+// MOE_ERR_TIMEOUT when it runs out.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tcgen05.cuh"
+
+namespace moeq4k {
+namespace ptc {
+
+constexpr int kThreads = 384;
+constexpr int kBM = 128;   // weight rows per tile
+constexpr int kBN = 256;   // tokens per tile (max)
+constexpr int kBK = 64;    // K per stage
+constexpr int kTileA = kBM * kBK * 2;
+constexpr int kTileB = kBN * kBK * 2;
+constexpr int kHead = 2048;  // barriers, item info, token list
+constexpr int kLoaders = 96;   // warps 1-3
+constexpr int kDeq = 256;      // warps 4-11
+constexpr int kMaxStages = 6;
+
+struct Params {
+    int mode;                 // 0: gate/up + SwiGLU -> h16; 1: down -> o
+    const uint8_t *A0, *A1;   // gate/up (mode 0) or down (mode 1) blobs
+    size_t mat_bytes;         // bytes of one expert's matrix
+    int nsb;                  // Q4_K blocks per row (K / 256)
+    int K;                    // reduction length
+    int row_tiles;            // weight rows per expert / 128
+    const __half *B;          // x16 [T][H] (mode 0) or h16 [T*k][I] (mode 1)
+    int b_div;                // B row of slot p is p / b_div
+    const int32_t *offs, *perm;
+    const TcChunk *chunks;
+    WsHeader *hdr;            // work counters, chunk count, status
+    __half *h16;              // mode 0 output [T*k][I]
+    float *o;                 // mode 1 output [T*k][H]
+    int I, H;
+    int nstages, stage_bytes;
+    unsigned long long wait_ns;
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_t deadline,
+                                         WsHeader *hdr, int site) {
+    if (mbar_wait(bar, parity, deadline)) return true;
+    record_status(hdr, MOE_ERR_TIMEOUT, site);
+    return false;
+}
+
+__device__ __forceinline__ float u6f(uint32_t v) { return __uint_as_float(0x4B000000u | v) - 8388608.0f; }
+
+// (d*sc, dmin*m) of sub-blocks 2c and 2c+1 from a 16-byte block head.
+__device__ __forceinline__ void head_scales(const uint4 &h, int c, float &a0, float &b0, float &a1,
+                                            float &b1) {
+    const int j0 = 2 * c, j1 = 2 * c + 1;
+    uint32_t s0, m0, s1, m1;
+    if (c < 2) {
+        s0 = (h.y >> (8 * j0)) & 63u;
+        m0 = (h.z >> (8 * j0)) & 63u;
+        s1 = (h.y >> (8 * j1)) & 63u;
+        m1 = (h.z >> (8 * j1)) & 63u;
+    } else {
+        const int a = j0 - 4, b = j1 - 4;
+        s0 = ((h.w >> (8 * a)) & 15u) | (((h.y >> (8 * a + 6)) & 3u) << 4);
+        m0 = ((h.w >> (8 * a + 4)) & 15u) | (((h.z >> (8 * a + 6)) & 3u) << 4);
+        s1 = ((h.w >> (8 * b)) & 15u) | (((h.y >> (8 * b + 6)) & 3u) << 4);
+        m1 = ((h.w >> (8 * b + 4)) & 15u) | (((h.z >> (8 * b + 6)) & 3u) << 4);
+    }
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&h.x));
+    a0 = dd.x * u6f(s0);
+    a1 = dd.x * u6f(s1);
+    b0 = dd.y * u6f(m0);
+    b1 = dd.y * u6f(m1);
+}
+
+// 1 + q/128 as fp32 from byte i of v (bytes hold 0x80 | q).
+__device__ __forceinline__ float opq(uint32_t v, int i) {
+    return __uint_as_float(__byte_perm(v, 0x3F000000u, 0x7044u | (uint32_t(i) << 8)));
+}
+
+// Eight weights (codes in bytes i..i+3 of words v0, v1; w = a*q - b) as one
+// 16-byte chunk of fp16.
+__device__ __forceinline__ uint4 weights8(uint32_t v0, uint32_t v1, float a, float b) {
+    // w = a*q - b = (128a)*(1 + q/128) - (128a + b)
+    const float A = 128.0f * a, C = -(A + b);
+    uint4 r;
+    __half2 h;
+    h = __floats2half2_rn(fmaf(A, opq(v0, 0), C), fmaf(A, opq(v0, 1), C));
+    r.x = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2half2_rn(fmaf(A, opq(v0, 2), C), fmaf(A, opq(v0, 3), C));
+    r.y = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2half2_rn(fmaf(A, opq(v1, 0), C), fmaf(A, opq(v1, 1), C));
+    r.z = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2half2_rn(fmaf(A, opq(v1, 2), C), fmaf(A, opq(v1, 3), C));
+    r.w = *reinterpret_cast<uint32_t *>(&h);
+    return r;
+}
+
+struct RawStage {
+    uint4 head, q0, q1;  // block head and the 32 code bytes of this stage's 64 weights
+};
+
+__device__ __forceinline__ RawStage load_raw(const uint8_t *row, int s) {
+    const uint8_t *blk = row + (s >> 2) * kBlockBytes;
+    const int c = s & 3;
+    RawStage r;
+    r.head = __ldg(reinterpret_cast<const uint4 *>(blk));
+    r.q0 = __ldg(reinterpret_cast<const uint4 *>(blk + 16 + 32 * c));
+    r.q1 = __ldg(reinterpret_cast<const uint4 *>(blk + 32 + 32 * c));
+    return r;
+}
+
+// Write `nchunks` 16-byte chunks (weights 8j..8j+7 for j in [j0, j0+nchunks))
+// of row `r` of the stage's 64 weights into a swizzled tile.
+__device__ __forceinline__ void store_row(uint8_t *tile, int r, const RawStage &raw, int s, int j0,
+                                          int nchunks) {
+    float a0, b0, a1, b1;
+    head_scales(raw.head, s & 3, a0, b0, a1, b1);
+    const uint32_t w[8] = {raw.q0.x, raw.q0.y, raw.q0.z, raw.q0.w,
+                           raw.q1.x, raw.q1.y, raw.q1.z, raw.q1.w};
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+        if (jj < j0 || jj >= j0 + nchunks) continue;
+        // chunk jj < 4: low nibbles of code bytes 8jj..8jj+7 (sub-block 2c);
+        // chunk jj >= 4: high nibbles of bytes 8(jj-4).. (sub-block 2c+1)
+        const int wb = 2 * (jj & 3);
+        uint32_t v0, v1;
+        if (jj < 4) {
+            v0 = (w[wb] & 0x0F0F0F0Fu) | 0x80808080u;
+            v1 = (w[wb + 1] & 0x0F0F0F0Fu) | 0x80808080u;
+        } else {
+            v0 = ((w[wb] >> 4) & 0x0F0F0F0Fu) | 0x80808080u;
+            v1 = ((w[wb + 1] >> 4) & 0x0F0F0F0Fu) | 0x80808080u;
+        }
+        const uint4 out = jj < 4 ? weights8(v0, v1, a0, b0) : weights8(v0, v1, a1, b1);
+        *reinterpret_cast<uint4 *>(tile + tc::sw128_offset(r, 8 * jj)) = out;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Params p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + kMaxStages;
+    uint64_t *done = empty + kMaxStages;
+    uint64_t *drain = done + 1;
+    uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(drain + 1);
+    int *info = reinterpret_cast<int *>(tmem_ptr + 4);   // [0] item, [1] abort
+    int *toks = reinterpret_cast<int *>(smem + 1024);    // slot ids of the chunk (<= 256)
+    uint8_t *stages = smem + kHead;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int NS = p.nstages;
+    const int S = p.K / kBK;  // stages per item
+    const uint64_t deadline = global_timer_ns() + p.wait_ns;
+    const uint32_t tcols = p.mode == 0 ? 512u : 256u;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full + s, kLoaders + kDeq);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init(done, 1);
+        mbar_init(drain, 1);
+        info[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tc::tmem_alloc(tmem_ptr, tcols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t taddr = *tmem_ptr;
+    const int total = p.hdr->tc_chunks * p.row_tiles;
+
+    uint32_t gs = 0;     // stages processed by this CTA (same count in every role)
+    uint32_t items = 0;  // items processed by this CTA
+    while (true) {
+        if (tid == 0) info[0] = int(atomicAdd(&p.hdr->tc_work[p.mode], 1u));
+        __syncthreads();
+        const int item = info[0];
+        if (item >= total || info[1]) break;
+        const TcChunk ch = p.chunks[item / p.row_tiles];
+        const int rt = item % p.row_tiles;
+        const int ntok = ch.tok_cnt;
+        const int nmma = (ntok + 15) & ~15;
+        for (int n = tid; n < ntok; n += kThreads) toks[n] = p.perm[p.offs[ch.e] + ch.tok_off + n];
+        __syncthreads();
+
+        if (warp >= 4) {
+            // ---- dequantise weight rows into the A tile(s)
+            const int dq = tid - 128;
+            int m, r, j0, nch;
+            if (p.mode == 0) {
+                m = dq >> 7;       // 0 gate, 1 up
+                r = dq & 127;
+                j0 = 0;
+                nch = 8;
+            } else {
+                m = 0;
+                r = dq >> 1;
+                j0 = (dq & 1) * 4;  // low or high nibbles
+                nch = 4;
+            }
+            const uint8_t *base = (m == 0 ? p.A0 : p.A1) + size_t(ch.e) * p.mat_bytes +
+                                  size_t(rt * kBM + r) * p.nsb * kBlockBytes;
+            RawStage cur = load_raw(base, 0);
+            RawStage nxt = S > 1 ? load_raw(base, 1) : cur;
+            for (int s = 0; s < S; ++s) {
+                const uint32_t g = gs + s, slot = g % NS;
+                RawStage nn = (s + 2 < S) ? load_raw(base, s + 2) : nxt;
+                if (g >= uint32_t(NS) &&
+                    !wait_bar(empty + slot, ((g / NS) - 1) & 1, deadline, p.hdr, 11)) {
+                    info[1] = 1;
+                    break;
+                }
+                uint8_t *tile = stages + size_t(slot) * p.stage_bytes + m * kTileA;
+                store_row(tile, r, cur, s, j0, nch);
+                fence_proxy_async_smem();
+                mbar_arrive(full + slot);
+                cur = nxt;
+                nxt = nn;
+            }
+        } else if (warp >= 1) {
+            // ---- gather the chunk's activation rows (fp16) into the B tile
+            const int lt = tid - 32;
+            for (int s = 0; s < S; ++s) {
+                const uint32_t g = gs + s, slot = g % NS;
+                if (g >= uint32_t(NS) &&
+                    !wait_bar(empty + slot, ((g / NS) - 1) & 1, deadline, p.hdr, 12)) {
+                    info[1] = 1;
+                    break;
+                }
+                uint8_t *tile = stages + size_t(slot) * p.stage_bytes + (p.mode == 0 ? 2 : 1) * kTileA;
+                for (int c = lt; c < nmma * 8; c += kLoaders) {
+                    const int n = c >> 3, j = c & 7;
+                    const bool valid = n < ntok;
+                    const __half *src = p.B + size_t(valid ? toks[n] / p.b_div : 0) * p.K + s * kBK + 8 * j;
+                    tc::cp_async_16_zfill(tile + tc::sw128_offset(n, 8 * j), src, valid);
+                }
+                cp_async_commit();
+                if (s > 0) {
+                    cp_async_wait_pending(1);
+                    fence_proxy_async_smem();
+                    mbar_arrive(full + (g - 1) % NS);
+                }
+            }
+            cp_async_wait_pending(0);
+            fence_proxy_async_smem();
+            if (!info[1]) mbar_arrive(full + (gs + S - 1) % NS);
+        } else if (tid == 0) {
+            // ---- MMA issue
+            const uint32_t idesc = tc::idesc_f16_f32(kBM, nmma);
+            for (int s = 0; s < S; ++s) {
+                const uint32_t g = gs + s, slot = g % NS;
+                if (!wait_bar(full + slot, (g / NS) & 1, deadline, p.hdr, 13)) {
+                    info[1] = 1;
+                    break;
+                }
+                tc::fence_after_sync();
+                uint8_t *st = stages + size_t(slot) * p.stage_bytes;
+                const uint32_t a0 = smem_addr(st), a1 = a0 + kTileA;
+                const uint32_t b = a0 + (p.mode == 0 ? 2 : 1) * kTileA;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    const uint64_t bd = tc::smem_desc_sw128(b + 32 * kk);
+                    const bool acc = s > 0 || kk > 0;
+                    tc::mma_f16(taddr, tc::smem_desc_sw128(a0 + 32 * kk), bd, idesc, acc);
+                    if (p.mode == 0) tc::mma_f16(taddr + 256, tc::smem_desc_sw128(a1 + 32 * kk), bd, idesc, acc);
+                }
+                tc::commit_arrive(empty + slot);
+            }
+            tc::commit_arrive(done);
+        }
+
+        // ---- epilogue: warps 0-3 own TMEM lanes 0-127 (the tile's weight rows)
+        if (warp < 4) {
+            // tcgen05.ld is warp-collective: keep the decision warp-uniform
+            const bool ok = __all_sync(0xffffffffu, wait_bar(done, items & 1, deadline, p.hdr, 14));
+            tc::fence_after_sync();
+            if (ok && !info[1]) {
+                const int row = rt * kBM + warp * 32 + lane;
+                const uint32_t lanebase = taddr + (uint32_t(warp * 32) << 16);
+                for (int n0 = 0; n0 < nmma; n0 += 8) {
+                    float g[8];
+                    tc::tmem_ld8(lanebase + n0, g);
+                    if (p.mode == 0) {
+                        float u[8];
+                        tc::tmem_ld8(lanebase + 256 + n0, u);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int n = n0 + j;
+                            if (n < ntok)
+                                p.h16[size_t(toks[n]) * p.I + row] = __float2half_rn(silu_mul(g[j], u[j]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int n = n0 + j;
+                            if (n < ntok) p.o[size_t(toks[n]) * p.H + row] = g[j];
+                        }
+                    }
+                }
+            }
+            tc::fence_before_sync();
+        }
+        gs += S;
+        ++items;
+        __syncthreads();
+    }
+    // every issued MMA must be complete before the tensor memory is released
+    if (tid == 0) {
+        tc::commit_arrive(drain);
+        wait_bar(drain, 0, global_timer_ns() + p.wait_ns, p.hdr, 15);
+    }
+    cp_async_wait_all();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(taddr, tcols);
+}
+
+// x fp32 [T][H] -> fp16
+__global__ void to_half_kernel(const float *__restrict__ x, __half *__restrict__ x16, size_t n4) {
+    for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n4;
+         i += size_t(gridDim.x) * blockDim.x) {
+        const float4 v = reinterpret_cast<const float4 *>(x)[i];
+        __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t *>(&a);
+        o.y = *reinterpret_cast<uint32_t *>(&b);
+        reinterpret_cast<uint2 *>(x16)[i] = o;
+    }
+}
+
+// Chunks of <= 256 slots per active expert, and the work counters reset.
+__global__ void plan_kernel(const int32_t *__restrict__ offs, const int32_t *__restrict__ active,
+                            const int32_t *__restrict__ nactive, TcChunk *chunks, WsHeader *hdr) {
+    if (threadIdx.x != 0) return;
+    int nc = 0;
+    const int na = *nactive;
+    for (int a = 0; a < na; ++a) {
+        const int e = active[a];
+        const int n = offs[e + 1] - offs[e];
+        for (int t = 0; t < n; t += kBN) {
+            chunks[nc].e = e;
+            chunks[nc].tok_off = t;
+            chunks[nc].tok_cnt = min(kBN, n - t);
+            ++nc;
+        }
+    }
+    hdr->tc_chunks = nc;
+    hdr->tc_work[0] = 0;
+    hdr->tc_work[1] = 0;
+}
+
+}  // namespace ptc
+
+namespace {
+int g_tc_smem_optin[64];
+}
+
+cudaError_t init_prefill_tc(int dev) {
+    int optin = 0;
+    cudaError_t err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (err != cudaSuccess) return err;
+    g_tc_smem_optin[dev] = optin;
+    return cudaFuncSetAttribute(ptc::grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin);
+}
+
+bool prefill_tc_supported(int T, int H, int E, int k, int I) {
+    return T * k >= 2048 && I % ptc::kBM == 0 && H % ptc::kBM == 0;
+}
+
+cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, const uint8_t *up,
+                              const uint8_t *down, int T, int H, int E, int k, int I,
+                              const int32_t *offs, const int32_t *perm, const int32_t *active,
+                              const int32_t *nactive, __half *x16, __half *h16, float *obuf,
+                              TcChunk *chunks, WsHeader *hdr, int num_sms,
+                              unsigned long long wait_ns, cudaStream_t s) {
+    using namespace ptc;
+    const size_t n4 = size_t(T) * H / 4;
+    to_half_kernel<<<num_sms * 4, 256, 0, s>>>(x, x16, n4);
+    plan_kernel<<<1, 32, 0, s>>>(offs, active, nactive, chunks, hdr);
+
+    Params p = {};
+    p.offs = offs;
+    p.perm = perm;
+    p.chunks = chunks;
+    p.hdr = hdr;
+    p.h16 = h16;
+    p.o = obuf;
+    p.I = I;
+    p.H = H;
+    p.wait_ns = wait_ns;
+    const int optin = g_tc_smem_optin[dev];
+
+    // gate/up: A = gate and up rows (I per expert), B = x16 rows (slot p -> token p / k)
+    p.mode = 0;
+    p.A0 = gate;
+    p.A1 = up;
+    p.mat_bytes = size_t(I) * (H / kQK) * kBlockBytes;
+    p.nsb = H / kQK;
+    p.K = H;
+    p.row_tiles = I / kBM;
+    p.B = x16;
+    p.b_div = k;
+    p.stage_bytes = 2 * kTileA + kTileB;
+    p.nstages = std::min(kMaxStages, (optin - kHead) / p.stage_bytes);
+    grouped_gemm_kernel<<<num_sms, kThreads, kHead + p.nstages * p.stage_bytes, s>>>(p);
+
+    // down: A = down rows (H per expert), B = h16 rows (slot p)
+    p.mode = 1;
+    p.A0 = down;
+    p.A1 = down;
+    p.mat_bytes = size_t(H) * (I / kQK) * kBlockBytes;
+    p.nsb = I / kQK;
+    p.K = I;
+    p.row_tiles = H / kBM;
+    p.B = h16;
+    p.b_div = 1;
+    p.stage_bytes = kTileA + kTileB;
+    p.nstages = std::min(kMaxStages, (optin - kHead) / p.stage_bytes);
+    grouped_gemm_kernel<<<num_sms, kThreads, kHead + p.nstages * p.stage_bytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace moeq4k

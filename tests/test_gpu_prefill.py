@@ -1,0 +1,41 @@
+"""Large batches run the tensor-core grouped GEMMs (tcgen05, fp16 operands,
+fp32 accumulation); compared with the fp64 oracle on sampled tokens, with
+ragged expert chunks (more than 256 slots for an expert, fewer than 16)."""
+import numpy as np
+import pytest
+
+from quantized_routed_expert_02_gb300 import synth
+from tests.cases import layer_case
+from tests.test_gpu_parity import check_layer, m, run_layer  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    # T, H, E, k, I, wr_std, zipf
+    (1024, 512, 16, 2, 256, 0.05, False),
+    (700, 768, 8, 4, 512, 0.05, False),
+    (2048, 256, 64, 1, 256, 0.05, True),
+    (513, 1024, 32, 8, 768, 0.03, True),
+]
+
+
+@pytest.mark.parametrize("T,H,E,k,I,std,zipf", SHAPES)
+def test_prefill_shapes(m, T, H, E, k, I, std, zipf):
+    shape = synth.custom_shape(T, H, E, k, I, wr_std=std, zipf_bias=zipf,
+                               cfg_id=70 + (T + H + E + k + I) % 20)
+    assert m.moe_layer_launch_count(T, H, E, k, I) == 8   # the tensor-core path
+    sample = tuple(range(0, T, max(1, T // 48))) + (T - 1,)
+    case = layer_case(shape, 0, sample)
+    idx, w, y, _, _ = run_layer(m, case)
+    check_layer(case, idx, w, y)
+
+
+def test_prefill_repeat_is_bitwise(m):
+    shape = synth.custom_shape(1024, 512, 16, 2, 256, cfg_id=88)
+    case = layer_case(shape, 0, (0, 1, 1023))
+    s = shape
+    _, _, y1, d, ws = run_layer(m, case)
+    for _ in range(2):
+        m.moe_layer(d["x"], d["Wr"], d["bias"], d["gate"], d["up"], d["down"], s.k, s.I,
+                    d["idx"], d["w"], d["y"], ws)
+        np.testing.assert_array_equal(d["y"].cpu().numpy(), y1)
