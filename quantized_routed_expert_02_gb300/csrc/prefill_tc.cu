@@ -12,17 +12,20 @@
 //
 // One persistent CTA per SM takes work items (expert chunk of <= 256 slots,
 // 128-row weight tile) from an atomic counter.  12 warps:
-//   warps 4-11  dequantise the Q4_K rows of the tile, 64 K per stage, into
-//               fp16 K-major tiles with the 128-byte swizzle (generic stores,
-//               then a proxy fence), two stages of raw bytes in flight;
+//   thread 1    stages the raw Q4_K bytes of the tile one block column at a
+//               time (128 rows x 144 B) with a 2-D TMA copy
+//               (cp.async.bulk.tensor) into a ring of raw stages;
+//   warps 4-11  dequantise them, 64 K per stage, into fp16 K-major tiles with
+//               the 128-byte swizzle (generic stores, then a proxy fence);
 //   warps 1-3   gather the fp16 activation rows of the chunk with 16-byte
-//               cp.async into the same swizzled layout;
+//               cp.async into the same swizzled layout, one row per thread;
 //   thread 0    issues tcgen05.mma (fp16 x fp16 -> fp32 in tensor memory)
 //               when a stage is full and commits its completion to the
 //               stage's "empty" mbarrier;
 //   warps 0-3   read the accumulators back (tcgen05.ld) for the epilogue.
 // Every wait is bounded by a global-timer deadline and records
 // MOE_ERR_TIMEOUT when it runs out.
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -46,6 +49,7 @@ constexpr int kDeq = 256;      // warps 4-11
 constexpr int kMaxStages = 6;
 
 struct Params {
+    CUtensorMap map0, map1;   // raw Q4_K bytes of A0 / A1 as [E*rows][nsb*144] uint8
     int mode;                 // 0: gate/up + SwiGLU -> h16; 1: down -> o
     const uint8_t *A0, *A1;   // gate/up (mode 0) or down (mode 1) blobs
     size_t mat_bytes;         // bytes of one expert's matrix
@@ -60,9 +64,23 @@ struct Params {
     __half *h16;              // mode 0 output [T*k][I]
     float *o;                 // mode 1 output [T*k][H]
     int I, H;
-    int nstages, stage_bytes;
+    int rows_per_expert;      // I (mode 0) or H (mode 1)
+    int nstages, stage_bytes; // fp16 operand ring
+    int nraw, raw_bytes;      // raw Q4_K ring (one block column of the tile per stage)
+    int raw_off;              // byte offset of the raw ring
     unsigned long long wait_ns;
 };
+
+constexpr int kRawTile = kBM * kBlockBytes;  // 128 rows x 144 B
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
 
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_t deadline,
                                          WsHeader *hdr, int site) {
@@ -124,13 +142,13 @@ struct RawStage {
     uint4 head, q0, q1;  // block head and the 32 code bytes of this stage's 64 weights
 };
 
-__device__ __forceinline__ RawStage load_raw(const uint8_t *row, int s) {
-    const uint8_t *blk = row + (s >> 2) * kBlockBytes;
+// The 48 bytes of K-stage s (head + codes) of one row of a raw block tile.
+__device__ __forceinline__ RawStage raw_from_smem(const uint8_t *blk, int s) {
     const int c = s & 3;
     RawStage r;
-    r.head = __ldg(reinterpret_cast<const uint4 *>(blk));
-    r.q0 = __ldg(reinterpret_cast<const uint4 *>(blk + 16 + 32 * c));
-    r.q1 = __ldg(reinterpret_cast<const uint4 *>(blk + 32 + 32 * c));
+    r.head = *reinterpret_cast<const uint4 *>(blk);
+    r.q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
+    r.q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
     return r;
 }
 
@@ -161,11 +179,13 @@ __device__ __forceinline__ void store_row(uint8_t *tile, int r, const RawStage &
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kMaxStages;
-    uint64_t *done = empty + kMaxStages;
+    uint64_t *rfull = empty + kMaxStages;
+    uint64_t *rempty = rfull + kMaxStages;
+    uint64_t *done = rempty + kMaxStages;
     uint64_t *drain = done + 1;
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(drain + 1);
     int *info = reinterpret_cast<int *>(tmem_ptr + 4);   // [0] item, [1] abort
@@ -183,6 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Params 
             mbar_init(full + s, kLoaders + kDeq);
             mbar_init(empty + s, 1);
         }
+        for (int s = 0; s < p.nraw; ++s) {
+            mbar_init(rfull + s, 1);
+            mbar_init(rempty + s, kDeq);
+        }
         mbar_init(done, 1);
         mbar_init(drain, 1);
         info[1] = 0;
@@ -195,6 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Params 
     const uint32_t taddr = *tmem_ptr;
     const int total = p.hdr->tc_chunks * p.row_tiles;
 
+    uint8_t *raw = smem + p.raw_off;
+    const int NR = p.nraw;
+    const int nsb = p.nsb;  // raw block-column stages per item
+    uint32_t grs = 0;    // raw stages processed by this CTA
     uint32_t gs = 0;     // stages processed by this CTA (same count in every role)
     uint32_t items = 0;  // items processed by this CTA
     while (true) {
@@ -210,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Params 
         __syncthreads();
 
         if (warp >= 4) {
-            // ---- dequantise weight rows into the A tile(s)
+            // ---- dequantise weight rows (raw block tiles in shared memory) into the A tile(s)
             const int dq = tid - 128;
             int m, r, j0, nch;
             if (p.mode == 0) {
@@ -224,13 +252,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Params 
                 j0 = (dq & 1) * 4;  // low or high nibbles
                 nch = 4;
             }
-            const uint8_t *base = (m == 0 ? p.A0 : p.A1) + size_t(ch.e) * p.mat_bytes +
-                                  size_t(rt * kBM + r) * p.nsb * kBlockBytes;
-            RawStage cur = load_raw(base, 0);
-            RawStage nxt = S > 1 ? load_raw(base, 1) : cur;
             for (int s = 0; s < S; ++s) {
                 const uint32_t g = gs + s, slot = g % NS;
-                RawStage nn = (s + 2 < S) ? load_raw(base, s + 2) : nxt;
+                const uint32_t rg = grs + (s >> 2), rslot = rg % NR;
+                if ((s & 3) == 0 && !wait_bar(rfull + rslot, (rg / NR) & 1, deadline, p.hdr, 16)) {
+                    info[1] = 1;
+                    break;
+                }
+                const RawStage cur = raw_from_smem(
+                    raw + size_t(rslot) * p.raw_bytes + m * kRawTile + r * kBlockBytes, s);
+                if ((s & 3) == 3) mbar_arrive(rempty + rslot);  // raw tile fully read
                 if (g >= uint32_t(NS) &&
                     !wait_bar(empty + slot, ((g / NS) - 1) & 1, deadline, p.hdr, 11)) {
                     info[1] = 1;
@@ -240,12 +271,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Params 
                 store_row(tile, r, cur, s, j0, nch);
                 fence_proxy_async_smem();
                 mbar_arrive(full + slot);
-                cur = nxt;
-                nxt = nn;
             }
         } else if (warp >= 1) {
-            // ---- gather the chunk's activation rows (fp16) into the B tile
+            // ---- gather the chunk's activation rows (fp16) into the B tile: one
+            // row per thread per pass, 8 x 16 B per row per stage
             const int lt = tid - 32;
+            const __half *rowsrc[3];
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+                const int n = lt + q * kLoaders;
+                rowsrc[q] = (n < ntok) ? p.B + size_t(toks[n] / p.b_div) * p.K : p.B;
+            }
             for (int s = 0; s < S; ++s) {
                 const uint32_t g = gs + s, slot = g % NS;
                 if (g >= uint32_t(NS) &&
@@ -254,11 +290,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Params 
                     break;
                 }
                 uint8_t *tile = stages + size_t(slot) * p.stage_bytes + (p.mode == 0 ? 2 : 1) * kTileA;
-                for (int c = lt; c < nmma * 8; c += kLoaders) {
-                    const int n = c >> 3, j = c & 7;
-                    const bool valid = n < ntok;
-                    const __half *src = p.B + size_t(valid ? toks[n] / p.b_div : 0) * p.K + s * kBK + 8 * j;
-                    tc::cp_async_16_zfill(tile + tc::sw128_offset(n, 8 * j), src, valid);
+#pragma unroll
+                for (int q = 0; q < 3; ++q) {
+                    const int n = lt + q * kLoaders;
+                    if (n < nmma) {
+                        const bool valid = n < ntok;
+                        const __half *src = rowsrc[q] + s * kBK;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            tc::cp_async_16_zfill(tile + tc::sw128_offset(n, 8 * j), valid ? src + 8 * j : p.B, valid);
+                    }
                 }
                 cp_async_commit();
                 if (s > 0) {
@@ -293,6 +334,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Params 
                 tc::commit_arrive(empty + slot);
             }
             tc::commit_arrive(done);
+        } else if (tid == 1) {
+            // ---- raw Q4_K block tiles by TMA, all block columns of the item (its own
+            // thread: it may wait on the raw ring while loaders and MMA make progress)
+                for (int b = 0; b < nsb; ++b) {
+                    const uint32_t rg = grs + b, rslot = rg % NR;
+                    if (rg >= uint32_t(NR) &&
+                        !wait_bar(rempty + rslot, ((rg / NR) - 1) & 1, deadline, p.hdr, 17)) {
+                        info[1] = 1;
+                        break;
+                    }
+                    uint8_t *dst = raw + size_t(rslot) * p.raw_bytes;
+                    const int y = ch.e * p.rows_per_expert + rt * kBM;
+                    mbar_arrive_expect_tx(rfull + rslot, p.mode == 0 ? 2 * kRawTile : kRawTile);
+                    tma_load_2d(dst, &p.map0, b * kBlockBytes, y, rfull + rslot);
+                    if (p.mode == 0) tma_load_2d(dst + kRawTile, &p.map1, b * kBlockBytes, y, rfull + rslot);
+                }
         }
 
         // ---- epilogue: warps 0-3 own TMEM lanes 0-127 (the tile's weight rows)
@@ -327,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Params 
             tc::fence_before_sync();
         }
         gs += S;
+        grs += nsb;
         ++items;
         __syncthreads();
     }
@@ -380,13 +438,40 @@ __global__ void plan_kernel(const int32_t *__restrict__ offs, const int32_t *__r
 
 namespace {
 int g_tc_smem_optin[64];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Raw bytes of one matrix family as a 2-D uint8 tensor: E*rows rows of
+// nsb*144 bytes, box = one block column of 128 rows.
+bool encode_q4k_map(CUtensorMap *map, const void *base, int E, int rows, int nsb) {
+    const cuuint64_t dims[2] = {cuuint64_t(nsb) * kBlockBytes, cuuint64_t(E) * rows};
+    const cuuint64_t strides[1] = {cuuint64_t(nsb) * kBlockBytes};
+    const cuuint32_t box[2] = {cuuint32_t(kBlockBytes), cuuint32_t(ptc::kBM)};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+}  // namespace
 
 cudaError_t init_prefill_tc(int dev) {
     int optin = 0;
     cudaError_t err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (err != cudaSuccess) return err;
     g_tc_smem_optin[dev] = optin;
+    if (g_encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (err != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return err != cudaSuccess ? err : cudaErrorNotSupported;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
     return cudaFuncSetAttribute(ptc::grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 optin);
 }
@@ -426,11 +511,19 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     p.nsb = H / kQK;
     p.K = H;
     p.row_tiles = I / kBM;
+    p.rows_per_expert = I;
     p.B = x16;
     p.b_div = k;
     p.stage_bytes = 2 * kTileA + kTileB;
-    p.nstages = std::min(kMaxStages, (optin - kHead) / p.stage_bytes);
-    grouped_gemm_kernel<<<num_sms, kThreads, kHead + p.nstages * p.stage_bytes, s>>>(p);
+    p.raw_bytes = 2 * kRawTile;
+    p.nstages = 2;
+    p.nraw = 2;
+    p.raw_off = kHead + p.nstages * p.stage_bytes;
+    if (!encode_q4k_map(&p.map0, gate, E, I, H / kQK) || !encode_q4k_map(&p.map1, up, E, I, H / kQK))
+        return cudaErrorInvalidValue;
+    size_t smem = size_t(p.raw_off) + size_t(p.nraw) * p.raw_bytes;
+    if (smem > size_t(optin)) return cudaErrorInvalidValue;
+    grouped_gemm_kernel<<<num_sms, kThreads, smem, s>>>(p);
 
     // down: A = down rows (H per expert), B = h16 rows (slot p)
     p.mode = 1;
@@ -440,11 +533,19 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     p.nsb = I / kQK;
     p.K = I;
     p.row_tiles = H / kBM;
+    p.rows_per_expert = H;
     p.B = h16;
     p.b_div = 1;
     p.stage_bytes = kTileA + kTileB;
-    p.nstages = std::min(kMaxStages, (optin - kHead) / p.stage_bytes);
-    grouped_gemm_kernel<<<num_sms, kThreads, kHead + p.nstages * p.stage_bytes, s>>>(p);
+    p.raw_bytes = kRawTile;
+    p.nstages = 3;
+    p.nraw = 3;
+    p.raw_off = kHead + p.nstages * p.stage_bytes;
+    if (!encode_q4k_map(&p.map0, down, E, H, I / kQK)) return cudaErrorInvalidValue;
+    p.map1 = p.map0;
+    smem = size_t(p.raw_off) + size_t(p.nraw) * p.raw_bytes;
+    if (smem > size_t(optin)) return cudaErrorInvalidValue;
+    grouped_gemm_kernel<<<num_sms, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
