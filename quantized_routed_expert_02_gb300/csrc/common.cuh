@@ -53,7 +53,7 @@ inline WsLayout ws_layout(int T, int H, int E, int k, int I, bool host_staging) 
     L.perm = off;    off = align256(off + sizeof(int32_t) * pairs);
     L.h = off;       off = align256(off + sizeof(float) * pairs * I);
     L.o = off;       off = align256(off + sizeof(float) * pairs * H);
-    L.x16 = off;     off = align256(off + 2 * size_t(T) * H);            // fp16 activations
+    L.x16 = off;     off = align256(off + 2 * pairs * H);                // fp16 activations, sorted rows
     L.h16 = off;     off = align256(off + 2 * pairs * I);                // fp16 SwiGLU output
     L.chunks = off;  off = align256(off + sizeof(TcChunk) * (pairs / 256 + E + 1));
     L.xstage = off;

@@ -9,6 +9,9 @@
 //             N = up to 256 tokens, K = H), epilogue h = SiLU(G) * U (fp16);
 //   down:     O = Wd[e] H_e^T (K = I), epilogue o[p, row] in fp32, followed
 //             by the slot-ordered combine kernel.
+// The activations are first gathered into expert-sorted rows (fp16), and h
+// is written in that order too, so every activation tile is one contiguous
+// block of rows.
 //
 // One persistent CTA per SM takes work items (expert chunk of <= 256 slots,
 // 128-row weight tile) from an atomic counter.  12 warps:
@@ -17,8 +20,9 @@
 //               (cp.async.bulk.tensor) into a ring of raw stages;
 //   warps 4-11  dequantise them, 64 K per stage, into fp16 K-major tiles with
 //               the 128-byte swizzle (generic stores, then a proxy fence);
-//   warps 1-3   gather the fp16 activation rows of the chunk with 16-byte
-//               cp.async into the same swizzled layout, one row per thread;
+//   thread 2    loads the chunk's activation tile (256 rows x 64 K, fp16,
+//               rows in expert-sorted order) with one 2-D TMA copy that
+//               applies the 128-byte swizzle;
 //   thread 0    issues tcgen05.mma (fp16 x fp16 -> fp32 in tensor memory)
 //               when a stage is full and commits its completion to the
 //               stage's "empty" mbarrier;
@@ -44,24 +48,23 @@ constexpr int kBK = 64;    // K per stage
 constexpr int kTileA = kBM * kBK * 2;
 constexpr int kTileB = kBN * kBK * 2;
 constexpr int kHead = 2048;  // barriers, item info, token list
-constexpr int kLoaders = 96;   // warps 1-3
 constexpr int kDeq = 256;      // warps 4-11
 constexpr int kMaxStages = 6;
 
 struct Params {
     CUtensorMap map0, map1;   // raw Q4_K bytes of A0 / A1 as [E*rows][nsb*144] uint8
+    CUtensorMap mapB;         // activations [T*k sorted rows][K] fp16, 128-byte swizzle
     int mode;                 // 0: gate/up + SwiGLU -> h16; 1: down -> o
     const uint8_t *A0, *A1;   // gate/up (mode 0) or down (mode 1) blobs
     size_t mat_bytes;         // bytes of one expert's matrix
     int nsb;                  // Q4_K blocks per row (K / 256)
     int K;                    // reduction length
     int row_tiles;            // weight rows per expert / 128
-    const __half *B;          // x16 [T][H] (mode 0) or h16 [T*k][I] (mode 1)
-    int b_div;                // B row of slot p is p / b_div
+
     const int32_t *offs, *perm;
     const TcChunk *chunks;
     WsHeader *hdr;            // work counters, chunk count, status
-    __half *h16;              // mode 0 output [T*k][I]
+    __half *h16;              // mode 0 output [T*k sorted rows][I]
     float *o;                 // mode 1 output [T*k][H]
     int I, H;
     int rows_per_expert;      // I (mode 0) or H (mode 1)
@@ -200,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(full + s, kLoaders + kDeq);
+            mbar_init(full + s, kDeq + 1);
             mbar_init(empty + s, 1);
         }
         for (int s = 0; s < p.nraw; ++s) {
@@ -272,45 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 fence_proxy_async_smem();
                 mbar_arrive(full + slot);
             }
-        } else if (warp >= 1) {
-            // ---- gather the chunk's activation rows (fp16) into the B tile: one
-            // row per thread per pass, 8 x 16 B per row per stage
-            const int lt = tid - 32;
-            const __half *rowsrc[3];
-#pragma unroll
-            for (int q = 0; q < 3; ++q) {
-                const int n = lt + q * kLoaders;
-                rowsrc[q] = (n < ntok) ? p.B + size_t(toks[n] / p.b_div) * p.K : p.B;
-            }
-            for (int s = 0; s < S; ++s) {
-                const uint32_t g = gs + s, slot = g % NS;
-                if (g >= uint32_t(NS) &&
-                    !wait_bar(empty + slot, ((g / NS) - 1) & 1, deadline, p.hdr, 12)) {
-                    info[1] = 1;
-                    break;
-                }
-                uint8_t *tile = stages + size_t(slot) * p.stage_bytes + (p.mode == 0 ? 2 : 1) * kTileA;
-#pragma unroll
-                for (int q = 0; q < 3; ++q) {
-                    const int n = lt + q * kLoaders;
-                    if (n < nmma) {
-                        const bool valid = n < ntok;
-                        const __half *src = rowsrc[q] + s * kBK;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            tc::cp_async_16_zfill(tile + tc::sw128_offset(n, 8 * j), valid ? src + 8 * j : p.B, valid);
-                    }
-                }
-                cp_async_commit();
-                if (s > 0) {
-                    cp_async_wait_pending(1);
-                    fence_proxy_async_smem();
-                    mbar_arrive(full + (g - 1) % NS);
-                }
-            }
-            cp_async_wait_pending(0);
-            fence_proxy_async_smem();
-            if (!info[1]) mbar_arrive(full + (gs + S - 1) % NS);
         } else if (tid == 0) {
             // ---- MMA issue
             const uint32_t idesc = tc::idesc_f16_f32(kBM, nmma);
@@ -334,6 +298,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 tc::commit_arrive(empty + slot);
             }
             tc::commit_arrive(done);
+        } else if (tid == 2) {
+            // ---- activation tile of each stage by TMA (256 sorted rows x 64 K)
+            const int row0 = p.offs[ch.e] + ch.tok_off;
+            for (int s2 = 0; s2 < S; ++s2) {
+                const uint32_t g = gs + s2, slot = g % NS;
+                if (g >= uint32_t(NS) &&
+                    !wait_bar(empty + slot, ((g / NS) - 1) & 1, deadline, p.hdr, 12)) {
+                    info[1] = 1;
+                    break;
+                }
+                uint8_t *tile = stages + size_t(slot) * p.stage_bytes + (p.mode == 0 ? 2 : 1) * kTileA;
+                mbar_arrive_expect_tx(full + slot, kTileB);
+                tma_load_2d(tile, &p.mapB, s2 * kBK, row0, full + slot);
+            }
         } else if (tid == 1) {
             // ---- raw Q4_K block tiles by TMA, all block columns of the item (its own
             // thread: it may wait on the raw ring while loaders and MMA make progress)
@@ -359,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             tc::fence_after_sync();
             if (ok && !info[1]) {
                 const int row = rt * kBM + warp * 32 + lane;
+                const int pos0 = p.offs[ch.e] + ch.tok_off;  // sorted row of column 0
                 const uint32_t lanebase = taddr + (uint32_t(warp * 32) << 16);
                 for (int n0 = 0; n0 < nmma; n0 += 8) {
                     float g[8];
@@ -370,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         for (int j = 0; j < 8; ++j) {
                             const int n = n0 + j;
                             if (n < ntok)
-                                p.h16[size_t(toks[n]) * p.I + row] = __float2half_rn(silu_mul(g[j], u[j]));
+                                p.h16[size_t(pos0 + n) * p.I + row] = __float2half_rn(silu_mul(g[j], u[j]));
                         }
                     } else {
 #pragma unroll
@@ -400,16 +379,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     if (warp == 0) tc::tmem_dealloc(taddr, tcols);
 }
 
-// x fp32 [T][H] -> fp16
-__global__ void to_half_kernel(const float *__restrict__ x, __half *__restrict__ x16, size_t n4) {
-    for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n4;
+// Activations in expert-sorted order: row i of xs = x[perm[i] / k] as fp16.
+__global__ void gather_half_kernel(const float *__restrict__ x, const int32_t *__restrict__ perm,
+                                   const int32_t *__restrict__ offs, int E, int k, int H,
+                                   __half *__restrict__ xs) {
+    const int nrows = offs[E];
+    const int per_row = H / 4;
+    const size_t total = size_t(nrows) * per_row;
+    for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total;
          i += size_t(gridDim.x) * blockDim.x) {
-        const float4 v = reinterpret_cast<const float4 *>(x)[i];
+        const int r = int(i / per_row), c = int(i % per_row);
+        const int t = perm[r] / k;
+        const float4 v = reinterpret_cast<const float4 *>(x + size_t(t) * H)[c];
         __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
         uint2 o;
         o.x = *reinterpret_cast<uint32_t *>(&a);
         o.y = *reinterpret_cast<uint32_t *>(&b);
-        reinterpret_cast<uint2 *>(x16)[i] = o;
+        reinterpret_cast<uint2 *>(xs + size_t(r) * H)[c] = o;
     }
 }
 
@@ -457,6 +443,18 @@ bool encode_q4k_map(CUtensorMap *map, const void *base, int E, int rows, int nsb
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+// Sorted activation rows as a 2-D fp16 tensor [rows][K]; box = 256 rows x 64
+// K, stored with the 128-byte swizzle the MMA descriptors expect.
+bool encode_act_map(CUtensorMap *map, const void *base, int rows, int K) {
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(ptc::kBK), cuuint32_t(ptc::kBN)};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 }  // namespace
 
 cudaError_t init_prefill_tc(int dev) {
@@ -487,9 +485,9 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
                               TcChunk *chunks, WsHeader *hdr, int num_sms,
                               unsigned long long wait_ns, cudaStream_t s) {
     using namespace ptc;
-    const size_t n4 = size_t(T) * H / 4;
-    to_half_kernel<<<num_sms * 4, 256, 0, s>>>(x, x16, n4);
+    gather_half_kernel<<<num_sms * 8, 256, 0, s>>>(x, perm, offs, E, k, H, x16);
     plan_kernel<<<1, 32, 0, s>>>(offs, active, nactive, chunks, hdr);
+    const int rows = T * k;
 
     Params p = {};
     p.offs = offs;
@@ -512,8 +510,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     p.K = H;
     p.row_tiles = I / kBM;
     p.rows_per_expert = I;
-    p.B = x16;
-    p.b_div = k;
+    if (!encode_act_map(&p.mapB, x16, rows, H)) return cudaErrorInvalidValue;
     p.stage_bytes = 2 * kTileA + kTileB;
     p.raw_bytes = 2 * kRawTile;
     p.nstages = 2;
@@ -534,8 +531,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     p.K = I;
     p.row_tiles = H / kBM;
     p.rows_per_expert = H;
-    p.B = h16;
-    p.b_div = 1;
+    if (!encode_act_map(&p.mapB, h16, rows, I)) return cudaErrorInvalidValue;
     p.stage_bytes = kTileA + kTileB;
     p.raw_bytes = kRawTile;
     p.nstages = 3;
