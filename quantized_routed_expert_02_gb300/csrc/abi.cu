@@ -35,6 +35,7 @@ moe_status moeq4k::device_info(int *sms, int *dev_out) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return MOE_ERR_CUDA;
         if (init_expert_ffn() != cudaSuccess) return MOE_ERR_CUDA;
+        if (init_router() != cudaSuccess) return MOE_ERR_CUDA;
         if (init_decode_fused(dev, n) != cudaSuccess) return MOE_ERR_CUDA;
         if (init_prefill_tc(dev) != cudaSuccess) return MOE_ERR_CUDA;
         g_dev[dev].sms = n;
@@ -149,9 +150,10 @@ int moe_layer_launch_count(int T, int H, int E, int k, int I) {
     int sms = 0, dev = 0;
     if (device_info(&sms, &dev) != MOE_OK) return 0;
     if (decode_fused_supported(dev, T, H, E, k, I)) return 1;
+    const int router = T >= 256 ? 1 : 2;
     if (prefill_tc_supported(T, H, E, k, I))
-        return 2 /* router */ + 1 /* permutation */ + 2 /* fp16 x, plan */ + 2 /* GEMMs */ + 1;
-    return 2 /* router */ + 1 /* permutation */ + 3 /* gate/up, down, combine */;
+        return router + 1 /* permutation */ + 2 /* fp16 rows, plan */ + 2 /* GEMMs */ + 1;
+    return router + 1 /* permutation */ + 3 /* gate/up, down, combine */;
 }
 
 void moe_debug_set_wait_limit(unsigned long long ns) { g_wait_ns = ns ? ns : 1000000000ull; }

@@ -43,6 +43,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Like mbar_try_wait, but the thread may be suspended (up to about
+// `suspend_ns`) until the phase completes instead of returning at once:
+// waiting threads then take no issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -53,6 +69,14 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // `deadline` (global timer, ns).  Returns false on time-out.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t deadline) {
     while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() > deadline) return false;
+    }
+    return true;
+}
+
+// Bounded wait that lets the waiting thread sleep between checks.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint64_t deadline) {
+    while (!mbar_try_wait_sleep(bar, parity, 100000u)) {
         if (global_timer_ns() > deadline) return false;
     }
     return true;

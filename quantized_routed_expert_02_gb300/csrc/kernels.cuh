@@ -11,6 +11,7 @@ moe_status device_info(int *sms, int *dev_out);
 // Shape limits shared by every entry point.
 moe_status validate_shape(int T, int H, int E, int k, int I);
 
+cudaError_t init_router();
 cudaError_t launch_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
                           int k, int32_t *idx, float *w, float *logits, cudaStream_t s);
 

@@ -87,7 +87,7 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_t deadline,
                                          WsHeader *hdr, int site) {
-    if (mbar_wait(bar, parity, deadline)) return true;
+    if (mbar_wait_sleep(bar, parity, deadline)) return true;
     record_status(hdr, MOE_ERR_TIMEOUT, site);
     return false;
 }

@@ -61,20 +61,18 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
 }
 
-__global__ void __launch_bounds__(256) router_topk_kernel(const float *__restrict__ logits,
-                                                          int T, int E, int k,
-                                                          int32_t *__restrict__ idx,
-                                                          float *__restrict__ w) {
+// Top-k of one token's E logits (read from `lg`, bias already added) by one
+// warp: k rounds of a warp-wide arg-max with the order (value descending,
+// index ascending); writes idx[0..k) and the renormalised weights.
+__device__ __forceinline__ void warp_topk(const float *lg, int E, int k, int32_t *idx, float *w) {
     constexpr int kPer = kMaxE / 32;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= T) return;
+    const int lane = threadIdx.x & 31;
     float v[kPer];
     bool taken[kPer];
 #pragma unroll
     for (int s = 0; s < kPer; ++s) {
         int e = lane + 32 * s;
-        v[s] = (e < E) ? logits[size_t(t) * E + e] : -INFINITY;
+        v[s] = (e < E) ? lg[e] : -INFINITY;
         taken[s] = (e >= E);
     }
     float sel_v = 0.f;   // lane j keeps slot j's logit
@@ -112,14 +110,116 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
     float ex = (lane < k) ? expf(sel_v - vmax) : 0.f;
     float z = warp_sum(ex);
     if (lane < k) {
-        idx[size_t(t) * k + lane] = sel_i;
-        w[size_t(t) * k + lane] = ex / z;
+        idx[lane] = sel_i;
+        w[lane] = ex / z;
     }
+}
+
+__global__ void __launch_bounds__(256) router_topk_kernel(const float *__restrict__ logits,
+                                                          int T, int E, int k,
+                                                          int32_t *__restrict__ idx,
+                                                          float *__restrict__ w) {
+    const int warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    warp_topk(logits + size_t(t) * E, E, k, idx + size_t(t) * k, w + size_t(t) * k);
+}
+
+// ---------------------------------------------------------------------------
+// Large batches: logits of 32 tokens x all E experts per CTA as a shared-
+// memory-tiled fp32 GEMM (each thread a 4 x 4 register tile, K in chunks of
+// 32, double-buffered), then the top-k of each token by one warp from the
+// CTA's logits in shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kRT = 32;   // tokens per CTA
+constexpr int kRE = 128;  // experts per pass
+constexpr int kRK = 32;   // K per chunk
+constexpr int kRouterBigSmem = int(sizeof(float)) * (2 * kRK * kRT + 2 * kRK * kRE + kRT * (kMaxE + 1));
+
+__global__ void __launch_bounds__(256) router_big_kernel(const float *__restrict__ x,
+                                                         const float *__restrict__ Wr,
+                                                         const float *__restrict__ bias, int T,
+                                                         int H, int E, int k,
+                                                         int32_t *__restrict__ idx,
+                                                         float *__restrict__ w) {
+    // dynamic shared memory: xs[2][kRK][kRT], ws[2][kRK][kRE] (k-major), lg[kRT][kMaxE + 1]
+    extern __shared__ __align__(16) float rsm[];
+    float (*xs)[kRK][kRT] = reinterpret_cast<float (*)[kRK][kRT]>(rsm);
+    float (*ws)[kRK][kRE] = reinterpret_cast<float (*)[kRK][kRE]>(rsm + 2 * kRK * kRT);
+    float (*lg)[kMaxE + 1] = reinterpret_cast<float (*)[kMaxE + 1]>(rsm + 2 * kRK * kRT + 2 * kRK * kRE);
+    const int tid = threadIdx.x, ty = tid >> 5, tx = tid & 31;
+    const int t0 = blockIdx.x * kRT;
+    const int nchunk = H / kRK;
+    for (int e0 = 0; e0 < E; e0 += kRE) {
+        float acc[4][4] = {};
+        auto load = [&](int c, int buf) {
+            // x: 32 tokens x 32 k = 256 float4, one per thread
+            {
+                const int t = tid >> 3, q = tid & 7;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t0 + t < T) v = __ldg(reinterpret_cast<const float4 *>(x + size_t(t0 + t) * H + c * kRK) + q);
+                xs[buf][4 * q + 0][t] = v.x;
+                xs[buf][4 * q + 1][t] = v.y;
+                xs[buf][4 * q + 2][t] = v.z;
+                xs[buf][4 * q + 3][t] = v.w;
+            }
+            // Wr: 128 experts x 32 k = 1024 float4, four per thread
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int f = tid + 256 * r, e = f >> 3, q = f & 7;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (e0 + e < E) v = __ldg(reinterpret_cast<const float4 *>(Wr + size_t(e0 + e) * H + c * kRK) + q);
+                ws[buf][4 * q + 0][e] = v.x;
+                ws[buf][4 * q + 1][e] = v.y;
+                ws[buf][4 * q + 2][e] = v.z;
+                ws[buf][4 * q + 3][e] = v.w;
+            }
+        };
+        load(0, 0);
+        __syncthreads();
+        for (int c = 0; c < nchunk; ++c) {
+            const int buf = c & 1;
+            if (c + 1 < nchunk) load(c + 1, buf ^ 1);
+#pragma unroll 8
+            for (int kk = 0; kk < kRK; ++kk) {
+                const float4 a = *reinterpret_cast<const float4 *>(&xs[buf][kk][ty * 4]);
+                const float4 b = *reinterpret_cast<const float4 *>(&ws[buf][kk][tx * 4]);
+                const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = e0 + tx * 4 + j;
+                if (e < E) lg[ty * 4 + i][e] = acc[i][j] + (bias ? bias[e] : 0.f);
+            }
+        __syncthreads();
+    }
+    // top-k: warp ty takes tokens ty, ty+8, ty+16, ty+24
+    for (int i = ty; i < kRT; i += 8) {
+        const int t = t0 + i;
+        if (t < T) warp_topk(&lg[i][0], E, k, idx + size_t(t) * k, w + size_t(t) * k);
+    }
+}
+
+cudaError_t init_router() {
+    return cudaFuncSetAttribute(router_big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kRouterBigSmem);
 }
 
 cudaError_t launch_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
                           int k, int32_t *idx, float *w, float *logits, cudaStream_t s) {
     dim3 blk(256);
+    if (T >= 256) {
+        router_big_kernel<<<(T + kRT - 1) / kRT, blk, kRouterBigSmem, s>>>(x, Wr, bias, T, H, E, k, idx, w);
+        return cudaGetLastError();
+    }
     if (T <= 2) {
         dim3 grid((E + 7) / 8, (T + 1) / 2);
         router_logits_kernel<2><<<grid, blk, 0, s>>>(x, Wr, bias, T, H, E, logits);
