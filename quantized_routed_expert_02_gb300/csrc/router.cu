@@ -180,6 +180,9 @@ __global__ void __launch_bounds__(256) router_big_kernel(const float *__restrict
         for (int c = 0; c < nchunk; ++c) {
             const int buf = c & 1;
             if (c + 1 < nchunk) load(c + 1, buf ^ 1);
+            // two-level sum: a fresh partial per 32-wide chunk keeps the fp32
+            // rounding of the 2048-term dot products small
+            float part[4][4] = {};
 #pragma unroll 8
             for (int kk = 0; kk < kRK; ++kk) {
                 const float4 a = *reinterpret_cast<const float4 *>(&xs[buf][kk][ty * 4]);
@@ -188,8 +191,12 @@ __global__ void __launch_bounds__(256) router_big_kernel(const float *__restrict
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                    for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
             }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] += part[i][j];
             __syncthreads();
         }
 #pragma unroll
