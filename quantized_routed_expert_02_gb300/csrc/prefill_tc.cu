@@ -15,18 +15,19 @@
 //
 // One persistent CTA per SM takes work items (expert chunk of <= 256 slots,
 // 128-row weight tile) from an atomic counter.  12 warps:
-//   thread 1    stages the raw Q4_K bytes of the tile one block column at a
+//   thread 32   stages the raw Q4_K bytes of the tile one block column at a
 //               time (128 rows x 144 B) with a 2-D TMA copy
 //               (cp.async.bulk.tensor) into a ring of raw stages;
 //   warps 4-11  dequantise them, 64 K per stage, into fp16 K-major tiles with
 //               the 128-byte swizzle (generic stores, then a proxy fence);
-//   thread 2    loads the chunk's activation tile (256 rows x 64 K, fp16,
+//   thread 64   loads the chunk's activation tile (256 rows x 64 K, fp16,
 //               rows in expert-sorted order) with one 2-D TMA copy that
 //               applies the 128-byte swizzle;
 //   thread 0    issues tcgen05.mma (fp16 x fp16 -> fp32 in tensor memory)
 //               when a stage is full and commits its completion to the
 //               stage's "empty" mbarrier;
-//   warps 0-3   read the accumulators back (tcgen05.ld) for the epilogue.
+//   warps 0-3   read the accumulators back (tcgen05.ld) for the epilogue;
+//               while the main loop runs they park on a named barrier.
 // Every wait is bounded by a global-timer deadline and records
 // MOE_ERR_TIMEOUT when it runs out.
 #include <cuda.h>
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     uint64_t *done = rempty + kMaxStages;
     uint64_t *drain = done + 1;
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(drain + 1);
-    int *info = reinterpret_cast<int *>(tmem_ptr + 4);   // [0] item, [1] abort
+    int *info = reinterpret_cast<int *>(tmem_ptr + 4);   // [0] item, [1] abort, [2] accumulators ready
     int *toks = reinterpret_cast<int *>(smem + 1024);    // slot ids of the chunk (<= 256)
     uint8_t *stages = smem + kHead;
 
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 tc::commit_arrive(empty + slot);
             }
             tc::commit_arrive(done);
-        } else if (tid == 2) {
+        } else if (tid == 64) {
             // ---- activation tile of each stage by TMA (256 sorted rows x 64 K)
             const int row0 = p.offs[ch.e] + ch.tok_off;
             for (int s2 = 0; s2 < S; ++s2) {
@@ -312,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 mbar_arrive_expect_tx(full + slot, kTileB);
                 tma_load_2d(tile, &p.mapB, s2 * kBK, row0, full + slot);
             }
-        } else if (tid == 1) {
+        } else if (tid == 32) {
             // ---- raw Q4_K block tiles by TMA, all block columns of the item (its own
             // thread: it may wait on the raw ring while loaders and MMA make progress)
                 for (int b = 0; b < nsb; ++b) {
@@ -332,8 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
         // ---- epilogue: warps 0-3 own TMEM lanes 0-127 (the tile's weight rows)
         if (warp < 4) {
-            // tcgen05.ld is warp-collective: keep the decision warp-uniform
-            const bool ok = __all_sync(0xffffffffu, wait_bar(done, items & 1, deadline, p.hdr, 14));
+            // idle threads sleep on a CTA barrier; thread 0 alone waits for the MMAs
+            named_bar_sync(2, 128);
+            if (tid == 0) info[2] = wait_bar(done, items & 1, deadline, p.hdr, 14) ? 1 : 0;
+            named_bar_sync(2, 128);
+            const bool ok = info[2] != 0;
             tc::fence_after_sync();
             if (ok && !info[1]) {
                 const int row = rt * kBM + warp * 32 + lane;
