@@ -204,12 +204,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(full + s, kDeq + 1);
+            mbar_init(full + s, kDeq / 32 + 1);   // one arrival per dequant warp + the TMA
             mbar_init(empty + s, 1);
         }
         for (int s = 0; s < p.nraw; ++s) {
             mbar_init(rfull + s, 1);
-            mbar_init(rempty + s, kDeq);
+            mbar_init(rempty + s, kDeq / 32);
         }
         mbar_init(done, 1);
         mbar_init(drain, 1);
@@ -265,7 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 const RawStage cur = raw_from_smem(
                     raw + size_t(rslot) * p.raw_bytes + m * kRawTile + r * kBlockBytes, s);
-                if ((s & 3) == 3) mbar_arrive(rempty + rslot);  // raw tile fully read
+                if ((s & 3) == 3) {  // raw tile fully read by this warp
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(rempty + rslot);
+                }
                 if (g >= uint32_t(NS) &&
                     !wait_bar(empty + slot, ((g / NS) - 1) & 1, deadline, p.hdr, 11)) {
                     info[1] = 1;
@@ -274,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 uint8_t *tile = stages + size_t(slot) * p.stage_bytes + m * kTileA;
                 store_row(tile, r, cur, s, j0, nch);
                 fence_proxy_async_smem();
-                mbar_arrive(full + slot);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full + slot);
             }
         } else if (tid == 0) {
             // ---- MMA issue
