@@ -14,11 +14,11 @@
 // block of rows.
 //
 // One persistent CTA per SM takes work items (expert chunk of <= 256 slots,
-// 128-row weight tile) from an atomic counter.  20 warps:
+// 128-row weight tile) from an atomic counter.  12 warps:
 //   thread 32   stages the raw Q4_K bytes of the tile one block column at a
 //               time (128 rows x 144 B) with a 2-D TMA copy
 //               (cp.async.bulk.tensor) into a ring of raw stages;
-//   warps 4-19  dequantise them, 64 K per stage, into fp16 K-major tiles with
+//   warps 4-11  dequantise them, 64 K per stage, into fp16 K-major tiles with
 //               the 128-byte swizzle (generic stores, then a proxy fence);
 //   thread 64   loads the chunk's activation tile (256 rows x 64 K, fp16,
 //               rows in expert-sorted order) with one 2-D TMA copy that
@@ -42,14 +42,14 @@
 namespace moeq4k {
 namespace ptc {
 
-constexpr int kThreads = 640;
+constexpr int kThreads = 384;
 constexpr int kBM = 128;   // weight rows per tile
 constexpr int kBN = 256;   // tokens per tile (max)
 constexpr int kBK = 64;    // K per stage
 constexpr int kTileA = kBM * kBK * 2;
 constexpr int kTileB = kBN * kBK * 2;
 constexpr int kHead = 2048;  // barriers, item info, token list
-constexpr int kDeq = 512;      // warps 4-19
+constexpr int kDeq = 256;      // warps 4-11
 constexpr int kMaxStages = 6;
 
 struct Params {
@@ -243,20 +243,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
         if (warp >= 4) {
             // ---- dequantise weight rows (raw block tiles in shared memory) into the A tile(s)
-            // 512 threads over the stage's 64 K of 256 rows (gate/up: 32 weights
-            // each) or 128 rows (down: 16 weights each), in 16-byte chunks
             const int dq = tid - 128;
             int m, r, j0, nch;
             if (p.mode == 0) {
-                m = dq >> 8;        // 0 gate, 1 up
-                r = (dq >> 1) & 127;
-                j0 = (dq & 1) * 4;  // low or high nibbles
-                nch = 4;
+                m = dq >> 7;       // 0 gate, 1 up
+                r = dq & 127;
+                j0 = 0;
+                nch = 8;
             } else {
                 m = 0;
-                r = dq >> 2;
-                j0 = (dq & 3) * 2;
-                nch = 2;
+                r = dq >> 1;
+                j0 = (dq & 1) * 4;  // low or high nibbles
+                nch = 4;
             }
             for (int s = 0; s < S; ++s) {
                 const uint32_t g = gs + s, slot = g % NS;
