@@ -89,8 +89,10 @@ MOE_API int moe_version(void);
 /*
  * Bytes of device workspace that moe_router / moe_permute / moe_ffn /
  * moe_layer need for this shape (0 when the shape is invalid).  The
- * workspace holds the sticky status word, the permutation, the expert
- * activations h [T*k, I] and the per-slot outputs [T*k, H].
+ * workspace holds the sticky status word, a call counter and a 2 MB region
+ * of tagged values that single-token calls keep between calls (both at the
+ * same place for every shape), the permutation, the expert activations
+ * h [T*k, I] and the per-slot outputs [T*k, H].
  */
 MOE_API size_t moe_workspace_bytes(int T, int H, int E, int k, int I);
 
@@ -101,8 +103,12 @@ MOE_API size_t moe_workspace_bytes(int T, int H, int E, int k, int I);
 MOE_API int moe_layer_launch_count(int T, int H, int E, int k, int I);
 
 /*
- * Zero the workspace header (status word and counters).  Call once after
- * allocating a workspace and whenever the sticky status should be cleared.
+ * Zero the workspace header (status word, counters) and the region of
+ * tagged values that single-token calls keep between calls: the first
+ * min(ws_bytes, 256 B + 2 MB) bytes.  Call once after allocating a
+ * workspace, before its first use (single-token calls rely on that region
+ * starting at zero), and whenever the sticky status should be cleared.  A
+ * workspace large enough for several shapes may serve all of them.
  * Enqueued on `stream`.
  */
 MOE_API moe_status moe_workspace_init(void *ws_dev, size_t ws_bytes, void *stream);
@@ -185,11 +191,11 @@ MOE_API moe_status moe_read_device_status(const void *ws_dev, void *stream, int3
  *
  * Scratch: a fixed 256 KB array in device global memory defined by the
  * library (held on every GPU that loads it until the process exits).  It
- * fits k*I <= 65216 and E <= 256; larger shapes return
+ * fits k*I <= 32480 and E <= 256; larger shapes return
  * MOE_ERR_SCRATCH_LIMIT.  Shapes the single-token kernel does not take
  * return MOE_ERR_INVALID_SHAPE.  The call allocates and frees nothing; it
- * clears the scratch's status word and barrier counter with an async memset
- * on `stream`, then launches one kernel.  All calls share the array: calls
+ * clears the scratch's status word with an async memset on `stream`, then
+ * launches one kernel.  All calls share the array: calls
  * that overlap on the GPU race and must be serialised by the caller.
  * The first call on each device looks up the array's device address; make
  * that first call before any stream capture.  Only argument and launch
@@ -204,10 +210,11 @@ MOE_API moe_status moe_layer_noalloc(const float *x_dev, const float *Wr_dev, co
  * Test hooks for the bounded device-side waits (not for production use).
  * moe_debug_set_wait_limit: upper bound, in ns, of every device-side wait
  * of later calls (0 restores the default of 1 s).  moe_debug_withhold_arrivals:
- * make the grid barrier of later single-token calls wait for n CTAs that
- * never arrive, so the wait runs out; such a call records MOE_ERR_TIMEOUT in
- * the workspace status, writes no output, and leaves the barrier counters
- * dirty: re-initialise the workspace (moe_workspace_init) afterwards.
+ * n != 0 makes CTA 0 of later single-token calls publish none of its router
+ * logits and h values, so the other CTAs' waits for them run out; such a
+ * call records MOE_ERR_TIMEOUT in the workspace status and writes no output.
+ * Re-initialise the workspace (moe_workspace_init) afterwards to clear the
+ * sticky status.
  */
 MOE_API void moe_debug_set_wait_limit(unsigned long long ns);
 MOE_API void moe_debug_withhold_arrivals(int n);

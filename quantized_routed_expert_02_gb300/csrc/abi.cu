@@ -1,6 +1,7 @@
 // C ABI of the moeq4k library: argument checks, workspace carving and launch
 // order.  Every entry point checks its arguments before anything is enqueued
 // and returns a moe_status; nothing here allocates device memory.
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -77,6 +78,12 @@ struct Ws {
     WsHeader *hdr() const { return reinterpret_cast<WsHeader *>(base); }
     int32_t *i32(size_t off) const { return reinterpret_cast<int32_t *>(base + off); }
     float *f32(size_t off) const { return reinterpret_cast<float *>(base + off); }
+    unsigned long long *u64(size_t off) const {
+        return reinterpret_cast<unsigned long long *>(base + off);
+    }
+    // the single-token kernel's profiling timeline: the per-slot activation
+    // regions, which that kernel does not use
+    int timeline_cap() const { return int((L.x16 - L.h) / sizeof(unsigned long long)); }
 };
 
 moe_status check_ws(void *ws, size_t ws_bytes, const WsLayout &L) {
@@ -163,7 +170,10 @@ void moe_debug_withhold_arrivals(int n) { g_withhold = n < 0 ? 0 : n; }
 moe_status moe_workspace_init(void *ws, size_t ws_bytes, void *stream) {
     MOE_TRY(check_ptr(ws, 256));
     if (ws_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
-    return cuda_status(cudaMemsetAsync(ws, 0, sizeof(WsHeader), static_cast<cudaStream_t>(stream)));
+    // the header and the tag region (the same place for every shape)
+    const size_t keep = sizeof(WsHeader) + align256(sizeof(unsigned long long) * kSyncWords);
+    return cuda_status(cudaMemsetAsync(ws, 0, std::min(ws_bytes, keep),
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
@@ -223,7 +233,7 @@ moe_status moe_ffn(const float *x, const int32_t *idx, const float *w, const voi
         return cuda_status(launch_decode_fused(
             dev, x, nullptr, nullptr, idx, w, nullptr, nullptr, static_cast<const uint8_t *>(gate),
             static_cast<const uint8_t *>(up), static_cast<const uint8_t *>(down), H, E, k, I, y,
-            W.f32(L.logits), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns,
+            W.u64(L.sync), W.hdr(), g_withhold, g_wait_ns, W.u64(L.h), W.timeline_cap(),
             static_cast<cudaStream_t>(stream)));
     }
     return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev,
@@ -253,7 +263,7 @@ moe_status moe_layer(const float *x, const float *Wr, const float *bias, const v
         return cuda_status(launch_decode_fused(
             dev, x, Wr, bias, nullptr, nullptr, idx, w, static_cast<const uint8_t *>(gate),
             static_cast<const uint8_t *>(up), static_cast<const uint8_t *>(down), H, E, k, I, y,
-            W.f32(L.logits), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns, s));
+            W.u64(L.sync), W.hdr(), g_withhold, g_wait_ns, W.u64(L.h), W.timeline_cap(), s));
     }
     MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), s)));
     return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev, s);

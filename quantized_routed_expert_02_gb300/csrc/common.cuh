@@ -16,13 +16,17 @@ constexpr int kMaxK = 32;
 constexpr int kMaxHI = 8192;
 
 // ---------------------------------------------------------------------------
-// Workspace layout (all regions 256-byte aligned).  The header is zeroed by
-// moe_workspace_init; everything else is scratch rewritten by every call.
+// Workspace layout (all regions 256-byte aligned).  moe_workspace_init zeroes
+// the whole workspace.  The header and the tag region must keep their
+// contents between calls; everything else is scratch rewritten by every call.
 // ---------------------------------------------------------------------------
 struct WsHeader {
     uint32_t status;                 // first device-side moe_status recorded (sticky)
     int32_t detail;                  // value that caused it
-    unsigned long long bar_arrivals; // grid barrier: CTA arrivals since initialisation
+    // Single-token kernel: every CTA adds 1 per call, so during the n-th call
+    // since initialisation (n = 0, 1, ...) a CTA's add returns a value in
+    // [n * nblk, (n + 1) * nblk); the call tags what it publishes with n + 1.
+    unsigned long long cta_calls;
     uint32_t tc_work[2];             // prefill GEMMs: next work item (gate/up, down)
     int32_t tc_chunks;               // prefill GEMMs: expert chunks of <= 256 slots
     uint32_t pad[57];
@@ -34,8 +38,17 @@ struct TcChunk {
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
+// Tag region of the single-token kernel, right after the header: the router
+// logits at words [0, E), h at words [kMaxE, kMaxE + k*I), each word
+// (call tag << 32 | fp32 bits).  Place and size are the same for every
+// shape, so the region never holds anything but tags (or the zeros of
+// moe_workspace_init), and tags only grow between initialisations: a word
+// left by an earlier call can never carry the current call's tag.
+constexpr size_t kSyncWords = size_t(kMaxE) + size_t(kMaxK) * kMaxHI;
+constexpr size_t kSyncHWord = kMaxE;
+
 struct WsLayout {
-    size_t counts, offs, active, nactive, perm, h, o, logits, x16, h16, chunks, xstage, ystage,
+    size_t sync, counts, offs, active, nactive, perm, h, o, logits, x16, h16, chunks, xstage, ystage,
         total;
 };
 
@@ -45,6 +58,7 @@ inline WsLayout ws_layout(int T, int H, int E, int k, int I, bool host_staging) 
     WsLayout L;
     size_t off = sizeof(WsHeader);
     size_t pairs = size_t(T) * k;
+    L.sync = off;    off = align256(off + sizeof(unsigned long long) * kSyncWords);
     L.counts = off;  off = align256(off + sizeof(int32_t) * E);
     L.offs = off;    off = align256(off + sizeof(int32_t) * (E + 1));
     L.active = off;  off = align256(off + sizeof(int32_t) * E);

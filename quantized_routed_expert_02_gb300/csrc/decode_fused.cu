@@ -13,25 +13,39 @@
 //  1. Every CTA stages x in shared memory and computes a share of the E
 //     router logits (Wr read with an L2 evict-last policy: it is re-read by
 //     every token, unlike the expert bytes, which are read evict-first).
-//  2. Grid barrier; every CTA reads the E logits and runs the same top-k and
+//     Each logit is published as one 64-bit word that also carries the
+//     call's tag, so readers need no barrier: they poll the words until
+//     every tag is the current one.
+//  2. Every CTA reads the E logits and runs the same top-k and
 //     renormalisation, so all CTAs know the k experts without a broadcast.
 //  3. The k*I gate/up row pairs are split evenly over the CTAs and, inside a
-//     CTA, over its warps.  Each warp streams its own rows into a private
-//     ring of shared-memory slots with 16-byte cp.async copies (every lane
+//     CTA, over its warps.  Each warp requests all of its rows at once into
+//     private shared-memory slots with 16-byte cp.async copies (every lane
 //     issues, so hundreds of requests per SM are in flight; one commit group
-//     per row, waited with cp.async.wait_group), decodes nibbles and 6-bit scales
-//     in registers, does fp32 FMAs against x in shared memory, and writes
-//     h = SiLU(g) * u to the workspace.  When the CTA's down rows (its share
-//     of the H output rows, for all k experts) fit beside the rings, all
-//     threads prefetch them right after the first gate/up rows.
-//  4. Grid barrier; each CTA stages h of all k slots, then for each of its
-//     output rows computes o_j = Wd[e_j][row] . h_j for j = 0..k-1 and
-//     y = sum_j w_j o_j in slot order: deterministic, no atomics.
-// The grid barrier is a monotonic 64-bit arrival counter (release add,
-// acquire polling), so it needs no reset between calls or graph replays.
-// The grid-barrier wait is bounded by a global-timer deadline; on expiry the
+//     per row, waited with cp.async.wait_group), then all threads request
+//     the CTA's down rows (its share of the H output rows, for all k
+//     experts).  Each value of h = SiLU(g) * u is published as a tagged word
+//     like the logits.
+//  4. Each CTA polls the k*I tagged h words into shared memory, then for
+//     each of its output rows computes o_j = Wd[e_j][row] . h_j for
+//     j = 0..k-1 and y = sum_j w_j o_j in slot order: deterministic, no
+//     atomics.
+// The tag of a call comes from a counter in the workspace header to which
+// every CTA adds 1 at its start, so it needs no reset between calls or graph
+// replays.  Every wait is bounded by a global-timer deadline; on expiry the
 // kernel records MOE_ERR_TIMEOUT, stops computing and lets its copies land
 // before returning.  (Copy completion needs no bound: loads always finish.)
+//
+// Arithmetic of the gate/up rows when H = 2048 (8 Q4_K blocks per row): lane
+// L always covers the same 64 elements of x (sub-block pair L % 4 of block
+// L / 4), so it keeps them in registers in an exact integer form: x / s, with
+// s = max|x| / 127 over each 32-element run, is split into three signed
+// base-254 digits (x ~= s (a + b/254 + c/254^2), each digit in [-127, 127];
+// the digits leave 6.1e-8 of the run's max|x|, the fp32 scalings add a few
+// ulps of x: below 2.5e-7 of the run's max|x| in all).  A 4-bit code times a
+// digit word is then one dp4a (four exact 8-bit products summed in int32),
+// and the fp32 scales of the block are applied once per sub-block.  Other
+// shapes, and all down rows, dot fp32 vectors in shared memory.
 #include <algorithm>
 
 #include "async_copy.cuh"
@@ -45,12 +59,17 @@ constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxNbw = 8;         // ring slots per warp
 constexpr int kHeadBytes = 4096;   // small shared arrays
+constexpr int kStageBatch = 8;     // h words in flight per thread while staging
 
 // Optional phase timeline for profiling builds (-DMOEQ4K_TIMELINE): thread 0
 // of each CTA stamps the global timer at phase boundaries into the
-// workspace's per-slot output region, which this path does not otherwise use.
+// workspace's per-slot activation region, which this path does not use.
 #ifdef MOEQ4K_TIMELINE
-#define TL_STAMP(p, i) ((p).timeline[blockIdx.x * 16 + (i)] = global_timer_ns())
+#define TL_STAMP(p, i)                                                             \
+    do {                                                                           \
+        if (int(blockIdx.x) * 16 + (i) < (p).timeline_cap)                         \
+            (p).timeline[blockIdx.x * 16 + (i)] = global_timer_ns();              \
+    } while (0)
 #else
 #define TL_STAMP(p, i) ((void)0)
 #endif
@@ -62,16 +81,27 @@ struct Params {
     int32_t *idx_out;
     float *w_out;
     const uint8_t *gate, *up, *down;
-    float *y, *logits, *hbuf;
+    float *y;
+    unsigned long long *sync;     // tag region: logits at [0, E), h at [kSyncHWord, +k*I)
     WsHeader *hdr;
     int H, E, k, I;
     int router_on;
-    int nbw, slot_bytes, ring_off;
-    int down_resident, down_off;  // CTA's down rows prefetched into [down_off, ...)
-    int withhold;                 // test hook: extra arrivals the grid barrier waits for
-    unsigned long long wait_ns;   // bound of the grid-barrier waits
+    int nbw, slot_bytes, ring_off;  // per-warp ring: nbw slots, one per gate/up row pair
+    int down_off;                   // the CTA's down rows, prefetched into [down_off, ...)
+    int dig_off;                  // x digit planes (3 x H bytes), then H/32 run scales
+    int withhold;                 // test hook: CTA 0 publishes nothing
+    unsigned long long wait_ns;   // bound of every wait
     unsigned long long *timeline; // profiling builds only
+    int timeline_cap;
 };
+
+__device__ __forceinline__ unsigned long long tagged(uint32_t tag, float v) {
+    return (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(v);
+}
+__device__ __forceinline__ uint32_t tag_of(unsigned long long w) { return uint32_t(w >> 32); }
+__device__ __forceinline__ float value_of(unsigned long long w) {
+    return __uint_as_float(uint32_t(w));
+}
 
 // Padded shared-memory vector: 4 floats of padding after every 64, so the
 // 8 lanes of a quarter-warp reading 16-float runs that are 64 floats apart
@@ -84,90 +114,14 @@ __device__ __forceinline__ float one_plus_q(uint32_t v, int i) {
     return __uint_as_float(__byte_perm(v, 0x3F000000u, 0x7044u | (uint32_t(i) << 8)));
 }
 
-// sum_b (1 + q_lo[b]/128) x_lo[b] and the same for the high nibbles, for one
-// 16-byte code chunk; x_lo = xs[0..15], x_hi = xs[32..47].
-__device__ __forceinline__ void chunk_acc(const uint4 &q, const float *xs, float &alo, float &ahi) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int wi = 0; wi < 4; ++wi) {
-        const uint32_t lo = (w[wi] & 0x0F0F0F0Fu) | 0x80808080u;
-        const uint32_t hi = ((w[wi] >> 4) & 0x0F0F0F0Fu) | 0x80808080u;
-        const float4 xl = *reinterpret_cast<const float4 *>(xs + 4 * wi);
-        const float4 xh = *reinterpret_cast<const float4 *>(xs + 32 + 4 * wi);
-        alo = fmaf(one_plus_q(lo, 0), xl.x, alo);
-        alo = fmaf(one_plus_q(lo, 1), xl.y, alo);
-        alo = fmaf(one_plus_q(lo, 2), xl.z, alo);
-        alo = fmaf(one_plus_q(lo, 3), xl.w, alo);
-        ahi = fmaf(one_plus_q(hi, 0), xh.x, ahi);
-        ahi = fmaf(one_plus_q(hi, 1), xh.y, ahi);
-        ahi = fmaf(one_plus_q(hi, 2), xh.z, ahi);
-        ahi = fmaf(one_plus_q(hi, 3), xh.w, ahi);
-    }
-}
-
 __device__ __forceinline__ float u6_to_float(uint32_t v) {
     return __uint_as_float(0x4B000000u | v) - 8388608.0f;
 }
 
-// One lane's share of a Q4_K row (nsb blocks in shared memory at `row`)
-// dotted with the padded vector `vec` (16-element run sums in `vsum`).  Lane
-// L takes code chunk L%8 of blocks L/8, L/8+4, ...
-template <int NSB>
-__device__ __forceinline__ float row_lane_dot(const uint8_t *row, int nsb_rt, const float *vec,
-                                              const float *vsum, int lane) {
-    const int nsb = NSB > 0 ? NSB : nsb_rt;
-    const int cq = lane & 7, c = cq >> 1, hf = cq & 1;
-    const bool upper = c >= 2;  // sub-blocks 4..7 keep their high scale bits elsewhere
-    const int j0 = 2 * c, j1 = 2 * c + 1;
-    float acc = 0.f;
-#pragma unroll(NSB > 8 ? 2 : 4)
-    for (int s = lane >> 3; s < nsb; s += 4) {
-        const uint8_t *blk = row + s * kBlockBytes;
-        const uint4 head = *reinterpret_cast<const uint4 *>(blk);
-        const uint4 q = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * cq);
-        const int base = s * kQK + 64 * c + 16 * hf;
-        const float *xs = vec + padded(base);
-        float alo = 0.f, ahi = 0.f;
-        chunk_acc(q, xs, alo, ahi);
-        const float slo = vsum[base >> 4], shi = vsum[(base >> 4) + 2];
-        uint32_t sc0, m0, sc1, m1;
-        if (!upper) {
-            sc0 = (head.y >> (8 * j0)) & 63u;
-            m0 = (head.z >> (8 * j0)) & 63u;
-            sc1 = (head.y >> (8 * j1)) & 63u;
-            m1 = (head.z >> (8 * j1)) & 63u;
-        } else {
-            const int a = j0 - 4, b = j1 - 4;
-            sc0 = ((head.w >> (8 * a)) & 15u) | (((head.y >> (8 * a + 6)) & 3u) << 4);
-            m0 = ((head.w >> (8 * a + 4)) & 15u) | (((head.z >> (8 * a + 6)) & 3u) << 4);
-            sc1 = ((head.w >> (8 * b)) & 15u) | (((head.y >> (8 * b + 6)) & 3u) << 4);
-            m1 = ((head.w >> (8 * b + 4)) & 15u) | (((head.z >> (8 * b + 6)) & 3u) << 4);
-        }
-        const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&head.x));
-        const float d128 = dd.x * 128.0f;
-        const float A0 = d128 * u6_to_float(sc0), A1 = d128 * u6_to_float(sc1);
-        const float B0 = dd.y * u6_to_float(m0), B1 = dd.y * u6_to_float(m1);
-        // d*sc*sum(q x) - dmin*m*sum(x), with sum(q x) = 128*(acc - sum(x))
-        acc = fmaf(A0, alo - slo, acc);
-        acc = fmaf(-B0, slo, acc);
-        acc = fmaf(A1, ahi - shi, acc);
-        acc = fmaf(-B1, shi, acc);
-    }
-    return acc;
-}
-
-// Contribution of one 16-byte code chunk (chunk cq of the block at `blk`)
-// to a row dot product with the padded vector `vec` / run sums `vsum`; the
-// block is block `s` of its row.
-__device__ __forceinline__ float block_chunk_dot(const uint8_t *blk, int s, int cq, const float *vec,
-                                                 const float *vsum) {
-    const int c = cq >> 1, hf = cq & 1;
-    const uint4 head = *reinterpret_cast<const uint4 *>(blk);
-    const uint4 q = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * cq);
-    const int base = s * kQK + 64 * c + 16 * hf;
-    float alo = 0.f, ahi = 0.f;
-    chunk_acc(q, vec + padded(base), alo, ahi);
-    const float slo = vsum[base >> 4], shi = vsum[(base >> 4) + 2];
+// Scale and min of sub-blocks 2c and 2c+1 of a block head, as dmul*d*sc and
+// dmin*m.
+__device__ __forceinline__ void pair_scales(const uint4 &head, int c, float dmul, float &A0,
+                                            float &B0, float &A1, float &B1) {
     const int j0 = 2 * c, j1 = 2 * c + 1;
     uint32_t sc0, m0, sc1, m1;
     if (c < 2) {
@@ -183,36 +137,9 @@ __device__ __forceinline__ float block_chunk_dot(const uint8_t *blk, int s, int 
         m1 = ((head.w >> (8 * b + 4)) & 15u) | (((head.z >> (8 * b + 6)) & 3u) << 4);
     }
     const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&head.x));
-    const float d128 = dd.x * 128.0f;
-    float acc = (d128 * u6_to_float(sc0)) * (alo - slo);
-    acc = fmaf(-dd.y * u6_to_float(m0), slo, acc);
-    acc = fmaf(d128 * u6_to_float(sc1), ahi - shi, acc);
-    acc = fmaf(-dd.y * u6_to_float(m1), shi, acc);
-    return acc;
-}
-
-// Scale and min of sub-blocks 2c and 2c+1 of a block head, as d*sc*128 and
-// dmin*m (the 128 undoes the 1 + q/128 encoding of the codes).
-__device__ __forceinline__ void pair_scales(const uint4 &head, int c, float &A0, float &B0, float &A1,
-                                            float &B1) {
-    const int j0 = 2 * c, j1 = 2 * c + 1;
-    uint32_t sc0, m0, sc1, m1;
-    if (c < 2) {
-        sc0 = (head.y >> (8 * j0)) & 63u;
-        m0 = (head.z >> (8 * j0)) & 63u;
-        sc1 = (head.y >> (8 * j1)) & 63u;
-        m1 = (head.z >> (8 * j1)) & 63u;
-    } else {
-        const int a = j0 - 4, b = j1 - 4;
-        sc0 = ((head.w >> (8 * a)) & 15u) | (((head.y >> (8 * a + 6)) & 3u) << 4);
-        m0 = ((head.w >> (8 * a + 4)) & 15u) | (((head.z >> (8 * a + 6)) & 3u) << 4);
-        sc1 = ((head.w >> (8 * b)) & 15u) | (((head.y >> (8 * b + 6)) & 3u) << 4);
-        m1 = ((head.w >> (8 * b + 4)) & 15u) | (((head.z >> (8 * b + 6)) & 3u) << 4);
-    }
-    const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&head.x));
-    const float d128 = dd.x * 128.0f;
-    A0 = d128 * u6_to_float(sc0);
-    A1 = d128 * u6_to_float(sc1);
+    const float dm = dd.x * dmul;
+    A0 = dm * u6_to_float(sc0);
+    A1 = dm * u6_to_float(sc1);
     B0 = dd.y * u6_to_float(m0);
     B1 = dd.y * u6_to_float(m1);
 }
@@ -244,7 +171,7 @@ __device__ __forceinline__ float pair_dot(const uint8_t *blk, int c, const float
         b1 = fmaf(one_plus_q(hi, 3), xh.w, b1);
     }
     float A0, B0, A1, B1;
-    pair_scales(head, c, A0, B0, A1, B1);
+    pair_scales(head, c, 128.0f, A0, B0, A1, B1);
     const float slo = s2[0], shi = s2[1];
     // d*sc*sum(q x) - dmin*m*sum(x), with sum(q x) = 128*(acc - sum(x))
     float acc = A0 * ((a0 + a1) - slo);
@@ -287,58 +214,141 @@ __device__ __forceinline__ void run_sums32(const float *vec, float *sum32, int c
     }
 }
 
-// Sum each 16-float run of `count` runs of the padded vector(s) into vsum.
-// Run q starts at logical element 16*(q % runs_per_vec) of vector q / runs_per_vec.
-__device__ __forceinline__ void run_sums(const float *vec, float *vsum, int count, int runs_per_vec,
-                                         int vec_stride) {
-    for (int q = threadIdx.x; q < count; q += kThreads) {
-        const int j = q / runs_per_vec, c = 16 * (q % runs_per_vec);
-        const float *v = vec + j * vec_stride + padded(c);
-        float s = 0.f;
+// ---------------------------------------------------------------------------
+// Integer form of x for the gate/up rows (H = 2048).
+// ---------------------------------------------------------------------------
+
+// d = c + sum_i a.byte[i] * b.byte[i], a's bytes unsigned, b's signed.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ int8_t digit(float f) {
+    return int8_t(max(-127, min(127, __float2int_rn(f))));
+}
+
+// The warp holds one 32-element run of x, one element per lane.  Writes the
+// lane's three base-254 digits of x / s (s = max|x| / 127 over the run) and
+// returns s / 254.  Each remainder step is exact in fp32 (t - rint(t)); only
+// the scalings by 127/max and by 254 round, at fp32 precision.  A run with a
+// non-finite element gets a NaN scale, so the non-finite value propagates.
+__device__ __forceinline__ float run_digits(float v, int8_t &da, int8_t &db, int8_t &dc) {
+    float mx = fabsf(v);
 #pragma unroll
-        for (int b = 0; b < 16; ++b) s += v[b];
-        vsum[q] = s;
-    }
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const bool finite = __all_sync(0xffffffffu, fabsf(v) <= 3.402823466e38f);
+    const float inv = mx > 0.f ? 127.0f / mx : 0.f;
+    const float t = finite ? v * inv : 0.f;
+    const float a = rintf(t);
+    const float r1 = (t - a) * 254.0f;
+    const float b = rintf(r1);
+    const float r2 = (r1 - b) * 254.0f;
+    da = digit(a);
+    db = digit(b);
+    dc = digit(rintf(r2));
+    return finite ? mx * (1.0f / (127.0f * 254.0f)) : __uint_as_float(0x7FC00000u);
 }
 
-// Grid barrier on a monotonic arrival counter: arrive (release), then wait
-// (acquire) until the counter reaches `target`.  All threads of the CTA call
-// it; returns false on time-out.
-__device__ __forceinline__ bool grid_sync(WsHeader *hdr, unsigned long long target,
-                                          uint64_t deadline, int *flag, bool publish_cta) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        // the release add publishes this thread's writes; other threads'
-        // writes (ordered before it by the CTA barrier) get a full fence
-        if (publish_cta) __threadfence();
-        red_release_add_u64(&hdr->bar_arrivals, 1ull);
-        bool ok = true;
-        while (ld_acquire_u64(&hdr->bar_arrivals) < target) {
-            if (global_timer_ns() > deadline) {
-                ok = false;
-                break;
-            }
-            __nanosleep(20);
-        }
-        *flag = ok ? 0 : 1;
+// One lane's 64 elements of x (sub-block pair c of block s, elements
+// 256 s + 64 c + [0, 64)) as digit words (4 consecutive elements each; words
+// 0-7 are sub-block 2c, 8-15 sub-block 2c+1), their scales and fp32 sums.
+struct XDigits {
+    uint32_t a[16], b[16], c[16];
+    float s0, s1;      // run scale / 254; s1 also / 16 (high nibbles are read unshifted)
+    float sum0, sum1;  // sum of x over each run
+};
+
+__device__ __forceinline__ void load_digits(XDigits &X, const uint8_t *planes, int H,
+                                            const float *scales, const float *sum32, int e0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 va = *reinterpret_cast<const uint4 *>(planes + e0 + 16 * q);
+        const uint4 vb = *reinterpret_cast<const uint4 *>(planes + H + e0 + 16 * q);
+        const uint4 vc = *reinterpret_cast<const uint4 *>(planes + 2 * H + e0 + 16 * q);
+        X.a[4 * q] = va.x, X.a[4 * q + 1] = va.y, X.a[4 * q + 2] = va.z, X.a[4 * q + 3] = va.w;
+        X.b[4 * q] = vb.x, X.b[4 * q + 1] = vb.y, X.b[4 * q + 2] = vb.z, X.b[4 * q + 3] = vb.w;
+        X.c[4 * q] = vc.x, X.c[4 * q + 1] = vc.y, X.c[4 * q + 2] = vc.z, X.c[4 * q + 3] = vc.w;
     }
-    __syncthreads();
-    return *flag == 0;
+    X.s0 = scales[e0 >> 5];
+    X.s1 = scales[(e0 >> 5) + 1] * 0.0625f;
+    X.sum0 = sum32[e0 >> 5];
+    X.sum1 = sum32[(e0 >> 5) + 1];
 }
 
+// Dot of sub-blocks 2c and 2c+1 of one block with the lane's x digits:
+// sum(q x) over a run is s/254 * ((254 A + B) + C/254) with A, B, C the
+// exact integer sums of the codes times each digit.
+__device__ __forceinline__ float pair_dot_digits(const uint8_t *blk, int c, const XDigits &X) {
+    const uint4 head = *reinterpret_cast<const uint4 *>(blk);
+    const uint4 qa = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
+    const uint4 qb = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
+    const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    int a0 = 0, b0 = 0, c0 = 0, a1 = 0, b1 = 0, c1 = 0;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const uint32_t lo = w[m] & 0x0F0F0F0Fu;  // codes of elements 4m..4m+3
+        const uint32_t hi = w[m] & 0xF0F0F0F0u;  // 16 x codes of elements 32+4m..32+4m+3
+        a0 = dp4a_us(lo, X.a[m], a0);
+        b0 = dp4a_us(lo, X.b[m], b0);
+        c0 = dp4a_us(lo, X.c[m], c0);
+        a1 = dp4a_us(hi, X.a[8 + m], a1);
+        b1 = dp4a_us(hi, X.b[8 + m], b1);
+        c1 = dp4a_us(hi, X.c[8 + m], c1);
+    }
+    // |254 a + b| < 2^28 (high nibbles) and < 2^24 (low): no overflow
+    const float qx0 = X.s0 * fmaf(float(c0), 1.0f / 254.0f, float(254 * a0 + b0));
+    const float qx1 = X.s1 * fmaf(float(c1), 1.0f / 254.0f, float(254 * a1 + b1));
+    float A0, B0, A1, B1;
+    pair_scales(head, c, 1.0f, A0, B0, A1, B1);
+    float acc = A0 * qx0;
+    acc = fmaf(-B0, X.sum0, acc);
+    acc = fmaf(A1, qx1, acc);
+    acc = fmaf(-B1, X.sum1, acc);
+    return acc;
+}
+
+// Warp sums of g and u in a fixed order; every lane of 0..15 gets the sum of
+// g, every lane gets the sum of u.
+__device__ __forceinline__ void warp_sum2(float &g, float &u, int lane) {
+    const bool upper = (lane & 16) != 0;
+    float keep = upper ? u : g;
+    keep += __shfl_xor_sync(0xffffffffu, upper ? g : u, 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+    g = keep;
+    u = __shfl_sync(0xffffffffu, keep, 16);
+}
+
+// Poll one tagged word until it carries `tag`; false when `deadline` passes.
+__device__ __forceinline__ bool await_word(const unsigned long long *p, uint32_t tag,
+                                           uint64_t deadline, unsigned long long &w) {
+    w = ld_relaxed_u64(p);
+    while (tag_of(w) != tag) {
+        if (global_timer_ns() > deadline) return false;
+        __nanosleep(32);
+        w = ld_relaxed_u64(p);
+    }
+    return true;
+}
 
 template <int NSB_H, int NSB_I>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params p) {
+    // The integer form of x applies when every lane covers one sub-block pair.
+    constexpr bool kDigits = (NSB_H == 8);
     extern __shared__ __align__(128) uint8_t smem[];
-    unsigned long long *base_sh = reinterpret_cast<unsigned long long *>(smem);
-    int *sel_e = reinterpret_cast<int *>(base_sh + 1);
+    uint32_t *tag_sh = reinterpret_cast<uint32_t *>(smem);
+    int *sel_e = reinterpret_cast<int *>(smem + 16);
     float *sel_w = reinterpret_cast<float *>(sel_e + 32);
-    int *flags = reinterpret_cast<int *>(sel_w + 32);  // [0] barrier result, [1] abort
+    int *flags = reinterpret_cast<int *>(sel_w + 32);  // [1] wait timed out
     float *red = reinterpret_cast<float *>(flags + 4); // partial sums, then logits + ranks (2*kMaxE)
     float *vec = reinterpret_cast<float *>(smem + kHeadBytes);
     const int H = p.H, E = p.E, k = p.k, I = p.I;
     const int vec_pad = max(padded_len(H), k * padded_len(I));
     float *vsum = vec + vec_pad;
+    uint8_t *planes = smem + p.dig_off;
+    float *xscale = reinterpret_cast<float *>(planes + 3 * H);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t deadline = global_timer_ns() + p.wait_ns;
@@ -348,16 +358,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     const size_t mat_gu = size_t(I) * row_gu, mat_dn = size_t(H) * row_dn;
     const int nbw = p.nbw;
     uint8_t *ring = smem + p.ring_off + size_t(warp) * nbw * p.slot_bytes;
+    const bool publish = !(p.withhold && blockIdx.x == 0);
 
+    // this call's tag: the add returns a value in [n * nblk, (n + 1) * nblk)
+    // for the n-th call; the result is only needed once x is staged
+    unsigned long long calls0 = 0;
     if (threadIdx.x == 0) {
         TL_STAMP(p, 0);
-        // this call's barrier rounds: every call adds 2 arrivals per CTA, and
-        // fewer than 2*nblk arrivals of this call can precede this read
-        const unsigned long long c0 = ld_acquire_u64(&p.hdr->bar_arrivals);
-        *base_sh = c0 - c0 % (2ull * nblk);
+        calls0 = atomicAdd(&p.hdr->cta_calls, 1ull);
         flags[1] = 0;
     }
-    // ---------------- 1. router logits (a share per CTA), grid barrier.
+    // ---------------- 1. router logits (a share per CTA).
     // The CTA's first logit is computed while x is staged: x and the router
     // row are requested together, so their latencies overlap.
     const uint64_t pol_last = l2_policy_evict_last();
@@ -379,16 +390,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         }
         a = warp_sum(a);
         if (lane == 0) red[warp] = a;
+        if (threadIdx.x == 0) *tag_sh = uint32_t(calls0 / nblk) + 1u;
         __syncthreads();
         if (logit && threadIdx.x == 0) {
             float sum = 0.f;
             for (int w = 0; w < kWarps; ++w) sum += red[w];
-            p.logits[e] = sum + (p.bias ? p.bias[e] : 0.f);
+            sum += p.bias ? p.bias[e] : 0.f;
+            if (publish) st_relaxed_u64(p.sync + e, tagged(*tag_sh, sum));
         }
         run_sums32(vec, vsum, H >> 5, H >> 5, 0);
+        if (kDigits) {
+            for (int r = warp; r < (H >> 5); r += kWarps) {
+                int8_t da, db, dc;
+                const float sc = run_digits(vec[padded(32 * r + lane)], da, db, dc);
+                planes[32 * r + lane] = uint8_t(da);
+                planes[H + 32 * r + lane] = uint8_t(db);
+                planes[2 * H + 32 * r + lane] = uint8_t(dc);
+                if (lane == 0) xscale[r] = sc;
+            }
+        }
         __syncthreads();
     }
-    const unsigned long long base = *base_sh;
+    const uint32_t tag = *tag_sh;
     if (threadIdx.x == 0) TL_STAMP(p, 1);
 
     if (p.router_on) {
@@ -409,20 +432,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             if (threadIdx.x == 0) {
                 float s = 0.f;
                 for (int w = 0; w < kWarps; ++w) s += red[w];
-                p.logits[e] = s + (p.bias ? p.bias[e] : 0.f);
+                s += p.bias ? p.bias[e] : 0.f;
+                if (publish) st_relaxed_u64(p.sync + e, tagged(tag, s));
             }
             __syncthreads();
         }
         if (threadIdx.x == 0) TL_STAMP(p, 2);
-        if (!grid_sync(p.hdr, base + nblk + p.withhold, deadline, flags, false)) {
-            if (threadIdx.x == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 1);
-            cp_async_wait_all();
-            return;  // no output written
-        }
-    } else if (threadIdx.x == 0) {
-        red_release_add_u64(&p.hdr->bar_arrivals, 1ull);  // keep 2 arrivals per call
     }
-    if (threadIdx.x == 0) TL_STAMP(p, 8);
 
     // ---------------- 2. top-k + renormalise, by rank: every CTA ranks the E
     // logits in the order (value descending, index ascending); the logit of
@@ -430,12 +446,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     if (p.router_on) {
         float *lsm = red;                     // E logits (red is free again)
         int *rank = reinterpret_cast<int *>(lsm + kMaxE);
-        for (int e = threadIdx.x; e < E; e += kThreads) {
-            float v = __ldcg(p.logits + e);
-            lsm[e] = (v == v) ? v : -INFINITY;   // a NaN never ranks first
-            rank[e] = 0;
+        if (threadIdx.x < E) {
+            unsigned long long wv;
+            if (!await_word(p.sync + threadIdx.x, tag, deadline, wv)) flags[1] = 1;
+            const float v = value_of(wv);
+            lsm[threadIdx.x] = (v == v) ? v : -INFINITY;   // a NaN never ranks first
+            rank[threadIdx.x] = 0;
         }
         __syncthreads();
+        if (flags[1]) {
+            if (threadIdx.x == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 1);
+            return;  // no copies issued yet, no output written
+        }
+        if (threadIdx.x == 0) TL_STAMP(p, 8);
         const int G = max(1, kThreads / E);      // threads per logit
         const int per = (E + G - 1) / G;         // comparisons per thread
         for (int t = threadIdx.x; t < E * G; t += kThreads) {
@@ -488,12 +511,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     const int n_mine = n_gu > warp ? (n_gu - warp + kWarps - 1) / kWarps : 0;  // rows warp+16i
     const uint64_t pol = l2_policy_evict_first();
     const int n16_gu = row_gu >> 4, n16_dn = row_dn >> 4;
+    unsigned long long *hsync = p.sync + kSyncHWord;
 
-    // issue the copies of this warp's i-th gate/up row pair into its ring slot
+    // issue the copies of this warp's i-th gate/up row pair into ring slot i
     auto issue_gu = [&](int i) {
         const int u = u0 + warp + kWarps * i, j = u / I, r = u % I;
         const int e = sel_e[j];
-        uint8_t *dst = ring + (i % nbw) * p.slot_bytes;
+        uint8_t *dst = ring + i * p.slot_bytes;
         if (e >= 0 && e < E) {
             const uint8_t *g = p.gate + e * mat_gu + size_t(r) * row_gu;
             const uint8_t *uu = p.up + e * mat_gu + size_t(r) * row_gu;
@@ -504,24 +528,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         }
         cp_async_commit();
     };
-    // issue the copies of this warp's i-th down row (all k experts) into a ring slot
-    auto issue_dn = [&](int i, int slot) {
-        const int r = r0 + warp + kWarps * i;
-        uint8_t *dst = ring + slot * p.slot_bytes;
-        for (int c = lane; c < k * n16_dn; c += 32) {
-            const int j = c / n16_dn, w16 = c % n16_dn;
-            const int e = sel_e[j];
-            if (e >= 0 && e < E)
-                cp_async_16(dst + 16 * c, p.down + e * mat_dn + size_t(r) * row_dn + 16 * w16, pol);
-        }
-        cp_async_commit();
-    };
-
-    const int first = min(nbw, n_mine);
-    for (int i = 0; i < first; ++i) issue_gu(i);
+    // every row of the warp has its own slot (the host only launches shapes
+    // where n_mine <= nbw), then the CTA's R output rows of all k experts,
+    // as k contiguous ranges: all weight bytes are requested up front
+    for (int i = 0; i < n_mine; ++i) issue_gu(i);
     uint8_t *dbuf = smem + p.down_off;
-    if (p.down_resident) {
-        // the CTA's R output rows of all k experts: k contiguous ranges
+    {
         const int per_j = R * n16_dn;
         for (int c = threadIdx.x; c < k * per_j; c += kThreads) {
             const int j = c / per_j, w16 = c % per_j;
@@ -529,83 +541,92 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             if (e >= 0 && e < E)
                 cp_async_16(dbuf + 16 * c, p.down + e * mat_dn + size_t(r0) * row_dn + 16 * w16, pol);
         }
-        cp_async_commit();  // one group after the first gate/up rows
+        cp_async_commit();  // one group after the gate/up rows
     }
 
+    XDigits X;
+    if (kDigits) load_digits(X, planes, H, xscale, vsum, 64 * lane);
+
     for (int i = 0; i < n_mine; ++i) {
-        const int slot = i % nbw;
-        // groups committed after row i: the rows issued beyond it, plus the
-        // down prefetch when it went in after the first rows
-        const int later = min(nbw - 1, n_mine - 1 - i) + ((p.down_resident && i < first) ? 1 : 0);
-        cp_async_wait_pending(later);
+        // groups committed after row i: the later rows and the down rows
+        cp_async_wait_pending(n_mine - i);
         __syncwarp();
         if (threadIdx.x == 0 && i == 0) TL_STAMP(p, 9);
         const int u = u0 + warp + kWarps * i, j = u / I, r = u % I;
         const int e = sel_e[j];
         if (e >= 0 && e < E) {
-            const uint8_t *src = ring + slot * p.slot_bytes;
-            const float g = warp_sum(row_dot_pairs<NSB_H>(src, nsb_h, vec, vsum, lane));
-            const float uu = warp_sum(row_dot_pairs<NSB_H>(src + row_gu, nsb_h, vec, vsum, lane));
-            if (lane == 0) p.hbuf[size_t(j) * I + r] = silu_mul(g, uu);
+            const uint8_t *src = ring + i * p.slot_bytes;
+            float g, uu;
+            if (kDigits) {
+                const uint8_t *blk = src + (lane >> 2) * kBlockBytes;
+                g = pair_dot_digits(blk, lane & 3, X);
+                uu = pair_dot_digits(blk + row_gu, lane & 3, X);
+                warp_sum2(g, uu, lane);
+            } else {
+                g = warp_sum(row_dot_pairs<NSB_H>(src, nsb_h, vec, vsum, lane));
+                uu = warp_sum(row_dot_pairs<NSB_H>(src + row_gu, nsb_h, vec, vsum, lane));
+            }
+            if (lane == 0 && publish)
+                st_relaxed_u64(hsync + size_t(j) * I + r, tagged(tag, silu_mul(g, uu)));
         }
         __syncwarp();
-        if (i + nbw < n_mine) issue_gu(i + nbw);
     }
     if (threadIdx.x == 0) TL_STAMP(p, 4);
 
-    // ---------------- 4. h complete everywhere -> down rows + combine
-    if (!grid_sync(p.hdr, base + 2ull * nblk + p.withhold, deadline, flags, true)) {
-        if (threadIdx.x == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 4);
-        flags[1] = 1;
+    // ---------------- 4. h of all k slots -> down rows + combine
+    __syncthreads();  // x in `vec` is dead once every warp is past its rows
+    const int ip = padded_len(I);
+    {
+        // kStageBatch two-word loads per thread in flight, then wait for
+        // any word whose tag is not yet the current one
+        const int n2 = (k * I) >> 1;
+        bool ok = true;
+        for (int q0 = threadIdx.x; q0 < n2; q0 += kStageBatch * kThreads) {
+            unsigned long long wa[kStageBatch], wb[kStageBatch];
+#pragma unroll
+            for (int t = 0; t < kStageBatch; ++t) {
+                const int q = q0 + t * kThreads;
+                wa[t] = wb[t] = tagged(tag, 0.f);  // slots of invalid experts stay 0
+                if (q < n2) {
+                    const int e = sel_e[(2 * q) / I];
+                    if (e >= 0 && e < E) ld_relaxed_v2u64(hsync + 2 * q, wa[t], wb[t]);
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kStageBatch; ++t) {
+                const int q = q0 + t * kThreads;
+                if (q >= n2) continue;
+                if (ok && tag_of(wa[t]) != tag) ok = await_word(hsync + 2 * q, tag, deadline, wa[t]);
+                if (ok && tag_of(wb[t]) != tag)
+                    ok = await_word(hsync + 2 * q + 1, tag, deadline, wb[t]);
+                const int j = (2 * q) / I, c = 2 * q - j * I;
+                *reinterpret_cast<float2 *>(vec + j * ip + padded(c)) =
+                    make_float2(value_of(wa[t]), value_of(wb[t]));
+            }
+        }
+        if (!ok) flags[1] = 1;
     }
     __syncthreads();
     if (threadIdx.x == 0) TL_STAMP(p, 5);
-    if (flags[1] == 0) {
-        const int ip = padded_len(I);
-        for (int q = threadIdx.x; q < (k * I) >> 5; q += kThreads) {  // one 32-float run each
-            const int j = (32 * q) / I, c = (32 * q) % I;
-            const float4 *src = reinterpret_cast<const float4 *>(p.hbuf) + 8 * q;
-            float4 v[8];
-#pragma unroll
-            for (int b = 0; b < 8; ++b) v[b] = __ldcg(src + b);
-            float *dst = vec + j * ip + padded(c);
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int b = 0; b < 8; b += 2) {
-                *reinterpret_cast<float4 *>(dst + 4 * b) = v[b];
-                *reinterpret_cast<float4 *>(dst + 4 * b + 4) = v[b + 1];
-                s0 += (v[b].x + v[b].y) + (v[b].z + v[b].w);
-                s1 += (v[b + 1].x + v[b + 1].y) + (v[b + 1].z + v[b + 1].w);
-            }
-            vsum[q] = s0 + s1;
-        }
+    if (flags[1]) {
+        if (threadIdx.x == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 4);
+    } else {
+        run_sums32(vec, vsum, (k * I) >> 5, I >> 5, ip);
         __syncthreads();
         if (threadIdx.x == 0) TL_STAMP(p, 6);
 
         const int n_rows = R > warp ? (R - warp + kWarps - 1) / kWarps : 0;  // rows warp+16i
-        if (p.down_resident) {
-            cp_async_wait_all();  // this thread's share of the prefetch
-            __syncthreads();      // everyone's share
-        }
+        cp_async_wait_all();  // this thread's share of the down rows
+        __syncthreads();      // everyone's share
         if (threadIdx.x == 0) TL_STAMP(p, 10);
-        const int first_dn = p.down_resident ? 0 : min(nbw, n_rows);
-        for (int i = 0; i < first_dn; ++i) issue_dn(i, i % nbw);
+        const size_t jstride = size_t(R) * row_dn;
         for (int i = 0; i < n_rows; ++i) {
             const int rr = warp + kWarps * i;  // row inside the CTA's share
-            const uint8_t *src;
-            size_t jstride;
-            if (p.down_resident) {
-                src = dbuf + size_t(rr) * row_dn;
-                jstride = size_t(R) * row_dn;
-            } else {
-                cp_async_wait_pending(min(nbw - 1, n_rows - 1 - i));
-                __syncwarp();
-                src = ring + (i % nbw) * p.slot_bytes;
-                jstride = row_dn;
-            }
-            // k experts x nsb_i blocks x 8 chunks, spread over the 32 lanes in a
-            // fixed order; each chunk's partial dot is weighted by its slot's
-            // router weight, then one warp reduction gives y (deterministic)
+            const uint8_t *src = dbuf + size_t(rr) * row_dn;
+            // k experts x nsb_i blocks x 4 sub-block pairs, spread over the 32
+            // lanes in a fixed order; each pair's partial dot is weighted by its
+            // slot's router weight, then one warp reduction gives y
+            // (deterministic)
             float yacc = 0.f;
             const int per_j = (NSB_I > 0 ? NSB_I : nsb_i) * 4;   // (block, pair) units per slot
             const int nunits = k * per_j;
@@ -621,8 +642,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             }
             yacc = warp_sum(yacc);
             if (lane == 0) p.y[r0 + rr] = yacc;
-            __syncwarp();
-            if (!p.down_resident && i + nbw < n_rows) issue_dn(i + nbw, (i + nbw) % nbw);
         }
     }
     // every copy this thread issued must land before the CTA's shared memory goes away
@@ -635,8 +654,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
 namespace {
 
 struct FusedConfig {
-    int nbw = 0, slot_bytes = 0, ring_off = 0, down_resident = 0, down_off = 0, smem = 0;
+    int nbw = 0, slot_bytes = 0, ring_off = 0, down_off = 0, dig_off = 0, smem = 0;
 };
+
+// The kernels instantiated for 8 blocks per gate/up row and 3 or 4 per down
+// row keep x as digits.
+bool uses_digits(int H, int I) { return H / kQK == 8 && (I / kQK == 3 || I / kQK == 4); }
 
 bool fused_config(int H, int E, int k, int I, int nblk, int max_smem, FusedConfig &c) {
     using namespace fused;
@@ -645,25 +668,30 @@ bool fused_config(int H, int E, int k, int I, int nblk, int max_smem, FusedConfi
     const int vec_pad = std::max(padded_len(H), k * padded_len(I));
     const int vec_sum = std::max(H, k * I) / 16;
     const int vec_end = int(align256(size_t(kHeadBytes) + sizeof(float) * size_t(vec_pad + vec_sum)));
+    // x as three digit planes plus one scale per 32-element run
+    const int dig_bytes =
+        uses_digits(H, I) ? int(align256(size_t(3) * H + sizeof(float) * (H / 32))) : 0;
+    const int dig_end = vec_end + dig_bytes;
     const int rmax = (H + nblk - 1) / nblk;
     const int down_bytes = int(align256(size_t(k) * rmax * row_dn));
-    // A: the CTA's down rows resident, rings hold gate/up row pairs
-    int slot = (2 * row_gu + 127) / 128 * 128;
-    int nbw = (max_smem - vec_end - down_bytes) / (kWarps * slot);
-    // Only shapes whose down rows fit resident take this kernel.  The variant
-    // that streams down rows through the per-warp rings after the second
-    // barrier (needed by the Qwen3-235B-A22B shape) raised an illegal
-    // instruction on GB300 and is not launched; those shapes run the
-    // multi-kernel path.
-    if (nbw < 2) return false;
-    c.down_resident = 1;
-    c.down_off = vec_end;
-    c.ring_off = vec_end + down_bytes;
-    nbw = std::min(nbw, kMaxNbw);
-    if (nbw < 1) return false;
-    c.nbw = nbw;
+    // the CTA's down rows resident, rings hold gate/up row pairs
+    const int slot = (2 * row_gu + 127) / 128 * 128;
+    const int nbw = std::min(kMaxNbw, (max_smem - dig_end - down_bytes) / (kWarps * slot));
+    // Only shapes where the CTA's down rows stay resident and every warp's
+    // gate/up rows have a ring slot each take this kernel: all weight bytes
+    // are requested at once.  Variants that reused ring slots (streaming
+    // down rows through the rings, or gate/up rows beyond the ring's size)
+    // raised illegal-instruction faults on GB300 and are not built; those
+    // shapes (Qwen3-235B-A22B among them) run the multi-kernel path.
+    const int units_max = (k * I + nblk - 1) / nblk;
+    const int rows_per_warp = (units_max + kWarps - 1) / kWarps;
+    if (nbw < 1 || nbw < rows_per_warp) return false;
+    c.dig_off = vec_end;
+    c.down_off = dig_end;
+    c.ring_off = dig_end + down_bytes;
+    c.nbw = rows_per_warp;
     c.slot_bytes = slot;
-    c.smem = c.ring_off + kWarps * nbw * slot;
+    c.smem = c.ring_off + kWarps * c.nbw * slot;
     return c.smem <= max_smem;
 }
 
@@ -675,8 +703,8 @@ void *kernel_ptr() {
 void *pick_kernel(int H, int I) {
     const int a = H / kQK, b = I / kQK;
     if (a == 8 && b == 3) return kernel_ptr<8, 3>();
-    if (a == 1 && b == 1) return kernel_ptr<1, 1>();
     if (a == 8 && b == 4) return kernel_ptr<8, 4>();
+    if (a == 1 && b == 1) return kernel_ptr<1, 1>();
     return kernel_ptr<0, 0>();
 }
 
@@ -690,7 +718,7 @@ cudaError_t init_decode_fused(int dev, int num_sms) {
     cudaError_t err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (err != cudaSuccess) return err;
     g_fused_max_smem[dev] = optin;
-    void *ks[] = {kernel_ptr<8, 3>(), kernel_ptr<1, 1>(), kernel_ptr<8, 4>(), kernel_ptr<0, 0>()};
+    void *ks[] = {kernel_ptr<8, 3>(), kernel_ptr<8, 4>(), kernel_ptr<1, 1>(), kernel_ptr<0, 0>()};
     for (void *kp : ks) {
         err = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (err != cudaSuccess) return err;
@@ -709,8 +737,9 @@ cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const 
                                 const int32_t *idx_in, const float *w_in, int32_t *idx_out,
                                 float *w_out, const uint8_t *gate, const uint8_t *up,
                                 const uint8_t *down, int H, int E, int k, int I, float *y,
-                                float *logits, float *hbuf, WsHeader *hdr, int withhold,
-                                unsigned long long wait_ns, cudaStream_t s) {
+                                unsigned long long *sync, WsHeader *hdr, int withhold,
+                                unsigned long long wait_ns, unsigned long long *timeline,
+                                int timeline_cap, cudaStream_t s) {
     FusedConfig c;
     if (!fused_config(H, E, k, I, g_fused_blocks[dev], g_fused_max_smem[dev], c))
         return cudaErrorInvalidValue;
@@ -726,8 +755,7 @@ cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const 
     p.up = up;
     p.down = down;
     p.y = y;
-    p.logits = logits;
-    p.hbuf = hbuf;
+    p.sync = sync;
     p.hdr = hdr;
     p.H = H;
     p.E = E;
@@ -737,11 +765,12 @@ cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const 
     p.nbw = c.nbw;
     p.slot_bytes = c.slot_bytes;
     p.ring_off = c.ring_off;
-    p.down_resident = c.down_resident;
     p.down_off = c.down_off;
+    p.dig_off = c.dig_off;
     p.withhold = withhold;
     p.wait_ns = wait_ns;
-    p.timeline = reinterpret_cast<unsigned long long *>(hbuf + size_t(k) * I);
+    p.timeline = timeline;
+    p.timeline_cap = timeline ? timeline_cap : 0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(g_fused_blocks[dev]);

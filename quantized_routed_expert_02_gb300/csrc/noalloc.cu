@@ -6,15 +6,17 @@
 // hot path.  They still own x, the weights and the outputs, but cannot
 // provide the scratch workspace the other entry points take.  This entry
 // point runs the same single-token kernel with its scratch (status word,
-// grid-barrier counter, router logits, expert activations h) in a fixed
+// call counter, tagged router logits and expert activations h) in a fixed
 // array in device global memory that the library itself defines.
 //
 // The array lives for as long as the library is loaded, on every GPU that
-// loads it.  All calls share it and it keeps the previous call's contents;
-// the call clears the part that must start at zero (status and barrier
-// counter) itself.  Calls that overlap on the GPU (different streams, or
-// several host threads) race on the array and must be serialised by the
-// caller.
+// loads it; it starts zeroed.  All calls share it and it keeps the previous
+// call's contents, which is what the kernel needs: the call counter only
+// grows, so the tags left by earlier calls never match a later call's.  The
+// call clears the status word itself.  Calls that overlap on the GPU
+// (different streams, or several host threads) race on the array and must
+// be serialised by the caller.
+#include <cstddef>
 #include <mutex>
 
 #include "common.cuh"
@@ -23,11 +25,12 @@
 namespace moeq4k {
 namespace {
 
-// Header (256 B) + router logits (up to 256 experts, 1 KB) + h (k*I floats).
+// Header (256 B), then the tag region: kSyncHWord words for the router
+// logits, then one word per value of h (k*I words).
 constexpr size_t kNoallocScratchBytes = 256 * 1024;
-constexpr size_t kNoallocLogitsOff = 256;
-constexpr size_t kNoallocHOff = 256 + 1024;
-constexpr size_t kNoallocMaxH = (kNoallocScratchBytes - kNoallocHOff) / sizeof(float);
+constexpr size_t kNoallocSyncOff = 256;
+constexpr size_t kNoallocMaxKI =
+    (kNoallocScratchBytes - kNoallocSyncOff) / sizeof(unsigned long long) - kSyncHWord;
 
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -60,8 +63,7 @@ extern "C" moe_status moe_layer_noalloc(const float *x, const float *Wr, const f
     moe_status st = validate_shape(T, H, E, k, I);
     if (st != MOE_OK) return st;
     if (T != 1) return MOE_ERR_INVALID_SHAPE;
-    if (size_t(k) * I > kNoallocMaxH || E * sizeof(float) > kNoallocHOff - kNoallocLogitsOff)
-        return MOE_ERR_SCRATCH_LIMIT;
+    if (size_t(k) * I > kNoallocMaxKI) return MOE_ERR_SCRATCH_LIMIT;
     const void *ptrs[] = {x, Wr, gate, up, down, idx, w, y};
     for (const void *q : ptrs) {
         if (q == nullptr) return MOE_ERR_NULL;
@@ -76,13 +78,14 @@ extern "C" moe_status moe_layer_noalloc(const float *x, const float *Wr, const f
     st = noalloc_scratch(dev, &scratch);
     if (st != MOE_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // status word and barrier counter start at zero on every call
-    if (cudaMemsetAsync(scratch, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
+    // the status word starts at zero on every call; the call counter must not
+    static_assert(offsetof(WsHeader, status) == 0 && offsetof(WsHeader, detail) == 4,
+                  "status and detail lead the header");
+    if (cudaMemsetAsync(scratch, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
     cudaError_t err = launch_decode_fused(
         dev, x, Wr, bias, nullptr, nullptr, idx, w, static_cast<const uint8_t *>(gate),
         static_cast<const uint8_t *>(up), static_cast<const uint8_t *>(down), H, E, k, I, y,
-        reinterpret_cast<float *>(scratch + kNoallocLogitsOff),
-        reinterpret_cast<float *>(scratch + kNoallocHOff), reinterpret_cast<WsHeader *>(scratch), 0,
-        1000000000ull, s);
+        reinterpret_cast<unsigned long long *>(scratch + kNoallocSyncOff),
+        reinterpret_cast<WsHeader *>(scratch), 0, 1000000000ull, nullptr, 0, s);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -106,7 +106,8 @@ def moe_layer_launch_count(T, H, E, k, I) -> int:
 
 
 def alloc_workspace(T, H, E, k, I, device="cuda", host_staging=False) -> torch.Tensor:
-    """A zero-initialised uint8 device workspace of the right size."""
+    """A uint8 device workspace of the right size, initialised with
+    moe_workspace_init (header and tag region zeroed)."""
     n = (moe_workspace_bytes_host if host_staging else moe_workspace_bytes)(T, H, E, k, I)
     if n == 0:
         raise MoeError(1, "moe_workspace_bytes")

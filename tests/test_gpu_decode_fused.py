@@ -63,10 +63,28 @@ def test_single_token_repeat_bitwise(m):
         np.testing.assert_array_equal(d["y"].cpu().numpy(), y1)
 
 
+def test_workspace_shared_with_batched_calls(m):
+    """One workspace serves single-token and batched calls in turn: the
+    batched path's scratch never disturbs the tagged values the single-token
+    kernel keeps between calls, so each single-token result is bit-identical
+    to the one from a fresh workspace."""
+    dec = layer_case(synth.SHAPES["a3b_decode"], 0, None)
+    bat = layer_case(synth.SHAPES["a3b_batch64_zipf"], 0, None)
+    sb = bat["shape"]
+    _, _, y_fresh, _, _ = run_layer(m, dec)
+    ws = m.alloc_workspace(sb.T, sb.H, sb.E, sb.k, sb.I, device=DEV)
+    for _ in range(2):
+        idx, w, y, _, _ = run_layer(m, dec, ws=ws)
+        check_layer(dec, idx, w, y)
+        np.testing.assert_array_equal(y, y_fresh)
+        idx, w, y, _, _ = run_layer(m, bat, ws=ws)
+        check_layer(bat, idx, w, y)
+
+
 def test_grid_barrier_timeout_is_reported(m):
-    """A grid-barrier arrival that never comes: the bounded wait runs out, the
-    call records MOE_ERR_TIMEOUT, and the workspace works again after
-    re-initialisation."""
+    """A published value that never comes (CTA 0 publishes none of its router
+    logits): the bounded waits run out, the call records MOE_ERR_TIMEOUT, and
+    the workspace works again after re-initialisation."""
     case = layer_case(synth.SHAPES["tiny"], 0, None)
     s = case["shape"]
     d = to_dev(case)

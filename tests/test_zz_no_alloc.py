@@ -79,7 +79,7 @@ def test_noalloc_rejects_oversize_and_batches():
     f.argtypes = [P, P, P, P, P, P, I_, I_, I_, I_, I_, P, P, P, P]
     f.restype = ctypes.c_int
     a = 1 << 20
-    # k*I = 32*8192 floats is beyond the fixed scratch
+    # k*I = 32*8192 values of h are beyond the fixed scratch
     assert f(a, a, None, a, a, a, 1, 256, 64, 32, 8192, a, a, a, None) == 9
     # more than one token is not this entry point's job
     assert f(a, a, None, a, a, a, 2, 256, 8, 2, 256, a, a, a, None) == 1
