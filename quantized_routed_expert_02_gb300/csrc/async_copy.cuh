@@ -88,43 +88,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
-// global to this CTA's shared memory; completion is signalled on `bar` as
-// transaction bytes.
-__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
-                                              uint64_t *bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
-// 16-byte read-only global load with an L2 cache policy.
-__device__ __forceinline__ float4 ldg_f4_policy(const float *p, uint64_t policy) {
-    float4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p), "l"(policy));
-    return v;
-}
-
-// 16-byte asynchronous global->shared copy (L1 bypass) with an L2 policy.
-__device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint64_t policy) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)),
-                 "l"(src), "l"(policy)
+// 16-byte asynchronous global->shared copy (L1 bypass).  No L2 cache-policy
+// operand: kernels whose copies carried one (createpolicy + .L2::cache_hint)
+// raised illegal-instruction faults on GB300.
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
                  : "memory");
 }
 
@@ -158,6 +126,10 @@ __device__ __forceinline__ void cp_async_wait_pending(int n) {
 
 __device__ __forceinline__ void red_release_add_u64(unsigned long long *p, unsigned long long v) {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_relaxed_add_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {

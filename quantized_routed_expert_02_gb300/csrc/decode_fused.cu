@@ -11,8 +11,7 @@
 // Design (one CTA of 16 warps per SM, cooperative launch so every CTA is
 // resident):
 //  1. Every CTA stages x in shared memory and computes a share of the E
-//     router logits (Wr read with an L2 evict-last policy: it is re-read by
-//     every token, unlike the expert bytes, which are read evict-first).
+//     router logits.
 //     Each logit is published as one 64-bit word that also carries the
 //     call's tag, so readers need no barrier: they poll the words until
 //     every tag is the current one.
@@ -25,7 +24,8 @@
 //     per row, waited with cp.async.wait_group), then all threads request
 //     the CTA's down rows (its share of the H output rows, for all k
 //     experts).  Each value of h = SiLU(g) * u is published as a tagged word
-//     like the logits.
+//     like the logits.  (Requesting only a few rows ahead of the compute was
+//     measured slower: the stream then falls short of the HBM bandwidth.)
 //  4. Each CTA polls the k*I tagged h words into shared memory, then for
 //     each of its output rows computes o_j = Wd[e_j][row] . h_j for
 //     j = 0..k-1 and y = sum_j w_j o_j in slot order: deterministic, no
@@ -58,8 +58,9 @@ namespace fused {
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxNbw = 8;         // ring slots per warp
-constexpr int kHeadBytes = 4096;   // small shared arrays
-constexpr int kStageBatch = 8;     // h words in flight per thread while staging
+constexpr int kHeadBytes = 5120;   // small shared arrays (see the kernel's first lines)
+constexpr int kStageBatch = 8;     // 64-value groups of h in flight per warp while staging
+constexpr uint64_t kBackoffNs = 300;  // wait after a poll that found a stale word
 
 // Optional phase timeline for profiling builds (-DMOEQ4K_TIMELINE): thread 0
 // of each CTA stamps the global timer at phase boundaries into the
@@ -197,20 +198,13 @@ __device__ __forceinline__ float row_dot_pairs(const uint8_t *row, int nsb_rt, c
     return acc;
 }
 
-// Sum each 32-float run of the padded vector(s) into sum32; run q starts at
-// logical element 32*(q % runs_per_vec) of vector q / runs_per_vec.
-__device__ __forceinline__ void run_sums32(const float *vec, float *sum32, int count,
-                                           int runs_per_vec, int vec_stride) {
-    for (int q = threadIdx.x; q < count; q += kThreads) {
-        const int j = q / runs_per_vec, c = 32 * (q % runs_per_vec);
-        const float *v = vec + j * vec_stride + padded(c);
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-        for (int b = 0; b < 32; b += 2) {
-            s0 += v[b];
-            s1 += v[b + 1];
-        }
-        sum32[q] = s0 + s1;
+// Sum each 32-float run of the padded vector into sum32, one warp per run
+// (consecutive words, no bank conflicts; fixed reduction order).
+__device__ __forceinline__ void run_sums32(const float *vec, float *sum32, int runs, int warp,
+                                           int lane) {
+    for (int r = warp; r < runs; r += kWarps) {
+        const float s = warp_sum(vec[padded(32 * r + lane)]);
+        if (lane == 0) sum32[r] = s;
     }
 }
 
@@ -229,18 +223,10 @@ __device__ __forceinline__ int8_t digit(float f) {
     return int8_t(max(-127, min(127, __float2int_rn(f))));
 }
 
-// The warp holds one 32-element run of x, one element per lane.  Writes the
-// lane's three base-254 digits of x / s (s = max|x| / 127 over the run) and
-// returns s / 254.  Each remainder step is exact in fp32 (t - rint(t)); only
-// the scalings by 127/max and by 254 round, at fp32 precision.  A run with a
-// non-finite element gets a NaN scale, so the non-finite value propagates.
-__device__ __forceinline__ float run_digits(float v, int8_t &da, int8_t &db, int8_t &dc) {
-    float mx = fabsf(v);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const bool finite = __all_sync(0xffffffffu, fabsf(v) <= 3.402823466e38f);
-    const float inv = mx > 0.f ? 127.0f / mx : 0.f;
-    const float t = finite ? v * inv : 0.f;
+// Three base-254 digits of t (|t| <= 127): t ~= a + b/254 + c/254^2, each
+// digit in [-127, 127].  Each remainder step is exact in fp32 (t - rint(t));
+// only the scaling by 254 rounds, at fp32 precision.
+__device__ __forceinline__ void digits3(float t, int8_t &da, int8_t &db, int8_t &dc) {
     const float a = rintf(t);
     const float r1 = (t - a) * 254.0f;
     const float b = rintf(r1);
@@ -248,25 +234,79 @@ __device__ __forceinline__ float run_digits(float v, int8_t &da, int8_t &db, int
     da = digit(a);
     db = digit(b);
     dc = digit(rintf(r2));
+}
+
+__device__ __forceinline__ bool finite_f(float v) { return fabsf(v) <= 3.402823466e38f; }
+
+// Unsigned key with the order of the float: larger value, larger key.
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// The warp holds one 32-element run of x, one element per lane.  Writes the
+// lane's digits of x / s (s = max|x| / 127 over the run) and returns s / 254.
+// Only the scaling by 127/max rounds besides digits3's.  A run with a
+// non-finite element gets a NaN scale, so the non-finite value propagates.
+__device__ __forceinline__ float run_digits(float v, int8_t &da, int8_t &db, int8_t &dc) {
+    float mx = fabsf(v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const bool finite = __all_sync(0xffffffffu, finite_f(v));
+    const float inv = mx > 0.f ? 127.0f / mx : 0.f;
+    digits3(finite ? v * inv : 0.f, da, db, dc);
     return finite ? mx * (1.0f / (127.0f * 254.0f)) : __uint_as_float(0x7FC00000u);
 }
 
-// One lane's 64 elements of x (sub-block pair c of block s, elements
-// 256 s + 64 c + [0, 64)) as digit words (4 consecutive elements each; words
-// 0-7 are sub-block 2c, 8-15 sub-block 2c+1), their scales and fp32 sums.
+// The same for a run held as two elements per lane by a half-warp (lanes
+// 0-15 hold one run, 16-31 the next); the digits of each element pack into
+// one 16-bit word per plane (element v0 in the low byte).
+__device__ __forceinline__ float run_digits_pair(float v0, float v1, int lane, uint32_t &pa,
+                                                 uint32_t &pb, uint32_t &pc) {
+    float mx = fmaxf(fabsf(v0), fabsf(v1));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const uint32_t bad = __ballot_sync(0xffffffffu, !(finite_f(v0) && finite_f(v1)));
+    const bool finite = ((bad >> (lane & 16)) & 0xFFFFu) == 0;
+    const float inv = mx > 0.f ? 127.0f / mx : 0.f;
+    int8_t a0, b0, c0, a1, b1, c1;
+    digits3(finite ? v0 * inv : 0.f, a0, b0, c0);
+    digits3(finite ? v1 * inv : 0.f, a1, b1, c1);
+    pa = uint32_t(uint8_t(a0)) | (uint32_t(uint8_t(a1)) << 8);
+    pb = uint32_t(uint8_t(b0)) | (uint32_t(uint8_t(b1)) << 8);
+    pc = uint32_t(uint8_t(c0)) | (uint32_t(uint8_t(c1)) << 8);
+    return finite ? mx * (1.0f / (127.0f * 254.0f)) : __uint_as_float(0x7FC00000u);
+}
+
+// Digit planes hold 64-element units (unit u = elements 64u .. 64u+63):
+// element e sits at byte plane_offset(e, nunits) of its plane, so that the
+// 16-byte chunk q of consecutive units is contiguous (a warp reading its
+// units' chunk q touches consecutive banks).
+__device__ __forceinline__ int plane_offset(int e, int nunits) {
+    const int u = e >> 6, w = e & 63;
+    return ((w >> 4) * nunits + u) * 16 + (w & 15);
+}
+
+// One thread's 64-element unit of a vector (sub-block pair c of block s) as
+// digit words (4 consecutive elements each; words 0-7 are sub-block 2c,
+// 8-15 sub-block 2c+1), their scales and fp32 sums.
 struct XDigits {
     uint32_t a[16], b[16], c[16];
     float s0, s1;      // run scale / 254; s1 also / 16 (high nibbles are read unshifted)
     float sum0, sum1;  // sum of x over each run
 };
 
-__device__ __forceinline__ void load_digits(XDigits &X, const uint8_t *planes, int H,
-                                            const float *scales, const float *sum32, int e0) {
+// Planes a, b, c are `plane_bytes` apart; `u` is the unit, of `nunits`.
+__device__ __forceinline__ void load_digits(XDigits &X, const uint8_t *planes, int plane_bytes,
+                                            int nunits, int u, const float *scales,
+                                            const float *sum32) {
+    const int e0 = 64 * u;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const uint4 va = *reinterpret_cast<const uint4 *>(planes + e0 + 16 * q);
-        const uint4 vb = *reinterpret_cast<const uint4 *>(planes + H + e0 + 16 * q);
-        const uint4 vc = *reinterpret_cast<const uint4 *>(planes + 2 * H + e0 + 16 * q);
+        const uint8_t *chunk = planes + (q * nunits + u) * 16;
+        const uint4 va = *reinterpret_cast<const uint4 *>(chunk);
+        const uint4 vb = *reinterpret_cast<const uint4 *>(chunk + plane_bytes);
+        const uint4 vc = *reinterpret_cast<const uint4 *>(chunk + 2 * plane_bytes);
         X.a[4 * q] = va.x, X.a[4 * q + 1] = va.y, X.a[4 * q + 2] = va.z, X.a[4 * q + 3] = va.w;
         X.b[4 * q] = vb.x, X.b[4 * q + 1] = vb.y, X.b[4 * q + 2] = vb.z, X.b[4 * q + 3] = vb.w;
         X.c[4 * q] = vc.x, X.c[4 * q + 1] = vc.y, X.c[4 * q + 2] = vc.z, X.c[4 * q + 3] = vc.w;
@@ -321,14 +361,34 @@ __device__ __forceinline__ void warp_sum2(float &g, float &u, int lane) {
     u = __shfl_sync(0xffffffffu, keep, 16);
 }
 
+// Busy-wait on the global timer (no memory traffic) for about `ns`.
+__device__ __forceinline__ void pause_ns(uint64_t ns) {
+    const uint64_t until = global_timer_ns() + ns;
+    while (global_timer_ns() < until) {
+    }
+}
+
 // Poll one tagged word until it carries `tag`; false when `deadline` passes.
+// A miss waits kBackoffNs before the next load: every CTA polls the same few
+// lines, and back-to-back reloads were measured to delay the stores they wait
+// for by microseconds.
 __device__ __forceinline__ bool await_word(const unsigned long long *p, uint32_t tag,
                                            uint64_t deadline, unsigned long long &w) {
     w = ld_relaxed_u64(p);
     while (tag_of(w) != tag) {
         if (global_timer_ns() > deadline) return false;
-        __nanosleep(32);
+        pause_ns(kBackoffNs);
         w = ld_relaxed_u64(p);
+    }
+    return true;
+}
+
+// One thread polls a counter until it reaches `target`; false when `deadline`
+// passes.
+__device__ __forceinline__ bool await_count(const unsigned long long *c, unsigned long long target,
+                                            uint64_t deadline) {
+    while (ld_relaxed_u64(c) < target) {
+        if (global_timer_ns() > deadline) return false;
     }
     return true;
 }
@@ -342,7 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     int *sel_e = reinterpret_cast<int *>(smem + 16);
     float *sel_w = reinterpret_cast<float *>(sel_e + 32);
     int *flags = reinterpret_cast<int *>(sel_w + 32);  // [1] wait timed out
-    float *red = reinterpret_cast<float *>(flags + 4); // partial sums, then logits + ranks (2*kMaxE)
+    float *red = reinterpret_cast<float *>(flags + 4); // kWarps partial sums, then kMaxE logits
+    uint32_t *skey = reinterpret_cast<uint32_t *>(smem + 1536);  // kMaxE logit keys
+    int *pcnt = reinterpret_cast<int *>(smem + 2560);            // kThreads partial ranks
     float *vec = reinterpret_cast<float *>(smem + kHeadBytes);
     const int H = p.H, E = p.E, k = p.k, I = p.I;
     const int vec_pad = max(padded_len(H), k * padded_len(I));
@@ -371,7 +433,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     // ---------------- 1. router logits (a share per CTA).
     // The CTA's first logit is computed while x is staged: x and the router
     // row are requested together, so their latencies overlap.
-    const uint64_t pol_last = l2_policy_evict_last();
     {
         const int e = blockIdx.x;
         const bool logit = p.router_on && e < E;
@@ -380,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         for (int i = threadIdx.x; i < (H >> 2); i += kThreads) {
             const float4 x4 = __ldg(reinterpret_cast<const float4 *>(p.x) + i);
             if (logit) {
-                const float4 w4 = ldg_f4_policy(wr + 4 * i, pol_last);
+                const float4 w4 = __ldg(reinterpret_cast<const float4 *>(wr) + i);
                 a = fmaf(w4.x, x4.x, a);
                 a = fmaf(w4.y, x4.y, a);
                 a = fmaf(w4.z, x4.z, a);
@@ -398,28 +459,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             sum += p.bias ? p.bias[e] : 0.f;
             if (publish) st_relaxed_u64(p.sync + e, tagged(*tag_sh, sum));
         }
-        run_sums32(vec, vsum, H >> 5, H >> 5, 0);
-        if (kDigits) {
-            for (int r = warp; r < (H >> 5); r += kWarps) {
-                int8_t da, db, dc;
-                const float sc = run_digits(vec[padded(32 * r + lane)], da, db, dc);
-                planes[32 * r + lane] = uint8_t(da);
-                planes[H + 32 * r + lane] = uint8_t(db);
-                planes[2 * H + 32 * r + lane] = uint8_t(dc);
-                if (lane == 0) xscale[r] = sc;
-            }
-        }
-        __syncthreads();
     }
     const uint32_t tag = *tag_sh;
     if (threadIdx.x == 0) TL_STAMP(p, 1);
 
-    if (p.router_on) {
+    if (p.router_on && blockIdx.x + nblk < unsigned(E)) {
+        __syncthreads();  // thread 0 is done with `red`
         for (int e = blockIdx.x + nblk; e < E; e += nblk) {
             const float *wr = p.Wr + size_t(e) * H;
             float a = 0.f;
             for (int i = threadIdx.x; i < (H >> 2); i += kThreads) {
-                const float4 w4 = ldg_f4_policy(wr + 4 * i, pol_last);
+                const float4 w4 = __ldg(reinterpret_cast<const float4 *>(wr) + i);
                 const float4 x4 = *reinterpret_cast<const float4 *>(vec + padded(4 * i));
                 a = fmaf(w4.x, x4.x, a);
                 a = fmaf(w4.y, x4.y, a);
@@ -437,45 +487,87 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             }
             __syncthreads();
         }
-        if (threadIdx.x == 0) TL_STAMP(p, 2);
     }
+    if (threadIdx.x == 0) TL_STAMP(p, 2);
 
-    // ---------------- 2. top-k + renormalise, by rank: every CTA ranks the E
-    // logits in the order (value descending, index ascending); the logit of
-    // rank j < k is slot j.  G threads share the comparisons of one logit.
-    if (p.router_on) {
-        float *lsm = red;                     // E logits (red is free again)
-        int *rank = reinterpret_cast<int *>(lsm + kMaxE);
-        if (threadIdx.x < E) {
+    // ---------------- 2. the first Ep threads (E rounded up to a warp) poll
+    // the E logits into shared memory, as floats and as order-preserving
+    // keys, while the other warps prepare x for the gate/up rows (run sums,
+    // and for digit kernels the digits).
+    const int Ep = p.router_on ? ((E + 31) & ~31) : 0;
+    float *lsm = red + kWarps;  // E logits, clear of the partial sums thread 0 may still read
+    if (int(threadIdx.x) < Ep) {
+        uint32_t key = 0;  // below every logit's key
+        if (int(threadIdx.x) < E) {
             unsigned long long wv;
             if (!await_word(p.sync + threadIdx.x, tag, deadline, wv)) flags[1] = 1;
-            const float v = value_of(wv);
-            lsm[threadIdx.x] = (v == v) ? v : -INFINITY;   // a NaN never ranks first
-            rank[threadIdx.x] = 0;
+            float v = value_of(wv);
+            v = (v == v) ? v + 0.0f : -INFINITY;  // a NaN never ranks first; -0 ties +0
+            lsm[threadIdx.x] = v;
+            key = ordered_key(v);
         }
-        __syncthreads();
-        if (flags[1]) {
-            if (threadIdx.x == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 1);
-            return;  // no copies issued yet, no output written
-        }
-        if (threadIdx.x == 0) TL_STAMP(p, 8);
-        const int G = max(1, kThreads / E);      // threads per logit
-        const int per = (E + G - 1) / G;         // comparisons per thread
-        for (int t = threadIdx.x; t < E * G; t += kThreads) {
-            const int e = t / G, part = t % G;
-            const float ve = lsm[e];
-            int cnt = 0;
-            const int b0 = part * per, b1 = min(E, b0 + per);
-            for (int o = b0; o < b1; ++o) {
-                const float vo = lsm[o];
-                cnt += (vo > ve || (vo == ve && o < e)) ? 1 : 0;
+        skey[threadIdx.x] = key;
+    } else {
+        const int w0 = Ep >> 5, nw = kWarps - w0;
+        if (kDigits) {
+            // run sums and digits of x, one warp per 32-element run
+            for (int r = warp - w0; r < (H >> 5); r += nw) {
+                const float v = vec[padded(32 * r + lane)];
+                const float sum = warp_sum(v);
+                int8_t da, db, dc;
+                const float sc = run_digits(v, da, db, dc);
+                const int off = plane_offset(32 * r + lane, H >> 6);
+                planes[off] = uint8_t(da);
+                planes[H + off] = uint8_t(db);
+                planes[2 * H + off] = uint8_t(dc);
+                if (lane == 0) {
+                    xscale[r] = sc;
+                    vsum[r] = sum;
+                }
             }
-            if (cnt) atomicAdd(rank + e, cnt);
+        } else {
+            for (int r = warp - w0; r < (H >> 5); r += nw) {
+                const float sum = warp_sum(vec[padded(32 * r + lane)]);
+                if (lane == 0) vsum[r] = sum;
+            }
+        }
+    }
+    __syncthreads();
+    if (flags[1]) {
+        if (threadIdx.x == 0) {
+            record_status(p.hdr, MOE_ERR_TIMEOUT, 1);
+            red_relaxed_add_u64(&p.hdr->rows_done, 1ull);  // keep one count per CTA and call
+        }
+        return;  // no copies issued yet, no output written
+    }
+    if (threadIdx.x == 0) TL_STAMP(p, 8);
+
+    // Top-k + renormalise, by rank in the order (value descending, index
+    // ascending): the logit of rank j < k is slot j; every CTA finds the same.
+    // Thread t counts, for logit t % Ep, the keys in part t / Ep of the list
+    // that rank above it (G parts; a warp shares its part, so every load is a
+    // broadcast of four keys; no branches).
+    if (p.router_on) {
+        int G = 1;
+        while (2 * G * Ep <= kThreads && G < 8) G *= 2;
+        const int per = Ep / G;  // a multiple of 4
+        if (int(threadIdx.x) < Ep * G) {
+            const int e = threadIdx.x % Ep, b0 = (threadIdx.x / Ep) * per;
+            const uint32_t ke = skey[e];
+            int cnt = 0;
+            for (int o = b0; o < b0 + per; o += 4) {
+                const uint4 k4 = *reinterpret_cast<const uint4 *>(skey + o);
+                cnt += int(k4.x > ke) + int(k4.y > ke) + int(k4.z > ke) + int(k4.w > ke);
+                cnt += int((k4.x == ke) & (o < e)) + int((k4.y == ke) & (o + 1 < e)) +
+                       int((k4.z == ke) & (o + 2 < e)) + int((k4.w == ke) & (o + 3 < e));
+            }
+            pcnt[threadIdx.x] = cnt;
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < E; e += kThreads) {
-            const int r = rank[e];
-            if (r < k) sel_e[r] = e;
+        if (int(threadIdx.x) < E) {
+            int r = 0;
+            for (int g = 0; g < G; ++g) r += pcnt[g * Ep + threadIdx.x];
+            if (r < k) sel_e[r] = threadIdx.x;
         }
         __syncthreads();
         if (warp == 0) {
@@ -509,7 +601,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     const int R = r1 - r0;
     const int n_gu = u1 - u0;
     const int n_mine = n_gu > warp ? (n_gu - warp + kWarps - 1) / kWarps : 0;  // rows warp+16i
-    const uint64_t pol = l2_policy_evict_first();
     const int n16_gu = row_gu >> 4, n16_dn = row_dn >> 4;
     unsigned long long *hsync = p.sync + kSyncHWord;
 
@@ -523,33 +614,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             const uint8_t *uu = p.up + e * mat_gu + size_t(r) * row_gu;
             for (int c = lane; c < 2 * n16_gu; c += 32) {
                 const uint8_t *src = c < n16_gu ? g + 16 * c : uu + 16 * (c - n16_gu);
-                cp_async_16(dst + 16 * c, src, pol);
+                cp_async_16(dst + 16 * c, src);
             }
         }
         cp_async_commit();
     };
-    // every row of the warp has its own slot (the host only launches shapes
-    // where n_mine <= nbw), then the CTA's R output rows of all k experts,
-    // as k contiguous ranges: all weight bytes are requested up front
-    for (int i = 0; i < n_mine; ++i) issue_gu(i);
+    // this thread's share of the CTA's R output rows of all k experts (k
+    // contiguous ranges), one commit group
     uint8_t *dbuf = smem + p.down_off;
-    {
+    auto issue_down = [&]() {
         const int per_j = R * n16_dn;
         for (int c = threadIdx.x; c < k * per_j; c += kThreads) {
             const int j = c / per_j, w16 = c % per_j;
             const int e = sel_e[j];
             if (e >= 0 && e < E)
-                cp_async_16(dbuf + 16 * c, p.down + e * mat_dn + size_t(r0) * row_dn + 16 * w16, pol);
+                cp_async_16(dbuf + 16 * c, p.down + e * mat_dn + size_t(r0) * row_dn + 16 * w16);
         }
-        cp_async_commit();  // one group after the gate/up rows
-    }
+        cp_async_commit();
+    };
+
+    // Every row of the warp has its own slot (the host only launches shapes
+    // where n_mine <= nbw): all gate/up rows are requested at once, then the
+    // down rows.  Commit groups: row 0, ..., row n_mine-1, the down rows.
+    // No cp.async targets shared memory that ordinary loads or stores used
+    // earlier in the kernel: kernels that did (slots reused for later rows,
+    // scratch arrays in the slots) raised illegal-instruction faults on
+    // GB300.
+    for (int i = 0; i < n_mine; ++i) issue_gu(i);
+    issue_down();
 
     XDigits X;
-    if (kDigits) load_digits(X, planes, H, xscale, vsum, 64 * lane);
+    if (kDigits) load_digits(X, planes, H, H >> 6, lane, xscale, vsum);
 
     for (int i = 0; i < n_mine; ++i) {
-        // groups committed after row i: the later rows and the down rows
-        cp_async_wait_pending(n_mine - i);
+        cp_async_wait_pending(n_mine - i);  // the later rows and the down rows may pend
         __syncwarp();
         if (threadIdx.x == 0 && i == 0) TL_STAMP(p, 9);
         const int u = u0 + warp + kWarps * i, j = u / I, r = u % I;
@@ -575,33 +673,79 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
 
     // ---------------- 4. h of all k slots -> down rows + combine
     __syncthreads();  // x in `vec` is dead once every warp is past its rows
+    // This CTA's h values are out: count it in the header, then thread 0
+    // waits until every CTA of the call has (one polled word per CTA keeps
+    // the polling cheap).  The tagged h words are then read once; a value
+    // whose store is not visible yet is re-read by the staging rounds.
+    if (threadIdx.x == 0) {
+        if (publish) red_relaxed_add_u64(&p.hdr->rows_done, 1ull);
+        if (!await_count(&p.hdr->rows_done, (unsigned long long)tag * nblk, deadline)) flags[1] = 1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) TL_STAMP(p, 6);
     const int ip = padded_len(I);
+    // digit kernels keep h as three digit planes of k*I bytes plus one scale
+    // per 32-element run, in place of the fp32 vector
+    uint8_t *hplanes = reinterpret_cast<uint8_t *>(vec);
+    float *hscale = reinterpret_cast<float *>(hplanes + 3 * k * I);
     {
-        // kStageBatch two-word loads per thread in flight, then wait for
-        // any word whose tag is not yet the current one
-        const int n2 = (k * I) >> 1;
+        // h as 64-value groups (a group never spans two slots: I is a multiple
+        // of 256); warp w stages groups w, w+16, ..., lane l holding values
+        // 64g + 2l and 64g + 2l + 1.  Each round reloads every word of the
+        // batch that does not carry the current tag yet, so a round costs
+        // one L2 round trip.  The two 32-element run sums of a group come
+        // from a reduction over each half-warp.
+        const int ngroups = (k * I) >> 6;
         bool ok = true;
-        for (int q0 = threadIdx.x; q0 < n2; q0 += kStageBatch * kThreads) {
+        const int gend = flags[1] == 0 ? ngroups : 0;  // CTA-uniform: skip after a time-out
+        for (int g0 = warp; g0 < gend; g0 += kStageBatch * kWarps) {
             unsigned long long wa[kStageBatch], wb[kStageBatch];
+            uint32_t pending = 0;
 #pragma unroll
             for (int t = 0; t < kStageBatch; ++t) {
-                const int q = q0 + t * kThreads;
+                const int g = g0 + t * kWarps;
                 wa[t] = wb[t] = tagged(tag, 0.f);  // slots of invalid experts stay 0
-                if (q < n2) {
-                    const int e = sel_e[(2 * q) / I];
-                    if (e >= 0 && e < E) ld_relaxed_v2u64(hsync + 2 * q, wa[t], wb[t]);
+                if (g < ngroups && ok) {
+                    const int e = sel_e[(64 * g) / I];
+                    if (e >= 0 && e < E) pending |= 1u << t;
                 }
+            }
+            while (pending) {
+#pragma unroll
+                for (int t = 0; t < kStageBatch; ++t)
+                    if (pending & (1u << t))
+                        ld_relaxed_v2u64(hsync + 64 * (g0 + t * kWarps) + 2 * lane, wa[t], wb[t]);
+#pragma unroll
+                for (int t = 0; t < kStageBatch; ++t)
+                    if (tag_of(wa[t]) == tag && tag_of(wb[t]) == tag) pending &= ~(1u << t);
+                if (pending && global_timer_ns() > deadline) {
+                    ok = false;
+                    break;
+                }
+                if (pending) pause_ns(kBackoffNs);
             }
 #pragma unroll
             for (int t = 0; t < kStageBatch; ++t) {
-                const int q = q0 + t * kThreads;
-                if (q >= n2) continue;
-                if (ok && tag_of(wa[t]) != tag) ok = await_word(hsync + 2 * q, tag, deadline, wa[t]);
-                if (ok && tag_of(wb[t]) != tag)
-                    ok = await_word(hsync + 2 * q + 1, tag, deadline, wb[t]);
-                const int j = (2 * q) / I, c = 2 * q - j * I;
-                *reinterpret_cast<float2 *>(vec + j * ip + padded(c)) =
-                    make_float2(value_of(wa[t]), value_of(wb[t]));
+                const int g = g0 + t * kWarps;
+                if (g >= ngroups) break;  // warp-uniform
+                const float v0 = value_of(wa[t]), v1 = value_of(wb[t]);
+                if (kDigits) {
+                    // digits of h in the planes at `vec`, one 16-bit word per lane
+                    uint32_t da, db, dc;
+                    const float sc = run_digits_pair(v0, v1, lane, da, db, dc);
+                    uint8_t *pl = hplanes + plane_offset(64 * g + 2 * lane, (k * I) >> 6);
+                    *reinterpret_cast<uint16_t *>(pl) = uint16_t(da);
+                    *reinterpret_cast<uint16_t *>(pl + k * I) = uint16_t(db);
+                    *reinterpret_cast<uint16_t *>(pl + 2 * k * I) = uint16_t(dc);
+                    if ((lane & 15) == 0) hscale[2 * g + (lane >> 4)] = sc;
+                } else {
+                    const int j = (64 * g) / I, c = 64 * g - j * I + 2 * lane;
+                    *reinterpret_cast<float2 *>(vec + j * ip + padded(c)) = make_float2(v0, v1);
+                }
+                float rs = v0 + v1;
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+                if ((lane & 15) == 0) vsum[2 * g + (lane >> 4)] = rs;
             }
         }
         if (!ok) flags[1] = 1;
@@ -611,37 +755,68 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     if (flags[1]) {
         if (threadIdx.x == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 4);
     } else {
-        run_sums32(vec, vsum, (k * I) >> 5, I >> 5, ip);
-        __syncthreads();
-        if (threadIdx.x == 0) TL_STAMP(p, 6);
 
-        const int n_rows = R > warp ? (R - warp + kWarps - 1) / kWarps : 0;  // rows warp+16i
         cp_async_wait_all();  // this thread's share of the down rows
         __syncthreads();      // everyone's share
         if (threadIdx.x == 0) TL_STAMP(p, 10);
         const size_t jstride = size_t(R) * row_dn;
-        for (int i = 0; i < n_rows; ++i) {
-            const int rr = warp + kWarps * i;  // row inside the CTA's share
-            const uint8_t *src = dbuf + size_t(rr) * row_dn;
-            // k experts x nsb_i blocks x 4 sub-block pairs, spread over the 32
-            // lanes in a fixed order; each pair's partial dot is weighted by its
-            // slot's router weight, then one warp reduction gives y
-            // (deterministic)
-            float yacc = 0.f;
-            const int per_j = (NSB_I > 0 ? NSB_I : nsb_i) * 4;   // (block, pair) units per slot
-            const int nunits = k * per_j;
-            for (int t = lane; t < nunits; t += 32) {
-                const int j = t / per_j, rem = t - j * per_j;
-                const int sb = rem >> 2, c = rem & 3;
+        if (kDigits) {
+            // Thread -> unit u = (slot j, block sb, pair c) of the down rows;
+            // its 64 elements of h_j stay in registers while it walks rows
+            // q, q + Q, ... of the CTA's share.  The weighted partial dots go
+            // to P[row][u] (in the gate/up slots, free now), then one warp per
+            // row sums them in a fixed order.
+            constexpr int kPer = (NSB_I > 0 ? NSB_I : 1) * 4;  // units per slot
+            const int Ud = k * kPer;                           // <= 512
+            const int Q = kThreads / Ud;
+            float *P = reinterpret_cast<float *>(smem + p.ring_off);
+            const int u = threadIdx.x % Ud, q = threadIdx.x / Ud;
+            if (q < Q) {
+                const int j = u / kPer, rem = u - j * kPer, sb = rem >> 2, c = rem & 3;
                 const int e = sel_e[j];
-                if (e < 0 || e >= E) continue;
-                const float part = pair_dot(src + j * jstride + sb * kBlockBytes, c,
-                                            vec + j * ip + padded(sb * kQK + 64 * c),
-                                            vsum + j * (I >> 5) + sb * 8 + 2 * c);
-                yacc = fmaf(sel_w[j], part, yacc);
+                const bool valid = e >= 0 && e < E;
+                const float wj = sel_w[j];
+                XDigits Xh;
+                load_digits(Xh, hplanes, k * I, (k * I) >> 6, (j * I + kQK * sb + 64 * c) >> 6,
+                            hscale, vsum);
+                const uint8_t *base = dbuf + j * jstride + sb * kBlockBytes;
+                for (int rr = q; rr < R; rr += Q) {
+                    const float part = valid ? wj * pair_dot_digits(base + rr * row_dn, c, Xh) : 0.f;
+                    P[rr * Ud + u] = part;
+                }
             }
-            yacc = warp_sum(yacc);
-            if (lane == 0) p.y[r0 + rr] = yacc;
+            __syncthreads();
+            for (int rr = warp; rr < R; rr += kWarps) {
+                float acc = 0.f;
+                for (int uu = lane; uu < Ud; uu += 32) acc += P[rr * Ud + uu];
+                acc = warp_sum(acc);
+                if (lane == 0) p.y[r0 + rr] = acc;
+            }
+        } else {
+            const int n_rows = R > warp ? (R - warp + kWarps - 1) / kWarps : 0;  // rows warp+16i
+            for (int i = 0; i < n_rows; ++i) {
+                const int rr = warp + kWarps * i;  // row inside the CTA's share
+                const uint8_t *src = dbuf + size_t(rr) * row_dn;
+                // k experts x nsb_i blocks x 4 sub-block pairs, spread over the
+                // 32 lanes in a fixed order; each pair's partial dot is
+                // weighted by its slot's router weight, then one warp reduction
+                // gives y (deterministic)
+                float yacc = 0.f;
+                const int per_j = (NSB_I > 0 ? NSB_I : nsb_i) * 4;  // (block, pair) units per slot
+                const int nunits = k * per_j;
+                for (int t = lane; t < nunits; t += 32) {
+                    const int j = t / per_j, rem = t - j * per_j;
+                    const int sb = rem >> 2, c = rem & 3;
+                    const int e = sel_e[j];
+                    if (e < 0 || e >= E) continue;
+                    const float part = pair_dot(src + j * jstride + sb * kBlockBytes, c,
+                                                vec + j * ip + padded(sb * kQK + 64 * c),
+                                                vsum + j * (I >> 5) + sb * 8 + 2 * c);
+                    yacc = fmaf(sel_w[j], part, yacc);
+                }
+                yacc = warp_sum(yacc);
+                if (lane == 0) p.y[r0 + rr] = yacc;
+            }
         }
     }
     // every copy this thread issued must land before the CTA's shared memory goes away
@@ -686,6 +861,10 @@ bool fused_config(int H, int E, int k, int I, int nblk, int max_smem, FusedConfi
     const int units_max = (k * I + nblk - 1) / nblk;
     const int rows_per_warp = (units_max + kWarps - 1) / kWarps;
     if (nbw < 1 || nbw < rows_per_warp) return false;
+    // digit kernels keep the down rows' partial dots (rmax x units) in the slots
+    if (uses_digits(H, I) &&
+        size_t(rmax) * k * (I / kQK) * 4 * sizeof(float) > size_t(kWarps) * rows_per_warp * slot)
+        return false;
     c.dig_off = vec_end;
     c.down_off = dig_end;
     c.ring_off = dig_end + down_bytes;
