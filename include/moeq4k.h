@@ -191,7 +191,7 @@ MOE_API moe_status moe_read_device_status(const void *ws_dev, void *stream, int3
  *
  * Scratch: a fixed 256 KB array in device global memory defined by the
  * library (held on every GPU that loads it until the process exits).  It
- * fits k*I <= 32480 and E <= 256; larger shapes return
+ * fits k*I <= 64960 and E <= 256; larger shapes return
  * MOE_ERR_SCRATCH_LIMIT.  Shapes the single-token kernel does not take
  * return MOE_ERR_INVALID_SHAPE.  The call allocates and frees nothing; it
  * clears the scratch's status word with an async memset on `stream`, then

@@ -81,9 +81,9 @@ struct Ws {
     unsigned long long *u64(size_t off) const {
         return reinterpret_cast<unsigned long long *>(base + off);
     }
-    // the single-token kernel's profiling timeline: the per-slot activation
-    // regions, which that kernel does not use
-    int timeline_cap() const { return int((L.x16 - L.h) / sizeof(unsigned long long)); }
+    // the single-token kernel's profiling timeline: the per-slot output
+    // region, which that kernel does not use
+    int timeline_cap() const { return int((L.x16 - L.o) / sizeof(unsigned long long)); }
 };
 
 moe_status check_ws(void *ws, size_t ws_bytes, const WsLayout &L) {
@@ -233,7 +233,7 @@ moe_status moe_ffn(const float *x, const int32_t *idx, const float *w, const voi
         return cuda_status(launch_decode_fused(
             dev, x, nullptr, nullptr, idx, w, nullptr, nullptr, static_cast<const uint8_t *>(gate),
             static_cast<const uint8_t *>(up), static_cast<const uint8_t *>(down), H, E, k, I, y,
-            W.u64(L.sync), W.hdr(), g_withhold, g_wait_ns, W.u64(L.h), W.timeline_cap(),
+            W.u64(L.sync), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns, W.u64(L.o), W.timeline_cap(),
             static_cast<cudaStream_t>(stream)));
     }
     return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev,
@@ -263,7 +263,7 @@ moe_status moe_layer(const float *x, const float *Wr, const float *bias, const v
         return cuda_status(launch_decode_fused(
             dev, x, Wr, bias, nullptr, nullptr, idx, w, static_cast<const uint8_t *>(gate),
             static_cast<const uint8_t *>(up), static_cast<const uint8_t *>(down), H, E, k, I, y,
-            W.u64(L.sync), W.hdr(), g_withhold, g_wait_ns, W.u64(L.h), W.timeline_cap(), s));
+            W.u64(L.sync), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns, W.u64(L.o), W.timeline_cap(), s));
     }
     MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), s)));
     return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev, s);

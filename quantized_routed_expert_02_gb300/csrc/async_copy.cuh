@@ -151,15 +151,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return v;
 }
 
-// Two adjacent words; each is single-copy atomic on its own.
-__device__ __forceinline__ void ld_relaxed_v2u64(const unsigned long long *p,
-                                                 unsigned long long &a, unsigned long long &b) {
-    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];"
-                 : "=l"(a), "=l"(b)
-                 : "l"(p)
-                 : "memory");
-}
-
 // Barrier over the first `nthreads` threads of the CTA (named barrier 1).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -27,8 +27,9 @@ struct WsHeader {
     // since initialisation (n = 0, 1, ...) a CTA's add returns a value in
     // [n * nblk, (n + 1) * nblk); the call tags what it publishes with n + 1.
     unsigned long long cta_calls;
-    // Single-token kernel: every CTA adds 1 once its gate/up rows are out, so
-    // the count reaches tag * nblk when the call's h is complete.
+    // Single-token kernel: every CTA adds 1 (release) once its values of h
+    // are stored, so the count reaches tag * nblk when the call's h is
+    // complete.
     unsigned long long rows_done;
     uint32_t tc_work[2];             // prefill GEMMs: next work item (gate/up, down)
     int32_t tc_chunks;               // prefill GEMMs: expert chunks of <= 256 slots
@@ -42,13 +43,11 @@ struct TcChunk {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 // Tag region of the single-token kernel, right after the header: the router
-// logits at words [0, E), h at [kSyncHWord, +k*I); each word is
-// (call tag << 32 | fp32 bits).  Place and size are the same for every
-// shape, so the region never holds anything but tags (or the zeros of
-// moe_workspace_init), and tags only grow between initialisations: a word
-// left by an earlier call can never carry the current call's tag.
-constexpr size_t kSyncHWord = kMaxE;
-constexpr size_t kSyncWords = kSyncHWord + size_t(kMaxK) * kMaxHI;
+// logits, each a word (call tag << 32 | fp32 bits).  Place and size are the
+// same for every shape, so the region never holds anything but tags (or the
+// zeros of moe_workspace_init), and tags only grow between initialisations:
+// a word left by an earlier call can never carry the current call's tag.
+constexpr size_t kSyncWords = kMaxE;
 
 struct WsLayout {
     size_t sync, counts, offs, active, nactive, perm, h, o, logits, x16, h16, chunks, xstage, ystage,

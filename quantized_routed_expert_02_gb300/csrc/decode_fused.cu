@@ -59,8 +59,8 @@ constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxNbw = 8;         // ring slots per warp
 constexpr int kHeadBytes = 5120;   // small shared arrays (see the kernel's first lines)
-constexpr int kStageBatch = 8;     // 64-value groups of h in flight per warp while staging
-constexpr uint64_t kBackoffNs = 300;  // wait after a poll that found a stale word
+constexpr int kStageBatch = 8;     // 128-value chunks of h in flight per warp while staging
+constexpr long long kBackoffCycles = 600;  // wait after a poll that found a stale word
 
 // Optional phase timeline for profiling builds (-DMOEQ4K_TIMELINE): thread 0
 // of each CTA stamps the global timer at phase boundaries into the
@@ -83,7 +83,8 @@ struct Params {
     float *w_out;
     const uint8_t *gate, *up, *down;
     float *y;
-    unsigned long long *sync;     // tag region: logits at [0, E), h at [kSyncHWord, +k*I)
+    unsigned long long *sync;     // tagged router logits [E]
+    float *hbuf;                  // h = SiLU(g) * u of the k slots [k, I]
     WsHeader *hdr;
     int H, E, k, I;
     int router_on;
@@ -219,23 +220,6 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
-__device__ __forceinline__ int8_t digit(float f) {
-    return int8_t(max(-127, min(127, __float2int_rn(f))));
-}
-
-// Three base-254 digits of t (|t| <= 127): t ~= a + b/254 + c/254^2, each
-// digit in [-127, 127].  Each remainder step is exact in fp32 (t - rint(t));
-// only the scaling by 254 rounds, at fp32 precision.
-__device__ __forceinline__ void digits3(float t, int8_t &da, int8_t &db, int8_t &dc) {
-    const float a = rintf(t);
-    const float r1 = (t - a) * 254.0f;
-    const float b = rintf(r1);
-    const float r2 = (r1 - b) * 254.0f;
-    da = digit(a);
-    db = digit(b);
-    dc = digit(rintf(r2));
-}
-
 __device__ __forceinline__ bool finite_f(float v) { return fabsf(v) <= 3.402823466e38f; }
 
 // Unsigned key with the order of the float: larger value, larger key.
@@ -244,37 +228,64 @@ __device__ __forceinline__ uint32_t ordered_key(float v) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// The warp holds one 32-element run of x, one element per lane.  Writes the
-// lane's digits of x / s (s = max|x| / 127 over the run) and returns s / 254.
-// Only the scaling by 127/max rounds besides digits3's.  A run with a
-// non-finite element gets a NaN scale, so the non-finite value propagates.
-__device__ __forceinline__ float run_digits(float v, int8_t &da, int8_t &db, int8_t &dc) {
-    float mx = fabsf(v);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const bool finite = __all_sync(0xffffffffu, finite_f(v));
-    const float inv = mx > 0.f ? 127.0f / mx : 0.f;
-    digits3(finite ? v * inv : 0.f, da, db, dc);
-    return finite ? mx * (1.0f / (127.0f * 254.0f)) : __uint_as_float(0x7FC00000u);
+// Round to nearest (ties to even) of |t| < 2^22 by adding 1.5 * 2^23: the
+// integer sits in the low mantissa bits.  Returns it, and the rounded value
+// in `r`.  The _rn intrinsics keep the adds out of any fused multiply-add.
+__device__ __forceinline__ int round_shift(float t, float &r) {
+    const float tm = __fadd_rn(t, 12582912.0f);
+    r = __fadd_rn(tm, -12582912.0f);
+    return __float_as_int(tm) - 0x4B400000;
 }
 
-// The same for a run held as two elements per lane by a half-warp (lanes
-// 0-15 hold one run, 16-31 the next); the digits of each element pack into
-// one 16-bit word per plane (element v0 in the low byte).
-__device__ __forceinline__ float run_digits_pair(float v0, float v1, int lane, uint32_t &pa,
-                                                 uint32_t &pb, uint32_t &pc) {
-    float mx = fmaxf(fabsf(v0), fabsf(v1));
+// Three base-254 digits of t (|t| <= 127): t ~= a + b/254 + c/254^2, each in
+// [-127, 127].  Each remainder t - rint(t) is exact in fp32; only the
+// scalings by 254 round, at fp32 precision.
+__device__ __forceinline__ void digits3(float t, int &a, int &b, int &c) {
+    float ra, rb, rc;
+    a = round_shift(t, ra);
+    const float r1 = __fmul_rn(__fsub_rn(t, ra), 254.0f);
+    b = round_shift(r1, rb);
+    const float r2 = __fmul_rn(__fsub_rn(r1, rb), 254.0f);
+    c = round_shift(r2, rc);
+}
+
+// Low bytes of four ints as one word (a0 in the lowest byte).
+__device__ __forceinline__ uint32_t pack4(int a0, int a1, int a2, int a3) {
+    return __byte_perm(__byte_perm(a0, a1, 0x0040), __byte_perm(a2, a3, 0x0040), 0x5410);
+}
+
+// A warp holds 128 consecutive elements, lane l the four at 4l (so lanes
+// 8q..8q+7 hold the q-th 32-element run).  Sum of the lane's run, in a fixed
+// order.
+__device__ __forceinline__ float run_sum4(const float4 v) {
+    float s = (v.x + v.y) + (v.z + v.w);
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const uint32_t bad = __ballot_sync(0xffffffffu, !(finite_f(v0) && finite_f(v1)));
-    const bool finite = ((bad >> (lane & 16)) & 0xFFFFu) == 0;
-    const float inv = mx > 0.f ? 127.0f / mx : 0.f;
-    int8_t a0, b0, c0, a1, b1, c1;
-    digits3(finite ? v0 * inv : 0.f, a0, b0, c0);
-    digits3(finite ? v1 * inv : 0.f, a1, b1, c1);
-    pa = uint32_t(uint8_t(a0)) | (uint32_t(uint8_t(a1)) << 8);
-    pb = uint32_t(uint8_t(b0)) | (uint32_t(uint8_t(b1)) << 8);
-    pc = uint32_t(uint8_t(c0)) | (uint32_t(uint8_t(c1)) << 8);
+    for (int o = 4; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
+}
+
+// The same layout: writes the lane's digits of x / s (s = max|x| / 127 over
+// its run) as one packed word per plane and the run's sum; returns s / 254.
+// Only the scaling by 127/max rounds besides digits3's.  A run with a
+// non-finite element gets a NaN scale, so the non-finite value propagates.
+__device__ __forceinline__ float run_digits4(const float4 v, int lane, uint32_t &wa, uint32_t &wb,
+                                             uint32_t &wc, float &sum) {
+    float mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    sum = run_sum4(v);
+    const uint32_t bad = __ballot_sync(
+        0xffffffffu, !(finite_f(v.x) && finite_f(v.y) && finite_f(v.z) && finite_f(v.w)));
+    const bool finite = ((bad >> (lane & 24)) & 0xFFu) == 0;
+    const float inv = (finite && mx > 0.f) ? 127.0f / mx : 0.f;
+    int a0, b0, c0, a1, b1, c1, a2, b2, c2, a3, b3, c3;
+    digits3(v.x * inv, a0, b0, c0);
+    digits3(v.y * inv, a1, b1, c1);
+    digits3(v.z * inv, a2, b2, c2);
+    digits3(v.w * inv, a3, b3, c3);
+    wa = pack4(a0, a1, a2, a3);
+    wb = pack4(b0, b1, b2, b3);
+    wc = pack4(c0, c1, c2, c3);
     return finite ? mx * (1.0f / (127.0f * 254.0f)) : __uint_as_float(0x7FC00000u);
 }
 
@@ -361,23 +372,23 @@ __device__ __forceinline__ void warp_sum2(float &g, float &u, int lane) {
     u = __shfl_sync(0xffffffffu, keep, 16);
 }
 
-// Busy-wait on the global timer (no memory traffic) for about `ns`.
-__device__ __forceinline__ void pause_ns(uint64_t ns) {
-    const uint64_t until = global_timer_ns() + ns;
-    while (global_timer_ns() < until) {
+// Busy-wait on the SM clock (no memory traffic) for about `cycles`.
+__device__ __forceinline__ void pause_cycles(long long cycles) {
+    const long long until = clock64() + cycles;
+    while (clock64() < until) {
     }
 }
 
 // Poll one tagged word until it carries `tag`; false when `deadline` passes.
-// A miss waits kBackoffNs before the next load: every CTA polls the same few
-// lines, and back-to-back reloads were measured to delay the stores they wait
-// for by microseconds.
+// A miss waits kBackoffCycles before the next load: every CTA polls the same
+// few lines, and back-to-back reloads were measured to delay the stores they
+// wait for by microseconds.
 __device__ __forceinline__ bool await_word(const unsigned long long *p, uint32_t tag,
                                            uint64_t deadline, unsigned long long &w) {
     w = ld_relaxed_u64(p);
     while (tag_of(w) != tag) {
         if (global_timer_ns() > deadline) return false;
-        pause_ns(kBackoffNs);
+        pause_cycles(kBackoffCycles);
         w = ld_relaxed_u64(p);
     }
     return true;
@@ -401,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     uint32_t *tag_sh = reinterpret_cast<uint32_t *>(smem);
     int *sel_e = reinterpret_cast<int *>(smem + 16);
     float *sel_w = reinterpret_cast<float *>(sel_e + 32);
-    int *flags = reinterpret_cast<int *>(sel_w + 32);  // [1] wait timed out
+    int *flags = reinterpret_cast<int *>(sel_w + 32);  // [1] wait timed out, [2] tied ranks
     float *red = reinterpret_cast<float *>(flags + 4); // kWarps partial sums, then kMaxE logits
     uint32_t *skey = reinterpret_cast<uint32_t *>(smem + 1536);  // kMaxE logit keys
     int *pcnt = reinterpret_cast<int *>(smem + 2560);            // kThreads partial ranks
@@ -429,7 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         TL_STAMP(p, 0);
         calls0 = atomicAdd(&p.hdr->cta_calls, 1ull);
         flags[1] = 0;
+        flags[2] = 0;
     }
+    if (threadIdx.x < 32) sel_e[threadIdx.x] = -1;
     // ---------------- 1. router logits (a share per CTA).
     // The CTA's first logit is computed while x is staged: x and the router
     // row are requested together, so their latencies overlap.
@@ -508,27 +521,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         }
         skey[threadIdx.x] = key;
     } else {
+        // x in 128-element chunks, lane l holding elements 4l..4l+3 of a chunk
+        // (8 lanes per 32-element run): run sums, and for digit kernels the
+        // digits (one packed word per plane and lane) and run scales
         const int w0 = Ep >> 5, nw = kWarps - w0;
-        if (kDigits) {
-            // run sums and digits of x, one warp per 32-element run
-            for (int r = warp - w0; r < (H >> 5); r += nw) {
-                const float v = vec[padded(32 * r + lane)];
-                const float sum = warp_sum(v);
-                int8_t da, db, dc;
-                const float sc = run_digits(v, da, db, dc);
-                const int off = plane_offset(32 * r + lane, H >> 6);
-                planes[off] = uint8_t(da);
-                planes[H + off] = uint8_t(db);
-                planes[2 * H + off] = uint8_t(dc);
-                if (lane == 0) {
-                    xscale[r] = sc;
-                    vsum[r] = sum;
+        for (int c = warp - w0; c < (H >> 7); c += nw) {
+            const int e0 = 128 * c + 4 * lane;
+            const float4 v = *reinterpret_cast<const float4 *>(vec + padded(e0));
+            if (kDigits) {
+                uint32_t wa, wb, wc;
+                float sum;
+                const float sc = run_digits4(v, lane, wa, wb, wc, sum);
+                const int off = plane_offset(e0, H >> 6);
+                *reinterpret_cast<uint32_t *>(planes + off) = wa;
+                *reinterpret_cast<uint32_t *>(planes + H + off) = wb;
+                *reinterpret_cast<uint32_t *>(planes + 2 * H + off) = wc;
+                if ((lane & 7) == 0) {
+                    xscale[e0 >> 5] = sc;
+                    vsum[e0 >> 5] = sum;
                 }
-            }
-        } else {
-            for (int r = warp - w0; r < (H >> 5); r += nw) {
-                const float sum = warp_sum(vec[padded(32 * r + lane)]);
-                if (lane == 0) vsum[r] = sum;
+            } else {
+                const float sum = run_sum4(v);
+                if ((lane & 7) == 0) vsum[e0 >> 5] = sum;
             }
         }
     }
@@ -542,47 +556,58 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     }
     if (threadIdx.x == 0) TL_STAMP(p, 8);
 
-    // Top-k + renormalise, by rank in the order (value descending, index
-    // ascending): the logit of rank j < k is slot j; every CTA finds the same.
-    // Thread t counts, for logit t % Ep, the keys in part t / Ep of the list
-    // that rank above it (G parts; a warp shares its part, so every load is a
-    // broadcast of four keys; no branches).
+    // Top-k by rank in the order (value descending, index ascending): the
+    // logit of rank j < k is slot j; every CTA finds the same.  Thread t
+    // counts, for logit t % Ep, the keys in part t / Ep of the list that are
+    // greater (G parts; a warp shares its part, so every load is a broadcast
+    // of four keys).  Equal keys get equal counts; when two logits claim the
+    // same rank below k, the counts are redone with ties ranked by index.
+    // The softmax weights are computed later, off this path.
     if (p.router_on) {
         int G = 1;
         while (2 * G * Ep <= kThreads && G < 8) G *= 2;
         const int per = Ep / G;  // a multiple of 4
-        if (int(threadIdx.x) < Ep * G) {
-            const int e = threadIdx.x % Ep, b0 = (threadIdx.x / Ep) * per;
+        const bool counter = int(threadIdx.x) < Ep * G;
+        const int e = threadIdx.x % Ep, b0 = (threadIdx.x / Ep) * per;
+        if (counter) {
             const uint32_t ke = skey[e];
             int cnt = 0;
             for (int o = b0; o < b0 + per; o += 4) {
                 const uint4 k4 = *reinterpret_cast<const uint4 *>(skey + o);
                 cnt += int(k4.x > ke) + int(k4.y > ke) + int(k4.z > ke) + int(k4.w > ke);
-                cnt += int((k4.x == ke) & (o < e)) + int((k4.y == ke) & (o + 1 < e)) +
-                       int((k4.z == ke) & (o + 2 < e)) + int((k4.w == ke) & (o + 3 < e));
             }
             pcnt[threadIdx.x] = cnt;
         }
+        if (threadIdx.x == 0) TL_STAMP(p, 11);
         __syncthreads();
+        if (threadIdx.x == 0) TL_STAMP(p, 12);
         if (int(threadIdx.x) < E) {
             int r = 0;
             for (int g = 0; g < G; ++g) r += pcnt[g * Ep + threadIdx.x];
-            if (r < k) sel_e[r] = threadIdx.x;
+            if (r < k && atomicCAS(sel_e + r, -1, int(threadIdx.x)) != -1) flags[2] = 1;
         }
         __syncthreads();
-        if (warp == 0) {
-            const float l = (lane < k) ? lsm[sel_e[lane]] : 0.f;
-            const float l0 = lsm[sel_e[0]];
-            const float ex = (lane < k) ? expf(l - l0) : 0.f;
-            const float z = warp_sum(ex);
-            if (lane < k) {
-                sel_w[lane] = ex / z;
-                if (blockIdx.x == 0) {
-                    p.idx_out[lane] = sel_e[lane];
-                    p.w_out[lane] = ex / z;
+        if (flags[2]) {
+            if (counter) {
+                const uint32_t ke = skey[e];
+                int cnt = 0;
+                for (int o = b0; o < b0 + per; o += 4) {
+                    const uint4 k4 = *reinterpret_cast<const uint4 *>(skey + o);
+                    cnt += int(k4.x > ke) + int(k4.y > ke) + int(k4.z > ke) + int(k4.w > ke);
+                    cnt += int((k4.x == ke) & (o < e)) + int((k4.y == ke) & (o + 1 < e)) +
+                           int((k4.z == ke) & (o + 2 < e)) + int((k4.w == ke) & (o + 3 < e));
                 }
+                pcnt[threadIdx.x] = cnt;
             }
+            __syncthreads();
+            if (int(threadIdx.x) < E) {
+                int r = 0;
+                for (int g = 0; g < G; ++g) r += pcnt[g * Ep + threadIdx.x];
+                if (r < k) sel_e[r] = threadIdx.x;
+            }
+            __syncthreads();
         }
+        if (threadIdx.x == 0) TL_STAMP(p, 13);
     } else if (warp == 0 && lane < k) {
         const int e = p.idx_in[lane];
         sel_e[lane] = e;
@@ -602,7 +627,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     const int n_gu = u1 - u0;
     const int n_mine = n_gu > warp ? (n_gu - warp + kWarps - 1) / kWarps : 0;  // rows warp+16i
     const int n16_gu = row_gu >> 4, n16_dn = row_dn >> 4;
-    unsigned long long *hsync = p.sync + kSyncHWord;
 
     // issue the copies of this warp's i-th gate/up row pair into ring slot i
     auto issue_gu = [&](int i) {
@@ -643,6 +667,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     for (int i = 0; i < n_mine; ++i) issue_gu(i);
     issue_down();
 
+    // the renormalised router weights of the k slots (softmax over the top k),
+    // needed only by the down rows
+    if (p.router_on && warp == 0) {
+        const float l = (lane < k) ? lsm[sel_e[lane]] : 0.f;
+        const float l0 = lsm[sel_e[0]];
+        const float ex = (lane < k) ? expf(l - l0) : 0.f;
+        const float z = warp_sum(ex);
+        if (lane < k) {
+            sel_w[lane] = ex / z;
+            if (blockIdx.x == 0) {
+                p.idx_out[lane] = sel_e[lane];
+                p.w_out[lane] = ex / z;
+            }
+        }
+    }
+
     XDigits X;
     if (kDigits) load_digits(X, planes, H, H >> 6, lane, xscale, vsum);
 
@@ -664,8 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
                 g = warp_sum(row_dot_pairs<NSB_H>(src, nsb_h, vec, vsum, lane));
                 uu = warp_sum(row_dot_pairs<NSB_H>(src + row_gu, nsb_h, vec, vsum, lane));
             }
-            if (lane == 0 && publish)
-                st_relaxed_u64(hsync + size_t(j) * I + r, tagged(tag, silu_mul(g, uu)));
+            if (lane == 0) p.hbuf[size_t(j) * I + r] = silu_mul(g, uu);
         }
         __syncwarp();
     }
@@ -673,12 +712,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
 
     // ---------------- 4. h of all k slots -> down rows + combine
     __syncthreads();  // x in `vec` is dead once every warp is past its rows
-    // This CTA's h values are out: count it in the header, then thread 0
-    // waits until every CTA of the call has (one polled word per CTA keeps
-    // the polling cheap).  The tagged h words are then read once; a value
-    // whose store is not visible yet is re-read by the staging rounds.
+    // This CTA's h values are out: count it in the header (release: the
+    // CTA barrier above orders every warp's h stores before it), then thread
+    // 0 waits until every CTA of the call has (acquire; one polled word per
+    // CTA keeps the polling cheap).  h is then read once.
     if (threadIdx.x == 0) {
-        if (publish) red_relaxed_add_u64(&p.hdr->rows_done, 1ull);
+        if (publish) {
+            __threadfence();
+            red_release_add_u64(&p.hdr->rows_done, 1ull);
+        }
         if (!await_count(&p.hdr->rows_done, (unsigned long long)tag * nblk, deadline)) flags[1] = 1;
     }
     __syncthreads();
@@ -688,68 +730,51 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     // per 32-element run, in place of the fp32 vector
     uint8_t *hplanes = reinterpret_cast<uint8_t *>(vec);
     float *hscale = reinterpret_cast<float *>(hplanes + 3 * k * I);
-    {
-        // h as 64-value groups (a group never spans two slots: I is a multiple
-        // of 256); warp w stages groups w, w+16, ..., lane l holding values
-        // 64g + 2l and 64g + 2l + 1.  Each round reloads every word of the
-        // batch that does not carry the current tag yet, so a round costs
-        // one L2 round trip.  The two 32-element run sums of a group come
-        // from a reduction over each half-warp.
-        const int ngroups = (k * I) >> 6;
-        bool ok = true;
-        const int gend = flags[1] == 0 ? ngroups : 0;  // CTA-uniform: skip after a time-out
-        for (int g0 = warp; g0 < gend; g0 += kStageBatch * kWarps) {
-            unsigned long long wa[kStageBatch], wb[kStageBatch];
-            uint32_t pending = 0;
+    if (flags[1] == 0) {
+        // h in 128-element chunks (a chunk never spans two slots: I is a
+        // multiple of 256); warp w stages chunks w, w+16, ..., lane l holding
+        // elements 4l..4l+3, kStageBatch chunks in flight per warp.  Slots of
+        // invalid experts read as 0.
+        const int nchunks = (k * I) >> 7;
+        const float4 *h4 = reinterpret_cast<const float4 *>(p.hbuf);
+        for (int c0 = warp; c0 < nchunks; c0 += kStageBatch * kWarps) {
+            float4 v[kStageBatch];
 #pragma unroll
             for (int t = 0; t < kStageBatch; ++t) {
-                const int g = g0 + t * kWarps;
-                wa[t] = wb[t] = tagged(tag, 0.f);  // slots of invalid experts stay 0
-                if (g < ngroups && ok) {
-                    const int e = sel_e[(64 * g) / I];
-                    if (e >= 0 && e < E) pending |= 1u << t;
+                const int c = c0 + t * kWarps, e0 = 128 * c + 4 * lane;
+                v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c < nchunks) {
+                    const int e = sel_e[e0 / I];
+                    if (e >= 0 && e < E) v[t] = __ldcg(h4 + (e0 >> 2));
                 }
             }
-            while (pending) {
-#pragma unroll
-                for (int t = 0; t < kStageBatch; ++t)
-                    if (pending & (1u << t))
-                        ld_relaxed_v2u64(hsync + 64 * (g0 + t * kWarps) + 2 * lane, wa[t], wb[t]);
-#pragma unroll
-                for (int t = 0; t < kStageBatch; ++t)
-                    if (tag_of(wa[t]) == tag && tag_of(wb[t]) == tag) pending &= ~(1u << t);
-                if (pending && global_timer_ns() > deadline) {
-                    ok = false;
-                    break;
-                }
-                if (pending) pause_ns(kBackoffNs);
-            }
+            if (threadIdx.x == 0 && c0 == 0) TL_STAMP(p, 14);
 #pragma unroll
             for (int t = 0; t < kStageBatch; ++t) {
-                const int g = g0 + t * kWarps;
-                if (g >= ngroups) break;  // warp-uniform
-                const float v0 = value_of(wa[t]), v1 = value_of(wb[t]);
+                const int c = c0 + t * kWarps, e0 = 128 * c + 4 * lane;
+                if (c >= nchunks) break;  // warp-uniform
                 if (kDigits) {
-                    // digits of h in the planes at `vec`, one 16-bit word per lane
-                    uint32_t da, db, dc;
-                    const float sc = run_digits_pair(v0, v1, lane, da, db, dc);
-                    uint8_t *pl = hplanes + plane_offset(64 * g + 2 * lane, (k * I) >> 6);
-                    *reinterpret_cast<uint16_t *>(pl) = uint16_t(da);
-                    *reinterpret_cast<uint16_t *>(pl + k * I) = uint16_t(db);
-                    *reinterpret_cast<uint16_t *>(pl + 2 * k * I) = uint16_t(dc);
-                    if ((lane & 15) == 0) hscale[2 * g + (lane >> 4)] = sc;
+                    uint32_t wa, wb, wc;
+                    float sum;
+                    const float sc = run_digits4(v[t], lane, wa, wb, wc, sum);
+                    const int off = plane_offset(e0, (k * I) >> 6);
+                    *reinterpret_cast<uint32_t *>(hplanes + off) = wa;
+                    *reinterpret_cast<uint32_t *>(hplanes + k * I + off) = wb;
+                    *reinterpret_cast<uint32_t *>(hplanes + 2 * k * I + off) = wc;
+                    if ((lane & 7) == 0) {
+                        hscale[e0 >> 5] = sc;
+                        vsum[e0 >> 5] = sum;
+                    }
                 } else {
-                    const int j = (64 * g) / I, c = 64 * g - j * I + 2 * lane;
-                    *reinterpret_cast<float2 *>(vec + j * ip + padded(c)) = make_float2(v0, v1);
+                    const int j = e0 / I;
+                    *reinterpret_cast<float4 *>(vec + j * ip + padded(e0 - j * I)) = v[t];
+                    const float sum = run_sum4(v[t]);
+                    if ((lane & 7) == 0) vsum[e0 >> 5] = sum;
                 }
-                float rs = v0 + v1;
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
-                if ((lane & 15) == 0) vsum[2 * g + (lane >> 4)] = rs;
             }
         }
-        if (!ok) flags[1] = 1;
     }
+    if (threadIdx.x == 0) TL_STAMP(p, 15);
     __syncthreads();
     if (threadIdx.x == 0) TL_STAMP(p, 5);
     if (flags[1]) {
@@ -916,7 +941,7 @@ cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const 
                                 const int32_t *idx_in, const float *w_in, int32_t *idx_out,
                                 float *w_out, const uint8_t *gate, const uint8_t *up,
                                 const uint8_t *down, int H, int E, int k, int I, float *y,
-                                unsigned long long *sync, WsHeader *hdr, int withhold,
+                                unsigned long long *sync, float *hbuf, WsHeader *hdr, int withhold,
                                 unsigned long long wait_ns, unsigned long long *timeline,
                                 int timeline_cap, cudaStream_t s) {
     FusedConfig c;
@@ -935,6 +960,7 @@ cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const 
     p.down = down;
     p.y = y;
     p.sync = sync;
+    p.hbuf = hbuf;
     p.hdr = hdr;
     p.H = H;
     p.E = E;

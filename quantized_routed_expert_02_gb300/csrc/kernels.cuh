@@ -43,13 +43,14 @@ cudaError_t init_decode_fused(int dev, int num_sms);
 bool decode_fused_supported(int dev, int T, int H, int E, int k, int I);
 // Wr == nullptr: routing comes from idx_in / w_in (moe_ffn); otherwise the
 // kernel routes and writes idx_out / w_out (moe_layer).  `sync` is the tag
-// region (kSyncWords words, zero or tags of earlier calls of this header);
-// `timeline` (timeline_cap words) is written only by profiling builds.
+// region (kSyncWords words, zero or tags of earlier calls of this header),
+// `hbuf` k*I floats of scratch; `timeline` (timeline_cap words) is written
+// only by profiling builds.
 cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const float *bias,
                                 const int32_t *idx_in, const float *w_in, int32_t *idx_out,
                                 float *w_out, const uint8_t *gate, const uint8_t *up,
                                 const uint8_t *down, int H, int E, int k, int I, float *y,
-                                unsigned long long *sync, WsHeader *hdr, int withhold,
+                                unsigned long long *sync, float *hbuf, WsHeader *hdr, int withhold,
                                 unsigned long long wait_ns, unsigned long long *timeline,
                                 int timeline_cap, cudaStream_t s);
 

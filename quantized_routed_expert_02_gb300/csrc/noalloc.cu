@@ -6,13 +6,13 @@
 // hot path.  They still own x, the weights and the outputs, but cannot
 // provide the scratch workspace the other entry points take.  This entry
 // point runs the same single-token kernel with its scratch (status word,
-// call counter, tagged router logits and expert activations h) in a fixed
+// call counters, tagged router logits and expert activations h) in a fixed
 // array in device global memory that the library itself defines.
 //
 // The array lives for as long as the library is loaded, on every GPU that
 // loads it; it starts zeroed.  All calls share it and it keeps the previous
-// call's contents, which is what the kernel needs: the call counter only
-// grows, so the tags left by earlier calls never match a later call's.  The
+// call's contents, which is what the kernel needs: the call counters only
+// grow, so the tags left by earlier calls never match a later call's.  The
 // call clears the status word itself.  Calls that overlap on the GPU
 // (different streams, or several host threads) race on the array and must
 // be serialised by the caller.
@@ -25,12 +25,12 @@
 namespace moeq4k {
 namespace {
 
-// Header (256 B), then the tag region: kSyncHWord words for the router
-// logits, then one word per value of h (k*I words).
+// Header (256 B), then the tagged router logits (kSyncWords words), then h
+// (k*I floats).
 constexpr size_t kNoallocScratchBytes = 256 * 1024;
 constexpr size_t kNoallocSyncOff = 256;
-constexpr size_t kNoallocMaxKI =
-    (kNoallocScratchBytes - kNoallocSyncOff) / sizeof(unsigned long long) - kSyncHWord;
+constexpr size_t kNoallocHOff = kNoallocSyncOff + sizeof(unsigned long long) * kSyncWords;
+constexpr size_t kNoallocMaxKI = (kNoallocScratchBytes - kNoallocHOff) / sizeof(float);
 
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -78,7 +78,7 @@ extern "C" moe_status moe_layer_noalloc(const float *x, const float *Wr, const f
     st = noalloc_scratch(dev, &scratch);
     if (st != MOE_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the status word starts at zero on every call; the call counter must not
+    // the status word starts at zero on every call; the call counters must not
     static_assert(offsetof(WsHeader, status) == 0 && offsetof(WsHeader, detail) == 4,
                   "status and detail lead the header");
     if (cudaMemsetAsync(scratch, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -86,6 +86,7 @@ extern "C" moe_status moe_layer_noalloc(const float *x, const float *Wr, const f
         dev, x, Wr, bias, nullptr, nullptr, idx, w, static_cast<const uint8_t *>(gate),
         static_cast<const uint8_t *>(up), static_cast<const uint8_t *>(down), H, E, k, I, y,
         reinterpret_cast<unsigned long long *>(scratch + kNoallocSyncOff),
-        reinterpret_cast<WsHeader *>(scratch), 0, 1000000000ull, nullptr, 0, s);
+        reinterpret_cast<float *>(scratch + kNoallocHOff), reinterpret_cast<WsHeader *>(scratch), 0,
+        1000000000ull, nullptr, 0, s);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
