@@ -344,6 +344,9 @@ def main():
     if dist is not None:
         dist.barrier()
     clk = clocks.stop(t_region0, t_region1)
+    code, detail = m.moe_read_device_status(ws, stream)
+    if code != 0:  # a device-side error or time-out inside the timed region voids the number
+        raise RuntimeError(f"device status after the timed region: {m.status_str(code)} ({detail})")
     ms = start.elapsed_time(end)
     if dist is not None:
         t = torch.tensor([ms], device=dev)
