@@ -159,12 +159,14 @@ def profiled_traffic(kernel_src, profile):
 
 
 def measured_peaks():
+    """(HBM GB/s, sustained dense bf16 TFLOP/s, kind) from MEASURED_PEAKS.json,
+    else the recipe's fallback figures."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return d.get("hbm_gbs"), "measured"
-    return 6800.0, "fallback"
+        return d.get("hbm_gbs"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1700.0, "fallback"
 
 
 # ---------------------------------------------------------------- oracle (CPU) timing
@@ -379,22 +381,36 @@ def main():
                "h2d_bytes_per_step": n_layers * T * H * 4,
                "d2h_bytes_per_step": n_layers * T * H * 4}
 
-    peak, peak_kind = measured_peaks()
+    peak, tflops_peak, peak_kind = measured_peaks()
     call_us = ms_per_step * 1e3 / n_layers
     achieved = (step_bytes / n_layers) / (call_us * 1e-6) / 1e9
     single = m.moe_layer_launch_count(T, H, E, k, I) == 1
     traffic = profiled_traffic("quantized_routed_expert_02_gb300/csrc/decode_fused.cu",
                                "decode_fused_a3b_decode.md") if (single and args.config == "a3b_decode") else None
-    roofline = {
-        "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-        "frac": round(achieved / peak, 4), "traffic": traffic,
+    # The tensor-core path (T*k >= 2048) is a dense contraction: its roofline is
+    # the slower of the bytes at HBM peak and the FLOPs at the tensor peak
+    # (fp16 operands; the dense fp16 and bf16 peaks are equal on this part).
+    flops_per_call = 6.0 * T * k * H * I
+    tensor_path = T * k >= 2048
+    hbm_floor_us = (step_bytes / n_layers) / (peak * 1e9) * 1e6
+    tensor_floor_us = flops_per_call / (tflops_peak * 1e12) * 1e6
+    if tensor_path and tensor_floor_us > hbm_floor_us:
+        tf = flops_per_call / (call_us * 1e-6) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tf, 1), "peak": tflops_peak,
+                    "unit": "TFLOP/s", "frac": round(tf / tflops_peak, 4), "traffic": None,
+                    "hbm_frac": round(achieved / peak, 4)}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": traffic}
+    roofline.update({
         "kernel": ("decode_fused_kernel (the only launch of a call; duration = timed region / calls)"
                    if single else "moe_layer call (all launches of one call)"),
-        "peak_kind": peak_kind,
+        "peak_kind": peak_kind + (" (sustained bf16 GEMM)" if roofline["bound"] == "tensor" else ""),
         "algorithmic_bytes_per_call": step_bytes / n_layers,
+        "flops_per_call": flops_per_call,
         "achieved_incl_router_weight": round(
             ((step_bytes + wr_bytes) / n_layers) / (call_us * 1e-6) / 1e9, 1),
-    }
+    })
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -414,7 +430,7 @@ def main():
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f32",
+            "dtype": "f16xf16->f32" if tensor_path else "f32",
             "data": "synthetic",
             "config": {
                 "workload": args.config, "T": T, "H": H, "E": E, "k": k, "I": I,
