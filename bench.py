@@ -387,11 +387,11 @@ def main():
     single = m.moe_layer_launch_count(T, H, E, k, I) == 1
     traffic = profiled_traffic("quantized_routed_expert_02_gb300/csrc/decode_fused.cu",
                                "decode_fused_a3b_decode.md") if (single and args.config == "a3b_decode") else None
-    # The tensor-core path (T*k >= 2048) is a dense contraction: its roofline is
+    # The tensor-core path (T*k >= 256 routed slots) is a dense contraction: its roofline is
     # the slower of the bytes at HBM peak and the FLOPs at the tensor peak
     # (fp16 operands; the dense fp16 and bf16 peaks are equal on this part).
     flops_per_call = 6.0 * T * k * H * I
-    tensor_path = T * k >= 2048
+    tensor_path = T * k >= 256
     hbm_floor_us = (step_bytes / n_layers) / (peak * 1e9) * 1e6
     tensor_floor_us = flops_per_call / (tflops_peak * 1e12) * 1e6
     if tensor_path and tensor_floor_us > hbm_floor_us:

@@ -119,26 +119,33 @@ __device__ __forceinline__ void head_scales(const uint4 &h, int c, float &a0, fl
     b1 = dd.y * u6f(m1);
 }
 
-// 1 + q/128 as fp32 from byte i of v (bytes hold 0x80 | q).
-__device__ __forceinline__ float opq(uint32_t v, int i) {
-    return __uint_as_float(__byte_perm(v, 0x3F000000u, 0x7044u | (uint32_t(i) << 8)));
-}
+// K order inside the fp16 operand tiles: within each aligned group of four,
+// positions 1 and 2 are swapped (the dequantiser below produces that order
+// two codes per instruction; the activation operands are written in the same
+// order, so every dot product is unchanged).
+__host__ __device__ inline int kperm(int k) { return (k & ~3) | ((k & 1) << 1) | ((k >> 1) & 1); }
 
-// Eight weights (codes in bytes i..i+3 of words v0, v1; w = a*q - b) as one
-// 16-byte chunk of fp16.
-__device__ __forceinline__ uint4 weights8(uint32_t v0, uint32_t v1, float a, float b) {
-    // w = a*q - b = (128a)*(1 + q/128) - (128a + b)
-    const float A = 128.0f * a, C = -(A + b);
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+// w = q*a - b for the 8 codes of one 16-byte output chunk: nibble `shift`
+// (0 low, 4 high) of bytes 0..3 of v0, then of v1.  (v >> s) & 0x000F000F |
+// 0x64006400 puts two codes into the low mantissa bits of the fp16 value
+// 1024 (bytes 0 and 2, or 1 and 3); subtracting 1024 is exact, then one
+// fused multiply-add per pair applies d*sc and dmin*m with one rounding.
+// Output order: codes 0, 2, 1, 3, 4, 6, 5, 7.
+__device__ __forceinline__ uint4 weights8(uint32_t v0, uint32_t v1, int shift, __half2 a2,
+                                          __half2 nb2) {
+    const __half2 k1024 = bits_h2(0x64006400u);
+    const uint32_t p0 = ((v0 >> shift) & 0x000F000Fu) | 0x64006400u;
+    const uint32_t p1 = ((v0 >> (shift + 8)) & 0x000F000Fu) | 0x64006400u;
+    const uint32_t p2 = ((v1 >> shift) & 0x000F000Fu) | 0x64006400u;
+    const uint32_t p3 = ((v1 >> (shift + 8)) & 0x000F000Fu) | 0x64006400u;
     uint4 r;
-    __half2 h;
-    h = __floats2half2_rn(fmaf(A, opq(v0, 0), C), fmaf(A, opq(v0, 1), C));
-    r.x = *reinterpret_cast<uint32_t *>(&h);
-    h = __floats2half2_rn(fmaf(A, opq(v0, 2), C), fmaf(A, opq(v0, 3), C));
-    r.y = *reinterpret_cast<uint32_t *>(&h);
-    h = __floats2half2_rn(fmaf(A, opq(v1, 0), C), fmaf(A, opq(v1, 1), C));
-    r.z = *reinterpret_cast<uint32_t *>(&h);
-    h = __floats2half2_rn(fmaf(A, opq(v1, 2), C), fmaf(A, opq(v1, 3), C));
-    r.w = *reinterpret_cast<uint32_t *>(&h);
+    r.x = h2_bits(__hfma2(__hsub2(bits_h2(p0), k1024), a2, nb2));
+    r.y = h2_bits(__hfma2(__hsub2(bits_h2(p1), k1024), a2, nb2));
+    r.z = h2_bits(__hfma2(__hsub2(bits_h2(p2), k1024), a2, nb2));
+    r.w = h2_bits(__hfma2(__hsub2(bits_h2(p3), k1024), a2, nb2));
     return r;
 }
 
@@ -156,12 +163,15 @@ __device__ __forceinline__ RawStage raw_from_smem(const uint8_t *blk, int s) {
     return r;
 }
 
-// Write `nchunks` 16-byte chunks (weights 8j..8j+7 for j in [j0, j0+nchunks))
-// of row `r` of the stage's 64 weights into a swizzled tile.
+// Write `nchunks` 16-byte chunks (weights 8j..8j+7 for j in [j0, j0+nchunks),
+// in the kperm order) of row `r` of the stage's 64 weights into a swizzled
+// tile.
 __device__ __forceinline__ void store_row(uint8_t *tile, int r, const RawStage &raw, int s, int j0,
                                           int nchunks) {
     float a0, b0, a1, b1;
     head_scales(raw.head, s & 3, a0, b0, a1, b1);
+    const __half2 A0 = __float2half2_rn(a0), A1 = __float2half2_rn(a1);
+    const __half2 NB0 = __float2half2_rn(-b0), NB1 = __float2half2_rn(-b1);
     const uint32_t w[8] = {raw.q0.x, raw.q0.y, raw.q0.z, raw.q0.w,
                            raw.q1.x, raw.q1.y, raw.q1.z, raw.q1.w};
 #pragma unroll
@@ -170,15 +180,8 @@ __device__ __forceinline__ void store_row(uint8_t *tile, int r, const RawStage &
         // chunk jj < 4: low nibbles of code bytes 8jj..8jj+7 (sub-block 2c);
         // chunk jj >= 4: high nibbles of bytes 8(jj-4).. (sub-block 2c+1)
         const int wb = 2 * (jj & 3);
-        uint32_t v0, v1;
-        if (jj < 4) {
-            v0 = (w[wb] & 0x0F0F0F0Fu) | 0x80808080u;
-            v1 = (w[wb + 1] & 0x0F0F0F0Fu) | 0x80808080u;
-        } else {
-            v0 = ((w[wb] >> 4) & 0x0F0F0F0Fu) | 0x80808080u;
-            v1 = ((w[wb + 1] >> 4) & 0x0F0F0F0Fu) | 0x80808080u;
-        }
-        const uint4 out = jj < 4 ? weights8(v0, v1, a0, b0) : weights8(v0, v1, a1, b1);
+        const uint4 out = jj < 4 ? weights8(w[wb], w[wb + 1], 0, A0, NB0)
+                                 : weights8(w[wb], w[wb + 1], 4, A1, NB1);
         *reinterpret_cast<uint4 *>(tile + tc::sw128_offset(r, 8 * jj)) = out;
     }
 }
@@ -345,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             tc::fence_after_sync();
             if (ok && !info[1]) {
                 const int row = rt * kBM + warp * 32 + lane;
+                const int prow = kperm(row);  // h is the down GEMM's K: stored in kperm order
                 const int pos0 = p.offs[ch.e] + ch.tok_off;  // sorted row of column 0
                 const uint32_t lanebase = taddr + (uint32_t(warp * 32) << 16);
                 for (int n0 = 0; n0 < nmma; n0 += 8) {
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         for (int j = 0; j < 8; ++j) {
                             const int n = n0 + j;
                             if (n < ntok)
-                                p.h16[size_t(pos0 + n) * p.I + row] = __float2half_rn(silu_mul(g[j], u[j]));
+                                p.h16[size_t(pos0 + n) * p.I + prow] = __float2half_rn(silu_mul(g[j], u[j]));
                         }
                     } else {
 #pragma unroll
@@ -387,7 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     if (warp == 0) tc::tmem_dealloc(taddr, tcols);
 }
 
-// Activations in expert-sorted order: row i of xs = x[perm[i] / k] as fp16.
+// Activations in expert-sorted order: row i of xs = x[perm[i] / k] as fp16,
+// each group of four elements in kperm order.
 __global__ void gather_half_kernel(const float *__restrict__ x, const int32_t *__restrict__ perm,
                                    const int32_t *__restrict__ offs, int E, int k, int H,
                                    __half *__restrict__ xs) {
@@ -399,7 +404,8 @@ __global__ void gather_half_kernel(const float *__restrict__ x, const int32_t *_
         const int r = int(i / per_row), c = int(i % per_row);
         const int t = perm[r] / k;
         const float4 v = reinterpret_cast<const float4 *>(x + size_t(t) * H)[c];
-        __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+        // kperm order within each group of four: x0, x2, x1, x3
+        __half2 a = __floats2half2_rn(v.x, v.z), b = __floats2half2_rn(v.y, v.w);
         uint2 o;
         o.x = *reinterpret_cast<uint32_t *>(&a);
         o.y = *reinterpret_cast<uint32_t *>(&b);
@@ -482,8 +488,13 @@ cudaError_t init_prefill_tc(int dev) {
                                 optin);
 }
 
+// Batches of at least kMinTcSlots routed slots take the tensor-core GEMMs:
+// their cost is one dequantisation per weight per expert chunk, whatever the
+// number of tokens, while the CUDA-core path's grows with the tokens.
+constexpr int kMinTcSlots = 256;
+
 bool prefill_tc_supported(int T, int H, int E, int k, int I) {
-    return T * k >= 2048 && I % ptc::kBM == 0 && H % ptc::kBM == 0;
+    return T * k >= kMinTcSlots && I % ptc::kBM == 0 && H % ptc::kBM == 0;
 }
 
 cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, const uint8_t *up,
