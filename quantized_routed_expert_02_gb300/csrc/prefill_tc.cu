@@ -26,8 +26,9 @@
 //   thread 0    issues tcgen05.mma (fp16 x fp16 -> fp32 in tensor memory)
 //               when a stage is full and commits its completion to the
 //               stage's "empty" mbarrier;
-//   warps 0-3   read the accumulators back (tcgen05.ld) for the epilogue;
-//               while the main loop runs they park on a named barrier.
+//   all warps   read the accumulators back (tcgen05.ld) for the epilogue
+//               once the item's MMAs are complete, each warp a third of the
+//               columns of its TMEM lane quadrant.
 // Every wait is bounded by a global-timer deadline and records
 // MOE_ERR_TIMEOUT when it runs out.
 #include <cuda.h>
@@ -338,42 +339,49 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
         }
 
-        // ---- epilogue: warps 0-3 own TMEM lanes 0-127 (the tile's weight rows)
-        if (warp < 4) {
-            // idle threads sleep on a CTA barrier; thread 0 alone waits for the MMAs
-            named_bar_sync(2, 128);
-            if (tid == 0) info[2] = wait_bar(done, items & 1, deadline, p.hdr, 14) ? 1 : 0;
-            named_bar_sync(2, 128);
-            const bool ok = info[2] != 0;
-            tc::fence_after_sync();
-            if (ok && !info[1]) {
-                const int row = rt * kBM + warp * 32 + lane;
-                const int prow = kperm(row);  // h is the down GEMM's K: stored in kperm order
-                const int pos0 = p.offs[ch.e] + ch.tok_off;  // sorted row of column 0
-                const uint32_t lanebase = taddr + (uint32_t(warp * 32) << 16);
-                for (int n0 = 0; n0 < nmma; n0 += 8) {
-                    float g[8];
-                    tc::tmem_ld8(lanebase + n0, g);
-                    if (p.mode == 0) {
-                        float u[8];
-                        tc::tmem_ld8(lanebase + 256 + n0, u);
+        // ---- epilogue, by all 12 warps: warp w reads the TMEM lanes of
+        // quadrant w % 4 (32 of the tile's weight rows) for column part w / 4
+        // of three (in 8-column units)
+        __syncthreads();  // every role is past its main loop
+        if (tid == 0) info[2] = wait_bar(done, items & 1, deadline, p.hdr, 14) ? 1 : 0;
+        __syncthreads();
+        tc::fence_after_sync();
+        if (info[2] != 0 && !info[1]) {
+            const int q = warp & 3, part = warp >> 2;
+            const int units = nmma >> 3;
+            const int u_lo = units * part / 3, u_hi = units * (part + 1) / 3;
+            const int row = rt * kBM + q * 32 + lane;
+            const int prow = kperm(row);  // h is the down GEMM's K: stored in kperm order
+            const int pos0 = p.offs[ch.e] + ch.tok_off;  // sorted row of column 0
+            const uint32_t lanebase = taddr + (uint32_t(q * 32) << 16);
+            for (int uu = u_lo; uu < u_hi; ++uu) {
+                const int n0 = 8 * uu;
+                float g[8];
+                tc::tmem_ld8(lanebase + n0, g);
+                if (p.mode == 0) {
+                    float u[8];
+                    tc::tmem_ld8(lanebase + 256 + n0, u);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int n = n0 + j;
-                            if (n < ntok)
-                                p.h16[size_t(pos0 + n) * p.I + prow] = __float2half_rn(silu_mul(g[j], u[j]));
+                    for (int j = 0; j < 8; ++j) {
+                        const int n = n0 + j;
+                        if (n < ntok) {
+                            // SiLU(g) * u with the fast exponential and divide: the
+                            // result is rounded to fp16
+                            const float e = __expf(fminf(-g[j], 80.0f));
+                            p.h16[size_t(pos0 + n) * p.I + prow] =
+                                __float2half_rn(__fdividef(g[j], 1.0f + e) * u[j]);
                         }
-                    } else {
+                    }
+                } else {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int n = n0 + j;
-                            if (n < ntok) p.o[size_t(toks[n]) * p.H + row] = g[j];
-                        }
+                    for (int j = 0; j < 8; ++j) {
+                        const int n = n0 + j;
+                        if (n < ntok) p.o[size_t(toks[n]) * p.H + row] = g[j];
                     }
                 }
             }
-            tc::fence_before_sync();
         }
+        tc::fence_before_sync();
         gs += S;
         grs += nsb;
         ++items;
