@@ -100,12 +100,12 @@ moe_status ffn_enqueue(const float *x, const int32_t *idx, const float *w, const
     const WsLayout &L = ws.L;
     MOE_TRY(cuda_status(launch_permute(idx, T, k, E, ws.i32(L.counts), ws.i32(L.offs),
                                        ws.i32(L.perm), ws.i32(L.active), ws.i32(L.nactive),
-                                       ws.hdr(), s)));
+                                       ws.i32(L.blockcnt), ws.i32(L.slotpos), ws.hdr(), s)));
     if (prefill_tc_supported(T, H, E, k, I)) {
         MOE_TRY(cuda_status(launch_prefill_tc(
             dev, x, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
             static_cast<const uint8_t *>(down), T, H, E, k, I, ws.i32(L.offs), ws.i32(L.perm),
-            ws.i32(L.active), ws.i32(L.nactive), reinterpret_cast<__half *>(ws.base + L.x16),
+            ws.i32(L.slotpos), ws.i32(L.active), ws.i32(L.nactive), reinterpret_cast<__half *>(ws.base + L.x16),
             reinterpret_cast<__half *>(ws.base + L.h16), ws.f32(L.o),
             reinterpret_cast<TcChunk *>(ws.base + L.chunks), ws.hdr(), sms, g_wait_ns, s)));
         return cuda_status(launch_combine(ws.f32(L.o), idx, w, T, H, E, k, y, sms, s));
@@ -158,9 +158,10 @@ int moe_layer_launch_count(int T, int H, int E, int k, int I) {
     if (device_info(&sms, &dev) != MOE_OK) return 0;
     if (decode_fused_supported(dev, T, H, E, k, I)) return 1;
     const int router = T >= 256 ? 1 : 2;
+    const int permutation = 3;  // count, scan, scatter
     if (prefill_tc_supported(T, H, E, k, I))
-        return router + 1 /* permutation */ + 2 /* fp16 rows, plan */ + 2 /* GEMMs */ + 1;
-    return router + 1 /* permutation */ + 3 /* gate/up, down, combine */;
+        return router + permutation + 2 /* fp16 rows, plan */ + 2 /* GEMMs */ + 1;
+    return router + permutation + 3 /* gate/up, down, combine */;
 }
 
 void moe_debug_set_wait_limit(unsigned long long ns) { g_wait_ns = ns ? ns : 1000000000ull; }
@@ -209,8 +210,8 @@ moe_status moe_permute(const int32_t *idx, int T, int k, int E, int32_t *counts,
     MOE_TRY(device_info(&sms, nullptr));
     Ws W{static_cast<uint8_t *>(ws), L};
     return cuda_status(launch_permute(idx, T, k, E, counts, offs, perm, W.i32(L.active),
-                                      W.i32(L.nactive), W.hdr(),
-                                      static_cast<cudaStream_t>(stream)));
+                                      W.i32(L.nactive), W.i32(L.blockcnt), W.i32(L.slotpos),
+                                      W.hdr(), static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_ffn(const float *x, const int32_t *idx, const float *w, const void *gate,

@@ -49,8 +49,11 @@ static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 // a word left by an earlier call can never carry the current call's tag.
 constexpr size_t kSyncWords = kMaxE;
 
+// Slots per block of the permutation kernels.
+constexpr int kPermSlots = 256;
+
 struct WsLayout {
-    size_t sync, counts, offs, active, nactive, perm, h, o, logits, x16, h16, chunks, xstage, ystage,
+    size_t sync, blockcnt, slotpos, counts, offs, active, nactive, perm, h, o, logits, x16, h16, chunks, xstage, ystage,
         total;
 };
 
@@ -65,6 +68,10 @@ inline WsLayout ws_layout(int T, int H, int E, int k, int I, bool host_staging) 
     L.offs = off;    off = align256(off + sizeof(int32_t) * (E + 1));
     L.active = off;  off = align256(off + sizeof(int32_t) * E);
     L.nactive = off; off = align256(off + sizeof(int32_t) * 4);
+    // permutation: per-block expert counts (then their per-expert prefix) and
+    // each slot's position in the sorted order
+    L.blockcnt = off; off = align256(off + sizeof(int32_t) * ((pairs + kPermSlots - 1) / kPermSlots) * E);
+    L.slotpos = off; off = align256(off + sizeof(int32_t) * pairs);
     L.logits = off;  off = align256(off + sizeof(float) * size_t(T) * E);
     L.perm = off;    off = align256(off + sizeof(int32_t) * pairs);
     L.h = off;       off = align256(off + sizeof(float) * pairs * I);

@@ -15,9 +15,11 @@ cudaError_t init_router();
 cudaError_t launch_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
                           int k, int32_t *idx, float *w, float *logits, cudaStream_t s);
 
+// Three launches (count, scan, scatter); blockcnt holds ceil(T*k / kPermSlots)
+// x E ints of scratch, slotpos receives each slot's sorted position.
 cudaError_t launch_permute(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offs,
-                           int32_t *perm, int32_t *active, int32_t *nactive, WsHeader *hdr,
-                           cudaStream_t s);
+                           int32_t *perm, int32_t *active, int32_t *nactive, int32_t *blockcnt,
+                           int32_t *slotpos, WsHeader *hdr, cudaStream_t s);
 
 cudaError_t init_expert_ffn();
 cudaError_t launch_expert_ffn(const float *x, const int32_t *idx, const float *w,
@@ -34,7 +36,8 @@ cudaError_t init_prefill_tc(int dev);
 bool prefill_tc_supported(int T, int H, int E, int k, int I);
 cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, const uint8_t *up,
                               const uint8_t *down, int T, int H, int E, int k, int I,
-                              const int32_t *offs, const int32_t *perm, const int32_t *active,
+                              const int32_t *offs, const int32_t *perm, const int32_t *slotpos,
+                              const int32_t *active,
                               const int32_t *nactive, __half *x16, __half *h16, float *obuf,
                               TcChunk *chunks, WsHeader *hdr, int num_sms,
                               unsigned long long wait_ns, cudaStream_t s);

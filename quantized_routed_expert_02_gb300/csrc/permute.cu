@@ -7,32 +7,38 @@
 // call whatever the batch size.  The order inside an expert's list is the
 // slot order p = t*k + j, so the grouping is deterministic (no atomics
 // decide positions).
+//
+// Three launches over blocks of kPermSlots consecutive slots:
+//   count    each block's per-expert counts;
+//   scan     per expert, the exclusive prefix of the block counts (in
+//            place), the totals, their exclusive scan (offs) and the list of
+//            active experts;
+//   scatter  each block ranks its slots among equal experts (warp
+//            __match_any_sync ranks, per-warp counts prefix-summed across the
+//            block's warps) and writes every slot to
+//              offs[e] + (slots of e in earlier blocks) + (in earlier warps)
+//                      + (earlier lanes),
+//            recording that position for the slot as well (-1 for a slot
+//            whose expert index is invalid).
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace moeq4k {
 
-// One CTA of 1024 threads.  Slots are processed in chunks of 1024 in slot
-// order; inside a chunk each warp ranks its lanes among equal experts with
-// __match_any_sync, per-warp counts are prefix-summed per expert across the
-// 32 warps, and every slot lands at
-//   offs[e] + (slots of e in earlier chunks) + (in earlier warps) + (earlier lanes).
-__global__ void __launch_bounds__(1024) permute_kernel(const int32_t *__restrict__ idx, int n,
-                                                       int E, int32_t *__restrict__ counts,
-                                                       int32_t *__restrict__ offs,
-                                                       int32_t *__restrict__ perm,
-                                                       int32_t *__restrict__ active,
-                                                       int32_t *__restrict__ nactive,
-                                                       WsHeader *hdr) {
-    __shared__ int32_t cnt[kMaxE];
-    __shared__ int32_t cursor[kMaxE];
-    __shared__ int32_t table[32][kMaxE];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+namespace {
+constexpr int kWarpsPerBlock = kPermSlots / 32;
+}
 
-    for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+__global__ void __launch_bounds__(kPermSlots) permute_count_kernel(const int32_t *__restrict__ idx,
+                                                                   int n, int E,
+                                                                   int32_t *__restrict__ blockcnt,
+                                                                   WsHeader *hdr) {
+    __shared__ int32_t cnt[kMaxE];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
-    for (int p = tid; p < n; p += blockDim.x) {
-        int e = idx[p];
+    const int p = blockIdx.x * kPermSlots + threadIdx.x;
+    if (p < n) {
+        const int e = idx[p];
         if (e >= 0 && e < E) {
             atomicAdd(&cnt[e], 1);
         } else {
@@ -40,80 +46,112 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t *__restrict
         }
     }
     __syncthreads();
-    // exclusive scan of cnt over E <= 256 entries: one warp
-    if (warp == 0) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[size_t(blockIdx.x) * E + e] = cnt[e];
+}
+
+// One CTA of 1024 threads.  Warp w scans the block counts of experts w,
+// w+32, ... (lanes take 32 consecutive blocks at a time, a shuffle scan with
+// a running carry), then warp 0 scans the expert totals.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int nblocks, int E,
+                                                            int32_t *__restrict__ blockcnt,
+                                                            int32_t *__restrict__ counts,
+                                                            int32_t *__restrict__ offs,
+                                                            int32_t *__restrict__ active,
+                                                            int32_t *__restrict__ nactive) {
+    __shared__ int32_t tot[kMaxE];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int e = warp; e < E; e += 32) {
         int carry = 0;
+        for (int b0 = 0; b0 < nblocks; b0 += 32) {
+            const int b = b0 + lane;
+            const int c = b < nblocks ? blockcnt[size_t(b) * E + e] : 0;
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            if (b < nblocks) blockcnt[size_t(b) * E + e] = carry + incl - c;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) tot[e] = carry;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0, na = 0;
         for (int base = 0; base < E; base += 32) {
-            int e = base + lane;
-            int v = (e < E) ? cnt[e] : 0;
+            const int ee = base + lane;
+            const int v = (ee < E) ? tot[ee] : 0;
             int incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                int u = __shfl_up_sync(0xffffffffu, incl, o);
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += u;
             }
-            if (e < E) {
-                cursor[e] = carry + incl - v;
-                offs[e] = carry + incl - v;
-                counts[e] = v;
+            if (ee < E) {
+                offs[ee] = carry + incl - v;
+                counts[ee] = v;
             }
             carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) offs[E] = carry;
-        // active experts in ascending order
-        int na = 0;
-        for (int base = 0; base < E; base += 32) {
-            int e = base + lane;
-            bool on = (e < E) && cnt[e] > 0;
-            unsigned m = __ballot_sync(0xffffffffu, on);
-            if (on) active[na + __popc(m & ((1u << lane) - 1u))] = e;
+            // active experts in ascending order
+            const bool on = (ee < E) && v > 0;
+            const unsigned m = __ballot_sync(0xffffffffu, on);
+            if (on) active[na + __popc(m & ((1u << lane) - 1u))] = ee;
             na += __popc(m);
         }
-        if (lane == 0) *nactive = na;
+        if (lane == 0) {
+            offs[E] = carry;
+            *nactive = na;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kPermSlots) permute_scatter_kernel(
+    const int32_t *__restrict__ idx, int n, int E, const int32_t *__restrict__ blockcnt,
+    const int32_t *__restrict__ offs, int32_t *__restrict__ perm, int32_t *__restrict__ slotpos,
+    WsHeader *hdr) {
+    __shared__ int32_t table[kWarpsPerBlock][kMaxE];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int p = blockIdx.x * kPermSlots + tid;
+    const int e = (p < n) ? idx[p] : -1;
+    const bool ok = (e >= 0 && e < E);
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    for (int i = tid; i < kWarpsPerBlock * E; i += blockDim.x) table[i / E][i % E] = 0;
+    __syncthreads();
+    if (ok && rank == 0) table[warp][e] = __popc(peers);
+    __syncthreads();
+    // per-expert exclusive prefix across the block's warps, plus the block's base
+    for (int ee = tid; ee < E; ee += blockDim.x) {
+        int run = offs[ee] + blockcnt[size_t(blockIdx.x) * E + ee];
+        for (int w = 0; w < kWarpsPerBlock; ++w) {
+            const int c = table[w][ee];
+            table[w][ee] = run;
+            run += c;
+        }
     }
     __syncthreads();
-
-    for (int base = 0; base < n; base += blockDim.x) {
-        const int p = base + tid;
-        int e = (p < n) ? idx[p] : -1;
-        bool ok = (e >= 0 && e < E);
-        int key = ok ? e : -1;
-        unsigned peers = __match_any_sync(0xffffffffu, key);
-        int rank = __popc(peers & ((1u << lane) - 1u));
-        bool leader = ok && (rank == 0);
-        for (int i = tid; i < 32 * E; i += blockDim.x) table[i / E][i % E] = 0;
-        __syncthreads();
-        if (leader) table[warp][e] = __popc(peers);
-        __syncthreads();
-        // per-expert exclusive prefix across warps; cnt[] now holds chunk totals
-        for (int ee = tid; ee < E; ee += blockDim.x) {
-            int run = 0;
-            for (int w = 0; w < 32; ++w) {
-                int c = table[w][ee];
-                table[w][ee] = run;
-                run += c;
-            }
-            cnt[ee] = run;
+    if (ok) {
+        const int pos = table[warp][e] + rank;
+        if (pos >= 0 && pos < n) {
+            perm[pos] = p;
+            slotpos[p] = pos;
+        } else {
+            record_status(hdr, MOE_ERR_INTERNAL, 400000000 + (pos & 0xffffff));
         }
-        __syncthreads();
-        if (ok) {
-            const int pos = cursor[e] + table[warp][e] + rank;
-            if (pos >= 0 && pos < n) {
-                perm[pos] = p;
-            } else {
-                record_status(hdr, MOE_ERR_INTERNAL, 400000000 + (pos & 0xffffff));
-            }
-        }
-        __syncthreads();
-        for (int ee = tid; ee < E; ee += blockDim.x) cursor[ee] += cnt[ee];
-        __syncthreads();
+    } else if (p < n) {
+        slotpos[p] = -1;  // an invalid expert index: the slot has no sorted row
     }
 }
 
 cudaError_t launch_permute(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offs,
-                           int32_t *perm, int32_t *active, int32_t *nactive, WsHeader *hdr,
-                           cudaStream_t s) {
-    permute_kernel<<<1, 1024, 0, s>>>(idx, T * k, E, counts, offs, perm, active, nactive, hdr);
+                           int32_t *perm, int32_t *active, int32_t *nactive, int32_t *blockcnt,
+                           int32_t *slotpos, WsHeader *hdr, cudaStream_t s) {
+    const int n = T * k;
+    const int nb = (n + kPermSlots - 1) / kPermSlots;
+    permute_count_kernel<<<nb, kPermSlots, 0, s>>>(idx, n, E, blockcnt, hdr);
+    permute_scan_kernel<<<1, 1024, 0, s>>>(nb, E, blockcnt, counts, offs, active, nactive);
+    permute_scatter_kernel<<<nb, kPermSlots, 0, s>>>(idx, n, E, blockcnt, offs, perm, slotpos, hdr);
     return cudaGetLastError();
 }
 

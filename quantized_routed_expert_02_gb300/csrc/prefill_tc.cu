@@ -399,47 +399,65 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     if (warp == 0) tc::tmem_dealloc(taddr, tcols);
 }
 
-// Activations in expert-sorted order: row i of xs = x[perm[i] / k] as fp16,
-// each group of four elements in kperm order.
-__global__ void gather_half_kernel(const float *__restrict__ x, const int32_t *__restrict__ perm,
-                                   const int32_t *__restrict__ offs, int E, int k, int H,
-                                   __half *__restrict__ xs) {
-    const int nrows = offs[E];
+// Activations in expert-sorted order: row slotpos[t*k + j] of xs = x[t] as
+// fp16 for every slot j of token t, each group of four elements in kperm
+// order.  Thread per (token, 4 elements): x is read once, written k times.
+__global__ void gather_half_kernel(const float *__restrict__ x, const int32_t *__restrict__ slotpos,
+                                   int T, int k, int H, __half *__restrict__ xs) {
     const int per_row = H / 4;
-    const size_t total = size_t(nrows) * per_row;
+    const size_t total = size_t(T) * per_row;
     for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total;
          i += size_t(gridDim.x) * blockDim.x) {
-        const int r = int(i / per_row), c = int(i % per_row);
-        const int t = perm[r] / k;
+        const int t = int(i / per_row), c = int(i % per_row);
         const float4 v = reinterpret_cast<const float4 *>(x + size_t(t) * H)[c];
         // kperm order within each group of four: x0, x2, x1, x3
         __half2 a = __floats2half2_rn(v.x, v.z), b = __floats2half2_rn(v.y, v.w);
         uint2 o;
         o.x = *reinterpret_cast<uint32_t *>(&a);
         o.y = *reinterpret_cast<uint32_t *>(&b);
-        reinterpret_cast<uint2 *>(xs + size_t(r) * H)[c] = o;
+        for (int j = 0; j < k; ++j) {
+            const int pos = slotpos[t * k + j];
+            if (pos < 0) continue;  // invalid expert index: no sorted row
+            reinterpret_cast<uint2 *>(xs + size_t(pos) * H)[c] = o;
+        }
     }
 }
 
-// Chunks of <= 256 slots per active expert, and the work counters reset.
+// Chunks of <= kBN slots per active expert, in active order, and the work
+// counters reset.  One warp: lanes take active experts in turns of 32, a
+// warp scan gives each expert's first chunk.
 __global__ void plan_kernel(const int32_t *__restrict__ offs, const int32_t *__restrict__ active,
                             const int32_t *__restrict__ nactive, TcChunk *chunks, WsHeader *hdr) {
-    if (threadIdx.x != 0) return;
-    int nc = 0;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x >= 32) return;
     const int na = *nactive;
-    for (int a = 0; a < na; ++a) {
-        const int e = active[a];
-        const int n = offs[e + 1] - offs[e];
-        for (int t = 0; t < n; t += kBN) {
-            chunks[nc].e = e;
-            chunks[nc].tok_off = t;
-            chunks[nc].tok_cnt = min(kBN, n - t);
-            ++nc;
+    int nc = 0;
+    for (int base = 0; base < na; base += 32) {
+        const int a = base + lane;
+        const int e = a < na ? active[a] : 0;
+        const int n = a < na ? offs[e + 1] - offs[e] : 0;
+        const int mine = (n + kBN - 1) / kBN;
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
         }
+        for (int c = 0; c < mine; ++c) {
+            TcChunk ch;
+            ch.e = e;
+            ch.tok_off = c * kBN;
+            ch.tok_cnt = min(kBN, n - c * kBN);
+            ch.pad = 0;
+            chunks[nc + incl - mine + c] = ch;
+        }
+        nc += __shfl_sync(0xffffffffu, incl, 31);
     }
-    hdr->tc_chunks = nc;
-    hdr->tc_work[0] = 0;
-    hdr->tc_work[1] = 0;
+    if (lane == 0) {
+        hdr->tc_chunks = nc;
+        hdr->tc_work[0] = 0;
+        hdr->tc_work[1] = 0;
+    }
 }
 
 }  // namespace ptc
@@ -507,12 +525,12 @@ bool prefill_tc_supported(int T, int H, int E, int k, int I) {
 
 cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, const uint8_t *up,
                               const uint8_t *down, int T, int H, int E, int k, int I,
-                              const int32_t *offs, const int32_t *perm, const int32_t *active,
-                              const int32_t *nactive, __half *x16, __half *h16, float *obuf,
-                              TcChunk *chunks, WsHeader *hdr, int num_sms,
-                              unsigned long long wait_ns, cudaStream_t s) {
+                              const int32_t *offs, const int32_t *perm, const int32_t *slotpos,
+                              const int32_t *active, const int32_t *nactive, __half *x16,
+                              __half *h16, float *obuf, TcChunk *chunks, WsHeader *hdr,
+                              int num_sms, unsigned long long wait_ns, cudaStream_t s) {
     using namespace ptc;
-    gather_half_kernel<<<num_sms * 8, 256, 0, s>>>(x, perm, offs, E, k, H, x16);
+    gather_half_kernel<<<num_sms * 8, 256, 0, s>>>(x, slotpos, T, k, H, x16);
     plan_kernel<<<1, 32, 0, s>>>(offs, active, nactive, chunks, hdr);
     const int rows = T * k;
 

@@ -24,7 +24,7 @@ SHAPES = [
 def test_prefill_shapes(m, T, H, E, k, I, std, zipf):
     shape = synth.custom_shape(T, H, E, k, I, wr_std=std, zipf_bias=zipf,
                                cfg_id=70 + (T + H + E + k + I) % 20)
-    assert m.moe_layer_launch_count(T, H, E, k, I) == (7 if T >= 256 else 8)   # tensor-core path
+    assert m.moe_layer_launch_count(T, H, E, k, I) == (9 if T >= 256 else 10)   # tensor-core path
     sample = tuple(range(0, T, max(1, T // 48))) + (T - 1,)
     case = layer_case(shape, 0, sample)
     idx, w, y, _, _ = run_layer(m, case)
