@@ -1,6 +1,7 @@
 // Thin wrappers over the sm_90+/sm_100 asynchronous-copy PTX the decode
 // kernel uses: mbarriers, 1-D bulk copies (cp.async.bulk, the TMA engine's
-// untiled mode), L2 cache policies and the global timer for bounded waits.
+// untiled mode), cp.async, release/acquire counters and the global timer for
+// bounded waits.
 #pragma once
 
 #include <stdint.h>

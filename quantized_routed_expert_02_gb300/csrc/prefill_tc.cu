@@ -13,19 +13,24 @@
 // is written in that order too, so every activation tile is one contiguous
 // block of rows.
 //
-// One persistent CTA per SM takes work items (expert chunk of <= 256 slots,
-// 128-row weight tile) from an atomic counter.  12 warps:
-//   thread 32   stages the raw Q4_K bytes of the tile one block column at a
-//               time (128 rows x 144 B) with a 2-D TMA copy
-//               (cp.async.bulk.tensor) into a ring of raw stages;
-//   warps 4-11  dequantise them, 64 K per stage, into fp16 K-major tiles with
-//               the 128-byte swizzle (generic stores, then a proxy fence);
-//   thread 64   loads the chunk's activation tile (256 rows x 64 K, fp16,
-//               rows in expert-sorted order) with one 2-D TMA copy that
-//               applies the 128-byte swizzle;
+// One persistent CTA per SM takes work items (expert chunk of <= 256 slots x
+// 128 rows each of gate and up, or 256 rows of down: two A operands that
+// share every activation tile) from an atomic counter.  12 warps:
+//   thread 32   stages the raw Q4_K bytes of each K stage (64 weights per
+//               row: the 16-byte block head and the 32 code bytes) for the
+//               tile's 128 rows with two 2-D TMA copies per matrix, into a
+//               ring of raw slots;
+//   warps 4-11  dequantise them into fp16 K-major tiles with the 128-byte
+//               swizzle (generic stores, then a proxy fence), into a 2-slot
+//               ring of weight tiles;
+//   thread 64   loads the chunk's activation tile (its sorted rows rounded
+//               up to 32, x 64 K, fp16) with 2-D TMA copies of 32 rows that
+//               apply the 128-byte swizzle, into a ring as deep as shared
+//               memory allows (3 slots): these come from L2 or HBM and need
+//               the most latency cover;
 //   thread 0    issues tcgen05.mma (fp16 x fp16 -> fp32 in tensor memory)
-//               when a stage is full and commits its completion to the
-//               stage's "empty" mbarrier;
+//               once a stage's weight and activation tiles are both in, and
+//               commits its completion to both rings' "empty" mbarriers;
 //   all warps   read the accumulators back (tcgen05.ld) for the epilogue
 //               once the item's MMAs are complete, each warp a third of the
 //               columns of its TMEM lane quadrant.
@@ -49,34 +54,37 @@ constexpr int kBN = 256;   // tokens per tile (max)
 constexpr int kBK = 64;    // K per stage
 constexpr int kTileA = kBM * kBK * 2;
 constexpr int kTileB = kBN * kBK * 2;
+constexpr int kBoxRows = 32;                   // activation rows per TMA box
+constexpr int kBoxB = kBoxRows * kBK * 2;
 constexpr int kHead = 2048;  // barriers, item info, token list
 constexpr int kDeq = 256;      // warps 4-11
-constexpr int kMaxStages = 6;
+constexpr int kMaxSlots = 8;   // per ring
+constexpr int kRawHead = kBM * 16;               // block heads of a tile's rows
+constexpr int kRawMat = kBM * (16 + 32);         // one matrix's raw bytes of a stage
 
 struct Params {
-    CUtensorMap map0, map1;   // raw Q4_K bytes of A0 / A1 as [E*rows][nsb*144] uint8
-    CUtensorMap mapB;         // activations [T*k sorted rows][K] fp16, 128-byte swizzle
-    int mode;                 // 0: gate/up + SwiGLU -> h16; 1: down -> o
-    const uint8_t *A0, *A1;   // gate/up (mode 0) or down (mode 1) blobs
-    size_t mat_bytes;         // bytes of one expert's matrix
-    int nsb;                  // Q4_K blocks per row (K / 256)
-    int K;                    // reduction length
-    int row_tiles;            // weight rows per expert / 128
+    CUtensorMap head0, codes0;  // raw Q4_K bytes of A0 as [E*rows][row bytes] uint8:
+    CUtensorMap head1, codes1;  //   boxes of 16 B (block head) and 32 B (codes) x 128 rows
+    CUtensorMap mapB;           // activations [T*k sorted rows][K] fp16, 128-byte swizzle
+    int mode;                   // 0: gate/up + SwiGLU -> h16; 1: down -> o
+    int K;                      // reduction length
+    int row_tiles;              // weight rows per expert / item_rows
+    int item_rows;              // weight rows per item: 128 (gate/up: 128 of each) or 256
+    int y_off1;                 // row offset of the second A operand: 0 (up) or 128 (down)
 
     const int32_t *offs, *perm;
     const TcChunk *chunks;
-    WsHeader *hdr;            // work counters, chunk count, status
-    __half *h16;              // mode 0 output [T*k sorted rows][I]
-    float *o;                 // mode 1 output [T*k][H]
+    WsHeader *hdr;              // work counters, chunk count, status
+    __half *h16;                // mode 0 output [T*k sorted rows][I]
+    float *o;                   // mode 1 output [T*k][H]
     int I, H;
-    int rows_per_expert;      // I (mode 0) or H (mode 1)
-    int nstages, stage_bytes; // fp16 operand ring
-    int nraw, raw_bytes;      // raw Q4_K ring (one block column of the tile per stage)
-    int raw_off;              // byte offset of the raw ring
+    int rows_per_expert;        // I (mode 0) or H (mode 1)
+    int nr, r_off;              // raw ring: slots, byte offset (slot = nmat * kRawMat bytes)
+    int na, a_off;              // weight-tile ring: slots, byte offset (slot = nmat * kTileA)
+    int nb, b_off;              // activation-tile ring: slots, byte offset (slot = kTileB)
     unsigned long long wait_ns;
 };
 
-constexpr int kRawTile = kBM * kBlockBytes;  // 128 rows x 144 B
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                             uint64_t *bar) {
@@ -154,14 +162,13 @@ struct RawStage {
     uint4 head, q0, q1;  // block head and the 32 code bytes of this stage's 64 weights
 };
 
-// The 48 bytes of K-stage s (head + codes) of one row of a raw block tile.
-__device__ __forceinline__ RawStage raw_from_smem(const uint8_t *blk, int s) {
-    const int c = s & 3;
-    RawStage r;
-    r.head = *reinterpret_cast<const uint4 *>(blk);
-    r.q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
-    r.q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
-    return r;
+// Row r of a matrix's raw stage: its 16-byte block head and 32 code bytes.
+__device__ __forceinline__ RawStage raw_from_smem(const uint8_t *mat, int r) {
+    RawStage v;
+    v.head = *reinterpret_cast<const uint4 *>(mat + 16 * r);
+    v.q0 = *reinterpret_cast<const uint4 *>(mat + kRawHead + 32 * r);
+    v.q1 = *reinterpret_cast<const uint4 *>(mat + kRawHead + 32 * r + 16);
+    return v;
 }
 
 // Write `nchunks` 16-byte chunks (weights 8j..8j+7 for j in [j0, j0+nchunks),
@@ -189,31 +196,40 @@ __device__ __forceinline__ void store_row(uint8_t *tile, int r, const RawStage &
 
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *empty = full + kMaxStages;
-    uint64_t *rfull = empty + kMaxStages;
-    uint64_t *rempty = rfull + kMaxStages;
-    uint64_t *done = rempty + kMaxStages;
+    uint64_t *rfull = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *rempty = rfull + kMaxSlots;
+    uint64_t *afull = rempty + kMaxSlots;
+    uint64_t *aempty = afull + kMaxSlots;
+    uint64_t *bfull = aempty + kMaxSlots;
+    uint64_t *bempty = bfull + kMaxSlots;
+    uint64_t *done = bempty + kMaxSlots;
     uint64_t *drain = done + 1;
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(drain + 1);
     int *info = reinterpret_cast<int *>(tmem_ptr + 4);   // [0] item, [1] abort, [2] accumulators ready
     int *toks = reinterpret_cast<int *>(smem + 1024);    // slot ids of the chunk (<= 256)
-    uint8_t *stages = smem + kHead;
+    uint8_t *rring = smem + p.r_off;
+    uint8_t *aring = smem + p.a_off;
+    uint8_t *bring = smem + p.b_off;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int NS = p.nstages;
+    const int NR = p.nr, NA = p.na, NB = p.nb;
+    constexpr int nmat = 2;  // two A operands per item: gate and up, or two 128-row halves
     const int S = p.K / kBK;  // stages per item
     const uint64_t deadline = global_timer_ns() + p.wait_ns;
-    const uint32_t tcols = p.mode == 0 ? 512u : 256u;
+    const uint32_t tcols = 512u;  // two 128 x 256 fp32 accumulators
 
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(full + s, kDeq / 32 + 1);   // one arrival per dequant warp + the TMA
-            mbar_init(empty + s, 1);
+        for (int i = 0; i < NR; ++i) {
+            mbar_init(rfull + i, 1);           // the TMA thread's arrival + its bytes
+            mbar_init(rempty + i, kDeq / 32);  // one arrival per dequant warp
         }
-        for (int s = 0; s < p.nraw; ++s) {
-            mbar_init(rfull + s, 1);
-            mbar_init(rempty + s, kDeq / 32);
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(afull + i, kDeq / 32);
+            mbar_init(aempty + i, 1);          // MMA completion
+        }
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(bfull + i, 1);
+            mbar_init(bempty + i, 1);
         }
         mbar_init(done, 1);
         mbar_init(drain, 1);
@@ -227,10 +243,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint32_t taddr = *tmem_ptr;
     const int total = p.hdr->tc_chunks * p.row_tiles;
 
-    uint8_t *raw = smem + p.raw_off;
-    const int NR = p.nraw;
-    const int nsb = p.nsb;  // raw block-column stages per item
-    uint32_t grs = 0;    // raw stages processed by this CTA
     uint32_t gs = 0;     // stages processed by this CTA (same count in every role)
     uint32_t items = 0;  // items processed by this CTA
     while (true) {
@@ -246,97 +258,92 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         __syncthreads();
 
         if (warp >= 4) {
-            // ---- dequantise weight rows (raw block tiles in shared memory) into the A tile(s)
+            // ---- dequantise weight rows (raw stage in shared memory) into the A tile(s)
             const int dq = tid - 128;
-            int m, r, j0, nch;
-            if (p.mode == 0) {
-                m = dq >> 7;       // 0 gate, 1 up
-                r = dq & 127;
-                j0 = 0;
-                nch = 8;
-            } else {
-                m = 0;
-                r = dq >> 1;
-                j0 = (dq & 1) * 4;  // low or high nibbles
-                nch = 4;
-            }
+            const int m = dq >> 7;  // A operand: gate / up, or the first / second 128 rows
+            const int r = dq & 127, j0 = 0, nch = 8;
             for (int s = 0; s < S; ++s) {
-                const uint32_t g = gs + s, slot = g % NS;
-                const uint32_t rg = grs + (s >> 2), rslot = rg % NR;
-                if ((s & 3) == 0 && !wait_bar(rfull + rslot, (rg / NR) & 1, deadline, p.hdr, 16)) {
+                const uint32_t g = gs + s, rs = g % NR, as = g % NA;
+                if (!wait_bar(rfull + rs, (g / NR) & 1, deadline, p.hdr, 16)) {
                     info[1] = 1;
                     break;
                 }
-                const RawStage cur = raw_from_smem(
-                    raw + size_t(rslot) * p.raw_bytes + m * kRawTile + r * kBlockBytes, s);
-                if ((s & 3) == 3) {  // raw tile fully read by this warp
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(rempty + rslot);
-                }
-                if (g >= uint32_t(NS) &&
-                    !wait_bar(empty + slot, ((g / NS) - 1) & 1, deadline, p.hdr, 11)) {
-                    info[1] = 1;
-                    break;
-                }
-                uint8_t *tile = stages + size_t(slot) * p.stage_bytes + m * kTileA;
-                store_row(tile, r, cur, s, j0, nch);
+                const RawStage cur = raw_from_smem(rring + size_t(rs) * nmat * kRawMat + m * kRawMat, r);
+                // The TMA that refills this slot writes through the async proxy:
+                // without a proxy fence after the reads, a refill could land
+                // before reads still in flight are performed.
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(full + slot);
+                if (lane == 0) mbar_arrive(rempty + rs);
+                if (g >= uint32_t(NA) &&
+                    !wait_bar(aempty + as, ((g / NA) - 1) & 1, deadline, p.hdr, 11)) {
+                    info[1] = 1;
+                    break;
+                }
+                store_row(aring + size_t(as) * nmat * kTileA + m * kTileA, r, cur, s, j0, nch);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(afull + as);
             }
         } else if (tid == 0) {
             // ---- MMA issue
             const uint32_t idesc = tc::idesc_f16_f32(kBM, nmma);
             for (int s = 0; s < S; ++s) {
-                const uint32_t g = gs + s, slot = g % NS;
-                if (!wait_bar(full + slot, (g / NS) & 1, deadline, p.hdr, 13)) {
+                const uint32_t g = gs + s, as = g % NA, bs = g % NB;
+                if (!wait_bar(afull + as, (g / NA) & 1, deadline, p.hdr, 13) ||
+                    !wait_bar(bfull + bs, (g / NB) & 1, deadline, p.hdr, 18)) {
                     info[1] = 1;
                     break;
                 }
                 tc::fence_after_sync();
-                uint8_t *st = stages + size_t(slot) * p.stage_bytes;
-                const uint32_t a0 = smem_addr(st), a1 = a0 + kTileA;
-                const uint32_t b = a0 + (p.mode == 0 ? 2 : 1) * kTileA;
+                const uint32_t a0 = smem_addr(aring + size_t(as) * nmat * kTileA), a1 = a0 + kTileA;
+                const uint32_t b = smem_addr(bring + size_t(bs) * kTileB);
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
                     const uint64_t bd = tc::smem_desc_sw128(b + 32 * kk);
                     const bool acc = s > 0 || kk > 0;
                     tc::mma_f16(taddr, tc::smem_desc_sw128(a0 + 32 * kk), bd, idesc, acc);
-                    if (p.mode == 0) tc::mma_f16(taddr + 256, tc::smem_desc_sw128(a1 + 32 * kk), bd, idesc, acc);
+                    tc::mma_f16(taddr + 256, tc::smem_desc_sw128(a1 + 32 * kk), bd, idesc, acc);
                 }
-                tc::commit_arrive(empty + slot);
+                tc::commit_arrive(aempty + as);
+                tc::commit_arrive(bempty + bs);
             }
             tc::commit_arrive(done);
         } else if (tid == 64) {
-            // ---- activation tile of each stage by TMA (256 sorted rows x 64 K)
+            // ---- activation tile of each stage by TMA: the chunk's sorted rows
+            // (rounded up to 32) x 64 K, in boxes of 32 rows
             const int row0 = p.offs[ch.e] + ch.tok_off;
-            for (int s2 = 0; s2 < S; ++s2) {
-                const uint32_t g = gs + s2, slot = g % NS;
-                if (g >= uint32_t(NS) &&
-                    !wait_bar(empty + slot, ((g / NS) - 1) & 1, deadline, p.hdr, 12)) {
+            const int nbox = (nmma + kBoxRows - 1) / kBoxRows;
+            for (int s = 0; s < S; ++s) {
+                const uint32_t g = gs + s, bs = g % NB;
+                if (g >= uint32_t(NB) &&
+                    !wait_bar(bempty + bs, ((g / NB) - 1) & 1, deadline, p.hdr, 12)) {
                     info[1] = 1;
                     break;
                 }
-                uint8_t *tile = stages + size_t(slot) * p.stage_bytes + (p.mode == 0 ? 2 : 1) * kTileA;
-                mbar_arrive_expect_tx(full + slot, kTileB);
-                tma_load_2d(tile, &p.mapB, s2 * kBK, row0, full + slot);
+                mbar_arrive_expect_tx(bfull + bs, nbox * kBoxB);
+                for (int i = 0; i < nbox; ++i)
+                    tma_load_2d(bring + size_t(bs) * kTileB + i * kBoxB, &p.mapB, s * kBK,
+                                row0 + i * kBoxRows, bfull + bs);
             }
         } else if (tid == 32) {
-            // ---- raw Q4_K block tiles by TMA, all block columns of the item (its own
-            // thread: it may wait on the raw ring while loaders and MMA make progress)
-                for (int b = 0; b < nsb; ++b) {
-                    const uint32_t rg = grs + b, rslot = rg % NR;
-                    if (rg >= uint32_t(NR) &&
-                        !wait_bar(rempty + rslot, ((rg / NR) - 1) & 1, deadline, p.hdr, 17)) {
-                        info[1] = 1;
-                        break;
-                    }
-                    uint8_t *dst = raw + size_t(rslot) * p.raw_bytes;
-                    const int y = ch.e * p.rows_per_expert + rt * kBM;
-                    mbar_arrive_expect_tx(rfull + rslot, p.mode == 0 ? 2 * kRawTile : kRawTile);
-                    tma_load_2d(dst, &p.map0, b * kBlockBytes, y, rfull + rslot);
-                    if (p.mode == 0) tma_load_2d(dst + kRawTile, &p.map1, b * kBlockBytes, y, rfull + rslot);
+            // ---- raw bytes of each stage by TMA: block head + the stage's 32 code bytes
+            const int y = ch.e * p.rows_per_expert + rt * p.item_rows;
+            for (int s = 0; s < S; ++s) {
+                const uint32_t g = gs + s, rs = g % NR;
+                if (g >= uint32_t(NR) &&
+                    !wait_bar(rempty + rs, ((g / NR) - 1) & 1, deadline, p.hdr, 17)) {
+                    info[1] = 1;
+                    break;
                 }
+                uint8_t *dst = rring + size_t(rs) * nmat * kRawMat;
+                const int xh = (s >> 2) * kBlockBytes, xq = xh + 16 + 32 * (s & 3);
+                mbar_arrive_expect_tx(rfull + rs, nmat * kRawMat);
+                tma_load_2d(dst, &p.head0, xh, y, rfull + rs);
+                tma_load_2d(dst + kRawHead, &p.codes0, xq, y, rfull + rs);
+                tma_load_2d(dst + kRawMat, &p.head1, xh, y + p.y_off1, rfull + rs);
+                tma_load_2d(dst + kRawMat + kRawHead, &p.codes1, xq, y + p.y_off1, rfull + rs);
+            }
         }
 
         // ---- epilogue, by all 12 warps: warp w reads the TMEM lanes of
@@ -350,17 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const int q = warp & 3, part = warp >> 2;
             const int units = nmma >> 3;
             const int u_lo = units * part / 3, u_hi = units * (part + 1) / 3;
-            const int row = rt * kBM + q * 32 + lane;
+            const int row = rt * p.item_rows + q * 32 + lane;
             const int prow = kperm(row);  // h is the down GEMM's K: stored in kperm order
             const int pos0 = p.offs[ch.e] + ch.tok_off;  // sorted row of column 0
             const uint32_t lanebase = taddr + (uint32_t(q * 32) << 16);
             for (int uu = u_lo; uu < u_hi; ++uu) {
                 const int n0 = 8 * uu;
-                float g[8];
+                float g[8], u[8];
                 tc::tmem_ld8(lanebase + n0, g);
+                tc::tmem_ld8(lanebase + 256 + n0, u);
                 if (p.mode == 0) {
-                    float u[8];
-                    tc::tmem_ld8(lanebase + 256 + n0, u);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int n = n0 + j;
@@ -376,14 +382,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int n = n0 + j;
-                        if (n < ntok) p.o[size_t(toks[n]) * p.H + row] = g[j];
+                        if (n < ntok) {
+                            float *orow = p.o + size_t(toks[n]) * p.H;
+                            orow[row] = g[j];
+                            orow[row + kBM] = u[j];
+                        }
                     }
                 }
             }
         }
         tc::fence_before_sync();
         gs += S;
-        grs += nsb;
         ++items;
         __syncthreads();
     }
@@ -472,23 +481,29 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 EncodeTiledFn g_encode = nullptr;
 
 // Raw bytes of one matrix family as a 2-D uint8 tensor: E*rows rows of
-// nsb*144 bytes, box = one block column of 128 rows.
-bool encode_q4k_map(CUtensorMap *map, const void *base, int E, int rows, int nsb) {
+// nsb*144 bytes; box = `box_bytes` (16: block head, 32: codes of one stage)
+// x 128 rows.  Every x coordinate used (block start, +16 + 32c) is a
+// multiple of 16 bytes.
+bool encode_raw_map(CUtensorMap *map, const void *base, int E, int rows, int nsb, int box_bytes) {
     const cuuint64_t dims[2] = {cuuint64_t(nsb) * kBlockBytes, cuuint64_t(E) * rows};
     const cuuint64_t strides[1] = {cuuint64_t(nsb) * kBlockBytes};
-    const cuuint32_t box[2] = {cuuint32_t(kBlockBytes), cuuint32_t(ptc::kBM)};
+    const cuuint32_t box[2] = {cuuint32_t(box_bytes), cuuint32_t(ptc::kBM)};
     const cuuint32_t estr[2] = {1, 1};
     return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-// Sorted activation rows as a 2-D fp16 tensor [rows][K]; box = 256 rows x 64
-// K, stored with the 128-byte swizzle the MMA descriptors expect.
+bool encode_raw_maps(CUtensorMap *head, CUtensorMap *codes, const void *base, int E, int rows, int nsb) {
+    return encode_raw_map(head, base, E, rows, nsb, 16) && encode_raw_map(codes, base, E, rows, nsb, 32);
+}
+// Sorted activation rows as a 2-D fp16 tensor [rows][K]; box = 32 rows x 64
+// K, stored with the 128-byte swizzle the MMA descriptors expect (the
+// swizzle pattern repeats every 8 rows, so boxes stack at 4 KB steps).
 bool encode_act_map(CUtensorMap *map, const void *base, int rows, int K) {
     const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
     const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
-    const cuuint32_t box[2] = {cuuint32_t(ptc::kBK), cuuint32_t(ptc::kBN)};
+    const cuuint32_t box[2] = {cuuint32_t(ptc::kBK), cuuint32_t(ptc::kBoxRows)};
     const cuuint32_t estr[2] = {1, 1};
     return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -520,7 +535,7 @@ cudaError_t init_prefill_tc(int dev) {
 constexpr int kMinTcSlots = 256;
 
 bool prefill_tc_supported(int T, int H, int E, int k, int I) {
-    return T * k >= kMinTcSlots && I % ptc::kBM == 0 && H % ptc::kBM == 0;
+    return T * k >= kMinTcSlots && I % ptc::kBM == 0 && H % (2 * ptc::kBM) == 0;
 }
 
 cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, const uint8_t *up,
@@ -546,46 +561,46 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     p.wait_ns = wait_ns;
     const int optin = g_tc_smem_optin[dev];
 
+    // Shared memory: header, raw ring, weight-tile ring (1024-aligned), then
+    // as many activation slots as fit.
+    auto rings = [&](int nmat, int nr) -> size_t {
+        p.nr = nr;
+        p.r_off = kHead;
+        p.na = 2;
+        p.a_off = (kHead + nr * nmat * kRawMat + 1023) & ~1023;
+        p.b_off = p.a_off + p.na * nmat * kTileA;
+        p.nb = std::min(kMaxSlots, (optin - p.b_off) / kTileB);
+        return p.nb < 2 ? 0 : size_t(p.b_off) + size_t(p.nb) * kTileB;
+    };
+
     // gate/up: A = gate and up rows (I per expert), B = x16 rows (slot p -> token p / k)
     p.mode = 0;
-    p.A0 = gate;
-    p.A1 = up;
-    p.mat_bytes = size_t(I) * (H / kQK) * kBlockBytes;
-    p.nsb = H / kQK;
     p.K = H;
     p.row_tiles = I / kBM;
+    p.item_rows = kBM;
+    p.y_off1 = 0;
     p.rows_per_expert = I;
     if (!encode_act_map(&p.mapB, x16, rows, H)) return cudaErrorInvalidValue;
-    p.stage_bytes = 2 * kTileA + kTileB;
-    p.raw_bytes = 2 * kRawTile;
-    p.nstages = 2;
-    p.nraw = 2;
-    p.raw_off = kHead + p.nstages * p.stage_bytes;
-    if (!encode_q4k_map(&p.map0, gate, E, I, H / kQK) || !encode_q4k_map(&p.map1, up, E, I, H / kQK))
+    if (!encode_raw_maps(&p.head0, &p.codes0, gate, E, I, H / kQK) ||
+        !encode_raw_maps(&p.head1, &p.codes1, up, E, I, H / kQK))
         return cudaErrorInvalidValue;
-    size_t smem = size_t(p.raw_off) + size_t(p.nraw) * p.raw_bytes;
-    if (smem > size_t(optin)) return cudaErrorInvalidValue;
+    size_t smem = rings(2, 4);
+    if (smem == 0) return cudaErrorInvalidValue;
     grouped_gemm_kernel<<<num_sms, kThreads, smem, s>>>(p);
 
     // down: A = down rows (H per expert), B = h16 rows (slot p)
     p.mode = 1;
-    p.A0 = down;
-    p.A1 = down;
-    p.mat_bytes = size_t(H) * (I / kQK) * kBlockBytes;
-    p.nsb = I / kQK;
     p.K = I;
-    p.row_tiles = H / kBM;
+    p.row_tiles = H / (2 * kBM);
+    p.item_rows = 2 * kBM;
+    p.y_off1 = kBM;
     p.rows_per_expert = H;
     if (!encode_act_map(&p.mapB, h16, rows, I)) return cudaErrorInvalidValue;
-    p.stage_bytes = kTileA + kTileB;
-    p.raw_bytes = kRawTile;
-    p.nstages = 3;
-    p.nraw = 3;
-    p.raw_off = kHead + p.nstages * p.stage_bytes;
-    if (!encode_q4k_map(&p.map0, down, E, H, I / kQK)) return cudaErrorInvalidValue;
-    p.map1 = p.map0;
-    smem = size_t(p.raw_off) + size_t(p.nraw) * p.raw_bytes;
-    if (smem > size_t(optin)) return cudaErrorInvalidValue;
+    if (!encode_raw_maps(&p.head0, &p.codes0, down, E, H, I / kQK)) return cudaErrorInvalidValue;
+    p.head1 = p.head0;
+    p.codes1 = p.codes0;
+    smem = rings(2, 4);
+    if (smem == 0) return cudaErrorInvalidValue;
     grouped_gemm_kernel<<<num_sms, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }

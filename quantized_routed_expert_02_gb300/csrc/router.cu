@@ -6,6 +6,9 @@
 // so the top-k of p is the top-k of the logits; after renormalisation the
 // full-softmax denominator cancels and w_j = exp(l_j - l_max) / sum over the
 // selected slots of exp(l - l_max).
+#include <cooperative_groups.h>
+
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -215,14 +218,151 @@ __global__ void __launch_bounds__(256) router_big_kernel(const float *__restrict
     }
 }
 
+// ---------------------------------------------------------------------------
+// Large batches, E <= 128: a cluster of four CTAs per tile of 128 tokens,
+// CTA r of the cluster taking the K quarter [r H/4, (r+1) H/4).  Each CTA
+// streams its x and Wr slices through a 4-stage cp.async ring (32 K per
+// stage, rows padded to 36 floats) and keeps an 8 x 8 register tile per
+// thread (tokens ty + 16 i, experts tx + 16 j: conflict-free shared reads).
+// The per-stage partial of each dot product is summed on its own, then added
+// to the running sum (two-level summation keeps the fp32 rounding of the
+// long dot products small).  The four partial tiles meet through distributed
+// shared memory: CTA r sums, in rank order 0..3, the partials of its 32
+// tokens, adds the bias and runs their top-k.  Fixed summation order, so the
+// logits are deterministic.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kST = 128;                 // tokens per cluster tile
+constexpr int kSE = 128;                 // experts (E <= 128)
+constexpr int kSplit = 4;                // K quarters = CTAs per cluster
+constexpr int kSK = 32;                  // K per stage
+constexpr int kSRow = kSK + 4;           // padded shared row (floats)
+constexpr int kSStages = 4;
+constexpr int kStageFloats = (kST + kSE) * kSRow;
+constexpr int kPS = kSE + 4;             // row of the partial tile (floats)
+constexpr int kSplitSmem = int(sizeof(float)) * kSStages * kStageFloats;
+static_assert(kST * kPS + (kST / kSplit) * (kSE + 1) <= kSStages * kStageFloats,
+              "partial and logit tiles reuse the stage ring");
+}  // namespace
+
+__global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(256, 1)
+    router_split_kernel(const float *__restrict__ x, const float *__restrict__ Wr,
+                        const float *__restrict__ bias, int T, int H, int E, int k,
+                        int32_t *__restrict__ idx, float *__restrict__ w) {
+    extern __shared__ __align__(16) float rsm[];
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    const int r = int(cl.block_rank());
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int t0 = blockIdx.x * kST;
+    const int kq = H / kSplit;
+    const int kbeg = r * kq;
+    const int nst = kq / kSK;
+
+    auto load = [&](int st) {
+        if (st < nst) {
+            float *xs = rsm + (st % kSStages) * kStageFloats, *ws = xs + kST * kSRow;
+            const int k0 = kbeg + st * kSK;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = tid + 256 * i;
+                const int row = c >> 3, q = c & 7;
+                // rows past T or E repeat the last valid row; their results are dropped
+                const int t = min(t0 + row, T - 1), e = min(row, E - 1);
+                cp_async_16(xs + row * kSRow + 4 * q, x + size_t(t) * H + k0 + 4 * q);
+                cp_async_16(ws + row * kSRow + 4 * q, Wr + size_t(e) * H + k0 + 4 * q);
+            }
+        }
+        cp_async_commit();  // an empty group past the end keeps the count uniform
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int st = 0; st < kSStages - 1; ++st) load(st);
+    for (int st = 0; st < nst; ++st) {
+        cp_async_wait_pending(kSStages - 2);  // stage st has landed (this thread's copies)
+        __syncthreads();                      // everyone's copies; the refilled slot is free
+        load(st + kSStages - 1);
+        const float *xs = rsm + (st % kSStages) * kStageFloats, *ws = xs + kST * kSRow;
+        float part[8][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) part[i][j] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < kSK; kk += 4) {
+            float4 a[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = *reinterpret_cast<const float4 *>(xs + (ty + 16 * i) * kSRow + kk);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 b = *reinterpret_cast<const float4 *>(ws + (tx + 16 * j) * kSRow + kk);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    part[i][j] = fmaf(a[i].x, b.x, part[i][j]);
+                    part[i][j] = fmaf(a[i].y, b.y, part[i][j]);
+                    part[i][j] = fmaf(a[i].z, b.z, part[i][j]);
+                    part[i][j] = fmaf(a[i].w, b.w, part[i][j]);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] += part[i][j];
+    }
+    cp_async_wait_all();
+    __syncthreads();  // the stage ring is free: it holds the partial tile now
+
+    float *ptile = rsm;  // [kST][kPS]
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ptile[(ty + 16 * i) * kPS + tx + 16 * j] = acc[i][j];
+    cl.sync();  // every CTA's partial tile is complete
+
+    constexpr int kTok = kST / kSplit;  // tokens reduced by this CTA
+    float *lg = rsm + kST * kPS;        // [kTok][kSE + 1]
+    const float *src[kSplit];
+#pragma unroll
+    for (int q = 0; q < kSplit; ++q) src[q] = cl.map_shared_rank(ptile, q);
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int lt = warp; lt < kTok; lt += 8) {
+        const int tt = r * kTok + lt;
+        for (int e = lane; e < E; e += 32) {
+            float v = src[0][tt * kPS + e];
+#pragma unroll
+            for (int q = 1; q < kSplit; ++q) v += src[q][tt * kPS + e];
+            lg[lt * (kSE + 1) + e] = v + (bias ? bias[e] : 0.f);
+        }
+    }
+    cl.sync();  // no CTA leaves while another reads its partial tile
+
+    for (int lt = warp; lt < kTok; lt += 8) {
+        const int t = t0 + r * kTok + lt;
+        if (t < T) warp_topk(&lg[lt * (kSE + 1)], E, k, idx + size_t(t) * k, w + size_t(t) * k);
+    }
+}
+
 cudaError_t init_router() {
-    return cudaFuncSetAttribute(router_big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kRouterBigSmem);
+    cudaError_t err = cudaFuncSetAttribute(router_big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kRouterBigSmem);
+    if (err != cudaSuccess) return err;
+    return cudaFuncSetAttribute(router_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSplitSmem);
 }
 
 cudaError_t launch_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
                           int k, int32_t *idx, float *w, float *logits, cudaStream_t s) {
     dim3 blk(256);
+    if (T >= 256 && E <= kSE && H % (kSplit * kSK) == 0) {
+        dim3 grid((T + kST - 1) / kST, kSplit);
+        router_split_kernel<<<grid, blk, kSplitSmem, s>>>(x, Wr, bias, T, H, E, k, idx, w);
+        return cudaGetLastError();
+    }
     if (T >= 256) {
         router_big_kernel<<<(T + kRT - 1) / kRT, blk, kRouterBigSmem, s>>>(x, Wr, bias, T, H, E, k, idx, w);
         return cudaGetLastError();
