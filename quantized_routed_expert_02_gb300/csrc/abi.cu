@@ -39,6 +39,7 @@ moe_status moeq4k::device_info(int *sms, int *dev_out) {
         if (init_router() != cudaSuccess) return MOE_ERR_CUDA;
         if (init_decode_fused(dev, n) != cudaSuccess) return MOE_ERR_CUDA;
         if (init_prefill_tc(dev) != cudaSuccess) return MOE_ERR_CUDA;
+        if (init_decode_stream(dev) != cudaSuccess) return MOE_ERR_CUDA;
         g_dev[dev].sms = n;
         g_dev[dev].id = dev;
         g_dev[dev].ready = true;
@@ -157,6 +158,7 @@ int moe_layer_launch_count(int T, int H, int E, int k, int I) {
     int sms = 0, dev = 0;
     if (device_info(&sms, &dev) != MOE_OK) return 0;
     if (decode_fused_supported(dev, T, H, E, k, I)) return 1;
+    if (decode_stream_supported(dev, T, H, E, k, I)) return 2 /* router */ + 2;
     const int router = T >= 256 ? 1 : 2;
     const int permutation = 3;  // count, scan, scatter
     if (prefill_tc_supported(T, H, E, k, I))
@@ -237,6 +239,12 @@ moe_status moe_ffn(const float *x, const int32_t *idx, const float *w, const voi
             W.u64(L.sync), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns, W.u64(L.o), W.timeline_cap(),
             static_cast<cudaStream_t>(stream)));
     }
+    if (decode_stream_supported(dev, T, H, E, k, I)) {
+        return cuda_status(launch_decode_stream(
+            x, idx, w, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
+            static_cast<const uint8_t *>(down), H, E, k, I, y, W.f32(L.h), W.hdr(), sms,
+            static_cast<cudaStream_t>(stream)));
+    }
     return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev,
                        static_cast<cudaStream_t>(stream));
 }
@@ -267,6 +275,11 @@ moe_status moe_layer(const float *x, const float *Wr, const float *bias, const v
             W.u64(L.sync), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns, W.u64(L.o), W.timeline_cap(), s));
     }
     MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), s)));
+    if (decode_stream_supported(dev, T, H, E, k, I)) {
+        return cuda_status(launch_decode_stream(
+            x, idx, w, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
+            static_cast<const uint8_t *>(down), H, E, k, I, y, W.f32(L.h), W.hdr(), sms, s));
+    }
     return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev, s);
 }
 

@@ -57,4 +57,14 @@ cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const 
                                 unsigned long long wait_ns, unsigned long long *timeline,
                                 int timeline_cap, cudaStream_t s);
 
+// One token whose rows do not fit the fused kernel: gate/up then down with
+// the slot-ordered combine folded in (two launches; idx / w from the router
+// or the caller; `hbuf` k*I floats of scratch).
+cudaError_t init_decode_stream(int dev);
+bool decode_stream_supported(int dev, int T, int H, int E, int k, int I);
+cudaError_t launch_decode_stream(const float *x, const int32_t *idx, const float *w,
+                                 const uint8_t *gate, const uint8_t *up, const uint8_t *down,
+                                 int H, int E, int k, int I, float *y, float *hbuf, WsHeader *hdr,
+                                 int num_sms, cudaStream_t s);
+
 }  // namespace moeq4k

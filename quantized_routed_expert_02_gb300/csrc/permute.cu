@@ -49,33 +49,37 @@ __global__ void __launch_bounds__(kPermSlots) permute_count_kernel(const int32_t
     for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[size_t(blockIdx.x) * E + e] = cnt[e];
 }
 
-// One CTA of 1024 threads.  Warp w scans the block counts of experts w,
-// w+32, ... (lanes take 32 consecutive blocks at a time, a shuffle scan with
-// a running carry), then warp 0 scans the expert totals.
+// One CTA of 1024 threads.  The block counts pass through shared memory 32
+// blocks at a time (coalesced loads and stores); thread e keeps expert e's
+// running total and rewrites its column of the tile as exclusive prefixes.
+// Then warp 0 scans the expert totals.
 __global__ void __launch_bounds__(1024) permute_scan_kernel(int nblocks, int E,
                                                             int32_t *__restrict__ blockcnt,
                                                             int32_t *__restrict__ counts,
                                                             int32_t *__restrict__ offs,
                                                             int32_t *__restrict__ active,
                                                             int32_t *__restrict__ nactive) {
+    __shared__ int32_t tile[32][kMaxE + 1];
     __shared__ int32_t tot[kMaxE];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int e = warp; e < E; e += 32) {
-        int carry = 0;
-        for (int b0 = 0; b0 < nblocks; b0 += 32) {
-            const int b = b0 + lane;
-            const int c = b < nblocks ? blockcnt[size_t(b) * E + e] : 0;
-            int incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += u;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int run = 0;  // thread e < E: slots of expert e in the blocks so far
+    for (int b0 = 0; b0 < nblocks; b0 += 32) {
+        const int nb = min(32, nblocks - b0);
+        int32_t *src = blockcnt + size_t(b0) * E;
+        for (int i = tid; i < nb * E; i += blockDim.x) tile[i / E][i % E] = src[i];
+        __syncthreads();
+        if (tid < E) {
+            for (int b = 0; b < nb; ++b) {
+                const int c = tile[b][tid];
+                tile[b][tid] = run;
+                run += c;
             }
-            if (b < nblocks) blockcnt[size_t(b) * E + e] = carry + incl - c;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (lane == 0) tot[e] = carry;
+        __syncthreads();
+        for (int i = tid; i < nb * E; i += blockDim.x) src[i] = tile[i / E][i % E];
+        __syncthreads();
     }
+    if (tid < E) tot[tid] = run;
     __syncthreads();
     if (warp == 0) {
         int carry = 0, na = 0;

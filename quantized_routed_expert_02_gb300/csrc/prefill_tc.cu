@@ -85,7 +85,6 @@ struct Params {
     unsigned long long wait_ns;
 };
 
-
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                             uint64_t *bar) {
     asm volatile(

@@ -56,6 +56,50 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const float *__restr
 }
 
 // ---------------------------------------------------------------------------
+// One or two tokens: one CTA per expert row, each thread a strided quarter-
+// warp share of the row (float4 steps), reduced in a fixed order (warp
+// shuffles, then the eight warp sums in order), so every row of Wr is read
+// by 256 threads at once.
+// ---------------------------------------------------------------------------
+template <int kTT>
+__global__ void __launch_bounds__(256) router_row_kernel(const float *__restrict__ x,
+                                                         const float *__restrict__ Wr,
+                                                         const float *__restrict__ bias, int T,
+                                                         int H, int E, float *__restrict__ logits) {
+    __shared__ float part[kTT][8];
+    const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float4 *wr = reinterpret_cast<const float4 *>(Wr + size_t(e) * H);
+    float acc[kTT];
+#pragma unroll
+    for (int i = 0; i < kTT; ++i) acc[i] = 0.f;
+    for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
+        const float4 a = __ldg(wr + c);
+#pragma unroll
+        for (int i = 0; i < kTT; ++i) {
+            if (i < T) {
+                const float4 b = __ldg(reinterpret_cast<const float4 *>(x + size_t(i) * H) + c);
+                acc[i] = fmaf(a.x, b.x, acc[i]);
+                acc[i] = fmaf(a.y, b.y, acc[i]);
+                acc[i] = fmaf(a.z, b.z, acc[i]);
+                acc[i] = fmaf(a.w, b.w, acc[i]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kTT; ++i) {
+        const float s = warp_sum(acc[i]);
+        if (lane == 0) part[i][warp] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < kTT && int(threadIdx.x) < T) {
+        const int i = threadIdx.x;
+        float s = 0.f;
+        for (int w = 0; w < 8; ++w) s += part[i][w];
+        logits[size_t(i) * E + e] = s + (bias ? bias[e] : 0.f);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Top-k + renormalise: one warp per token.  Lane L holds logits of experts
 // L, L+32, ...; k rounds of a warp-wide arg-max with the order (value
 // descending, index ascending).
@@ -368,8 +412,7 @@ cudaError_t launch_router(const float *x, const float *Wr, const float *bias, in
         return cudaGetLastError();
     }
     if (T <= 2) {
-        dim3 grid((E + 7) / 8, (T + 1) / 2);
-        router_logits_kernel<2><<<grid, blk, 0, s>>>(x, Wr, bias, T, H, E, logits);
+        router_row_kernel<2><<<E, blk, 0, s>>>(x, Wr, bias, T, H, E, logits);
     } else {
         dim3 grid((E + 7) / 8, (T + 7) / 8);
         router_logits_kernel<8><<<grid, blk, 0, s>>>(x, Wr, bias, T, H, E, logits);
