@@ -5,20 +5,27 @@
 // forward_qwen3_moe.rs (aprender-serve 0.35.0), step 2h of
 // forward_single_qwen3_moe_with_cache: each of the token's k experts computes
 // h_j = SiLU(Wg[e_j] x) * (Wu[e_j] x), its down projection o_j = Wd[e_j] h_j,
-// and y = sum_j w_j o_j in slot order.  Two launches after the router:
-//   gate/up  persistent CTAs stage x once (padded, with 32-element sums) and
-//            take (slot, row) items; a warp loads the whole gate and up row
-//            (lane L: sub-block pair L%4 of blocks L/4, L/4+8, ...) before
-//            any arithmetic, so every warp keeps ~6 KB of reads in flight;
-//   down     persistent CTAs stage the k vectors h_j; a warp takes an output
-//            row r, loads row r of four experts' down matrices at a time
-//            (fewer for rows longer than 2048) and folds o_j into
-//            y[r] = sum_j w_j o_j in slot order, so no o buffer and no
-//            separate combine pass exist.
-// Weights are read once per call with read-only 16-byte loads; the dot
-// products are fp32 (one byte-permute and one FMA per weight).
+// and y = sum_j w_j o_j in slot order.  Two launches after the router, each
+// with one persistent CTA per SM:
+//   gate/up  x becomes integer digit planes in shared memory; thread t keeps
+//            the digits of unit t % (H/64) of x (a sub-block pair: 64
+//            elements) in registers and, round after round, loads that
+//            unit's 48 bytes of one gate row and one up row (the next
+//            round's loads issued before this round's arithmetic), dots them
+//            with dp4a, and leaves the partial sums in shared memory, where
+//            one warp per row adds them in a fixed order;
+//   down     the same with the concatenated h_1..h_k (k*I/64 units): a
+//            thread's unit belongs to one slot j, so it dots row r of
+//            Wd[e_j]; the warp that finishes row r sums each slot's units
+//            and folds o_j into y[r] = sum_j w_j o_j in slot order, so no o
+//            buffer and no separate combine pass exist.
+// Shapes the digit layout does not cover (H not a power of two, or k*I/64
+// above the CTA's 512 threads) take fp32 fallbacks with the same results up
+// to rounding: warp per (slot, row) for gate/up, warp per output row for
+// down.  Weights are read once per call with read-only 16-byte loads.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "q4k_dot.cuh"
 
 namespace moeq4k {
 namespace dst {
@@ -27,18 +34,8 @@ constexpr int kGuThreads = 256;
 constexpr int kGuBlocksPerSm = 2;
 constexpr int kDnThreads = 512;
 constexpr int kDnPairsInFlight = 4;  // per lane: slots x blocks of down rows loaded together
-
-// Padded shared-memory vector: 4 floats of padding after every 64, so the
-// lanes of a warp reading 64-element units 64 floats apart hit distinct banks.
-__device__ __forceinline__ int padded(int i) { return i + ((i >> 6) << 2); }
-__host__ __device__ inline int padded_len(int n) { return n + (n >> 4); }
-
-// 1 + q/128 as fp32 from byte i of v, where v's bytes are 0x80 | q.
-__device__ __forceinline__ float one_plus_q(uint32_t v, int i) {
-    return __uint_as_float(__byte_perm(v, 0x3F000000u, 0x7044u | (uint32_t(i) << 8)));
-}
-
-__device__ __forceinline__ float u6f(uint32_t v) { return __uint_as_float(0x4B000000u | v) - 8388608.0f; }
+constexpr int kDgThreads = 512;      // digit kernels: one thread per unit of the vector
+constexpr int kDnRowsPerThread = 2;  // down digit kernel: rows per thread and round
 
 // The 48 bytes a lane needs for sub-blocks 2c and 2c+1 of one block: the
 // block head and the 32 code bytes qs[32c .. 32c+31].
@@ -54,53 +51,12 @@ __device__ __forceinline__ Pair load_pair(const uint8_t *blk, int c) {
     return p;
 }
 
-// sum over sub-blocks 2c, 2c+1 of (d sc q - dmin m) x: `xs` points at the
-// block's element 64c of the padded vector, `s2` at its two 32-element sums.
-// The codes enter as 1 + q/128, so sum(q x) = 128 (sum((1 + q/128) x) - sum(x)).
 __device__ __forceinline__ float pair_dot(const Pair &P, int c, const float *xs, const float *s2) {
-    const uint32_t w[8] = {P.qa.x, P.qa.y, P.qa.z, P.qa.w, P.qb.x, P.qb.y, P.qb.z, P.qb.w};
-    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-#pragma unroll
-    for (int wi = 0; wi < 8; ++wi) {
-        const uint32_t lo = (w[wi] & 0x0F0F0F0Fu) | 0x80808080u;
-        const uint32_t hi = ((w[wi] >> 4) & 0x0F0F0F0Fu) | 0x80808080u;
-        const float4 xl = *reinterpret_cast<const float4 *>(xs + 4 * wi);
-        const float4 xh = *reinterpret_cast<const float4 *>(xs + 32 + 4 * wi);
-        a0 = fmaf(one_plus_q(lo, 0), xl.x, a0);
-        a1 = fmaf(one_plus_q(lo, 1), xl.y, a1);
-        a0 = fmaf(one_plus_q(lo, 2), xl.z, a0);
-        a1 = fmaf(one_plus_q(lo, 3), xl.w, a1);
-        b0 = fmaf(one_plus_q(hi, 0), xh.x, b0);
-        b1 = fmaf(one_plus_q(hi, 1), xh.y, b1);
-        b0 = fmaf(one_plus_q(hi, 2), xh.z, b0);
-        b1 = fmaf(one_plus_q(hi, 3), xh.w, b1);
-    }
-    // scales and mins of sub-blocks 2c (j0) and 2c+1 (j1)
-    const uint4 &h = P.head;
-    const int j0 = 2 * c, j1 = 2 * c + 1;
-    uint32_t sc0, m0, sc1, m1;
-    if (c < 2) {
-        sc0 = (h.y >> (8 * j0)) & 63u;
-        m0 = (h.z >> (8 * j0)) & 63u;
-        sc1 = (h.y >> (8 * j1)) & 63u;
-        m1 = (h.z >> (8 * j1)) & 63u;
-    } else {
-        const int a = j0 - 4, b = j1 - 4;
-        sc0 = ((h.w >> (8 * a)) & 15u) | (((h.y >> (8 * a + 6)) & 3u) << 4);
-        m0 = ((h.w >> (8 * a + 4)) & 15u) | (((h.z >> (8 * a + 6)) & 3u) << 4);
-        sc1 = ((h.w >> (8 * b)) & 15u) | (((h.y >> (8 * b + 6)) & 3u) << 4);
-        m1 = ((h.w >> (8 * b + 4)) & 15u) | (((h.z >> (8 * b + 6)) & 3u) << 4);
-    }
-    const float2 dd = q4k_d_dmin(h);
-    const float dm = dd.x * 128.0f;
-    const float A0 = dm * u6f(sc0), A1 = dm * u6f(sc1);
-    const float B0 = dd.y * u6f(m0), B1 = dd.y * u6f(m1);
-    const float slo = s2[0], shi = s2[1];
-    float acc = A0 * ((a0 + a1) - slo);
-    acc = fmaf(-B0, slo, acc);
-    acc = fmaf(A1, (b0 + b1) - shi, acc);
-    acc = fmaf(-B1, shi, acc);
-    return acc;
+    return moeq4k::pair_dot(P.head, P.qa, P.qb, c, xs, s2);
+}
+
+__device__ __forceinline__ float pair_dot_digits(const Pair &P, int c, const XDigits &X) {
+    return moeq4k::pair_dot_digits(P.head, P.qa, P.qb, c, X);
 }
 
 // Stage n floats of `src` into the padded vector `dst` and their 32-element
@@ -242,6 +198,197 @@ __global__ void __launch_bounds__(kDnThreads, 1)
     }
 }
 
+// A vector of n floats (n a multiple of 128) as three digit planes (n bytes
+// each, unit-major 16-byte chunks: plane_offset), a scale and a sum per
+// 32-element run.  Warps take 128-element chunks, lane l elements 4l..4l+3.
+__device__ __forceinline__ void stage_digits(const float *__restrict__ src, int n, uint8_t *planes,
+                                             float *scales, float *sums) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int nunits = n >> 6;
+    for (int ch = warp; ch < (n >> 7); ch += nw) {
+        const int e0 = 128 * ch + 4 * lane;
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(src + e0));
+        uint32_t wa, wb, wc;
+        float sum;
+        const float sc = run_digits4(v, lane, wa, wb, wc, sum);
+        const int off = plane_offset(e0, nunits);
+        *reinterpret_cast<uint32_t *>(planes + off) = wa;
+        *reinterpret_cast<uint32_t *>(planes + n + off) = wb;
+        *reinterpret_cast<uint32_t *>(planes + 2 * n + off) = wc;
+        if ((lane & 7) == 0) {
+            scales[e0 >> 5] = sc;
+            sums[e0 >> 5] = sum;
+        }
+    }
+}
+
+// The CTA's contiguous share [*lo, *hi) of n work units.
+__device__ __forceinline__ void cta_share(int n, int *lo, int *hi) {
+    const int per = (n + gridDim.x - 1) / gridDim.x;
+    *lo = min(n, int(blockIdx.x) * per);
+    *hi = min(n, *lo + per);
+}
+
+// h[j*I + r] = SiLU(Wg[e_j][r] . x) * (Wu[e_j][r] . x) with x as digits.
+// UX = H/64 units (a power of two <= 512); Q = 512/UX items per round.
+__global__ void __launch_bounds__(kDgThreads, 1)
+    stream_gateup_digits_kernel(const float *__restrict__ x, const uint8_t *__restrict__ gate,
+                                const uint8_t *__restrict__ up, const int32_t *__restrict__ idx,
+                                int k, int E, int H, int I, float *__restrict__ h, WsHeader *hdr) {
+    extern __shared__ __align__(16) uint8_t smd[];
+    const int UX = H >> 6, Q = kDgThreads / UX;
+    uint8_t *planes = smd;                                      // 3H bytes
+    float *xscale = reinterpret_cast<float *>(smd + 3 * H);     // H/32
+    float *xsum = xscale + H / 32;                              // H/32
+    float *P = xsum + H / 32;                                   // [2][Q][2][UX]
+    int *eid = reinterpret_cast<int *>(P + 2 * kDgThreads * 2);  // [k]
+    load_experts(idx, k, E, eid, hdr);
+    stage_digits(x, H, planes, xscale, xsum);
+    __syncthreads();
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    const int u = tid % UX, q = tid / UX, sb = u >> 2, c = u & 3;
+    XDigits X;
+    load_digits(X, planes, H, UX, u, xscale, xsum);
+    const size_t row_bytes = size_t(H / kQK) * kBlockBytes, mat = size_t(I) * row_bytes;
+    int it0, it1;
+    cta_share(k * I, &it0, &it1);
+    const int rounds = (it1 - it0 + Q - 1) / Q;
+
+    // this thread's item of round rd: its gate and up bytes, if any
+    auto load = [&](int rd, Pair &pg, Pair &pu) -> bool {
+        const int item = it0 + rd * Q + q;
+        if (item >= it1) return false;
+        const int j = item / I, r = item - j * I, e = eid[j];
+        if (e < 0) return false;
+        const size_t off = size_t(e) * mat + size_t(r) * row_bytes + size_t(sb) * kBlockBytes;
+        pg = load_pair(gate + off, c);
+        pu = load_pair(up + off, c);
+        return true;
+    };
+    Pair cg, cu, ng, nu;
+    bool have = rounds > 0 && load(0, cg, cu);
+    for (int rd = 0; rd < rounds; ++rd) {
+        const bool have_next = rd + 1 < rounds && load(rd + 1, ng, nu);
+        float g = 0.f, v = 0.f;
+        if (have) {
+            g = pair_dot_digits(cg, c, X);
+            v = pair_dot_digits(cu, c, X);
+        }
+        float *Pb = P + (rd & 1) * (kDgThreads * 2);
+        Pb[(2 * q) * UX + u] = g;
+        Pb[(2 * q + 1) * UX + u] = v;
+        __syncthreads();  // also orders the reuse of the other buffer two rounds on
+        for (int qq = warp; qq < Q; qq += nw) {
+            const int item = it0 + rd * Q + qq;
+            if (item >= it1) break;
+            const int j = item / I, r = item - j * I;
+            if (eid[j] < 0) continue;
+            float gs = 0.f, us = 0.f;
+            for (int uu = lane; uu < UX; uu += 32) {
+                gs += Pb[(2 * qq) * UX + uu];
+                us += Pb[(2 * qq + 1) * UX + uu];
+            }
+            gs = warp_sum(gs);
+            us = warp_sum(us);
+            if (lane == 0) h[size_t(j) * I + r] = silu_mul(gs, us);
+        }
+        cg = ng;
+        cu = nu;
+        have = have_next;
+    }
+}
+
+// y[r] = sum_j w_j (Wd[e_j][r] . h_j) with h_1..h_k as one digit vector of
+// n = k*I elements: thread t < Q*UD owns unit t % UD (UD = n/64 <= 512) and
+// kDnRowsPerThread rows per round.
+__global__ void __launch_bounds__(kDgThreads, 1)
+    stream_down_digits_kernel(const float *__restrict__ h, const uint8_t *__restrict__ down,
+                              const int32_t *__restrict__ idx, const float *__restrict__ w, int k,
+                              int E, int H, int I, float *__restrict__ y, WsHeader *hdr) {
+    extern __shared__ __align__(16) uint8_t smd[];
+    constexpr int RB = kDnRowsPerThread;
+    const int n = k * I, UD = n >> 6, upr = I >> 6, Q = kDgThreads / UD;
+    uint8_t *planes = smd;                                      // 3n bytes
+    float *hscale = reinterpret_cast<float *>(smd + 3 * size_t(n));
+    float *hsum = hscale + n / 32;
+    float *P = hsum + n / 32;                                   // [2][Q*RB][UD]
+    float *wj = P + 2 * RB * kDgThreads;                        // [k]
+    int *eid = reinterpret_cast<int *>(wj + k);                 // [k]
+    load_experts(idx, k, E, eid, hdr);
+    for (int j = threadIdx.x; j < k; j += blockDim.x) wj[j] = w[j];
+    stage_digits(h, n, planes, hscale, hsum);
+    __syncthreads();
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    const bool active = tid < Q * UD;
+    const int u = tid % UD, q = tid / UD;
+    const int j = u / upr, uin = u - j * upr, sb = uin >> 2, c = uin & 3;
+    const int e = active ? eid[j] : -1;
+    XDigits X;
+    if (active) load_digits(X, planes, n, UD, u, hscale, hsum);
+    const size_t row_bytes = size_t(I / kQK) * kBlockBytes, mat = size_t(H) * row_bytes;
+    const uint8_t *base = down + (e >= 0 ? size_t(e) * mat : 0) + size_t(sb) * kBlockBytes;
+    int r0, r1;
+    cta_share(H, &r0, &r1);
+    const int per_round = Q * RB;
+    const int rounds = (r1 - r0 + per_round - 1) / per_round;
+
+    auto load = [&](int rd, Pair (&pr)[RB], bool (&ok)[RB]) {
+#pragma unroll
+        for (int b = 0; b < RB; ++b) {
+            const int r = r0 + rd * per_round + q * RB + b;
+            ok[b] = e >= 0 && r < r1;
+            if (ok[b]) pr[b] = load_pair(base + size_t(r) * row_bytes, c);
+        }
+    };
+    Pair cur[RB], nxt[RB];
+    bool cok[RB] = {}, nok[RB] = {};
+    if (rounds > 0) load(0, cur, cok);
+    for (int rd = 0; rd < rounds; ++rd) {
+        if (rd + 1 < rounds) {
+            load(rd + 1, nxt, nok);
+        } else {
+#pragma unroll
+            for (int b = 0; b < RB; ++b) nok[b] = false;
+        }
+        float *Pb = P + (rd & 1) * (RB * kDgThreads);
+        if (active) {
+#pragma unroll
+            for (int b = 0; b < RB; ++b)
+                Pb[(q * RB + b) * UD + u] = cok[b] ? pair_dot_digits(cur[b], c, X) : 0.f;
+        }
+        __syncthreads();  // also orders the reuse of the other buffer two rounds on
+        for (int ri = warp; ri < per_round; ri += nw) {
+            const int r = r0 + rd * per_round + ri;
+            if (r >= r1) break;
+            float acc = 0.f;
+            for (int jj = 0; jj < k; ++jj) {
+                if (eid[jj] < 0) continue;
+                float part = 0.f;
+                for (int v = lane; v < upr; v += 32) part += Pb[ri * UD + jj * upr + v];
+                acc = fmaf(wj[jj], warp_sum(part), acc);
+            }
+            if (lane == 0) y[r] = acc;
+        }
+#pragma unroll
+        for (int b = 0; b < RB; ++b) {
+            cur[b] = nxt[b];
+            cok[b] = nok[b];
+        }
+    }
+}
+
+bool gateup_digits_ok(int H) { return H >= 256 && H <= 64 * kDgThreads && (H & (H - 1)) == 0; }
+bool down_digits_ok(int k, int I) { return size_t(k) * I <= size_t(64) * kDgThreads; }
+size_t gateup_digits_smem(int H, int k) {
+    return 3 * size_t(H) + sizeof(float) * (H / 16 + 4 * kDgThreads) + sizeof(int) * k;
+}
+size_t down_digits_smem(int k, int I) {
+    const size_t n = size_t(k) * I;
+    return 3 * n + sizeof(float) * (n / 16 + 2 * kDnRowsPerThread * kDgThreads + k) + sizeof(int) * k;
+}
+
 size_t gateup_smem(int H, int k) { return sizeof(float) * (padded_len(H) + H / 32) + sizeof(int) * k; }
 size_t down_smem(int I, int k) {
     return sizeof(float) * size_t(k) * (padded_len(I) + I / 32 + 1) + sizeof(int) * k;
@@ -266,14 +413,18 @@ cudaError_t init_decode_stream(int dev) {
         err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (err != cudaSuccess) return err;
     }
-    return cudaSuccess;
+    return cudaFuncSetAttribute(stream_down_digits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin);
 }
 
 bool decode_stream_supported(int dev, int T, int H, int E, int k, int I) {
     using namespace dst;
     if (T != 1 || H % kQK != 0 || I % kQK != 0 || H > 8192 || I > 8192) return false;
     const size_t optin = size_t(g_stream_smem_optin[dev]);
-    return gateup_smem(H, k) <= 48 * 1024 && down_smem(I, k) <= optin;
+    const bool gu = gateup_digits_ok(H) ? gateup_digits_smem(H, k) <= 48 * 1024
+                                        : gateup_smem(H, k) <= 48 * 1024;
+    const bool dn = down_digits_ok(k, I) ? down_digits_smem(k, I) <= optin : down_smem(I, k) <= optin;
+    return gu && dn;
 }
 
 cudaError_t launch_decode_stream(const float *x, const int32_t *idx, const float *w,
@@ -284,13 +435,19 @@ cudaError_t launch_decode_stream(const float *x, const int32_t *idx, const float
     const int nbh = (H / kQK + 7) / 8, nbi = (I / kQK + 7) / 8;
     const size_t sg = gateup_smem(H, k), sd = down_smem(I, k);
     const int gg = num_sms * kGuBlocksPerSm;
-    if (nbh <= 1)
+    if (gateup_digits_ok(H))
+        stream_gateup_digits_kernel<<<num_sms, kDgThreads, gateup_digits_smem(H, k), s>>>(
+            x, gate, up, idx, k, E, H, I, hbuf, hdr);
+    else if (nbh <= 1)
         stream_gateup_kernel<1><<<gg, kGuThreads, sg, s>>>(x, gate, up, idx, k, E, H, I, hbuf, hdr);
     else if (nbh <= 2)
         stream_gateup_kernel<2><<<gg, kGuThreads, sg, s>>>(x, gate, up, idx, k, E, H, I, hbuf, hdr);
     else
         stream_gateup_kernel<4><<<gg, kGuThreads, sg, s>>>(x, gate, up, idx, k, E, H, I, hbuf, hdr);
-    if (nbi <= 1)
+    if (down_digits_ok(k, I))
+        stream_down_digits_kernel<<<num_sms, kDgThreads, down_digits_smem(k, I), s>>>(
+            hbuf, down, idx, w, k, E, H, I, y, hdr);
+    else if (nbi <= 1)
         stream_down_kernel<1><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
     else if (nbi <= 2)
         stream_down_kernel<2><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);

@@ -1,6 +1,7 @@
 """Single-token calls whose expert rows do not fit the fused kernel (the
 Qwen3-235B-A22B shape among them): router, then the streamed gate/up and
-down launches with the slot-ordered combine folded into the down pass."""
+down launches (integer-digit dot products, fp32 fallbacks) with the
+slot-ordered combine folded into the down pass."""
 import numpy as np
 import pytest
 
@@ -19,10 +20,14 @@ def test_a22b_single_token_takes_the_streamed_path(m):
     assert m.moe_layer_launch_count(s.T, s.H, s.E, s.k, s.I) == STREAM_LAUNCHES
 
 
-# rows longer than one lane's share (H = 8192: four blocks per lane), many
-# slots (k = 32), odd block counts per row (I = 1280: five blocks)
+# Integer-digit kernels for both launches: the A22B row lengths, many slots
+# (k = 32, k*I/64 = 512 units: every thread of the CTA), long x (H = 8192:
+# 128 units), odd block counts per down row (I = 1280: five blocks).  The
+# fp32 fallbacks: gate/up for H = 1280 (not a power of two), down for
+# k*I/64 = 768 units (more than the CTA's threads).
 @pytest.mark.parametrize("H,E,k,I", [(4096, 8, 8, 1536), (1024, 32, 32, 1024),
-                                     (8192, 4, 2, 1280), (2048, 16, 16, 2048)])
+                                     (8192, 4, 2, 1280), (2048, 16, 16, 2048),
+                                     (1280, 8, 8, 2048), (1024, 16, 12, 4096)])
 def test_streamed_shapes(m, H, E, k, I):
     assert m.moe_layer_launch_count(1, H, E, k, I) == STREAM_LAUNCHES
     shape = synth.custom_shape(1, H, E, k, I, wr_std=0.03, cfg_id=20 + (H + E + k + I) % 30)
