@@ -89,6 +89,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Hint: bring `bytes` of global memory at `src` into L2 (TMA engine, no
+// completion to wait for).  `src` 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 16-byte asynchronous global->shared copy (L1 bypass).  No L2 cache-policy
 // operand: kernels whose copies carried one (createpolicy + .L2::cache_hint)
 // raised illegal-instruction faults on GB300.

@@ -23,6 +23,7 @@
 // above the CTA's 512 threads) take fp32 fallbacks with the same results up
 // to rounding: warp per (slot, row) for gate/up, warp per output row for
 // down.  Weights are read once per call with read-only 16-byte loads.
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
 #include "q4k_dot.cuh"
@@ -86,6 +87,13 @@ __device__ __forceinline__ void load_experts(const int32_t *idx, int k, int E, i
         }
         eid[j] = e;
     }
+}
+
+// The CTA's contiguous share [*lo, *hi) of n work units.
+__device__ __forceinline__ void cta_share(int n, int *lo, int *hi) {
+    const int per = (n + gridDim.x - 1) / gridDim.x;
+    *lo = min(n, int(blockIdx.x) * per);
+    *hi = min(n, *lo + per);
 }
 
 // h[j*I + r] = SiLU(Wg[e_j][r] . x) * (Wu[e_j][r] . x).  NB = blocks per
@@ -204,29 +212,33 @@ __global__ void __launch_bounds__(kDnThreads, 1)
 __device__ __forceinline__ void stage_digits(const float *__restrict__ src, int n, uint8_t *planes,
                                              float *scales, float *sums) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    const int nunits = n >> 6;
-    for (int ch = warp; ch < (n >> 7); ch += nw) {
-        const int e0 = 128 * ch + 4 * lane;
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(src + e0));
-        uint32_t wa, wb, wc;
-        float sum;
-        const float sc = run_digits4(v, lane, wa, wb, wc, sum);
-        const int off = plane_offset(e0, nunits);
-        *reinterpret_cast<uint32_t *>(planes + off) = wa;
-        *reinterpret_cast<uint32_t *>(planes + n + off) = wb;
-        *reinterpret_cast<uint32_t *>(planes + 2 * n + off) = wc;
-        if ((lane & 7) == 0) {
-            scales[e0 >> 5] = sc;
-            sums[e0 >> 5] = sum;
+    const int nunits = n >> 6, nch = n >> 7;
+    constexpr int kBatch = 4;  // chunks a warp loads before converting any
+    for (int base = warp; base < nch; base += kBatch * nw) {
+        float4 v[kBatch];
+#pragma unroll
+        for (int t = 0; t < kBatch; ++t) {
+            const int ch = base + t * nw;
+            if (ch < nch) v[t] = __ldg(reinterpret_cast<const float4 *>(src + 128 * ch + 4 * lane));
+        }
+#pragma unroll
+        for (int t = 0; t < kBatch; ++t) {
+            const int ch = base + t * nw;
+            if (ch >= nch) break;  // uniform over the warp
+            const int e0 = 128 * ch + 4 * lane;
+            uint32_t wa, wb, wc;
+            float sum;
+            const float sc = run_digits4(v[t], lane, wa, wb, wc, sum);
+            const int off = plane_offset(e0, nunits);
+            *reinterpret_cast<uint32_t *>(planes + off) = wa;
+            *reinterpret_cast<uint32_t *>(planes + n + off) = wb;
+            *reinterpret_cast<uint32_t *>(planes + 2 * n + off) = wc;
+            if ((lane & 7) == 0) {
+                scales[e0 >> 5] = sc;
+                sums[e0 >> 5] = sum;
+            }
         }
     }
-}
-
-// The CTA's contiguous share [*lo, *hi) of n work units.
-__device__ __forceinline__ void cta_share(int n, int *lo, int *hi) {
-    const int per = (n + gridDim.x - 1) / gridDim.x;
-    *lo = min(n, int(blockIdx.x) * per);
-    *hi = min(n, *lo + per);
 }
 
 // h[j*I + r] = SiLU(Wg[e_j][r] . x) * (Wu[e_j][r] . x) with x as digits.
@@ -243,13 +255,10 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     float *P = xsum + H / 32;                                   // [2][Q][2][UX]
     int *eid = reinterpret_cast<int *>(P + 2 * kDgThreads * 2);  // [k]
     load_experts(idx, k, E, eid, hdr);
-    stage_digits(x, H, planes, xscale, xsum);
     __syncthreads();
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
     const int u = tid % UX, q = tid / UX, sb = u >> 2, c = u & 3;
-    XDigits X;
-    load_digits(X, planes, H, UX, u, xscale, xsum);
     const size_t row_bytes = size_t(H / kQK) * kBlockBytes, mat = size_t(I) * row_bytes;
     int it0, it1;
     cta_share(k * I, &it0, &it1);
@@ -266,8 +275,13 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         pu = load_pair(up + off, c);
         return true;
     };
+    // the first round's rows are requested before x is converted
     Pair cg, cu, ng, nu;
     bool have = rounds > 0 && load(0, cg, cu);
+    stage_digits(x, H, planes, xscale, xsum);
+    __syncthreads();
+    XDigits X;
+    load_digits(X, planes, H, UX, u, xscale, xsum);
     for (int rd = 0; rd < rounds; ++rd) {
         const bool have_next = rd + 1 < rounds && load(rd + 1, ng, nu);
         float g = 0.f, v = 0.f;
@@ -317,7 +331,6 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     int *eid = reinterpret_cast<int *>(wj + k);                 // [k]
     load_experts(idx, k, E, eid, hdr);
     for (int j = threadIdx.x; j < k; j += blockDim.x) wj[j] = w[j];
-    stage_digits(h, n, planes, hscale, hsum);
     __syncthreads();
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
@@ -325,8 +338,6 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     const int u = tid % UD, q = tid / UD;
     const int j = u / upr, uin = u - j * upr, sb = uin >> 2, c = uin & 3;
     const int e = active ? eid[j] : -1;
-    XDigits X;
-    if (active) load_digits(X, planes, n, UD, u, hscale, hsum);
     const size_t row_bytes = size_t(I / kQK) * kBlockBytes, mat = size_t(H) * row_bytes;
     const uint8_t *base = down + (e >= 0 ? size_t(e) * mat : 0) + size_t(sb) * kBlockBytes;
     int r0, r1;
@@ -342,9 +353,14 @@ __global__ void __launch_bounds__(kDgThreads, 1)
             if (ok[b]) pr[b] = load_pair(base + size_t(r) * row_bytes, c);
         }
     };
+    // the first round's rows are requested before h is converted
     Pair cur[RB], nxt[RB];
     bool cok[RB] = {}, nok[RB] = {};
     if (rounds > 0) load(0, cur, cok);
+    stage_digits(h, n, planes, hscale, hsum);
+    __syncthreads();
+    XDigits X;
+    if (active) load_digits(X, planes, n, UD, u, hscale, hsum);
     for (int rd = 0; rd < rounds; ++rd) {
         if (rd + 1 < rounds) {
             load(rd + 1, nxt, nok);
@@ -362,12 +378,23 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         for (int ri = warp; ri < per_round; ri += nw) {
             const int r = r0 + rd * per_round + ri;
             if (r >= r1) break;
+            // eight slots' butterflies interleaved, then o_j folded in slot order
             float acc = 0.f;
-            for (int jj = 0; jj < k; ++jj) {
-                if (eid[jj] < 0) continue;
-                float part = 0.f;
-                for (int v = lane; v < upr; v += 32) part += Pb[ri * UD + jj * upr + v];
-                acc = fmaf(wj[jj], warp_sum(part), acc);
+            for (int j0 = 0; j0 < k; j0 += 8) {
+                float part[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    part[t] = 0.f;
+                    if (j0 + t < k)
+                        for (int v = lane; v < upr; v += 32) part[t] += Pb[ri * UD + (j0 + t) * upr + v];
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) part[t] += __shfl_xor_sync(0xffffffffu, part[t], o);
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    if (j0 + t < k && eid[j0 + t] >= 0) acc = fmaf(wj[j0 + t], part[t], acc);
             }
             if (lane == 0) y[r] = acc;
         }
