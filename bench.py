@@ -42,7 +42,7 @@ DEFAULT_CONFIG = "a3b_decode"
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.SHAPES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

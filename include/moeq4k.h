@@ -89,10 +89,11 @@ MOE_API int moe_version(void);
 /*
  * Bytes of device workspace that moe_router / moe_permute / moe_ffn /
  * moe_layer need for this shape (0 when the shape is invalid).  The
- * workspace holds the sticky status word, a call counter and a 2 MB region
- * of tagged values that single-token calls keep between calls (both at the
- * same place for every shape), the permutation, the expert activations
- * h [T*k, I] and the per-slot outputs [T*k, H].
+ * workspace holds the sticky status word, call and work counters and a
+ * 2 KB region of tagged router logits that single-token calls keep between
+ * calls (both at the same place for every shape), the permutation, the
+ * expert activations h [T*k, I], the per-slot outputs [T*k, H] and the
+ * fp16 activation rows of the tensor-core path.
  */
 MOE_API size_t moe_workspace_bytes(int T, int H, int E, int k, int I);
 
@@ -105,7 +106,7 @@ MOE_API int moe_layer_launch_count(int T, int H, int E, int k, int I);
 /*
  * Zero the workspace header (status word, counters) and the region of
  * tagged values that single-token calls keep between calls: the first
- * min(ws_bytes, 256 B + 2 MB) bytes.  Call once after allocating a
+ * min(ws_bytes, 256 B + 2 KB) bytes.  Call once after allocating a
  * workspace, before its first use (single-token calls rely on that region
  * starting at zero), and whenever the sticky status should be cleared.  A
  * workspace large enough for several shapes may serve all of them.
