@@ -78,7 +78,7 @@ inline WsLayout ws_layout(int T, int H, int E, int k, int I, bool host_staging) 
     L.o = off;       off = align256(off + sizeof(float) * pairs * H);
     L.x16 = off;     off = align256(off + 2 * pairs * H);                // fp16 activations, sorted rows
     L.h16 = off;     off = align256(off + 2 * pairs * I);                // fp16 SwiGLU output
-    L.chunks = off;  off = align256(off + sizeof(TcChunk) * (pairs / 256 + E + 1));
+    L.chunks = off;  off = align256(off + sizeof(TcChunk) * (pairs / 32 + E + 1));  // chunks of >= 32 slots
     L.xstage = off;
     L.ystage = off;
     if (host_staging) {

@@ -13,21 +13,23 @@
 // is written in that order too, so every activation tile is one contiguous
 // block of rows.
 //
-// One persistent CTA per SM takes work items (expert chunk of <= 256 slots x
+// One persistent CTA per SM takes work items (expert chunk of <= cap slots x
 // 128 rows each of gate and up, or 256 rows of down: two A operands that
-// share every activation tile) from an atomic counter.  12 warps:
+// share every activation tile) from an atomic counter; cap is 256, or the
+// batch's token count rounded up to 32 when that is smaller.  12 warps:
 //   thread 32   stages the raw Q4_K bytes of each K stage (64 weights per
 //               row: the 16-byte block head and the 32 code bytes) for the
 //               tile's 128 rows with two 2-D TMA copies per matrix, into a
-//               ring of raw slots;
+//               ring of raw slots as deep as shared memory allows (5 stages
+//               at cap 256, up to 16 for small batches): these come from HBM
+//               and need the most latency cover;
 //   warps 4-11  dequantise them into fp16 K-major tiles with the 128-byte
 //               swizzle (generic stores, then a proxy fence), into a 2-slot
 //               ring of weight tiles;
 //   thread 64   loads the chunk's activation tile (its sorted rows rounded
 //               up to 32, x 64 K, fp16) with 2-D TMA copies of 32 rows that
-//               apply the 128-byte swizzle, into a ring as deep as shared
-//               memory allows (3 slots): these come from L2 or HBM and need
-//               the most latency cover;
+//               apply the 128-byte swizzle, into a ring of 3 slots of cap
+//               rows (4 when cap <= 64);
 //   thread 0    issues tcgen05.mma (fp16 x fp16 -> fp32 in tensor memory)
 //               once a stage's weight and activation tiles are both in, and
 //               commits its completion to both rings' "empty" mbarriers;
@@ -53,12 +55,11 @@ constexpr int kBM = 128;   // weight rows per tile
 constexpr int kBN = 256;   // tokens per tile (max)
 constexpr int kBK = 64;    // K per stage
 constexpr int kTileA = kBM * kBK * 2;
-constexpr int kTileB = kBN * kBK * 2;
 constexpr int kBoxRows = 32;                   // activation rows per TMA box
 constexpr int kBoxB = kBoxRows * kBK * 2;
 constexpr int kHead = 2048;  // barriers, item info, token list
 constexpr int kDeq = 256;      // warps 4-11
-constexpr int kMaxSlots = 8;   // per ring
+constexpr int kMaxSlots = 16;  // per ring
 constexpr int kRawHead = kBM * 16;               // block heads of a tile's rows
 constexpr int kRawMat = kBM * (16 + 32);         // one matrix's raw bytes of a stage
 
@@ -81,7 +82,8 @@ struct Params {
     int rows_per_expert;        // I (mode 0) or H (mode 1)
     int nr, r_off;              // raw ring: slots, byte offset (slot = nmat * kRawMat bytes)
     int na, a_off;              // weight-tile ring: slots, byte offset (slot = nmat * kTileA)
-    int nb, b_off;              // activation-tile ring: slots, byte offset (slot = kTileB)
+    int nb, b_off, b_slot;      // activation-tile ring: slots, byte offset, bytes per slot
+                                //   (chunk capacity x 128 B)
     unsigned long long wait_ns;
 };
 
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 tc::fence_after_sync();
                 const uint32_t a0 = smem_addr(aring + size_t(as) * nmat * kTileA), a1 = a0 + kTileA;
-                const uint32_t b = smem_addr(bring + size_t(bs) * kTileB);
+                const uint32_t b = smem_addr(bring + size_t(bs) * p.b_slot);
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
                     const uint64_t bd = tc::smem_desc_sw128(b + 32 * kk);
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 mbar_arrive_expect_tx(bfull + bs, nbox * kBoxB);
                 for (int i = 0; i < nbox; ++i)
-                    tma_load_2d(bring + size_t(bs) * kTileB + i * kBoxB, &p.mapB, s * kBK,
+                    tma_load_2d(bring + size_t(bs) * p.b_slot + i * kBoxB, &p.mapB, s * kBK,
                                 row0 + i * kBoxRows, bfull + bs);
             }
         } else if (tid == 32) {
@@ -431,11 +433,12 @@ __global__ void gather_half_kernel(const float *__restrict__ x, const int32_t *_
     }
 }
 
-// Chunks of <= kBN slots per active expert, in active order, and the work
+// Chunks of <= cap slots per active expert, in active order, and the work
 // counters reset.  One warp: lanes take active experts in turns of 32, a
 // warp scan gives each expert's first chunk.
 __global__ void plan_kernel(const int32_t *__restrict__ offs, const int32_t *__restrict__ active,
-                            const int32_t *__restrict__ nactive, TcChunk *chunks, WsHeader *hdr) {
+                            const int32_t *__restrict__ nactive, int cap, TcChunk *chunks,
+                            WsHeader *hdr) {
     const int lane = threadIdx.x & 31;
     if (threadIdx.x >= 32) return;
     const int na = *nactive;
@@ -444,7 +447,7 @@ __global__ void plan_kernel(const int32_t *__restrict__ offs, const int32_t *__r
         const int a = base + lane;
         const int e = a < na ? active[a] : 0;
         const int n = a < na ? offs[e + 1] - offs[e] : 0;
-        const int mine = (n + kBN - 1) / kBN;
+        const int mine = (n + cap - 1) / cap;
         int incl = mine;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -454,8 +457,8 @@ __global__ void plan_kernel(const int32_t *__restrict__ offs, const int32_t *__r
         for (int c = 0; c < mine; ++c) {
             TcChunk ch;
             ch.e = e;
-            ch.tok_off = c * kBN;
-            ch.tok_cnt = min(kBN, n - c * kBN);
+            ch.tok_off = c * cap;
+            ch.tok_cnt = min(cap, n - c * cap);
             ch.pad = 0;
             chunks[nc + incl - mine + c] = ch;
         }
@@ -545,7 +548,11 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
                               int num_sms, unsigned long long wait_ns, cudaStream_t s) {
     using namespace ptc;
     gather_half_kernel<<<num_sms * 8, 256, 0, s>>>(x, slotpos, T, k, H, x16);
-    plan_kernel<<<1, 32, 0, s>>>(offs, active, nactive, chunks, hdr);
+    // Chunk capacity: up to 256 slots, no more than the batch's tokens
+    // (rounded to 32) so that small batches get deep rings; a larger expert
+    // list (a caller's routing with repeated experts) is split into more chunks.
+    const int cap = std::min(kBN, (T + kBoxRows - 1) / kBoxRows * kBoxRows);
+    plan_kernel<<<1, 32, 0, s>>>(offs, active, nactive, cap, chunks, hdr);
     const int rows = T * k;
 
     Params p = {};
@@ -561,15 +568,21 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     const int optin = g_tc_smem_optin[dev];
 
     // Shared memory: header, raw ring, weight-tile ring (1024-aligned), then
-    // as many activation slots as fit.
-    auto rings = [&](int nmat, int nr) -> size_t {
-        p.nr = nr;
-        p.r_off = kHead;
+    // the activation ring (3 slots of the chunk capacity, 4 for chunks of at
+    // most 64 slots); the raw ring takes what is left, up to kMaxSlots stages.
+    auto rings = [&](int nmat) -> size_t {
         p.na = 2;
-        p.a_off = (kHead + nr * nmat * kRawMat + 1023) & ~1023;
-        p.b_off = p.a_off + p.na * nmat * kTileA;
-        p.nb = std::min(kMaxSlots, (optin - p.b_off) / kTileB);
-        return p.nb < 2 ? 0 : size_t(p.b_off) + size_t(p.nb) * kTileB;
+        p.b_slot = cap * kBK * 2;
+        p.nb = cap <= 64 ? 4 : 3;
+        p.r_off = kHead;
+        for (int nr = kMaxSlots; nr >= 2; --nr) {
+            p.nr = nr;
+            p.a_off = (kHead + nr * nmat * kRawMat + 1023) & ~1023;
+            p.b_off = p.a_off + p.na * nmat * kTileA;
+            const size_t smem = size_t(p.b_off) + size_t(p.nb) * p.b_slot;
+            if (smem <= size_t(optin)) return smem;
+        }
+        return 0;
     };
 
     // gate/up: A = gate and up rows (I per expert), B = x16 rows (slot p -> token p / k)
@@ -583,7 +596,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     if (!encode_raw_maps(&p.head0, &p.codes0, gate, E, I, H / kQK) ||
         !encode_raw_maps(&p.head1, &p.codes1, up, E, I, H / kQK))
         return cudaErrorInvalidValue;
-    size_t smem = rings(2, 4);
+    size_t smem = rings(2);
     if (smem == 0) return cudaErrorInvalidValue;
     grouped_gemm_kernel<<<num_sms, kThreads, smem, s>>>(p);
 
@@ -598,7 +611,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     if (!encode_raw_maps(&p.head0, &p.codes0, down, E, H, I / kQK)) return cudaErrorInvalidValue;
     p.head1 = p.head0;
     p.codes1 = p.codes0;
-    smem = rings(2, 4);
+    smem = rings(2);
     if (smem == 0) return cudaErrorInvalidValue;
     grouped_gemm_kernel<<<num_sms, kThreads, smem, s>>>(p);
     return cudaGetLastError();

@@ -40,3 +40,29 @@ def test_prefill_repeat_is_bitwise(m):
         m.moe_layer(d["x"], d["Wr"], d["bias"], d["gate"], d["up"], d["down"], s.k, s.I,
                     d["idx"], d["w"], d["y"], ws)
         np.testing.assert_array_equal(d["y"].cpu().numpy(), y1)
+
+
+def test_caller_routing_beyond_chunk_capacity(m, oracle):
+    """A small batch caps its chunks at the token count rounded up to 32 (64
+    here); a caller's routing that repeats experts gives experts 0 and 1 about
+    160 slots each, which the plan splits into several chunks."""
+    import torch
+    from tests.cases import y_tolerance
+    from tests.test_gpu_parity import DEV, to_dev
+    shape = synth.custom_shape(40, 512, 8, 8, 256, cfg_id=91)
+    assert m.moe_layer_launch_count(40, 512, 8, 8, 256) == 10  # tensor-core path, per-token router
+    case = layer_case(shape, 0, (0, 1, 17, 39))
+    rng = np.random.default_rng(91)
+    idx_np = rng.integers(0, 2, (40, 8)).astype(np.int32)
+    idx_np[::5, 3] = 5
+    w_np = rng.uniform(-1.0, 1.0, (40, 8)).astype(np.float32)
+    yo, skipped = oracle.ffn(case["x"], idx_np, w_np.astype(np.float64), case["blobs"]["gate"],
+                             case["blobs"]["up"], case["blobs"]["down"], shape.E, shape.I)
+    assert skipped == 0
+    d = to_dev(case)
+    ws = m.alloc_workspace(40, shape.H, shape.E, shape.k, shape.I, device=DEV)
+    m.moe_ffn(d["x"], torch.from_numpy(idx_np).to(DEV), torch.from_numpy(w_np).to(DEV),
+              d["gate"], d["up"], d["down"], shape.E, shape.I, d["y"], ws)
+    assert m.moe_read_device_status(ws)[0] == 0
+    y = d["y"].cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(y - yo)) <= y_tolerance(yo)
