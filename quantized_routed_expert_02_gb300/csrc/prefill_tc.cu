@@ -24,8 +24,9 @@
 //               at cap 256, up to 16 for small batches): these come from HBM
 //               and need the most latency cover;
 //   warps 4-11  dequantise them into fp16 K-major tiles with the 128-byte
-//               swizzle (generic stores, then a proxy fence), into a 2-slot
-//               ring of weight tiles;
+//               swizzle (generic stores, then a proxy fence), into a ring of
+//               weight tiles (2 slots; 4 when cap <= 64, where each stage's
+//               MMAs are short and the ring covers their completion latency);
 //   thread 64   loads the chunk's activation tile (its sorted rows rounded
 //               up to 32, x 64 K, fp16) with 2-D TMA copies of 32 rows that
 //               apply the 128-byte swizzle, into a ring of 3 slots of cap
@@ -571,7 +572,9 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     // the activation ring (3 slots of the chunk capacity, 4 for chunks of at
     // most 64 slots); the raw ring takes what is left, up to kMaxSlots stages.
     auto rings = [&](int nmat) -> size_t {
-        p.na = 2;
+        // small chunks make each stage's MMAs short, so the weight-tile ring
+        // must cover the MMA completion round trips: 4 slots instead of 2
+        p.na = cap <= 64 ? 4 : 2;
         p.b_slot = cap * kBK * 2;
         p.nb = cap <= 64 ? 4 : 3;
         p.r_off = kHead;

@@ -56,6 +56,63 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const float *__restr
 }
 
 // ---------------------------------------------------------------------------
+// 3..255 tokens: a CTA stages kXT tokens of x in shared memory (coalesced),
+// then each warp takes one expert row of Wr, requests its share of the row
+// in batches of four float4 per lane before any arithmetic, and dots it with
+// the staged tokens (fixed per-lane order, then a warp sum).
+// ---------------------------------------------------------------------------
+constexpr int kXT = 8;  // tokens per CTA
+constexpr int kRouterTileSmemMax = 128 * 1024;  // x tile of up to H = 4096
+
+__global__ void __launch_bounds__(256) router_tile_kernel(const float *__restrict__ x,
+                                                          const float *__restrict__ Wr,
+                                                          const float *__restrict__ bias, int T,
+                                                          int H, int E, float *__restrict__ logits) {
+    extern __shared__ __align__(16) float xt[];  // [kXT][H]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.y * kXT, n4 = H >> 2;
+    for (int i = threadIdx.x; i < kXT * n4; i += blockDim.x) {
+        const int tok = i / n4, c = i - tok * n4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t0 + tok < T) v = __ldg(reinterpret_cast<const float4 *>(x + size_t(t0 + tok) * H) + c);
+        reinterpret_cast<float4 *>(xt)[i] = v;
+    }
+    __syncthreads();
+    const int e = blockIdx.x * 8 + warp;
+    if (e >= E) return;
+    const float4 *wr = reinterpret_cast<const float4 *>(Wr + size_t(e) * H);
+    const float4 *x4 = reinterpret_cast<const float4 *>(xt);
+    float acc[kXT];
+#pragma unroll
+    for (int t = 0; t < kXT; ++t) acc[t] = 0.f;
+    for (int c0 = lane; c0 < n4; c0 += 4 * 32) {
+        float4 a[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            if (c0 + 32 * b < n4) a[b] = __ldg(wr + c0 + 32 * b);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int c = c0 + 32 * b;
+            if (c >= n4) break;
+#pragma unroll
+            for (int t = 0; t < kXT; ++t) {
+                const float4 v = x4[t * n4 + c];
+                acc[t] = fmaf(a[b].x, v.x, acc[t]);
+                acc[t] = fmaf(a[b].y, v.y, acc[t]);
+                acc[t] = fmaf(a[b].z, v.z, acc[t]);
+                acc[t] = fmaf(a[b].w, v.w, acc[t]);
+            }
+        }
+    }
+    const float b = bias ? bias[e] : 0.f;
+#pragma unroll
+    for (int t = 0; t < kXT; ++t) {
+        const float sum = warp_sum(acc[t]);
+        if (lane == 0 && t0 + t < T) logits[size_t(t0 + t) * E + e] = sum + b;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // One or two tokens: one CTA per expert row, each thread a strided quarter-
 // warp share of the row (float4 steps), reduced in a fixed order (warp
 // shuffles, then the eight warp sums in order), so every row of Wr is read
@@ -395,6 +452,9 @@ cudaError_t init_router() {
     cudaError_t err = cudaFuncSetAttribute(router_big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kRouterBigSmem);
     if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(router_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kRouterTileSmemMax);
+    if (err != cudaSuccess) return err;
     return cudaFuncSetAttribute(router_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kSplitSmem);
 }
@@ -413,6 +473,9 @@ cudaError_t launch_router(const float *x, const float *Wr, const float *bias, in
     }
     if (T <= 2) {
         router_row_kernel<2><<<E, blk, 0, s>>>(x, Wr, bias, T, H, E, logits);
+    } else if (size_t(kXT) * H * sizeof(float) <= size_t(kRouterTileSmemMax)) {
+        dim3 grid((E + 7) / 8, (T + kXT - 1) / kXT);
+        router_tile_kernel<<<grid, blk, size_t(kXT) * H * sizeof(float), s>>>(x, Wr, bias, T, H, E, logits);
     } else {
         dim3 grid((E + 7) / 8, (T + 7) / 8);
         router_logits_kernel<8><<<grid, blk, 0, s>>>(x, Wr, bias, T, H, E, logits);
