@@ -158,8 +158,8 @@ int moe_layer_launch_count(int T, int H, int E, int k, int I) {
     int sms = 0, dev = 0;
     if (device_info(&sms, &dev) != MOE_OK) return 0;
     if (decode_fused_supported(dev, T, H, E, k, I)) return 1;
-    if (decode_stream_supported(dev, T, H, E, k, I)) return 2 /* router */ + 2;
-    const int router = T >= 256 ? 1 : 2;
+    if (decode_stream_supported(dev, T, H, E, k, I)) return 1 /* router */ + 2;
+    const int router = (T >= 256 || T <= 2) ? 1 : 2;
     const int permutation = 3;  // count, scan, scatter
     if (prefill_tc_supported(T, H, E, k, I))
         return router + permutation + 2 /* fp16 rows, plan */ + 2 /* GEMMs */ + 1;
@@ -194,7 +194,7 @@ moe_status moe_router(const float *x, const float *Wr, const float *bias, int T,
     int sms = 0;
     MOE_TRY(device_info(&sms, nullptr));
     Ws W{static_cast<uint8_t *>(ws), L};
-    return cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits),
+    return cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(),
                                      static_cast<cudaStream_t>(stream)));
 }
 
@@ -274,7 +274,7 @@ moe_status moe_layer(const float *x, const float *Wr, const float *bias, const v
             static_cast<const uint8_t *>(up), static_cast<const uint8_t *>(down), H, E, k, I, y,
             W.u64(L.sync), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns, W.u64(L.o), W.timeline_cap(), s));
     }
-    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), s)));
+    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(), s)));
     if (decode_stream_supported(dev, T, H, E, k, I)) {
         return cuda_status(launch_decode_stream(
             x, idx, w, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),

@@ -33,7 +33,12 @@ struct WsHeader {
     unsigned long long rows_done;
     uint32_t tc_work[2];             // prefill GEMMs: next work item (gate/up, down)
     int32_t tc_chunks;               // prefill GEMMs: expert chunks of <= 256 slots
-    uint32_t pad[55];
+    uint32_t pad0;
+    // One- and two-token router: every CTA (one per expert) adds 1 once its
+    // logits are stored; the CTA whose add returns E - 1 ranks them and sets
+    // the count back to 0 for the next call.
+    unsigned long long router_rows;
+    uint32_t pad[52];
 };
 
 // One expert's chunk of at most 256 routed slots (prefill GEMM column tile).

@@ -113,50 +113,6 @@ __global__ void __launch_bounds__(256) router_tile_kernel(const float *__restric
 }
 
 // ---------------------------------------------------------------------------
-// One or two tokens: one CTA per expert row, each thread a strided quarter-
-// warp share of the row (float4 steps), reduced in a fixed order (warp
-// shuffles, then the eight warp sums in order), so every row of Wr is read
-// by 256 threads at once.
-// ---------------------------------------------------------------------------
-template <int kTT>
-__global__ void __launch_bounds__(256) router_row_kernel(const float *__restrict__ x,
-                                                         const float *__restrict__ Wr,
-                                                         const float *__restrict__ bias, int T,
-                                                         int H, int E, float *__restrict__ logits) {
-    __shared__ float part[kTT][8];
-    const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float4 *wr = reinterpret_cast<const float4 *>(Wr + size_t(e) * H);
-    float acc[kTT];
-#pragma unroll
-    for (int i = 0; i < kTT; ++i) acc[i] = 0.f;
-    for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
-        const float4 a = __ldg(wr + c);
-#pragma unroll
-        for (int i = 0; i < kTT; ++i) {
-            if (i < T) {
-                const float4 b = __ldg(reinterpret_cast<const float4 *>(x + size_t(i) * H) + c);
-                acc[i] = fmaf(a.x, b.x, acc[i]);
-                acc[i] = fmaf(a.y, b.y, acc[i]);
-                acc[i] = fmaf(a.z, b.z, acc[i]);
-                acc[i] = fmaf(a.w, b.w, acc[i]);
-            }
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < kTT; ++i) {
-        const float s = warp_sum(acc[i]);
-        if (lane == 0) part[i][warp] = s;
-    }
-    __syncthreads();
-    if (threadIdx.x < kTT && int(threadIdx.x) < T) {
-        const int i = threadIdx.x;
-        float s = 0.f;
-        for (int w = 0; w < 8; ++w) s += part[i][w];
-        logits[size_t(i) * E + e] = s + (bias ? bias[e] : 0.f);
-    }
-}
-
-// ---------------------------------------------------------------------------
 // Top-k + renormalise: one warp per token.  Lane L holds logits of experts
 // L, L+32, ...; k rounds of a warp-wide arg-max with the order (value
 // descending, index ascending).
@@ -227,6 +183,66 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;
     warp_topk(logits + size_t(t) * E, E, k, idx + size_t(t) * k, w + size_t(t) * k);
+}
+
+// ---------------------------------------------------------------------------
+// One or two tokens: one CTA per expert row, each thread a strided share of
+// the row (float4 steps), reduced in a fixed order (warp shuffles, then the
+// eight warp sums in order), so every row of Wr is read by 256 threads at
+// once.  The last CTA to store its logits ranks them (top-k + renormalise):
+// one launch for the whole router.
+// ---------------------------------------------------------------------------
+template <int kTT>
+__global__ void __launch_bounds__(256) router_row_kernel(const float *__restrict__ x,
+                                                         const float *__restrict__ Wr,
+                                                         const float *__restrict__ bias, int T,
+                                                         int H, int E, int k,
+                                                         float *__restrict__ logits,
+                                                         int32_t *__restrict__ idx,
+                                                         float *__restrict__ w, WsHeader *hdr) {
+    __shared__ float part[kTT][8];
+    __shared__ float lg[kTT][kMaxE];
+    __shared__ int last;
+    const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float4 *wr = reinterpret_cast<const float4 *>(Wr + size_t(e) * H);
+    float acc[kTT];
+#pragma unroll
+    for (int i = 0; i < kTT; ++i) acc[i] = 0.f;
+    for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
+        const float4 a = __ldg(wr + c);
+#pragma unroll
+        for (int i = 0; i < kTT; ++i) {
+            if (i < T) {
+                const float4 b = __ldg(reinterpret_cast<const float4 *>(x + size_t(i) * H) + c);
+                acc[i] = fmaf(a.x, b.x, acc[i]);
+                acc[i] = fmaf(a.y, b.y, acc[i]);
+                acc[i] = fmaf(a.z, b.z, acc[i]);
+                acc[i] = fmaf(a.w, b.w, acc[i]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kTT; ++i) {
+        const float s = warp_sum(acc[i]);
+        if (lane == 0) part[i][warp] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < kTT && int(threadIdx.x) < T) {
+        const int i = threadIdx.x;
+        float s = 0.f;
+        for (int ww = 0; ww < 8; ++ww) s += part[i][ww];
+        logits[size_t(i) * E + e] = s + (bias ? bias[e] : 0.f);
+        __threadfence();  // the logit is visible GPU-wide before this CTA is counted
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(&hdr->router_rows, 1ull) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    for (int i = threadIdx.x; i < T * E; i += blockDim.x) lg[i / E][i % E] = __ldcg(logits + i);
+    __syncthreads();
+    if (warp < T) warp_topk(&lg[warp][0], E, k, idx + size_t(warp) * k, w + size_t(warp) * k);
+    if (threadIdx.x == 0) atomicExch(&hdr->router_rows, 0ull);  // every CTA has counted itself
 }
 
 // ---------------------------------------------------------------------------
@@ -460,7 +476,8 @@ cudaError_t init_router() {
 }
 
 cudaError_t launch_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
-                          int k, int32_t *idx, float *w, float *logits, cudaStream_t s) {
+                          int k, int32_t *idx, float *w, float *logits, WsHeader *hdr,
+                          cudaStream_t s) {
     dim3 blk(256);
     if (T >= 256 && E <= kSE && H % (kSplit * kSK) == 0) {
         dim3 grid((T + kST - 1) / kST, kSplit);
@@ -472,8 +489,10 @@ cudaError_t launch_router(const float *x, const float *Wr, const float *bias, in
         return cudaGetLastError();
     }
     if (T <= 2) {
-        router_row_kernel<2><<<E, blk, 0, s>>>(x, Wr, bias, T, H, E, logits);
-    } else if (size_t(kXT) * H * sizeof(float) <= size_t(kRouterTileSmemMax)) {
+        router_row_kernel<2><<<E, blk, 0, s>>>(x, Wr, bias, T, H, E, k, logits, idx, w, hdr);
+        return cudaGetLastError();
+    }
+    if (size_t(kXT) * H * sizeof(float) <= size_t(kRouterTileSmemMax)) {
         dim3 grid((E + 7) / 8, (T + kXT - 1) / kXT);
         router_tile_kernel<<<grid, blk, size_t(kXT) * H * sizeof(float), s>>>(x, Wr, bias, T, H, E, logits);
     } else {
