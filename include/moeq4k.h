@@ -108,7 +108,8 @@ MOE_API int moe_layer_launch_count(int T, int H, int E, int k, int I);
  * tagged values that single-token calls keep between calls: the first
  * min(ws_bytes, 256 B + 2 KB) bytes.  Call once after allocating a
  * workspace, before its first use (single-token calls rely on that region
- * starting at zero), and whenever the sticky status should be cleared.  A
+ * and the one- and two-token router on a header count starting at zero),
+ * and whenever the sticky status should be cleared.  A
  * workspace large enough for several shapes may serve all of them.
  * Enqueued on `stream`.
  */
@@ -118,7 +119,9 @@ MOE_API moe_status moe_workspace_init(void *ws_dev, size_t ws_bytes, void *strea
  * Router (logits, softmax, top-k, renormalise) for T tokens.
  *  x_dev [T,H] fp32, Wr_dev [E,H] fp32, bias_dev [E] fp32 or NULL.
  *  Writes idx_dev [T,k] int32 (descending logit, ties -> lowest index) and
- *  w_dev [T,k] fp32 (sums to 1 per token).
+ *  w_dev [T,k] fp32 (sums to 1 per token).  The workspace must have been
+ *  initialised (moe_workspace_init); calls that share a workspace must not
+ *  overlap on the GPU (true of every call taking a workspace).
  */
 MOE_API moe_status moe_router(const float *x_dev, const float *Wr_dev, const float *bias_dev,
                       int T, int H, int E, int k,
@@ -186,7 +189,7 @@ MOE_API moe_status moe_read_device_status(const void *ws_dev, void *stream, int3
  * moe_layer for one token without any workspace, for callers that cannot
  * allocate device memory (for example a plugin whose host framework owns
  * every device allocation, or a decode loop that must not reach an
- * allocator on its hot path).  The paper has no counterpart: it exists for
+ * allocator on its hot path).  No step of the layer needs it: it exists for
  * those callers only.  Same arguments as moe_layer with T = 1 and no
  * workspace; x, weights, idx, w and y are still the caller's device buffers.
  *
