@@ -54,6 +54,25 @@ def parse_args():
     return ap.parse_args()
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(value, dist=None, device="cpu"):
+    """The largest `value` over all ranks (every rank receives it); the value
+    itself without a process group."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, seconds):
+    """Units per second of the whole job: each of `world` replicas processed
+    `units_per_rank`, and the job took the slowest rank's `seconds`."""
+    return units_per_rank * world / seconds
+
+
 # ---------------------------------------------------------------- inputs
 
 def _gen_layer(job):
@@ -349,14 +368,10 @@ def main():
     code, detail = m.moe_read_device_status(ws, stream)
     if code != 0:  # a device-side error or time-out inside the timed region voids the number
         raise RuntimeError(f"device status after the timed region: {m.status_str(code)} ({detail})")
-    ms = start.elapsed_time(end)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), dist, dev)
     ms_per_step = ms / args.steps
     tokens_per_step = T * n_layers
-    value = tokens_per_step * args.steps * world / (ms / 1e3)
+    value = whole_job_rate(tokens_per_step * args.steps, world, ms / 1e3)
 
     # end to end through the host-buffer entry point (copies inside the timed region)
     e2e = None
@@ -372,12 +387,8 @@ def main():
             for L in layers:
                 m.moe_layer_host(L["x_host"], L["Wr"], bias, L["gate"], L["up"], L["down"], k, I,
                                  L["idx"], L["w"], y_host, ws_host, stream=stream)
-        dt = time.perf_counter() - t0
-        if dist is not None:
-            t = torch.tensor([dt], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": T * n_layers * e2e_steps * world / dt, "unit": "tokens/s",
+        dt = max_over_ranks(time.perf_counter() - t0, dist, dev)
+        e2e = {"value": whole_job_rate(T * n_layers * e2e_steps, world, dt), "unit": "tokens/s",
                "h2d_bytes_per_step": n_layers * T * H * 4,
                "d2h_bytes_per_step": n_layers * T * H * 4}
 
