@@ -23,7 +23,6 @@
 // above the CTA's 512 threads) take fp32 fallbacks with the same results up
 // to rounding: warp per (slot, row) for gate/up, warp per output row for
 // down.  Weights are read once per call with read-only 16-byte loads.
-#include "async_copy.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
 #include "q4k_dot.cuh"

@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
     uint32_t gs = 0;     // stages processed by this CTA (same count in every role)
     uint32_t items = 0;  // items processed by this CTA
+    uint32_t issued = 0; // threads 32 and 64: stages whose copies this thread issued
     while (true) {
         if (tid == 0) info[0] = int(atomicAdd(&p.hdr->tc_work[p.mode], 1u));
         __syncthreads();
@@ -324,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     break;
                 }
                 mbar_arrive_expect_tx(bfull + bs, nbox * kBoxB);
+                ++issued;
                 for (int i = 0; i < nbox; ++i)
                     tma_load_2d(bring + size_t(bs) * p.b_slot + i * kBoxB, &p.mapB, s * kBK,
                                 row0 + i * kBoxRows, bfull + bs);
@@ -341,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 uint8_t *dst = rring + size_t(rs) * nmat * kRawMat;
                 const int xh = (s >> 2) * kBlockBytes, xq = xh + 16 + 32 * (s & 3);
                 mbar_arrive_expect_tx(rfull + rs, nmat * kRawMat);
+                ++issued;
                 tma_load_2d(dst, &p.head0, xh, y, rfull + rs);
                 tma_load_2d(dst + kRawHead, &p.codes0, xq, y, rfull + rs);
                 tma_load_2d(dst + kRawMat, &p.head1, xh, y + p.y_off1, rfull + rs);
@@ -403,7 +406,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         tc::commit_arrive(drain);
         wait_bar(drain, 0, global_timer_ns() + p.wait_ns, p.hdr, 15);
     }
-    cp_async_wait_all();
+    // After a timed-out wait the consumers may have left copies unawaited:
+    // each copying thread waits (bounded) for the last phase it started on
+    // every slot of its ring, so no copy still targets this CTA's shared
+    // memory when it exits.  (Without a time-out every phase was consumed.)
+    if (info[1] && (tid == 32 || tid == 64)) {
+        uint64_t *bars = tid == 32 ? rfull : bfull;
+        const uint32_t n = tid == 32 ? uint32_t(NR) : uint32_t(NB);
+        const uint64_t limit = global_timer_ns() + p.wait_ns;
+        for (uint32_t i = 0; i < n && i < issued; ++i) {
+            const uint32_t g = issued - 1 - i;
+            wait_bar(bars + g % n, (g / n) & 1, limit, p.hdr, 19);
+        }
+    }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
