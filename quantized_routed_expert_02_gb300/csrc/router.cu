@@ -235,7 +235,9 @@ __global__ void __launch_bounds__(256) router_row_kernel(const float *__restrict
         __threadfence();  // the logit is visible GPU-wide before this CTA is counted
     }
     __syncthreads();
-    if (threadIdx.x == 0) last = atomicAdd(&hdr->router_rows, 1ull) == gridDim.x - 1;
+    // exactly one CTA of the call sees E - 1 modulo E, whatever value the
+    // count held before the call (it is set back to 0 below)
+    if (threadIdx.x == 0) last = atomicAdd(&hdr->router_rows, 1ull) % gridDim.x == gridDim.x - 1;
     __syncthreads();
     if (!last) return;
     __threadfence();
