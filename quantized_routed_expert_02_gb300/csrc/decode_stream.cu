@@ -14,11 +14,13 @@
 //            round's loads issued before this round's arithmetic), dots them
 //            with dp4a, and leaves the partial sums in shared memory, where
 //            one warp per row adds them in a fixed order;
-//   down     the same with the concatenated h_1..h_k (k*I/64 units): a
-//            thread's unit belongs to one slot j, so it dots row r of
-//            Wd[e_j]; the warp that finishes row r sums each slot's units
-//            and folds o_j into y[r] = sum_j w_j o_j in slot order, so no o
-//            buffer and no separate combine pass exist.
+//   down     the concatenated h_1..h_k (k*I/64 units) as digit planes; a
+//            warp per output row r, lanes over the units (a unit belongs to
+//            one slot j and dots row r of Wd[e_j]), all of a lane's row bytes
+//            requested before its arithmetic, the digits read from shared
+//            memory at the dot; y[r] = sum over units of w_j times the unit's
+//            dot, one fixed-order warp sum: no o buffer, no combine pass and
+//            no CTA-wide barrier after the staging.
 // Shapes the digit layout does not cover (H not a power of two, or k*I/64
 // above the CTA's 512 threads) take fp32 fallbacks with the same results up
 // to rounding: warp per (slot, row) for gate/up, warp per output row for
@@ -35,7 +37,6 @@ constexpr int kGuBlocksPerSm = 2;
 constexpr int kDnThreads = 512;
 constexpr int kDnPairsInFlight = 4;  // per lane: slots x blocks of down rows loaded together
 constexpr int kDgThreads = 512;      // digit kernels: one thread per unit of the vector
-constexpr int kDnRowsPerThread = 2;  // down digit kernel: rows per thread and round
 
 // The 48 bytes a lane needs for sub-blocks 2c and 2c+1 of one block: the
 // block head and the 32 code bytes qs[32c .. 32c+31].
@@ -312,107 +313,119 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     }
 }
 
-// y[r] = sum_j w_j (Wd[e_j][r] . h_j) with h_1..h_k as one digit vector of
-// n = k*I elements: thread t < Q*UD owns unit t % UD (UD = n/64 <= 512) and
-// kDnRowsPerThread rows per round.
+// Dot of sub-blocks 2c and 2c+1 of one block with unit u of a digit vector
+// read straight from the shared planes (the digits of a unit are not kept in
+// registers: a lane visits several units per row).  Same integer sums and
+// scalings as pair_dot_digits.
+__device__ __forceinline__ float pair_dot_digits_smem(const Pair &P, int c, const uint8_t *planes,
+                                                      int plane_bytes, int nunits, int u,
+                                                      const float *scales, const float *sums) {
+    const uint32_t w[8] = {P.qa.x, P.qa.y, P.qa.z, P.qa.w, P.qb.x, P.qb.y, P.qb.z, P.qb.w};
+    int a0 = 0, b0 = 0, c0 = 0, a1 = 0, b1 = 0, c1 = 0;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        // chunk `half` holds the low sub-block's elements 16 half ..; chunk
+        // 2 + half the high sub-block's
+        const uint8_t *lo_ch = planes + (half * nunits + u) * 16;
+        const uint8_t *hi_ch = planes + ((2 + half) * nunits + u) * 16;
+        const uint4 la = *reinterpret_cast<const uint4 *>(lo_ch);
+        const uint4 lb = *reinterpret_cast<const uint4 *>(lo_ch + plane_bytes);
+        const uint4 lc = *reinterpret_cast<const uint4 *>(lo_ch + 2 * plane_bytes);
+        const uint4 ha = *reinterpret_cast<const uint4 *>(hi_ch);
+        const uint4 hb = *reinterpret_cast<const uint4 *>(hi_ch + plane_bytes);
+        const uint4 hc = *reinterpret_cast<const uint4 *>(hi_ch + 2 * plane_bytes);
+        const uint32_t da[4] = {la.x, la.y, la.z, la.w}, db[4] = {lb.x, lb.y, lb.z, lb.w},
+                       dc[4] = {lc.x, lc.y, lc.z, lc.w};
+        const uint32_t ea[4] = {ha.x, ha.y, ha.z, ha.w}, eb[4] = {hb.x, hb.y, hb.z, hb.w},
+                       ec[4] = {hc.x, hc.y, hc.z, hc.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t q = w[4 * half + i];
+            const uint32_t lo = q & 0x0F0F0F0Fu, hi = q & 0xF0F0F0F0u;
+            a0 = dp4a_us(lo, da[i], a0);
+            b0 = dp4a_us(lo, db[i], b0);
+            c0 = dp4a_us(lo, dc[i], c0);
+            a1 = dp4a_us(hi, ea[i], a1);
+            b1 = dp4a_us(hi, eb[i], b1);
+            c1 = dp4a_us(hi, ec[i], c1);
+        }
+    }
+    const int r0 = (64 * u) >> 5;
+    const float qx0 = scales[r0] * fmaf(float(c0), 1.0f / 254.0f, float(254 * a0 + b0));
+    const float qx1 = scales[r0 + 1] * 0.0625f * fmaf(float(c1), 1.0f / 254.0f, float(254 * a1 + b1));
+    float A0, B0, A1, B1;
+    pair_scales(P.head, c, 1.0f, A0, B0, A1, B1);
+    float acc = A0 * qx0;
+    acc = fmaf(-B0, sums[r0], acc);
+    acc = fmaf(A1, qx1, acc);
+    acc = fmaf(-B1, sums[r0 + 1], acc);
+    return acc;
+}
+
+// y[r] = sum over the n/64 units u of the concatenated h digits of
+// w_{j(u)} * (unit u of row r of Wd[e_j] . h_j): a warp per output row,
+// lanes over units (unit lane + 32 g), all of a lane's G units requested
+// before any arithmetic; one fixed-order warp sum per row.  The CTA's rows
+// are a contiguous share, so its warps read consecutive rows of every
+// expert at once.  No CTA-wide barrier after the staging.
+template <int G>
 __global__ void __launch_bounds__(kDgThreads, 1)
-    stream_down_digits_kernel(const float *__restrict__ h, const uint8_t *__restrict__ down,
-                              const int32_t *__restrict__ idx, const float *__restrict__ w, int k,
-                              int E, int H, int I, float *__restrict__ y, WsHeader *hdr) {
+    stream_down_rows_kernel(const float *__restrict__ h, const uint8_t *__restrict__ down,
+                            const int32_t *__restrict__ idx, const float *__restrict__ w, int k,
+                            int E, int H, int I, float *__restrict__ y, WsHeader *hdr) {
     extern __shared__ __align__(16) uint8_t smd[];
-    constexpr int RB = kDnRowsPerThread;
-    const int n = k * I, UD = n >> 6, upr = I >> 6, Q = kDgThreads / UD;
+    const int n = k * I, UD = n >> 6, upr = I >> 6;
     uint8_t *planes = smd;                                      // 3n bytes
     float *hscale = reinterpret_cast<float *>(smd + 3 * size_t(n));
     float *hsum = hscale + n / 32;
-    float *P = hsum + n / 32;                                   // [2][Q*RB][UD]
-    float *wj = P + 2 * RB * kDgThreads;                        // [k]
+    float *wj = hsum + n / 32;                                  // [k]
     int *eid = reinterpret_cast<int *>(wj + k);                 // [k]
     load_experts(idx, k, E, eid, hdr);
     for (int j = threadIdx.x; j < k; j += blockDim.x) wj[j] = w[j];
-    __syncthreads();
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
-    const bool active = tid < Q * UD;
-    const int u = tid % UD, q = tid / UD;
-    const int j = u / upr, uin = u - j * upr, sb = uin >> 2, c = uin & 3;
-    const int e = active ? eid[j] : -1;
-    const size_t row_bytes = size_t(I / kQK) * kBlockBytes, mat = size_t(H) * row_bytes;
-    const uint8_t *base = down + (e >= 0 ? size_t(e) * mat : 0) + size_t(sb) * kBlockBytes;
-    int r0, r1;
-    cta_share(H, &r0, &r1);
-    const int per_round = Q * RB;
-    const int rounds = (r1 - r0 + per_round - 1) / per_round;
-
-    auto load = [&](int rd, Pair (&pr)[RB], bool (&ok)[RB]) {
-#pragma unroll
-        for (int b = 0; b < RB; ++b) {
-            const int r = r0 + rd * per_round + q * RB + b;
-            ok[b] = e >= 0 && r < r1;
-            if (ok[b]) pr[b] = load_pair(base + size_t(r) * row_bytes, c);
-        }
-    };
-    // the first round's rows are requested before h is converted
-    Pair cur[RB], nxt[RB];
-    bool cok[RB] = {}, nok[RB] = {};
-    if (rounds > 0) load(0, cur, cok);
     stage_digits(h, n, planes, hscale, hsum);
     __syncthreads();
-    XDigits X;
-    if (active) load_digits(X, planes, n, UD, u, hscale, hsum);
-    for (int rd = 0; rd < rounds; ++rd) {
-        if (rd + 1 < rounds) {
-            load(rd + 1, nxt, nok);
-        } else {
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const size_t row_bytes = size_t(I / kQK) * kBlockBytes, mat = size_t(H) * row_bytes;
+    int r0, r1;
+    cta_share(H, &r0, &r1);
+    for (int r = r0 + warp; r < r1; r += nw) {
+        float acc = 0.f;
+        for (int u0 = 0; u0 < UD; u0 += 32 * G) {
+            Pair P[G];
+            bool ok[G];
 #pragma unroll
-            for (int b = 0; b < RB; ++b) nok[b] = false;
-        }
-        float *Pb = P + (rd & 1) * (RB * kDgThreads);
-        if (active) {
-#pragma unroll
-            for (int b = 0; b < RB; ++b)
-                Pb[(q * RB + b) * UD + u] = cok[b] ? pair_dot_digits(cur[b], c, X) : 0.f;
-        }
-        __syncthreads();  // also orders the reuse of the other buffer two rounds on
-        for (int ri = warp; ri < per_round; ri += nw) {
-            const int r = r0 + rd * per_round + ri;
-            if (r >= r1) break;
-            // eight slots' butterflies interleaved, then o_j folded in slot order
-            float acc = 0.f;
-            for (int j0 = 0; j0 < k; j0 += 8) {
-                float part[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    part[t] = 0.f;
-                    if (j0 + t < k)
-                        for (int v = lane; v < upr; v += 32) part[t] += Pb[ri * UD + (j0 + t) * upr + v];
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) part[t] += __shfl_xor_sync(0xffffffffu, part[t], o);
-#pragma unroll
-                for (int t = 0; t < 8; ++t)
-                    if (j0 + t < k && eid[j0 + t] >= 0) acc = fmaf(wj[j0 + t], part[t], acc);
+            for (int g = 0; g < G; ++g) {
+                const int u = u0 + lane + 32 * g;
+                const int j = u / upr, uin = u - j * upr;
+                ok[g] = u < UD && eid[min(j, k - 1)] >= 0;
+                if (ok[g])
+                    P[g] = load_pair(down + size_t(eid[j]) * mat + size_t(r) * row_bytes +
+                                         size_t(uin >> 2) * kBlockBytes,
+                                     uin & 3);
             }
-            if (lane == 0) y[r] = acc;
-        }
 #pragma unroll
-        for (int b = 0; b < RB; ++b) {
-            cur[b] = nxt[b];
-            cok[b] = nok[b];
+            for (int g = 0; g < G; ++g) {
+                if (!ok[g]) continue;
+                const int u = u0 + lane + 32 * g;
+                const int j = u / upr, uin = u - j * upr;
+                acc = fmaf(wj[j], pair_dot_digits_smem(P[g], uin & 3, planes, n, UD, u, hscale, hsum),
+                           acc);
+            }
         }
+        acc = warp_sum(acc);
+        if (lane == 0) y[r] = acc;
     }
 }
 
 bool gateup_digits_ok(int H) { return H >= 256 && H <= 64 * kDgThreads && (H & (H - 1)) == 0; }
-bool down_digits_ok(int k, int I) { return size_t(k) * I <= size_t(64) * kDgThreads; }
+bool down_digits_ok(int k, int I) { return size_t(k) * I <= size_t(64) * 512; }
 size_t gateup_digits_smem(int H, int k) {
     return 3 * size_t(H) + sizeof(float) * (H / 16 + 4 * kDgThreads) + sizeof(int) * k;
 }
 size_t down_digits_smem(int k, int I) {
     const size_t n = size_t(k) * I;
-    return 3 * n + sizeof(float) * (n / 16 + 2 * kDnRowsPerThread * kDgThreads + k) + sizeof(int) * k;
+    return 3 * n + sizeof(float) * (n / 16 + k) + sizeof(int) * k;
 }
 
 size_t gateup_smem(int H, int k) { return sizeof(float) * (padded_len(H) + H / 32) + sizeof(int) * k; }
@@ -439,8 +452,16 @@ cudaError_t init_decode_stream(int dev) {
         err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (err != cudaSuccess) return err;
     }
-    return cudaFuncSetAttribute(stream_down_digits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                optin);
+    const void *rows[] = {reinterpret_cast<const void *>(stream_down_rows_kernel<1>),
+                          reinterpret_cast<const void *>(stream_down_rows_kernel<2>),
+                          reinterpret_cast<const void *>(stream_down_rows_kernel<4>),
+                          reinterpret_cast<const void *>(stream_down_rows_kernel<6>),
+                          reinterpret_cast<const void *>(stream_down_rows_kernel<8>)};
+    for (const void *f : rows) {
+        err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
 }
 
 bool decode_stream_supported(int dev, int T, int H, int E, int k, int I) {
@@ -470,9 +491,20 @@ cudaError_t launch_decode_stream(const float *x, const int32_t *idx, const float
         stream_gateup_kernel<2><<<gg, kGuThreads, sg, s>>>(x, gate, up, idx, k, E, H, I, hbuf, hdr);
     else
         stream_gateup_kernel<4><<<gg, kGuThreads, sg, s>>>(x, gate, up, idx, k, E, H, I, hbuf, hdr);
-    if (down_digits_ok(k, I))
-        stream_down_digits_kernel<<<num_sms, kDgThreads, down_digits_smem(k, I), s>>>(
-            hbuf, down, idx, w, k, E, H, I, y, hdr);
+    if (down_digits_ok(k, I)) {
+        const int ud = k * I / 64;  // units per output row; lanes take ceil(ud / 32) each
+        const size_t sdd = down_digits_smem(k, I);
+        if (ud <= 32)
+            stream_down_rows_kernel<1><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+        else if (ud <= 64)
+            stream_down_rows_kernel<2><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+        else if (ud <= 128)
+            stream_down_rows_kernel<4><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+        else if (ud <= 192)
+            stream_down_rows_kernel<6><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+        else
+            stream_down_rows_kernel<8><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+    }
     else if (nbi <= 1)
         stream_down_kernel<1><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
     else if (nbi <= 2)
