@@ -71,3 +71,23 @@ def test_reference_arm_prints_on_rank_zero_only(capsys):
         config, steps, warmup, gpus = "tiny", 1, 0, 2
     bench.run_reference(A, rank=1, world=2)
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line(capsys):
+    """The reference arm (the oracle on the host cores) prints one JSON line
+    with the contract's keys, on the same metric and workload as the GPU arm."""
+    import json
+    import bench
+
+    class A:
+        config, steps, warmup, gpus = "tiny", 1, 0, 1
+    bench.run_reference(A, rank=0, world=1)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["metric"] == "MoE FFN tokens/s (one layer)" and line["unit"] == "tokens/s"
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "tiny"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s",
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
