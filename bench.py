@@ -4,28 +4,40 @@
 One step is one pass of the layer (router -> permutation -> gate/up+SwiGLU
 -> down -> slot-ordered combine) over every layer of a rotation of
 independently seeded layers, i.e. `layers` calls of moe_layer with T tokens
-each.  The rotation's weights (48 x 340 MB for the Qwen3-30B-A3B shape) are
-far larger than L2, and consecutive uses of one layer are separated by every
-other layer's traffic, so no L2 flush is needed.
+each.  The rotation's weights (48 x 340 MB for the Qwen3-30B-A3B shape,
+8 x 1.36 GB for the Qwen3-235B-A22B shape) are far larger than L2, and
+consecutive uses of one layer are separated by every other layer's traffic,
+so no L2 flush is needed.
+
+The headline workload (`--config`, default the Qwen3-30B-A3B single token)
+gives the line's top-level numbers, timed over exactly `--steps` steps.
+Every other workload (`--configs`, default all) is timed the same way in the
+same run and reported under `per_config`, each with its own roofline, clock
+record and CPU baseline.  The three Qwen3-30B-A3B workloads share one set of
+48 expert-weight layers and router matrices (the batched ones add their own
+activations, and the 64-token one its router bias); the two Qwen3-235B-A22B
+workloads share their 8 layers.
 
 Prints one JSON line (rank 0).  `value` is MoE-FFN tokens per second through
-one layer (T * layers_per_step * steps / time, summed over ranks); the
-roofline object compares the achieved algorithmic bytes per call (unique
-selected experts' Q4_K bytes + x + y + idx + w) with the measured HBM copy
-bandwidth.
+one layer (T * layers_per_step * steps / time, summed over ranks).  The
+roofline compares the achieved algorithmic bytes per call (unique selected
+experts' Q4_K bytes + x + y + idx + w) with the measured HBM copy bandwidth,
+or, where the tensor-core FLOPs bind, the achieved FLOP rate with the
+measured dense bf16 GEMM rate (burst: each step is milliseconds long).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--configs all|none|a,b]
   python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -37,6 +49,15 @@ import numpy as np  # noqa: E402
 from quantized_routed_expert_02_gb300 import synth  # noqa: E402
 
 DEFAULT_CONFIG = "a3b_decode"
+METRIC = "MoE FFN tokens/s (one layer)"
+# every workload, in the order they are reported
+ALL_CONFIGS = ("tiny", "a3b_decode", "a3b_batch64_zipf", "a3b_prefill", "a22b_decode",
+               "a22b_batch32")
+# the workload whose expert matrices and router weights a workload uses
+FAMILY = {"tiny": "tiny", "a3b_decode": "a3b_decode", "a3b_batch64_zipf": "a3b_decode",
+          "a3b_prefill": "a3b_decode", "a22b_decode": "a22b_decode",
+          "a22b_batch32": "a22b_decode"}
+MIN_REGION_S = 0.3   # per-config timed regions at least this long (clock samples inside)
 
 
 def parse_args():
@@ -45,10 +66,12 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.SHAPES))
+    ap.add_argument("--configs", default="all",
+                    help="other workloads timed in the same run: all, none, or a comma list")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--layers", type=int, default=0, help="override the rotation length")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0,
-                    help="bound on the oracle's CPU-baseline sample")
+    ap.add_argument("--layers", type=int, default=0, help="override every rotation's length")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="bound on the headline's oracle CPU-baseline sample (all cores)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -76,24 +99,33 @@ def whole_job_rate(units_per_rank, world, seconds):
 # ---------------------------------------------------------------- inputs
 
 def _gen_layer(job):
+    """(layer, x, Wr, blobs) of one layer of workload `name`; replicas (ranks)
+    draw their own activations over the same weights."""
     name, layer, rank = job
     shape = synth.SHAPES[name]
-    blobs = synth.expert_blobs(shape, layer)
-    Wr = synth.router_weights(shape, layer)
+    fam = synth.SHAPES[FAMILY[name]]
+    blobs = synth.expert_blobs(fam, layer)
+    Wr = synth.router_weights(fam, layer)
     x = synth.activations_fast(shape, layer + 7919 * rank)
     return layer, x, Wr, blobs
 
 
-def generate(name, n_layers, rank, workers):
-    import multiprocessing as mp
-    jobs = [(name, layer, rank) for layer in range(n_layers)]
+def _gen_weights(job):
+    fam_name, layer = job
+    fam = synth.SHAPES[fam_name]
+    return layer, synth.router_weights(fam, layer), synth.expert_blobs(fam, layer)
+
+
+def generate_weights(fam_name, n_layers, workers):
+    jobs = [(fam_name, layer) for layer in range(n_layers)]
     if workers <= 1 or n_layers == 1:
         for j in jobs:
-            yield _gen_layer(j)
+            yield _gen_weights(j)
         return
+    import multiprocessing as mp
     ctx = mp.get_context("spawn")
     with ctx.Pool(workers) as pool:
-        for r in pool.imap(_gen_layer, jobs):
+        for r in pool.imap(_gen_weights, jobs):
             yield r
 
 
@@ -130,19 +162,14 @@ class ClockSampler:
         self.thread = threading.Thread(target=self._reader, daemon=True)
         self.thread.start()
 
-    def stop(self, t0, t1):
+    def summary(self, t0, t1):
+        """Median SM clock and throttle reasons of the samples inside [t0, t1]
+        (the nearest ones when the region is shorter than the period)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        if self.thread is not None:
-            self.thread.join(timeout=2)
-        inside = [r for t, r in self.rows if t0 <= t <= t1]
-        # a region shorter than the sampling period: take the samples nearest to it
-        near = inside or [r for t, r in self.rows if t0 - 0.1 <= t <= t1 + 0.1]
+        rows = list(self.rows)
+        inside = [r for t, r in rows if t0 <= t <= t1]
+        near = inside or [r for t, r in rows if t0 - 0.1 <= t <= t1 + 0.1]
         sm, smax, reasons = [], None, set()
         for r in near:
             try:
@@ -157,74 +184,113 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm),
                 "samples_inside_timed_region": len(inside)}
 
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
 
-def profiled_traffic(kernel_src, profile):
-    """DRAM bytes per launch recorded by the ncu summary in profiles/, if that
-    summary was taken of the kernel source as it is now (hash match)."""
-    import hashlib
+
+def profiled_traffic(kernel_src, profile_json):
+    """DRAM bytes per launch recorded (from one ncu capture) in the data file
+    profiles/<profile_json>, if that capture was taken of the kernel source
+    as it is now (hash match); else None."""
     try:
         src = open(os.path.join(ROOT, kernel_src), "rb").read()
-        text = open(os.path.join(ROOT, "profiles", profile)).read()
-    except OSError:
+        with open(os.path.join(ROOT, "profiles", profile_json)) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    h = hashlib.sha256(src).hexdigest()[:16]
-    fields = dict(ln.split(":", 1) for ln in text.splitlines() if ":" in ln and not ln.startswith(" "))
-    if fields.get("source-sha256-16", "").strip() != h:
+    if rec.get("source_sha256_16") != hashlib.sha256(src).hexdigest()[:16]:
         return None
-    try:
-        return int(fields["dram_bytes_per_launch"].strip())
-    except (KeyError, ValueError):
-        return None
+    v = rec.get("dram_bytes_per_launch")
+    return int(v) if isinstance(v, (int, float)) else None
 
 
 def measured_peaks():
-    """(HBM GB/s, sustained dense bf16 TFLOP/s, kind) from MEASURED_PEAKS.json,
-    else the recipe's fallback figures."""
+    """HBM GB/s and dense bf16 TFLOP/s (burst and sustained) from
+    MEASURED_PEAKS.json, else the recipe's fallback figures."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return d.get("hbm_gbs"), d.get("bf16_tflops_sustained"), "measured"
-    return 6800.0, 1700.0, "fallback"
+        return dict(hbm=d.get("hbm_gbs"), tf_burst=d.get("bf16_tflops"),
+                    tf_sustained=d.get("bf16_tflops_sustained"), kind="measured")
+    return dict(hbm=6800.0, tf_burst=1900.0, tf_sustained=1700.0, kind="fallback")
 
 
 # ---------------------------------------------------------------- oracle (CPU) timing
 
-def oracle_sample(name, seconds, layers_available, rank=0):
-    """Time the fp64 oracle on whole layer calls of the workload until
-    `seconds` of CPU time have been spent (at least one call)."""
+def _oracle_inputs(name, layer, rank):
+    """One layer's inputs for the oracle; single-token layers generate only
+    the routed experts' matrices (the oracle never reads the others)."""
+    from oracle.oracle import Oracle
+    shape = synth.SHAPES[name]
+    fam = synth.SHAPES[FAMILY[name]]
+    Wr = synth.router_weights(fam, layer)
+    x = synth.activations_fast(shape, layer + 7919 * rank)
+    bias = synth.router_bias(shape)
+    experts = None
+    if shape.T * shape.k < shape.E:
+        r = Oracle().router(x, Wr, bias, shape.k)
+        experts = sorted(set(r["idx"].ravel().tolist()))
+    return x, Wr, bias, synth.expert_blobs(fam, layer, experts=experts)
+
+
+def oracle_sample(name, seconds, rank=0, threads=0, max_tokens=64, inputs=None):
+    """Time the fp64 oracle (router on every token, FFN on at most
+    `max_tokens` of them) on calls of one layer of the workload until
+    `seconds` of wall time have been spent (at least one call).  `threads` =
+    0: all host cores.  `inputs`: that layer's (x, Wr, bias, blobs)."""
     from oracle.oracle import Oracle
     shape = synth.SHAPES[name]
     o = Oracle()
-    calls, t_total, layer = 0, 0.0, 0
+    o.set_threads(threads if threads > 0 else (os.cpu_count() or 1))
+    used = o.max_threads()
     T = shape.T
     tokens = None
-    if T > 64:
-        # prefill: a bounded token subset of one layer per call
-        tokens = np.arange(0, T, max(1, T // 64), dtype=np.int32)[:64]
+    if T > max_tokens:
+        tokens = np.arange(0, T, max(1, T // max_tokens), dtype=np.int32)[:max_tokens]
+    ntok = T if tokens is None else len(tokens)
+    calls, t_total = 0, 0.0
+    if inputs is None:
+        inputs = _oracle_inputs(name, 0, rank)
+    x, Wr, bias, blobs = inputs
     while True:
-        _, x, Wr, blobs = _gen_layer((name, layer % max(1, layers_available), rank))
-        bias = synth.router_bias(shape)
         t0 = time.perf_counter()
         r = o.router(x, Wr, bias, shape.k)
         o.ffn(x, r["idx"], r["w"], blobs["gate"], blobs["up"], blobs["down"], shape.E, shape.I,
               tokens=tokens)
         t_total += time.perf_counter() - t0
         calls += 1
-        layer += 1
         if t_total >= seconds:
             break
-    ntok = T if tokens is None else len(tokens)
-    threads = min(o.max_threads(), ntok)
+    o.set_threads(os.cpu_count() or 1)
     return {
         "value": ntok * calls / t_total,
         "unit": "tokens/s",
-        "cores": threads,
+        "cores": used,
         "kind": "oracle",
         "sample": (f"{calls} layer call(s) of {name} (T={T}"
                    + (f", FFN on {ntok} of {T} tokens, router on all" if tokens is not None else "")
-                   + f"), fp64 C oracle, {t_total:.1f} s"),
+                   + f"), fp64 C oracle on {used} thread(s), {t_total:.1f} s"),
     }
+
+
+def cpu_baseline(name, seconds, rank=0):
+    """The oracle on all host cores, with a one-thread figure beside it."""
+    inputs = _oracle_inputs(name, 0, rank)
+    allc = oracle_sample(name, seconds, rank, threads=0, inputs=inputs)
+    one = oracle_sample(name, max(0.5, seconds / 2), rank, threads=1, max_tokens=8,
+                        inputs=inputs)
+    allc["host_cores"] = os.cpu_count()
+    allc["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
+    return allc
 
 
 def run_reference(args, rank, world):
@@ -234,12 +300,12 @@ def run_reference(args, rank, world):
     times = []
     last = None
     for step in range(args.warmup + args.steps):
-        last = oracle_sample(args.config, 0.0, 1, 0)
+        last = oracle_sample(args.config, 0.0, 0)
         if step >= args.warmup:
             times.append(last["value"])
     value = statistics.median(times)
     line = {
-        "impl": "reference", "metric": "MoE FFN tokens/s (one layer)", "value": value,
+        "impl": "reference", "metric": METRIC, "value": value,
         "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
@@ -255,6 +321,133 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------- GPU arm
 
+class Workload:
+    """One workload's rotation on the device: per layer the activations
+    (device and pinned host copies) and the outputs; the expert matrices and
+    router weights are the family's tensors, shared."""
+
+    def __init__(self, name, fam_layers, rank, dev, torch):
+        shape = synth.SHAPES[name]
+        self.name, self.shape = name, shape
+        T, H, k = shape.T, shape.H, shape.k
+        self.layers = []
+        for i, F in enumerate(fam_layers):
+            x = synth.activations_fast(shape, i + 7919 * rank)
+            self.layers.append(dict(
+                F, x=torch.from_numpy(x).to(dev), x_host=torch.from_numpy(x).pin_memory(),
+                idx=torch.empty(T, k, dtype=torch.int32, device=dev),
+                w=torch.empty(T, k, dtype=torch.float32, device=dev),
+                y=torch.empty(T, H, dtype=torch.float32, device=dev)))
+        b = synth.router_bias(shape)
+        self.bias = None if b is None else torch.from_numpy(b).to(dev)
+
+
+def time_workload(m, torch, W, steps, warmup, dev, dist, clocks, peaks):
+    """CUDA-graph one step (the whole rotation), warm it up, time `steps`
+    replays with CUDA events on the launching stream; returns the record."""
+    s = W.shape
+    T, H, E, k, I = s.T, s.H, s.E, s.k, s.I
+    n_layers = len(W.layers)
+    ws = m.alloc_workspace(T, H, E, k, I, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def one_step(st):
+        for L in W.layers:
+            m.moe_layer(L["x"], L["Wr"], W.bias, L["gate"], L["up"], L["down"], k, I,
+                        L["idx"], L["w"], L["y"], ws, stream=st)
+
+    with torch.cuda.stream(stream):
+        one_step(stream)
+    stream.synchronize()
+    code, detail = m.moe_read_device_status(ws, stream)
+    if code != 0:
+        raise RuntimeError(f"{W.name}: device status {m.status_str(code)} ({detail})")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        one_step(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            graph.replay()
+    torch.cuda.synchronize()
+
+    # algorithmic bytes of one step, from the routing each call made
+    per_expert = s.expert_bytes
+    act_bytes = T * H * 4 * 2 + T * k * 8
+    uniques = [int(torch.unique(L["idx"]).numel()) for L in W.layers]
+    step_bytes = sum(u * per_expert + act_bytes for u in uniques)
+    wr_bytes = n_layers * E * H * 4
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    if dist is not None:
+        dist.barrier()
+    time.sleep(0.05)  # let the sampler read the samples taken up to t1
+    clk = clocks.summary(t0, t1)
+    code, detail = m.moe_read_device_status(ws, stream)
+    if code != 0:  # a device-side error or time-out inside the timed region voids the number
+        raise RuntimeError(f"{W.name}: device status after the timed region: "
+                           f"{m.status_str(code)} ({detail})")
+    ms = max_over_ranks(start.elapsed_time(end), dist, dev)
+    call_us = ms * 1e3 / (steps * n_layers)
+    launches_per_call = m.moe_layer_launch_count(T, H, E, k, I)
+
+    # roofline: HBM bytes, or for the tensor-core path (T*k >= 256 routed
+    # slots) the slower of the bytes at the HBM peak and the expert FLOPs at
+    # the dense 16-bit tensor peak (fp16 operands; the dense fp16 and bf16
+    # peaks are equal on this part).  Each step is milliseconds long: the
+    # burst GEMM rate is the peak.
+    bytes_call = step_bytes / n_layers
+    achieved = bytes_call / (call_us * 1e-6) / 1e9
+    flops_call = 6.0 * T * k * H * I
+    tensor_path = T * k >= 256
+    hbm_floor_us = bytes_call / (peaks["hbm"] * 1e9) * 1e6
+    tensor_floor_us = flops_call / (peaks["tf_burst"] * 1e12) * 1e6
+    if tensor_path and tensor_floor_us > hbm_floor_us:
+        tf = flops_call / (call_us * 1e-6) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["tf_burst"],
+                    "unit": "TFLOP/s", "frac": round(tf / peaks["tf_burst"], 4), "traffic": None,
+                    "peak_kind": peaks["kind"] + " (burst dense bf16 GEMM)",
+                    "frac_of_sustained": round(tf / peaks["tf_sustained"], 4),
+                    "hbm_frac": round(achieved / peaks["hbm"], 4)}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4), "traffic": None,
+                    "peak_kind": peaks["kind"] + " (copy bandwidth)"}
+    roofline.update({
+        "algorithmic_bytes_per_call": bytes_call,
+        "flops_per_call": flops_call,
+        "floor_us_per_call": round(max(hbm_floor_us, tensor_floor_us if tensor_path else 0.0), 3),
+        "achieved_incl_router_weight_gbs": round(
+            ((step_bytes + wr_bytes) / n_layers) / (call_us * 1e-6) / 1e9, 1),
+    })
+    rec = {
+        "workload": W.name, "T": T, "H": H, "E": E, "k": k, "I": I,
+        "layers_per_step": n_layers, "steps": steps,
+        "us_per_layer_call": round(call_us, 3),
+        "tokens_per_s": round(T / (call_us * 1e-6), 1),
+        "unique_experts_per_call": round(sum(uniques) / len(uniques), 2),
+        "launches_per_call": launches_per_call,
+        "gpu_launches": launches_per_call * n_layers * steps,
+        "dtype": "f16xf16->f32" if tensor_path else "f32",
+        "roofline": roofline,
+        "clocks": clk,
+        "_ms": ms, "_ws": ws, "_stream": stream,
+    }
+    del graph
+    return rec
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -264,8 +457,16 @@ def main():
         run_reference(args, rank, world)
         return
 
-    shape = synth.SHAPES[args.config]
-    n_layers = args.layers or shape.layers
+    if args.configs == "all":
+        others = [c for c in ALL_CONFIGS if c != args.config]
+    elif args.configs == "none":
+        others = []
+    else:
+        others = [c for c in args.configs.split(",") if c and c != args.config]
+        for c in others:
+            if c not in synth.SHAPES:
+                raise SystemExit(f"unknown workload {c}")
+    names = [args.config] + others
     workers = max(1, min(16, (os.cpu_count() or 2) // max(1, world)))
 
     import torch
@@ -278,185 +479,130 @@ def main():
 
     from quantized_routed_expert_02_gb300 import moeq4k as m
 
-    T, H, E, k, I = shape.T, shape.H, shape.E, shape.k, shape.I
-    layers = []
+    # expert matrices and router weights, once per family
     t_gen = time.perf_counter()
-    for layer, x, Wr, blobs in generate(args.config, n_layers, rank, workers):
-        L = dict(
-            x=torch.from_numpy(x).to(dev),
-            x_host=torch.from_numpy(x).pin_memory(),
-            Wr=torch.from_numpy(Wr).to(dev),
-            gate=torch.from_numpy(blobs["gate"]).to(dev),
-            up=torch.from_numpy(blobs["up"]).to(dev),
-            down=torch.from_numpy(blobs["down"]).to(dev),
-            idx=torch.empty(T, k, dtype=torch.int32, device=dev),
-            w=torch.empty(T, k, dtype=torch.float32, device=dev),
-            y=torch.empty(T, H, dtype=torch.float32, device=dev),
-        )
-        layers.append(L)
-        del blobs
+    families = {}
+    for name in names:
+        fam = FAMILY[name]
+        if fam in families:
+            continue
+        n_layers = args.layers or synth.SHAPES[fam].layers
+        fl = [None] * n_layers
+        for layer, Wr, blobs in generate_weights(fam, n_layers, workers):
+            fl[layer] = dict(Wr=torch.from_numpy(Wr).to(dev),
+                             gate=torch.from_numpy(blobs["gate"]).to(dev),
+                             up=torch.from_numpy(blobs["up"]).to(dev),
+                             down=torch.from_numpy(blobs["down"]).to(dev))
+            del blobs
+        families[fam] = fl
+    workloads = {n: Workload(n, families[FAMILY[n]], rank, dev, torch) for n in names}
     t_gen = time.perf_counter() - t_gen
-    b = synth.router_bias(shape)
-    bias = None if b is None else torch.from_numpy(b).to(dev)
-    ws = m.alloc_workspace(T, H, E, k, I, device=dev)
-    ws_host = m.alloc_workspace(T, H, E, k, I, device=dev, host_staging=True)
-    y_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
 
-    stream = torch.cuda.Stream(device=dev)
-
-    def one_step(s):
-        for L in layers:
-            m.moe_layer(L["x"], L["Wr"], bias, L["gate"], L["up"], L["down"], k, I,
-                        L["idx"], L["w"], L["y"], ws, stream=s)
-
-    # eager warm-up, then capture one step (the whole rotation) as a CUDA graph
-    with torch.cuda.stream(stream):
-        one_step(stream)
-    stream.synchronize()
-    code, detail = m.moe_read_device_status(ws, stream)
-    if code != 0:
-        raise RuntimeError(f"device status {m.status_str(code)} ({detail})")
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        one_step(stream)
-
-    # CUDAGraph.replay() launches on the current stream: make it `stream`
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            graph.replay()
-    torch.cuda.synchronize()
-
-    # algorithmic bytes of one step, from the routing each call made
-    per_expert = 2 * shape.gate_bytes + shape.down_bytes
-    act_bytes = T * H * 4 * 2 + T * k * 8
-    step_bytes = 0
-    uniques = []
-    for L in layers:
-        u = int(torch.unique(L["idx"]).numel())
-        uniques.append(u)
-        step_bytes += u * per_expert + act_bytes
-    wr_bytes = n_layers * E * H * 4
-
-    gpu_id = 0
+    gpu_id = str(local_rank)
     try:
         props = torch.cuda.get_device_properties(dev)
         gpu_id = str(props.uuid)
         if not gpu_id.startswith("GPU-"):
             gpu_id = "GPU-" + gpu_id
     except Exception:
-        gpu_id = str(local_rank)
+        pass
     clocks = ClockSampler(gpu_id)
-
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    t_region0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        end.record(stream)
-    torch.cuda.synchronize()
-    t_region1 = time.perf_counter()
-    if dist is not None:
-        dist.barrier()
-    clk = clocks.stop(t_region0, t_region1)
-    code, detail = m.moe_read_device_status(ws, stream)
-    if code != 0:  # a device-side error or time-out inside the timed region voids the number
-        raise RuntimeError(f"device status after the timed region: {m.status_str(code)} ({detail})")
-    ms = max_over_ranks(start.elapsed_time(end), dist, dev)
-    ms_per_step = ms / args.steps
-    tokens_per_step = T * n_layers
-    value = whole_job_rate(tokens_per_step * args.steps, world, ms / 1e3)
+    peaks = measured_peaks()
+
+    # the headline: exactly --steps steps
+    head = time_workload(m, torch, workloads[args.config], args.steps, args.warmup, dev, dist,
+                         clocks, peaks)
+    # the other workloads: at least --steps steps, and a timed region long
+    # enough to hold clock samples
+    per = {}
+    for name in others:
+        W = workloads[name]
+        probe = time_workload(m, torch, W, 2, 1, dev, dist, clocks, peaks)
+        step_s = probe["_ms"] / 2e3
+        steps = max(args.steps, int(math.ceil(MIN_REGION_S / max(step_s, 1e-6))))
+        per[name] = time_workload(m, torch, W, steps, args.warmup, dev, dist, clocks, peaks)
+    clocks.stop()
+
+    W = workloads[args.config]
+    s = W.shape
+    T, H, E, k, I = s.T, s.H, s.E, s.k, s.I
+    n_layers = len(W.layers)
+    value = whole_job_rate(T * n_layers * args.steps, world, head["_ms"] / 1e3)
+    ms_per_step = head["_ms"] / args.steps
+
+    # the single-token fused kernel is the only launch of its calls: its
+    # ncu DRAM bytes (recorded per source revision) are the call's traffic
+    if head["launches_per_call"] == 1 and args.config == "a3b_decode":
+        head["roofline"]["traffic"] = profiled_traffic(
+            "quantized_routed_expert_02_gb300/csrc/decode_fused.cu", "decode_fused_a3b_decode.json")
+        head["roofline"]["kernel"] = ("decode_fused_kernel (the only launch of a call; duration = "
+                                      "timed region / calls)")
+    else:
+        head["roofline"]["kernel"] = "moe_layer call (all launches of one call)"
 
     # end to end through the host-buffer entry point (copies inside the timed region)
     e2e = None
     if not args.no_e2e:
+        ws_host = m.alloc_workspace(T, H, E, k, I, device=dev, host_staging=True)
+        y_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
+        stream = head["_stream"]
         e2e_steps = max(1, min(args.steps, 10))
-        for L in layers[:2]:
-            m.moe_layer_host(L["x_host"], L["Wr"], bias, L["gate"], L["up"], L["down"], k, I,
+        for L in W.layers[:2]:
+            m.moe_layer_host(L["x_host"], L["Wr"], W.bias, L["gate"], L["up"], L["down"], k, I,
                              L["idx"], L["w"], y_host, ws_host, stream=stream)
         if dist is not None:
             dist.barrier()
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
-            for L in layers:
-                m.moe_layer_host(L["x_host"], L["Wr"], bias, L["gate"], L["up"], L["down"], k, I,
-                                 L["idx"], L["w"], y_host, ws_host, stream=stream)
+            for L in W.layers:
+                m.moe_layer_host(L["x_host"], L["Wr"], W.bias, L["gate"], L["up"], L["down"], k,
+                                 I, L["idx"], L["w"], y_host, ws_host, stream=stream)
         dt = max_over_ranks(time.perf_counter() - t0, dist, dev)
         e2e = {"value": whole_job_rate(T * n_layers * e2e_steps, world, dt), "unit": "tokens/s",
                "h2d_bytes_per_step": n_layers * T * H * 4,
-               "d2h_bytes_per_step": n_layers * T * H * 4}
+               "d2h_bytes_per_step": n_layers * T * H * 4,
+               "api": "moe_layer_host (pinned host x and y; copies and a synchronize per call)"}
 
-    peak, tflops_peak, peak_kind = measured_peaks()
-    call_us = ms_per_step * 1e3 / n_layers
-    achieved = (step_bytes / n_layers) / (call_us * 1e-6) / 1e9
-    single = m.moe_layer_launch_count(T, H, E, k, I) == 1
-    traffic = profiled_traffic("quantized_routed_expert_02_gb300/csrc/decode_fused.cu",
-                               "decode_fused_a3b_decode.md") if (single and args.config == "a3b_decode") else None
-    # The tensor-core path (T*k >= 256 routed slots) is a dense contraction: its roofline is
-    # the slower of the bytes at HBM peak and the FLOPs at the tensor peak
-    # (fp16 operands; the dense fp16 and bf16 peaks are equal on this part).
-    flops_per_call = 6.0 * T * k * H * I
-    tensor_path = T * k >= 256
-    hbm_floor_us = (step_bytes / n_layers) / (peak * 1e9) * 1e6
-    tensor_floor_us = flops_per_call / (tflops_peak * 1e12) * 1e6
-    if tensor_path and tensor_floor_us > hbm_floor_us:
-        tf = flops_per_call / (call_us * 1e-6) / 1e12
-        roofline = {"bound": "tensor", "achieved": round(tf, 1), "peak": tflops_peak,
-                    "unit": "TFLOP/s", "frac": round(tf / tflops_peak, 4), "traffic": None,
-                    "hbm_frac": round(achieved / peak, 4)}
-    else:
-        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "traffic": traffic}
-    roofline.update({
-        "kernel": ("decode_fused_kernel (the only launch of a call; duration = timed region / calls)"
-                   if single else "moe_layer call (all launches of one call)"),
-        "peak_kind": peak_kind + (" (sustained bf16 GEMM)" if roofline["bound"] == "tensor" else ""),
-        "algorithmic_bytes_per_call": step_bytes / n_layers,
-        "flops_per_call": flops_per_call,
-        "achieved_incl_router_weight": round(
-            ((step_bytes + wr_bytes) / n_layers) / (call_us * 1e-6) / 1e9, 1),
-    })
-
-    cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = oracle_sample(args.config, args.cpu_seconds, n_layers, rank)
+        head["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds, rank)
+        for name in others:
+            per[name]["cpu_baseline"] = cpu_baseline(name, 2.0, rank)
 
-    launches = m.moe_layer_launch_count(T, H, E, k, I) * n_layers * args.steps
+    def public(rec):
+        return {kk: v for kk, v in rec.items() if not kk.startswith("_")}
+
     if rank == 0:
         line = {
-            "metric": "MoE FFN tokens/s (one layer)",
+            "metric": METRIC,
             "value": round(value, 1),
             "unit": "tokens/s",
             "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 5),
-            "us_per_layer_call": round(call_us, 3),
+            "us_per_layer_call": head["us_per_layer_call"],
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f16xf16->f32" if tensor_path else "f32",
+            "dtype": head["dtype"],
             "data": "synthetic",
             "config": {
                 "workload": args.config, "T": T, "H": H, "E": E, "k": k, "I": I,
                 "layers_per_step": n_layers, "weights": "Q4_K",
-                "unique_experts_per_call": round(sum(uniques) / len(uniques), 2),
+                "unique_experts_per_call": head["unique_experts_per_call"],
                 "l2": "inputs larger than L2 (layer rotation, no flush)",
                 "parallelism": f"replicas x{world}",
                 "graph": "one CUDA graph per step",
                 "input_gen_s": round(t_gen, 1),
             },
-            "roofline": roofline,
-            "cpu_baseline": cpu,
+            "roofline": head["roofline"],
+            "cpu_baseline": head.get("cpu_baseline"),
             "e2e": e2e,
-            "gpu_launches": launches,
-            "clocks": clk,
+            "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"],
+            "per_config": {name: public(per[name]) for name in others},
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

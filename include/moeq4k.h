@@ -140,11 +140,18 @@ MOE_API moe_status moe_permute(const int32_t *idx_dev, int T, int k, int E,
                        void *ws_dev, size_t ws_bytes, void *stream);
 
 /*
- * Expert FFN and combine for a given routing.
+ * Expert FFN and combine for a given routing (forward_qwen3_moe.rs,
+ * aprender-serve 0.35.0, step 2h of forward_single_qwen3_moe_with_cache: the
+ * gate x up SwiGLU of each selected expert, weighted by the router weights
+ * and summed; doc of forward_qwen3_moe, argument `data`: each expert is a
+ * fused dequant + matvec over its Q4_K bytes in place).
  *  x_dev [T,H] fp32; idx_dev [T,k] int32; w_dev [T,k] fp32 (any values;
  *  they need not sum to 1); gate/up/down: Q4_K blobs as above.
  *  Writes y_dev [T,H] fp32: y[t] = sum_j w[t,j] * expert_{idx[t,j]}(x[t]),
  *  summed in slot order j = 0..k-1.  Duplicate experts in a row are legal.
+ *  An index outside [0,E) contributes nothing and sets the sticky status
+ *  MOE_ERR_EXPERT_RANGE (same page, Errors of forward_qwen3_moe: an
+ *  out-of-range expert is an error).  Argument errors as for every call.
  */
 MOE_API moe_status moe_ffn(const float *x_dev, const int32_t *idx_dev, const float *w_dev,
                    const void *gate_dev, const void *up_dev, const void *down_dev,

@@ -173,14 +173,26 @@ void moq_expert(const double *xv, const uint8_t *gate_e, const uint8_t *up_e,
                 const uint8_t *down_e, int H, int I, double *h, double *o)
 {
     int nsb_h = H / QK, nsb_i = I / QK;
-    double tmp[QK];
+    /* Rows are independent: when this runs outside a parallel region (fewer
+     * tokens than threads), the rows are shared out over the threads.  Each
+     * row's dot product is the same sequential sum either way. */
+#ifdef _OPENMP
+    int outer = !omp_in_parallel();
+#else
+    int outer = 0;
+#endif
+#pragma omp parallel for schedule(static) if (outer)
     for (int r = 0; r < I; r++) {
+        double tmp[QK];
         double g = row_dot(gate_e + (long)r * nsb_h * BLK, H, xv, tmp);
         double u = row_dot(up_e + (long)r * nsb_h * BLK, H, xv, tmp);
         h[r] = g / (1.0 + exp(-g)) * u;
     }
-    for (int r = 0; r < H; r++)
+#pragma omp parallel for schedule(static) if (outer)
+    for (int r = 0; r < H; r++) {
+        double tmp[QK];
         o[r] = row_dot(down_e + (long)r * nsb_i * BLK, I, h, tmp);
+    }
 }
 
 /*
@@ -198,7 +210,14 @@ long moq_ffn(const float *x, const int32_t *idx, const double *w,
     long down_bytes = (long)H * (I / QK) * BLK;
     int n = tokens ? ntok : T;
     long skipped = 0;
-#pragma omp parallel for schedule(dynamic) reduction(+ : skipped)
+    /* Tokens in parallel when there are at least as many as threads; else
+     * one token at a time, with each expert's rows in parallel. */
+#ifdef _OPENMP
+    int by_token = n >= omp_get_max_threads();
+#else
+    int by_token = 0;
+#endif
+#pragma omp parallel for schedule(dynamic) reduction(+ : skipped) if (by_token)
     for (int a = 0; a < n; a++) {
         int t = tokens ? tokens[a] : a;
         double *xv = malloc(sizeof(double) * (size_t)H);

@@ -35,8 +35,9 @@ struct WsHeader {
     int32_t tc_chunks;               // prefill GEMMs: expert chunks of <= 256 slots
     uint32_t pad0;
     // One- and two-token router: every CTA (one per expert) adds 1 once its
-    // logits are stored; the CTA whose add returns E - 1 modulo E ranks them
-    // and sets the count back to 0 for the next call.
+    // logits are stored; the CTA whose add returns E - 1 ranks them and sets
+    // the count back to 0 for the next call (a count >= E at an add means an
+    // uninitialised header and is recorded as MOE_ERR_INTERNAL).
     unsigned long long router_rows;
     uint32_t pad[52];
 };

@@ -455,8 +455,7 @@ cudaError_t init_decode_stream(int dev) {
     const void *rows[] = {reinterpret_cast<const void *>(stream_down_rows_kernel<1>),
                           reinterpret_cast<const void *>(stream_down_rows_kernel<2>),
                           reinterpret_cast<const void *>(stream_down_rows_kernel<4>),
-                          reinterpret_cast<const void *>(stream_down_rows_kernel<6>),
-                          reinterpret_cast<const void *>(stream_down_rows_kernel<8>)};
+                          reinterpret_cast<const void *>(stream_down_rows_kernel<6>)};
     for (const void *f : rows) {
         err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (err != cudaSuccess) return err;
@@ -502,8 +501,9 @@ cudaError_t launch_decode_stream(const float *x, const int32_t *idx, const float
             stream_down_rows_kernel<4><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
         else if (ud <= 192)
             stream_down_rows_kernel<6><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
-        else
-            stream_down_rows_kernel<8><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+        else  // four units per lane in flight, looping over the rest (a wider
+              // batch of loads per lane would spill at the 128-register cap)
+            stream_down_rows_kernel<4><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
     }
     else if (nbi <= 1)
         stream_down_kernel<1><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);

@@ -235,9 +235,18 @@ __global__ void __launch_bounds__(256) router_row_kernel(const float *__restrict
         __threadfence();  // the logit is visible GPU-wide before this CTA is counted
     }
     __syncthreads();
-    // exactly one CTA of the call sees E - 1 modulo E, whatever value the
-    // count held before the call (it is set back to 0 below)
-    if (threadIdx.x == 0) last = atomicAdd(&hdr->router_rows, 1ull) % gridDim.x == gridDim.x - 1;
+    // The count starts every call at 0 (moe_workspace_init, then the ranking
+    // CTA of each call sets it back), so exactly the last CTA to count itself
+    // sees gridDim.x - 1 and every other logit is stored by then.  A count at
+    // or past gridDim.x means the header was never initialised (or was
+    // overwritten): that is recorded, and no CTA ranks logits it cannot
+    // trust; the count stays off until the workspace is re-initialised.
+    if (threadIdx.x == 0) {
+        const unsigned long long prev = atomicAdd(&hdr->router_rows, 1ull);
+        last = prev == gridDim.x - 1;
+        if (prev >= gridDim.x)
+            record_status(hdr, MOE_ERR_INTERNAL, 500000000 + int(prev % 1000000ull));
+    }
     __syncthreads();
     if (!last) return;
     __threadfence();

@@ -16,12 +16,26 @@ from quantized_routed_expert_02_gb300 import synth
 GAP = 1e-5
 
 
-def tie_free_x(o: Oracle, shape, layer, Wr, bias, max_rounds=32):
+def exact_ties_only(logits_row: np.ndarray, k: int, gap: float = GAP, depth: int = 1) -> bool:
+    """True when every adjacent pair among the k + depth largest logits is
+    either exactly equal (a deliberate tie: identical router rows give
+    identical logits on both sides) or at least ``gap`` apart."""
+    top = np.sort(logits_row)[::-1][:min(k + depth, logits_row.size)]
+    d = top[:-1] - top[1:]
+    return bool(np.all((d == 0.0) | (d >= gap)))
+
+
+def tie_free_x(o: Oracle, shape, layer, Wr, bias, max_rounds=32, accept=None):
+    """x rows redrawn until ``accept(logits_row)`` holds for every row
+    (default: no adjacent gap below GAP among the top k+1 logits)."""
+    if accept is None:
+        def accept(row):
+            return near_tie_free(row, shape.k, GAP)
     x = np.stack([synth.x_row(shape, layer, t, 0) for t in range(shape.T)])
     attempt = np.zeros(shape.T, dtype=np.int32)
     for _ in range(max_rounds):
         lg = o.router(x, Wr, bias, shape.k)["logits"]
-        bad = [t for t in range(shape.T) if not near_tie_free(lg[t], shape.k, GAP)]
+        bad = [t for t in range(shape.T) if not accept(lg[t])]
         if not bad:
             return x, attempt
         for t in bad:

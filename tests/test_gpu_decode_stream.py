@@ -25,9 +25,15 @@ def test_a22b_single_token_takes_the_streamed_path(m):
 # 128 units), odd block counts per down row (I = 1280: five blocks).  The
 # fp32 fallbacks: gate/up for H = 1280 (not a power of two), down for
 # k*I/64 = 768 units (more than the CTA's threads).
+# The down launch's per-lane width G = ceil(k*I/64 / 32) is a template
+# argument: (8192, 4, 2, 1024) has 32 units per row (G = 1), (8192, 4, 2,
+# 1280) 40 (G = 2), (8192, 4, 4, 1536) 96 (G = 4), the A22B shape 192 (G = 6);
+# (1024, 32, 32, 1024) and (2048, 16, 16, 2048) have 512 and take G = 4 in
+# four rounds.
 @pytest.mark.parametrize("H,E,k,I", [(4096, 8, 8, 1536), (1024, 32, 32, 1024),
                                      (8192, 4, 2, 1280), (2048, 16, 16, 2048),
-                                     (1280, 8, 8, 2048), (1024, 16, 12, 4096)])
+                                     (1280, 8, 8, 2048), (1024, 16, 12, 4096),
+                                     (8192, 4, 2, 1024), (8192, 4, 4, 1536)])
 def test_streamed_shapes(m, H, E, k, I):
     assert m.moe_layer_launch_count(1, H, E, k, I) == STREAM_LAUNCHES
     shape = synth.custom_shape(1, H, E, k, I, wr_std=0.03, cfg_id=20 + (H + E + k + I) % 30)

@@ -71,13 +71,13 @@ def check_layer(case, idx, w, y):
 
 # ---------------------------------------------------------------- full workloads
 
-SAMPLE_PREFILL = tuple(range(0, 4096, 97)) + (4095,)
-
+# every token of every workload is compared (the 4096-token prefill too:
+# the oracle runs its tokens on all host cores)
 WORKLOADS = [
     ("tiny", None),
     ("a3b_decode", None),
     ("a3b_batch64_zipf", None),
-    ("a3b_prefill", SAMPLE_PREFILL),
+    ("a3b_prefill", None),
     ("a22b_decode", None),
     ("a22b_batch32", None),
 ]
@@ -97,8 +97,9 @@ def test_a3b_decode_second_layer(m):
 
 
 def test_router_all_tokens_prefill(m):
-    """Routing of every one of the 4096 prefill tokens is bit-exact."""
-    case = layer_case(synth.SHAPES["a3b_prefill"], 0, SAMPLE_PREFILL)
+    """Routing of every one of the 4096 prefill tokens is bit-exact (the
+    router entry point on its own)."""
+    case = layer_case(synth.SHAPES["a3b_prefill"], 0, None)
     s = case["shape"]
     d = to_dev(case)
     ws = m.alloc_workspace(s.T, s.H, s.E, s.k, s.I, device=DEV)
