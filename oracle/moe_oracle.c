@@ -248,6 +248,40 @@ long moq_ffn(const float *x, const int32_t *idx, const double *w,
 }
 
 /*
+ * Pre-FFN RMSNorm (forward_qwen3_moe.rs, aprender-serve 0.35.0, step 2f of
+ * forward_qwen3_moe and step 2g of forward_single_qwen3_moe_with_cache:
+ * ffn_input = rms_norm(hidden, ffn_norm_weight, eps)).  The pages name the
+ * operation, not its formula; the reading is the usual root-mean-square
+ * norm, per token row:
+ *     out[i] = x[i] / sqrt(mean_i(x[i]^2) + eps) * gamma[i]
+ * computed in fp64 and rounded once to fp32 at the end, because the pages'
+ * ffn_input is an f32 vector that the MoE FFN then consumes.
+ */
+void moq_rmsnorm(const float *x, const float *gamma, double eps, int T, int H, float *out)
+{
+    for (int t = 0; t < T; t++) {
+        const float *xt = x + (long)t * H;
+        double ss = 0.0;
+        for (int i = 0; i < H; i++)
+            ss += (double)xt[i] * (double)xt[i];
+        double inv = 1.0 / sqrt(ss / (double)H + eps);
+        for (int i = 0; i < H; i++)
+            out[(long)t * H + i] = (float)((double)xt[i] * inv * (double)gamma[i]);
+    }
+}
+
+/*
+ * Residual after the MoE FFN (same page, step 2h of forward_qwen3_moe and
+ * step 2i of forward_single_qwen3_moe_with_cache: hidden += ffn_output):
+ * out = hidden + y, elementwise, in fp64.
+ */
+void moq_add_residual(const float *hidden, const double *y, long n, double *out)
+{
+    for (long i = 0; i < n; i++)
+        out[i] = (double)hidden[i] + y[i];
+}
+
+/*
  * Token->expert permutation: counts[e] = number of (t,j) slots routed to e,
  * offs = exclusive prefix sum of counts (E+1 entries), perm = slot ids
  * p = t*k + j ordered by (expert, p).  Out-of-range slots are left out.

@@ -48,6 +48,8 @@ def _load(path: str = _SO):
     lib.moq_ffn.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P, i, P]
     lib.moq_ffn.restype = l
     lib.moq_permutation.argtypes = [P, i, i, i, P, P, P]
+    lib.moq_rmsnorm.argtypes = [P, P, ctypes.c_double, i, i, P]
+    lib.moq_add_residual.argtypes = [P, P, l, P]
     lib.moq_set_threads.argtypes = [i]
     lib.moq_max_threads.restype = i
     return lib
@@ -150,6 +152,36 @@ class Oracle:
         r = self.router(x, Wr, bias, k)
         y, skipped = self.ffn(x, r["idx"], r["w"], gate, up, down, E, I, tokens)
         r["y"] = y
+        return r
+
+    def rmsnorm(self, x, gamma, eps):
+        """fp32 [T,H]: x / sqrt(mean(x^2) + eps) * gamma per row (fp64 inside)."""
+        x = _c(x, np.float32)
+        T, H = x.shape
+        g = _c(gamma, np.float32).reshape(-1)
+        assert g.size == H
+        out = np.empty((T, H), dtype=np.float32)
+        self.L.moq_rmsnorm(_p(x), _p(g), float(eps), T, H, _p(out))
+        return out
+
+    def add_residual(self, hidden, y):
+        hidden = _c(hidden, np.float32)
+        y = _c(y, np.float64)
+        assert hidden.shape == y.shape
+        out = np.empty(y.shape, dtype=np.float64)
+        self.L.moq_add_residual(_p(hidden), _p(y), y.size, _p(out))
+        return out
+
+    def block(self, hidden, norm_w, eps, Wr, bias, k, gate, up, down, E, I, residual=True,
+              tokens=None):
+        """The layer with the steps on each side of it: ffn_in = RMSNorm(hidden)
+        (skipped when ``norm_w`` is None), the router and FFN on ffn_in, and
+        out = hidden + y (``residual``) or y.  Returns the layer's dict plus
+        ``ffn_in`` and ``out``."""
+        ffn_in = _c(hidden, np.float32) if norm_w is None else self.rmsnorm(hidden, norm_w, eps)
+        r = self.layer(ffn_in, Wr, bias, k, gate, up, down, E, I, tokens)
+        r["ffn_in"] = ffn_in
+        r["out"] = self.add_residual(hidden, r["y"]) if residual else r["y"].copy()
         return r
 
 

@@ -41,6 +41,17 @@ MUTANTS = {
                              "perm[cursor[idx[p]]++] = (int32_t)(n - 1 - p);"),
     "gate_up_swapped_in_ffn": ("moq_expert(xv, gate + e * gate_bytes, up + e * gate_bytes,",
                                "moq_expert(xv, up + e * gate_bytes, gate + e * gate_bytes,"),
+    "rmsnorm_no_sqrt": ("double inv = 1.0 / sqrt(ss / (double)H + eps);",
+                        "double inv = 1.0 / (ss / (double)H + eps);"),
+    "rmsnorm_sum_not_mean": ("double inv = 1.0 / sqrt(ss / (double)H + eps);",
+                             "double inv = 1.0 / sqrt(ss + eps);"),
+    "rmsnorm_eps_outside_root": ("double inv = 1.0 / sqrt(ss / (double)H + eps);",
+                                 "double inv = 1.0 / (sqrt(ss / (double)H) + eps);"),
+    "rmsnorm_gamma_ignored": ("out[(long)t * H + i] = (float)((double)xt[i] * inv * (double)gamma[i]);",
+                              "out[(long)t * H + i] = (float)((double)xt[i] * inv);"),
+    "residual_dropped": ("out[i] = (double)hidden[i] + y[i];", "out[i] = y[i];"),
+    "residual_doubled": ("out[i] = (double)hidden[i] + y[i];",
+                         "out[i] = 2.0 * (double)hidden[i] + y[i];"),
 }
 
 

@@ -316,3 +316,90 @@ def test_ffn_brute_force_rectangular(oracle, H, I):
         want = sum(w[t, j] * _dense_ffn(_dense(oracle, shape, blobs, idx[t, j]),
                                         x[t].astype(np.float64)) for j in range(2))
         np.testing.assert_allclose(y[t], want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
+
+
+# ---------------------------------------------------------------- pre-FFN RMSNorm and residual
+# forward_qwen3_moe.rs (aprender-serve 0.35.0), steps 2f-2h of
+# forward_qwen3_moe: ffn_input = rms_norm(hidden, ffn_norm_weight, eps), the
+# MoE FFN on it, hidden += ffn_output.
+
+def test_rmsnorm_constant_row(oracle):
+    """A constant row c has root-mean-square |c|: with eps = 0 the norm is
+    sign(c) * gamma exactly; with eps > 0 it is c / sqrt(c^2 + eps) * gamma."""
+    H = 256
+    gamma = np.linspace(-2.0, 3.0, H).astype(np.float32)
+    for c in (0.75, -3.0, 1024.0):
+        x = np.full((1, H), c, dtype=np.float32)
+        np.testing.assert_array_equal(oracle.rmsnorm(x, gamma, 0.0)[0],
+                                      (np.sign(c) * gamma).astype(np.float32))
+        eps = 0.5
+        want = (c / math.sqrt(c * c + eps)) * gamma.astype(np.float64)
+        got = oracle.rmsnorm(x, gamma, eps)[0].astype(np.float64)
+        assert np.max(np.abs(got - want)) <= 1e-6 * np.max(np.abs(want))
+
+
+def test_rmsnorm_hand_example(oracle):
+    """x = (1, 2, 3, 4): mean of squares 30/4 = 7.5, 1/sqrt(7.5) =
+    0.36514837167011..., gamma = (1, 0.5, 2, -1)."""
+    x = np.array([[1.0, 2.0, 3.0, 4.0]], dtype=np.float32)
+    gamma = np.array([1.0, 0.5, 2.0, -1.0], dtype=np.float32)
+    want = np.array([0.3651483716701107, 0.3651483716701107, 2.1908902300206643,
+                     -1.4605934866804429])
+    got = oracle.rmsnorm(x, gamma, 0.0)[0].astype(np.float64)
+    assert np.max(np.abs(got - want)) <= 1e-7
+
+
+def test_rmsnorm_scale_invariance_and_unit_rms(oracle):
+    """With eps = 0 the norm ignores a positive scale of its row (bitwise
+    for a power of two) and, with gamma = 1, has root-mean-square 1."""
+    rng = np.random.default_rng(11)
+    x = rng.normal(0.0, 1.0, (3, 512)).astype(np.float32)
+    ones = np.ones(512, dtype=np.float32)
+    a = oracle.rmsnorm(x, ones, 0.0)
+    np.testing.assert_array_equal(oracle.rmsnorm(4.0 * x, ones, 0.0), a)
+    assert np.max(np.abs(oracle.rmsnorm(3.0 * x, ones, 0.0) - a)) <= 1e-6
+    rms = np.sqrt(np.mean(a.astype(np.float64) ** 2, axis=1))
+    assert np.max(np.abs(rms - 1.0)) <= 1e-6
+
+
+def _block_inputs(T=3, H=256, E=8, k=2, I=256, cfg=93):
+    shape = synth.custom_shape(T, H, E, k, I, wr_std=0.05, cfg_id=cfg)
+    blobs = synth.expert_blobs(shape, 0)
+    Wr = synth.router_weights(shape, 0)
+    hidden = (3.0 * synth.activations_fast(shape, 0)).astype(np.float32)
+    return shape, blobs, Wr, hidden
+
+
+def test_block_zero_norm_weight_returns_hidden(oracle):
+    """gamma = 0 makes the FFN input zero: every logit is 0, so the top k
+    are experts 0..k-1 (lowest indices) with weight 1/k, every expert maps 0
+    to 0, and the block's output is the residual stream itself."""
+    shape, blobs, Wr, hidden = _block_inputs()
+    r = oracle.block(hidden, np.zeros(shape.H, np.float32), 1e-6, Wr, None, shape.k,
+                     blobs["gate"], blobs["up"], blobs["down"], shape.E, shape.I)
+    np.testing.assert_array_equal(r["idx"], np.tile(np.arange(shape.k), (shape.T, 1)))
+    np.testing.assert_array_equal(r["y"], 0.0)
+    np.testing.assert_array_equal(r["out"], hidden.astype(np.float64))
+
+
+def test_block_output_is_hidden_plus_ffn_of_normed(oracle):
+    """With eps = 0, scaling the residual stream by 4 leaves the normed FFN
+    input, the routing and the FFN output bit-identical; the output is
+    hidden + y (so the two outputs differ by exactly 3 * hidden)."""
+    shape, blobs, Wr, hidden = _block_inputs()
+    gamma = np.linspace(0.5, 1.5, shape.H).astype(np.float32)
+    args = (Wr, None, shape.k, blobs["gate"], blobs["up"], blobs["down"], shape.E, shape.I)
+    r1 = oracle.block(hidden, gamma, 0.0, *args)
+    r4 = oracle.block(4.0 * hidden, gamma, 0.0, *args)
+    np.testing.assert_array_equal(r1["ffn_in"], r4["ffn_in"])
+    np.testing.assert_array_equal(r1["idx"], r4["idx"])
+    np.testing.assert_array_equal(r1["y"], r4["y"])
+    assert np.max(np.abs(r1["y"])) > 1.0
+    h64 = hidden.astype(np.float64)
+    assert np.max(np.abs(r1["out"] - (h64 + r1["y"]))) == 0.0
+    assert np.max(np.abs((r4["out"] - r1["out"]) - 3.0 * h64)) <= 1e-9 * np.max(np.abs(r1["out"]))
+    # without the norm the FFN sees the residual stream itself
+    r0 = oracle.block(hidden, None, 0.0, *args)
+    np.testing.assert_array_equal(r0["ffn_in"], hidden)
+    ref = oracle.layer(hidden, *args)
+    np.testing.assert_array_equal(r0["y"], ref["y"])
