@@ -169,6 +169,40 @@ MOE_API moe_status moe_layer(const float *x_dev, const float *Wr_dev, const floa
                      void *ws_dev, size_t ws_bytes, void *stream);
 
 /*
+ * The layer with the steps on each side of it in a decoder block
+ * (forward_qwen3_moe.rs, aprender-serve 0.35.0, steps 2f-2h of
+ * forward_qwen3_moe and 2g-2i of forward_single_qwen3_moe_with_cache):
+ *   ffn_in = RMSNorm(hidden) = hidden / sqrt(mean(hidden^2) + norm_eps) * norm_w
+ *            (per token row; ffn_in = hidden when norm_w_dev is NULL),
+ *   the router and the expert FFN of moe_layer on ffn_in (idx_dev, w_dev,
+ *   and the FFN output y),
+ *   out = hidden + y when add_residual != 0 (hidden += ffn_output), else y.
+ *  hidden_dev [T,H] fp32; norm_w_dev [H] fp32 or NULL; norm_eps >= 0 and
+ *  finite; out_dev [T,H] fp32 may be hidden_dev itself (an in-place
+ *  residual update: every read of hidden precedes the write of its element).
+ *  The single-token fused kernel applies the norm while staging the row and
+ *  adds the residual at its output store; the other paths run one extra
+ *  launch for the norm (into the workspace) and add the residual in the
+ *  final combine.
+ * Stage capture (forward_qwen3_moe_cuda_traced.rs, aprender-serve 0.34.0, doc
+ * of forward_qwen3_moe_cuda_traced_with_plan: the MoeRouter stage is the
+ * chosen token's k post-softmax, renormalised weights, MoeFfnOut its [H]
+ * FFN output before the residual): when 0 <= capture_token < T, cap_idx_dev
+ * [k] int32 and cap_w_dev [k] fp32 receive that token's routing and
+ * cap_ffn_dev [H] fp32 its FFN output before the residual add (each
+ * pointer NULL to skip it); capture_token = -1 captures nothing and costs
+ * nothing.  capture_token outside [-1, T) is MOE_ERR_INVALID_SHAPE.
+ *  Workspace: moe_workspace_bytes(T, H, E, k, I), as for moe_layer.
+ */
+MOE_API moe_status moe_layer_block(const float *hidden_dev, const float *norm_w_dev, float norm_eps,
+                                   const float *Wr_dev, const float *bias_dev,
+                                   const void *gate_dev, const void *up_dev, const void *down_dev,
+                                   int T, int H, int E, int k, int I,
+                                   int32_t *idx_dev, float *w_dev, float *out_dev, int add_residual,
+                                   int capture_token, int32_t *cap_idx_dev, float *cap_w_dev,
+                                   float *cap_ffn_dev, void *ws_dev, size_t ws_bytes, void *stream);
+
+/*
  * The whole layer for a caller whose activations live in host memory:
  * copies x_host [T,H] fp32 to the device, runs moe_layer, copies y back to
  * y_host [T,H] fp32, and synchronises `stream` before returning.  Page-locked

@@ -97,7 +97,8 @@ inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK 
 
 moe_status ffn_enqueue(const float *x, const int32_t *idx, const float *w, const void *gate,
                        const void *up, const void *down, int T, int H, int E, int k, int I,
-                       float *y, const Ws &ws, int sms, int dev, cudaStream_t s) {
+                       float *y, const Ws &ws, int sms, int dev, const OutEpilogue &ep,
+                       cudaStream_t s) {
     const WsLayout &L = ws.L;
     MOE_TRY(cuda_status(launch_permute(idx, T, k, E, ws.i32(L.counts), ws.i32(L.offs),
                                        ws.i32(L.perm), ws.i32(L.active), ws.i32(L.nactive),
@@ -109,12 +110,36 @@ moe_status ffn_enqueue(const float *x, const int32_t *idx, const float *w, const
             ws.i32(L.slotpos), ws.i32(L.active), ws.i32(L.nactive), reinterpret_cast<__half *>(ws.base + L.x16),
             reinterpret_cast<__half *>(ws.base + L.h16), ws.f32(L.o),
             reinterpret_cast<TcChunk *>(ws.base + L.chunks), ws.hdr(), sms, g_wait_ns, s)));
-        return cuda_status(launch_combine(ws.f32(L.o), idx, w, T, H, E, k, y, sms, s));
+        return cuda_status(launch_combine(ws.f32(L.o), idx, w, T, H, E, k, y, ep, sms, s));
     }
     return cuda_status(launch_expert_ffn(
         x, idx, w, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
         static_cast<const uint8_t *>(down), T, H, E, k, I, y, ws.i32(L.offs), ws.i32(L.perm),
-        ws.i32(L.active), ws.i32(L.nactive), ws.f32(L.h), ws.f32(L.o), ws.hdr(), sms, s));
+        ws.i32(L.active), ws.i32(L.nactive), ws.f32(L.h), ws.f32(L.o), ws.hdr(), ep, sms, s));
+}
+
+// Router then FFN for every shape (moe_layer and moe_layer_block): x is the
+// FFN input; norm_w (nullable) asks the single-token fused kernel to
+// RMS-normalise x itself (the other paths get an already normalised x).
+moe_status layer_enqueue(const float *x, const float *norm_w, float eps, const float *Wr,
+                         const float *bias, const void *gate, const void *up, const void *down,
+                         int T, int H, int E, int k, int I, int32_t *idx, float *w, float *y,
+                         const Ws &W, int sms, int dev, const OutEpilogue &ep, cudaStream_t s) {
+    const WsLayout &L = W.L;
+    if (decode_fused_supported(dev, T, H, E, k, I)) {
+        return cuda_status(launch_decode_fused(
+            dev, x, norm_w, eps, ep, Wr, bias, nullptr, nullptr, idx, w,
+            static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
+            static_cast<const uint8_t *>(down), H, E, k, I, y, W.u64(L.sync), W.f32(L.h), W.hdr(),
+            g_withhold, g_wait_ns, W.u64(L.o), W.timeline_cap(), s));
+    }
+    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(), s)));
+    if (decode_stream_supported(dev, T, H, E, k, I)) {
+        return cuda_status(launch_decode_stream(
+            x, idx, w, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
+            static_cast<const uint8_t *>(down), H, E, k, I, y, W.f32(L.h), W.hdr(), ep, sms, s));
+    }
+    return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev, ep, s);
 }
 
 }  // namespace
@@ -232,20 +257,21 @@ moe_status moe_ffn(const float *x, const int32_t *idx, const float *w, const voi
     int sms = 0, dev = 0;
     MOE_TRY(device_info(&sms, &dev));
     Ws W{static_cast<uint8_t *>(ws), L};
+    const OutEpilogue none;
     if (decode_fused_supported(dev, T, H, E, k, I)) {
         return cuda_status(launch_decode_fused(
-            dev, x, nullptr, nullptr, idx, w, nullptr, nullptr, static_cast<const uint8_t *>(gate),
-            static_cast<const uint8_t *>(up), static_cast<const uint8_t *>(down), H, E, k, I, y,
-            W.u64(L.sync), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns, W.u64(L.o), W.timeline_cap(),
-            static_cast<cudaStream_t>(stream)));
+            dev, x, nullptr, 0.f, none, nullptr, nullptr, idx, w, nullptr, nullptr,
+            static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
+            static_cast<const uint8_t *>(down), H, E, k, I, y, W.u64(L.sync), W.f32(L.h), W.hdr(),
+            g_withhold, g_wait_ns, W.u64(L.o), W.timeline_cap(), static_cast<cudaStream_t>(stream)));
     }
     if (decode_stream_supported(dev, T, H, E, k, I)) {
         return cuda_status(launch_decode_stream(
             x, idx, w, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
-            static_cast<const uint8_t *>(down), H, E, k, I, y, W.f32(L.h), W.hdr(), sms,
+            static_cast<const uint8_t *>(down), H, E, k, I, y, W.f32(L.h), W.hdr(), none, sms,
             static_cast<cudaStream_t>(stream)));
     }
-    return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev,
+    return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev, none,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -267,20 +293,64 @@ moe_status moe_layer(const float *x, const float *Wr, const float *bias, const v
     int sms = 0, dev = 0;
     MOE_TRY(device_info(&sms, &dev));
     Ws W{static_cast<uint8_t *>(ws), L};
+    return layer_enqueue(x, nullptr, 0.f, Wr, bias, gate, up, down, T, H, E, k, I, idx, w, y, W,
+                         sms, dev, OutEpilogue{}, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_block(const float *hidden, const float *norm_w, float norm_eps,
+                           const float *Wr, const float *bias, const void *gate, const void *up,
+                           const void *down, int T, int H, int E, int k, int I, int32_t *idx,
+                           float *w, float *out, int add_residual, int capture_token,
+                           int32_t *cap_idx, float *cap_w, float *cap_ffn, void *ws,
+                           size_t ws_bytes, void *stream) {
+    MOE_TRY(check_shape(T, H, E, k, I));
+    MOE_TRY(check_ptr(hidden, 16));
+    if (norm_w && !aligned(norm_w, 16)) return MOE_ERR_MISALIGNED;
+    if (!(norm_eps >= 0.f) || !(norm_eps <= 3.402823466e38f)) return MOE_ERR_INVALID_SHAPE;
+    MOE_TRY(check_ptr(Wr, 16));
+    if (bias && !aligned(bias, 16)) return MOE_ERR_MISALIGNED;
+    MOE_TRY(check_ptr(gate, 16));
+    MOE_TRY(check_ptr(up, 16));
+    MOE_TRY(check_ptr(down, 16));
+    MOE_TRY(check_ptr(idx, 16));
+    MOE_TRY(check_ptr(w, 16));
+    MOE_TRY(check_ptr(out, 16));
+    if (capture_token < -1 || capture_token >= T) return MOE_ERR_INVALID_SHAPE;
+    if ((cap_idx && !aligned(cap_idx, 4)) || (cap_w && !aligned(cap_w, 4)) ||
+        (cap_ffn && !aligned(cap_ffn, 16)))
+        return MOE_ERR_MISALIGNED;
+    WsLayout L = ws_layout(T, H, E, k, I, false);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    int sms = 0, dev = 0;
+    MOE_TRY(device_info(&sms, &dev));
+    Ws W{static_cast<uint8_t *>(ws), L};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (decode_fused_supported(dev, T, H, E, k, I)) {
-        return cuda_status(launch_decode_fused(
-            dev, x, Wr, bias, nullptr, nullptr, idx, w, static_cast<const uint8_t *>(gate),
-            static_cast<const uint8_t *>(up), static_cast<const uint8_t *>(down), H, E, k, I, y,
-            W.u64(L.sync), W.f32(L.h), W.hdr(), g_withhold, g_wait_ns, W.u64(L.o), W.timeline_cap(), s));
+    OutEpilogue ep;
+    ep.residual = add_residual ? hidden : nullptr;
+    ep.capture = capture_token >= 0 ? cap_ffn : nullptr;
+    ep.cap_t = capture_token;
+    // The fused single-token kernel normalises x while staging it; every
+    // other path reads a normalised copy from the workspace.
+    const float *ffn_in = hidden;
+    const float *fused_norm = nullptr;
+    if (norm_w != nullptr) {
+        if (decode_fused_supported(dev, T, H, E, k, I)) {
+            fused_norm = norm_w;
+        } else {
+            MOE_TRY(cuda_status(launch_rmsnorm(hidden, norm_w, norm_eps, T, H, W.f32(L.xn), s)));
+            ffn_in = W.f32(L.xn);
+        }
     }
-    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(), s)));
-    if (decode_stream_supported(dev, T, H, E, k, I)) {
-        return cuda_status(launch_decode_stream(
-            x, idx, w, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
-            static_cast<const uint8_t *>(down), H, E, k, I, y, W.f32(L.h), W.hdr(), sms, s));
-    }
-    return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev, s);
+    MOE_TRY(layer_enqueue(ffn_in, fused_norm, norm_eps, Wr, bias, gate, up, down, T, H, E, k, I,
+                          idx, w, out, W, sms, dev, ep, s));
+    // the router stage of the captured token: its k expert ids and weights
+    if (capture_token >= 0 && cap_idx != nullptr)
+        MOE_TRY(cuda_status(cudaMemcpyAsync(cap_idx, idx + size_t(capture_token) * k,
+                                            sizeof(int32_t) * k, cudaMemcpyDeviceToDevice, s)));
+    if (capture_token >= 0 && cap_w != nullptr)
+        MOE_TRY(cuda_status(cudaMemcpyAsync(cap_w, w + size_t(capture_token) * k,
+                                            sizeof(float) * k, cudaMemcpyDeviceToDevice, s)));
+    return MOE_OK;
 }
 
 moe_status moe_layer_host(const float *x_host, const float *Wr, const float *bias,

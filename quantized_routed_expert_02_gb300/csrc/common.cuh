@@ -59,8 +59,8 @@ constexpr size_t kSyncWords = kMaxE;
 constexpr int kPermSlots = 256;
 
 struct WsLayout {
-    size_t sync, blockcnt, slotpos, counts, offs, active, nactive, perm, h, o, logits, x16, h16, chunks, xstage, ystage,
-        total;
+    size_t sync, blockcnt, slotpos, counts, offs, active, nactive, perm, h, o, logits, x16, h16, chunks, xn, xstage,
+        ystage, total;
 };
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -85,6 +85,7 @@ inline WsLayout ws_layout(int T, int H, int E, int k, int I, bool host_staging) 
     L.x16 = off;     off = align256(off + 2 * pairs * H);                // fp16 activations, sorted rows
     L.h16 = off;     off = align256(off + 2 * pairs * I);                // fp16 SwiGLU output
     L.chunks = off;  off = align256(off + sizeof(TcChunk) * (pairs / 32 + E + 1));  // chunks of >= 32 slots
+    L.xn = off;      off = align256(off + sizeof(float) * size_t(T) * H);  // normed FFN input
     L.xstage = off;
     L.ystage = off;
     if (host_staging) {
@@ -93,6 +94,22 @@ inline WsLayout ws_layout(int T, int H, int E, int k, int I, bool host_staging) 
     }
     L.total = off;
     return L;
+}
+
+// What the final store of an output value does besides storing it (the
+// steps on the far side of the layer): add the residual stream
+// (hidden += ffn_output) and copy one token's pre-residual output row to a
+// capture buffer (the [H] FFN-output stage of a traced forward).
+struct OutEpilogue {
+    const float *residual = nullptr;  // [T,H] added to every output value, or null
+    float *capture = nullptr;         // [H] receives token cap_t's pre-residual row, or null
+    int cap_t = -1;
+};
+
+// The value to store at y[t*H + r] for the FFN output v.
+__device__ __forceinline__ float epilogue_value(const OutEpilogue &ep, int t, int H, int r, float v) {
+    if (ep.capture != nullptr && t == ep.cap_t) ep.capture[r] = v;
+    return ep.residual != nullptr ? ep.residual[size_t(t) * H + r] + v : v;
 }
 
 // Record the first device-side error (later ones are dropped).

@@ -78,6 +78,9 @@ constexpr long long kBackoffCycles = 600;  // wait after a poll that found a sta
 
 struct Params {
     const float *x, *Wr, *bias;
+    const float *norm_w;          // pre-FFN RMSNorm weight [H], or null (x used as is)
+    float eps;                    // the norm's epsilon
+    OutEpilogue ep;               // residual add and output capture at the y store
     const int32_t *idx_in;
     const float *w_in;
     int32_t *idx_out;
@@ -179,7 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     int *sel_e = reinterpret_cast<int *>(smem + 16);
     float *sel_w = reinterpret_cast<float *>(sel_e + 32);
     int *flags = reinterpret_cast<int *>(sel_w + 32);  // [1] wait timed out, [2] tied ranks
-    float *red = reinterpret_cast<float *>(flags + 4); // kWarps partial sums, then kMaxE logits
+    float *red = reinterpret_cast<float *>(flags + 4); // kWarps partial sums, then kMaxE logits,
+                                                       // then kWarps partial sums of squares
     uint32_t *skey = reinterpret_cast<uint32_t *>(smem + 1536);  // kMaxE logit keys
     int *pcnt = reinterpret_cast<int *>(smem + 2560);            // kThreads partial ranks
     float *vec = reinterpret_cast<float *>(smem + kHeadBytes);
@@ -211,14 +215,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     if (threadIdx.x < 32) sel_e[threadIdx.x] = -1;
     // ---------------- 1. router logits (a share per CTA).
     // The CTA's first logit is computed while x is staged: x and the router
-    // row are requested together, so their latencies overlap.
+    // row are requested together, so their latencies overlap.  With the
+    // pre-FFN RMSNorm, the same pass stages x * gamma, sums x^2 and dots
+    // x * gamma with the router row; the 1/rms scale (one number per token)
+    // is applied to the logit and, in place, to the staged vector.
     {
         const int e = blockIdx.x;
         const bool logit = p.router_on && e < E;
+        const bool norm = p.norm_w != nullptr;
         const float *wr = p.Wr + size_t(logit ? e : 0) * H;
-        float a = 0.f;
+        float a = 0.f, ss = 0.f;
         for (int i = threadIdx.x; i < (H >> 2); i += kThreads) {
-            const float4 x4 = __ldg(reinterpret_cast<const float4 *>(p.x) + i);
+            float4 x4 = __ldg(reinterpret_cast<const float4 *>(p.x) + i);
+            if (norm) {
+                ss = fmaf(x4.x, x4.x, ss);
+                ss = fmaf(x4.y, x4.y, ss);
+                ss = fmaf(x4.z, x4.z, ss);
+                ss = fmaf(x4.w, x4.w, ss);
+                const float4 g4 = __ldg(reinterpret_cast<const float4 *>(p.norm_w) + i);
+                x4 = make_float4(x4.x * g4.x, x4.y * g4.y, x4.z * g4.z, x4.w * g4.w);
+            }
             if (logit) {
                 const float4 w4 = __ldg(reinterpret_cast<const float4 *>(wr) + i);
                 a = fmaf(w4.x, x4.x, a);
@@ -228,15 +244,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             }
             *reinterpret_cast<float4 *>(vec + padded(4 * i)) = x4;
         }
+        float *red2 = red + kWarps + kMaxE;
         a = warp_sum(a);
         if (lane == 0) red[warp] = a;
+        if (norm) {
+            ss = warp_sum(ss);
+            if (lane == 0) red2[warp] = ss;
+        }
         if (threadIdx.x == 0) *tag_sh = uint32_t(calls0 / nblk) + 1u;
         __syncthreads();
+        float inv = 1.f;
+        if (norm) {  // every thread forms the same scale from the same sums in the same order
+            float s2 = 0.f;
+            for (int w = 0; w < kWarps; ++w) s2 += red2[w];
+            inv = 1.0f / sqrtf(s2 / float(H) + p.eps);
+        }
         if (logit && threadIdx.x == 0) {
             float sum = 0.f;
             for (int w = 0; w < kWarps; ++w) sum += red[w];
+            if (norm) sum *= inv;
             sum += p.bias ? p.bias[e] : 0.f;
             if (publish) st_relaxed_u64(p.sync + e, tagged(*tag_sh, sum));
+        }
+        if (norm) {
+            // each thread rescales the elements it staged
+            for (int i = threadIdx.x; i < (H >> 2); i += kThreads) {
+                float4 *v = reinterpret_cast<float4 *>(vec + padded(4 * i));
+                const float4 t4 = *v;
+                *v = make_float4(t4.x * inv, t4.y * inv, t4.z * inv, t4.w * inv);
+            }
+            __syncthreads();
         }
     }
     const uint32_t tag = *tag_sh;
@@ -581,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
                 float acc = 0.f;
                 for (int uu = lane; uu < Ud; uu += 32) acc += P[rr * Ud + uu];
                 acc = warp_sum(acc);
-                if (lane == 0) p.y[r0 + rr] = acc;
+                if (lane == 0) p.y[r0 + rr] = epilogue_value(p.ep, 0, H, r0 + rr, acc);
             }
         } else {
             const int n_rows = R > warp ? (R - warp + kWarps - 1) / kWarps : 0;  // rows warp+16i
@@ -606,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
                     yacc = fmaf(sel_w[j], part, yacc);
                 }
                 yacc = warp_sum(yacc);
-                if (lane == 0) p.y[r0 + rr] = yacc;
+                if (lane == 0) p.y[r0 + rr] = epilogue_value(p.ep, 0, H, r0 + rr, yacc);
             }
         }
     }
@@ -703,7 +740,8 @@ bool decode_fused_supported(int dev, int T, int H, int E, int k, int I) {
     return fused_config(H, E, k, I, g_fused_blocks[dev], g_fused_max_smem[dev], c);
 }
 
-cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const float *bias,
+cudaError_t launch_decode_fused(int dev, const float *x, const float *norm_w, float eps,
+                                const OutEpilogue &ep, const float *Wr, const float *bias,
                                 const int32_t *idx_in, const float *w_in, int32_t *idx_out,
                                 float *w_out, const uint8_t *gate, const uint8_t *up,
                                 const uint8_t *down, int H, int E, int k, int I, float *y,
@@ -715,6 +753,9 @@ cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const 
         return cudaErrorInvalidValue;
     fused::Params p;
     p.x = x;
+    p.norm_w = norm_w;
+    p.eps = eps;
+    p.ep = ep;
     p.Wr = Wr;
     p.bias = bias;
     p.idx_in = idx_in;

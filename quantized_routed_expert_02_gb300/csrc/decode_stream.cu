@@ -154,7 +154,7 @@ template <int NB>
 __global__ void __launch_bounds__(kDnThreads, 1)
     stream_down_kernel(const float *__restrict__ h, const uint8_t *__restrict__ down,
                        const int32_t *__restrict__ idx, const float *__restrict__ w, int k, int E,
-                       int H, int I, float *__restrict__ y, WsHeader *hdr) {
+                       int H, int I, float *__restrict__ y, WsHeader *hdr, const OutEpilogue ep) {
     extern __shared__ __align__(16) float sm[];
     const int plen = padded_len(I), runs = I / 32;
     float *hs = sm;                       // [k][plen]
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kDnThreads, 1)
                 acc = fmaf(wj[j], warp_sum(part), acc);
             }
         }
-        if (lane == 0) y[r] = acc;
+        if (lane == 0) y[r] = epilogue_value(ep, 0, H, r, acc);
     }
 }
 
@@ -372,7 +372,8 @@ template <int G>
 __global__ void __launch_bounds__(kDgThreads, 1)
     stream_down_rows_kernel(const float *__restrict__ h, const uint8_t *__restrict__ down,
                             const int32_t *__restrict__ idx, const float *__restrict__ w, int k,
-                            int E, int H, int I, float *__restrict__ y, WsHeader *hdr) {
+                            int E, int H, int I, float *__restrict__ y, WsHeader *hdr,
+                            const OutEpilogue ep) {
     extern __shared__ __align__(16) uint8_t smd[];
     const int n = k * I, UD = n >> 6, upr = I >> 6;
     uint8_t *planes = smd;                                      // 3n bytes
@@ -414,7 +415,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
             }
         }
         acc = warp_sum(acc);
-        if (lane == 0) y[r] = acc;
+        if (lane == 0) y[r] = epilogue_value(ep, 0, H, r, acc);
     }
 }
 
@@ -476,7 +477,7 @@ bool decode_stream_supported(int dev, int T, int H, int E, int k, int I) {
 cudaError_t launch_decode_stream(const float *x, const int32_t *idx, const float *w,
                                  const uint8_t *gate, const uint8_t *up, const uint8_t *down,
                                  int H, int E, int k, int I, float *y, float *hbuf, WsHeader *hdr,
-                                 int num_sms, cudaStream_t s) {
+                                 const OutEpilogue &ep, int num_sms, cudaStream_t s) {
     using namespace dst;
     const int nbh = (H / kQK + 7) / 8, nbi = (I / kQK + 7) / 8;
     const size_t sg = gateup_smem(H, k), sd = down_smem(I, k);
@@ -494,23 +495,23 @@ cudaError_t launch_decode_stream(const float *x, const int32_t *idx, const float
         const int ud = k * I / 64;  // units per output row; lanes take ceil(ud / 32) each
         const size_t sdd = down_digits_smem(k, I);
         if (ud <= 32)
-            stream_down_rows_kernel<1><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+            stream_down_rows_kernel<1><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
         else if (ud <= 64)
-            stream_down_rows_kernel<2><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+            stream_down_rows_kernel<2><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
         else if (ud <= 128)
-            stream_down_rows_kernel<4><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+            stream_down_rows_kernel<4><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
         else if (ud <= 192)
-            stream_down_rows_kernel<6><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+            stream_down_rows_kernel<6><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
         else  // four units per lane in flight, looping over the rest (a wider
               // batch of loads per lane would spill at the 128-register cap)
-            stream_down_rows_kernel<4><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+            stream_down_rows_kernel<4><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
     }
     else if (nbi <= 1)
-        stream_down_kernel<1><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+        stream_down_kernel<1><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
     else if (nbi <= 2)
-        stream_down_kernel<2><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+        stream_down_kernel<2><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
     else
-        stream_down_kernel<4><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr);
+        stream_down_kernel<4><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
     return cudaGetLastError();
 }
 

@@ -187,11 +187,13 @@ __global__ void __launch_bounds__(256) down_kernel(const float *__restrict__ h,
 }
 
 // y[t, :] = sum_j w[t,j] * o[t*k+j, :], j = 0..k-1 in order; slots with an
-// expert index outside [0,E) are skipped.
+// expert index outside [0,E) are skipped.  The epilogue then copies token
+// cap_t's row out and adds the residual stream.
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ o,
                                                       const int32_t *__restrict__ idx,
                                                       const float *__restrict__ w, int T, int H,
-                                                      int E, int k, float *__restrict__ y) {
+                                                      int E, int k, float *__restrict__ y,
+                                                      const OutEpilogue ep) {
     const int h4 = H >> 2;
     const size_t total = size_t(T) * h4;
     for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total;
@@ -208,15 +210,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
             acc.z = fmaf(wj, v.z, acc.z);
             acc.w = fmaf(wj, v.w, acc.w);
         }
+        if (ep.capture != nullptr && t == ep.cap_t) reinterpret_cast<float4 *>(ep.capture)[c] = acc;
+        if (ep.residual != nullptr) {
+            const float4 r = reinterpret_cast<const float4 *>(ep.residual + size_t(t) * H)[c];
+            acc = make_float4(r.x + acc.x, r.y + acc.y, r.z + acc.z, r.w + acc.w);
+        }
         reinterpret_cast<float4 *>(y + size_t(t) * H)[c] = acc;
     }
 }
 
 cudaError_t launch_combine(const float *obuf, const int32_t *idx, const float *w, int T, int H,
-                           int E, int k, float *y, int num_sms, cudaStream_t s) {
+                           int E, int k, float *y, const OutEpilogue &ep, int num_sms,
+                           cudaStream_t s) {
     const size_t total = size_t(T) * (H / 4);
     const size_t g3s = (total + 255) / 256, g3cap = size_t(num_sms) * 16;
-    combine_kernel<<<int(g3s < g3cap ? g3s : g3cap), 256, 0, s>>>(obuf, idx, w, T, H, E, k, y);
+    combine_kernel<<<int(g3s < g3cap ? g3s : g3cap), 256, 0, s>>>(obuf, idx, w, T, H, E, k, y, ep);
     return cudaGetLastError();
 }
 
@@ -231,8 +239,8 @@ cudaError_t launch_expert_ffn(const float *x, const int32_t *idx, const float *w
                               const uint8_t *gate, const uint8_t *up, const uint8_t *down, int T,
                               int H, int E, int k, int I, float *y, const int32_t *offs,
                               const int32_t *perm, const int32_t *active, const int32_t *nactive,
-                              float *hbuf, float *obuf, WsHeader *hdr, int num_sms,
-                              cudaStream_t s) {
+                              float *hbuf, float *obuf, WsHeader *hdr, const OutEpilogue &ep,
+                              int num_sms, cudaStream_t s) {
     const int max_active = min(E, T * k);
     const size_t smem_gu = sizeof(float) * kTokGroup * (H + H / 16);
     const size_t smem_dn = sizeof(float) * kTokGroup * (I + I / 16);
@@ -246,7 +254,7 @@ cudaError_t launch_expert_ffn(const float *x, const int32_t *idx, const float *w
     const size_t total = size_t(T) * (H / 4);
     const size_t g3s = (total + 255) / 256, g3cap = size_t(num_sms) * 16;
     int g3 = int(g3s < g3cap ? g3s : g3cap);
-    combine_kernel<<<g3, 256, 0, s>>>(obuf, idx, w, T, H, E, k, y);
+    combine_kernel<<<g3, 256, 0, s>>>(obuf, idx, w, T, H, E, k, y, ep);
     return cudaGetLastError();
 }
 

@@ -28,11 +28,16 @@ cudaError_t launch_expert_ffn(const float *x, const int32_t *idx, const float *w
                               const uint8_t *gate, const uint8_t *up, const uint8_t *down, int T,
                               int H, int E, int k, int I, float *y, const int32_t *offs,
                               const int32_t *perm, const int32_t *active, const int32_t *nactive,
-                              float *hbuf, float *obuf, WsHeader *hdr, int num_sms,
-                              cudaStream_t s);
+                              float *hbuf, float *obuf, WsHeader *hdr, const OutEpilogue &ep,
+                              int num_sms, cudaStream_t s);
 
 cudaError_t launch_combine(const float *obuf, const int32_t *idx, const float *w, int T, int H,
-                           int E, int k, float *y, int num_sms, cudaStream_t s);
+                           int E, int k, float *y, const OutEpilogue &ep, int num_sms,
+                           cudaStream_t s);
+
+// Pre-FFN RMSNorm of T rows: xn = x / sqrt(mean(x^2) + eps) * gamma.
+cudaError_t launch_rmsnorm(const float *x, const float *gamma, float eps, int T, int H, float *xn,
+                           cudaStream_t s);
 
 cudaError_t init_prefill_tc(int dev);
 bool prefill_tc_supported(int T, int H, int E, int k, int I);
@@ -50,8 +55,10 @@ bool decode_fused_supported(int dev, int T, int H, int E, int k, int I);
 // kernel routes and writes idx_out / w_out (moe_layer).  `sync` is the tag
 // region (kSyncWords words, zero or tags of earlier calls of this header),
 // `hbuf` k*I floats of scratch; `timeline` (timeline_cap words) is written
-// only by profiling builds.
-cudaError_t launch_decode_fused(int dev, const float *x, const float *Wr, const float *bias,
+// only by profiling builds.  `norm_w` (nullable): x is RMS-normalised with
+// it (and `eps`) before anything uses it; `ep`: the output epilogue.
+cudaError_t launch_decode_fused(int dev, const float *x, const float *norm_w, float eps,
+                                const OutEpilogue &ep, const float *Wr, const float *bias,
                                 const int32_t *idx_in, const float *w_in, int32_t *idx_out,
                                 float *w_out, const uint8_t *gate, const uint8_t *up,
                                 const uint8_t *down, int H, int E, int k, int I, float *y,
@@ -67,6 +74,6 @@ bool decode_stream_supported(int dev, int T, int H, int E, int k, int I);
 cudaError_t launch_decode_stream(const float *x, const int32_t *idx, const float *w,
                                  const uint8_t *gate, const uint8_t *up, const uint8_t *down,
                                  int H, int E, int k, int I, float *y, float *hbuf, WsHeader *hdr,
-                                 int num_sms, cudaStream_t s);
+                                 const OutEpilogue &ep, int num_sms, cudaStream_t s);
 
 }  // namespace moeq4k

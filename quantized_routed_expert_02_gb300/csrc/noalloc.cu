@@ -83,7 +83,8 @@ extern "C" moe_status moe_layer_noalloc(const float *x, const float *Wr, const f
                   "status and detail lead the header");
     if (cudaMemsetAsync(scratch, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
     cudaError_t err = launch_decode_fused(
-        dev, x, Wr, bias, nullptr, nullptr, idx, w, static_cast<const uint8_t *>(gate),
+        dev, x, nullptr, 0.f, OutEpilogue{}, Wr, bias, nullptr, nullptr, idx, w,
+        static_cast<const uint8_t *>(gate),
         static_cast<const uint8_t *>(up), static_cast<const uint8_t *>(down), H, E, k, I, y,
         reinterpret_cast<unsigned long long *>(scratch + kNoallocSyncOff),
         reinterpret_cast<float *>(scratch + kNoallocHOff), reinterpret_cast<WsHeader *>(scratch), 0,

@@ -41,6 +41,8 @@ _SIGS = {
                   ctypes.c_int),
     "moe_layer_host": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P],
                        ctypes.c_int),
+    "moe_layer_block": ([_P, _P, ctypes.c_float, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
+                         _P, _I, _I, _P, _P, _P, _P, _S, _P], ctypes.c_int),
     "moe_read_device_status": ([_P, _P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
     "moe_layer_noalloc": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P],
                           ctypes.c_int),
@@ -147,6 +149,20 @@ def moe_layer(x, Wr, bias, gate, up, down, k, I, idx, w, y, ws, stream=None) -> 
     _check(_lib.moe_layer(_ptr(x), _ptr(Wr), _ptr(bias), _ptr(gate), _ptr(up), _ptr(down),
                           T, H, E, k, I, _ptr(idx), _ptr(w), _ptr(y), _ptr(ws), ws.numel(),
                           _stream(stream)), "moe_layer")
+
+
+def moe_layer_block(hidden, norm_w, eps, Wr, bias, gate, up, down, k, I, idx, w, out, ws,
+                    add_residual=True, capture_token=-1, cap_idx=None, cap_w=None, cap_ffn=None,
+                    stream=None) -> None:
+    """RMSNorm (``norm_w`` None: none) -> router -> expert FFN -> residual
+    add; optional capture of one token's routing and pre-residual output."""
+    T, H = hidden.shape
+    E = Wr.shape[0]
+    _check(_lib.moe_layer_block(_ptr(hidden), _ptr(norm_w), float(eps), _ptr(Wr), _ptr(bias),
+                                _ptr(gate), _ptr(up), _ptr(down), T, H, E, k, I, _ptr(idx),
+                                _ptr(w), _ptr(out), 1 if add_residual else 0, int(capture_token),
+                                _ptr(cap_idx), _ptr(cap_w), _ptr(cap_ffn), _ptr(ws), ws.numel(),
+                                _stream(stream)), "moe_layer_block")
 
 
 def moe_layer_host(x_host, Wr, bias, gate, up, down, k, I, idx, w, y_host, ws,
