@@ -87,6 +87,17 @@ struct Ws {
     int timeline_cap() const { return int((L.x16 - L.o) / sizeof(unsigned long long)); }
 };
 
+// Profiling builds: the grouped GEMMs' per-stage stamps go to the fp32
+// expert-activation region, which the tensor-core path does not use.
+unsigned long long *gemm_timeline(const Ws &ws) {
+#ifdef MOEQ4K_TIMELINE
+    if (ws.L.o - ws.L.h >= 2 * 12 * 256 * sizeof(unsigned long long)) return ws.u64(ws.L.h);
+#else
+    (void)ws;
+#endif
+    return nullptr;
+}
+
 moe_status check_ws(void *ws, size_t ws_bytes, const WsLayout &L) {
     MOE_TRY(check_ptr(ws, 256));
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
@@ -109,7 +120,8 @@ moe_status ffn_enqueue(const float *x, const int32_t *idx, const float *w, const
             static_cast<const uint8_t *>(down), T, H, E, k, I, ws.i32(L.offs), ws.i32(L.perm),
             ws.i32(L.slotpos), ws.i32(L.active), ws.i32(L.nactive), reinterpret_cast<__half *>(ws.base + L.x16),
             reinterpret_cast<__half *>(ws.base + L.h16), ws.f32(L.o),
-            reinterpret_cast<TcChunk *>(ws.base + L.chunks), ws.hdr(), sms, g_wait_ns, s)));
+            reinterpret_cast<TcChunk *>(ws.base + L.chunks), ws.hdr(), sms, g_wait_ns,
+            gemm_timeline(ws), s)));
         return cuda_status(launch_combine(ws.f32(L.o), idx, w, T, H, E, k, y, ep, sms, s));
     }
     return cuda_status(launch_expert_ffn(

@@ -5,40 +5,41 @@
 // forward_qwen3_moe.rs (aprender-serve 0.35.0), step 2g of forward_qwen3_moe
 // runs every position through the layer on its own; tokens are independent,
 // so the slots routed to one expert form the columns of one GEMM per expert:
-//   gate/up:  G = Wg[e] X_e^T, U = Wu[e] X_e^T  (M = 128 weight rows per tile,
-//             N = up to 256 tokens, K = H), epilogue h = SiLU(G) * U (fp16);
-//   down:     O = Wd[e] H_e^T (K = I), epilogue o[p, row] in fp32, followed
+//   gate/up:  G = X_e Wg[e]^T, U = X_e Wu[e]^T  (128 weight rows of each per
+//             tile, up to 256 tokens, K = H), epilogue h = SiLU(G) * U (fp16);
+//   down:     O = H_e Wd[e]^T (K = I), epilogue o[p, row] in fp32, followed
 //             by the slot-ordered combine kernel.
 // The activations are first gathered into expert-sorted rows (fp16), and h
 // is written in that order too, so every activation tile is one contiguous
 // block of rows.
 //
-// One persistent CTA per SM takes work items (expert chunk of <= cap slots x
-// 128 rows each of gate and up, or 256 rows of down: two A operands that
-// share every activation tile) from an atomic counter; cap is 256, or the
-// batch's token count rounded up to 32 when that is smaller.  12 warps:
-//   thread 32   stages the raw Q4_K bytes of each K stage (64 weights per
-//               row: the 16-byte block head and the 32 code bytes) for the
-//               tile's 128 rows with two 2-D TMA copies per matrix, into a
-//               ring of raw slots as deep as shared memory allows (5 stages
-//               at cap 256, up to 16 for small batches): these come from HBM
-//               and need the most latency cover;
-//   warps 4-11  dequantise them into fp16 K-major tiles with the 128-byte
-//               swizzle (generic stores, then a proxy fence), into a ring of
-//               weight tiles (2 slots; 4 when cap <= 64, where each stage's
-//               MMAs are short and the ring covers their completion latency);
-//   thread 64   loads the chunk's activation tile (its sorted rows rounded
-//               up to 32, x 64 K, fp16) with 2-D TMA copies of 32 rows that
-//               apply the 128-byte swizzle, into a ring of 3 slots of cap
-//               rows (4 when cap <= 64);
-//   thread 0    issues tcgen05.mma (fp16 x fp16 -> fp32 in tensor memory)
-//               once a stage's weight and activation tiles are both in, and
-//               commits its completion to both rings' "empty" mbarriers;
-//   all warps   read the accumulators back (tcgen05.ld) for the epilogue
-//               once the item's MMAs are complete, each warp a third of the
-//               columns of its TMEM lane quadrant.
-// Every wait is bounded by a global-timer deadline and records
-// MOE_ERR_TIMEOUT when it runs out.
+// One persistent CTA per SM; work items (expert chunk of <= cap slots x 128
+// rows each of gate and up, or 256 rows of down) are taken round-robin
+// (item = CTA + i * grid), row tile fastest, so every role walks the same
+// sequence without an exchange and one running stage count per ring carries
+// the pipeline across item boundaries.  cap = the batch's token count
+// rounded up to 32, at most 256.  20 warps:
+//   thread 32   raw Q4_K bytes by TMA: one whole block (144 contiguous bytes)
+//               of each of the tile's rows per raw stage, 2 x 128 rows;
+//   warps 4-19  dequantise each raw stage into four 64-K stages of fp16
+//               K-major tiles with the 128-byte swizzle (generic stores, then
+//               a proxy fence), thread = (row, half of the stage's codes);
+//               after the first stages of the next item they run the
+//               previous item's epilogue;
+//   thread 64   the chunk's activation rows of each stage by TMA (boxes of 32
+//               rows, 128-byte swizzle) into a ring of chunk-sized slots;
+//   thread 0    issues tcgen05.mma with the tokens as the M operand:
+//               D[tokens][256 weight rows] (+)= A[128 tokens][16 K] x
+//               B[256 rows][16 K]^T, the activation tile as M = 128 (two
+//               halves for 256-slot chunks) and the stage's gate and up (or
+//               two down) tiles as one N = 256 operand: four (eight) MMAs per
+//               64-K stage whatever the token count; accumulators fp32 in
+//               tensor memory, double-buffered for chunks of <= 128 slots so an
+//               item's epilogue overlaps the next item's MMAs.
+// The epilogue reads one token per TMEM lane and writes whole 16-byte runs
+// of that token's row: h = SiLU(g) * u in fp16 (gate/up), or the per-slot
+// fp32 outputs (down).  Every wait is bounded by a global-timer deadline and
+// records MOE_ERR_TIMEOUT when it runs out.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -51,22 +52,25 @@
 namespace moeq4k {
 namespace ptc {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 640;  // 4 role warps + 16 dequantise/epilogue warps
 constexpr int kBM = 128;   // weight rows per tile
-constexpr int kBN = 256;   // tokens per tile (max)
+constexpr int kBN = 256;   // tokens per tile (max): two M = 128 halves
 constexpr int kBK = 64;    // K per stage
 constexpr int kTileA = kBM * kBK * 2;
 constexpr int kBoxRows = 32;                   // activation rows per TMA box
 constexpr int kBoxB = kBoxRows * kBK * 2;
+constexpr int kActSlot = kBM * kBK * 2;        // activation tile: 128 rows x 64 K fp16
+constexpr int kStageSlot = 2 * kTileA;         // stage ring slot: the two weight tiles
 constexpr int kHead = 2048;  // barriers, item info, token list
-constexpr int kDeq = 256;      // warps 4-11
+constexpr int kDeq = 512;      // warps 4-19
 constexpr int kMaxSlots = 16;  // per ring
-constexpr int kRawHead = kBM * 16;               // block heads of a tile's rows
-constexpr int kRawMat = kBM * (16 + 32);         // one matrix's raw bytes of a stage
+constexpr int kSub = kQK / kBK;                  // MMA stages per Q4_K block (4)
+constexpr int kRawMat = kBM * kBlockBytes;       // one matrix's raw bytes of a raw stage:
+                                                 // one whole block (144 B) of each row
 
 struct Params {
-    CUtensorMap head0, codes0;  // raw Q4_K bytes of A0 as [E*rows][row bytes] uint8:
-    CUtensorMap head1, codes1;  //   boxes of 16 B (block head) and 32 B (codes) x 128 rows
+    CUtensorMap raw0, raw1;     // raw Q4_K bytes of the two A operands as [E*rows][row bytes]
+                                //   uint8: boxes of one block (144 B) x 128 rows
     CUtensorMap mapB;           // activations [T*k sorted rows][K] fp16, 128-byte swizzle
     int mode;                   // 0: gate/up + SwiGLU -> h16; 1: down -> o
     int K;                      // reduction length
@@ -82,11 +86,28 @@ struct Params {
     int I, H;
     int rows_per_expert;        // I (mode 0) or H (mode 1)
     int nr, r_off;              // raw ring: slots, byte offset (slot = nmat * kRawMat bytes)
-    int na, a_off;              // weight-tile ring: slots, byte offset (slot = nmat * kTileA)
-    int nb, b_off, b_slot;      // activation-tile ring: slots, byte offset, bytes per slot
-                                //   (chunk capacity x 128 B)
+    int mh;                     // M halves: 1 (chunks of <= 128 slots, two accumulator
+                                //   buffers) or 2 (<= 256 slots, one buffer of two halves)
+    int ns, s_off;              // stage ring: slots, byte offset (slot = kStageSlot bytes)
+    int nb, b_off, b_slot;      // activation ring: slots, byte offset, bytes per slot (the
+                                //   chunk capacity x 128 B; kActSlot - b_slot bytes of
+                                //   padding follow the last slot)
     unsigned long long wait_ns;
+    unsigned long long *timeline;  // profiling builds only: per-stage role stamps of CTA 0
 };
+
+// Optional per-stage timeline for profiling builds (-DMOEQ4K_TIMELINE): the
+// listed thread of CTA 0 stamps the global timer for event `ev` of global
+// stage (or item) `g` < 256.
+#ifdef MOEQ4K_TIMELINE
+#define GT_STAMP(p, ev, g)                                                        \
+    do {                                                                          \
+        if (blockIdx.x == 0 && (p).timeline != nullptr && (g) < 256u)             \
+            (p).timeline[(ev) * 256 + (g)] = global_timer_ns();                  \
+    } while (0)
+#else
+#define GT_STAMP(p, ev, g) ((void)0)
+#endif
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                             uint64_t *bar) {
@@ -104,31 +125,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_
     return false;
 }
 
-__device__ __forceinline__ float u6f(uint32_t v) { return __uint_as_float(0x4B000000u | v) - 8388608.0f; }
-
-// (d*sc, dmin*m) of sub-blocks 2c and 2c+1 from a 16-byte block head.
-__device__ __forceinline__ void head_scales(const uint4 &h, int c, float &a0, float &b0, float &a1,
-                                            float &b1) {
-    const int j0 = 2 * c, j1 = 2 * c + 1;
-    uint32_t s0, m0, s1, m1;
-    if (c < 2) {
-        s0 = (h.y >> (8 * j0)) & 63u;
-        m0 = (h.z >> (8 * j0)) & 63u;
-        s1 = (h.y >> (8 * j1)) & 63u;
-        m1 = (h.z >> (8 * j1)) & 63u;
-    } else {
-        const int a = j0 - 4, b = j1 - 4;
-        s0 = ((h.w >> (8 * a)) & 15u) | (((h.y >> (8 * a + 6)) & 3u) << 4);
-        m0 = ((h.w >> (8 * a + 4)) & 15u) | (((h.z >> (8 * a + 6)) & 3u) << 4);
-        s1 = ((h.w >> (8 * b)) & 15u) | (((h.y >> (8 * b + 6)) & 3u) << 4);
-        m1 = ((h.w >> (8 * b + 4)) & 15u) | (((h.z >> (8 * b + 6)) & 3u) << 4);
-    }
-    const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&h.x));
-    a0 = dd.x * u6f(s0);
-    a1 = dd.x * u6f(s1);
-    b0 = dd.y * u6f(m0);
-    b1 = dd.y * u6f(m1);
-}
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
 // K order inside the fp16 operand tiles: within each aligned group of four,
 // positions 1 and 2 are swapped (the dequantiser below produces that order
@@ -136,287 +134,478 @@ __device__ __forceinline__ void head_scales(const uint4 &h, int c, float &a0, fl
 // order, so every dot product is unchanged).
 __host__ __device__ inline int kperm(int k) { return (k & ~3) | ((k & 1) << 1) | ((k >> 1) & 1); }
 
-__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
-__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
-
-// w = q*a - b for the 8 codes of one 16-byte output chunk: nibble `shift`
-// (0 low, 4 high) of bytes 0..3 of v0, then of v1.  (v >> s) & 0x000F000F |
-// 0x64006400 puts two codes into the low mantissa bits of the fp16 value
-// 1024 (bytes 0 and 2, or 1 and 3); subtracting 1024 is exact, then one
-// fused multiply-add per pair applies d*sc and dmin*m with one rounding.
-// Output order: codes 0, 2, 1, 3, 4, 6, 5, 7.
-__device__ __forceinline__ uint4 weights8(uint32_t v0, uint32_t v1, int shift, __half2 a2,
-                                          __half2 nb2) {
+// d*sc and -dmin*m of sub-blocks 2c and 2c+1 from a 16-byte block head, as
+// fp16 pairs A = (d*sc0, d*sc1), NB = (-dmin*m0, -dmin*m1).  The 6-bit
+// fields land in the low mantissa bits of the fp16 value 1024 (exact), 1024
+// is subtracted exactly, and one fp16 multiply per pair rounds each product
+// once.  Fields: sub-block j < 4: sc = scales[j] & 63, m = scales[j+4] & 63;
+// j >= 4: sc = scales[j+4] & 15 | (scales[j-4] >> 6) << 4,
+//         m = scales[j+4] >> 4 | (scales[j] >> 6) << 4 (head.y = scales[0..3],
+// head.z = scales[4..7], head.w = scales[8..11]).
+__device__ __forceinline__ void stage_scales_h2(const uint4 &h, int c, __half2 &A, __half2 &NB) {
+    // bytes 2(c%2) and 2(c%2)+1 of a head word to bits 0-7 and 16-23
+    const uint32_t sel = 0x4140u + 0x202u * uint32_t(c & 1);
+    uint32_t sc, mm;
+    if (c < 2) {
+        sc = __byte_perm(h.y, 0u, sel);
+        mm = __byte_perm(h.z, 0u, sel);
+    } else {
+        const uint32_t wp = __byte_perm(h.w, 0u, sel);
+        const uint32_t yp = __byte_perm(h.y, 0u, sel);
+        const uint32_t zp = __byte_perm(h.z, 0u, sel);
+        sc = (wp & 0x000F000Fu) | ((yp >> 2) & 0x00300030u);
+        mm = ((wp >> 4) & 0x000F000Fu) | ((zp >> 2) & 0x00300030u);
+    }
     const __half2 k1024 = bits_h2(0x64006400u);
-    const uint32_t p0 = ((v0 >> shift) & 0x000F000Fu) | 0x64006400u;
-    const uint32_t p1 = ((v0 >> (shift + 8)) & 0x000F000Fu) | 0x64006400u;
-    const uint32_t p2 = ((v1 >> shift) & 0x000F000Fu) | 0x64006400u;
-    const uint32_t p3 = ((v1 >> (shift + 8)) & 0x000F000Fu) | 0x64006400u;
+    const __half2 scv = __hsub2(bits_h2((sc & 0x003F003Fu) | 0x64006400u), k1024);
+    const __half2 mneg = __hsub2(k1024, bits_h2((mm & 0x003F003Fu) | 0x64006400u));
+    A = __hmul2(bits_h2(__byte_perm(h.x, 0u, 0x1010u)), scv);    // (d, d) * (sc0, sc1)
+    NB = __hmul2(bits_h2(__byte_perm(h.x, 0u, 0x3232u)), mneg);  // (dmin, dmin) * (-m0, -m1)
+}
+
+// (v & 0x000F000F) | 0x64006400: the codes in bits 0-3 and 16-19 as the fp16
+// values 1024 + q (exact).
+__device__ __forceinline__ uint32_t code_pair(uint32_t v) { return (v & 0x000F000Fu) | 0x64006400u; }
+
+// q*a + nb for one pair: the subtraction of 1024 is exact, the fused
+// multiply-add rounds once.
+__device__ __forceinline__ uint32_t weight_pair(uint32_t p, __half2 a, __half2 nb) {
+    return h2_bits(__hfma2(__hsub2(bits_h2(p), bits_h2(0x64006400u)), a, nb));
+}
+
+// The 8 weights of one 16-byte tile chunk from code words va, vb (bytes
+// 4i..4i+7 of the stage's codes): nibble SH (0 low, 4 high) of bytes 0..3
+// of va then of vb, in the kperm order 0, 2, 1, 3, 4, 6, 5, 7.
+template <int SH>
+__device__ __forceinline__ uint4 chunk8(uint32_t va, uint32_t vb, __half2 a, __half2 nb) {
     uint4 r;
-    r.x = h2_bits(__hfma2(__hsub2(bits_h2(p0), k1024), a2, nb2));
-    r.y = h2_bits(__hfma2(__hsub2(bits_h2(p1), k1024), a2, nb2));
-    r.z = h2_bits(__hfma2(__hsub2(bits_h2(p2), k1024), a2, nb2));
-    r.w = h2_bits(__hfma2(__hsub2(bits_h2(p3), k1024), a2, nb2));
+    r.x = weight_pair(code_pair(va >> SH), a, nb);
+    r.y = weight_pair(code_pair(va >> (SH + 8)), a, nb);
+    r.z = weight_pair(code_pair(vb >> SH), a, nb);
+    r.w = weight_pair(code_pair(vb >> (SH + 8)), a, nb);
     return r;
 }
 
-struct RawStage {
-    uint4 head, q0, q1;  // block head and the 32 code bytes of this stage's 64 weights
-};
-
-// Row r of a matrix's raw stage: its 16-byte block head and 32 code bytes.
-__device__ __forceinline__ RawStage raw_from_smem(const uint8_t *mat, int r) {
-    RawStage v;
-    v.head = *reinterpret_cast<const uint4 *>(mat + 16 * r);
-    v.q0 = *reinterpret_cast<const uint4 *>(mat + kRawHead + 32 * r);
-    v.q1 = *reinterpret_cast<const uint4 *>(mat + kRawHead + 32 * r + 16);
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
     return v;
 }
 
-// Write `nchunks` 16-byte chunks (weights 8j..8j+7 for j in [j0, j0+nchunks),
-// in the kperm order) of row `r` of the stage's 64 weights into a swizzled
-// tile.
-__device__ __forceinline__ void store_row(uint8_t *tile, int r, const RawStage &raw, int s, int j0,
-                                          int nchunks) {
-    float a0, b0, a1, b1;
-    head_scales(raw.head, s & 3, a0, b0, a1, b1);
-    const __half2 A0 = __float2half2_rn(a0), A1 = __float2half2_rn(a1);
-    const __half2 NB0 = __float2half2_rn(-b0), NB1 = __float2half2_rn(-b1);
-    const uint32_t w[8] = {raw.q0.x, raw.q0.y, raw.q0.z, raw.q0.w,
-                           raw.q1.x, raw.q1.y, raw.q1.z, raw.q1.w};
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-        if (jj < j0 || jj >= j0 + nchunks) continue;
-        // chunk jj < 4: low nibbles of code bytes 8jj..8jj+7 (sub-block 2c);
-        // chunk jj >= 4: high nibbles of bytes 8(jj-4).. (sub-block 2c+1)
-        const int wb = 2 * (jj & 3);
-        const uint4 out = jj < 4 ? weights8(w[wb], w[wb + 1], 0, A0, NB0)
-                                 : weights8(w[wb], w[wb + 1], 4, A1, NB1);
-        *reinterpret_cast<uint4 *>(tile + tc::sw128_offset(r, 8 * jj)) = out;
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4 &v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// A bounded wait by every lane of a warp, with one verdict for the warp (a
+// lane that saw the phase complete just as another hit the deadline still
+// takes the abort path with it), so the warp never splits at a __syncwarp.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t deadline,
+                                          WsHeader *hdr, int site) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, deadline, hdr, site));
+}
+
+// Position in a ring of n slots: the slot and the parity of its current
+// phase (how many times the ring wrapped, mod 2), advanced without division.
+struct RingPos {
+    uint32_t slot = 0, phase = 0;
+    __device__ __forceinline__ void next(uint32_t n) {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1u;
+        }
     }
+};
+
+// One work item: expert chunk `ch` (its sorted slots) x weight-row tile `rt`.
+struct Item {
+    TcChunk ch;
+    int rt, nmma, row0;  // MMA width (slots rounded up to 16), first sorted activation row
+};
+
+// Items run row-tile fastest: the row tiles of one chunk (which share its
+// activation rows) and the chunks of one expert (which share its weight rows)
+// are consecutive items, so they run at the same time on neighbouring CTAs
+// and the second and later reads of those bytes are L2 hits.
+__device__ __forceinline__ Item item_of(const Params &p, int it, int nch) {
+    (void)nch;
+    Item I;
+    I.ch = p.chunks[it / p.row_tiles];
+    I.rt = it % p.row_tiles;
+    I.nmma = (I.ch.tok_cnt + 15) & ~15;
+    I.row0 = p.offs[I.ch.e] + I.ch.tok_off;
+    return I;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *rfull = reinterpret_cast<uint64_t *>(smem);
     uint64_t *rempty = rfull + kMaxSlots;
-    uint64_t *afull = rempty + kMaxSlots;
-    uint64_t *aempty = afull + kMaxSlots;
-    uint64_t *bfull = aempty + kMaxSlots;
-    uint64_t *bempty = bfull + kMaxSlots;
-    uint64_t *done = bempty + kMaxSlots;
-    uint64_t *drain = done + 1;
+    // stage ring: the two weight tiles of an MMA stage (2 x 16 KB per slot);
+    // activation ring: the chunk's activation rows of an MMA stage
+    uint64_t *sfull = rempty + kMaxSlots;   // weight tiles written
+    uint64_t *sempty = sfull + kMaxSlots;   // the stage slot's MMAs are complete
+    uint64_t *bfull = sempty + kMaxSlots;   // the activation copy's bytes (TMA only)
+    uint64_t *bempty = bfull + kMaxSlots;   // the activation slot's MMAs are complete
+    uint64_t *accfull = bempty + kMaxSlots;  // [2] an item's accumulators are complete
+    uint64_t *accempty = accfull + 2;        // [2] the epilogue has read them
+    uint64_t *drain = accempty + 2;
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(drain + 1);
-    int *info = reinterpret_cast<int *>(tmem_ptr + 4);   // [0] item, [1] abort, [2] accumulators ready
-    int *toks = reinterpret_cast<int *>(smem + 1024);    // slot ids of the chunk (<= 256)
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_ptr + 4);
     uint8_t *rring = smem + p.r_off;
-    uint8_t *aring = smem + p.a_off;
+    uint8_t *sring = smem + p.s_off;
     uint8_t *bring = smem + p.b_off;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int NR = p.nr, NA = p.na, NB = p.nb;
+    const int NR = p.nr, NS = p.ns, NB = p.nb;
     constexpr int nmat = 2;  // two A operands per item: gate and up, or two 128-row halves
-    const int S = p.K / kBK;  // stages per item
+    const int S = p.K / kBK;  // MMA stages per item
+    const int SR = S / kSub;  // raw stages per item
     const uint64_t deadline = global_timer_ns() + p.wait_ns;
-    const uint32_t tcols = 512u;  // two 128 x 256 fp32 accumulators
+    const uint32_t tcols = 512u;  // two 256-column accumulators (buffers, or M halves)
+    const uint32_t nbuf = p.mh == 2 ? 1u : 2u;  // accumulator buffers (item li uses li % nbuf)
 
     if (tid == 0) {
         for (int i = 0; i < NR; ++i) {
             mbar_init(rfull + i, 1);           // the TMA thread's arrival + its bytes
             mbar_init(rempty + i, kDeq / 32);  // one arrival per dequant warp
         }
-        for (int i = 0; i < NA; ++i) {
-            mbar_init(afull + i, kDeq / 32);
-            mbar_init(aempty + i, 1);          // MMA completion
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(sfull + i, kDeq / 32);   // one arrival per dequant warp
+            mbar_init(sempty + i, 1);          // MMA completion
         }
         for (int i = 0; i < NB; ++i) {
-            mbar_init(bfull + i, 1);
-            mbar_init(bempty + i, 1);
+            mbar_init(bfull + i, 1);           // the TMA thread's arrival + its bytes
+            mbar_init(bempty + i, 1);          // MMA completion
         }
-        mbar_init(done, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(accfull + i, 1);             // MMA completion of the item's last stage
+            mbar_init(accempty + i, kDeq / 32);    // every epilogue warp has read them
+        }
         mbar_init(drain, 1);
-        info[1] = 0;
+        *abort_flag = 0;
         fence_mbar_init();
     }
+    // the activation ring starts as zeros: the MMA reads all 128 rows of a
+    // slot, and rows no copy has written must hold finite values
+    // the activation ring (and the padding after it) starts as zeros: the MMA
+    // reads 128 rows from a slot's start, and rows no copy has written must
+    // hold finite values
+    for (int i = tid; i < (NB * p.b_slot + max(0, kActSlot - p.b_slot)) / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(bring)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();  // before any TMA write into the ring
     if (warp == 0) tc::tmem_alloc(tmem_ptr, tcols);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t taddr = *tmem_ptr;
-    const int total = p.hdr->tc_chunks * p.row_tiles;
+    const int nch = p.hdr->tc_chunks;
+    const int total = nch * p.row_tiles;
+    // Items are taken round-robin (item = blockIdx.x + i * gridDim.x), so every
+    // role walks the same sequence with no exchange, and one running stage
+    // count per ring carries the pipeline across item boundaries.
+    uint32_t issued = 0;  // threads 32 and 64: copies issued (for the abort drain)
 
-    uint32_t gs = 0;     // stages processed by this CTA (same count in every role)
-    uint32_t items = 0;  // items processed by this CTA
-    uint32_t issued = 0; // threads 32 and 64: stages whose copies this thread issued
-    while (true) {
-        if (tid == 0) info[0] = int(atomicAdd(&p.hdr->tc_work[p.mode], 1u));
-        __syncthreads();
-        const int item = info[0];
-        if (item >= total || info[1]) break;
-        const TcChunk ch = p.chunks[item / p.row_tiles];
-        const int rt = item % p.row_tiles;
-        const int ntok = ch.tok_cnt;
-        const int nmma = (ntok + 15) & ~15;
-        for (int n = tid; n < ntok; n += kThreads) toks[n] = p.perm[p.offs[ch.e] + ch.tok_off + n];
-        __syncthreads();
+    if (warp >= 4) {
+        // ---- dequantise weight rows into the A tiles; after the first stages
+        // of the next item, run the previous item's epilogue
+        // thread -> (row r of A operand m, half hh of the stage's 32 code bytes:
+        // words 4hh..4hh+3, i.e. tile chunks 2hh, 2hh+1 (low nibbles) and
+        // 2hh+4, 2hh+5 (high nibbles))
+        const int dq = tid - 128;
+        const int r = dq & 127;
+        const int m = (dq >> 7) & 1;  // A operand: gate / up, or the first / second 128 rows
+        const int hh = dq >> 8;
+        const uint32_t rbase = smem_addr(rring) + uint32_t(m * kRawMat) + uint32_t(kBlockBytes) * r;
+        const uint32_t til0 = smem_addr(sring) + uint32_t(m * kTileA);
+        // this thread's four tile chunks: 2hh, 2hh+1 (low nibbles), 2hh+4, 2hh+5 (high)
+        uint32_t soff[4];
+        soff[0] = tc::sw128_offset(r, 8 * (2 * hh));
+        soff[1] = tc::sw128_offset(r, 8 * (2 * hh + 1));
+        soff[2] = tc::sw128_offset(r, 8 * (2 * hh + 4));
+        soff[3] = tc::sw128_offset(r, 8 * (2 * hh + 5));
+        const int q = warp & 3, part = (warp - 4) >> 2;  // TMEM lane quadrant, column quarter
 
-        if (warp >= 4) {
-            // ---- dequantise weight rows (raw stage in shared memory) into the A tile(s)
-            const int dq = tid - 128;
-            const int m = dq >> 7;  // A operand: gate / up, or the first / second 128 rows
-            const int r = dq & 127, j0 = 0, nch = 8;
-            for (int s = 0; s < S; ++s) {
-                const uint32_t g = gs + s, rs = g % NR, as = g % NA;
-                if (!wait_bar(rfull + rs, (g / NR) & 1, deadline, p.hdr, 16)) {
-                    info[1] = 1;
-                    break;
-                }
-                const RawStage cur = raw_from_smem(rring + size_t(rs) * nmat * kRawMat + m * kRawMat, r);
-                // The TMA that refills this slot writes through the async proxy:
-                // without a proxy fence after the reads, a refill could land
-                // before reads still in flight are performed.
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(rempty + rs);
-                if (g >= uint32_t(NA) &&
-                    !wait_bar(aempty + as, ((g / NA) - 1) & 1, deadline, p.hdr, 11)) {
-                    info[1] = 1;
-                    break;
-                }
-                store_row(aring + size_t(as) * nmat * kTileA + m * kTileA, r, cur, s, j0, nch);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(afull + as);
-            }
-        } else if (tid == 0) {
-            // ---- MMA issue
-            const uint32_t idesc = tc::idesc_f16_f32(kBM, nmma);
-            for (int s = 0; s < S; ++s) {
-                const uint32_t g = gs + s, as = g % NA, bs = g % NB;
-                if (!wait_bar(afull + as, (g / NA) & 1, deadline, p.hdr, 13) ||
-                    !wait_bar(bfull + bs, (g / NB) & 1, deadline, p.hdr, 18)) {
-                    info[1] = 1;
-                    break;
-                }
-                tc::fence_after_sync();
-                const uint32_t a0 = smem_addr(aring + size_t(as) * nmat * kTileA), a1 = a0 + kTileA;
-                const uint32_t b = smem_addr(bring + size_t(bs) * p.b_slot);
+        // The epilogue of item `E` (the li_e-th of this CTA) from accumulator
+        // buffer li_e & 1.  The accumulator is D[token][weight row]: TMEM lane
+        // = the chunk's token (slot) n, column = weight row c of the item's 256
+        // (gate rows 0-127 then up rows 0-127, or 256 down rows).  Warp (q,
+        // part) reads lanes 32q.. (tokens 32q..32q+31) and half `part` of the
+        // rows; each thread then writes whole 16-byte runs of its token's row.
+        auto epilogue = [&](const Item &E, uint32_t li_e) -> bool {
+            const uint32_t buf = li_e % nbuf, use = li_e / nbuf;
+            if (!warp_wait(accfull + buf, use & 1u, deadline, p.hdr, 14)) return false;
+            tc::fence_after_sync();
+            const int ntok = E.ch.tok_cnt;
+            for (int h = 0; h < p.mh; ++h) {
+            // warp-uniform: quadrants past the chunk's tokens have no output
+            if (128 * h + 32 * q < ntok) {
+                const int n = 128 * h + 32 * q + lane;
+                const bool valid = n < ntok;
+                const uint32_t lanebase = taddr + (buf + uint32_t(h)) * 256u + (uint32_t(q * 32) << 16);
+                if (p.mode == 0) {
+                    // h = SiLU(g) * u for rows 32*part .. +31 of the item's 128,
+                    // stored in the kperm order of the down GEMM's K
+                    __half *hrow = p.h16 + size_t(E.row0 + n) * p.I + E.rt * kBM;
+                    for (int c0 = 32 * part; c0 < 32 * part + 32; c0 += 8) {
+                        float g[8], u[8];
+                        tc::tmem_ld8(lanebase + c0, g);
+                        tc::tmem_ld8(lanebase + 128 + c0, u);
+                        float h[8];
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                    const uint64_t bd = tc::smem_desc_sw128(b + 32 * kk);
-                    const bool acc = s > 0 || kk > 0;
-                    tc::mma_f16(taddr, tc::smem_desc_sw128(a0 + 32 * kk), bd, idesc, acc);
-                    tc::mma_f16(taddr + 256, tc::smem_desc_sw128(a1 + 32 * kk), bd, idesc, acc);
+                        for (int j = 0; j < 8; ++j) {
+                            // SiLU(g) * u with the fast exponential and divide: the
+                            // result is rounded to fp16
+                            const float e = __expf(fminf(-g[j], 80.0f));
+                            h[j] = __fdividef(g[j], 1.0f + e) * u[j];
+                        }
+                        uint4 o;  // positions c0 + (0, 2, 1, 3, 4, 6, 5, 7) hold h[0..7]
+                        o.x = h2_bits(__floats2half2_rn(h[0], h[2]));
+                        o.y = h2_bits(__floats2half2_rn(h[1], h[3]));
+                        o.z = h2_bits(__floats2half2_rn(h[4], h[6]));
+                        o.w = h2_bits(__floats2half2_rn(h[5], h[7]));
+                        if (valid) *reinterpret_cast<uint4 *>(hrow + c0) = o;
+                    }
+                } else {
+                    // per-slot outputs: rows 64*part .. +63 of the item's 256
+                    float *orow = p.o + size_t(valid ? p.perm[E.row0 + n] : 0) * p.H +
+                                  E.rt * p.item_rows;
+                    for (int c0 = 64 * part; c0 < 64 * part + 64; c0 += 8) {
+                        float v[8];
+                        tc::tmem_ld8(lanebase + c0, v);
+                        if (valid) {
+                            *reinterpret_cast<float4 *>(orow + c0) = make_float4(v[0], v[1], v[2], v[3]);
+                            *reinterpret_cast<float4 *>(orow + c0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                        }
+                    }
                 }
-                tc::commit_arrive(aempty + as);
-                tc::commit_arrive(bempty + bs);
             }
-            tc::commit_arrive(done);
-        } else if (tid == 64) {
-            // ---- activation tile of each stage by TMA: the chunk's sorted rows
-            // (rounded up to 32) x 64 K, in boxes of 32 rows
-            const int row0 = p.offs[ch.e] + ch.tok_off;
-            const int nbox = (nmma + kBoxRows - 1) / kBoxRows;
-            for (int s = 0; s < S; ++s) {
-                const uint32_t g = gs + s, bs = g % NB;
-                if (g >= uint32_t(NB) &&
-                    !wait_bar(bempty + bs, ((g / NB) - 1) & 1, deadline, p.hdr, 12)) {
-                    info[1] = 1;
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(accempty + buf);
+            return true;
+        };
+
+        uint32_t g = 0, gr = 0, li = 0;
+        RingPos rp, ap;  // raw ring, stage ring
+        Item prev;
+        bool have_prev = false;
+        bool ok = true;
+        for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++li) {
+            const Item cur = item_of(p, it, nch);
+            if (tid == 128) GT_STAMP(p, 8, li);
+            const int epi_at = min(S, NS) - 1;  // stage after which the previous epilogue runs
+            for (int sr = 0; ok && sr < SR; ++sr, ++gr, rp.next(NR)) {
+                const uint32_t rs = rp.slot;
+                if (!warp_wait(rfull + rs, rp.phase, deadline, p.hdr, 16)) {
+                    ok = false;
                     break;
                 }
+                const uint32_t rsl = rbase + rs * uint32_t(nmat * kRawMat);
+                const uint4 head = lds128(rsl);
+                for (int c = 0; c < kSub; ++c, ++g, ap.next(NS)) {
+                    const int s = sr * kSub + c;
+                    const uint32_t as = ap.slot;
+                    if (tid == 128) GT_STAMP(p, 1, g);
+                    // code bytes 32c..32c+31 of the block: low nibbles = sub-block
+                    // 2c (K 0..31 of the stage), high = 2c+1 (K 32..63)
+                    const uint4 qv = lds128(rsl + 16u + 32u * c + 16u * hh);
+                    if (c == kSub - 1) {
+                        // The TMA that refills this raw slot writes through the async
+                        // proxy: without a proxy fence after the reads, a refill could
+                        // land before reads still in flight are performed.
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(rempty + rs);
+                    }
+                    if (g >= uint32_t(NS) && !warp_wait(sempty + as, ap.phase ^ 1u, deadline, p.hdr, 11)) {
+                        ok = false;
+                        break;
+                    }
+                    if (tid == 128) GT_STAMP(p, 2, g);
+                    __half2 A, NB;
+                    stage_scales_h2(head, c, A, NB);
+                    const __half2 a0 = __low2half2(A), a1 = __high2half2(A);
+                    const __half2 n0 = __low2half2(NB), n1 = __high2half2(NB);
+                    const uint32_t tile = til0 + as * uint32_t(kStageSlot);
+                    sts128(tile + soff[0], chunk8<0>(qv.x, qv.y, a0, n0));
+                    sts128(tile + soff[1], chunk8<0>(qv.z, qv.w, a0, n0));
+                    sts128(tile + soff[2], chunk8<4>(qv.x, qv.y, a1, n1));
+                    sts128(tile + soff[3], chunk8<4>(qv.z, qv.w, a1, n1));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    // one lane also waits for the stage's activation tile, so the
+                    // slot's "full" phase implies both operands are in place
+                    if (lane == 0) mbar_arrive(sfull + as);
+                    if (tid == 128) GT_STAMP(p, 3, g);
+                    if (have_prev && s == epi_at) {
+                        if (tid == 128) GT_STAMP(p, 9, li - 1);
+                        if (!epilogue(prev, li - 1)) ok = false;
+                        if (tid == 128) GT_STAMP(p, 10, li - 1);
+                        have_prev = false;
+                    }
+                }
+            }
+            prev = cur;
+            have_prev = true;
+        }
+        if (ok && have_prev) {
+            if (tid == 128) GT_STAMP(p, 9, li - 1);
+            ok = epilogue(prev, li - 1);
+            if (tid == 128) GT_STAMP(p, 10, li - 1);
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (tid == 0) {
+        // ---- MMA issue: accumulators of item li in buffer li & 1
+        uint32_t g = 0, li = 0;
+        RingPos sp, bp;  // stage ring, activation ring
+        const uint32_t ring0 = smem_addr(sring), act0 = smem_addr(bring);
+        bool ok = true;
+#ifdef MOEQ4K_TIMELINE
+        long long cyc[6] = {0, 0, 0, 0, 0, 0};  // afull wait, bfull wait, MMA issue, commits, loop, stages
+        long long c0 = clock64(), c1;
+#define MMA_CYC(i) (c1 = clock64(), cyc[i] += c1 - c0, c0 = c1)
+#else
+#define MMA_CYC(i) ((void)0)
+#endif
+        for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++li) {
+            const Item cur = item_of(p, it, nch);
+            const uint32_t buf = li % nbuf, use = li / nbuf;
+            if (use >= 1 && !wait_bar(accempty + buf, (use - 1) & 1u, deadline, p.hdr, 19)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            // D[128 tokens][256 weight rows] (+)= A[128 tokens][16 K] x B[256 rows][16 K]^T:
+            // the activation tile is the M operand, the stage's two 128-row weight
+            // tiles (contiguous 8-row swizzle groups) are one N = 256 operand
+            const uint32_t idesc = tc::idesc_f16_f32(kBM, 2 * kBM);
+            const uint32_t d = taddr + buf * 256u;  // half h at d + 256 h (p.mh == 2: buf = 0)
+            const bool two_halves = p.mh == 2;
+            for (int s = 0; s < S; ++s, ++g, sp.next(NS), bp.next(NB)) {
+                const uint32_t ss = sp.slot, bs = bp.slot;
+                MMA_CYC(4);
+                if (!wait_bar(sfull + ss, sp.phase, deadline, p.hdr, 13)) {
+                    ok = false;
+                    break;
+                }
+                MMA_CYC(0);
+                if (!wait_bar(bfull + bs, bp.phase, deadline, p.hdr, 18)) {
+                    ok = false;
+                    break;
+                }
+                MMA_CYC(1);
+                tc::fence_after_sync();
+                // descriptors of the stage's first 16-wide K slice; each next slice
+                // starts 32 bytes on (2 in the descriptor's address field)
+                const uint32_t wts = ring0 + ss * uint32_t(kStageSlot);
+                const uint64_t dw = tc::smem_desc_sw128(wts);
+                const uint64_t da = tc::smem_desc_sw128(act0 + bs * uint32_t(p.b_slot));
+                if (two_halves) {
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        // rows 128.. of the activation tile start 16 KB on (1024 in the
+                        // descriptor's address field) and accumulate 256 columns on
+                        tc::mma_f16(d, da + uint64_t(2 * kk), dw + uint64_t(2 * kk), idesc, s > 0 || kk > 0);
+                        tc::mma_f16(d + 256u, da + uint64_t(2 * kk + 1024), dw + uint64_t(2 * kk), idesc,
+                                    s > 0 || kk > 0);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        tc::mma_f16(d, da + uint64_t(2 * kk), dw + uint64_t(2 * kk), idesc, s > 0 || kk > 0);
+                }
+                MMA_CYC(2);
+                tc::commit_arrive(sempty + ss);
+                tc::commit_arrive(bempty + bs);
+                MMA_CYC(3);
+#ifdef MOEQ4K_TIMELINE
+                ++cyc[5];
+#endif
+            }
+            if (ok) tc::commit_arrive(accfull + buf);
+        }
+        if (!ok) *abort_flag = 1;
+#ifdef MOEQ4K_TIMELINE
+        if (blockIdx.x == 0 && p.timeline != nullptr)
+            for (int i = 0; i < 6; ++i) p.timeline[11 * 256 + 128 + i] = (unsigned long long)cyc[i];
+#endif
+#undef MMA_CYC
+        // every issued MMA must be complete before the tensor memory is released
+        tc::commit_arrive(drain);
+        wait_bar(drain, 0, global_timer_ns() + p.wait_ns, p.hdr, 15);
+    } else if (tid == 64) {
+        // ---- activation tile of each stage by TMA: the chunk's sorted rows
+        // (rounded up to 32) x 64 K, in boxes of 32 rows
+        uint32_t g = 0;
+        RingPos bp;
+        bool ok = true;
+        for (int it = blockIdx.x; ok && it < total; it += gridDim.x) {
+            const Item cur = item_of(p, it, nch);
+            // the boxes of 32 rows holding the chunk's rows; the M operand's
+            // other rows keep what the slot held before (zeros, or earlier
+            // activations: finite values) and give accumulator rows the
+            // epilogue never reads
+            const int nbox = (cur.nmma + kBoxRows - 1) / kBoxRows;
+            for (int s = 0; s < S; ++s, ++g, bp.next(NB)) {
+                const uint32_t bs = bp.slot;
+                if (*abort_flag ||
+                    (g >= uint32_t(NB) && !wait_bar(bempty + bs, bp.phase ^ 1u, deadline, p.hdr, 12))) {
+                    ok = false;
+                    break;
+                }
+                GT_STAMP(p, 7, g);
                 mbar_arrive_expect_tx(bfull + bs, nbox * kBoxB);
                 ++issued;
                 for (int i = 0; i < nbox; ++i)
                     tma_load_2d(bring + size_t(bs) * p.b_slot + i * kBoxB, &p.mapB, s * kBK,
-                                row0 + i * kBoxRows, bfull + bs);
+                                cur.row0 + i * kBoxRows, bfull + bs);
             }
-        } else if (tid == 32) {
-            // ---- raw bytes of each stage by TMA: block head + the stage's 32 code bytes
-            const int y = ch.e * p.rows_per_expert + rt * p.item_rows;
-            for (int s = 0; s < S; ++s) {
-                const uint32_t g = gs + s, rs = g % NR;
-                if (g >= uint32_t(NR) &&
-                    !wait_bar(rempty + rs, ((g / NR) - 1) & 1, deadline, p.hdr, 17)) {
-                    info[1] = 1;
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (tid == 32) {
+        // ---- raw bytes by TMA, one whole block (144 B) of each of the
+        // tile's rows per raw stage: one contiguous segment per row
+        uint32_t gr = 0;
+        RingPos rp;
+        bool ok = true;
+        for (int it = blockIdx.x; ok && it < total; it += gridDim.x) {
+            const Item cur = item_of(p, it, nch);
+            const int y = cur.ch.e * p.rows_per_expert + cur.rt * p.item_rows;
+            for (int sr = 0; sr < SR; ++sr, ++gr, rp.next(NR)) {
+                const uint32_t rs = rp.slot;
+                if (*abort_flag ||
+                    (gr >= uint32_t(NR) && !wait_bar(rempty + rs, rp.phase ^ 1u, deadline, p.hdr, 17))) {
+                    ok = false;
                     break;
                 }
                 uint8_t *dst = rring + size_t(rs) * nmat * kRawMat;
-                const int xh = (s >> 2) * kBlockBytes, xq = xh + 16 + 32 * (s & 3);
+                GT_STAMP(p, 0, gr * kSub);
                 mbar_arrive_expect_tx(rfull + rs, nmat * kRawMat);
                 ++issued;
-                tma_load_2d(dst, &p.head0, xh, y, rfull + rs);
-                tma_load_2d(dst + kRawHead, &p.codes0, xq, y, rfull + rs);
-                tma_load_2d(dst + kRawMat, &p.head1, xh, y + p.y_off1, rfull + rs);
-                tma_load_2d(dst + kRawMat + kRawHead, &p.codes1, xq, y + p.y_off1, rfull + rs);
+                tma_load_2d(dst, &p.raw0, sr * kBlockBytes, y, rfull + rs);
+                tma_load_2d(dst + kRawMat, &p.raw1, sr * kBlockBytes, y + p.y_off1, rfull + rs);
             }
         }
-
-        // ---- epilogue, by all 12 warps: warp w reads the TMEM lanes of
-        // quadrant w % 4 (32 of the tile's weight rows) for column part w / 4
-        // of three (in 8-column units)
-        __syncthreads();  // every role is past its main loop
-        if (tid == 0) info[2] = wait_bar(done, items & 1, deadline, p.hdr, 14) ? 1 : 0;
-        __syncthreads();
-        tc::fence_after_sync();
-        if (info[2] != 0 && !info[1]) {
-            const int q = warp & 3, part = warp >> 2;
-            const int units = nmma >> 3;
-            const int u_lo = units * part / 3, u_hi = units * (part + 1) / 3;
-            const int row = rt * p.item_rows + q * 32 + lane;
-            const int prow = kperm(row);  // h is the down GEMM's K: stored in kperm order
-            const int pos0 = p.offs[ch.e] + ch.tok_off;  // sorted row of column 0
-            const uint32_t lanebase = taddr + (uint32_t(q * 32) << 16);
-            for (int uu = u_lo; uu < u_hi; ++uu) {
-                const int n0 = 8 * uu;
-                float g[8], u[8];
-                tc::tmem_ld8(lanebase + n0, g);
-                tc::tmem_ld8(lanebase + 256 + n0, u);
-                if (p.mode == 0) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int n = n0 + j;
-                        if (n < ntok) {
-                            // SiLU(g) * u with the fast exponential and divide: the
-                            // result is rounded to fp16
-                            const float e = __expf(fminf(-g[j], 80.0f));
-                            p.h16[size_t(pos0 + n) * p.I + prow] =
-                                __float2half_rn(__fdividef(g[j], 1.0f + e) * u[j]);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int n = n0 + j;
-                        if (n < ntok) {
-                            float *orow = p.o + size_t(toks[n]) * p.H;
-                            orow[row] = g[j];
-                            orow[row + kBM] = u[j];
-                        }
-                    }
-                }
-            }
-        }
-        tc::fence_before_sync();
-        gs += S;
-        ++items;
-        __syncthreads();
+        if (!ok) *abort_flag = 1;
     }
-    // every issued MMA must be complete before the tensor memory is released
-    if (tid == 0) {
-        tc::commit_arrive(drain);
-        wait_bar(drain, 0, global_timer_ns() + p.wait_ns, p.hdr, 15);
-    }
+    __syncthreads();
     // After a timed-out wait the consumers may have left copies unawaited:
     // each copying thread waits (bounded) for the last phase it started on
     // every slot of its ring, so no copy still targets this CTA's shared
     // memory when it exits.  (Without a time-out every phase was consumed.)
-    if (info[1] && (tid == 32 || tid == 64)) {
+    if (*abort_flag && (tid == 32 || tid == 64)) {
         uint64_t *bars = tid == 32 ? rfull : bfull;
         const uint32_t n = tid == 32 ? uint32_t(NR) : uint32_t(NB);
         const uint64_t limit = global_timer_ns() + p.wait_ns;
         for (uint32_t i = 0; i < n && i < issued; ++i) {
-            const uint32_t g = issued - 1 - i;
-            wait_bar(bars + g % n, (g / n) & 1, limit, p.hdr, 19);
+            const uint32_t gg = issued - 1 - i;
+            wait_bar(bars + gg % n, (gg / n) & 1, limit, p.hdr, 19);
         }
     }
     tc::fence_before_sync();
@@ -499,21 +688,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 EncodeTiledFn g_encode = nullptr;
 
 // Raw bytes of one matrix family as a 2-D uint8 tensor: E*rows rows of
-// nsb*144 bytes; box = `box_bytes` (16: block head, 32: codes of one stage)
-// x 128 rows.  Every x coordinate used (block start, +16 + 32c) is a
-// multiple of 16 bytes.
-bool encode_raw_map(CUtensorMap *map, const void *base, int E, int rows, int nsb, int box_bytes) {
+// nsb*144 bytes; box = one block (144 B, a multiple of 16) x 128 rows.
+// Every x coordinate used (a block start, 144*b) is a multiple of 16 bytes.
+bool encode_raw_map(CUtensorMap *map, const void *base, int E, int rows, int nsb) {
     const cuuint64_t dims[2] = {cuuint64_t(nsb) * kBlockBytes, cuuint64_t(E) * rows};
     const cuuint64_t strides[1] = {cuuint64_t(nsb) * kBlockBytes};
-    const cuuint32_t box[2] = {cuuint32_t(box_bytes), cuuint32_t(ptc::kBM)};
+    const cuuint32_t box[2] = {cuuint32_t(kBlockBytes), cuuint32_t(ptc::kBM)};
     const cuuint32_t estr[2] = {1, 1};
     return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-bool encode_raw_maps(CUtensorMap *head, CUtensorMap *codes, const void *base, int E, int rows, int nsb) {
-    return encode_raw_map(head, base, E, rows, nsb, 16) && encode_raw_map(codes, base, E, rows, nsb, 32);
 }
 // Sorted activation rows as a 2-D fp16 tensor [rows][K]; box = 32 rows x 64
 // K, stored with the 128-byte swizzle the MMA descriptors expect (the
@@ -561,7 +746,8 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
                               const int32_t *offs, const int32_t *perm, const int32_t *slotpos,
                               const int32_t *active, const int32_t *nactive, __half *x16,
                               __half *h16, float *obuf, TcChunk *chunks, WsHeader *hdr,
-                              int num_sms, unsigned long long wait_ns, cudaStream_t s) {
+                              int num_sms, unsigned long long wait_ns,
+                              unsigned long long *timeline, cudaStream_t s) {
     using namespace ptc;
     gather_half_kernel<<<num_sms * 8, 256, 0, s>>>(x, slotpos, T, k, H, x16);
     // Chunk capacity: up to 256 slots, no more than the batch's tokens
@@ -572,6 +758,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     const int rows = T * k;
 
     Params p = {};
+    p.mh = cap > kBM ? 2 : 1;
     p.offs = offs;
     p.perm = perm;
     p.chunks = chunks;
@@ -581,25 +768,37 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     p.I = I;
     p.H = H;
     p.wait_ns = wait_ns;
+    p.timeline = timeline;  // gate/up GEMM; the down GEMM stamps the next 12 x 256 words
     const int optin = g_tc_smem_optin[dev];
 
     // Shared memory: header, raw ring, weight-tile ring (1024-aligned), then
     // the activation ring (3 slots of the chunk capacity, 4 for chunks of at
     // most 64 slots); the raw ring takes what is left, up to kMaxSlots stages.
     auto rings = [&](int nmat) -> size_t {
-        // small chunks make each stage's MMAs short, so the weight-tile ring
-        // must cover the MMA completion round trips: 4 slots instead of 2
-        p.na = cap <= 64 ? 4 : 2;
-        p.b_slot = cap * kBK * 2;
-        p.nb = cap <= 64 ? 4 : 3;
+        (void)nmat;
+        // The stage ring (weight tiles) covers the round trip tile ready ->
+        // MMA issued -> complete -> slot free; the raw ring (one block of every
+        // row per slot) covers the HBM latency of the weights; the activation
+        // ring (slots of the chunk capacity's rows, padded so the MMA's
+        // 128-row read of the last slot stays inside the ring) covers the
+        // copies of the activation rows.  Preference: at least 6 activation
+        // slots, then the deepest stage ring (4..2), raw ring (3..2) and
+        // activation ring (8..2).
         p.r_off = kHead;
-        for (int nr = kMaxSlots; nr >= 2; --nr) {
-            p.nr = nr;
-            p.a_off = (kHead + nr * nmat * kRawMat + 1023) & ~1023;
-            p.b_off = p.a_off + p.na * nmat * kTileA;
-            const size_t smem = size_t(p.b_off) + size_t(p.nb) * p.b_slot;
-            if (smem <= size_t(optin)) return smem;
-        }
+        p.b_slot = cap * kBK * 2;
+        const int pad = std::max(0, kActSlot - p.b_slot);
+        for (int nb_min = 6; nb_min >= 2; nb_min -= 4)
+            for (int ns = 4; ns >= 2; --ns)
+                for (int nr = 3; nr >= 2; --nr)
+                    for (int nb = 8; nb >= nb_min; --nb) {
+                        const int s_off = (kHead + nr * 2 * kRawMat + 1023) & ~1023;
+                        const int b_off = s_off + ns * kStageSlot;
+                        const size_t smem = size_t(b_off) + size_t(nb) * p.b_slot + pad;
+                        if (smem <= size_t(optin)) {
+                            p.nr = nr, p.ns = ns, p.nb = nb, p.s_off = s_off, p.b_off = b_off;
+                            return smem;
+                        }
+                    }
         return 0;
     };
 
@@ -611,8 +810,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     p.y_off1 = 0;
     p.rows_per_expert = I;
     if (!encode_act_map(&p.mapB, x16, rows, H)) return cudaErrorInvalidValue;
-    if (!encode_raw_maps(&p.head0, &p.codes0, gate, E, I, H / kQK) ||
-        !encode_raw_maps(&p.head1, &p.codes1, up, E, I, H / kQK))
+    if (!encode_raw_map(&p.raw0, gate, E, I, H / kQK) || !encode_raw_map(&p.raw1, up, E, I, H / kQK))
         return cudaErrorInvalidValue;
     size_t smem = rings(2);
     if (smem == 0) return cudaErrorInvalidValue;
@@ -620,15 +818,15 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
 
     // down: A = down rows (H per expert), B = h16 rows (slot p)
     p.mode = 1;
+    p.timeline = timeline ? timeline + 12 * 256 : nullptr;
     p.K = I;
     p.row_tiles = H / (2 * kBM);
     p.item_rows = 2 * kBM;
     p.y_off1 = kBM;
     p.rows_per_expert = H;
     if (!encode_act_map(&p.mapB, h16, rows, I)) return cudaErrorInvalidValue;
-    if (!encode_raw_maps(&p.head0, &p.codes0, down, E, H, I / kQK)) return cudaErrorInvalidValue;
-    p.head1 = p.head0;
-    p.codes1 = p.codes0;
+    if (!encode_raw_map(&p.raw0, down, E, H, I / kQK)) return cudaErrorInvalidValue;
+    p.raw1 = p.raw0;
     smem = rings(2);
     if (smem == 0) return cudaErrorInvalidValue;
     grouped_gemm_kernel<<<num_sms, kThreads, smem, s>>>(p);
