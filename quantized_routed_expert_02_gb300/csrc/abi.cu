@@ -120,7 +120,8 @@ moe_status ffn_enqueue(const float *x, const int32_t *idx, const float *w, const
             static_cast<const uint8_t *>(down), T, H, E, k, I, ws.i32(L.offs), ws.i32(L.perm),
             ws.i32(L.slotpos), ws.i32(L.active), ws.i32(L.nactive), reinterpret_cast<__half *>(ws.base + L.x16),
             reinterpret_cast<__half *>(ws.base + L.h16), ws.f32(L.o),
-            reinterpret_cast<TcChunk *>(ws.base + L.chunks), ws.hdr(), sms, g_wait_ns,
+            reinterpret_cast<TcChunk *>(ws.base + L.chunks),
+            reinterpret_cast<TcChunk *>(ws.base + L.chunks_dn), ws.hdr(), sms, g_wait_ns,
             gemm_timeline(ws), s)));
         return cuda_status(launch_combine(ws.f32(L.o), idx, w, T, H, E, k, y, ep, sms, s));
     }
@@ -198,8 +199,12 @@ int moe_layer_launch_count(int T, int H, int E, int k, int I) {
     if (decode_stream_supported(dev, T, H, E, k, I)) return 1 /* router */ + 2;
     const int router = (T >= 256 || T <= 2) ? 1 : 2;
     const int permutation = 3;  // count, scan, scatter
-    if (prefill_tc_supported(T, H, E, k, I))
-        return router + permutation + 2 /* fp16 rows, plan */ + 2 /* GEMMs */ + 1;
+    if (prefill_tc_supported(T, H, E, k, I)) {
+        // fp16 rows, the chunk plan (a second one for the down GEMM's
+        // 128-slot chunks when the batch exceeds 128 tokens), GEMMs, combine
+        const int plans = T > 128 ? 2 : 1;
+        return router + permutation + 1 + plans + 2 + 1;
+    }
     return router + permutation + 3 /* gate/up, down, combine */;
 }
 

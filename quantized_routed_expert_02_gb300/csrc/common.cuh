@@ -31,9 +31,9 @@ struct WsHeader {
     // are stored, so the count reaches tag * nblk when the call's h is
     // complete.
     unsigned long long rows_done;
-    uint32_t tc_work[2];             // prefill GEMMs: next work item (gate/up, down)
-    int32_t tc_chunks;               // prefill GEMMs: expert chunks of <= 256 slots
-    uint32_t pad0;
+    uint32_t pad1[2];
+    int32_t tc_chunks;               // grouped GEMMs: expert chunks of the gate/up GEMM
+    int32_t tc_chunks_dn;            //   and of the down GEMM (capacity <= 128 slots)
     // One- and two-token router: every CTA (one per expert) adds 1 once its
     // logits are stored; the CTA whose add returns E - 1 ranks them and sets
     // the count back to 0 for the next call (a count >= E at an add means an
@@ -59,7 +59,7 @@ constexpr size_t kSyncWords = kMaxE;
 constexpr int kPermSlots = 256;
 
 struct WsLayout {
-    size_t sync, blockcnt, slotpos, counts, offs, active, nactive, perm, h, o, logits, x16, h16, chunks, xn, xstage,
+    size_t sync, blockcnt, slotpos, counts, offs, active, nactive, perm, h, o, logits, x16, h16, chunks, chunks_dn, xn, xstage,
         ystage, total;
 };
 
@@ -85,6 +85,7 @@ inline WsLayout ws_layout(int T, int H, int E, int k, int I, bool host_staging) 
     L.x16 = off;     off = align256(off + 2 * pairs * H);                // fp16 activations, sorted rows
     L.h16 = off;     off = align256(off + 2 * pairs * I);                // fp16 SwiGLU output
     L.chunks = off;  off = align256(off + sizeof(TcChunk) * (pairs / 32 + E + 1));  // chunks of >= 32 slots
+    L.chunks_dn = off; off = align256(off + sizeof(TcChunk) * (pairs / 32 + E + 1));
     L.xn = off;      off = align256(off + sizeof(float) * size_t(T) * H);  // normed FFN input
     L.xstage = off;
     L.ystage = off;

@@ -46,7 +46,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
                               const int32_t *offs, const int32_t *perm, const int32_t *slotpos,
                               const int32_t *active,
                               const int32_t *nactive, __half *x16, __half *h16, float *obuf,
-                              TcChunk *chunks, WsHeader *hdr, int num_sms,
+                              TcChunk *chunks, TcChunk *chunks_dn, WsHeader *hdr, int num_sms,
                               unsigned long long wait_ns, unsigned long long *timeline,
                               cudaStream_t s);
 

@@ -80,6 +80,7 @@ struct Params {
 
     const int32_t *offs, *perm;
     const TcChunk *chunks;
+    const int32_t *nchunks;     // number of chunks (written by the plan kernel)
     WsHeader *hdr;              // work counters, chunk count, status
     __half *h16;                // mode 0 output [T*k sorted rows][I]
     float *o;                   // mode 1 output [T*k][H]
@@ -303,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t taddr = *tmem_ptr;
-    const int nch = p.hdr->tc_chunks;
+    const int nch = *p.nchunks;
     const int total = nch * p.row_tiles;
     // Items are taken round-robin (item = blockIdx.x + i * gridDim.x), so every
     // role walks the same sequence with no exchange, and one running stage
@@ -638,12 +639,12 @@ __global__ void gather_half_kernel(const float *__restrict__ x, const int32_t *_
     }
 }
 
-// Chunks of <= cap slots per active expert, in active order, and the work
-// counters reset.  One warp: lanes take active experts in turns of 32, a
-// warp scan gives each expert's first chunk.
+// Chunks of <= cap slots per active expert, in active order; their number
+// goes to *count.  One warp: lanes take active experts in turns of 32, a warp
+// scan gives each expert's first chunk.
 __global__ void plan_kernel(const int32_t *__restrict__ offs, const int32_t *__restrict__ active,
                             const int32_t *__restrict__ nactive, int cap, TcChunk *chunks,
-                            WsHeader *hdr) {
+                            int32_t *count) {
     const int lane = threadIdx.x & 31;
     if (threadIdx.x >= 32) return;
     const int na = *nactive;
@@ -669,11 +670,7 @@ __global__ void plan_kernel(const int32_t *__restrict__ offs, const int32_t *__r
         }
         nc += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) {
-        hdr->tc_chunks = nc;
-        hdr->tc_work[0] = 0;
-        hdr->tc_work[1] = 0;
-    }
+    if (lane == 0) *count = nc;
 }
 
 }  // namespace ptc
@@ -745,23 +742,32 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
                               const uint8_t *down, int T, int H, int E, int k, int I,
                               const int32_t *offs, const int32_t *perm, const int32_t *slotpos,
                               const int32_t *active, const int32_t *nactive, __half *x16,
-                              __half *h16, float *obuf, TcChunk *chunks, WsHeader *hdr,
+                              __half *h16, float *obuf, TcChunk *chunks, TcChunk *chunks_dn,
+                              WsHeader *hdr,
                               int num_sms, unsigned long long wait_ns,
                               unsigned long long *timeline, cudaStream_t s) {
     using namespace ptc;
     gather_half_kernel<<<num_sms * 8, 256, 0, s>>>(x, slotpos, T, k, H, x16);
-    // Chunk capacity: up to 256 slots, no more than the batch's tokens
-    // (rounded to 32) so that small batches get deep rings; a larger expert
-    // list (a caller's routing with repeated experts) is split into more chunks.
-    const int cap = std::min(kBN, (T + kBoxRows - 1) / kBoxRows * kBoxRows);
-    plan_kernel<<<1, 32, 0, s>>>(offs, active, nactive, cap, chunks, hdr);
+    // Chunk capacity: no more than the batch's tokens (rounded to 32), so
+    // small batches get deep rings; up to 256 slots (two M halves, one
+    // accumulator buffer) for gate/up, up to 128 for down, whose large fp32
+    // epilogue then overlaps the next item's MMAs (two accumulator buffers).
+    // A larger expert list (a caller's routing with repeated experts) is
+    // split into more chunks.
+    const int tcap = (T + kBoxRows - 1) / kBoxRows * kBoxRows;
+    const int cap_gu = std::min(kBN, tcap), cap_dn = std::min(kBM, tcap);
+    plan_kernel<<<1, 32, 0, s>>>(offs, active, nactive, cap_gu, chunks, &hdr->tc_chunks);
+    if (cap_dn != cap_gu)
+        plan_kernel<<<1, 32, 0, s>>>(offs, active, nactive, cap_dn, chunks_dn, &hdr->tc_chunks_dn);
     const int rows = T * k;
 
     Params p = {};
+    int cap = cap_gu;
     p.mh = cap > kBM ? 2 : 1;
     p.offs = offs;
     p.perm = perm;
     p.chunks = chunks;
+    p.nchunks = &hdr->tc_chunks;
     p.hdr = hdr;
     p.h16 = h16;
     p.o = obuf;
@@ -818,6 +824,12 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
 
     // down: A = down rows (H per expert), B = h16 rows (slot p)
     p.mode = 1;
+    cap = cap_dn;
+    p.mh = cap > kBM ? 2 : 1;
+    if (cap_dn != cap_gu) {
+        p.chunks = chunks_dn;
+        p.nchunks = &hdr->tc_chunks_dn;
+    }
     p.timeline = timeline ? timeline + 12 * 256 : nullptr;
     p.K = I;
     p.row_tiles = H / (2 * kBM);
