@@ -95,6 +95,17 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// 1-D bulk copy (TMA engine) of `bytes` from global `src` to this CTA's
+// shared `dst`, completing as transaction bytes on mbarrier `bar`.  Both
+// addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // 16-byte asynchronous global->shared copy (L1 bypass).  No L2 cache-policy
 // operand: kernels whose copies carried one (createpolicy + .L2::cache_hint)
 // raised illegal-instruction faults on GB300.

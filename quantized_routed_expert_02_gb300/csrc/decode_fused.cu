@@ -59,9 +59,9 @@ namespace fused {
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxNbw = 8;         // ring slots per warp
-constexpr int kHeadBytes = 5120;   // small shared arrays (see the kernel's first lines)
+constexpr int kHeadBytes = 6144;   // small shared arrays and barriers (see the kernel's first lines)
 constexpr int kStageBatch = 8;     // 128-value chunks of h in flight per warp while staging
-constexpr long long kBackoffCycles = 600;  // wait after a poll that found a stale word
+constexpr long long kPollPauseCycles = 128;  // pause after a poll round that found a stale word
 
 // Optional phase timeline for profiling builds (-DMOEQ4K_TIMELINE): thread 0
 // of each CTA stamps the global timer at phase boundaries into the
@@ -148,21 +148,6 @@ __device__ __forceinline__ void pause_cycles(long long cycles) {
     }
 }
 
-// Poll one tagged word until it carries `tag`; false when `deadline` passes.
-// A miss waits kBackoffCycles before the next load: every CTA polls the same
-// few lines, and back-to-back reloads were measured to delay the stores they
-// wait for by microseconds.
-__device__ __forceinline__ bool await_word(const unsigned long long *p, uint32_t tag,
-                                           uint64_t deadline, unsigned long long &w) {
-    w = ld_relaxed_u64(p);
-    while (tag_of(w) != tag) {
-        if (global_timer_ns() > deadline) return false;
-        pause_cycles(kBackoffCycles);
-        w = ld_relaxed_u64(p);
-    }
-    return true;
-}
-
 // One thread polls a counter until it reaches `target`; false when `deadline`
 // passes.
 __device__ __forceinline__ bool await_count(const unsigned long long *c, unsigned long long target,
@@ -186,6 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
                                                        // then kWarps partial sums of squares
     uint32_t *skey = reinterpret_cast<uint32_t *>(smem + 1536);  // kMaxE logit keys
     int *pcnt = reinterpret_cast<int *>(smem + 2560);            // kThreads partial ranks
+    // one mbarrier per gate/up row pair of each warp (bytes of its two bulk
+    // copies), one for the CTA's down rows
+    uint64_t *rbar = reinterpret_cast<uint64_t *>(smem + 4608);  // [kWarps][kMaxNbw]
+    uint64_t *dbar = rbar + kWarps * kMaxNbw;
     float *vec = reinterpret_cast<float *>(smem + kHeadBytes);
     const int H = p.H, E = p.E, k = p.k, I = p.I;
     const int vec_pad = max(padded_len(H), k * padded_len(I));
@@ -211,6 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         calls0 = atomicAdd(&p.hdr->cta_calls, 1ull);
         flags[1] = 0;
         flags[2] = 0;
+        for (int i = 0; i < kWarps * kMaxNbw + 1; ++i) mbar_init(rbar + i, 1);
+        fence_mbar_init();
     }
     if (threadIdx.x < 32) sel_e[threadIdx.x] = -1;
     // ---------------- 1. router logits (a share per CTA).
@@ -306,28 +297,53 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     }
     if (threadIdx.x == 0) TL_STAMP(p, 2);
 
-    // ---------------- 2. the first Ep threads (E rounded up to a warp) poll
-    // the E logits into shared memory, as floats and as order-preserving
-    // keys, while the other warps prepare x for the gate/up rows (run sums,
-    // and for digit kernels the digits).
+    // ---------------- 2. warp 0 polls the E logits into shared memory, as
+    // floats and as order-preserving keys, while the other warps prepare x
+    // for the gate/up rows (run sums, and for digit kernels the digits).
+    // Lane l holds words l, l+32, ...; every round reloads all of the lane's
+    // still-stale words together, so a round costs one L2 round trip.
     const int Ep = p.router_on ? ((E + 31) & ~31) : 0;
     float *lsm = red + kWarps;  // E logits, clear of the partial sums thread 0 may still read
-    if (int(threadIdx.x) < Ep) {
-        uint32_t key = 0;  // below every logit's key
-        if (int(threadIdx.x) < E) {
-            unsigned long long wv;
-            if (!await_word(p.sync + threadIdx.x, tag, deadline, wv)) flags[1] = 1;
-            float v = value_of(wv);
-            v = (v == v) ? v + 0.0f : -INFINITY;  // a NaN never ranks first; -0 ties +0
-            lsm[threadIdx.x] = v;
-            key = ordered_key(v);
+    if (p.router_on && warp == 0) {
+        constexpr int kPer = kMaxE / 32;
+        bool got[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) got[i] = lane + 32 * i >= E;
+        bool timed_out = false;
+        while (true) {
+            unsigned long long wv[kPer];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i)
+                if (!got[i]) wv[i] = ld_relaxed_u64(p.sync + lane + 32 * i);
+            bool all = true;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                if (got[i]) continue;
+                if (tag_of(wv[i]) != tag) {
+                    all = false;
+                    continue;
+                }
+                got[i] = true;
+                const int e = lane + 32 * i;
+                float v = value_of(wv[i]);
+                v = (v == v) ? v + 0.0f : -INFINITY;  // a NaN never ranks first; -0 ties +0
+                lsm[e] = v;
+                skey[e] = ordered_key(v);
+            }
+            if (__all_sync(0xffffffffu, all)) break;
+            if (global_timer_ns() > deadline) {
+                timed_out = true;
+                break;
+            }
+            pause_cycles(kPollPauseCycles);
         }
-        skey[threadIdx.x] = key;
+        for (int e = E + lane; e < Ep; e += 32) skey[e] = 0;  // below every logit's key
+        if (timed_out && lane == 0) flags[1] = 1;
     } else {
         // x in 128-element chunks, lane l holding elements 4l..4l+3 of a chunk
         // (8 lanes per 32-element run): run sums, and for digit kernels the
         // digits (one packed word per plane and lane) and run scales
-        const int w0 = Ep >> 5, nw = kWarps - w0;
+        const int w0 = p.router_on ? 1 : 0, nw = kWarps - w0;
         for (int c = warp - w0; c < (H >> 7); c += nw) {
             const int e0 = 128 * c + 4 * lane;
             const float4 v = *reinterpret_cast<const float4 *>(vec + padded(e0));
@@ -429,46 +445,52 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     const int R = r1 - r0;
     const int n_gu = u1 - u0;
     const int n_mine = n_gu > warp ? (n_gu - warp + kWarps - 1) / kWarps : 0;  // rows warp+16i
-    const int n16_gu = row_gu >> 4, n16_dn = row_dn >> 4;
 
-    // issue the copies of this warp's i-th gate/up row pair into ring slot i
+    // Lane 0 of each warp issues its i-th gate/up row pair as two bulk copies
+    // (the gate row, then the up row: one contiguous segment each) into ring
+    // slot i, counted on the row's mbarrier; a row of an invalid expert is
+    // marked complete with no bytes.
     auto issue_gu = [&](int i) {
         const int u = u0 + warp + kWarps * i, j = u / I, r = u % I;
         const int e = sel_e[j];
         uint8_t *dst = ring + i * p.slot_bytes;
+        uint64_t *bar = rbar + warp * kMaxNbw + i;
         if (e >= 0 && e < E) {
-            const uint8_t *g = p.gate + e * mat_gu + size_t(r) * row_gu;
-            const uint8_t *uu = p.up + e * mat_gu + size_t(r) * row_gu;
-            for (int c = lane; c < 2 * n16_gu; c += 32) {
-                const uint8_t *src = c < n16_gu ? g + 16 * c : uu + 16 * (c - n16_gu);
-                cp_async_16(dst + 16 * c, src);
-            }
+            mbar_arrive_expect_tx(bar, uint32_t(2 * row_gu));
+            bulk_g2s(dst, p.gate + e * mat_gu + size_t(r) * row_gu, uint32_t(row_gu), bar);
+            bulk_g2s(dst + row_gu, p.up + e * mat_gu + size_t(r) * row_gu, uint32_t(row_gu), bar);
+        } else {
+            mbar_arrive(bar);
         }
-        cp_async_commit();
     };
-    // this thread's share of the CTA's R output rows of all k experts (k
-    // contiguous ranges), one commit group
+    // the CTA's R output rows of each of the k experts: one contiguous range
+    // per slot, one bulk copy each, all counted on the down mbarrier
     uint8_t *dbuf = smem + p.down_off;
+    const uint32_t dbytes = uint32_t(R) * uint32_t(row_dn);
     auto issue_down = [&]() {
-        const int per_j = R * n16_dn;
-        for (int c = threadIdx.x; c < k * per_j; c += kThreads) {
-            const int j = c / per_j, w16 = c % per_j;
+        uint32_t total = 0;
+        for (int j = 0; j < k; ++j)
+            if (sel_e[j] >= 0 && sel_e[j] < E) total += dbytes;
+        mbar_arrive_expect_tx(dbar, total);
+        if (dbytes == 0) return;
+        for (int j = 0; j < k; ++j) {
             const int e = sel_e[j];
             if (e >= 0 && e < E)
-                cp_async_16(dbuf + 16 * c, p.down + e * mat_dn + size_t(r0) * row_dn + 16 * w16);
+                bulk_g2s(dbuf + size_t(j) * dbytes, p.down + e * mat_dn + size_t(r0) * row_dn, dbytes,
+                         dbar);
         }
-        cp_async_commit();
     };
 
     // Every row of the warp has its own slot (the host only launches shapes
     // where n_mine <= nbw): all gate/up rows are requested at once, then the
-    // down rows.  Commit groups: row 0, ..., row n_mine-1, the down rows.
-    // No cp.async targets shared memory that ordinary loads or stores used
-    // earlier in the kernel: kernels that did (slots reused for later rows,
-    // scratch arrays in the slots) raised illegal-instruction faults on
-    // GB300.
-    for (int i = 0; i < n_mine; ++i) issue_gu(i);
-    issue_down();
+    // down rows; a bulk copy's bytes arrive in one piece, and each row has
+    // its own barrier, so rows are consumed as they land.  No copy targets
+    // shared memory that ordinary loads or stores used earlier in the
+    // kernel: kernels that did (slots reused for later rows, scratch arrays
+    // in the slots) raised illegal-instruction faults on GB300.
+    if (lane == 0)
+        for (int i = 0; i < n_mine; ++i) issue_gu(i);
+    if (threadIdx.x == 0) issue_down();
 
     // the renormalised router weights of the k slots (softmax over the top k),
     // needed only by the down rows
@@ -490,7 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     if (kDigits) load_digits(X, planes, H, H >> 6, lane, xscale, vsum);
 
     for (int i = 0; i < n_mine; ++i) {
-        cp_async_wait_pending(n_mine - i);  // the later rows and the down rows may pend
+        if (!mbar_wait(rbar + warp * kMaxNbw + i, 0, deadline) && lane == 0) {
+            flags[1] = 1;
+            record_status(p.hdr, MOE_ERR_TIMEOUT, 5);
+        }
         __syncwarp();
         if (threadIdx.x == 0 && i == 0) TL_STAMP(p, 9);
         const int u = u0 + warp + kWarps * i, j = u / I, r = u % I;
@@ -584,8 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         if (threadIdx.x == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 4);
     } else {
 
-        cp_async_wait_all();  // this thread's share of the down rows
-        __syncthreads();      // everyone's share
+        if (threadIdx.x == 0 && !mbar_wait(dbar, 0, deadline)) flags[1] = 1;
+        __syncthreads();  // the down rows have landed
         if (threadIdx.x == 0) TL_STAMP(p, 10);
         const size_t jstride = size_t(R) * row_dn;
         if (kDigits) {
@@ -647,8 +672,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             }
         }
     }
-    // every copy this thread issued must land before the CTA's shared memory goes away
-    cp_async_wait_all();
+    // every copy must land before the CTA's shared memory goes away (on a
+    // timed-out path some barriers were not waited for): a second bounded wait
+    {
+        const uint64_t limit = global_timer_ns() + p.wait_ns;
+        if (lane == 0)
+            for (int i = 0; i < n_mine; ++i) mbar_wait(rbar + warp * kMaxNbw + i, 0, limit);
+        if (threadIdx.x == 0) mbar_wait(dbar, 0, limit);
+    }
     if (threadIdx.x == 0) TL_STAMP(p, 7);
 }
 
