@@ -10,31 +10,32 @@
 //
 // Design (one CTA of 16 warps per SM, cooperative launch so every CTA is
 // resident):
-//  1. Every CTA stages x in shared memory and computes a share of the E
-//     router logits.
+//  1. Every CTA stages x in shared memory (applying the pre-FFN RMSNorm when
+//     a norm weight is given) and computes a share of the E router logits.
 //     Each logit is published as one 64-bit word that also carries the
 //     call's tag, so readers need no barrier: they poll the words until
 //     every tag is the current one.
-//  2. Every CTA reads the E logits and runs the same top-k and
+//  2. Warp 0 of every CTA polls the E logits while the other warps prepare
+//     x for the dots; every CTA then runs the same top-k and
 //     renormalisation, so all CTAs know the k experts without a broadcast.
 //  3. The k*I gate/up row pairs are split evenly over the CTAs and, inside a
-//     CTA, over its warps.  Each warp requests all of its rows at once into
-//     private shared-memory slots with 16-byte cp.async copies (every lane
-//     issues, so hundreds of requests per SM are in flight; one commit group
-//     per row, waited with cp.async.wait_group), then all threads request
-//     the CTA's down rows (its share of the H output rows, for all k
-//     experts).  Each value of h = SiLU(g) * u is published as a tagged word
-//     like the logits.  (Requesting only a few rows ahead of the compute was
-//     measured slower: the stream then falls short of the HBM bandwidth.)
-//  4. Each CTA polls the k*I tagged h words into shared memory, then for
-//     each of its output rows computes o_j = Wd[e_j][row] . h_j for
-//     j = 0..k-1 and y = sum_j w_j o_j in slot order: deterministic, no
-//     atomics.
+//     CTA, over its warps.  Lane 0 of each warp requests all of the warp's
+//     row pairs at once into private shared-memory slots, one 1-D bulk copy
+//     per row and one mbarrier per pair; thread 0 requests the CTA's down
+//     rows (its share of the H output rows, for all k experts, one bulk
+//     copy per slot).  h = SiLU(g) * u is stored to the workspace.
+//     (Requesting only a few rows ahead of the compute was measured slower:
+//     the stream then falls short of the HBM bandwidth.)
+//  4. Each CTA adds itself to a "rows done" counter (release); thread 0
+//     waits for the call's full count (acquire), the CTA stages the k*I
+//     values of h, and for each of its output rows computes
+//     o_j = Wd[e_j][row] . h_j for j = 0..k-1 and y = sum_j w_j o_j in a
+//     fixed order: deterministic, no atomics.
 // The tag of a call comes from a counter in the workspace header to which
 // every CTA adds 1 at its start, so it needs no reset between calls or graph
 // replays.  Every wait is bounded by a global-timer deadline; on expiry the
-// kernel records MOE_ERR_TIMEOUT, stops computing and lets its copies land
-// before returning.  (Copy completion needs no bound: loads always finish.)
+// kernel records MOE_ERR_TIMEOUT, stops computing and waits (bounded) for
+// its copies to land before returning.
 //
 // Arithmetic of the gate/up rows when H = 2048 (8 Q4_K blocks per row): lane
 // L always covers the same 64 elements of x (sub-block pair L % 4 of block
