@@ -18,24 +18,27 @@
 // (item = CTA + i * grid), row tile fastest, so every role walks the same
 // sequence without an exchange and one running stage count per ring carries
 // the pipeline across item boundaries.  cap = the batch's token count
-// rounded up to 32, at most 256.  20 warps:
-//   thread 32   raw Q4_K bytes by TMA: one whole block (144 contiguous bytes)
+// rounded up to 32, at most 256 for gate/up and 128 for down.  20 warps; the
+// three issuing roles run on whole warps (every lane computes the same
+// operands, one elected lane issues):
+//   warp 1      raw Q4_K bytes by TMA: one whole block (144 contiguous bytes)
 //               of each of the tile's rows per raw stage, 2 x 128 rows;
 //   warps 4-19  dequantise each raw stage into four 64-K stages of fp16
 //               K-major tiles with the 128-byte swizzle (generic stores, then
 //               a proxy fence), thread = (row, half of the stage's codes);
 //               after the first stages of the next item they run the
 //               previous item's epilogue;
-//   thread 64   the chunk's activation rows of each stage by TMA (boxes of 32
+//   warp 2      the chunk's activation rows of each stage by TMA (boxes of 32
 //               rows, 128-byte swizzle) into a ring of chunk-sized slots;
-//   thread 0    issues tcgen05.mma with the tokens as the M operand:
+//   warp 0      issues tcgen05.mma with the tokens as the M operand:
 //               D[tokens][256 weight rows] (+)= A[128 tokens][16 K] x
-//               B[256 rows][16 K]^T, the activation tile as M = 128 (two
-//               halves for 256-slot chunks) and the stage's gate and up (or
-//               two down) tiles as one N = 256 operand: four (eight) MMAs per
-//               64-K stage whatever the token count; accumulators fp32 in
-//               tensor memory, double-buffered for chunks of <= 128 slots so an
-//               item's epilogue overlaps the next item's MMAs.
+//               B[256 rows][16 K]^T, the activation tile as M = 128 (a second
+//               half for chunks of more than 128 slots) and the stage's gate
+//               and up (or two down) tiles as one N = 256 operand: four
+//               (eight) MMAs per 64-K stage whatever the token count;
+//               accumulators fp32 in tensor memory, double-buffered for
+//               chunks of <= 128 slots so an item's epilogue overlaps the
+//               next item's MMAs.
 // The epilogue reads one token per TMEM lane and writes whole 16-byte runs
 // of that token's row: h = SiLU(g) * u in fp16 (gate/up), or the per-slot
 // fp32 outputs (down).  Every wait is bounded by a global-timer deadline and
@@ -210,6 +213,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64
     return __all_sync(0xffffffffu, wait_bar(bar, parity, deadline, hdr, site));
 }
 
+// One lane of a fully active warp, chosen once by elect.sync.  The issuing
+// roles run on whole warps so the operands of their tcgen05 / TMA
+// instructions are computed by every lane alike (warp-uniform), and only the
+// elected lane issues; a role's MMAs and the commits that track them come
+// from that same lane.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t is = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(is));
+    return is != 0u;
+}
+
 // Position in a ring of n slots: the slot and the parity of its current
 // phase (how many times the ring wrapped, mod 2), advanced without division.
 struct RingPos {
@@ -309,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     // Items are taken round-robin (item = blockIdx.x + i * gridDim.x), so every
     // role walks the same sequence with no exchange, and one running stage
     // count per ring carries the pipeline across item boundaries.
-    uint32_t issued = 0;  // threads 32 and 64: copies issued (for the abort drain)
+    uint32_t issued = 0;  // warps 1 and 2: copy phases started (for the abort drain)
 
     if (warp >= 4) {
         // ---- dequantise weight rows into the A tiles; after the first stages
@@ -461,8 +477,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             if (tid == 128) GT_STAMP(p, 10, li - 1);
         }
         if (!ok) *abort_flag = 1;
-    } else if (tid == 0) {
-        // ---- MMA issue: accumulators of item li in buffer li & 1
+    } else if (warp == 0) {
+        // ---- MMA issue: accumulators of item li in buffer li % nbuf.  The
+        // whole warp walks the loop (waits by all lanes with one verdict);
+        // the elected lane issues the MMAs and their commits.
+        const bool leader = elect_one();
         uint32_t g = 0, li = 0;
         RingPos sp, bp;  // stage ring, activation ring
         const uint32_t ring0 = smem_addr(sring), act0 = smem_addr(bring);
@@ -477,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++li) {
             const Item cur = item_of(p, it, nch);
             const uint32_t buf = li % nbuf, use = li / nbuf;
-            if (use >= 1 && !wait_bar(accempty + buf, (use - 1) & 1u, deadline, p.hdr, 19)) {
+            if (use >= 1 && !warp_wait(accempty + buf, (use - 1) & 1u, deadline, p.hdr, 19)) {
                 ok = false;
                 break;
             }
@@ -487,16 +506,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             // tiles (contiguous 8-row swizzle groups) are one N = 256 operand
             const uint32_t idesc = tc::idesc_f16_f32(kBM, 2 * kBM);
             const uint32_t d = taddr + buf * 256u;  // half h at d + 256 h (p.mh == 2: buf = 0)
-            const bool two_halves = p.mh == 2;
+            // the second 128-token half only for chunks that reach into it
+            const bool two_halves = __all_sync(0xffffffffu, p.mh == 2 && cur.nmma > kBM);
             for (int s = 0; s < S; ++s, ++g, sp.next(NS), bp.next(NB)) {
                 const uint32_t ss = sp.slot, bs = bp.slot;
                 MMA_CYC(4);
-                if (!wait_bar(sfull + ss, sp.phase, deadline, p.hdr, 13)) {
+                if (!warp_wait(sfull + ss, sp.phase, deadline, p.hdr, 13)) {
                     ok = false;
                     break;
                 }
                 MMA_CYC(0);
-                if (!wait_bar(bfull + bs, bp.phase, deadline, p.hdr, 18)) {
+                if (!warp_wait(bfull + bs, bp.phase, deadline, p.hdr, 18)) {
                     ok = false;
                     break;
                 }
@@ -507,42 +527,51 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const uint32_t wts = ring0 + ss * uint32_t(kStageSlot);
                 const uint64_t dw = tc::smem_desc_sw128(wts);
                 const uint64_t da = tc::smem_desc_sw128(act0 + bs * uint32_t(p.b_slot));
-                if (two_halves) {
+                if (leader) {
+                    if (two_halves) {
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        // rows 128.. of the activation tile start 16 KB on (1024 in the
-                        // descriptor's address field) and accumulate 256 columns on
-                        tc::mma_f16(d, da + uint64_t(2 * kk), dw + uint64_t(2 * kk), idesc, s > 0 || kk > 0);
-                        tc::mma_f16(d + 256u, da + uint64_t(2 * kk + 1024), dw + uint64_t(2 * kk), idesc,
-                                    s > 0 || kk > 0);
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            // rows 128.. of the activation tile start 16 KB on (1024 in
+                            // the descriptor's address field) and accumulate 256 columns on
+                            tc::mma_f16(d, da + uint64_t(2 * kk), dw + uint64_t(2 * kk), idesc,
+                                        s > 0 || kk > 0);
+                            tc::mma_f16(d + 256u, da + uint64_t(2 * kk + 1024), dw + uint64_t(2 * kk),
+                                        idesc, s > 0 || kk > 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            tc::mma_f16(d, da + uint64_t(2 * kk), dw + uint64_t(2 * kk), idesc,
+                                        s > 0 || kk > 0);
                     }
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        tc::mma_f16(d, da + uint64_t(2 * kk), dw + uint64_t(2 * kk), idesc, s > 0 || kk > 0);
+                    MMA_CYC(2);
+                    tc::commit_arrive(sempty + ss);
+                    tc::commit_arrive(bempty + bs);
+                    MMA_CYC(3);
                 }
-                MMA_CYC(2);
-                tc::commit_arrive(sempty + ss);
-                tc::commit_arrive(bempty + bs);
-                MMA_CYC(3);
+                __syncwarp();
 #ifdef MOEQ4K_TIMELINE
                 ++cyc[5];
 #endif
             }
-            if (ok) tc::commit_arrive(accfull + buf);
+            if (ok && leader) tc::commit_arrive(accfull + buf);
+            __syncwarp();
         }
         if (!ok) *abort_flag = 1;
 #ifdef MOEQ4K_TIMELINE
-        if (blockIdx.x == 0 && p.timeline != nullptr)
+        if (blockIdx.x == 0 && p.timeline != nullptr && leader)
             for (int i = 0; i < 6; ++i) p.timeline[11 * 256 + 128 + i] = (unsigned long long)cyc[i];
 #endif
 #undef MMA_CYC
         // every issued MMA must be complete before the tensor memory is released
-        tc::commit_arrive(drain);
-        wait_bar(drain, 0, global_timer_ns() + p.wait_ns, p.hdr, 15);
-    } else if (tid == 64) {
+        if (leader) tc::commit_arrive(drain);
+        __syncwarp();
+        warp_wait(drain, 0, global_timer_ns() + p.wait_ns, p.hdr, 15);
+    } else if (warp == 2) {
         // ---- activation tile of each stage by TMA: the chunk's sorted rows
-        // (rounded up to 32) x 64 K, in boxes of 32 rows
+        // (rounded up to 32) x 64 K, in boxes of 32 rows; the whole warp walks
+        // the loop, the elected lane issues
+        const bool leader = elect_one();
         uint32_t g = 0;
         RingPos bp;
         bool ok = true;
@@ -555,23 +584,28 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const int nbox = (cur.nmma + kBoxRows - 1) / kBoxRows;
             for (int s = 0; s < S; ++s, ++g, bp.next(NB)) {
                 const uint32_t bs = bp.slot;
-                if (*abort_flag ||
-                    (g >= uint32_t(NB) && !wait_bar(bempty + bs, bp.phase ^ 1u, deadline, p.hdr, 12))) {
+                if (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                    (g >= uint32_t(NB) && !warp_wait(bempty + bs, bp.phase ^ 1u, deadline, p.hdr, 12))) {
                     ok = false;
                     break;
                 }
-                GT_STAMP(p, 7, g);
-                mbar_arrive_expect_tx(bfull + bs, nbox * kBoxB);
                 ++issued;
-                for (int i = 0; i < nbox; ++i)
-                    tma_load_2d(bring + size_t(bs) * p.b_slot + i * kBoxB, &p.mapB, s * kBK,
-                                cur.row0 + i * kBoxRows, bfull + bs);
+                if (leader) {
+                    GT_STAMP(p, 7, g);
+                    mbar_arrive_expect_tx(bfull + bs, nbox * kBoxB);
+                    for (int i = 0; i < nbox; ++i)
+                        tma_load_2d(bring + size_t(bs) * p.b_slot + i * kBoxB, &p.mapB, s * kBK,
+                                    cur.row0 + i * kBoxRows, bfull + bs);
+                }
+                __syncwarp();
             }
         }
         if (!ok) *abort_flag = 1;
-    } else if (tid == 32) {
+    } else if (warp == 1) {
         // ---- raw bytes by TMA, one whole block (144 B) of each of the
-        // tile's rows per raw stage: one contiguous segment per row
+        // tile's rows per raw stage: one contiguous segment per row; the whole
+        // warp walks the loop, the elected lane issues
+        const bool leader = elect_one();
         uint32_t gr = 0;
         RingPos rp;
         bool ok = true;
@@ -580,17 +614,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const int y = cur.ch.e * p.rows_per_expert + cur.rt * p.item_rows;
             for (int sr = 0; sr < SR; ++sr, ++gr, rp.next(NR)) {
                 const uint32_t rs = rp.slot;
-                if (*abort_flag ||
-                    (gr >= uint32_t(NR) && !wait_bar(rempty + rs, rp.phase ^ 1u, deadline, p.hdr, 17))) {
+                if (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                    (gr >= uint32_t(NR) && !warp_wait(rempty + rs, rp.phase ^ 1u, deadline, p.hdr, 17))) {
                     ok = false;
                     break;
                 }
-                uint8_t *dst = rring + size_t(rs) * nmat * kRawMat;
-                GT_STAMP(p, 0, gr * kSub);
-                mbar_arrive_expect_tx(rfull + rs, nmat * kRawMat);
                 ++issued;
-                tma_load_2d(dst, &p.raw0, sr * kBlockBytes, y, rfull + rs);
-                tma_load_2d(dst + kRawMat, &p.raw1, sr * kBlockBytes, y + p.y_off1, rfull + rs);
+                if (leader) {
+                    uint8_t *dst = rring + size_t(rs) * nmat * kRawMat;
+                    GT_STAMP(p, 0, gr * kSub);
+                    mbar_arrive_expect_tx(rfull + rs, nmat * kRawMat);
+                    tma_load_2d(dst, &p.raw0, sr * kBlockBytes, y, rfull + rs);
+                    tma_load_2d(dst + kRawMat, &p.raw1, sr * kBlockBytes, y + p.y_off1, rfull + rs);
+                }
+                __syncwarp();
             }
         }
         if (!ok) *abort_flag = 1;
@@ -600,9 +637,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     // each copying thread waits (bounded) for the last phase it started on
     // every slot of its ring, so no copy still targets this CTA's shared
     // memory when it exits.  (Without a time-out every phase was consumed.)
-    if (*abort_flag && (tid == 32 || tid == 64)) {
-        uint64_t *bars = tid == 32 ? rfull : bfull;
-        const uint32_t n = tid == 32 ? uint32_t(NR) : uint32_t(NB);
+    if (*abort_flag && (warp == 1 || warp == 2) && lane == 0) {
+        uint64_t *bars = warp == 1 ? rfull : bfull;
+        const uint32_t n = warp == 1 ? uint32_t(NR) : uint32_t(NB);
         const uint64_t limit = global_timer_ns() + p.wait_ns;
         for (uint32_t i = 0; i < n && i < issued; ++i) {
             const uint32_t gg = issued - 1 - i;
