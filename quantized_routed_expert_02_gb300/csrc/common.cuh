@@ -113,6 +113,38 @@ __device__ __forceinline__ float epilogue_value(const OutEpilogue &ep, int t, in
     return ep.residual != nullptr ? ep.residual[size_t(t) * H + r] + v : v;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialisation (launch_pdl below) and begins with
+// pdl_enter(): it waits until the grids it depends on have completed and their
+// writes are visible, then lets the next grid in the stream be launched, so
+// that grid's launch and set-up overlap this one's tail instead of following
+// its end.  Work that reads nothing a predecessor may write (an L2 prefetch
+// of weights) may run between pdl_trigger() and pdl_wait().
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_enter() {
+    pdl_wait();
+    pdl_trigger();
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Record the first device-side error (later ones are dropped).
 __device__ inline void record_status(WsHeader *hdr, moe_status s, int32_t detail) {
     if (atomicCAS(&hdr->status, 0u, uint32_t(s)) == 0u) {

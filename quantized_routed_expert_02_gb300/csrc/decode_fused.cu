@@ -184,6 +184,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     float *xscale = reinterpret_cast<float *>(planes + 3 * H);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Let the next grid in the stream launch now (it waits in its own
+    // pdl_wait() until this one has completed), warm L2 with this CTA's
+    // router row (a prefetch changes nothing a predecessor could be writing),
+    // then wait for the predecessor grid: x may be its output.
+    pdl_trigger();
+    if (threadIdx.x == 0 && p.router_on && int(blockIdx.x) < p.E)
+        bulk_prefetch_l2(p.Wr + size_t(blockIdx.x) * p.H, uint32_t(p.H) * 4u);
+    pdl_wait();
     const uint64_t deadline = global_timer_ns() + p.wait_ns;
     const unsigned nblk = gridDim.x;
     const int nsb_h = H / kQK, nsb_i = I / kQK;
@@ -821,11 +829,13 @@ cudaError_t launch_decode_fused(int dev, const float *x, const float *norm_w, fl
     cfg.blockDim = dim3(fused::kThreads);
     cfg.dynamicSmemBytes = c.smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     void *args[] = {&p};
     return cudaLaunchKernelExC(&cfg, pick_kernel(H, I), args);
 }

@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kGuThreads, kGuBlocksPerSm)
     stream_gateup_kernel(const float *__restrict__ x, const uint8_t *__restrict__ gate,
                          const uint8_t *__restrict__ up, const int32_t *__restrict__ idx, int k,
                          int E, int H, int I, float *__restrict__ h, WsHeader *hdr) {
+    pdl_enter();
     extern __shared__ __align__(16) float sm[];
     float *xs = sm;
     float *s32 = xs + padded_len(H);
@@ -155,6 +156,7 @@ __global__ void __launch_bounds__(kDnThreads, 1)
     stream_down_kernel(const float *__restrict__ h, const uint8_t *__restrict__ down,
                        const int32_t *__restrict__ idx, const float *__restrict__ w, int k, int E,
                        int H, int I, float *__restrict__ y, WsHeader *hdr, const OutEpilogue ep) {
+    pdl_enter();
     extern __shared__ __align__(16) float sm[];
     const int plen = padded_len(I), runs = I / 32;
     float *hs = sm;                       // [k][plen]
@@ -247,6 +249,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     stream_gateup_digits_kernel(const float *__restrict__ x, const uint8_t *__restrict__ gate,
                                 const uint8_t *__restrict__ up, const int32_t *__restrict__ idx,
                                 int k, int E, int H, int I, float *__restrict__ h, WsHeader *hdr) {
+    pdl_enter();
     extern __shared__ __align__(16) uint8_t smd[];
     const int UX = H >> 6, Q = kDgThreads / UX;
     uint8_t *planes = smd;                                      // 3H bytes
@@ -374,6 +377,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
                             const int32_t *__restrict__ idx, const float *__restrict__ w, int k,
                             int E, int H, int I, float *__restrict__ y, WsHeader *hdr,
                             const OutEpilogue ep) {
+    pdl_enter();
     extern __shared__ __align__(16) uint8_t smd[];
     const int n = k * I, UD = n >> 6, upr = I >> 6;
     uint8_t *planes = smd;                                      // 3n bytes
@@ -483,35 +487,35 @@ cudaError_t launch_decode_stream(const float *x, const int32_t *idx, const float
     const size_t sg = gateup_smem(H, k), sd = down_smem(I, k);
     const int gg = num_sms * kGuBlocksPerSm;
     if (gateup_digits_ok(H))
-        stream_gateup_digits_kernel<<<num_sms, kDgThreads, gateup_digits_smem(H, k), s>>>(
-            x, gate, up, idx, k, E, H, I, hbuf, hdr);
+        launch_pdl(stream_gateup_digits_kernel, dim3(num_sms), dim3(kDgThreads),
+                   gateup_digits_smem(H, k), s, x, gate, up, idx, k, E, H, I, hbuf, hdr);
     else if (nbh <= 1)
-        stream_gateup_kernel<1><<<gg, kGuThreads, sg, s>>>(x, gate, up, idx, k, E, H, I, hbuf, hdr);
+        launch_pdl(stream_gateup_kernel<1>, dim3(gg), dim3(kGuThreads), size_t(sg), s, x, gate, up, idx, k, E, H, I, hbuf, hdr);
     else if (nbh <= 2)
-        stream_gateup_kernel<2><<<gg, kGuThreads, sg, s>>>(x, gate, up, idx, k, E, H, I, hbuf, hdr);
+        launch_pdl(stream_gateup_kernel<2>, dim3(gg), dim3(kGuThreads), size_t(sg), s, x, gate, up, idx, k, E, H, I, hbuf, hdr);
     else
-        stream_gateup_kernel<4><<<gg, kGuThreads, sg, s>>>(x, gate, up, idx, k, E, H, I, hbuf, hdr);
+        launch_pdl(stream_gateup_kernel<4>, dim3(gg), dim3(kGuThreads), size_t(sg), s, x, gate, up, idx, k, E, H, I, hbuf, hdr);
     if (down_digits_ok(k, I)) {
         const int ud = k * I / 64;  // units per output row; lanes take ceil(ud / 32) each
         const size_t sdd = down_digits_smem(k, I);
         if (ud <= 32)
-            stream_down_rows_kernel<1><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
+            launch_pdl(stream_down_rows_kernel<1>, dim3(num_sms), dim3(kDgThreads), size_t(sdd), s, hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
         else if (ud <= 64)
-            stream_down_rows_kernel<2><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
+            launch_pdl(stream_down_rows_kernel<2>, dim3(num_sms), dim3(kDgThreads), size_t(sdd), s, hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
         else if (ud <= 128)
-            stream_down_rows_kernel<4><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
+            launch_pdl(stream_down_rows_kernel<4>, dim3(num_sms), dim3(kDgThreads), size_t(sdd), s, hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
         else if (ud <= 192)
-            stream_down_rows_kernel<6><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
+            launch_pdl(stream_down_rows_kernel<6>, dim3(num_sms), dim3(kDgThreads), size_t(sdd), s, hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
         else  // four units per lane in flight, looping over the rest (a wider
               // batch of loads per lane would spill at the 128-register cap)
-            stream_down_rows_kernel<4><<<num_sms, kDgThreads, sdd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
+            launch_pdl(stream_down_rows_kernel<4>, dim3(num_sms), dim3(kDgThreads), size_t(sdd), s, hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
     }
     else if (nbi <= 1)
-        stream_down_kernel<1><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
+        launch_pdl(stream_down_kernel<1>, dim3(num_sms), dim3(kDnThreads), size_t(sd), s, hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
     else if (nbi <= 2)
-        stream_down_kernel<2><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
+        launch_pdl(stream_down_kernel<2>, dim3(num_sms), dim3(kDnThreads), size_t(sd), s, hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
     else
-        stream_down_kernel<4><<<num_sms, kDnThreads, sd, s>>>(hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
+        launch_pdl(stream_down_kernel<4>, dim3(num_sms), dim3(kDnThreads), size_t(sd), s, hbuf, down, idx, w, k, E, H, I, y, hdr, ep);
     return cudaGetLastError();
 }
 

@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(256) gateup_kernel(const float *__restrict__ x
                                                      const int32_t *__restrict__ nactive,
                                                      int H, int I, int k, int E, int npairs,
                                                      float *__restrict__ h, WsHeader *hdr) {
+    pdl_enter();
     extern __shared__ float smem[];
     float *xs = smem;                         // [kTokGroup][H]
     float *xsum = smem + kTokGroup * H;       // [kTokGroup][H/16]
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(256) down_kernel(const float *__restrict__ h,
                                                    const int32_t *__restrict__ nactive,
                                                    int H, int I, int E, int npairs,
                                                    float *__restrict__ o, WsHeader *hdr) {
+    pdl_enter();
     extern __shared__ float smem[];
     float *hs = smem;                         // [kTokGroup][I]
     float *hsum = smem + kTokGroup * I;       // [kTokGroup][I/16]
@@ -194,6 +196,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
                                                       const float *__restrict__ w, int T, int H,
                                                       int E, int k, float *__restrict__ y,
                                                       const OutEpilogue ep) {
+    pdl_enter();
     const int h4 = H >> 2;
     const size_t total = size_t(T) * h4;
     for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total;
@@ -224,7 +227,7 @@ cudaError_t launch_combine(const float *obuf, const int32_t *idx, const float *w
                            cudaStream_t s) {
     const size_t total = size_t(T) * (H / 4);
     const size_t g3s = (total + 255) / 256, g3cap = size_t(num_sms) * 16;
-    combine_kernel<<<int(g3s < g3cap ? g3s : g3cap), 256, 0, s>>>(obuf, idx, w, T, H, E, k, y, ep);
+    launch_pdl(combine_kernel, dim3(int(g3s < g3cap ? g3s : g3cap)), dim3(256), size_t(0), s, obuf, idx, w, T, H, E, k, y, ep);
     return cudaGetLastError();
 }
 
@@ -246,15 +249,15 @@ cudaError_t launch_expert_ffn(const float *x, const int32_t *idx, const float *w
     const size_t smem_dn = sizeof(float) * kTokGroup * (I + I / 16);
     const int cap = num_sms * 8;
     int g1 = min(max_active * (I / kRowsPerItem), cap);
-    gateup_kernel<<<g1, 256, smem_gu, s>>>(x, gate, up, offs, perm, active, nactive, H, I, k, E,
+    launch_pdl(gateup_kernel, dim3(g1), dim3(256), size_t(smem_gu), s, x, gate, up, offs, perm, active, nactive, H, I, k, E,
                                            T * k, hbuf, hdr);
     int g2 = min(max_active * (H / kRowsPerItem), cap);
-    down_kernel<<<g2, 256, smem_dn, s>>>(hbuf, down, offs, perm, active, nactive, H, I, E, T * k,
+    launch_pdl(down_kernel, dim3(g2), dim3(256), size_t(smem_dn), s, hbuf, down, offs, perm, active, nactive, H, I, E, T * k,
                                          obuf, hdr);
     const size_t total = size_t(T) * (H / 4);
     const size_t g3s = (total + 255) / 256, g3cap = size_t(num_sms) * 16;
     int g3 = int(g3s < g3cap ? g3s : g3cap);
-    combine_kernel<<<g3, 256, 0, s>>>(obuf, idx, w, T, H, E, k, y, ep);
+    launch_pdl(combine_kernel, dim3(g3), dim3(256), size_t(0), s, obuf, idx, w, T, H, E, k, y, ep);
     return cudaGetLastError();
 }
 

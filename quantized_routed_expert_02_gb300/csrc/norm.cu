@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float *__re
                                                                const float *__restrict__ gamma,
                                                                float eps, int H,
                                                                float *__restrict__ xn) {
+    pdl_enter();
     __shared__ float part[kNormThreads / 32];
     __shared__ float inv_sh;
     const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float *__re
 
 cudaError_t launch_rmsnorm(const float *x, const float *gamma, float eps, int T, int H, float *xn,
                            cudaStream_t s) {
-    rmsnorm_kernel<<<T, kNormThreads, 0, s>>>(x, gamma, eps, H, xn);
+    launch_pdl(rmsnorm_kernel, dim3(T), dim3(kNormThreads), size_t(0), s, x, gamma, eps, H, xn);
     return cudaGetLastError();
 }
 

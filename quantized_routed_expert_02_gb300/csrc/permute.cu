@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(kPermSlots) permute_count_kernel(const int32_t
                                                                    int n, int E,
                                                                    int32_t *__restrict__ blockcnt,
                                                                    WsHeader *hdr) {
+    pdl_enter();
     __shared__ int32_t cnt[kMaxE];
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
@@ -59,6 +60,7 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int nblocks, int E,
                                                             int32_t *__restrict__ offs,
                                                             int32_t *__restrict__ active,
                                                             int32_t *__restrict__ nactive) {
+    pdl_enter();
     __shared__ int32_t tile[32][kMaxE + 1];
     __shared__ int32_t tot[kMaxE];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -114,6 +116,7 @@ __global__ void __launch_bounds__(kPermSlots) permute_scatter_kernel(
     const int32_t *__restrict__ idx, int n, int E, const int32_t *__restrict__ blockcnt,
     const int32_t *__restrict__ offs, int32_t *__restrict__ perm, int32_t *__restrict__ slotpos,
     WsHeader *hdr) {
+    pdl_enter();
     __shared__ int32_t table[kWarpsPerBlock][kMaxE];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int p = blockIdx.x * kPermSlots + tid;
@@ -153,9 +156,9 @@ cudaError_t launch_permute(const int32_t *idx, int T, int k, int E, int32_t *cou
                            int32_t *slotpos, WsHeader *hdr, cudaStream_t s) {
     const int n = T * k;
     const int nb = (n + kPermSlots - 1) / kPermSlots;
-    permute_count_kernel<<<nb, kPermSlots, 0, s>>>(idx, n, E, blockcnt, hdr);
-    permute_scan_kernel<<<1, 1024, 0, s>>>(nb, E, blockcnt, counts, offs, active, nactive);
-    permute_scatter_kernel<<<nb, kPermSlots, 0, s>>>(idx, n, E, blockcnt, offs, perm, slotpos, hdr);
+    launch_pdl(permute_count_kernel, dim3(nb), dim3(kPermSlots), size_t(0), s, idx, n, E, blockcnt, hdr);
+    launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), size_t(0), s, nb, E, blockcnt, counts, offs, active, nactive);
+    launch_pdl(permute_scatter_kernel, dim3(nb), dim3(kPermSlots), size_t(0), s, idx, n, E, blockcnt, offs, perm, slotpos, hdr);
     return cudaGetLastError();
 }
 

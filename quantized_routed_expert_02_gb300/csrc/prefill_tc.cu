@@ -259,6 +259,7 @@ __device__ __forceinline__ Item item_of(const Params &p, int it, int nch) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ Params p) {
+    pdl_enter();
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *rfull = reinterpret_cast<uint64_t *>(smem);
     uint64_t *rempty = rfull + kMaxSlots;
@@ -657,6 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 // order.  Thread per (token, 4 elements): x is read once, written k times.
 __global__ void gather_half_kernel(const float *__restrict__ x, const int32_t *__restrict__ slotpos,
                                    int T, int k, int H, __half *__restrict__ xs) {
+    pdl_enter();
     const int per_row = H / 4;
     const size_t total = size_t(T) * per_row;
     for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total;
@@ -682,6 +684,7 @@ __global__ void gather_half_kernel(const float *__restrict__ x, const int32_t *_
 __global__ void plan_kernel(const int32_t *__restrict__ offs, const int32_t *__restrict__ active,
                             const int32_t *__restrict__ nactive, int cap, TcChunk *chunks,
                             int32_t *count) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     if (threadIdx.x >= 32) return;
     const int na = *nactive;
@@ -784,7 +787,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
                               int num_sms, unsigned long long wait_ns,
                               unsigned long long *timeline, cudaStream_t s) {
     using namespace ptc;
-    gather_half_kernel<<<num_sms * 8, 256, 0, s>>>(x, slotpos, T, k, H, x16);
+    launch_pdl(gather_half_kernel, dim3(num_sms * 8), dim3(256), size_t(0), s, x, slotpos, T, k, H, x16);
     // Chunk capacity: no more than the batch's tokens (rounded to 32), so
     // small batches get deep rings; up to 256 slots (two M halves, one
     // accumulator buffer) for gate/up, up to 128 for down, whose large fp32
@@ -793,9 +796,9 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     // split into more chunks.
     const int tcap = (T + kBoxRows - 1) / kBoxRows * kBoxRows;
     const int cap_gu = std::min(kBN, tcap), cap_dn = std::min(kBM, tcap);
-    plan_kernel<<<1, 32, 0, s>>>(offs, active, nactive, cap_gu, chunks, &hdr->tc_chunks);
+    launch_pdl(plan_kernel, dim3(1), dim3(32), size_t(0), s, offs, active, nactive, cap_gu, chunks, &hdr->tc_chunks);
     if (cap_dn != cap_gu)
-        plan_kernel<<<1, 32, 0, s>>>(offs, active, nactive, cap_dn, chunks_dn, &hdr->tc_chunks_dn);
+        launch_pdl(plan_kernel, dim3(1), dim3(32), size_t(0), s, offs, active, nactive, cap_dn, chunks_dn, &hdr->tc_chunks_dn);
     const int rows = T * k;
 
     Params p = {};
@@ -857,7 +860,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
         return cudaErrorInvalidValue;
     size_t smem = rings(2);
     if (smem == 0) return cudaErrorInvalidValue;
-    grouped_gemm_kernel<<<num_sms, kThreads, smem, s>>>(p);
+    launch_pdl(grouped_gemm_kernel, dim3(num_sms), dim3(kThreads), size_t(smem), s, p);
 
     // down: A = down rows (H per expert), B = h16 rows (slot p)
     p.mode = 1;
@@ -878,7 +881,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     p.raw1 = p.raw0;
     smem = rings(2);
     if (smem == 0) return cudaErrorInvalidValue;
-    grouped_gemm_kernel<<<num_sms, kThreads, smem, s>>>(p);
+    launch_pdl(grouped_gemm_kernel, dim3(num_sms), dim3(kThreads), size_t(smem), s, p);
     return cudaGetLastError();
 }
 

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const float *__restr
                                                             const float *__restrict__ bias,
                                                             int T, int H, int E,
                                                             float *__restrict__ logits) {
+    pdl_enter();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * 8 + warp;
     const int t0 = blockIdx.y * kTT;
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(256) router_tile_kernel(const float *__restric
                                                           const float *__restrict__ Wr,
                                                           const float *__restrict__ bias, int T,
                                                           int H, int E, float *__restrict__ logits) {
+    pdl_enter();
     extern __shared__ __align__(16) float xt[];  // [kXT][H]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.y * kXT, n4 = H >> 2;
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
                                                           int T, int E, int k,
                                                           int32_t *__restrict__ idx,
                                                           float *__restrict__ w) {
+    pdl_enter();
     const int warp = threadIdx.x >> 5;
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;
@@ -200,6 +203,7 @@ __global__ void __launch_bounds__(256) router_row_kernel(const float *__restrict
                                                          float *__restrict__ logits,
                                                          int32_t *__restrict__ idx,
                                                          float *__restrict__ w, WsHeader *hdr) {
+    pdl_enter();
     __shared__ float part[kTT][8];
     __shared__ float lg[kTT][kMaxE];
     __shared__ int last;
@@ -273,6 +277,7 @@ __global__ void __launch_bounds__(256) router_big_kernel(const float *__restrict
                                                          int H, int E, int k,
                                                          int32_t *__restrict__ idx,
                                                          float *__restrict__ w) {
+    pdl_enter();
     // dynamic shared memory: xs[2][kRK][kRT], ws[2][kRK][kRE] (k-major), lg[kRT][kMaxE + 1]
     extern __shared__ __align__(16) float rsm[];
     float (*xs)[kRK][kRT] = reinterpret_cast<float (*)[kRK][kRT]>(rsm);
@@ -377,6 +382,7 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(256, 1)
     router_split_kernel(const float *__restrict__ x, const float *__restrict__ Wr,
                         const float *__restrict__ bias, int T, int H, int E, int k,
                         int32_t *__restrict__ idx, float *__restrict__ w) {
+    pdl_enter();
     extern __shared__ __align__(16) float rsm[];
     namespace cg = cooperative_groups;
     cg::cluster_group cl = cg::this_cluster();
@@ -492,25 +498,25 @@ cudaError_t launch_router(const float *x, const float *Wr, const float *bias, in
     dim3 blk(256);
     if (T >= 256 && E <= kSE && H % (kSplit * kSK) == 0) {
         dim3 grid((T + kST - 1) / kST, kSplit);
-        router_split_kernel<<<grid, blk, kSplitSmem, s>>>(x, Wr, bias, T, H, E, k, idx, w);
+        launch_pdl(router_split_kernel, dim3(grid), dim3(blk), size_t(kSplitSmem), s, x, Wr, bias, T, H, E, k, idx, w);
         return cudaGetLastError();
     }
     if (T >= 256) {
-        router_big_kernel<<<(T + kRT - 1) / kRT, blk, kRouterBigSmem, s>>>(x, Wr, bias, T, H, E, k, idx, w);
+        launch_pdl(router_big_kernel, dim3((T + kRT - 1) / kRT), dim3(blk), size_t(kRouterBigSmem), s, x, Wr, bias, T, H, E, k, idx, w);
         return cudaGetLastError();
     }
     if (T <= 2) {
-        router_row_kernel<2><<<E, blk, 0, s>>>(x, Wr, bias, T, H, E, k, logits, idx, w, hdr);
+        launch_pdl(router_row_kernel<2>, dim3(E), dim3(blk), size_t(0), s, x, Wr, bias, T, H, E, k, logits, idx, w, hdr);
         return cudaGetLastError();
     }
     if (size_t(kXT) * H * sizeof(float) <= size_t(kRouterTileSmemMax)) {
         dim3 grid((E + 7) / 8, (T + kXT - 1) / kXT);
-        router_tile_kernel<<<grid, blk, size_t(kXT) * H * sizeof(float), s>>>(x, Wr, bias, T, H, E, logits);
+        launch_pdl(router_tile_kernel, dim3(grid), dim3(blk), size_t(size_t(kXT) * H * sizeof(float)), s, x, Wr, bias, T, H, E, logits);
     } else {
         dim3 grid((E + 7) / 8, (T + 7) / 8);
-        router_logits_kernel<8><<<grid, blk, 0, s>>>(x, Wr, bias, T, H, E, logits);
+        launch_pdl(router_logits_kernel<8>, dim3(grid), dim3(blk), size_t(0), s, x, Wr, bias, T, H, E, logits);
     }
-    router_topk_kernel<<<(T + 7) / 8, blk, 0, s>>>(logits, T, E, k, idx, w);
+    launch_pdl(router_topk_kernel, dim3((T + 7) / 8), dim3(blk), size_t(0), s, logits, T, E, k, idx, w);
     return cudaGetLastError();
 }
 
