@@ -248,6 +248,172 @@ long moq_ffn(const float *x, const int32_t *idx, const double *w,
 }
 
 /*
+ * Q8_K activations (qwen3_moe_dispatch.rs, aprender-serve 0.70.2, doc of
+ * cpu_reference: the production CPU path quantises activations to Q8_K for
+ * its integer dot products; the fp32-activation path above is the other
+ * scope).  The pages name the format, not its arithmetic.  Reading: every
+ * block of 256 consecutive activations gets one fp32 scale d and 256 signed
+ * 8-bit codes q with v ~= d q, symmetric around zero, the block's largest
+ * magnitude at +-127:
+ *     amax = max_i |v_i|;   amax = 0 gives d = 0 and all codes 0;
+ *     otherwise s = 127 / amax and d = amax / 127 (fp32 divisions, rounded
+ *     to nearest), q_i = v_i * s (fp32 product) rounded to the nearest
+ *     integer, halves to even.
+ * Every step is fp32, so a kernel taking the same steps decides the same
+ * codes.  `sums` receives each 32-element sub-block's code sum.
+ */
+void moq_q8k_quantize(const float *v, long nblocks, int8_t *q, float *d, int32_t *sums)
+{
+    for (long b = 0; b < nblocks; b++) {
+        const float *vb = v + b * QK;
+        int8_t *qb = q + b * QK;
+        float amax = 0.0f;
+        for (int i = 0; i < QK; i++)
+            if (fabsf(vb[i]) > amax)
+                amax = fabsf(vb[i]);
+        if (amax == 0.0f) {
+            d[b] = 0.0f;
+            for (int i = 0; i < QK; i++)
+                qb[i] = 0;
+        } else {
+            float s = 127.0f / amax;
+            d[b] = amax / 127.0f;
+            for (int i = 0; i < QK; i++) {
+                float t = vb[i] * s;
+                qb[i] = (int8_t)rintf(t);   /* default rounding mode: halves to even */
+            }
+        }
+        for (int j = 0; j < QK / 32; j++) {
+            int32_t acc = 0;
+            for (int i = 0; i < 32; i++)
+                acc += qb[32 * j + i];
+            sums[b * (QK / 32) + j] = acc;
+        }
+    }
+}
+
+/*
+ * Dot product of one Q4_K row (nsb blocks) with a Q8_K vector of the same
+ * length: per block b and sub-block j, with the exact integers
+ * P = sum_i q4_i q8_i and S = sum_i q8_i (the sub-block's code sum),
+ *     sum_b d8_b * sum_j (d4_b sc_j P - dmin_b m_j S)
+ * in fp64, i.e. the dot of the dequantised row with the vector d8 q8.
+ */
+double moq_row_dot_q8k(const uint8_t *row, int nsb, const int8_t *q, const float *d,
+                       const int32_t *sums)
+{
+    double acc = 0.0;
+    for (int b = 0; b < nsb; b++) {
+        const uint8_t *blk = row + (long)b * BLK;
+        double d4 = half_bits_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+        double dmin = half_bits_to_double((uint16_t)(blk[2] | (blk[3] << 8)));
+        const uint8_t *qs = blk + 16;
+        const int8_t *qb = q + (long)b * QK;
+        double bacc = 0.0;
+        for (int j = 0; j < QK / 32; j++) {
+            int sc, m;
+            scale_min(blk + 4, j, &sc, &m);
+            long P = 0;
+            for (int l = 0; l < 32; l++) {
+                uint8_t byte = qs[32 * (j / 2) + l];   /* sub-blocks 2c, 2c+1 share 32 bytes */
+                int q4 = (j % 2) ? (byte >> 4) : (byte & 15);
+                P += (long)q4 * qb[32 * j + l];
+            }
+            bacc += d4 * (double)sc * (double)P - dmin * (double)m * (double)sums[b * (QK / 32) + j];
+        }
+        acc += (double)d[b] * bacc;
+    }
+    return acc;
+}
+
+/*
+ * One expert on one token with Q8_K activations: g, u = Q4_K x Q8_K dots
+ * with the quantised x; h = SiLU(g) u in fp64, rounded to fp32 and quantised
+ * (the down projection's input is an activation vector too); o = the
+ * Q4_K x Q8_K dots of the down rows with the quantised h.
+ */
+static void expert_q8k(const int8_t *xq, const float *xd, const int32_t *xs, const uint8_t *gate_e,
+                       const uint8_t *up_e, const uint8_t *down_e, int H, int I, float *hf,
+                       int8_t *hq, float *hd, int32_t *hs, double *o)
+{
+    int nsb_h = H / QK, nsb_i = I / QK;
+#ifdef _OPENMP
+    int outer = !omp_in_parallel();
+#else
+    int outer = 0;
+#endif
+#pragma omp parallel for schedule(static) if (outer)
+    for (int r = 0; r < I; r++) {
+        double g = moq_row_dot_q8k(gate_e + (long)r * nsb_h * BLK, nsb_h, xq, xd, xs);
+        double u = moq_row_dot_q8k(up_e + (long)r * nsb_h * BLK, nsb_h, xq, xd, xs);
+        hf[r] = (float)(g / (1.0 + exp(-g)) * u);
+    }
+    moq_q8k_quantize(hf, nsb_i, hq, hd, hs);
+#pragma omp parallel for schedule(static) if (outer)
+    for (int r = 0; r < H; r++)
+        o[r] = moq_row_dot_q8k(down_e + (long)r * nsb_i * BLK, nsb_i, hq, hd, hs);
+}
+
+/*
+ * The FFN with Q8_K activations for the listed tokens (all T when `tokens`
+ * is NULL): x[t] is quantised, each routed expert runs expert_q8k, and
+ * y[t] = sum_j w[t,j] o_j in slot order.  Returns the number of slots
+ * skipped for an out-of-range expert index.
+ */
+long moq_ffn_q8k(const float *x, const int32_t *idx, const double *w,
+                 const uint8_t *gate, const uint8_t *up, const uint8_t *down,
+                 int T, int H, int E, int k, int I,
+                 const int32_t *tokens, int ntok, double *y)
+{
+    long gate_bytes = (long)I * (H / QK) * BLK;
+    long down_bytes = (long)H * (I / QK) * BLK;
+    int n = tokens ? ntok : T;
+    long skipped = 0;
+#ifdef _OPENMP
+    int by_token = n >= omp_get_max_threads();
+#else
+    int by_token = 0;
+#endif
+#pragma omp parallel for schedule(dynamic) reduction(+ : skipped) if (by_token)
+    for (int a = 0; a < n; a++) {
+        int t = tokens ? tokens[a] : a;
+        int8_t *xq = malloc((size_t)H);
+        float *xd = malloc(sizeof(float) * (size_t)(H / QK));
+        int32_t *xs = malloc(sizeof(int32_t) * (size_t)(H / 32));
+        float *hf = malloc(sizeof(float) * (size_t)I);
+        int8_t *hq = malloc((size_t)I);
+        float *hd = malloc(sizeof(float) * (size_t)(I / QK));
+        int32_t *hs = malloc(sizeof(int32_t) * (size_t)(I / 32));
+        double *o = malloc(sizeof(double) * (size_t)H);
+        double *yt = y + (long)t * H;
+        moq_q8k_quantize(x + (long)t * H, H / QK, xq, xd, xs);
+        for (int i = 0; i < H; i++)
+            yt[i] = 0.0;
+        for (int j = 0; j < k; j++) {
+            int e = idx[(long)t * k + j];
+            if (e < 0 || e >= E) {
+                skipped++;
+                continue;
+            }
+            expert_q8k(xq, xd, xs, gate + e * gate_bytes, up + e * gate_bytes, down + e * down_bytes,
+                       H, I, hf, hq, hd, hs, o);
+            double w_slot = w[(long)t * k + j];
+            for (int i = 0; i < H; i++)
+                yt[i] += w_slot * o[i];
+        }
+        free(xq);
+        free(xd);
+        free(xs);
+        free(hf);
+        free(hq);
+        free(hd);
+        free(hs);
+        free(o);
+    }
+    return skipped;
+}
+
+/*
  * Pre-FFN RMSNorm (forward_qwen3_moe.rs, aprender-serve 0.35.0, step 2f of
  * forward_qwen3_moe and step 2g of forward_single_qwen3_moe_with_cache:
  * ffn_input = rms_norm(hidden, ffn_norm_weight, eps)).  The pages name the

@@ -50,6 +50,11 @@ def _load(path: str = _SO):
     lib.moq_permutation.argtypes = [P, i, i, i, P, P, P]
     lib.moq_rmsnorm.argtypes = [P, P, ctypes.c_double, i, i, P]
     lib.moq_add_residual.argtypes = [P, P, l, P]
+    lib.moq_q8k_quantize.argtypes = [P, l, P, P, P]
+    lib.moq_row_dot_q8k.argtypes = [P, i, P, P, P]
+    lib.moq_row_dot_q8k.restype = ctypes.c_double
+    lib.moq_ffn_q8k.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P, i, P]
+    lib.moq_ffn_q8k.restype = l
     lib.moq_set_threads.argtypes = [i]
     lib.moq_max_threads.restype = i
     return lib
@@ -151,6 +156,52 @@ class Oracle:
     def layer(self, x, Wr, bias, k, gate, up, down, E, I, tokens=None):
         r = self.router(x, Wr, bias, k)
         y, skipped = self.ffn(x, r["idx"], r["w"], gate, up, down, E, I, tokens)
+        r["y"] = y
+        return r
+
+    # ---- Q8_K activations (the integer-dot variant of the layer)
+
+    def q8k_quantize(self, v):
+        """Q8_K blocks of fp32 rows v [rows, n] (n a multiple of 256): codes
+        int8 [rows, n], scales fp32 [rows, n/256], sub-block code sums int32
+        [rows, n/32]."""
+        v = _c(v, np.float32)
+        if v.ndim == 1:
+            v = v.reshape(1, -1)
+        rows, n = v.shape
+        assert n % 256 == 0
+        q = np.empty((rows, n), dtype=np.int8)
+        d = np.empty((rows, n // 256), dtype=np.float32)
+        sums = np.empty((rows, n // 32), dtype=np.int32)
+        self.L.moq_q8k_quantize(_p(v), rows * (n // 256), _p(q), _p(d), _p(sums))
+        return q, d, sums
+
+    def row_dot_q8k(self, row, ncols, q, d, sums):
+        """fp64 dot of one Q4_K row (bytes) with one Q8_K vector."""
+        return float(self.L.moq_row_dot_q8k(_p(_c(row, np.uint8)), ncols // 256,
+                                            _p(_c(q, np.int8)), _p(_c(d, np.float32)),
+                                            _p(_c(sums, np.int32))))
+
+    def ffn_q8k(self, x, idx, w, gate, up, down, E, I, tokens=None):
+        """y [T,H] fp64 with Q8_K activations (rows not in ``tokens`` NaN)
+        and the skip count."""
+        x = _c(x, np.float32)
+        T, H = x.shape
+        idx = _c(idx, np.int32)
+        k = idx.shape[1]
+        w = _c(w, np.float64)
+        y = np.full((T, H), np.nan, dtype=np.float64)
+        tok = None if tokens is None else _c(tokens, np.int32)
+        skipped = self.L.moq_ffn_q8k(_p(x), _p(idx), _p(w), _p(_c(gate, np.uint8)),
+                                     _p(_c(up, np.uint8)), _p(_c(down, np.uint8)),
+                                     T, H, E, k, I, None if tok is None else _p(tok),
+                                     0 if tok is None else tok.size, _p(y))
+        return y, int(skipped)
+
+    def layer_q8k(self, x, Wr, bias, k, gate, up, down, E, I, tokens=None):
+        """The fp32 router, then the FFN with Q8_K activations."""
+        r = self.router(x, Wr, bias, k)
+        y, skipped = self.ffn_q8k(x, r["idx"], r["w"], gate, up, down, E, I, tokens)
         r["y"] = y
         return r
 

@@ -14,6 +14,14 @@ from tests import test_oracle_pins as pins
 SRC = os.path.join(os.path.dirname(orc.__file__), "moe_oracle.c")
 
 MUTANTS = {
+    "q8k_scale_128": ("float s = 127.0f / amax;", "float s = 128.0f / amax;"),
+    "q8k_codes_truncated": ("qb[i] = (int8_t)rintf(t);", "qb[i] = (int8_t)t;"),
+    "q8k_min_term_dropped": ("bacc += d4 * (double)sc * (double)P - dmin * (double)m * (double)sums[b * (QK / 32) + j];",
+                             "bacc += d4 * (double)sc * (double)P;"),
+    "q8k_vector_scale_dropped": ("acc += (double)d[b] * bacc;", "acc += bacc;"),
+    "q8k_h_not_requantised": ("o[r] = moq_row_dot_q8k(down_e + (long)r * nsb_i * BLK, nsb_i, hq, hd, hs);",
+                              "o[r] = moq_row_dot_q8k(down_e + (long)r * nsb_i * BLK, nsb_i, xq, xd, xs);"),
+    "q8k_sums_of_wrong_subblock": ("acc += qb[32 * j + i];", "acc += qb[(32 * j + i + 32) % QK];"),
     "nibbles_swapped": ("int q = hi ? (byte >> 4) : (byte & 15);",
                         "int q = hi ? (byte & 15) : (byte >> 4);"),
     "scale_high_bits_shift": ("*sc = (scales[j + 4] & 15) | ((scales[j - 4] >> 6) << 4);",

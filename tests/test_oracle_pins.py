@@ -403,3 +403,122 @@ def test_block_output_is_hidden_plus_ffn_of_normed(oracle):
     np.testing.assert_array_equal(r0["ffn_in"], hidden)
     ref = oracle.layer(hidden, *args)
     np.testing.assert_array_equal(r0["y"], ref["y"])
+
+
+# ---------------------------------------------------------------- Q8_K activations
+#
+# The Q8_K-activation variant (qwen3_moe_dispatch.rs, aprender-serve 0.70.2,
+# doc of cpu_reference: the production CPU path's activations are Q8_K).
+# Reading pinned here: per 256-element block, d = amax / 127 and codes
+# q = round-half-even(v * (127 / amax)) in fp32, with sub-block code sums.
+
+def test_q8k_hand_block(oracle):
+    """v_i = i - 128: amax = 128, the scale 127/128 = 0.9921875 is exact and
+    so is every product (i - 128) * 0.9921875, so the codes are the rounded
+    exact values: -128 -> -127, -65 -> -64.49 -> -64, -64 -> -63.5 -> -64
+    (half to even), 63 -> 62.51 -> 63, 64 -> 63.5 -> 64 (half to even),
+    127 -> 126.01 -> 126."""
+    v = (np.arange(256) - 128).astype(np.float32)
+    q, d, sums = oracle.q8k_quantize(v)
+    assert d[0, 0] == np.float32(128.0) / np.float32(127.0)
+    hand = {0: -127, 63: -64, 64: -64, 65: -63, 128: 0, 191: 63, 192: 64, 255: 126}
+    for i, want in hand.items():
+        assert q[0, i] == want, (i, q[0, i], want)
+    # every code: the exact product rounded half to even (Python's round on a Fraction)
+    from fractions import Fraction
+    exact = [round(Fraction(i - 128) * Fraction(127, 128)) for i in range(256)]
+    np.testing.assert_array_equal(q[0].astype(int), exact)
+    np.testing.assert_array_equal(sums[0], [sum(exact[32 * j:32 * j + 32]) for j in range(8)])
+
+
+def test_q8k_zero_and_single_value_blocks(oracle):
+    v = np.zeros((2, 256), np.float32)
+    v[1, 7] = -3.0
+    q, d, sums = oracle.q8k_quantize(v)
+    assert d[0, 0] == 0.0 and not q[0].any() and not sums[0].any()
+    assert d[1, 0] == np.float32(3.0) / np.float32(127.0)
+    assert q[1, 7] == -127 and np.count_nonzero(q[1]) == 1
+    assert sums[1, 0] == -127 and not sums[1, 1:].any()
+
+
+def test_q8k_reconstruction_bound(oracle):
+    """Every code reconstructs its value to within half a step, the block's
+    largest magnitude lands on +-127, and the sums are the sub-block sums."""
+    rng = np.random.default_rng(31)
+    v = rng.normal(0, 1, (6, 512)).astype(np.float32)
+    v[1] *= 1e-3
+    v[2, :256] *= 1e4
+    v[3, 256:] = 0.0
+    q, d, sums = oracle.q8k_quantize(v)
+    for r in range(6):
+        for b in range(2):
+            vb = v[r, 256 * b:256 * b + 256].astype(np.float64)
+            qb = q[r, 256 * b:256 * b + 256].astype(np.float64)
+            db = float(d[r, b])
+            if not np.any(vb):
+                assert db == 0.0 and not np.any(qb)
+                continue
+            assert np.max(np.abs(qb * db - vb)) <= 0.5 * db * (1 + 1e-5)
+            assert np.max(np.abs(qb)) == 127
+    np.testing.assert_array_equal(sums, q.astype(np.int32).reshape(6, -1, 32).sum(axis=2))
+
+
+def test_q8k_row_dot_is_dense_dot_of_dequantised(oracle):
+    """The integer form (P, S sums with the block scales) equals the fp64 dot
+    of the dequantised Q4_K row with the dequantised vector d * q."""
+    rng = np.random.default_rng(32)
+    row = synth.random_blocks(rng, 3)
+    v = rng.normal(0, 1, 768).astype(np.float32)
+    q, d, sums = oracle.q8k_quantize(v)
+    dense_row = oracle.decode_rows(row, 1, 768)[0]
+    vdq = q[0].astype(np.float64) * np.repeat(d[0].astype(np.float64), 256)
+    want = float(dense_row @ vdq)
+    got = oracle.row_dot_q8k(row, 768, q[0], d[0], sums[0])
+    assert abs(got - want) <= 1e-12 * max(1.0, float(np.abs(dense_row).sum() * np.abs(vdq).max()))
+
+
+def test_q8k_ffn_is_dense_composition(oracle):
+    """The Q8_K FFN against dense NumPy matrices: x quantised (the pinned
+    quantiser), g and u dense products with the dequantised x, h = SiLU(g) u
+    rounded to fp32 and quantised, o = W_down times the dequantised h,
+    y = sum_j w_j o_j."""
+    shape, blobs = _tiny_layer(E=4, seed=6)
+    rng = np.random.default_rng(33)
+    T = 3
+    x = rng.normal(0, 1, (T, shape.H)).astype(np.float32)
+    idx = np.array([[1, 3], [2, 2], [0, 1]], np.int32)
+    w = np.array([[0.6, 0.4], [0.5, 0.5], [0.9, 0.1]])
+    y, skipped = oracle.ffn_q8k(x, idx, w, blobs["gate"], blobs["up"], blobs["down"], shape.E,
+                                shape.I)
+    assert skipped == 0
+
+    def deq(v):
+        q, d, _ = oracle.q8k_quantize(v)
+        return q[0].astype(np.float64) * np.repeat(d[0].astype(np.float64), 256)
+
+    dense = {e: _dense(oracle, shape, blobs, e) for e in range(4)}
+    for t in range(T):
+        xv = deq(x[t])
+        want = np.zeros(shape.H)
+        for j in range(2):
+            g, u, dn = dense[idx[t, j]]
+            h = (_silu(g @ xv) * (u @ xv)).astype(np.float32)
+            want += w[t, j] * (dn @ deq(h))
+        np.testing.assert_allclose(y[t], want, rtol=1e-9, atol=1e-12 * np.abs(want).max())
+
+
+def test_q8k_ffn_close_to_fp32_ffn(oracle):
+    """Eight-bit activations cost little accuracy on one layer: the output's
+    cosine with the fp32-activation FFN stays above 0.99 on every token (the
+    pages measure 0.985 for a whole model's logits, after every layer)."""
+    shape, blobs = _tiny_layer(E=8, seed=7)
+    rng = np.random.default_rng(34)
+    x = rng.normal(0, 1, (4, shape.H)).astype(np.float32)
+    idx = np.array([[0, 5], [1, 2], [7, 3], [4, 6]], np.int32)
+    w = np.full((4, 2), 0.5)
+    args = (blobs["gate"], blobs["up"], blobs["down"], shape.E, shape.I)
+    yq, _ = oracle.ffn_q8k(x, idx, w, *args)
+    yf, _ = oracle.ffn(x, idx, w, *args)
+    for t in range(4):
+        cos = float(yq[t] @ yf[t] / (np.linalg.norm(yq[t]) * np.linalg.norm(yf[t])))
+        assert 0.99 < cos < 1.0
