@@ -227,6 +227,53 @@ MOE_API moe_status moe_layer_host(const float *x_host, const float *Wr_dev, cons
 MOE_API moe_status moe_read_device_status(const void *ws_dev, void *stream, int32_t *detail);
 
 /*
+ * Q8_K activations (qwen3_moe_dispatch.rs, aprender-serve 0.70.2, doc of
+ * cpu_reference: the production CPU path runs the layer on Q8_K
+ * activations, as opposed to the fp32-activation path of moe_layer).  Every
+ * activation vector that meets a Q4_K matrix is quantised per block of 256
+ * consecutive values to one fp32 scale d and 256 signed 8-bit codes q
+ * (v ~= d q):  amax = max |v|;  amax = 0 gives d = 0 and all codes 0;
+ * otherwise d = amax / 127 and q_i = v_i * (127 / amax) rounded to the
+ * nearest integer, halves to even, every step in fp32.
+ *
+ * moe_quantize_q8k: `rows` rows of n fp32 values (n a multiple of 256,
+ * rows * n <= 2^31) at v_dev [rows, n] (16-byte aligned) -> q_dev int8
+ * [rows, n] (16-byte aligned), d_dev fp32 [rows, n/256], sums_dev int32
+ * [rows, n/32] (each 32-value sub-block's code sum).  Errors:
+ * MOE_ERR_INVALID_SHAPE, MOE_ERR_NULL, MOE_ERR_MISALIGNED.
+ */
+MOE_API moe_status moe_quantize_q8k(const float *v_dev, int rows, int n, int8_t *q_dev,
+                                    float *d_dev, int32_t *sums_dev, void *stream);
+
+/*
+ * moe_ffn with Q8_K activations: x[t] is quantised; each routed expert's
+ * g = W_gate x and u = W_up x are integer Q4_K x Q8_K dot products (per
+ * sub-block of 32: d8 (d4 sc P - dmin m S), P the integer dot of the 4-bit
+ * and 8-bit codes, S the 8-bit codes' sum); h = SiLU(g) u in fp32 is
+ * quantised the same way; o = W_down h likewise; y[t] = sum_j w_j o_j.
+ * Arguments, layouts, workspace and errors as moe_ffn (the same workspace
+ * size; a slot with an expert index outside [0, E) contributes 0 and is
+ * recorded as MOE_ERR_EXPERT_RANGE).  Four launches.
+ */
+MOE_API moe_status moe_ffn_q8k(const float *x_dev, const int32_t *idx_dev, const float *w_dev,
+                       const void *gate_dev, const void *up_dev, const void *down_dev,
+                       int T, int H, int E, int k, int I, float *y_dev,
+                       void *ws_dev, size_t ws_bytes, void *stream);
+
+/*
+ * moe_router (fp32 logits: the router is a dense f32 matvec, not a Q4_K one)
+ * then moe_ffn_q8k.  Arguments as moe_layer.
+ */
+MOE_API moe_status moe_layer_q8k(const float *x_dev, const float *Wr_dev, const float *bias_dev,
+                         const void *gate_dev, const void *up_dev, const void *down_dev,
+                         int T, int H, int E, int k, int I,
+                         int32_t *idx_dev, float *w_dev, float *y_dev,
+                         void *ws_dev, size_t ws_bytes, void *stream);
+
+/* Number of kernel launches one moe_layer_q8k call enqueues (0: invalid shape). */
+MOE_API int moe_layer_q8k_launch_count(int T, int H, int E, int k, int I);
+
+/*
  * moe_layer for one token without any workspace, for callers that cannot
  * allocate device memory (for example a plugin whose host framework owns
  * every device allocation, or a decode loop that must not reach an

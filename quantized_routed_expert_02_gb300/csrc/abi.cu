@@ -155,6 +155,37 @@ moe_status layer_enqueue(const float *x, const float *norm_w, float eps, const f
     return ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, dev, ep, s);
 }
 
+// The Q8_K-activation FFN's scratch inside the fp16 activation regions,
+// which that path does not otherwise use: codes, then block scales, then
+// sub-block code sums (1.14 n bytes for n values; the regions hold 2 n).
+struct Q8Scratch {
+    int8_t *xq, *hq;
+    float *xd, *hd;
+    int32_t *xs, *hs;
+};
+
+Q8Scratch q8_scratch(const Ws &W, int T, int H, int k, int I) {
+    const size_t nx = size_t(T) * H, nh = size_t(T) * k * I;
+    Q8Scratch q;
+    q.xq = reinterpret_cast<int8_t *>(W.base + W.L.x16);
+    q.xd = reinterpret_cast<float *>(W.base + W.L.x16 + nx);
+    q.xs = reinterpret_cast<int32_t *>(W.base + W.L.x16 + nx + nx / 64);
+    q.hq = reinterpret_cast<int8_t *>(W.base + W.L.h16);
+    q.hd = reinterpret_cast<float *>(W.base + W.L.h16 + nh);
+    q.hs = reinterpret_cast<int32_t *>(W.base + W.L.h16 + nh + nh / 64);
+    return q;
+}
+
+moe_status q8k_ffn_enqueue(const float *x, const int32_t *idx, const float *w, const void *gate,
+                           const void *up, const void *down, int T, int H, int E, int k, int I,
+                           float *y, const Ws &W, int sms, cudaStream_t s) {
+    const Q8Scratch q = q8_scratch(W, T, H, k, I);
+    return cuda_status(launch_q8k_ffn(x, idx, w, static_cast<const uint8_t *>(gate),
+                                      static_cast<const uint8_t *>(up),
+                                      static_cast<const uint8_t *>(down), T, H, E, k, I, y, q.xq,
+                                      q.xd, q.xs, W.f32(W.L.h), q.hq, q.hd, q.hs, W.hdr(), sms, s));
+}
+
 }  // namespace
 
 moe_status moeq4k::validate_shape(int T, int H, int E, int k, int I) {
@@ -206,6 +237,12 @@ int moe_layer_launch_count(int T, int H, int E, int k, int I) {
         return router + permutation + 1 + plans + 2 + 1;
     }
     return router + permutation + 3 /* gate/up, down, combine */;
+}
+
+int moe_layer_q8k_launch_count(int T, int H, int E, int k, int I) {
+    if (check_shape(T, H, E, k, I) != MOE_OK) return 0;
+    const int router = (T >= 256 || T <= 2) ? 1 : 2;
+    return router + 4;  // quantise x, gate/up, quantise h, down (with the combine)
 }
 
 void moe_debug_set_wait_limit(unsigned long long ns) { g_wait_ns = ns ? ns : 1000000000ull; }
@@ -387,6 +424,64 @@ moe_status moe_layer_host(const float *x_host, const float *Wr, const float *bia
                       stream));
     MOE_TRY(cuda_status(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s)));
     return cuda_status(cudaStreamSynchronize(s));
+}
+
+moe_status moe_quantize_q8k(const float *v, int rows, int n, int8_t *q, float *d, int32_t *sums,
+                            void *stream) {
+    if (rows < 1 || n < kQK || n % kQK != 0 || int64_t(rows) * n > (int64_t(1) << 31))
+        return MOE_ERR_INVALID_SHAPE;
+    MOE_TRY(check_ptr(v, 16));
+    MOE_TRY(check_ptr(q, 16));
+    MOE_TRY(check_ptr(d, 4));
+    MOE_TRY(check_ptr(sums, 4));
+    int sms = 0;
+    MOE_TRY(device_info(&sms, nullptr));
+    return cuda_status(launch_q8k_quantize(v, rows, n, q, d, sums, sms,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_ffn_q8k(const float *x, const int32_t *idx, const float *w, const void *gate,
+                       const void *up, const void *down, int T, int H, int E, int k, int I,
+                       float *y, void *ws, size_t ws_bytes, void *stream) {
+    MOE_TRY(check_shape(T, H, E, k, I));
+    MOE_TRY(check_ptr(x, 16));
+    MOE_TRY(check_ptr(idx, 16));
+    MOE_TRY(check_ptr(w, 16));
+    MOE_TRY(check_ptr(gate, 16));
+    MOE_TRY(check_ptr(up, 16));
+    MOE_TRY(check_ptr(down, 16));
+    MOE_TRY(check_ptr(y, 16));
+    WsLayout L = ws_layout(T, H, E, k, I, false);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    int sms = 0;
+    MOE_TRY(device_info(&sms, nullptr));
+    Ws W{static_cast<uint8_t *>(ws), L};
+    return q8k_ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms,
+                           static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_q8k(const float *x, const float *Wr, const float *bias, const void *gate,
+                         const void *up, const void *down, int T, int H, int E, int k, int I,
+                         int32_t *idx, float *w, float *y, void *ws, size_t ws_bytes,
+                         void *stream) {
+    MOE_TRY(check_shape(T, H, E, k, I));
+    MOE_TRY(check_ptr(x, 16));
+    MOE_TRY(check_ptr(Wr, 16));
+    if (bias && !aligned(bias, 16)) return MOE_ERR_MISALIGNED;
+    MOE_TRY(check_ptr(gate, 16));
+    MOE_TRY(check_ptr(up, 16));
+    MOE_TRY(check_ptr(down, 16));
+    MOE_TRY(check_ptr(idx, 16));
+    MOE_TRY(check_ptr(w, 16));
+    MOE_TRY(check_ptr(y, 16));
+    WsLayout L = ws_layout(T, H, E, k, I, false);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    int sms = 0;
+    MOE_TRY(device_info(&sms, nullptr));
+    Ws W{static_cast<uint8_t *>(ws), L};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(), s)));
+    return q8k_ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, s);
 }
 
 moe_status moe_read_device_status(const void *ws, void *stream, int32_t *detail) {

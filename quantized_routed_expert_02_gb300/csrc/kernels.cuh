@@ -77,4 +77,16 @@ cudaError_t launch_decode_stream(const float *x, const int32_t *idx, const float
                                  int H, int E, int k, int I, float *y, float *hbuf, WsHeader *hdr,
                                  const OutEpilogue &ep, int num_sms, cudaStream_t s);
 
+// Q8_K activations: `rows` fp32 rows of n values (n a multiple of 256) ->
+// codes [rows, n], block scales [rows, n/256], sub-block code sums
+// [rows, n/32]; and the expert FFN on them (x and h quantised; `hbuf`
+// T*k*I floats of scratch; xq/xd/xs and hq/hd/hs the quantised x and h).
+cudaError_t launch_q8k_quantize(const float *v, long rows, int n, int8_t *q, float *d,
+                                int32_t *sums, int num_sms, cudaStream_t s);
+cudaError_t launch_q8k_ffn(const float *x, const int32_t *idx, const float *w, const uint8_t *gate,
+                           const uint8_t *up, const uint8_t *down, int T, int H, int E, int k,
+                           int I, float *y, int8_t *xq, float *xd, int32_t *xs, float *hbuf,
+                           int8_t *hq, float *hd, int32_t *hs, WsHeader *hdr, int num_sms,
+                           cudaStream_t s);
+
 }  // namespace moeq4k

@@ -43,6 +43,11 @@ _SIGS = {
                        ctypes.c_int),
     "moe_layer_block": ([_P, _P, ctypes.c_float, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
                          _P, _I, _I, _P, _P, _P, _P, _S, _P], ctypes.c_int),
+    "moe_quantize_q8k": ([_P, _I, _I, _P, _P, _P, _P], ctypes.c_int),
+    "moe_ffn_q8k": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _S, _P], ctypes.c_int),
+    "moe_layer_q8k": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P],
+                      ctypes.c_int),
+    "moe_layer_q8k_launch_count": ([_I, _I, _I, _I, _I], ctypes.c_int),
     "moe_read_device_status": ([_P, _P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
     "moe_layer_noalloc": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P],
                           ctypes.c_int),
@@ -105,6 +110,10 @@ def moe_workspace_bytes_host(T, H, E, k, I) -> int:
 
 def moe_layer_launch_count(T, H, E, k, I) -> int:
     return _lib.moe_layer_launch_count(T, H, E, k, I)
+
+
+def moe_layer_q8k_launch_count(T, H, E, k, I) -> int:
+    return _lib.moe_layer_q8k_launch_count(T, H, E, k, I)
 
 
 def alloc_workspace(T, H, E, k, I, device="cuda", host_staging=False) -> torch.Tensor:
@@ -182,6 +191,30 @@ def moe_layer_noalloc(x, Wr, bias, gate, up, down, k, I, idx, w, y, stream=None)
     _check(_lib.moe_layer_noalloc(_ptr(x), _ptr(Wr), _ptr(bias), _ptr(gate), _ptr(up), _ptr(down),
                                   T, H, E, k, I, _ptr(idx), _ptr(w), _ptr(y), _stream(stream)),
            "moe_layer_noalloc")
+
+
+def moe_quantize_q8k(v, q, d, sums, stream=None) -> None:
+    """Q8_K blocks of the fp32 rows ``v`` [rows, n]: int8 codes ``q`` [rows, n],
+    fp32 scales ``d`` [rows, n/256], int32 sub-block sums ``sums`` [rows, n/32]."""
+    rows, n = v.shape
+    _check(_lib.moe_quantize_q8k(_ptr(v), rows, n, _ptr(q), _ptr(d), _ptr(sums), _stream(stream)),
+           "moe_quantize_q8k")
+
+
+def moe_ffn_q8k(x, idx, w, gate, up, down, E, I, y, ws, stream=None) -> None:
+    T, H = x.shape
+    k = idx.shape[1]
+    _check(_lib.moe_ffn_q8k(_ptr(x), _ptr(idx), _ptr(w), _ptr(gate), _ptr(up), _ptr(down),
+                            T, H, E, k, I, _ptr(y), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_ffn_q8k")
+
+
+def moe_layer_q8k(x, Wr, bias, gate, up, down, k, I, idx, w, y, ws, stream=None) -> None:
+    T, H = x.shape
+    E = Wr.shape[0]
+    _check(_lib.moe_layer_q8k(_ptr(x), _ptr(Wr), _ptr(bias), _ptr(gate), _ptr(up), _ptr(down),
+                              T, H, E, k, I, _ptr(idx), _ptr(w), _ptr(y), _ptr(ws), ws.numel(),
+                              _stream(stream)), "moe_layer_q8k")
 
 
 def moe_read_device_status(ws, stream=None):
