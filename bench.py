@@ -13,7 +13,9 @@ The headline workload (`--config`, default the Qwen3-30B-A3B single token)
 gives the line's top-level numbers, timed over exactly `--steps` steps.
 Every other workload (`--configs`, default all) is timed the same way in the
 same run and reported under `per_config`, each with its own roofline, clock
-record and CPU baseline.  The three Qwen3-30B-A3B workloads share one set of
+record and CPU baseline; so is the Q8_K-activation variant of the layer on
+the single-token workloads (`<workload>_q8k`, with the cosine of its output
+against the fp32-activation output on the same inputs).  The three Qwen3-30B-A3B workloads share one set of
 48 expert-weight layers and router matrices (the batched ones add their own
 activations, and the 64-token one its router bias); the two Qwen3-235B-A22B
 workloads share their 8 layers.
@@ -72,6 +74,8 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=0, help="override every rotation's length")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="bound on the headline's oracle CPU-baseline sample (all cores)")
+    ap.add_argument("--q8k", default="a3b_decode,a22b_decode",
+                    help="workloads also timed with Q8_K activations: a comma list or none")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -242,7 +246,7 @@ def _oracle_inputs(name, layer, rank):
     return x, Wr, bias, synth.expert_blobs(fam, layer, experts=experts)
 
 
-def oracle_sample(name, seconds, rank=0, threads=0, max_tokens=64, inputs=None):
+def oracle_sample(name, seconds, rank=0, threads=0, max_tokens=64, inputs=None, q8k=False):
     """Time the fp64 oracle (router on every token, FFN on at most
     `max_tokens` of them) on calls of one layer of the workload until
     `seconds` of wall time have been spent (at least one call).  `threads` =
@@ -264,8 +268,8 @@ def oracle_sample(name, seconds, rank=0, threads=0, max_tokens=64, inputs=None):
     while True:
         t0 = time.perf_counter()
         r = o.router(x, Wr, bias, shape.k)
-        o.ffn(x, r["idx"], r["w"], blobs["gate"], blobs["up"], blobs["down"], shape.E, shape.I,
-              tokens=tokens)
+        (o.ffn_q8k if q8k else o.ffn)(x, r["idx"], r["w"], blobs["gate"], blobs["up"],
+                                      blobs["down"], shape.E, shape.I, tokens=tokens)
         t_total += time.perf_counter() - t0
         calls += 1
         if t_total >= seconds:
@@ -276,18 +280,18 @@ def oracle_sample(name, seconds, rank=0, threads=0, max_tokens=64, inputs=None):
         "unit": "tokens/s",
         "cores": used,
         "kind": "oracle",
-        "sample": (f"{calls} layer call(s) of {name} (T={T}"
+        "sample": (f"{calls} layer call(s) of {name}{' (Q8_K activations)' if q8k else ''} (T={T}"
                    + (f", FFN on {ntok} of {T} tokens, router on all" if tokens is not None else "")
                    + f"), fp64 C oracle on {used} thread(s), {t_total:.1f} s"),
     }
 
 
-def cpu_baseline(name, seconds, rank=0):
+def cpu_baseline(name, seconds, rank=0, q8k=False):
     """The oracle on all host cores, with a one-thread figure beside it."""
     inputs = _oracle_inputs(name, 0, rank)
-    allc = oracle_sample(name, seconds, rank, threads=0, inputs=inputs)
+    allc = oracle_sample(name, seconds, rank, threads=0, inputs=inputs, q8k=q8k)
     one = oracle_sample(name, max(0.5, seconds / 2), rank, threads=1, max_tokens=8,
-                        inputs=inputs)
+                        inputs=inputs, q8k=q8k)
     allc["host_cores"] = os.cpu_count()
     allc["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
     return allc
@@ -342,19 +346,21 @@ class Workload:
         self.bias = None if b is None else torch.from_numpy(b).to(dev)
 
 
-def time_workload(m, torch, W, steps, warmup, dev, dist, clocks, peaks):
+def time_workload(m, torch, W, steps, warmup, dev, dist, clocks, peaks, q8k=False):
     """CUDA-graph one step (the whole rotation), warm it up, time `steps`
-    replays with CUDA events on the launching stream; returns the record."""
+    replays with CUDA events on the launching stream; returns the record.
+    `q8k`: the Q8_K-activation variant of the layer (moe_layer_q8k)."""
     s = W.shape
     T, H, E, k, I = s.T, s.H, s.E, s.k, s.I
     n_layers = len(W.layers)
     ws = m.alloc_workspace(T, H, E, k, I, device=dev)
     stream = torch.cuda.Stream(device=dev)
+    layer_fn = m.moe_layer_q8k if q8k else m.moe_layer
 
     def one_step(st):
         for L in W.layers:
-            m.moe_layer(L["x"], L["Wr"], W.bias, L["gate"], L["up"], L["down"], k, I,
-                        L["idx"], L["w"], L["y"], ws, stream=st)
+            layer_fn(L["x"], L["Wr"], W.bias, L["gate"], L["up"], L["down"], k, I,
+                     L["idx"], L["w"], L["y"], ws, stream=st)
 
     with torch.cuda.stream(stream):
         one_step(stream)
@@ -400,7 +406,8 @@ def time_workload(m, torch, W, steps, warmup, dev, dist, clocks, peaks):
                            f"{m.status_str(code)} ({detail})")
     ms = max_over_ranks(start.elapsed_time(end), dist, dev)
     call_us = ms * 1e3 / (steps * n_layers)
-    launches_per_call = m.moe_layer_launch_count(T, H, E, k, I)
+    launches_per_call = (m.moe_layer_q8k_launch_count if q8k else m.moe_layer_launch_count)(
+        T, H, E, k, I)
 
     # roofline: HBM bytes, or for the tensor-core path (T*k >= 256 routed
     # slots) the slower of the bytes at the HBM peak and the expert FLOPs at
@@ -410,7 +417,7 @@ def time_workload(m, torch, W, steps, warmup, dev, dist, clocks, peaks):
     bytes_call = step_bytes / n_layers
     achieved = bytes_call / (call_us * 1e-6) / 1e9
     flops_call = 6.0 * T * k * H * I
-    tensor_path = T * k >= 256
+    tensor_path = T * k >= 256 and not q8k
     hbm_floor_us = bytes_call / (peaks["hbm"] * 1e9) * 1e6
     tensor_floor_us = flops_call / (peaks["tf_burst"] * 1e12) * 1e6
     if tensor_path and tensor_floor_us > hbm_floor_us:
@@ -432,14 +439,15 @@ def time_workload(m, torch, W, steps, warmup, dev, dist, clocks, peaks):
             ((step_bytes + wr_bytes) / n_layers) / (call_us * 1e-6) / 1e9, 1),
     })
     rec = {
-        "workload": W.name, "T": T, "H": H, "E": E, "k": k, "I": I,
+        "workload": W.name + ("_q8k" if q8k else ""), "T": T, "H": H, "E": E, "k": k, "I": I,
         "layers_per_step": n_layers, "steps": steps,
         "us_per_layer_call": round(call_us, 3),
         "tokens_per_s": round(T / (call_us * 1e-6), 1),
         "unique_experts_per_call": round(sum(uniques) / len(uniques), 2),
         "launches_per_call": launches_per_call,
         "gpu_launches": launches_per_call * n_layers * steps,
-        "dtype": "f16xf16->f32" if tensor_path else "f32",
+        "dtype": ("s8 (Q8_K activations) x u4 -> s32" if q8k
+                  else "f16xf16->f32" if tensor_path else "f32"),
         "roofline": roofline,
         "clocks": clk,
         "_ms": ms, "_ws": ws, "_stream": stream,
@@ -523,6 +531,25 @@ def main():
         step_s = probe["_ms"] / 2e3
         steps = max(args.steps, int(math.ceil(MIN_REGION_S / max(step_s, 1e-6))))
         per[name] = time_workload(m, torch, W, steps, args.warmup, dev, dist, clocks, peaks)
+    # the Q8_K-activation variant on the same inputs, with its output's
+    # cosine against the fp32-activation path's (the y buffers hold the last
+    # fp32 replay's outputs when the variant starts)
+    q8k_names = [] if args.q8k == "none" else [n for n in args.q8k.split(",") if n in workloads]
+    for name in q8k_names:
+        W = workloads[name]
+        y_fp32 = [L["y"].double().clone() for L in W.layers]
+        probe = time_workload(m, torch, W, 2, 1, dev, dist, clocks, peaks, q8k=True)
+        step_s = probe["_ms"] / 2e3
+        steps = max(args.steps, int(math.ceil(MIN_REGION_S / max(step_s, 1e-6))))
+        rec = time_workload(m, torch, W, steps, args.warmup, dev, dist, clocks, peaks, q8k=True)
+        cos = []
+        for L, yf in zip(W.layers, y_fp32):
+            yq = L["y"].double()
+            cos += (torch.sum(yq * yf, dim=1) / (yq.norm(dim=1) * yf.norm(dim=1))).tolist()
+        rec["cosine_vs_fp32_activations"] = {
+            "min": round(min(cos), 6), "mean": round(sum(cos) / len(cos), 6),
+            "over": f"{len(W.layers)} layers x {W.shape.T} tokens, same inputs"}
+        per[name + "_q8k"] = rec
     clocks.stop()
 
     W = workloads[args.config]
@@ -569,6 +596,8 @@ def main():
         head["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds, rank)
         for name in others:
             per[name]["cpu_baseline"] = cpu_baseline(name, 2.0, rank)
+        for name in q8k_names:
+            per[name + "_q8k"]["cpu_baseline"] = cpu_baseline(name, 2.0, rank, q8k=True)
 
     def public(rec):
         return {kk: v for kk, v in rec.items() if not kk.startswith("_")}
@@ -602,7 +631,7 @@ def main():
             "e2e": e2e,
             "gpu_launches": head["gpu_launches"],
             "clocks": head["clocks"],
-            "per_config": {name: public(per[name]) for name in others},
+            "per_config": {name: public(rec) for name, rec in per.items()},
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
