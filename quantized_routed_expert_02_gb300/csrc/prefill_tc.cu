@@ -258,6 +258,72 @@ __device__ __forceinline__ Item item_of(const Params &p, int it, int nch) {
     return I;
 }
 
+// The epilogue of item `E` (the li_e-th of this CTA) from accumulator
+// buffer li_e % nbuf, run by the sixteen dequantising warps (warp (q, part):
+// TMEM lane quadrant q, column quarter `part`).  The accumulator is
+// D[token][weight row]: TMEM lane = the chunk's token (slot) n, column =
+// weight row c of the item's 256 (gate rows 0-127 then up rows 0-127, or 256
+// down rows).  Warp (q, part) reads lanes 32q.. (tokens 32q..32q+31) and a
+// quarter of the rows; each thread then writes whole 16-byte runs of its
+// token's row.  Not inlined: the stage loop that calls it is unrolled.
+__device__ __noinline__ bool item_epilogue(const Params &p, const Item &E, uint32_t li_e,
+                                           uint32_t nbuf, uint32_t taddr, uint64_t *accfull,
+                                           uint64_t *accempty, uint64_t deadline, int q, int part,
+                                           int lane) {
+            const uint32_t buf = li_e % nbuf, use = li_e / nbuf;
+            if (!warp_wait(accfull + buf, use & 1u, deadline, p.hdr, 14)) return false;
+            tc::fence_after_sync();
+            const int ntok = E.ch.tok_cnt;
+            for (int h = 0; h < p.mh; ++h) {
+            // warp-uniform: quadrants past the chunk's tokens have no output
+            if (128 * h + 32 * q < ntok) {
+                const int n = 128 * h + 32 * q + lane;
+                const bool valid = n < ntok;
+                const uint32_t lanebase = taddr + (buf + uint32_t(h)) * 256u + (uint32_t(q * 32) << 16);
+                if (p.mode == 0) {
+                    // h = SiLU(g) * u for rows 32*part .. +31 of the item's 128,
+                    // stored in the kperm order of the down GEMM's K
+                    __half *hrow = p.h16 + size_t(E.row0 + n) * p.I + E.rt * kBM;
+                    for (int c0 = 32 * part; c0 < 32 * part + 32; c0 += 8) {
+                        float g[8], u[8];
+                        tc::tmem_ld8(lanebase + c0, g);
+                        tc::tmem_ld8(lanebase + 128 + c0, u);
+                        float h[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            // SiLU(g) * u with the fast exponential and divide: the
+                            // result is rounded to fp16
+                            const float e = __expf(fminf(-g[j], 80.0f));
+                            h[j] = __fdividef(g[j], 1.0f + e) * u[j];
+                        }
+                        uint4 o;  // positions c0 + (0, 2, 1, 3, 4, 6, 5, 7) hold h[0..7]
+                        o.x = h2_bits(__floats2half2_rn(h[0], h[2]));
+                        o.y = h2_bits(__floats2half2_rn(h[1], h[3]));
+                        o.z = h2_bits(__floats2half2_rn(h[4], h[6]));
+                        o.w = h2_bits(__floats2half2_rn(h[5], h[7]));
+                        if (valid) *reinterpret_cast<uint4 *>(hrow + c0) = o;
+                    }
+                } else {
+                    // per-slot outputs: rows 64*part .. +63 of the item's 256
+                    float *orow = p.o + size_t(valid ? p.perm[E.row0 + n] : 0) * p.H +
+                                  E.rt * p.item_rows;
+                    for (int c0 = 64 * part; c0 < 64 * part + 64; c0 += 8) {
+                        float v[8];
+                        tc::tmem_ld8(lanebase + c0, v);
+                        if (valid) {
+                            *reinterpret_cast<float4 *>(orow + c0) = make_float4(v[0], v[1], v[2], v[3]);
+                            *reinterpret_cast<float4 *>(orow + c0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                        }
+                    }
+                }
+            }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(accempty + buf);
+            return true;
+        }
+
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ Params p) {
     pdl_enter();
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -348,67 +414,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         soff[3] = tc::sw128_offset(r, 8 * (2 * hh + 5));
         const int q = warp & 3, part = (warp - 4) >> 2;  // TMEM lane quadrant, column quarter
 
-        // The epilogue of item `E` (the li_e-th of this CTA) from accumulator
-        // buffer li_e & 1.  The accumulator is D[token][weight row]: TMEM lane
-        // = the chunk's token (slot) n, column = weight row c of the item's 256
-        // (gate rows 0-127 then up rows 0-127, or 256 down rows).  Warp (q,
-        // part) reads lanes 32q.. (tokens 32q..32q+31) and half `part` of the
-        // rows; each thread then writes whole 16-byte runs of its token's row.
-        auto epilogue = [&](const Item &E, uint32_t li_e) -> bool {
-            const uint32_t buf = li_e % nbuf, use = li_e / nbuf;
-            if (!warp_wait(accfull + buf, use & 1u, deadline, p.hdr, 14)) return false;
-            tc::fence_after_sync();
-            const int ntok = E.ch.tok_cnt;
-            for (int h = 0; h < p.mh; ++h) {
-            // warp-uniform: quadrants past the chunk's tokens have no output
-            if (128 * h + 32 * q < ntok) {
-                const int n = 128 * h + 32 * q + lane;
-                const bool valid = n < ntok;
-                const uint32_t lanebase = taddr + (buf + uint32_t(h)) * 256u + (uint32_t(q * 32) << 16);
-                if (p.mode == 0) {
-                    // h = SiLU(g) * u for rows 32*part .. +31 of the item's 128,
-                    // stored in the kperm order of the down GEMM's K
-                    __half *hrow = p.h16 + size_t(E.row0 + n) * p.I + E.rt * kBM;
-                    for (int c0 = 32 * part; c0 < 32 * part + 32; c0 += 8) {
-                        float g[8], u[8];
-                        tc::tmem_ld8(lanebase + c0, g);
-                        tc::tmem_ld8(lanebase + 128 + c0, u);
-                        float h[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            // SiLU(g) * u with the fast exponential and divide: the
-                            // result is rounded to fp16
-                            const float e = __expf(fminf(-g[j], 80.0f));
-                            h[j] = __fdividef(g[j], 1.0f + e) * u[j];
-                        }
-                        uint4 o;  // positions c0 + (0, 2, 1, 3, 4, 6, 5, 7) hold h[0..7]
-                        o.x = h2_bits(__floats2half2_rn(h[0], h[2]));
-                        o.y = h2_bits(__floats2half2_rn(h[1], h[3]));
-                        o.z = h2_bits(__floats2half2_rn(h[4], h[6]));
-                        o.w = h2_bits(__floats2half2_rn(h[5], h[7]));
-                        if (valid) *reinterpret_cast<uint4 *>(hrow + c0) = o;
-                    }
-                } else {
-                    // per-slot outputs: rows 64*part .. +63 of the item's 256
-                    float *orow = p.o + size_t(valid ? p.perm[E.row0 + n] : 0) * p.H +
-                                  E.rt * p.item_rows;
-                    for (int c0 = 64 * part; c0 < 64 * part + 64; c0 += 8) {
-                        float v[8];
-                        tc::tmem_ld8(lanebase + c0, v);
-                        if (valid) {
-                            *reinterpret_cast<float4 *>(orow + c0) = make_float4(v[0], v[1], v[2], v[3]);
-                            *reinterpret_cast<float4 *>(orow + c0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
-                        }
-                    }
-                }
-            }
-            }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(accempty + buf);
-            return true;
-        };
-
         uint32_t g = 0, gr = 0, li = 0;
         RingPos rp, ap;  // raw ring, stage ring
         Item prev;
@@ -426,7 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 const uint32_t rsl = rbase + rs * uint32_t(nmat * kRawMat);
                 const uint4 head = lds128(rsl);
-                for (int c = 0; c < kSub; ++c, ++g, ap.next(NS)) {
+#pragma unroll
+                for (int c = 0; c < kSub; ++c) {
                     const int s = sr * kSub + c;
                     const uint32_t as = ap.slot;
                     if (tid == 128) GT_STAMP(p, 1, g);
@@ -461,9 +467,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     // slot's "full" phase implies both operands are in place
                     if (lane == 0) mbar_arrive(sfull + as);
                     if (tid == 128) GT_STAMP(p, 3, g);
+                    ++g;
+                    ap.next(NS);
                     if (have_prev && s == epi_at) {
                         if (tid == 128) GT_STAMP(p, 9, li - 1);
-                        if (!epilogue(prev, li - 1)) ok = false;
+                        if (!item_epilogue(p, prev, li - 1, nbuf, taddr, accfull, accempty, deadline,
+                                           q, part, lane))
+                            ok = false;
                         if (tid == 128) GT_STAMP(p, 10, li - 1);
                         have_prev = false;
                     }
@@ -474,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
         if (ok && have_prev) {
             if (tid == 128) GT_STAMP(p, 9, li - 1);
-            ok = epilogue(prev, li - 1);
+            ok = item_epilogue(p, prev, li - 1, nbuf, taddr, accfull, accempty, deadline, q, part,
+                               lane);
             if (tid == 128) GT_STAMP(p, 10, li - 1);
         }
         if (!ok) *abort_flag = 1;
