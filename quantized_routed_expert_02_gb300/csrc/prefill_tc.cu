@@ -310,10 +310,7 @@ __device__ __noinline__ bool item_epilogue(const Params &p, const Item &E, uint3
                     for (int c0 = 64 * part; c0 < 64 * part + 64; c0 += 8) {
                         float v[8];
                         tc::tmem_ld8(lanebase + c0, v);
-                        if (valid) {
-                            *reinterpret_cast<float4 *>(orow + c0) = make_float4(v[0], v[1], v[2], v[3]);
-                            *reinterpret_cast<float4 *>(orow + c0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
-                        }
+                        if (valid) tc::st_global_v8(orow + c0, v);  // 32-byte aligned
                     }
                 }
             }

@@ -96,6 +96,13 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
     for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// 32-byte global store of eight fp32 values (address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(float *p, const float (&v)[8]) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]),
+                 "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+}
+
 // 16-byte cp.async that writes zeros when `valid` is false (no global read).
 __device__ __forceinline__ void cp_async_16_zfill(void *dst, const void *src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
