@@ -48,6 +48,48 @@ struct TcChunk {
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
+// Chunks of <= cap slots for each active expert, in active order, written by
+// one warp (lanes take active experts in turns of 32; a warp scan gives each
+// expert's first chunk); their number goes to *count.  `offs`: the experts'
+// first sorted slots (E + 1 entries), `active`: the na active experts.
+__device__ inline void warp_plan_chunks(const int32_t *offs, const int32_t *active, int na, int cap,
+                                        TcChunk *chunks, int32_t *count) {
+    const int lane = threadIdx.x & 31;
+    int nc = 0;
+    for (int base = 0; base < na; base += 32) {
+        const int a = base + lane;
+        const int e = a < na ? active[a] : 0;
+        const int n = a < na ? offs[e + 1] - offs[e] : 0;
+        const int mine = (n + cap - 1) / cap;
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        for (int c = 0; c < mine; ++c) {
+            TcChunk ch;
+            ch.e = e;
+            ch.tok_off = c * cap;
+            ch.tok_cnt = min(cap, n - c * cap);
+            ch.pad = 0;
+            chunks[nc + incl - mine + c] = ch;
+        }
+        nc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) *count = nc;
+}
+
+// A chunk plan the permutation launch may write on the way (cap 0: none).
+struct ChunkPlan {
+    int cap = 0;
+    TcChunk *chunks = nullptr;
+    int32_t *count = nullptr;
+};
+
+// Routed slots up to which the permutation runs as one CTA in one launch.
+constexpr int kSmallPermSlots = 4096;
+
 // Tag region of the single-token kernel, right after the header: the router
 // logits, each a word (call tag << 32 | fp32 bits).  Place and size are the
 // same for every shape, so the region never holds anything but tags (or the

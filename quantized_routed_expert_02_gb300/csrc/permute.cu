@@ -8,7 +8,8 @@
 // slot order p = t*k + j, so the grouping is deterministic (no atomics
 // decide positions).
 //
-// Three launches over blocks of kPermSlots consecutive slots:
+// Batches of up to kSmallPermSlots slots take one single-CTA launch (below);
+// larger ones three launches over blocks of kPermSlots consecutive slots:
 //   count    each block's per-expert counts;
 //   scan     per expert, the exclusive prefix of the block counts (in
 //            place), the totals, their exclusive scan (offs) and the list of
@@ -151,10 +152,128 @@ __global__ void __launch_bounds__(kPermSlots) permute_scatter_kernel(
     }
 }
 
+// Up to kSmallPermSlots slots, one CTA of 1024 threads does it all: shared
+// per-expert counts, the scan of the totals (offs, counts, the active list),
+// then the slots in passes of 1024 in slot order: warp ranks among equal
+// experts (__match_any_sync), per-warp counts prefix-summed across the 32
+// warps on top of each expert's running base, positions written.  Stable by
+// construction, so the result equals the multi-launch path's.  Warps 0 and
+// 1 then write the chunk plans asked for.
+constexpr int kSmallPerSlot = kSmallPermSlots / 1024;  // slots per thread
+
+__global__ void __launch_bounds__(1024) permute_small_kernel(
+    const int32_t *__restrict__ idx, int n, int E, int32_t *__restrict__ counts,
+    int32_t *__restrict__ offs, int32_t *__restrict__ perm, int32_t *__restrict__ slotpos,
+    int32_t *__restrict__ active, int32_t *__restrict__ nactive, WsHeader *hdr, ChunkPlan pa,
+    ChunkPlan pb) {
+    pdl_enter();
+    __shared__ int32_t run[kMaxE];          // counts, then each expert's next position
+    __shared__ int32_t s_offs[kMaxE + 1];
+    __shared__ int32_t s_active[kMaxE];
+    __shared__ int32_t s_na;
+    __shared__ int32_t table[32][kMaxE];    // per-warp counts of one pass
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < E; e += 1024) run[e] = 0;
+    __syncthreads();
+    int ev[kSmallPerSlot];
+#pragma unroll
+    for (int i = 0; i < kSmallPerSlot; ++i) {
+        const int p = 1024 * i + tid;
+        ev[i] = p < n ? idx[p] : -1;
+        if (ev[i] >= 0 && ev[i] < E) {
+            atomicAdd(&run[ev[i]], 1);
+        } else if (p < n) {
+            record_status(hdr, MOE_ERR_EXPERT_RANGE, ev[i]);
+            ev[i] = -1;
+        } else {
+            ev[i] = -1;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0, na = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int ee = base + lane;
+            const int v = (ee < E) ? run[ee] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            if (ee < E) {
+                s_offs[ee] = carry + incl - v;
+                offs[ee] = carry + incl - v;
+                counts[ee] = v;
+            }
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+            const bool on = (ee < E) && v > 0;
+            const unsigned m = __ballot_sync(0xffffffffu, on);
+            if (on) {
+                const int a = na + __popc(m & ((1u << lane) - 1u));
+                active[a] = ee;
+                s_active[a] = ee;
+            }
+            na += __popc(m);
+        }
+        if (lane == 0) {
+            s_offs[E] = carry;
+            offs[E] = carry;
+            *nactive = na;
+            s_na = na;
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += 1024) run[e] = s_offs[e];
+    for (int i = 0; i < kSmallPerSlot; ++i) {
+        if (1024 * i >= n) break;  // uniform
+        for (int q = tid; q < 32 * E; q += 1024) table[q / E][q % E] = 0;
+        __syncthreads();
+        const int p = 1024 * i + tid;
+        const int e = ev[i];
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (e >= 0 && rank == 0) table[warp][e] = __popc(peers);
+        __syncthreads();
+        for (int ee = tid; ee < E; ee += 1024) {
+            int r = run[ee];
+            for (int w = 0; w < 32; ++w) {
+                const int c = table[w][ee];
+                table[w][ee] = r;
+                r += c;
+            }
+            run[ee] = r;
+        }
+        __syncthreads();
+        if (e >= 0) {
+            const int pos = table[warp][e] + rank;
+            if (pos >= 0 && pos < n) {
+                perm[pos] = p;
+                slotpos[p] = pos;
+            } else {
+                record_status(hdr, MOE_ERR_INTERNAL, 410000000 + (pos & 0xffffff));
+            }
+        } else if (p < n) {
+            slotpos[p] = -1;  // an invalid expert index: the slot has no sorted row
+        }
+        __syncthreads();  // before the next pass clears the table
+    }
+    if (warp == 0 && pa.cap > 0) warp_plan_chunks(s_offs, s_active, s_na, pa.cap, pa.chunks, pa.count);
+    if (warp == 1 && pb.cap > 0) warp_plan_chunks(s_offs, s_active, s_na, pb.cap, pb.chunks, pb.count);
+}
+
+bool permute_writes_plans(int T, int k) { return int64_t(T) * k <= kSmallPermSlots; }
+
 cudaError_t launch_permute(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offs,
                            int32_t *perm, int32_t *active, int32_t *nactive, int32_t *blockcnt,
-                           int32_t *slotpos, WsHeader *hdr, cudaStream_t s) {
+                           int32_t *slotpos, WsHeader *hdr, cudaStream_t s, const ChunkPlan &pa,
+                           const ChunkPlan &pb) {
     const int n = T * k;
+    if (permute_writes_plans(T, k)) {
+        launch_pdl(permute_small_kernel, dim3(1), dim3(1024), size_t(0), s, idx, n, E, counts, offs,
+                   perm, slotpos, active, nactive, hdr, pa, pb);
+        return cudaGetLastError();
+    }
     const int nb = (n + kPermSlots - 1) / kPermSlots;
     launch_pdl(permute_count_kernel, dim3(nb), dim3(kPermSlots), size_t(0), s, idx, n, E, blockcnt, hdr);
     launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), size_t(0), s, nb, E, blockcnt, counts, offs, active, nactive);

@@ -686,39 +686,14 @@ __global__ void gather_half_kernel(const float *__restrict__ x, const int32_t *_
     }
 }
 
-// Chunks of <= cap slots per active expert, in active order; their number
-// goes to *count.  One warp: lanes take active experts in turns of 32, a warp
-// scan gives each expert's first chunk.
+// The chunk plan as its own launch (batches whose permutation takes several
+// launches): one warp, warp_plan_chunks.
 __global__ void plan_kernel(const int32_t *__restrict__ offs, const int32_t *__restrict__ active,
                             const int32_t *__restrict__ nactive, int cap, TcChunk *chunks,
                             int32_t *count) {
     pdl_enter();
-    const int lane = threadIdx.x & 31;
     if (threadIdx.x >= 32) return;
-    const int na = *nactive;
-    int nc = 0;
-    for (int base = 0; base < na; base += 32) {
-        const int a = base + lane;
-        const int e = a < na ? active[a] : 0;
-        const int n = a < na ? offs[e + 1] - offs[e] : 0;
-        const int mine = (n + cap - 1) / cap;
-        int incl = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += u;
-        }
-        for (int c = 0; c < mine; ++c) {
-            TcChunk ch;
-            ch.e = e;
-            ch.tok_off = c * cap;
-            ch.tok_cnt = min(cap, n - c * cap);
-            ch.pad = 0;
-            chunks[nc + incl - mine + c] = ch;
-        }
-        nc += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) *count = nc;
+    warp_plan_chunks(offs, active, *nactive, cap, chunks, count);
 }
 
 }  // namespace ptc
@@ -786,27 +761,36 @@ bool prefill_tc_supported(int T, int H, int E, int k, int I) {
     return T * k >= kMinTcSlots && I % ptc::kBM == 0 && H % (2 * ptc::kBM) == 0;
 }
 
+// Chunk capacity: no more than the batch's tokens (rounded to 32), so small
+// batches get deep rings; up to 256 slots (two M halves, one accumulator
+// buffer) for gate/up, up to 128 for down, whose large fp32 epilogue then
+// overlaps the next item's MMAs (two accumulator buffers).  A larger expert
+// list (a caller's routing with repeated experts) is split into more chunks.
+void prefill_tc_caps(int T, int *cap_gu, int *cap_dn) {
+    const int tcap = (T + ptc::kBoxRows - 1) / ptc::kBoxRows * ptc::kBoxRows;
+    *cap_gu = std::min(ptc::kBN, tcap);
+    *cap_dn = std::min(ptc::kBM, tcap);
+}
+
 cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, const uint8_t *up,
                               const uint8_t *down, int T, int H, int E, int k, int I,
                               const int32_t *offs, const int32_t *perm, const int32_t *slotpos,
                               const int32_t *active, const int32_t *nactive, __half *x16,
                               __half *h16, float *obuf, TcChunk *chunks, TcChunk *chunks_dn,
-                              WsHeader *hdr,
+                              WsHeader *hdr, bool planned,
                               int num_sms, unsigned long long wait_ns,
                               unsigned long long *timeline, cudaStream_t s) {
     using namespace ptc;
     launch_pdl(gather_half_kernel, dim3(num_sms * 8), dim3(256), size_t(0), s, x, slotpos, T, k, H, x16);
-    // Chunk capacity: no more than the batch's tokens (rounded to 32), so
-    // small batches get deep rings; up to 256 slots (two M halves, one
-    // accumulator buffer) for gate/up, up to 128 for down, whose large fp32
-    // epilogue then overlaps the next item's MMAs (two accumulator buffers).
-    // A larger expert list (a caller's routing with repeated experts) is
-    // split into more chunks.
-    const int tcap = (T + kBoxRows - 1) / kBoxRows * kBoxRows;
-    const int cap_gu = std::min(kBN, tcap), cap_dn = std::min(kBM, tcap);
-    launch_pdl(plan_kernel, dim3(1), dim3(32), size_t(0), s, offs, active, nactive, cap_gu, chunks, &hdr->tc_chunks);
-    if (cap_dn != cap_gu)
-        launch_pdl(plan_kernel, dim3(1), dim3(32), size_t(0), s, offs, active, nactive, cap_dn, chunks_dn, &hdr->tc_chunks_dn);
+    int cap_gu = 0, cap_dn = 0;
+    prefill_tc_caps(T, &cap_gu, &cap_dn);
+    if (!planned) {  // else the permutation launch wrote the plans
+        launch_pdl(plan_kernel, dim3(1), dim3(32), size_t(0), s, offs, active, nactive, cap_gu, chunks,
+                   &hdr->tc_chunks);
+        if (cap_dn != cap_gu)
+            launch_pdl(plan_kernel, dim3(1), dim3(32), size_t(0), s, offs, active, nactive, cap_dn,
+                       chunks_dn, &hdr->tc_chunks_dn);
+    }
     const int rows = T * k;
 
     Params p = {};

@@ -20,13 +20,22 @@ SHAPES = [
 ]
 
 
+def tensor_path_launches(T, k):
+    """Launches of a tensor-core-path call: the router (one launch from 256
+    tokens, two below), the permutation (one launch that also writes the
+    chunk plans up to 4096 routed slots; else three, and the plans are their
+    own launches: two above 128 tokens), fp16 rows, two GEMMs, combine."""
+    router = 1 if T >= 256 else 2
+    if T * k <= 4096:
+        return router + 1 + 1 + 2 + 1
+    return router + 3 + 1 + (2 if T > 128 else 1) + 2 + 1
+
+
 @pytest.mark.parametrize("T,H,E,k,I,std,zipf", SHAPES)
 def test_prefill_shapes(m, T, H, E, k, I, std, zipf):
     shape = synth.custom_shape(T, H, E, k, I, wr_std=std, zipf_bias=zipf,
                                cfg_id=70 + (T + H + E + k + I) % 20)
-    # tensor-core path: router (one launch from 256 tokens), permutation (3),
-    # fp16 rows, chunk plans (two above 128 tokens), two GEMMs, combine
-    assert m.moe_layer_launch_count(T, H, E, k, I) == (10 if T >= 256 else 11)
+    assert m.moe_layer_launch_count(T, H, E, k, I) == tensor_path_launches(T, k)
     case = layer_case(shape, 0, None)   # every token
     idx, w, y, _, _ = run_layer(m, case)
     check_layer(case, idx, w, y)
@@ -51,7 +60,7 @@ def test_caller_routing_beyond_chunk_capacity(m, oracle):
     from tests.cases import y_tolerance
     from tests.test_gpu_parity import DEV, to_dev
     shape = synth.custom_shape(40, 512, 8, 8, 256, cfg_id=91)
-    assert m.moe_layer_launch_count(40, 512, 8, 8, 256) == 10  # tensor-core path, per-token router
+    assert m.moe_layer_launch_count(40, 512, 8, 8, 256) == tensor_path_launches(40, 8)
     case = layer_case(shape, 0, (0, 1, 17, 39))
     rng = np.random.default_rng(91)
     idx_np = rng.integers(0, 2, (40, 8)).astype(np.int32)
