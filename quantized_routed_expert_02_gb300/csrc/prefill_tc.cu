@@ -33,9 +33,10 @@
 //   warp 0      issues tcgen05.mma with the tokens as the M operand:
 //               D[tokens][256 weight rows] (+)= A[128 tokens][16 K] x
 //               B[256 rows][16 K]^T, the activation tile as M = 128 (a second
-//               half for chunks of more than 128 slots) and the stage's gate
-//               and up (or two down) tiles as one N = 256 operand: four
-//               (eight) MMAs per 64-K stage whatever the token count;
+//               half for chunks of more than 128 slots; M = 64 when no chunk
+//               exceeds 64 slots) and the stage's gate and up (or two down)
+//               tiles as one N = 256 operand: four (eight) MMAs per 64-K
+//               stage whatever the token count;
 //               accumulators fp32 in tensor memory, double-buffered for
 //               chunks of <= 128 slots so an item's epilogue overlaps the
 //               next item's MMAs.
@@ -92,6 +93,9 @@ struct Params {
     int nr, r_off;              // raw ring: slots, byte offset (slot = nmat * kRawMat bytes)
     int mh;                     // M halves: 1 (chunks of <= 128 slots, two accumulator
                                 //   buffers) or 2 (<= 256 slots, one buffer of two halves)
+    int mrows;                  // MMA M: 64 when every chunk has <= 64 slots, else 128
+                                //   (M = 64 puts D's rows 16q..16q+15 on TMEM lanes
+                                //   32q..32q+15 of lane quadrant q)
     int ns, s_off;              // stage ring: slots, byte offset (slot = kStageSlot bytes)
     int nb, b_off, b_slot;      // activation ring: slots, byte offset, bytes per slot (the
                                 //   chunk capacity x 128 B; kActSlot - b_slot bytes of
@@ -274,11 +278,12 @@ __device__ __noinline__ bool item_epilogue(const Params &p, const Item &E, uint3
             if (!warp_wait(accfull + buf, use & 1u, deadline, p.hdr, 14)) return false;
             tc::fence_after_sync();
             const int ntok = E.ch.tok_cnt;
+            const int tq = p.mrows / 4;  // tokens per TMEM lane quadrant
             for (int h = 0; h < p.mh; ++h) {
             // warp-uniform: quadrants past the chunk's tokens have no output
-            if (128 * h + 32 * q < ntok) {
-                const int n = 128 * h + 32 * q + lane;
-                const bool valid = n < ntok;
+            if (128 * h + tq * q < ntok) {
+                const int n = 128 * h + tq * q + lane;
+                const bool valid = lane < tq && n < ntok;
                 const uint32_t lanebase = taddr + (buf + uint32_t(h)) * 256u + (uint32_t(q * 32) << 16);
                 if (p.mode == 0) {
                     // h = SiLU(g) * u for rows 32*part .. +31 of the item's 128,
@@ -376,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     // the activation ring (and the padding after it) starts as zeros: the MMA
     // reads 128 rows from a slot's start, and rows no copy has written must
     // hold finite values
-    for (int i = tid; i < (NB * p.b_slot + max(0, kActSlot - p.b_slot)) / 16; i += kThreads)
+    for (int i = tid; i < (NB * p.b_slot + max(0, p.mrows * kBK * 2 - p.b_slot)) / 16; i += kThreads)
         reinterpret_cast<uint4 *>(bring)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();  // before any TMA write into the ring
     if (warp == 0) tc::tmem_alloc(tmem_ptr, tcols);
@@ -510,10 +515,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 break;
             }
             tc::fence_after_sync();
-            // D[128 tokens][256 weight rows] (+)= A[128 tokens][16 K] x B[256 rows][16 K]^T:
+            // D[M tokens][256 weight rows] (+)= A[M tokens][16 K] x B[256 rows][16 K]^T:
             // the activation tile is the M operand, the stage's two 128-row weight
             // tiles (contiguous 8-row swizzle groups) are one N = 256 operand
-            const uint32_t idesc = tc::idesc_f16_f32(kBM, 2 * kBM);
+            const uint32_t idesc = tc::idesc_f16_f32(p.mrows, 2 * kBM);
             const uint32_t d = taddr + buf * 256u;  // half h at d + 256 h (p.mh == 2: buf = 0)
             // the second 128-token half only for chunks that reach into it
             const bool two_halves = __all_sync(0xffffffffu, p.mh == 2 && cur.nmma > kBM);
@@ -796,6 +801,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     Params p = {};
     int cap = cap_gu;
     p.mh = cap > kBM ? 2 : 1;
+    p.mrows = cap <= 64 ? 64 : kBM;
     p.offs = offs;
     p.perm = perm;
     p.chunks = chunks;
@@ -818,13 +824,13 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
         // MMA issued -> complete -> slot free; the raw ring (one block of every
         // row per slot) covers the HBM latency of the weights; the activation
         // ring (slots of the chunk capacity's rows, padded so the MMA's
-        // 128-row read of the last slot stays inside the ring) covers the
+        // M-row read of the last slot stays inside the ring) covers the
         // copies of the activation rows.  Preference: at least 6 activation
         // slots, then the deepest stage ring (4..2), raw ring (3..2) and
         // activation ring (8..2).
         p.r_off = kHead;
         p.b_slot = cap * kBK * 2;
-        const int pad = std::max(0, kActSlot - p.b_slot);
+        const int pad = std::max(0, p.mrows * kBK * 2 - p.b_slot);
         for (int nb_min = 6; nb_min >= 2; nb_min -= 4)
             for (int ns = 4; ns >= 2; --ns)
                 for (int nr = 3; nr >= 2; --nr)
@@ -858,6 +864,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     p.mode = 1;
     cap = cap_dn;
     p.mh = cap > kBM ? 2 : 1;
+    p.mrows = cap <= 64 ? 64 : kBM;
     if (cap_dn != cap_gu) {
         p.chunks = chunks_dn;
         p.nchunks = &hdr->tc_chunks_dn;
