@@ -816,8 +816,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     const int optin = g_tc_smem_optin[dev];
 
     // Shared memory: header, raw ring, weight-tile ring (1024-aligned), then
-    // the activation ring (3 slots of the chunk capacity, 4 for chunks of at
-    // most 64 slots); the raw ring takes what is left, up to kMaxSlots stages.
+    // the activation ring, sized by rings() below.
     auto rings = [&](int nmat) -> size_t {
         (void)nmat;
         // The stage ring (weight tiles) covers the round trip tile ready ->
@@ -825,13 +824,14 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
         // row per slot) covers the HBM latency of the weights; the activation
         // ring (slots of the chunk capacity's rows, padded so the MMA's
         // M-row read of the last slot stays inside the ring) covers the
-        // copies of the activation rows.  Preference: at least 6 activation
-        // slots, then the deepest stage ring (4..2), raw ring (3..2) and
-        // activation ring (8..2).
+        // copies of the activation rows.  Preference, for chunks of at most
+        // 64 slots: at least 4 activation slots, then the deepest stage ring
+        // (4..2), raw ring (3..2) and activation ring (8..2); larger chunks
+        // (and, failing that, small ones) take at least 2 activation slots.
         p.r_off = kHead;
         p.b_slot = cap * kBK * 2;
         const int pad = std::max(0, p.mrows * kBK * 2 - p.b_slot);
-        for (int nb_min = 6; nb_min >= 2; nb_min -= 4)
+        for (int nb_min = cap <= 64 ? 4 : 2; nb_min >= 2; nb_min -= 2)
             for (int ns = 4; ns >= 2; --ns)
                 for (int nr = 3; nr >= 2; --nr)
                     for (int nb = 8; nb >= nb_min; --nb) {
