@@ -112,10 +112,9 @@ moe_status ffn_enqueue(const float *x, const int32_t *idx, const float *w, const
                        cudaStream_t s) {
     const WsLayout &L = ws.L;
     const bool tensor = prefill_tc_supported(T, H, E, k, I);
-    // the tensor-core path's chunk plans, written by a one-launch permutation
+    // the tensor-core path's chunk plans, written by the permutation
     ChunkPlan pa, pb;
-    const bool planned = tensor && permute_writes_plans(T, k);
-    if (planned) {
+    if (tensor) {
         int cap_gu = 0, cap_dn = 0;
         prefill_tc_caps(T, &cap_gu, &cap_dn);
         pa.cap = cap_gu;
@@ -137,7 +136,7 @@ moe_status ffn_enqueue(const float *x, const int32_t *idx, const float *w, const
             ws.i32(L.slotpos), ws.i32(L.active), ws.i32(L.nactive), reinterpret_cast<__half *>(ws.base + L.x16),
             reinterpret_cast<__half *>(ws.base + L.h16), ws.f32(L.o),
             reinterpret_cast<TcChunk *>(ws.base + L.chunks),
-            reinterpret_cast<TcChunk *>(ws.base + L.chunks_dn), ws.hdr(), planned, sms, g_wait_ns,
+            reinterpret_cast<TcChunk *>(ws.base + L.chunks_dn), ws.hdr(), sms, g_wait_ns,
             gemm_timeline(ws), s)));
         return cuda_status(launch_combine(ws.f32(L.o), idx, w, T, H, E, k, y, ep, sms, s));
     }
@@ -245,16 +244,12 @@ int moe_layer_launch_count(int T, int H, int E, int k, int I) {
     if (decode_fused_supported(dev, T, H, E, k, I)) return 1;
     if (decode_stream_supported(dev, T, H, E, k, I)) return 1 /* router */ + 2;
     const int router = (T >= 256 || T <= 2) ? 1 : 2;
-    // one launch up to kSmallPermSlots routed slots (it also writes the chunk
-    // plans), else count, scan, scatter
-    const bool small = permute_writes_plans(T, k);
-    const int permutation = small ? 1 : 3;
+    // one launch up to kSmallPermSlots routed slots, else count, scan,
+    // scatter (the permutation also writes the GEMMs' chunk plans)
+    const int permutation = int64_t(T) * k <= kSmallPermSlots ? 1 : 3;
     if (prefill_tc_supported(T, H, E, k, I)) {
-        // fp16 rows, the chunk plans when the permutation did not write them
-        // (a second one for the down GEMM's 128-slot chunks above 128
-        // tokens), GEMMs, combine
-        const int plans = small ? 0 : (T > 128 ? 2 : 1);
-        return router + permutation + 1 + plans + 2 + 1;
+        // fp16 rows, GEMMs, combine
+        return router + permutation + 1 + 2 + 1;
     }
     return router + permutation + 3 /* gate/up, down, combine */;
 }

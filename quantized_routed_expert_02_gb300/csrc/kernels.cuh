@@ -20,9 +20,8 @@ cudaError_t launch_router(const float *x, const float *Wr, const float *bias, in
 // Three launches (count, scan, scatter); blockcnt holds ceil(T*k / kPermSlots)
 // x E ints of scratch, slotpos receives each slot's sorted position.
 // Up to kSmallPermSlots routed slots the permutation is one launch of one
-// CTA, which also writes the chunk plans `pa` / `pb` when their cap is
-// non-zero (permute_writes_plans); above, three launches and no plans.
-bool permute_writes_plans(int T, int k);
+// CTA, above that three launches; either way the chunk plans `pa` / `pb` are
+// written on the way when their cap is non-zero.
 cudaError_t launch_permute(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offs,
                            int32_t *perm, int32_t *active, int32_t *nactive, int32_t *blockcnt,
                            int32_t *slotpos, WsHeader *hdr, cudaStream_t s,
@@ -48,14 +47,13 @@ cudaError_t init_prefill_tc(int dev);
 bool prefill_tc_supported(int T, int H, int E, int k, int I);
 // The chunk capacities of the gate/up and down GEMMs for a batch of T tokens.
 void prefill_tc_caps(int T, int *cap_gu, int *cap_dn);
-// `planned`: the chunk plans are already written (by the permutation launch).
+// The chunk plans (`chunks`, `chunks_dn`) are written by the permutation.
 cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, const uint8_t *up,
                               const uint8_t *down, int T, int H, int E, int k, int I,
                               const int32_t *offs, const int32_t *perm, const int32_t *slotpos,
                               const int32_t *active,
                               const int32_t *nactive, __half *x16, __half *h16, float *obuf,
-                              TcChunk *chunks, TcChunk *chunks_dn, WsHeader *hdr, bool planned,
-                              int num_sms, unsigned long long wait_ns, unsigned long long *timeline,
+                              TcChunk *chunks, TcChunk *chunks_dn, WsHeader *hdr, int num_sms, unsigned long long wait_ns, unsigned long long *timeline,
                               cudaStream_t s);
 
 cudaError_t init_decode_fused(int dev, int num_sms);

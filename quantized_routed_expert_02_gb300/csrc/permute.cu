@@ -9,7 +9,9 @@
 // decide positions).
 //
 // Batches of up to kSmallPermSlots slots take one single-CTA launch (below);
-// larger ones three launches over blocks of kPermSlots consecutive slots:
+// larger ones three launches over blocks of kPermSlots consecutive slots
+// (either way the launch that knows the expert offsets also writes the
+// grouped GEMMs' chunk plans when asked):
 //   count    each block's per-expert counts;
 //   scan     per expert, the exclusive prefix of the block counts (in
 //            place), the totals, their exclusive scan (offs) and the list of
@@ -54,16 +56,21 @@ __global__ void __launch_bounds__(kPermSlots) permute_count_kernel(const int32_t
 // One CTA of 1024 threads.  The block counts pass through shared memory 32
 // blocks at a time (coalesced loads and stores); thread e keeps expert e's
 // running total and rewrites its column of the tile as exclusive prefixes.
-// Then warp 0 scans the expert totals.
+// Then warp 0 scans the expert totals, and warps 0 and 1 write the chunk
+// plans asked for.
 __global__ void __launch_bounds__(1024) permute_scan_kernel(int nblocks, int E,
                                                             int32_t *__restrict__ blockcnt,
                                                             int32_t *__restrict__ counts,
                                                             int32_t *__restrict__ offs,
                                                             int32_t *__restrict__ active,
-                                                            int32_t *__restrict__ nactive) {
+                                                            int32_t *__restrict__ nactive,
+                                                            ChunkPlan pa, ChunkPlan pb) {
     pdl_enter();
     __shared__ int32_t tile[32][kMaxE + 1];
     __shared__ int32_t tot[kMaxE];
+    __shared__ int32_t s_offs[kMaxE + 1];
+    __shared__ int32_t s_active[kMaxE];
+    __shared__ int32_t s_na;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int run = 0;  // thread e < E: slots of expert e in the blocks so far
     for (int b0 = 0; b0 < nblocks; b0 += 32) {
@@ -97,20 +104,30 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int nblocks, int E,
             }
             if (ee < E) {
                 offs[ee] = carry + incl - v;
+                s_offs[ee] = carry + incl - v;
                 counts[ee] = v;
             }
             carry += __shfl_sync(0xffffffffu, incl, 31);
             // active experts in ascending order
             const bool on = (ee < E) && v > 0;
             const unsigned m = __ballot_sync(0xffffffffu, on);
-            if (on) active[na + __popc(m & ((1u << lane) - 1u))] = ee;
+            if (on) {
+                const int a = na + __popc(m & ((1u << lane) - 1u));
+                active[a] = ee;
+                s_active[a] = ee;
+            }
             na += __popc(m);
         }
         if (lane == 0) {
             offs[E] = carry;
+            s_offs[E] = carry;
             *nactive = na;
+            s_na = na;
         }
     }
+    __syncthreads();
+    if (warp == 0 && pa.cap > 0) warp_plan_chunks(s_offs, s_active, s_na, pa.cap, pa.chunks, pa.count);
+    if (warp == 1 && pb.cap > 0) warp_plan_chunks(s_offs, s_active, s_na, pb.cap, pb.chunks, pb.count);
 }
 
 __global__ void __launch_bounds__(kPermSlots) permute_scatter_kernel(
@@ -262,21 +279,20 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(
     if (warp == 1 && pb.cap > 0) warp_plan_chunks(s_offs, s_active, s_na, pb.cap, pb.chunks, pb.count);
 }
 
-bool permute_writes_plans(int T, int k) { return int64_t(T) * k <= kSmallPermSlots; }
-
 cudaError_t launch_permute(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offs,
                            int32_t *perm, int32_t *active, int32_t *nactive, int32_t *blockcnt,
                            int32_t *slotpos, WsHeader *hdr, cudaStream_t s, const ChunkPlan &pa,
                            const ChunkPlan &pb) {
     const int n = T * k;
-    if (permute_writes_plans(T, k)) {
+    if (n <= kSmallPermSlots) {
         launch_pdl(permute_small_kernel, dim3(1), dim3(1024), size_t(0), s, idx, n, E, counts, offs,
                    perm, slotpos, active, nactive, hdr, pa, pb);
         return cudaGetLastError();
     }
     const int nb = (n + kPermSlots - 1) / kPermSlots;
     launch_pdl(permute_count_kernel, dim3(nb), dim3(kPermSlots), size_t(0), s, idx, n, E, blockcnt, hdr);
-    launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), size_t(0), s, nb, E, blockcnt, counts, offs, active, nactive);
+    launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), size_t(0), s, nb, E, blockcnt, counts, offs,
+               active, nactive, pa, pb);
     launch_pdl(permute_scatter_kernel, dim3(nb), dim3(kPermSlots), size_t(0), s, idx, n, E, blockcnt, offs, perm, slotpos, hdr);
     return cudaGetLastError();
 }

@@ -710,16 +710,6 @@ __global__ void gather_half_kernel(const float *__restrict__ x, const int32_t *_
     }
 }
 
-// The chunk plan as its own launch (batches whose permutation takes several
-// launches): one warp, warp_plan_chunks.
-__global__ void plan_kernel(const int32_t *__restrict__ offs, const int32_t *__restrict__ active,
-                            const int32_t *__restrict__ nactive, int cap, TcChunk *chunks,
-                            int32_t *count) {
-    pdl_enter();
-    if (threadIdx.x >= 32) return;
-    warp_plan_chunks(offs, active, *nactive, cap, chunks, count);
-}
-
 }  // namespace ptc
 
 namespace {
@@ -801,20 +791,13 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
                               const int32_t *offs, const int32_t *perm, const int32_t *slotpos,
                               const int32_t *active, const int32_t *nactive, __half *x16,
                               __half *h16, float *obuf, TcChunk *chunks, TcChunk *chunks_dn,
-                              WsHeader *hdr, bool planned,
+                              WsHeader *hdr,
                               int num_sms, unsigned long long wait_ns,
                               unsigned long long *timeline, cudaStream_t s) {
     using namespace ptc;
     launch_pdl(gather_half_kernel, dim3(num_sms * 8), dim3(256), size_t(0), s, x, slotpos, T, k, H, x16);
-    int cap_gu = 0, cap_dn = 0;
+    int cap_gu = 0, cap_dn = 0;  // the plans for these capacities came with the permutation
     prefill_tc_caps(T, &cap_gu, &cap_dn);
-    if (!planned) {  // else the permutation launch wrote the plans
-        launch_pdl(plan_kernel, dim3(1), dim3(32), size_t(0), s, offs, active, nactive, cap_gu, chunks,
-                   &hdr->tc_chunks);
-        if (cap_dn != cap_gu)
-            launch_pdl(plan_kernel, dim3(1), dim3(32), size_t(0), s, offs, active, nactive, cap_dn,
-                       chunks_dn, &hdr->tc_chunks_dn);
-    }
     const int rows = T * k;
 
     Params p = {};

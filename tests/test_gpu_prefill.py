@@ -22,13 +22,10 @@ SHAPES = [
 
 def tensor_path_launches(T, k):
     """Launches of a tensor-core-path call: the router (one launch from 256
-    tokens, two below), the permutation (one launch that also writes the
-    chunk plans up to 4096 routed slots; else three, and the plans are their
-    own launches: two above 128 tokens), fp16 rows, two GEMMs, combine."""
+    tokens, two below), the permutation with the chunk plans (one launch up
+    to 4096 routed slots, else three), fp16 rows, two GEMMs, combine."""
     router = 1 if T >= 256 else 2
-    if T * k <= 4096:
-        return router + 1 + 1 + 2 + 1
-    return router + 3 + 1 + (2 if T > 128 else 1) + 2 + 1
+    return router + (1 if T * k <= 4096 else 3) + 1 + 2 + 1
 
 
 @pytest.mark.parametrize("T,H,E,k,I,std,zipf", SHAPES)
