@@ -39,6 +39,7 @@ moe_status moeq4k::device_info(int *sms, int *dev_out) {
         if (init_router() != cudaSuccess) return MOE_ERR_CUDA;
         if (init_decode_fused(dev, n) != cudaSuccess) return MOE_ERR_CUDA;
         if (init_prefill_tc(dev) != cudaSuccess) return MOE_ERR_CUDA;
+        if (init_router_tc() != cudaSuccess) return MOE_ERR_CUDA;
         if (init_decode_stream(dev) != cudaSuccess) return MOE_ERR_CUDA;
         g_dev[dev].sms = n;
         g_dev[dev].id = dev;

@@ -270,4 +270,67 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return g / (1.0f + expf(-g)) * u;
 }
 
+// ---------------------------------------------------------------------------
+// Top-k + renormalise by one warp (every router kernel ends here): lane L
+// holds the logits of experts L, L+32, ...; k rounds of a warp-wide arg-max in
+// the order (value descending, index ascending).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+    return v > bv || (v == bv && i < bi);
+}
+
+// Top-k of one token's E logits (read from `lg`, bias already added) by one
+// warp: k rounds of a warp-wide arg-max with the order (value descending,
+// index ascending); writes idx[0..k) and the renormalised weights.
+__device__ __forceinline__ void warp_topk(const float *lg, int E, int k, int32_t *idx, float *w) {
+    constexpr int kPer = kMaxE / 32;
+    const int lane = threadIdx.x & 31;
+    float v[kPer];
+    bool taken[kPer];
+#pragma unroll
+    for (int s = 0; s < kPer; ++s) {
+        int e = lane + 32 * s;
+        v[s] = (e < E) ? lg[e] : -INFINITY;
+        taken[s] = (e >= E);
+    }
+    float sel_v = 0.f;   // lane j keeps slot j's logit
+    int sel_i = 0;
+    float vmax = 0.f;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int s = 0; s < kPer; ++s) {
+            int e = lane + 32 * s;
+            if (!taken[s] && better(v[s], e, bv, bi)) {
+                bv = v[s];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (better(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < kPer; ++s)
+            if (bi == lane + 32 * s) taken[s] = true;
+        if (j == 0) vmax = bv;
+        if (lane == j) {
+            sel_v = bv;
+            sel_i = bi;
+        }
+    }
+    float ex = (lane < k) ? expf(sel_v - vmax) : 0.f;
+    float z = warp_sum(ex);
+    if (lane < k) {
+        idx[lane] = sel_i;
+        w[lane] = ex / z;
+    }
+}
+
 }  // namespace moeq4k

@@ -1,6 +1,8 @@
 // Launch wrappers of the moeq4k kernels (host side).
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace moeq4k {
@@ -45,6 +47,20 @@ cudaError_t launch_rmsnorm(const float *x, const float *gamma, float eps, int T,
 
 cudaError_t init_prefill_tc(int dev);
 bool prefill_tc_supported(int T, int H, int E, int k, int I);
+// A 2-D TMA map of a row-major fp32 matrix [rows][cols] (cols a multiple of
+// 4, base 16-byte aligned): boxes of 32 columns (one 128-byte row) x
+// box_rows rows with the 128-byte swizzle; out-of-range elements read as
+// zero.  Needs init_prefill_tc first.  False on failure.
+bool encode_fp32_sw128_map(CUtensorMap *map, const float *base, int rows, int cols, int box_rows);
+
+// Router logits of T >= 256 tokens (E <= 128, H a multiple of 128) on the
+// tensor cores (three-pass TF32), with the top-k fused.
+bool router_tc_supported(int T, int H, int E);
+cudaError_t init_router_tc();
+cudaError_t launch_router_tc(const float *x, const float *Wr, const float *bias, int T, int H, int E,
+                             int k, int32_t *idx, float *w, WsHeader *hdr,
+                             unsigned long long wait_ns, cudaStream_t s);
+
 // The chunk capacities of the gate/up and down GEMMs for a batch of T tokens.
 void prefill_tc_caps(int T, int *cap_gu, int *cap_dn);
 // The chunk plans (`chunks`, `chunks_dn`) are written by the permutation.

@@ -6,8 +6,6 @@
 // so the top-k of p is the top-k of the logits; after renormalisation the
 // full-softmax denominator cancels and w_j = exp(l_j - l_max) / sum over the
 // selected slots of exp(l - l_max).
-#include <cooperative_groups.h>
-
 #include "async_copy.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
@@ -119,64 +117,6 @@ __global__ void __launch_bounds__(256) router_tile_kernel(const float *__restric
 // L, L+32, ...; k rounds of a warp-wide arg-max with the order (value
 // descending, index ascending).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-    return v > bv || (v == bv && i < bi);
-}
-
-// Top-k of one token's E logits (read from `lg`, bias already added) by one
-// warp: k rounds of a warp-wide arg-max with the order (value descending,
-// index ascending); writes idx[0..k) and the renormalised weights.
-__device__ __forceinline__ void warp_topk(const float *lg, int E, int k, int32_t *idx, float *w) {
-    constexpr int kPer = kMaxE / 32;
-    const int lane = threadIdx.x & 31;
-    float v[kPer];
-    bool taken[kPer];
-#pragma unroll
-    for (int s = 0; s < kPer; ++s) {
-        int e = lane + 32 * s;
-        v[s] = (e < E) ? lg[e] : -INFINITY;
-        taken[s] = (e >= E);
-    }
-    float sel_v = 0.f;   // lane j keeps slot j's logit
-    int sel_i = 0;
-    float vmax = 0.f;
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int s = 0; s < kPer; ++s) {
-            int e = lane + 32 * s;
-            if (!taken[s] && better(v[s], e, bv, bi)) {
-                bv = v[s];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (better(ov, oi, bv, bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-#pragma unroll
-        for (int s = 0; s < kPer; ++s)
-            if (bi == lane + 32 * s) taken[s] = true;
-        if (j == 0) vmax = bv;
-        if (lane == j) {
-            sel_v = bv;
-            sel_i = bi;
-        }
-    }
-    float ex = (lane < k) ? expf(sel_v - vmax) : 0.f;
-    float z = warp_sum(ex);
-    if (lane < k) {
-        idx[lane] = sel_i;
-        w[lane] = ex / z;
-    }
-}
-
 __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restrict__ logits,
                                                           int T, int E, int k,
                                                           int32_t *__restrict__ idx,
@@ -351,136 +291,6 @@ __global__ void __launch_bounds__(256) router_big_kernel(const float *__restrict
     }
 }
 
-// ---------------------------------------------------------------------------
-// Large batches, E <= 128: a cluster of four CTAs per tile of 128 tokens,
-// CTA r of the cluster taking the K quarter [r H/4, (r+1) H/4).  Each CTA
-// streams its x and Wr slices through a 4-stage cp.async ring (32 K per
-// stage, rows padded to 36 floats) and keeps an 8 x 8 register tile per
-// thread (tokens ty + 16 i, experts tx + 16 j: conflict-free shared reads).
-// The per-stage partial of each dot product is summed on its own, then added
-// to the running sum (two-level summation keeps the fp32 rounding of the
-// long dot products small).  The four partial tiles meet through distributed
-// shared memory: CTA r sums, in rank order 0..3, the partials of its 32
-// tokens, adds the bias and runs their top-k.  Fixed summation order, so the
-// logits are deterministic.
-// ---------------------------------------------------------------------------
-namespace {
-constexpr int kST = 128;                 // tokens per cluster tile
-constexpr int kSE = 128;                 // experts (E <= 128)
-constexpr int kSplit = 4;                // K quarters = CTAs per cluster
-constexpr int kSK = 32;                  // K per stage
-constexpr int kSRow = kSK + 4;           // padded shared row (floats)
-constexpr int kSStages = 4;
-constexpr int kStageFloats = (kST + kSE) * kSRow;
-constexpr int kPS = kSE + 4;             // row of the partial tile (floats)
-constexpr int kSplitSmem = int(sizeof(float)) * kSStages * kStageFloats;
-static_assert(kST * kPS + (kST / kSplit) * (kSE + 1) <= kSStages * kStageFloats,
-              "partial and logit tiles reuse the stage ring");
-}  // namespace
-
-__global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(256, 1)
-    router_split_kernel(const float *__restrict__ x, const float *__restrict__ Wr,
-                        const float *__restrict__ bias, int T, int H, int E, int k,
-                        int32_t *__restrict__ idx, float *__restrict__ w) {
-    pdl_enter();
-    extern __shared__ __align__(16) float rsm[];
-    namespace cg = cooperative_groups;
-    cg::cluster_group cl = cg::this_cluster();
-    const int r = int(cl.block_rank());
-    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int t0 = blockIdx.x * kST;
-    const int kq = H / kSplit;
-    const int kbeg = r * kq;
-    const int nst = kq / kSK;
-
-    auto load = [&](int st) {
-        if (st < nst) {
-            float *xs = rsm + (st % kSStages) * kStageFloats, *ws = xs + kST * kSRow;
-            const int k0 = kbeg + st * kSK;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c = tid + 256 * i;
-                const int row = c >> 3, q = c & 7;
-                // rows past T or E repeat the last valid row; their results are dropped
-                const int t = min(t0 + row, T - 1), e = min(row, E - 1);
-                cp_async_16(xs + row * kSRow + 4 * q, x + size_t(t) * H + k0 + 4 * q);
-                cp_async_16(ws + row * kSRow + 4 * q, Wr + size_t(e) * H + k0 + 4 * q);
-            }
-        }
-        cp_async_commit();  // an empty group past the end keeps the count uniform
-    };
-
-    float acc[8][8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-    for (int st = 0; st < kSStages - 1; ++st) load(st);
-    for (int st = 0; st < nst; ++st) {
-        cp_async_wait_pending(kSStages - 2);  // stage st has landed (this thread's copies)
-        __syncthreads();                      // everyone's copies; the refilled slot is free
-        load(st + kSStages - 1);
-        const float *xs = rsm + (st % kSStages) * kStageFloats, *ws = xs + kST * kSRow;
-        float part[8][8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) part[i][j] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < kSK; kk += 4) {
-            float4 a[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a[i] = *reinterpret_cast<const float4 *>(xs + (ty + 16 * i) * kSRow + kk);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 b = *reinterpret_cast<const float4 *>(ws + (tx + 16 * j) * kSRow + kk);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    part[i][j] = fmaf(a[i].x, b.x, part[i][j]);
-                    part[i][j] = fmaf(a[i].y, b.y, part[i][j]);
-                    part[i][j] = fmaf(a[i].z, b.z, part[i][j]);
-                    part[i][j] = fmaf(a[i].w, b.w, part[i][j]);
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] += part[i][j];
-    }
-    cp_async_wait_all();
-    __syncthreads();  // the stage ring is free: it holds the partial tile now
-
-    float *ptile = rsm;  // [kST][kPS]
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ptile[(ty + 16 * i) * kPS + tx + 16 * j] = acc[i][j];
-    cl.sync();  // every CTA's partial tile is complete
-
-    constexpr int kTok = kST / kSplit;  // tokens reduced by this CTA
-    float *lg = rsm + kST * kPS;        // [kTok][kSE + 1]
-    const float *src[kSplit];
-#pragma unroll
-    for (int q = 0; q < kSplit; ++q) src[q] = cl.map_shared_rank(ptile, q);
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int lt = warp; lt < kTok; lt += 8) {
-        const int tt = r * kTok + lt;
-        for (int e = lane; e < E; e += 32) {
-            float v = src[0][tt * kPS + e];
-#pragma unroll
-            for (int q = 1; q < kSplit; ++q) v += src[q][tt * kPS + e];
-            lg[lt * (kSE + 1) + e] = v + (bias ? bias[e] : 0.f);
-        }
-    }
-    cl.sync();  // no CTA leaves while another reads its partial tile
-
-    for (int lt = warp; lt < kTok; lt += 8) {
-        const int t = t0 + r * kTok + lt;
-        if (t < T) warp_topk(&lg[lt * (kSE + 1)], E, k, idx + size_t(t) * k, w + size_t(t) * k);
-    }
-}
-
 cudaError_t init_router() {
     cudaError_t err = cudaFuncSetAttribute(router_big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kRouterBigSmem);
@@ -488,19 +298,16 @@ cudaError_t init_router() {
     err = cudaFuncSetAttribute(router_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kRouterTileSmemMax);
     if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(router_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSplitSmem);
+    return cudaSuccess;
 }
 
 cudaError_t launch_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
                           int k, int32_t *idx, float *w, float *logits, WsHeader *hdr,
                           cudaStream_t s) {
     dim3 blk(256);
-    if (T >= 256 && E <= kSE && H % (kSplit * kSK) == 0) {
-        dim3 grid((T + kST - 1) / kST, kSplit);
-        launch_pdl(router_split_kernel, dim3(grid), dim3(blk), size_t(kSplitSmem), s, x, Wr, bias, T, H, E, k, idx, w);
-        return cudaGetLastError();
-    }
+    // T >= 256, E <= 128: tensor cores (three-pass TF32, router_tc.cu)
+    if (router_tc_supported(T, H, E))
+        return launch_router_tc(x, Wr, bias, T, H, E, k, idx, w, hdr, 1000000000ull, s);
     if (T >= 256) {
         launch_pdl(router_big_kernel, dim3((T + kRT - 1) / kRT), dim3(blk), size_t(kRouterBigSmem), s, x, Wr, bias, T, H, E, k, idx, w);
         return cudaGetLastError();

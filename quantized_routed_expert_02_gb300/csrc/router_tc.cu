@@ -1,0 +1,290 @@
+// Router logits of large batches on the tensor cores, top-k fused.
+//
+// forward_qwen3_moe_cuda_traced.rs (aprender-serve 0.34.0), doc of
+// forward_qwen3_moe_cuda_traced_with_plan: the router stage is the k
+// post-softmax, renormalised top-k weights of a token; the logits are the
+// fp32 product l = x Wr^T (+ bias).
+//
+// The tensor cores have no fp32 operand type; tf32 keeps 11 of fp32's 24
+// significand bits.  Each operand value v is split as v = hi(v) + lo(v),
+// hi(v) = v with its low 13 significand bits cleared (exactly a tf32
+// value), lo(v) = v - hi(v) (exact in fp32), and
+//     x . w ~= hi(x) . hi(w) + lo(x) . hi(w) + hi(x) . lo(w),
+// which drops lo(x) . lo(w) (below 2^-22 of |x w|) and the tf32 rounding of
+// the lo parts (below 2^-21): a relative error near 2^-20 per product, so a
+// logit's error stays near 1e-6 of the sum of |x_h w_h|, far below the gaps
+// the selection depends on.  Three MMAs per K step, fp32 accumulation in
+// tensor memory.
+//
+// A cluster of four CTAs per tile of 128 tokens, CTA r taking the K quarter
+// r.  Per 32-K stage: TMA brings the x and Wr tiles (128 rows x 128 bytes,
+// 128-byte swizzle); every thread splits its share of the two tiles in place
+// (hi back into the tile, lo into two more tiles: the split is elementwise,
+// so the swizzled layout carries over); thread 0 issues twelve MMAs
+// (M = 128 tokens, N = 128 experts, K = 8 each) and commits; a three-stage
+// ring overlaps the copies, the split and the MMAs.  The four partial tiles
+// meet through distributed shared memory: CTA r adds the quarters in rank
+// order for its 32 tokens, adds the bias and ranks them (one warp per
+// token).  Fixed MMA and reduction order: deterministic.  Every wait is
+// bounded by a global-timer deadline; a timed-out wait records
+// MOE_ERR_TIMEOUT and the cluster writes no routing.
+#include <cooperative_groups.h>
+#include <cuda.h>
+
+#include "async_copy.cuh"
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tcgen05.cuh"
+
+namespace moeq4k {
+namespace rtc {
+
+constexpr int kTM = 128;                  // tokens per cluster tile (MMA M)
+constexpr int kEN = 128;                  // experts (MMA N), E <= 128
+constexpr int kSplit = 4;                 // K quarters = CTAs per cluster
+constexpr int kBK = 32;                   // K per stage: one 128-byte fp32 row
+constexpr int kStages = 5;                // copy ring: the x and Wr tiles of a stage
+constexpr int kTile = kTM * kBK * 4;      // 16 KB
+constexpr int kStage = 2 * kTile;         // x, Wr (hi written back in place)
+constexpr int kLo = 2 * kTile;            // lo(x), lo(Wr) of a stage; two buffers
+constexpr int kHead = 1024;               // barriers and flags
+constexpr int kSmem = 1024 + kHead + kStages * kStage + 2 * kLo;  // + slack to align to 1024
+constexpr int kThreads = 256;
+constexpr int kPS = kEN + 4;              // row of the partial tile (floats)
+constexpr int kTok = kTM / kSplit;        // tokens ranked by each CTA
+static_assert(kTM * kPS * 4 + kTok * (kEN + 1) * 4 <= kStages * kStage,
+              "the partial and logit tiles reuse the copy ring");
+static_assert(kSmem <= 232448, "shared memory of one CTA");
+
+struct Params {
+    CUtensorMap mx, mw;   // x [T][H] and Wr [E][H], fp32, boxes of 32 K x 128 rows
+    const float *bias;
+    int T, H, E, k;
+    int32_t *idx;
+    float *w;
+    WsHeader *hdr;
+    unsigned long long wait_ns;
+};
+
+__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                       uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// hi(v) (low 13 significand bits cleared) and lo(v) = v - hi(v), four at once.
+__device__ __forceinline__ void split4(const float4 v, float4 &hi, float4 &lo) {
+    hi.x = __uint_as_float(__float_as_uint(v.x) & 0xFFFFE000u);
+    hi.y = __uint_as_float(__float_as_uint(v.y) & 0xFFFFE000u);
+    hi.z = __uint_as_float(__float_as_uint(v.z) & 0xFFFFE000u);
+    hi.w = __uint_as_float(__float_as_uint(v.w) & 0xFFFFE000u);
+    lo = make_float4(v.x - hi.x, v.y - hi.y, v.z - hi.z, v.w - hi.w);
+}
+
+__global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
+    router_tc_kernel(const __grid_constant__ Params p) {
+    pdl_enter();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [kStages] a stage's tiles landed
+    uint64_t *done = full + kStages;                      // [kStages] the MMAs reading the slot are complete
+    uint64_t *fin = done + kStages;                       // every MMA complete
+    uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(fin + 1);
+    volatile int *failed = reinterpret_cast<volatile int *>(tmem_ptr + 2);
+    uint8_t *ring = smem + kHead;                   // copy ring
+    uint8_t *lobuf = ring + kStages * kStage;       // two lo buffers
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    const int r = int(cl.block_rank());
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = blockIdx.x * kTM;
+    const int kq = p.H / kSplit, kbeg = r * kq, nst = kq / kBK;
+    const uint64_t deadline = global_timer_ns() + p.wait_ns;
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(full + i, 1);  // the copying thread's arrival + the tiles' bytes
+            mbar_init(done + i, 1);  // the stage's MMAs (commit)
+        }
+        mbar_init(fin, 1);
+        *failed = 0;
+        fence_mbar_init();
+    }
+    // two accumulators of 128 fp32 columns, D[128 tokens][128 experts]: stage
+    // st accumulates into buffer st % 2 from zero, and every warp adds the
+    // finished stage into fp32 registers while the next stage's MMAs run
+    constexpr uint32_t kCols = 2 * kEN;
+    if (warp == 0) tc::tmem_alloc(tmem_ptr, kCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t taddr = *tmem_ptr;
+
+    auto issue = [&](int st) {  // thread 0: stage st's two tiles into slot st % kStages
+        const int slot = st % kStages;
+        uint8_t *dst = ring + slot * kStage;
+        mbar_arrive_expect_tx(full + slot, 2 * kTile);
+        tma_2d(dst, &p.mx, kbeg + st * kBK, t0, full + slot);
+        tma_2d(dst + kTile, &p.mw, kbeg + st * kBK, 0, full + slot);
+    };
+    if (tid == 0)
+        for (int st = 0; st < kStages && st < nst; ++st) issue(st);
+    int issued = kStages < nst ? kStages : nst;
+
+    // this warp's accumulator lanes and columns: quadrant warp % 4, half warp / 4
+    const uint32_t lane_off = (uint32_t((warp & 3) * 32) << 16) + uint32_t((warp >> 2) * 64);
+    float racc[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) racc[j] = 0.f;
+    auto add_stage = [&](int st) {  // stage st's accumulator into racc (its MMAs are complete)
+        const uint32_t lb = taddr + uint32_t(st & 1) * kEN + lane_off;
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 8) {
+            float v[8];
+            tc::tmem_ld8(lb + c0, v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) racc[c0 + j] += v[j];
+        }
+    };
+
+    const uint32_t idesc = tc::idesc_tf32_f32(kTM, kEN);
+    for (int st = 0; st < nst; ++st) {
+        const int slot = st % kStages;
+        const uint32_t ph = uint32_t(st / kStages) & 1u;
+        uint8_t *base = ring + slot * kStage;
+        uint8_t *lo = lobuf + (st & 1) * kLo;  // free: stage st - 2's MMAs were waited for
+        if (!mbar_wait(full + slot, ph, deadline)) *failed = 1;
+        __syncthreads();  // a flag set before the barrier is seen by every thread after it
+        const bool ok = *failed == 0;
+        if (ok) {
+            // hi back into the x and Wr tiles, lo into the stage's lo buffer
+            float4 *t = reinterpret_cast<float4 *>(base);
+            float4 *tl = reinterpret_cast<float4 *>(lo);
+#pragma unroll 4
+            for (int i = tid; i < 2 * kTile / 16; i += kThreads) {
+                float4 hi, lv;
+                split4(t[i], hi, lv);
+                t[i] = hi;
+                tl[i] = lv;
+            }
+            fence_proxy_async_smem();  // generic stores before the MMA's async-proxy reads
+        }
+        __syncthreads();
+        if (tid == 0 && ok) {
+            tc::fence_after_sync();
+            const uint32_t a = smem_addr(base), al = smem_addr(lo);
+            const uint64_t dx = tc::smem_desc_sw128(a), dw = tc::smem_desc_sw128(a + kTile);
+            const uint64_t dxl = tc::smem_desc_sw128(al), dwl = tc::smem_desc_sw128(al + kTile);
+            const uint32_t dacc = taddr + uint32_t(st & 1) * kEN;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 8; ++kk) {  // K = 8 per MMA: 32 bytes (2 in the address field)
+                const uint64_t o = uint64_t(2 * kk);
+                tc::mma_tf32(dacc, dx + o, dw + o, idesc, kk > 0);
+                tc::mma_tf32(dacc, dxl + o, dw + o, idesc, true);
+                tc::mma_tf32(dacc, dx + o, dwl + o, idesc, true);
+            }
+            tc::commit_arrive(done + slot);
+        }
+        if (st >= 1) {
+            // stage st - 1: its MMAs complete -> refill its copy slot (thread 0) and
+            // add its accumulator (every warp)
+            const int ps = (st - 1) % kStages;
+            if (!mbar_wait(done + ps, uint32_t((st - 1) / kStages) & 1u, deadline)) *failed = 1;
+            if (tid == 0 && st + kStages - 1 < nst && *failed == 0) issue(st + kStages - 1);
+            if (st + kStages - 1 < nst) ++issued;  // every thread keeps the same count
+            tc::fence_after_sync();
+            add_stage(st - 1);
+            tc::fence_before_sync();
+        }
+    }
+    // every MMA complete; the last stage's accumulator into racc
+    if (tid == 0) tc::commit_arrive(fin);
+    if (!mbar_wait(fin, 0, deadline)) *failed = 1;
+    // copies still in flight after a time-out must land before the ring is reused
+    if (tid == 0) {
+        const uint64_t limit = global_timer_ns() + p.wait_ns;
+        for (int i = 0; i < kStages && i < issued; ++i) {
+            const int st = issued - 1 - i;
+            mbar_wait(full + st % kStages, uint32_t(st / kStages) & 1u, limit);
+        }
+    }
+    tc::fence_after_sync();
+    if (nst > 0) add_stage(nst - 1);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(taddr, kCols);
+
+    float *ptile = reinterpret_cast<float *>(ring);  // [kTM][kPS]
+    {
+        float *row = ptile + (32 * (warp & 3) + lane) * kPS + (warp >> 2) * 64;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) row[j] = racc[j];
+    }
+    cl.sync();  // every CTA's partial tile and flag are complete
+
+    bool any_failed = false;
+#pragma unroll
+    for (int q = 0; q < kSplit; ++q)
+        any_failed |= *cl.map_shared_rank(const_cast<int *>(failed), q) != 0;
+    float *lg = ptile + kTM * kPS;  // [kTok][kEN + 1]
+    const float *src[kSplit];
+#pragma unroll
+    for (int q = 0; q < kSplit; ++q) src[q] = cl.map_shared_rank(ptile, q);
+    for (int lt = warp; lt < kTok; lt += kThreads / 32) {
+        const int tt = r * kTok + lt;
+        for (int e = lane; e < p.E; e += 32) {
+            float v = src[0][tt * kPS + e];
+#pragma unroll
+            for (int q = 1; q < kSplit; ++q) v += src[q][tt * kPS + e];
+            lg[lt * (kEN + 1) + e] = v + (p.bias ? p.bias[e] : 0.f);
+        }
+    }
+    cl.sync();  // no CTA leaves while another reads its partial tile
+    if (any_failed) {
+        if (tid == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 30 + r);
+        return;
+    }
+    for (int lt = warp; lt < kTok; lt += kThreads / 32) {
+        const int t = t0 + r * kTok + lt;
+        if (t < p.T)
+            warp_topk(&lg[lt * (kEN + 1)], p.E, p.k, p.idx + size_t(t) * p.k,
+                      p.w + size_t(t) * p.k);
+    }
+}
+
+}  // namespace rtc
+
+bool router_tc_supported(int T, int H, int E) {
+    return T >= 256 && E <= rtc::kEN && H % (rtc::kSplit * rtc::kBK) == 0;
+}
+
+cudaError_t init_router_tc() {
+    return cudaFuncSetAttribute(rtc::router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                rtc::kSmem);
+}
+
+cudaError_t launch_router_tc(const float *x, const float *Wr, const float *bias, int T, int H, int E,
+                             int k, int32_t *idx, float *w, WsHeader *hdr,
+                             unsigned long long wait_ns, cudaStream_t s) {
+    using namespace rtc;
+    Params p = {};
+    if (!encode_fp32_sw128_map(&p.mx, x, T, H, kTM) || !encode_fp32_sw128_map(&p.mw, Wr, E, H, kEN))
+        return cudaErrorInvalidValue;
+    p.bias = bias;
+    p.T = T;
+    p.H = H;
+    p.E = E;
+    p.k = k;
+    p.idx = idx;
+    p.w = w;
+    p.hdr = hdr;
+    p.wait_ns = wait_ns;
+    launch_pdl(router_tc_kernel, dim3((T + kTM - 1) / kTM, kSplit), dim3(kThreads), size_t(kSmem), s, p);
+    return cudaGetLastError();
+}
+
+}  // namespace moeq4k

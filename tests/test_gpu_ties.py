@@ -9,7 +9,8 @@ logits stays at least 1e-5 apart (rows of x are redrawn until it does).
 
 Paths: the single-token fused kernel, the one/two-token row router (also in
 front of the streamed single-token launches), the 3..255-token tile router
-and its wide-H variant, the split-K cluster router (T >= 256, E <= 128) and
+and its wide-H variant, the tensor-core cluster router (three-pass TF32,
+T >= 256, E <= 128) and
 the large-E router (T >= 256, E > 128).  Expert indices must match the
 oracle bit for bit, the weights within 1e-6, and y within the tolerance.
 """
@@ -170,9 +171,9 @@ ROUTER_PATHS = [
     (3, 2048, 128, 8),     # tile kernel + per-token top-k
     (64, 2048, 128, 8),    # tile kernel, the batched-decode size
     (5, 8192, 16, 3),      # wide rows: warp-per-row logits kernel + top-k
-    (300, 2048, 128, 8),   # split-K cluster kernel with the top-k fused
+    (300, 2048, 128, 8),   # tensor-core cluster kernel with the top-k fused
     (256, 1024, 256, 8),   # large-E kernel (E > 128) with the top-k fused
-    (260, 512, 64, 1),     # split-K, k = 1: a tie decides the arg-max
+    (260, 512, 64, 1),     # tensor-core kernel, k = 1: a tie decides the arg-max
 ]
 
 
