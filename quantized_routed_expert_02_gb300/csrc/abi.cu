@@ -162,7 +162,7 @@ moe_status layer_enqueue(const float *x, const float *norm_w, float eps, const f
             static_cast<const uint8_t *>(down), H, E, k, I, y, W.u64(L.sync), W.f32(L.h), W.hdr(),
             g_withhold, g_wait_ns, W.u64(L.o), W.timeline_cap(), s));
     }
-    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(), s)));
+    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(), sms, s)));
     if (decode_stream_supported(dev, T, H, E, k, I)) {
         return cuda_status(launch_decode_stream(
             x, idx, w, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
@@ -244,7 +244,7 @@ int moe_layer_launch_count(int T, int H, int E, int k, int I) {
     if (device_info(&sms, &dev) != MOE_OK) return 0;
     if (decode_fused_supported(dev, T, H, E, k, I)) return 1;
     if (decode_stream_supported(dev, T, H, E, k, I)) return 1 /* router */ + 2;
-    const int router = (T >= 256 || T <= 2) ? 1 : 2;
+    const int router = 1;
     // one launch up to kSmallPermSlots routed slots, else count, scan,
     // scatter (the permutation also writes the GEMMs' chunk plans)
     const int permutation = int64_t(T) * k <= kSmallPermSlots ? 1 : 3;
@@ -257,8 +257,7 @@ int moe_layer_launch_count(int T, int H, int E, int k, int I) {
 
 int moe_layer_q8k_launch_count(int T, int H, int E, int k, int I) {
     if (check_shape(T, H, E, k, I) != MOE_OK) return 0;
-    const int router = (T >= 256 || T <= 2) ? 1 : 2;
-    return router + 4;  // quantise x, gate/up, quantise h, down (with the combine)
+    return 1 /* router */ + 4;  // quantise x, gate/up, quantise h, down (with the combine)
 }
 
 void moe_debug_set_wait_limit(unsigned long long ns) { g_wait_ns = ns ? ns : 1000000000ull; }
@@ -290,7 +289,7 @@ moe_status moe_router(const float *x, const float *Wr, const float *bias, int T,
     MOE_TRY(device_info(&sms, nullptr));
     Ws W{static_cast<uint8_t *>(ws), L};
     return cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(),
-                                     static_cast<cudaStream_t>(stream)));
+                                     sms, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_permute(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offs,
@@ -496,7 +495,7 @@ moe_status moe_layer_q8k(const float *x, const float *Wr, const float *bias, con
     MOE_TRY(device_info(&sms, nullptr));
     Ws W{static_cast<uint8_t *>(ws), L};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(), s)));
+    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(), sms, s)));
     return q8k_ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, s);
 }
 

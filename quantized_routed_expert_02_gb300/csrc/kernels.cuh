@@ -16,7 +16,7 @@ moe_status validate_shape(int T, int H, int E, int k, int I);
 cudaError_t init_router();
 // `hdr` carries the one- and two-token router's running CTA count.
 cudaError_t launch_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
-                          int k, int32_t *idx, float *w, float *logits, WsHeader *hdr,
+                          int k, int32_t *idx, float *w, float *logits, WsHeader *hdr, int num_sms,
                           cudaStream_t s);
 
 // Three launches (count, scan, scatter); blockcnt holds ceil(T*k / kPermSlots)
@@ -52,6 +52,8 @@ bool prefill_tc_supported(int T, int H, int E, int k, int I);
 // box_rows rows with the 128-byte swizzle; out-of-range elements read as
 // zero.  Needs init_prefill_tc first.  False on failure.
 bool encode_fp32_sw128_map(CUtensorMap *map, const float *base, int rows, int cols, int box_rows);
+bool encode_fp32_box_map(CUtensorMap *map, const float *base, int rows, int cols, int box_cols,
+                         int box_rows);
 
 // Router logits of T >= 256 tokens (E <= 128, H a multiple of 128) on the
 // tensor cores (three-pass TF32), with the top-k fused.

@@ -761,6 +761,22 @@ bool encode_fp32_sw128_map(CUtensorMap *map, const float *base, int rows, int co
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A row-major fp32 matrix [rows][cols] as a 2-D tensor with boxes of
+// box_cols x box_rows and no swizzle (the box lands as box_rows rows of
+// box_cols floats); rows past the end arrive as zeros.
+bool encode_fp32_box_map(CUtensorMap *map, const float *base, int rows, int cols, int box_cols,
+                         int box_rows) {
+    if (g_encode == nullptr) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(cols) * sizeof(float)};
+    const cuuint32_t box[2] = {cuuint32_t(box_cols), cuuint32_t(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t init_prefill_tc(int dev) {
     int optin = 0;
     cudaError_t err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);

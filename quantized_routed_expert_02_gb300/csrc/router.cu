@@ -6,6 +6,10 @@
 // so the top-k of p is the top-k of the logits; after renormalisation the
 // full-softmax denominator cancels and w_j = exp(l_j - l_max) / sum over the
 // selected slots of exp(l - l_max).
+#include <cooperative_groups.h>
+
+#include <algorithm>
+
 #include "async_copy.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
@@ -13,119 +17,329 @@
 namespace moeq4k {
 
 // ---------------------------------------------------------------------------
-// Logits: one warp per expert row of Wr, a tile of kTT tokens per CTA.  Each
-// lane walks the row in float4 steps, so a warp reads 512 contiguous bytes
-// of Wr and of every x row per step.
+// 3..255 tokens: a cluster of kCS CTAs per tile of TT tokens; CTA r takes
+// expert group r (EG = ceil(E / kCS) consecutive rows of Wr).
+//  - Copies: per K chunk of kKC floats, one TMA box of the group's Wr rows
+//    (requested before the wait on the preceding launch) and one of the
+//    tile's x rows, into a ring of shared-memory slots, every slot requested
+//    at once (rows past E or T arrive as zeros).
+//  - Dots: the eight warps split each chunk's 64 float4 columns, warp v
+//    taking columns 8v..8v+7; lane = (column, expert subset): lane L dots
+//    column 8v + (L & 7) of rows L/8, L/8 + 4, ... of the group with the
+//    column of every token.  Each shared-memory byte is read about once.
+//  - Sums: a reduce-scatter over the eight column lanes (fixed butterfly),
+//    then the eight warps' partials added in warp order, plus the bias.
+//  - Exchange: warp t of every group CTA stores its logits of token t into
+//    the shared memory of CTA t of the cluster and arrives (release, cluster
+//    scope) on that CTA's barrier; CTA t waits for the eight arrivals.
+//  - Ranking: thread e counts the experts that beat expert e in the order
+//    (logit descending, index ascending); ranks below k name the selection
+//    in order, and one warp renormalises.
+// One launch, no logits in global memory, a fixed summation order.  Every
+// wait is bounded; a timed-out wait records MOE_ERR_TIMEOUT and the cluster
+// writes no routing for the tile.
 // ---------------------------------------------------------------------------
-template <int kTT>
-__global__ void __launch_bounds__(256) router_logits_kernel(const float *__restrict__ x,
-                                                            const float *__restrict__ Wr,
-                                                            const float *__restrict__ bias,
-                                                            int T, int H, int E,
-                                                            float *__restrict__ logits) {
-    pdl_enter();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * 8 + warp;
-    const int t0 = blockIdx.y * kTT;
-    if (e >= E) return;
-    const float4 *wr = reinterpret_cast<const float4 *>(Wr + size_t(e) * H);
-    float acc[kTT];
-#pragma unroll
-    for (int i = 0; i < kTT; ++i) acc[i] = 0.f;
-    const int n4 = H >> 2;
-    for (int c = lane; c < n4; c += 32) {
-        float4 a = __ldg(wr + c);
-#pragma unroll
-        for (int i = 0; i < kTT; ++i) {
-            if (t0 + i < T) {
-                float4 b = __ldg(reinterpret_cast<const float4 *>(x + size_t(t0 + i) * H) + c);
-                acc[i] = fmaf(a.x, b.x, acc[i]);
-                acc[i] = fmaf(a.y, b.y, acc[i]);
-                acc[i] = fmaf(a.z, b.z, acc[i]);
-                acc[i] = fmaf(a.w, b.w, acc[i]);
-            }
-        }
-    }
-    const float b = bias ? bias[e] : 0.f;
-#pragma unroll
-    for (int i = 0; i < kTT; ++i) {
-        float s = warp_sum(acc[i]);
-        if (lane == 0 && t0 + i < T) logits[size_t(t0 + i) * E + e] = s + b;
+namespace rcl {
+constexpr int kCS = 8;                // CTAs per cluster: expert groups
+constexpr int kKC = 256;              // K per chunk (floats): one box row of 1 KB
+constexpr int kCols = kKC / 4;        // float4 columns per chunk
+constexpr int kMaxSlots = 16;         // ring slots
+constexpr int kMaxEG = kMaxE / kCS;   // rows of Wr per group (32)
+constexpr int kMaxTT = 8;             // tokens per tile
+constexpr int kFlagOff = 8 * (kMaxSlots + 1);             // after full[], got: failed, flags_in[kCS]
+constexpr int kInboxOff = 256;                            // the ranked token's logits
+constexpr int kRedOff = kInboxOff + kMaxE * 4;            // [8 warps][kMaxEG * kMaxTT]
+constexpr int kSelOff = kRedOff + 8 * kMaxEG * kMaxTT * 4;  // the selection, in rank order
+constexpr int kHead = (kSelOff + 2 * kMaxK * 4 + 1023) / 1024 * 1024;
+constexpr int kRingSolo = 200 * 1024;  // ring bytes when the clusters fit one CTA per SM
+constexpr int kRingPair = 100 * 1024;  // ... and when two CTAs share an SM
+constexpr int kSmemMax = 1024 + kHead + kRingSolo;  // + slack to align the base to 1024
+static_assert(kFlagOff + 4 * (1 + kCS) <= kInboxOff, "barriers and flags");
+static_assert(kSmemMax <= 232448, "shared memory of one CTA");
+
+struct Params {
+    CUtensorMap mx, mw;  // x [T][H], Wr [E][H] fp32; boxes kKC x TT rows, kKC x EG rows
+    const float *bias;
+    int T, H, E, k, nslots;
+    int32_t *idx;
+    float *w;
+    WsHeader *hdr;
+    unsigned long long wait_ns;
+};
+
+__device__ __forceinline__ void tma_box(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Split cluster barrier, executed by every thread of the cluster: the
+// arrive is relaxed (what other CTAs need to see before the wait returns is
+// the mbarrier initialisation, which fence.mbarrier_init publishes at
+// cluster scope); the wait returns once every thread has arrived.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Asynchronous store of one 32-bit word into the shared memory of CTA `rank`
+// of the cluster (at the offset of `dst` here), completing as 4 transaction
+// bytes on that CTA's mbarrier at the offset of `bar`.
+__device__ __forceinline__ void st_async_remote(void *dst, uint32_t v, uint64_t *bar, int rank) {
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(dst)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_addr(bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra),
+                 "r"(v), "r"(rb)
+                 : "memory");
+}
+
+// Bounded wait for a phase completed by other CTAs of the cluster
+// (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t deadline) {
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_addr(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (global_timer_ns() > deadline) return false;
     }
 }
 
-// ---------------------------------------------------------------------------
-// 3..255 tokens: a CTA stages kXT tokens of x in shared memory (coalesced),
-// then each warp takes one expert row of Wr, requests its share of the row
-// in batches of four float4 per lane before any arithmetic, and dots it with
-// the staged tokens (fixed per-lane order, then a warp sum).
-// ---------------------------------------------------------------------------
-constexpr int kXT = 8;  // tokens per CTA
-constexpr int kRouterTileSmemMax = 128 * 1024;  // x tile of up to H = 4096
+// Sum each of the V values of a lane over the eight lanes that share
+// lane / 8 (lane bits 0-2), by a reduce-scatter in a fixed order.  After it,
+// lane L holds the sums of the values V/8 * (L & 7) + i, i < V/8, in a[i]
+// (V >= 8); for V = 4, a[0] holds value (L & 7) / 2.
+template <int V, int N>  // one step: N values per lane -> N / 2 (or a plain butterfly at N = 1)
+__device__ __forceinline__ void fold_step(float (&a)[V], int lane, int o) {
+    if constexpr (N > 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const float send = up ? a[i] : a[i + N / 2];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+            a[i] = (up ? a[i + N / 2] : a[i]) + recv;
+        }
+    } else {
+        a[0] += __shfl_xor_sync(0xffffffffu, a[0], o);
+    }
+}
+template <int V>
+__device__ __forceinline__ void fold8(float (&a)[V], int lane) {
+    static_assert(V >= 4 && (V & (V - 1)) == 0, "a power of two, at least 4");
+    fold_step<V, V>(a, lane, 4);
+    fold_step<V, V / 2>(a, lane, 2);
+    fold_step<V, (V / 4 > 1 ? V / 4 : 1)>(a, lane, 1);
+}
+}  // namespace rcl
 
-__global__ void __launch_bounds__(256) router_tile_kernel(const float *__restrict__ x,
-                                                          const float *__restrict__ Wr,
-                                                          const float *__restrict__ bias, int T,
-                                                          int H, int E, float *__restrict__ logits) {
-    pdl_enter();
-    extern __shared__ __align__(16) float xt[];  // [kXT][H]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t0 = blockIdx.y * kXT, n4 = H >> 2;
-    for (int i = threadIdx.x; i < kXT * n4; i += blockDim.x) {
-        const int tok = i / n4, c = i - tok * n4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (t0 + tok < T) v = __ldg(reinterpret_cast<const float4 *>(x + size_t(t0 + tok) * H) + c);
-        reinterpret_cast<float4 *>(xt)[i] = v;
+template <int TT, int NEL>
+__global__ void __cluster_dims__(rcl::kCS, 1, 1) __launch_bounds__(256)
+    router_cluster_kernel(const __grid_constant__ rcl::Params p) {
+    using namespace rcl;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm);  // [nslots] a chunk's boxes landed
+    uint64_t *got = full + kMaxSlots;                   // the eight groups' logits of my token
+    int *failed = reinterpret_cast<int *>(sm + kFlagOff);  // a wait of this CTA timed out
+    int *flags_in = failed + 1;  // [kCS] group g's flag for my token (1: its waits timed out)
+    float *inbox = reinterpret_cast<float *>(sm + kInboxOff);
+    float *red = reinterpret_cast<float *>(sm + kRedOff);
+    float *sel_v = reinterpret_cast<float *>(sm + kSelOff);
+    int *sel_i = reinterpret_cast<int *>(sel_v + kMaxK);
+    float *ring = reinterpret_cast<float *>(sm + kHead);
+    namespace cg = cooperative_groups;
+    const int r = int(cg::this_cluster().block_rank());
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int EG = (p.E + kCS - 1) / kCS;
+    const int e0 = r * EG;
+    const int ne = max(0, min(EG, p.E - e0));  // rows of this CTA's group
+    const int t0 = blockIdx.y * TT;
+    const int nt = min(TT, p.T - t0);          // tokens of this tile
+    const int rows = EG + TT;                  // rows per ring slot: the Wr box, then the x box
+    const int nch = p.H / kKC;
+    const int nslots = p.nslots;
+    const uint32_t wbytes = ne > 0 ? uint32_t(EG) * kKC * 4u : 0u;
+    const uint32_t chunk_bytes = wbytes + uint32_t(TT) * kKC * 4u;
+    const uint64_t deadline = global_timer_ns() + p.wait_ns;
+    auto slot_of = [&](int c) { return ring + size_t(c % nslots) * rows * kKC; };
+
+    const int npre = min(nslots, nch);
+    if (tid == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.mx)) : "memory");
+        for (int i = 0; i < nslots; ++i) mbar_init(full + i, 1);
+        // my token's logits: E words from the groups and one flag word from each
+        mbar_init(got, 1);
+        *failed = 0;
+        fence_mbar_init();
+        if (r < nt) mbar_arrive_expect_tx(got, uint32_t(p.E + kCS) * 4u);
+        for (int c = 0; c < npre; ++c) {
+            mbar_arrive_expect_tx(full + c, chunk_bytes);
+            if (ne > 0) tma_box(slot_of(c), &p.mw, c * kKC, e0, full + c);
+        }
+    }
+    __syncthreads();   // every slot's byte count is set before any x box can land
+    cluster_arrive();  // this CTA's barriers exist; waited for before the exchange
+    pdl_enter();      // x, idx and w belong to the stream's order from here
+    if (tid == 32)
+        for (int c = 0; c < npre; ++c) tma_box(slot_of(c) + EG * kKC, &p.mx, c * kKC, t0, full + c);
+    int issued = npre;  // chunks requested (thread 0's count)
+
+    float acc[NEL * TT];
+#pragma unroll
+    for (int i = 0; i < NEL * TT; ++i) acc[i] = 0.f;
+    const int q = 8 * warp + (lane & 7);  // this lane's float4 column of a chunk
+    const int g = lane >> 3;              // ... and expert subset: rows g, g + 4, ...
+    for (int c = 0; c < nch; ++c) {
+        const int slot = c % nslots;
+        // after a time-out every later wait returns at once (the deadline has passed)
+        if (!mbar_wait(full + slot, uint32_t(c / nslots) & 1u, deadline)) atomicExch(failed, 1);
+        const float4 *wb = reinterpret_cast<const float4 *>(ring + size_t(slot) * rows * kKC);
+        const float4 *xb = wb + EG * kCols;
+        float4 xv[TT];
+#pragma unroll
+        for (int t = 0; t < TT; ++t) xv[t] = xb[t * kCols + q];
+#pragma unroll
+        for (int m = 0; m < NEL; ++m) {
+            const int el = g + 4 * m;
+            if (el < ne) {
+                const float4 a = wb[el * kCols + q];
+#pragma unroll
+                for (int t = 0; t < TT; ++t) {
+                    float s = acc[m * TT + t];
+                    s = fmaf(a.x, xv[t].x, s);
+                    s = fmaf(a.y, xv[t].y, s);
+                    s = fmaf(a.z, xv[t].z, s);
+                    s = fmaf(a.w, xv[t].w, s);
+                    acc[m * TT + t] = s;
+                }
+            }
+        }
+        if (nch > nslots) {  // the ring wraps: refill this slot once every warp is done with it
+            __syncthreads();
+            if (tid == 0 && c + nslots < nch && *reinterpret_cast<volatile int *>(failed) == 0) {
+                const int cn = c + nslots;
+                mbar_arrive_expect_tx(full + slot, chunk_bytes);
+                if (ne > 0) tma_box(slot_of(cn), &p.mw, cn * kKC, e0, full + slot);
+                tma_box(slot_of(cn) + EG * kKC, &p.mx, cn * kKC, t0, full + slot);
+                ++issued;
+            }
+        }
+    }
+    // fold the column lanes; lane L now holds values V/8 * (L & 7) + i (value
+    // m * TT + t is row g + 4m, token t), or value (L & 7) / 2 when V = 4
+    constexpr int V = NEL * TT;
+    fold8<V>(acc, lane);
+    {
+        float *rw = red + warp * (kMaxEG * kMaxTT);  // [EG * TT] of this warp, row-major (row, token)
+        if constexpr (V >= 8) {
+#pragma unroll
+            for (int i = 0; i < V / 8; ++i) {
+                const int v = (V / 8) * (lane & 7) + i, m = v / TT, t = v - m * TT;
+                const int el = g + 4 * m;
+                if (el < EG) rw[el * TT + t] = acc[i];
+            }
+        } else if ((lane & 1) == 0) {
+            const int v = (lane & 7) >> 1, m = v / TT, t = v - m * TT;
+            const int el = g + 4 * m;
+            if (el < EG) rw[el * TT + t] = acc[0];
+        }
     }
     __syncthreads();
-    const int e = blockIdx.x * 8 + warp;
-    if (e >= E) return;
-    const float4 *wr = reinterpret_cast<const float4 *>(Wr + size_t(e) * H);
-    const float4 *x4 = reinterpret_cast<const float4 *>(xt);
-    float acc[kXT];
-#pragma unroll
-    for (int t = 0; t < kXT; ++t) acc[t] = 0.f;
-    for (int c0 = lane; c0 < n4; c0 += 4 * 32) {
-        float4 a[4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-            if (c0 + 32 * b < n4) a[b] = __ldg(wr + c0 + 32 * b);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int c = c0 + 32 * b;
-            if (c >= n4) break;
-#pragma unroll
-            for (int t = 0; t < kXT; ++t) {
-                const float4 v = x4[t * n4 + c];
-                acc[t] = fmaf(a[b].x, v.x, acc[t]);
-                acc[t] = fmaf(a[b].y, v.y, acc[t]);
-                acc[t] = fmaf(a[b].z, v.z, acc[t]);
-                acc[t] = fmaf(a[b].w, v.w, acc[t]);
-            }
+    const bool bad = *reinterpret_cast<volatile int *>(failed) != 0;
+    if (bad && tid == 0) {
+        // copies still in flight land before the CTA's shared memory is released:
+        // the latest phase of every slot
+        const uint64_t limit = global_timer_ns() + p.wait_ns;
+        for (int i = 0; i < nslots && i < issued; ++i) {
+            const int cc = issued - 1 - i;
+            mbar_wait(full + cc % nslots, uint32_t(cc / nslots) & 1u, limit);
         }
     }
-    const float b = bias ? bias[e] : 0.f;
+    cluster_wait();  // every CTA's barriers are initialised
+    namespace cgx = cooperative_groups;
+    cgx::cluster_group cl = cgx::this_cluster();
+    // warp t sends token t's logits of this group, and this group's flag, to CTA t
+    if (warp < nt) {
+        const int t = warp;
+        for (int el = lane; el < ne; el += 32) {
+            float sum = 0.f;
 #pragma unroll
-    for (int t = 0; t < kXT; ++t) {
-        const float sum = warp_sum(acc[t]);
-        if (lane == 0 && t0 + t < T) logits[size_t(t0 + t) * E + e] = sum + b;
+            for (int v = 0; v < 8; ++v) sum += red[v * (kMaxEG * kMaxTT) + el * TT + t];
+            sum += p.bias ? p.bias[e0 + el] : 0.f;
+            st_async_remote(inbox + e0 + el, __float_as_uint(sum), got, t);
+        }
+        if (lane == 0) st_async_remote(flags_in + r, bad ? 1u : 0u, got, t);
     }
-}
-
-// ---------------------------------------------------------------------------
-// Top-k + renormalise: one warp per token.  Lane L holds logits of experts
-// L, L+32, ...; k rounds of a warp-wide arg-max with the order (value
-// descending, index ascending).
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) router_topk_kernel(const float *__restrict__ logits,
-                                                          int T, int E, int k,
-                                                          int32_t *__restrict__ idx,
-                                                          float *__restrict__ w) {
-    pdl_enter();
-    const int warp = threadIdx.x >> 5;
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= T) return;
-    warp_topk(logits + size_t(t) * E, E, k, idx + size_t(t) * k, w + size_t(t) * k);
+    if (r >= nt) return;  // no token of this tile is ranked here; nothing is sent to this CTA
+    // CTA r ranks token t0 + r once the eight groups' logits are in
+    if (!mbar_wait_cluster(got, 0u, deadline + p.wait_ns)) {
+        if (tid == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 41);
+        return;
+    }
+    bool any_failed = false;
+#pragma unroll
+    for (int g2 = 0; g2 < kCS; ++g2) any_failed |= flags_in[g2] != 0;
+    if (any_failed) {
+        if (tid == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 40);
+        return;
+    }
+    const int E = p.E, k = p.k;
+    const int E4 = (E + 3) & ~3;
+    // a NaN logit ranks as -inf (the order is then total and every rank
+    // unique); pads past E lose every comparison
+    if (tid < E4) {
+        const float v = tid < E ? inbox[tid] : -INFINITY;
+        inbox[tid] = v != v ? -INFINITY : v;
+    }
+    __syncthreads();
+    {
+        // rank of expert e in the order (logit descending, index ascending): the
+        // experts that beat it, counted by two threads (halves of the list) for
+        // E <= 128, else by one
+        const bool pair = E <= 128;
+        const int e = pair ? tid >> 1 : tid;
+        const int nq = E4 / 4, half = pair ? (nq + 1) / 2 : nq;
+        const int q0 = pair && (tid & 1) ? half : 0, q1 = pair && !(tid & 1) ? half : nq;
+        const float v = e < E ? inbox[e] : 0.f;
+        int rank = 0;
+        const float4 *in4 = reinterpret_cast<const float4 *>(inbox);
+#pragma unroll 4
+        for (int j4 = q0; j4 < q1; ++j4) {
+            const float4 u = in4[j4];
+            const int j = 4 * j4;
+            rank += (u.x > v || (u.x == v && j < e)) ? 1 : 0;
+            rank += (u.y > v || (u.y == v && j + 1 < e)) ? 1 : 0;
+            rank += (u.z > v || (u.z == v && j + 2 < e)) ? 1 : 0;
+            rank += (u.w > v || (u.w == v && j + 3 < e)) ? 1 : 0;
+        }
+        if (pair) rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+        if (e < E && rank < k && (!pair || (tid & 1) == 0)) {
+            sel_v[rank] = v;
+            sel_i[rank] = e;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int t = t0 + r;
+        const float vmax = sel_v[0];
+        const float ex = lane < k ? expf(sel_v[lane] - vmax) : 0.f;
+        const float z = warp_sum(ex);
+        if (lane < k) {
+            p.idx[size_t(t) * k + lane] = sel_i[lane];
+            p.w[size_t(t) * k + lane] = ex / z;
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -295,14 +509,41 @@ cudaError_t init_router() {
     cudaError_t err = cudaFuncSetAttribute(router_big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kRouterBigSmem);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(router_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kRouterTileSmemMax);
-    if (err != cudaSuccess) return err;
+    for (void *fn : {(void *)router_cluster_kernel<1, 4>, (void *)router_cluster_kernel<2, 4>,
+                     (void *)router_cluster_kernel<4, 4>, (void *)router_cluster_kernel<8, 4>,
+                     (void *)router_cluster_kernel<1, 8>, (void *)router_cluster_kernel<2, 8>,
+                     (void *)router_cluster_kernel<4, 8>, (void *)router_cluster_kernel<8, 8>}) {
+        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, rcl::kSmemMax);
+        if (err != cudaSuccess) return err;
+    }
     return cudaSuccess;
 }
 
+// Tokens per cluster tile for 3..255 tokens: the largest of 8, 4, 2 that
+// still gives at least 8 tiles (64 CTAs), else 1.  More tokens per tile
+// means fewer reads of every group's Wr rows; on one SM the bytes arrive at
+// a few tens of GB/s, so the tile stays small enough to spread over 64 SMs
+// or more (measured at 64 tokens: 8 tiles of 8 beat 16 tiles of 4 by 3 %
+// of the layer call, at 32 A22B tokens by 1.5 %).
+int router_tile_tokens(int T) {
+    for (int tt = 8; tt > 1; tt >>= 1)
+        if ((T + tt - 1) / tt >= 8) return tt;
+    return 1;
+}
+
+template <int NEL>
+static void launch_cluster(int tt, dim3 grid, size_t smem, cudaStream_t s, const rcl::Params &p) {
+    const dim3 blk(256);
+    switch (tt) {
+        case 8: launch_pdl(router_cluster_kernel<8, NEL>, grid, blk, smem, s, p); break;
+        case 4: launch_pdl(router_cluster_kernel<4, NEL>, grid, blk, smem, s, p); break;
+        case 2: launch_pdl(router_cluster_kernel<2, NEL>, grid, blk, smem, s, p); break;
+        default: launch_pdl(router_cluster_kernel<1, NEL>, grid, blk, smem, s, p); break;
+    }
+}
+
 cudaError_t launch_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
-                          int k, int32_t *idx, float *w, float *logits, WsHeader *hdr,
+                          int k, int32_t *idx, float *w, float *logits, WsHeader *hdr, int num_sms,
                           cudaStream_t s) {
     dim3 blk(256);
     // T >= 256, E <= 128: tensor cores (three-pass TF32, router_tc.cu)
@@ -316,14 +557,33 @@ cudaError_t launch_router(const float *x, const float *Wr, const float *bias, in
         launch_pdl(router_row_kernel<2>, dim3(E), dim3(blk), size_t(0), s, x, Wr, bias, T, H, E, k, logits, idx, w, hdr);
         return cudaGetLastError();
     }
-    if (size_t(kXT) * H * sizeof(float) <= size_t(kRouterTileSmemMax)) {
-        dim3 grid((E + 7) / 8, (T + kXT - 1) / kXT);
-        launch_pdl(router_tile_kernel, dim3(grid), dim3(blk), size_t(size_t(kXT) * H * sizeof(float)), s, x, Wr, bias, T, H, E, logits);
-    } else {
-        dim3 grid((E + 7) / 8, (T + 7) / 8);
-        launch_pdl(router_logits_kernel<8>, dim3(grid), dim3(blk), size_t(0), s, x, Wr, bias, T, H, E, logits);
-    }
-    launch_pdl(router_topk_kernel, dim3((T + 7) / 8), dim3(blk), size_t(0), s, logits, T, E, k, idx, w);
+    using namespace rcl;
+    const int tt = router_tile_tokens(T);
+    const int tiles = (T + tt - 1) / tt;
+    const int EG = (E + kCS - 1) / kCS;
+    const int slot_bytes = (EG + tt) * kKC * 4;
+    const int budget = tiles * kCS <= num_sms ? kRingSolo : kRingPair;
+    const int nslots = std::min({H / kKC, kMaxSlots, budget / slot_bytes});
+    if (nslots < 1) return cudaErrorInvalidValue;
+    Params p = {};
+    if (!encode_fp32_box_map(&p.mx, x, T, H, kKC, tt) || !encode_fp32_box_map(&p.mw, Wr, E, H, kKC, EG))
+        return cudaErrorInvalidValue;
+    p.bias = bias;
+    p.T = T;
+    p.H = H;
+    p.E = E;
+    p.k = k;
+    p.nslots = nslots;
+    p.idx = idx;
+    p.w = w;
+    p.hdr = hdr;
+    p.wait_ns = 1000000000ull;
+    const size_t smem = size_t(1024 + kHead) + size_t(nslots) * slot_bytes;
+    const dim3 grid(kCS, tiles);
+    if (EG <= 16)
+        launch_cluster<4>(tt, grid, smem, s, p);
+    else
+        launch_cluster<8>(tt, grid, smem, s, p);
     return cudaGetLastError();
 }
 

@@ -21,11 +21,11 @@ SHAPES = [
 
 
 def tensor_path_launches(T, k):
-    """Launches of a tensor-core-path call: the router (one launch from 256
-    tokens, two below), the permutation with the chunk plans (one launch up
-    to 4096 routed slots, else three), fp16 rows, two GEMMs, combine."""
-    router = 1 if T >= 256 else 2
-    return router + (1 if T * k <= 4096 else 3) + 1 + 2 + 1
+    """Launches of a tensor-core-path call: the router (one launch, top-k
+    fused, at every batch size), the permutation with the chunk plans (one
+    launch up to 4096 routed slots, else three), fp16 rows, two GEMMs,
+    combine."""
+    return 1 + (1 if T * k <= 4096 else 3) + 1 + 2 + 1
 
 
 @pytest.mark.parametrize("T,H,E,k,I,std,zipf", SHAPES)

@@ -8,10 +8,10 @@ sides and only the index rule can decide it.  Every other pair of the top
 logits stays at least 1e-5 apart (rows of x are redrawn until it does).
 
 Paths: the single-token fused kernel, the one/two-token row router (also in
-front of the streamed single-token launches), the 3..255-token tile router
-and its wide-H variant, the tensor-core cluster router (three-pass TF32,
-T >= 256, E <= 128) and
-the large-E router (T >= 256, E > 128).  Expert indices must match the
+front of the streamed single-token launches), the 3..255-token cluster
+router (1, 2, 4 or 8 tokens per cluster tile), the tensor-core cluster
+router (three-pass TF32, T >= 256, E <= 128) and the large-E router
+(T >= 256, E > 128).  Expert indices must match the
 oracle bit for bit, the weights within 1e-6, and y within the tolerance.
 """
 import numpy as np
@@ -168,9 +168,11 @@ ROUTER_PATHS = [
     # T, H, E, k: which router kernel
     (1, 2048, 128, 8),     # one/two-token row kernel (top-k in its last CTA)
     (2, 2048, 128, 7),     # the same with two tokens, odd k
-    (3, 2048, 128, 8),     # tile kernel + per-token top-k
-    (64, 2048, 128, 8),    # tile kernel, the batched-decode size
-    (5, 8192, 16, 3),      # wide rows: warp-per-row logits kernel + top-k
+    (3, 2048, 128, 8),     # cluster router, one token per tile
+    (32, 4096, 128, 8),    # two tokens per tile, 16 K chunks through an 11-slot ring
+    (64, 2048, 128, 8),    # four tokens per tile, the batched-decode size
+    (5, 8192, 16, 3),      # two experts per group, 32 K chunks through a 16-slot ring
+    (200, 1024, 256, 8),   # eight tokens per tile, four experts per warp, two CTAs per SM
     (300, 2048, 128, 8),   # tensor-core cluster kernel with the top-k fused
     (256, 1024, 256, 8),   # large-E kernel (E > 128) with the top-k fused
     (260, 512, 64, 1),     # tensor-core kernel, k = 1: a tie decides the arg-max
