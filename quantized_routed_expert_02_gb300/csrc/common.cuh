@@ -271,66 +271,96 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 }
 
 // ---------------------------------------------------------------------------
-// Top-k + renormalise by one warp (every router kernel ends here): lane L
-// holds the logits of experts L, L+32, ...; k rounds of a warp-wide arg-max in
-// the order (value descending, index ascending).
+// Top-k + renormalise by one warp (the routers end here).  The order is
+// (logit descending, expert index ascending).  Each lane holds the logits
+// of experts lane, lane + 32, ... as order-preserving integer keys, sorted
+// once by that order; each of the k rounds takes the largest key over the
+// warp and then the smallest expert index among the lanes showing it (two
+// warp reductions), and the winning lane drops its head.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-    return v > bv || (v == bv && i < bi);
+// Key of a logit: larger logits give larger keys, -0 the key of +0 (they
+// compare equal), NaN the key 0 (below -inf: a NaN is taken only after
+// every number).  logit_of_key inverts it (NaN -> a NaN).
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    if (v != v) return 0u;
+    uint32_t u = __float_as_uint(v);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float logit_of_key(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
-// Top-k of one token's E logits (read from `lg`, bias already added) by one
-// warp: k rounds of a warp-wide arg-max with the order (value descending,
-// index ascending); writes idx[0..k) and the renormalised weights.
+// (key, index) a comes first: larger key, or equal key and smaller index
+__device__ __forceinline__ bool topk_first(uint32_t ka, uint32_t ia, uint32_t kb, uint32_t ib) {
+    return ka > kb || (ka == kb && ia < ib);
+}
+
+// Top-k of one token's E <= 32 * kPer logits (bias already added) by one
+// warp, lane L holding the logits of experts L + 32 s in v[s]; writes
+// idx[0..k) in selection order and the renormalised weights
+// w_j = exp(l_j - l_max) / sum over the selection of exp(l - l_max).
+template <int kPer>
+__device__ __forceinline__ void warp_topk_regs(const float (&v)[kPer], int E, int k, int32_t *idx,
+                                               float *w) {
+    const int lane = threadIdx.x & 31;
+    uint32_t key[kPer], id[kPer];
+#pragma unroll
+    for (int s = 0; s < kPer; ++s) {
+        const int e = lane + 32 * s;
+        key[s] = e < E ? logit_key(v[s]) : 0u;
+        id[s] = e < E ? uint32_t(e) : 0xffffffffu;  // past E: after every expert
+    }
+    // sort the lane's candidates (insertion into the sorted prefix, unrolled)
+#pragma unroll
+    for (int s = 1; s < kPer; ++s) {
+#pragma unroll
+        for (int j = s; j > 0; --j) {
+            if (topk_first(key[j], id[j], key[j - 1], id[j - 1])) {
+                const uint32_t tk = key[j], ti = id[j];
+                key[j] = key[j - 1];
+                id[j] = id[j - 1];
+                key[j - 1] = tk;
+                id[j - 1] = ti;
+            }
+        }
+    }
+    uint32_t sel_key = 0u, sel_i = 0u, kmax = 0u;
+    for (int j = 0; j < k; ++j) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
+        const uint32_t win = __reduce_min_sync(0xffffffffu, key[0] == m ? id[0] : 0xffffffffu);
+        if (id[0] == win) {  // the winner drops its head
+#pragma unroll
+            for (int s = 0; s + 1 < kPer; ++s) {
+                key[s] = key[s + 1];
+                id[s] = id[s + 1];
+            }
+            key[kPer - 1] = 0u;
+            id[kPer - 1] = 0xffffffffu;
+        }
+        if (j == 0) kmax = m;
+        if (lane == j) {
+            sel_key = m;
+            sel_i = win;
+        }
+    }
+    const float vmax = logit_of_key(kmax);
+    float ex = (lane < k) ? expf(logit_of_key(sel_key) - vmax) : 0.f;
+    float z = warp_sum(ex);
+    if (lane < k) {
+        idx[lane] = int32_t(sel_i);
+        w[lane] = ex / z;
+    }
+}
+
+// The same, reading the logits from `lg` (E <= kMaxE).
 __device__ __forceinline__ void warp_topk(const float *lg, int E, int k, int32_t *idx, float *w) {
     constexpr int kPer = kMaxE / 32;
     const int lane = threadIdx.x & 31;
     float v[kPer];
-    bool taken[kPer];
 #pragma unroll
-    for (int s = 0; s < kPer; ++s) {
-        int e = lane + 32 * s;
-        v[s] = (e < E) ? lg[e] : -INFINITY;
-        taken[s] = (e >= E);
-    }
-    float sel_v = 0.f;   // lane j keeps slot j's logit
-    int sel_i = 0;
-    float vmax = 0.f;
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int s = 0; s < kPer; ++s) {
-            int e = lane + 32 * s;
-            if (!taken[s] && better(v[s], e, bv, bi)) {
-                bv = v[s];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (better(ov, oi, bv, bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-#pragma unroll
-        for (int s = 0; s < kPer; ++s)
-            if (bi == lane + 32 * s) taken[s] = true;
-        if (j == 0) vmax = bv;
-        if (lane == j) {
-            sel_v = bv;
-            sel_i = bi;
-        }
-    }
-    float ex = (lane < k) ? expf(sel_v - vmax) : 0.f;
-    float z = warp_sum(ex);
-    if (lane < k) {
-        idx[lane] = sel_i;
-        w[lane] = ex / z;
-    }
+    for (int s = 0; s < kPer; ++s) v[s] = lane + 32 * s < E ? lg[lane + 32 * s] : 0.f;
+    warp_topk_regs<kPer>(v, E, k, idx, w);
 }
 
 }  // namespace moeq4k

@@ -18,16 +18,19 @@
 //
 // A cluster of four CTAs per tile of 128 tokens, CTA r taking the K quarter
 // r.  Per 32-K stage: TMA brings the x and Wr tiles (128 rows x 128 bytes,
-// 128-byte swizzle); every thread splits its share of the two tiles in place
-// (hi back into the tile, lo into two more tiles: the split is elementwise,
-// so the swizzled layout carries over); thread 0 issues twelve MMAs
-// (M = 128 tokens, N = 128 experts, K = 8 each) and commits; a three-stage
-// ring overlaps the copies, the split and the MMAs.  The four partial tiles
-// meet through distributed shared memory: CTA r adds the quarters in rank
-// order for its 32 tokens, adds the bias and ranks them (one warp per
-// token).  Fixed MMA and reduction order: deterministic.  Every wait is
-// bounded by a global-timer deadline; a timed-out wait records
-// MOE_ERR_TIMEOUT and the cluster writes no routing.
+// 128-byte swizzle) into a five-slot ring; every thread splits its share of
+// the two tiles in place (hi back into the tile, lo into one of two lo
+// buffers: the split is elementwise, so the swizzled layout carries over);
+// thread 0 issues twelve MMAs (M = 128 tokens, N = 128 experts, K = 8 each)
+// into the stage's own accumulator and commits.  Stage st's accumulator is
+// added into fp32 registers during stage st + 2 (three accumulators), so the
+// tensor pipe runs two stages behind the split.  The four partial tiles meet
+// through distributed shared memory: CTA r loads the quarters of its 32
+// tokens (every load issued before the first sum), adds them in rank order
+// with the bias and ranks each token with one warp, from registers.  Fixed
+// MMA and reduction order: deterministic.  Every wait is bounded by a
+// global-timer deadline; a timed-out wait records MOE_ERR_TIMEOUT and the
+// cluster writes no routing.
 #include <cooperative_groups.h>
 #include <cuda.h>
 
@@ -52,8 +55,7 @@ constexpr int kSmem = 1024 + kHead + kStages * kStage + 2 * kLo;  // + slack to 
 constexpr int kThreads = 256;
 constexpr int kPS = kEN + 4;              // row of the partial tile (floats)
 constexpr int kTok = kTM / kSplit;        // tokens ranked by each CTA
-static_assert(kTM * kPS * 4 + kTok * (kEN + 1) * 4 <= kStages * kStage,
-              "the partial and logit tiles reuse the copy ring");
+static_assert(kTM * kPS * 4 <= kStages * kStage, "the partial tile reuses the copy ring");
 static_assert(kSmem <= 232448, "shared memory of one CTA");
 
 struct Params {
@@ -114,10 +116,11 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
         *failed = 0;
         fence_mbar_init();
     }
-    // two accumulators of 128 fp32 columns, D[128 tokens][128 experts]: stage
-    // st accumulates into buffer st % 2 from zero, and every warp adds the
-    // finished stage into fp32 registers while the next stage's MMAs run
-    constexpr uint32_t kCols = 2 * kEN;
+    // three accumulators of 128 fp32 columns, D[128 tokens][128 experts]
+    // (512 columns allocated): stage st accumulates into buffer st % 3 from
+    // zero, and every warp adds stage st - 2 into fp32 registers while the
+    // MMAs of stages st - 1 and st run
+    constexpr uint32_t kCols = 4 * kEN;
     if (warp == 0) tc::tmem_alloc(tmem_ptr, kCols);
     tc::fence_before_sync();
     __syncthreads();
@@ -141,7 +144,7 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int j = 0; j < 64; ++j) racc[j] = 0.f;
     auto add_stage = [&](int st) {  // stage st's accumulator into racc (its MMAs are complete)
-        const uint32_t lb = taddr + uint32_t(st & 1) * kEN + lane_off;
+        const uint32_t lb = taddr + uint32_t(st % 3) * kEN + lane_off;
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 8) {
             float v[8];
@@ -156,7 +159,18 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
         const int slot = st % kStages;
         const uint32_t ph = uint32_t(st / kStages) & 1u;
         uint8_t *base = ring + slot * kStage;
-        uint8_t *lo = lobuf + (st & 1) * kLo;  // free: stage st - 2's MMAs were waited for
+        uint8_t *lo = lobuf + (st & 1) * kLo;
+        if (st >= 2) {
+            // stage st - 2's MMAs complete: its copy slot is refilled (thread 0),
+            // its lo buffer (this stage's) is free and its accumulator is added
+            const int ps = (st - 2) % kStages;
+            if (!mbar_wait(done + ps, uint32_t((st - 2) / kStages) & 1u, deadline)) *failed = 1;
+            if (tid == 0 && st - 2 + kStages < nst && *failed == 0) issue(st - 2 + kStages);
+            if (st - 2 + kStages < nst) ++issued;  // every thread keeps the same count
+            tc::fence_after_sync();
+            add_stage(st - 2);
+            tc::fence_before_sync();
+        }
         if (!mbar_wait(full + slot, ph, deadline)) *failed = 1;
         __syncthreads();  // a flag set before the barrier is seen by every thread after it
         const bool ok = *failed == 0;
@@ -179,7 +193,7 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
             const uint32_t a = smem_addr(base), al = smem_addr(lo);
             const uint64_t dx = tc::smem_desc_sw128(a), dw = tc::smem_desc_sw128(a + kTile);
             const uint64_t dxl = tc::smem_desc_sw128(al), dwl = tc::smem_desc_sw128(al + kTile);
-            const uint32_t dacc = taddr + uint32_t(st & 1) * kEN;
+            const uint32_t dacc = taddr + uint32_t(st % 3) * kEN;
 #pragma unroll
             for (int kk = 0; kk < kBK / 8; ++kk) {  // K = 8 per MMA: 32 bytes (2 in the address field)
                 const uint64_t o = uint64_t(2 * kk);
@@ -188,17 +202,6 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
                 tc::mma_tf32(dacc, dx + o, dwl + o, idesc, true);
             }
             tc::commit_arrive(done + slot);
-        }
-        if (st >= 1) {
-            // stage st - 1: its MMAs complete -> refill its copy slot (thread 0) and
-            // add its accumulator (every warp)
-            const int ps = (st - 1) % kStages;
-            if (!mbar_wait(done + ps, uint32_t((st - 1) / kStages) & 1u, deadline)) *failed = 1;
-            if (tid == 0 && st + kStages - 1 < nst && *failed == 0) issue(st + kStages - 1);
-            if (st + kStages - 1 < nst) ++issued;  // every thread keeps the same count
-            tc::fence_after_sync();
-            add_stage(st - 1);
-            tc::fence_before_sync();
         }
     }
     // every MMA complete; the last stage's accumulator into racc
@@ -213,6 +216,7 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
         }
     }
     tc::fence_after_sync();
+    if (nst > 1) add_stage(nst - 2);
     if (nst > 0) add_stage(nst - 1);
     tc::fence_before_sync();
     __syncthreads();
@@ -220,9 +224,12 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
 
     float *ptile = reinterpret_cast<float *>(ring);  // [kTM][kPS]
     {
-        float *row = ptile + (32 * (warp & 3) + lane) * kPS + (warp >> 2) * 64;
+        // 16-byte stores: with rows of kPS = 132 floats the eight lanes of each
+        // quarter-warp phase hit distinct bank quads
+        float4 *row = reinterpret_cast<float4 *>(ptile + (32 * (warp & 3) + lane) * kPS + (warp >> 2) * 64);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) row[j] = racc[j];
+        for (int j = 0; j < 16; ++j)
+            row[j] = make_float4(racc[4 * j], racc[4 * j + 1], racc[4 * j + 2], racc[4 * j + 3]);
     }
     cl.sync();  // every CTA's partial tile and flag are complete
 
@@ -230,29 +237,40 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int q = 0; q < kSplit; ++q)
         any_failed |= *cl.map_shared_rank(const_cast<int *>(failed), q) != 0;
-    float *lg = ptile + kTM * kPS;  // [kTok][kEN + 1]
+    // CTA r sums the four quarters of its 32 tokens in rank order: warp v takes
+    // tokens v, v + 8, ..., lane L experts L + 32 s; every distributed load is
+    // issued before the first sum
+    constexpr int kTW = kTok / (kThreads / 32);  // tokens per warp
+    constexpr int kEL = kEN / 32;                // experts per lane
     const float *src[kSplit];
 #pragma unroll
     for (int q = 0; q < kSplit; ++q) src[q] = cl.map_shared_rank(ptile, q);
-    for (int lt = warp; lt < kTok; lt += kThreads / 32) {
-        const int tt = r * kTok + lt;
-        for (int e = lane; e < p.E; e += 32) {
-            float v = src[0][tt * kPS + e];
+    float part[kTW][kEL][kSplit];
 #pragma unroll
-            for (int q = 1; q < kSplit; ++q) v += src[q][tt * kPS + e];
-            lg[lt * (kEN + 1) + e] = v + (p.bias ? p.bias[e] : 0.f);
-        }
-    }
+    for (int i = 0; i < kTW; ++i)
+#pragma unroll
+        for (int s = 0; s < kEL; ++s)
+#pragma unroll
+            for (int q = 0; q < kSplit; ++q)
+                part[i][s][q] = src[q][(r * kTok + warp + 8 * i) * kPS + lane + 32 * s];
     cl.sync();  // no CTA leaves while another reads its partial tile
     if (any_failed) {
         if (tid == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 30 + r);
         return;
     }
-    for (int lt = warp; lt < kTok; lt += kThreads / 32) {
-        const int t = t0 + r * kTok + lt;
-        if (t < p.T)
-            warp_topk(&lg[lt * (kEN + 1)], p.E, p.k, p.idx + size_t(t) * p.k,
-                      p.w + size_t(t) * p.k);
+#pragma unroll
+    for (int i = 0; i < kTW; ++i) {
+        const int t = t0 + r * kTok + warp + 8 * i;
+        float lg[kEL];
+#pragma unroll
+        for (int s = 0; s < kEL; ++s) {
+            const int e = lane + 32 * s;
+            float v = part[i][s][0];
+#pragma unroll
+            for (int q = 1; q < kSplit; ++q) v += part[i][s][q];
+            lg[s] = v + (p.bias && e < p.E ? p.bias[e] : 0.f);
+        }
+        if (t < p.T) warp_topk_regs<kEL>(lg, p.E, p.k, p.idx + size_t(t) * p.k, p.w + size_t(t) * p.k);
     }
 }
 
