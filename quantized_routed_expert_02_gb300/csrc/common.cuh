@@ -101,8 +101,8 @@ constexpr size_t kSyncWords = kMaxE;
 constexpr int kPermSlots = 256;
 
 struct WsLayout {
-    size_t sync, blockcnt, slotpos, counts, offs, active, nactive, perm, h, o, logits, x16, h16, chunks, chunks_dn, xn, xstage,
-        ystage, total;
+    size_t sync, blockcnt, slotpos, counts, offs, active, nactive, perm, h, o, logits, x16, h16, chunks, chunks_dn, ready,
+        xn, xstage, ystage, total;
 };
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -128,6 +128,7 @@ inline WsLayout ws_layout(int T, int H, int E, int k, int I, bool host_staging) 
     L.h16 = off;     off = align256(off + 2 * pairs * I);                // fp16 SwiGLU output
     L.chunks = off;  off = align256(off + sizeof(TcChunk) * (pairs / 32 + E + 1));  // chunks of >= 32 slots
     L.chunks_dn = off; off = align256(off + sizeof(TcChunk) * (pairs / 32 + E + 1));
+    L.ready = off;   off = align256(off + sizeof(uint32_t) * kMaxE);      // gate/up rows done per expert
     L.xn = off;      off = align256(off + sizeof(float) * size_t(T) * H);  // normed FFN input
     L.xstage = off;
     L.ystage = off;

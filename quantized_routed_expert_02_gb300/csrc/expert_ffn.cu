@@ -203,15 +203,32 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
          i += size_t(gridDim.x) * blockDim.x) {
         const int t = int(i / h4), c = int(i % h4);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            const int e = idx[size_t(t) * k + j];
-            if (e < 0 || e >= E) continue;
-            const float wj = w[size_t(t) * k + j];
-            const float4 v = reinterpret_cast<const float4 *>(o + (size_t(t) * k + j) * H)[c];
-            acc.x = fmaf(wj, v.x, acc.x);
-            acc.y = fmaf(wj, v.y, acc.y);
-            acc.z = fmaf(wj, v.z, acc.z);
-            acc.w = fmaf(wj, v.w, acc.w);
+        // eight slots at a time: every index, weight and output row of the
+        // group is requested before the first multiply-add, which then run in
+        // slot order (a slot with an index outside [0, E) adds nothing)
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            bool ok[8];
+            float wj[8];
+            float4 v[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int j = j0 + jj;
+                const int e = j < k ? idx[size_t(t) * k + j] : -1;
+                ok[jj] = e >= 0 && e < E;
+                wj[jj] = ok[jj] ? w[size_t(t) * k + j] : 0.f;
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+                v[jj] = ok[jj] ? reinterpret_cast<const float4 *>(o + (size_t(t) * k + j0 + jj) * H)[c]
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                if (!ok[jj]) continue;
+                acc.x = fmaf(wj[jj], v[jj].x, acc.x);
+                acc.y = fmaf(wj[jj], v[jj].y, acc.y);
+                acc.z = fmaf(wj[jj], v[jj].z, acc.z);
+                acc.w = fmaf(wj[jj], v[jj].w, acc.w);
+            }
         }
         if (ep.capture != nullptr && t == ep.cap_t) reinterpret_cast<float4 *>(ep.capture)[c] = acc;
         if (ep.residual != nullptr) {

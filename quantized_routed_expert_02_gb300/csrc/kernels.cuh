@@ -71,7 +71,8 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
                               const int32_t *offs, const int32_t *perm, const int32_t *slotpos,
                               const int32_t *active,
                               const int32_t *nactive, __half *x16, __half *h16, float *obuf,
-                              TcChunk *chunks, TcChunk *chunks_dn, WsHeader *hdr, int num_sms, unsigned long long wait_ns, unsigned long long *timeline,
+                              TcChunk *chunks, TcChunk *chunks_dn, unsigned int *ready, WsHeader *hdr,
+                              int num_sms, unsigned long long wait_ns, unsigned long long *timeline,
                               cudaStream_t s);
 
 cudaError_t init_decode_fused(int dev, int num_sms);
