@@ -296,27 +296,25 @@ __global__ void __cluster_dims__(rcl::kCS, 1, 1) __launch_bounds__(256)
     }
     const int E = p.E, k = p.k;
     const int E4 = (E + 3) & ~3;
-    // a NaN logit ranks as -inf (the order is then total and every rank
-    // unique); pads past E lose every comparison
-    if (tid < E4) {
-        const float v = tid < E ? inbox[tid] : -INFINITY;
-        inbox[tid] = v != v ? -INFINITY : v;
-    }
+    // the logits as order-preserving keys (logit_key: -0 as +0, NaN below
+    // every number, as warp_topk ranks them); pads past E lose every comparison
+    uint32_t *keys = reinterpret_cast<uint32_t *>(inbox);
+    if (tid < E4) keys[tid] = tid < E ? logit_key(inbox[tid]) : 0u;
     __syncthreads();
     {
-        // rank of expert e in the order (logit descending, index ascending): the
+        // rank of expert e in the order (key descending, index ascending): the
         // experts that beat it, counted by two threads (halves of the list) for
         // E <= 128, else by one
         const bool pair = E <= 128;
         const int e = pair ? tid >> 1 : tid;
         const int nq = E4 / 4, half = pair ? (nq + 1) / 2 : nq;
         const int q0 = pair && (tid & 1) ? half : 0, q1 = pair && !(tid & 1) ? half : nq;
-        const float v = e < E ? inbox[e] : 0.f;
+        const uint32_t v = e < E ? keys[e] : 0u;
         int rank = 0;
-        const float4 *in4 = reinterpret_cast<const float4 *>(inbox);
+        const uint4 *in4 = reinterpret_cast<const uint4 *>(keys);
 #pragma unroll 4
         for (int j4 = q0; j4 < q1; ++j4) {
-            const float4 u = in4[j4];
+            const uint4 u = in4[j4];
             const int j = 4 * j4;
             rank += (u.x > v || (u.x == v && j < e)) ? 1 : 0;
             rank += (u.y > v || (u.y == v && j + 1 < e)) ? 1 : 0;
@@ -325,7 +323,7 @@ __global__ void __cluster_dims__(rcl::kCS, 1, 1) __launch_bounds__(256)
         }
         if (pair) rank += __shfl_xor_sync(0xffffffffu, rank, 1);
         if (e < E && rank < k && (!pair || (tid & 1) == 0)) {
-            sel_v[rank] = v;
+            sel_v[rank] = logit_of_key(v);
             sel_i[rank] = e;
         }
     }
