@@ -52,7 +52,8 @@ constexpr int kStage = 2 * kTile;         // x, Wr (hi written back in place)
 constexpr int kLo = 2 * kTile;            // lo(x), lo(Wr) of a stage; two buffers
 constexpr int kHead = 1024;               // barriers and flags
 constexpr int kSmem = 1024 + kHead + kStages * kStage + 2 * kLo;  // + slack to align to 1024
-constexpr int kThreads = 256;
+constexpr int kSplitWarps = 8;           // split / accumulate warps
+constexpr int kThreads = 32 * (kSplitWarps + 1);  // + the MMA warp
 constexpr int kPS = kEN + 4;              // row of the partial tile (floats)
 constexpr int kTok = kTM / kSplit;        // tokens ranked by each CTA
 static_assert(kTM * kPS * 4 <= kStages * kStage, "the partial tile reuses the copy ring");
@@ -94,7 +95,9 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [kStages] a stage's tiles landed
     uint64_t *done = full + kStages;                      // [kStages] the MMAs reading the slot are complete
-    uint64_t *fin = done + kStages;                       // every MMA complete
+    uint64_t *splitb = done + kStages;                    // [kStages] the eight split warps are done with it
+    uint64_t *accfree = splitb + kStages;                 // [3] an accumulator has been added to registers
+    uint64_t *fin = accfree + 3;                          // every MMA complete
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(fin + 1);
     volatile int *failed = reinterpret_cast<volatile int *>(tmem_ptr + 2);
     uint8_t *ring = smem + kHead;                   // copy ring
@@ -109,17 +112,19 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(full + i, 1);  // the copying thread's arrival + the tiles' bytes
-            mbar_init(done + i, 1);  // the stage's MMAs (commit)
+            mbar_init(full + i, 1);            // the copying thread's arrival + the tiles' bytes
+            mbar_init(done + i, 1);            // the stage's MMAs (commit)
+            mbar_init(splitb + i, kSplitWarps);  // one arrival per split warp
         }
+        for (int i = 0; i < 3; ++i) mbar_init(accfree + i, kSplitWarps);
         mbar_init(fin, 1);
         *failed = 0;
         fence_mbar_init();
     }
     // three accumulators of 128 fp32 columns, D[128 tokens][128 experts]
     // (512 columns allocated): stage st accumulates into buffer st % 3 from
-    // zero, and every warp adds stage st - 2 into fp32 registers while the
-    // MMAs of stages st - 1 and st run
+    // zero, and the split warps add stage st - 2 into fp32 registers while
+    // the MMAs of stages st - 1 and st run
     constexpr uint32_t kCols = 4 * kEN;
     if (warp == 0) tc::tmem_alloc(tmem_ptr, kCols);
     tc::fence_before_sync();
@@ -138,7 +143,7 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
         for (int st = 0; st < kStages && st < nst; ++st) issue(st);
     int issued = kStages < nst ? kStages : nst;
 
-    // this warp's accumulator lanes and columns: quadrant warp % 4, half warp / 4
+    // split warp w: accumulator lanes and columns of quadrant w % 4, half w / 4
     const uint32_t lane_off = (uint32_t((warp & 3) * 32) << 16) + uint32_t((warp >> 2) * 64);
     float racc[64];
 #pragma unroll
@@ -153,61 +158,89 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 8; ++j) racc[c0 + j] += v[j];
         }
     };
-
-    const uint32_t idesc = tc::idesc_tf32_f32(kTM, kEN);
-    for (int st = 0; st < nst; ++st) {
-        const int slot = st % kStages;
-        const uint32_t ph = uint32_t(st / kStages) & 1u;
-        uint8_t *base = ring + slot * kStage;
-        uint8_t *lo = lobuf + (st & 1) * kLo;
-        if (st >= 2) {
-            // stage st - 2's MMAs complete: its copy slot is refilled (thread 0),
-            // its lo buffer (this stage's) is free and its accumulator is added
-            const int ps = (st - 2) % kStages;
-            if (!mbar_wait(done + ps, uint32_t((st - 2) / kStages) & 1u, deadline)) *failed = 1;
-            if (tid == 0 && st - 2 + kStages < nst && *failed == 0) issue(st - 2 + kStages);
-            if (st - 2 + kStages < nst) ++issued;  // every thread keeps the same count
-            tc::fence_after_sync();
-            add_stage(st - 2);
-            tc::fence_before_sync();
+    // stage st - 2's MMAs complete: its copy slot is refilled (thread 0), its
+    // lo buffer (stage st's) is free, and its accumulator is added and released
+    auto retire = [&](int st2) {
+        const int ps = st2 % kStages;
+        if (!mbar_wait(done + ps, uint32_t(st2 / kStages) & 1u, deadline)) *failed = 1;
+        if (tid == 0 && st2 + kStages < nst && *failed == 0) {
+            issue(st2 + kStages);
+            ++issued;
         }
-        if (!mbar_wait(full + slot, ph, deadline)) *failed = 1;
-        __syncthreads();  // a flag set before the barrier is seen by every thread after it
-        const bool ok = *failed == 0;
-        if (ok) {
+        tc::fence_after_sync();
+        add_stage(st2);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(accfree + st2 % 3);
+    };
+
+    if (warp < kSplitWarps) {
+        // ---- split warps: every thread splits its share of each stage's tiles
+        // and adds finished accumulators; no CTA-wide barrier in the loop
+        for (int st = 0; st < nst; ++st) {
+            const int slot = st % kStages;
+            uint8_t *base = ring + slot * kStage;
+            uint8_t *lo = lobuf + (st & 1) * kLo;
+            if (st >= 2) retire(st - 2);
+            if (!mbar_wait(full + slot, uint32_t(st / kStages) & 1u, deadline)) *failed = 1;
             // hi back into the x and Wr tiles, lo into the stage's lo buffer
             float4 *t = reinterpret_cast<float4 *>(base);
             float4 *tl = reinterpret_cast<float4 *>(lo);
 #pragma unroll 4
-            for (int i = tid; i < 2 * kTile / 16; i += kThreads) {
+            for (int i = tid; i < 2 * kTile / 16; i += kSplitWarps * 32) {
                 float4 hi, lv;
                 split4(t[i], hi, lv);
                 t[i] = hi;
                 tl[i] = lv;
             }
             fence_proxy_async_smem();  // generic stores before the MMA's async-proxy reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(splitb + slot);
         }
-        __syncthreads();
-        if (tid == 0 && ok) {
-            tc::fence_after_sync();
-            const uint32_t a = smem_addr(base), al = smem_addr(lo);
-            const uint64_t dx = tc::smem_desc_sw128(a), dw = tc::smem_desc_sw128(a + kTile);
-            const uint64_t dxl = tc::smem_desc_sw128(al), dwl = tc::smem_desc_sw128(al + kTile);
-            const uint32_t dacc = taddr + uint32_t(st % 3) * kEN;
-#pragma unroll
-            for (int kk = 0; kk < kBK / 8; ++kk) {  // K = 8 per MMA: 32 bytes (2 in the address field)
-                const uint64_t o = uint64_t(2 * kk);
-                tc::mma_tf32(dacc, dx + o, dw + o, idesc, kk > 0);
-                tc::mma_tf32(dacc, dxl + o, dw + o, idesc, true);
-                tc::mma_tf32(dacc, dx + o, dwl + o, idesc, true);
+        if (nst > 1) retire(nst - 2);
+        if (nst > 0) retire(nst - 1);
+    } else {
+        // ---- MMA warp: stage st's twelve MMAs once the eight split warps are
+        // done with its slot and stage st - 3's accumulator buffer is free; the
+        // whole warp walks the loop, one elected lane issues
+        uint32_t is = 0;
+        asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+                     : "=r"(is));
+        const bool leader = is != 0u;
+        const uint32_t idesc = tc::idesc_tf32_f32(kTM, kEN);
+        for (int st = 0; st < nst; ++st) {
+            const int slot = st % kStages;
+            bool ok = mbar_wait(splitb + slot, uint32_t(st / kStages) & 1u, deadline);
+            if (st >= 3) ok = mbar_wait(accfree + st % 3, uint32_t(st / 3 - 1) & 1u, deadline) && ok;
+            if (!__all_sync(0xffffffffu, ok)) {
+                *failed = 1;
+                break;  // no more MMAs: the split warps' waits then run out as well
             }
-            tc::commit_arrive(done + slot);
+            tc::fence_after_sync();
+            if (leader) {
+                uint8_t *base = ring + slot * kStage;
+                uint8_t *lo = lobuf + (st & 1) * kLo;
+                const uint32_t a = smem_addr(base), al = smem_addr(lo);
+                const uint64_t dx = tc::smem_desc_sw128(a), dw = tc::smem_desc_sw128(a + kTile);
+                const uint64_t dxl = tc::smem_desc_sw128(al), dwl = tc::smem_desc_sw128(al + kTile);
+                const uint32_t dacc = taddr + uint32_t(st % 3) * kEN;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 8; ++kk) {  // K = 8 per MMA: 32 bytes (2 in the address field)
+                    const uint64_t o = uint64_t(2 * kk);
+                    tc::mma_tf32(dacc, dx + o, dw + o, idesc, kk > 0);
+                    tc::mma_tf32(dacc, dxl + o, dw + o, idesc, true);
+                    tc::mma_tf32(dacc, dx + o, dwl + o, idesc, true);
+                }
+                tc::commit_arrive(done + slot);
+            }
+            __syncwarp();
         }
+        if (leader) tc::commit_arrive(fin);
+        __syncwarp();
+        if (!mbar_wait(fin, 0, deadline)) *failed = 1;
     }
-    // every MMA complete; the last stage's accumulator into racc
-    if (tid == 0) tc::commit_arrive(fin);
-    if (!mbar_wait(fin, 0, deadline)) *failed = 1;
     // copies still in flight after a time-out must land before the ring is reused
+    __syncthreads();
     if (tid == 0) {
         const uint64_t limit = global_timer_ns() + p.wait_ns;
         for (int i = 0; i < kStages && i < issued; ++i) {
@@ -215,15 +248,13 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
             mbar_wait(full + st % kStages, uint32_t(st / kStages) & 1u, limit);
         }
     }
-    tc::fence_after_sync();
-    if (nst > 1) add_stage(nst - 2);
-    if (nst > 0) add_stage(nst - 1);
     tc::fence_before_sync();
     __syncthreads();
+    tc::fence_after_sync();
     if (warp == 0) tc::tmem_dealloc(taddr, kCols);
 
     float *ptile = reinterpret_cast<float *>(ring);  // [kTM][kPS]
-    {
+    if (warp < kSplitWarps) {
         // 16-byte stores: with rows of kPS = 132 floats the eight lanes of each
         // quarter-warp phase hit distinct bank quads
         float4 *row = reinterpret_cast<float4 *>(ptile + (32 * (warp & 3) + lane) * kPS + (warp >> 2) * 64);
@@ -240,27 +271,29 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
     // CTA r sums the four quarters of its 32 tokens in rank order: warp v takes
     // tokens v, v + 8, ..., lane L experts L + 32 s; every distributed load is
     // issued before the first sum
-    constexpr int kTW = kTok / (kThreads / 32);  // tokens per warp
+    constexpr int kTW = kTok / kSplitWarps;      // tokens per split warp
     constexpr int kEL = kEN / 32;                // experts per lane
     const float *src[kSplit];
 #pragma unroll
     for (int q = 0; q < kSplit; ++q) src[q] = cl.map_shared_rank(ptile, q);
     float part[kTW][kEL][kSplit];
+    const int tw = warp < kSplitWarps ? warp : 0;  // the MMA warp loads nothing it uses
 #pragma unroll
     for (int i = 0; i < kTW; ++i)
 #pragma unroll
         for (int s = 0; s < kEL; ++s)
 #pragma unroll
             for (int q = 0; q < kSplit; ++q)
-                part[i][s][q] = src[q][(r * kTok + warp + 8 * i) * kPS + lane + 32 * s];
+                part[i][s][q] = src[q][(r * kTok + tw + kSplitWarps * i) * kPS + lane + 32 * s];
     cl.sync();  // no CTA leaves while another reads its partial tile
     if (any_failed) {
         if (tid == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 30 + r);
         return;
     }
+    if (warp >= kSplitWarps) return;
 #pragma unroll
     for (int i = 0; i < kTW; ++i) {
-        const int t = t0 + r * kTok + warp + 8 * i;
+        const int t = t0 + r * kTok + warp + kSplitWarps * i;
         float lg[kEL];
 #pragma unroll
         for (int s = 0; s < kEL; ++s) {
