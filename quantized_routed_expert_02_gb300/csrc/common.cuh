@@ -297,61 +297,86 @@ __device__ __forceinline__ bool topk_first(uint32_t ka, uint32_t ia, uint32_t kb
     return ka > kb || (ka == kb && ia < ib);
 }
 
-// Top-k of one token's E <= 32 * kPer logits (bias already added) by one
-// warp, lane L holding the logits of experts L + 32 s in v[s]; writes
-// idx[0..k) in selection order and the renormalised weights
-// w_j = exp(l_j - l_max) / sum over the selection of exp(l - l_max).
+// Top-k of NT tokens' E <= 32 * kPer logits each (bias already added) by one
+// warp, lane L holding the logits of experts L + 32 s of token u in v[u][s];
+// the tokens' rounds run interleaved (independent chains).  For token u with
+// out[u] set, writes idx[u][0..k) in selection order and the renormalised
+// weights w_j = exp(l_j - l_max) / sum over the selection of exp(l - l_max).
+template <int kPer, int NT>
+__device__ __forceinline__ void warp_topk_multi(const float (&v)[NT][kPer], int E, int k,
+                                                int32_t *const (&idx)[NT], float *const (&w)[NT],
+                                                const bool (&out)[NT]) {
+    const int lane = threadIdx.x & 31;
+    uint32_t key[NT][kPer], id[NT][kPer];
+#pragma unroll
+    for (int u = 0; u < NT; ++u)
+#pragma unroll
+        for (int s = 0; s < kPer; ++s) {
+            const int e = lane + 32 * s;
+            key[u][s] = e < E ? logit_key(v[u][s]) : 0u;
+            id[u][s] = e < E ? uint32_t(e) : 0xffffffffu;  // past E: after every expert
+        }
+    // sort each token's candidates in this lane (insertion, unrolled)
+#pragma unroll
+    for (int u = 0; u < NT; ++u)
+#pragma unroll
+        for (int s = 1; s < kPer; ++s)
+#pragma unroll
+            for (int j = s; j > 0; --j)
+                if (topk_first(key[u][j], id[u][j], key[u][j - 1], id[u][j - 1])) {
+                    const uint32_t tk = key[u][j], ti = id[u][j];
+                    key[u][j] = key[u][j - 1];
+                    id[u][j] = id[u][j - 1];
+                    key[u][j - 1] = tk;
+                    id[u][j - 1] = ti;
+                }
+    uint32_t sel_key[NT], sel_i[NT], kmax[NT];
+#pragma unroll
+    for (int u = 0; u < NT; ++u) sel_key[u] = sel_i[u] = kmax[u] = 0u;
+    for (int j = 0; j < k; ++j) {
+#pragma unroll
+        for (int u = 0; u < NT; ++u) {
+            const uint32_t m = __reduce_max_sync(0xffffffffu, key[u][0]);
+            const uint32_t win = __reduce_min_sync(0xffffffffu, key[u][0] == m ? id[u][0] : 0xffffffffu);
+            if (id[u][0] == win) {  // the winner drops its head
+#pragma unroll
+                for (int s = 0; s + 1 < kPer; ++s) {
+                    key[u][s] = key[u][s + 1];
+                    id[u][s] = id[u][s + 1];
+                }
+                key[u][kPer - 1] = 0u;
+                id[u][kPer - 1] = 0xffffffffu;
+            }
+            if (j == 0) kmax[u] = m;
+            if (lane == j) {
+                sel_key[u] = m;
+                sel_i[u] = win;
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < NT; ++u) {
+        const float vmax = logit_of_key(kmax[u]);
+        const float ex = (lane < k) ? expf(logit_of_key(sel_key[u]) - vmax) : 0.f;
+        const float z = warp_sum(ex);
+        if (out[u] && lane < k) {
+            idx[u][lane] = int32_t(sel_i[u]);
+            w[u][lane] = ex / z;
+        }
+    }
+}
+
+// One token (kPer logits per lane in v).
 template <int kPer>
 __device__ __forceinline__ void warp_topk_regs(const float (&v)[kPer], int E, int k, int32_t *idx,
                                                float *w) {
-    const int lane = threadIdx.x & 31;
-    uint32_t key[kPer], id[kPer];
+    float vv[1][kPer];
 #pragma unroll
-    for (int s = 0; s < kPer; ++s) {
-        const int e = lane + 32 * s;
-        key[s] = e < E ? logit_key(v[s]) : 0u;
-        id[s] = e < E ? uint32_t(e) : 0xffffffffu;  // past E: after every expert
-    }
-    // sort the lane's candidates (insertion into the sorted prefix, unrolled)
-#pragma unroll
-    for (int s = 1; s < kPer; ++s) {
-#pragma unroll
-        for (int j = s; j > 0; --j) {
-            if (topk_first(key[j], id[j], key[j - 1], id[j - 1])) {
-                const uint32_t tk = key[j], ti = id[j];
-                key[j] = key[j - 1];
-                id[j] = id[j - 1];
-                key[j - 1] = tk;
-                id[j - 1] = ti;
-            }
-        }
-    }
-    uint32_t sel_key = 0u, sel_i = 0u, kmax = 0u;
-    for (int j = 0; j < k; ++j) {
-        const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
-        const uint32_t win = __reduce_min_sync(0xffffffffu, key[0] == m ? id[0] : 0xffffffffu);
-        if (id[0] == win) {  // the winner drops its head
-#pragma unroll
-            for (int s = 0; s + 1 < kPer; ++s) {
-                key[s] = key[s + 1];
-                id[s] = id[s + 1];
-            }
-            key[kPer - 1] = 0u;
-            id[kPer - 1] = 0xffffffffu;
-        }
-        if (j == 0) kmax = m;
-        if (lane == j) {
-            sel_key = m;
-            sel_i = win;
-        }
-    }
-    const float vmax = logit_of_key(kmax);
-    float ex = (lane < k) ? expf(logit_of_key(sel_key) - vmax) : 0.f;
-    float z = warp_sum(ex);
-    if (lane < k) {
-        idx[lane] = int32_t(sel_i);
-        w[lane] = ex / z;
-    }
+    for (int s = 0; s < kPer; ++s) vv[0][s] = v[s];
+    int32_t *const ii[1] = {idx};
+    float *const ww[1] = {w};
+    const bool oo[1] = {true};
+    warp_topk_multi<kPer, 1>(vv, E, k, ii, ww, oo);
 }
 
 // The same, reading the logits from `lg` (E <= kMaxE).

@@ -56,7 +56,7 @@ constexpr int kSplitWarps = 8;           // split / accumulate warps
 constexpr int kThreads = 32 * (kSplitWarps + 1);  // + the MMA warp
 constexpr int kPS = kEN + 4;              // row of the partial tile (floats)
 constexpr int kTok = kTM / kSplit;        // tokens ranked by each CTA
-static_assert(kTM * kPS * 4 <= kStages * kStage, "the partial tile reuses the copy ring");
+static_assert(kSplit * kTok * kPS * 4 <= kStages * kStage, "the received quarters reuse the copy ring");
 static_assert(kSmem <= 232448, "shared memory of one CTA");
 
 struct Params {
@@ -76,6 +76,44 @@ __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x,
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
         : "memory");
+}
+
+// 16-byte / 4-byte asynchronous stores into CTA `rank` of the cluster (at
+// the offset of `dst` here), completing as transaction bytes on that CTA's
+// mbarrier at the offset of `bar`.
+__device__ __forceinline__ uint32_t cluster_addr(const void *p, int rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(p)), "r"(rank));
+    return ra;
+}
+__device__ __forceinline__ void st_async_v4_remote(float *dst, float a, float b, float c, float d,
+                                                   uint64_t *bar, int rank) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     cluster_addr(dst, rank)),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_addr(bar, rank))
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_u32_remote(uint32_t *dst, uint32_t v, uint64_t *bar, int rank) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                     cluster_addr(dst, rank)),
+                 "r"(v), "r"(cluster_addr(bar, rank))
+                 : "memory");
+}
+// Bounded wait for a phase completed by other CTAs of the cluster (acquire
+// at cluster scope).
+__device__ __forceinline__ bool mbar_wait_cluster_acq(uint64_t *bar, uint32_t parity, uint64_t deadline) {
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_addr(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (global_timer_ns() > deadline) return false;
+    }
 }
 
 // hi(v) (low 13 significand bits cleared) and lo(v) = v - hi(v), four at once.
@@ -100,6 +138,8 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
     uint64_t *fin = accfree + 3;                          // every MMA complete
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(fin + 1);
     volatile int *failed = reinterpret_cast<volatile int *>(tmem_ptr + 2);
+    uint64_t *pgot = reinterpret_cast<uint64_t *>(tmem_ptr + 4);  // the four quarters of my tokens
+    uint32_t *flags_in = reinterpret_cast<uint32_t *>(pgot + 1);   // [kSplit] each sender's flag
     uint8_t *ring = smem + kHead;                   // copy ring
     uint8_t *lobuf = ring + kStages * kStage;       // two lo buffers
     namespace cg = cooperative_groups;
@@ -118,6 +158,7 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 3; ++i) mbar_init(accfree + i, kSplitWarps);
         mbar_init(fin, 1);
+        mbar_init(pgot, 1);
         *failed = 0;
         fence_mbar_init();
     }
@@ -253,58 +294,68 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     if (warp == 0) tc::tmem_dealloc(taddr, kCols);
 
-    float *ptile = reinterpret_cast<float *>(ring);  // [kTM][kPS]
+    // The four K quarters of CTA r's 32 tokens land in its ring (free once
+    // every CTA of the cluster is past its loop): split warp w sends its 64
+    // partial columns of token row 32 (w % 4) + lane, owned by CTA w % 4, as
+    // 16-byte asynchronous stores completing on the owner's barrier, and
+    // every CTA sends each owner its flag the same way.
+    float *recv = reinterpret_cast<float *>(ring);  // [kSplit][kTok][kPS]
+    constexpr uint32_t kRecvBytes = uint32_t(kSplit) * kTok * kEN * 4u + uint32_t(kSplit) * 4u;
+    if (tid == 0) mbar_arrive_expect_tx(pgot, kRecvBytes);
+    cl.sync();  // every CTA's ring is free and its barrier armed
     if (warp < kSplitWarps) {
-        // 16-byte stores: with rows of kPS = 132 floats the eight lanes of each
-        // quarter-warp phase hit distinct bank quads
-        float4 *row = reinterpret_cast<float4 *>(ptile + (32 * (warp & 3) + lane) * kPS + (warp >> 2) * 64);
+        const int owner = warp & 3;
+        float *dst = recv + (size_t(r) * kTok + lane) * kPS + (warp >> 2) * 64;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            row[j] = make_float4(racc[4 * j], racc[4 * j + 1], racc[4 * j + 2], racc[4 * j + 3]);
+            st_async_v4_remote(dst + 4 * j, racc[4 * j], racc[4 * j + 1], racc[4 * j + 2], racc[4 * j + 3],
+                               pgot, owner);
     }
-    cl.sync();  // every CTA's partial tile and flag are complete
-
-    bool any_failed = false;
+    if (tid == 0)
 #pragma unroll
-    for (int q = 0; q < kSplit; ++q)
-        any_failed |= *cl.map_shared_rank(const_cast<int *>(failed), q) != 0;
-    // CTA r sums the four quarters of its 32 tokens in rank order: warp v takes
-    // tokens v, v + 8, ..., lane L experts L + 32 s; every distributed load is
-    // issued before the first sum
+        for (int q = 0; q < kSplit; ++q) st_async_u32_remote(flags_in + r, uint32_t(*failed), pgot, q);
+    if (warp >= kSplitWarps) return;
+    const bool got = mbar_wait_cluster_acq(pgot, 0u, deadline + p.wait_ns);
+    bool any_failed = !got;
+#pragma unroll
+    for (int q = 0; q < kSplit; ++q) any_failed |= flags_in[q] != 0u;
+    if (any_failed) {
+        if (tid == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 30 + r);
+        return;
+    }
+    // CTA r sums the quarters of its tokens in rank order: warp v takes tokens
+    // v, v + 8, ..., lane L experts L + 32 s
     constexpr int kTW = kTok / kSplitWarps;      // tokens per split warp
     constexpr int kEL = kEN / 32;                // experts per lane
-    const float *src[kSplit];
-#pragma unroll
-    for (int q = 0; q < kSplit; ++q) src[q] = cl.map_shared_rank(ptile, q);
     float part[kTW][kEL][kSplit];
-    const int tw = warp < kSplitWarps ? warp : 0;  // the MMA warp loads nothing it uses
 #pragma unroll
     for (int i = 0; i < kTW; ++i)
 #pragma unroll
         for (int s = 0; s < kEL; ++s)
 #pragma unroll
             for (int q = 0; q < kSplit; ++q)
-                part[i][s][q] = src[q][(r * kTok + tw + kSplitWarps * i) * kPS + lane + 32 * s];
-    cl.sync();  // no CTA leaves while another reads its partial tile
-    if (any_failed) {
-        if (tid == 0) record_status(p.hdr, MOE_ERR_TIMEOUT, 30 + r);
-        return;
-    }
-    if (warp >= kSplitWarps) return;
+                part[i][s][q] = recv[(size_t(q) * kTok + warp + kSplitWarps * i) * kPS + lane + 32 * s];
+    // the warp's kTW tokens ranked together (interleaved rounds)
+    float lg[kTW][kEL];
+    int32_t *oi[kTW];
+    float *ow[kTW];
+    bool oo[kTW];
 #pragma unroll
     for (int i = 0; i < kTW; ++i) {
         const int t = t0 + r * kTok + warp + kSplitWarps * i;
-        float lg[kEL];
+        oo[i] = t < p.T;
+        oi[i] = p.idx + size_t(oo[i] ? t : 0) * p.k;
+        ow[i] = p.w + size_t(oo[i] ? t : 0) * p.k;
 #pragma unroll
         for (int s = 0; s < kEL; ++s) {
             const int e = lane + 32 * s;
             float v = part[i][s][0];
 #pragma unroll
             for (int q = 1; q < kSplit; ++q) v += part[i][s][q];
-            lg[s] = v + (p.bias && e < p.E ? p.bias[e] : 0.f);
+            lg[i][s] = v + (p.bias && e < p.E ? p.bias[e] : 0.f);
         }
-        if (t < p.T) warp_topk_regs<kEL>(lg, p.E, p.k, p.idx + size_t(t) * p.k, p.w + size_t(t) * p.k);
     }
+    warp_topk_multi<kEL, kTW>(lg, p.E, p.k, oi, ow, oo);
 }
 
 }  // namespace rtc
