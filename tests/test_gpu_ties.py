@@ -173,6 +173,7 @@ ROUTER_PATHS = [
     (64, 2048, 128, 8),    # four tokens per tile, the batched-decode size
     (5, 8192, 16, 3),      # two experts per group, 32 K chunks through a 16-slot ring
     (200, 1024, 256, 8),   # eight tokens per tile, four experts per warp, two CTAs per SM
+    (100, 512, 256, 32),   # k = 32: the rank count's largest selection, 64 sums per lane
     (300, 2048, 128, 8),   # tensor-core cluster kernel with the top-k fused
     (256, 1024, 256, 8),   # large-E kernel (E > 128) with the top-k fused
     (260, 512, 64, 1),     # tensor-core kernel, k = 1: a tie decides the arg-max
