@@ -305,6 +305,9 @@ MOE_API moe_status moe_layer_noalloc(const float *x_dev, const float *Wr_dev, co
  * n != 0 makes CTA 0 of later single-token calls publish none of its router
  * logits and h values, so the other CTAs' waits for them run out; such a
  * call records MOE_ERR_TIMEOUT in the workspace status and writes no output.
+ * On the tensor-core batch path, CTA 0 of the gate/up GEMM then counts none
+ * of its finished h rows, so the down GEMM's waits for those experts run
+ * out: MOE_ERR_TIMEOUT again, and y holds no valid output.
  * Re-initialise the workspace (moe_workspace_init) afterwards to clear the
  * sticky status.
  */

@@ -138,7 +138,7 @@ moe_status ffn_enqueue(const float *x, const int32_t *idx, const float *w, const
             reinterpret_cast<__half *>(ws.base + L.h16), ws.f32(L.o),
             reinterpret_cast<TcChunk *>(ws.base + L.chunks),
             reinterpret_cast<TcChunk *>(ws.base + L.chunks_dn),
-            reinterpret_cast<unsigned int *>(ws.base + L.ready), ws.hdr(), sms, g_wait_ns,
+            reinterpret_cast<unsigned int *>(ws.base + L.ready), ws.hdr(), sms, g_wait_ns, g_withhold,
             gemm_timeline(ws), s)));
         return cuda_status(launch_combine(ws.f32(L.o), idx, w, T, H, E, k, y, ep, sms, s));
     }

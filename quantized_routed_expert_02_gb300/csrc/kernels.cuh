@@ -72,7 +72,8 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
                               const int32_t *active,
                               const int32_t *nactive, __half *x16, __half *h16, float *obuf,
                               TcChunk *chunks, TcChunk *chunks_dn, unsigned int *ready, WsHeader *hdr,
-                              int num_sms, unsigned long long wait_ns, unsigned long long *timeline,
+                              int num_sms, unsigned long long wait_ns, int withhold,
+                              unsigned long long *timeline,
                               cudaStream_t s);
 
 cudaError_t init_decode_fused(int dev, int num_sms);

@@ -113,6 +113,7 @@ struct Params {
     // once the count reaches ceil(slots / ready_cap) * ready_tiles * 16.
     unsigned int *ready;
     int ready_cap, ready_tiles;
+    int withhold;  // test hook: CTA 0 of the gate/up launch counts none of its pieces
 };
 
 // Optional per-stage timeline for profiling builds (-DMOEQ4K_TIMELINE): the
@@ -351,7 +352,7 @@ __device__ __noinline__ bool item_epilogue(const Params &p, const Item &E, uint3
             }
             }
             tc::fence_before_sync();
-            if (p.mode == 0 && p.ready != nullptr) {
+            if (p.mode == 0 && p.ready != nullptr && !(p.withhold && blockIdx.x == 0)) {
                 // this warp's h rows of the item are stored: visible GPU-wide
                 // before the count that the down launch acquires
                 __threadfence();
@@ -876,7 +877,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
                               const int32_t *active, const int32_t *nactive, __half *x16,
                               __half *h16, float *obuf, TcChunk *chunks, TcChunk *chunks_dn,
                               unsigned int *ready, WsHeader *hdr,
-                              int num_sms, unsigned long long wait_ns,
+                              int num_sms, unsigned long long wait_ns, int withhold,
                               unsigned long long *timeline, cudaStream_t s) {
     using namespace ptc;
     launch_pdl(gather_half_kernel, dim3(num_sms * 8), dim3(256), size_t(0), s, x, slotpos, T, k, H, x16,
@@ -903,6 +904,7 @@ cudaError_t launch_prefill_tc(int dev, const float *x, const uint8_t *gate, cons
     p.ready = ready;
     p.ready_cap = cap_gu;
     p.ready_tiles = I / kBM;
+    p.withhold = withhold;
     const int optin = g_tc_smem_optin[dev];
 
     // Shared memory: header, raw ring, weight-tile ring (1024-aligned), then

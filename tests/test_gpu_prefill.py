@@ -73,3 +73,34 @@ def test_caller_routing_beyond_chunk_capacity(m, oracle):
     assert m.moe_read_device_status(ws)[0] == 0
     y = d["y"].cpu().numpy().astype(np.float64)
     assert np.max(np.abs(y - yo)) <= y_tolerance(yo)
+
+
+def test_down_readiness_timeout_is_reported(m):
+    """The down GEMM waits per expert for the gate/up launch's count of
+    finished h rows.  With CTA 0 of the gate/up launch counting none of its
+    rows (test hook) that count never completes: the bounded wait runs out,
+    the call records MOE_ERR_TIMEOUT (at the readiness wait, or at the MMA
+    warp's wait for the same activation tile) instead of hanging, and the
+    workspace works again after re-initialisation."""
+    from tests.test_gpu_parity import DEV, to_dev
+    shape = synth.custom_shape(64, 512, 16, 8, 256, cfg_id=93)
+    s = shape
+    assert m.moe_layer_launch_count(s.T, s.H, s.E, s.k, s.I) == tensor_path_launches(s.T, s.k)
+    case = layer_case(shape, 0, (0, 31, 63))
+    d = to_dev(case)
+    ws = m.alloc_workspace(s.T, s.H, s.E, s.k, s.I, device=DEV)
+    try:
+        m.moe_debug_set_wait_limit(20_000_000)      # 20 ms
+        m.moe_debug_withhold_arrivals(1)
+        m.moe_layer(d["x"], d["Wr"], d["bias"], d["gate"], d["up"], d["down"], s.k, s.I,
+                    d["idx"], d["w"], d["y"], ws)
+        code, detail = m.moe_read_device_status(ws)
+        # 21: the readiness wait; 18: the MMA warp's wait for the same
+        # activation tile (both run out at the same deadline)
+        assert m.status_str(code) == "MOE_ERR_TIMEOUT" and detail in (18, 21), (code, detail)
+    finally:
+        m.moe_debug_withhold_arrivals(0)
+        m.moe_debug_set_wait_limit(0)
+    m.moe_workspace_init(ws)
+    idx, w, y, _, _ = run_layer(m, case, ws=ws)
+    check_layer(case, idx, w, y)
