@@ -179,6 +179,48 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return v;
 }
 
+// Distributed shared memory (thread-block clusters).  cluster_smem_addr:
+// the shared::cluster address of `p`'s offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_smem_addr(const void *p, int rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(p)), "r"(rank));
+    return ra;
+}
+
+// Asynchronous stores into CTA `rank` of the cluster (at the offset of `dst`
+// here), completing as 4 or 16 transaction bytes on that CTA's mbarrier at
+// the offset of `bar`; the registers are read at issue.
+__device__ __forceinline__ void st_async_u32(void *dst, uint32_t v, uint64_t *bar, int rank) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                     cluster_smem_addr(dst, rank)),
+                 "r"(v), "r"(cluster_smem_addr(bar, rank))
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_v4f(float *dst, float a, float b, float c, float d,
+                                             uint64_t *bar, int rank) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     cluster_smem_addr(dst, rank)),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_smem_addr(bar, rank))
+                 : "memory");
+}
+
+// Bounded wait for a phase completed by other CTAs of the cluster (acquire
+// at cluster scope).  Returns false on time-out.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t deadline) {
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_addr(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (global_timer_ns() > deadline) return false;
+    }
+}
+
 // Barrier over the first `nthreads` threads of the CTA (named barrier 1).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

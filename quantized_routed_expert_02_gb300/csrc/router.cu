@@ -29,12 +29,15 @@ namespace moeq4k {
 //    column of every token.  Each shared-memory byte is read about once.
 //  - Sums: a reduce-scatter over the eight column lanes (fixed butterfly),
 //    then the eight warps' partials added in warp order, plus the bias.
-//  - Exchange: warp t of every group CTA stores its logits of token t into
-//    the shared memory of CTA t of the cluster and arrives (release, cluster
-//    scope) on that CTA's barrier; CTA t waits for the eight arrivals.
-//  - Ranking: thread e counts the experts that beat expert e in the order
-//    (logit descending, index ascending); ranks below k name the selection
-//    in order, and one warp renormalises.
+//  - Exchange: warp t of every group CTA sends its logits of token t, and
+//    its failure flag, into the shared memory of CTA t of the cluster with
+//    st.async, completing as transaction bytes on CTA t's barrier; CTA t
+//    waits for its E + 8 words.
+//  - Ranking: the logits become order-preserving keys (logit_key: NaN below
+//    every number, as in warp_topk); a thread pair per expert (one thread
+//    above 128 experts) counts the experts that beat it in the order (key
+//    descending, index ascending); ranks below k name the selection in
+//    order, and one warp renormalises.
 // One launch, no logits in global memory, a fixed summation order.  Every
 // wait is bounded; a timed-out wait records MOE_ERR_TIMEOUT and the cluster
 // writes no routing for the tile.
@@ -84,35 +87,6 @@ __device__ __forceinline__ void cluster_arrive() {
 }
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Asynchronous store of one 32-bit word into the shared memory of CTA `rank`
-// of the cluster (at the offset of `dst` here), completing as 4 transaction
-// bytes on that CTA's mbarrier at the offset of `bar`.
-__device__ __forceinline__ void st_async_remote(void *dst, uint32_t v, uint64_t *bar, int rank) {
-    uint32_t ra, rb;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(dst)), "r"(rank));
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_addr(bar)), "r"(rank));
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra),
-                 "r"(v), "r"(rb)
-                 : "memory");
-}
-
-// Bounded wait for a phase completed by other CTAs of the cluster
-// (acquire at cluster scope).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t deadline) {
-    for (;;) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(smem_addr(bar)), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if (global_timer_ns() > deadline) return false;
-    }
 }
 
 // Sum each of the V values of a lane over the eight lanes that share
@@ -277,9 +251,9 @@ __global__ void __cluster_dims__(rcl::kCS, 1, 1) __launch_bounds__(256)
 #pragma unroll
             for (int v = 0; v < 8; ++v) sum += red[v * (kMaxEG * kMaxTT) + el * TT + t];
             sum += p.bias ? p.bias[e0 + el] : 0.f;
-            st_async_remote(inbox + e0 + el, __float_as_uint(sum), got, t);
+            st_async_u32(inbox + e0 + el, __float_as_uint(sum), got, t);
         }
-        if (lane == 0) st_async_remote(flags_in + r, bad ? 1u : 0u, got, t);
+        if (lane == 0) st_async_u32(flags_in + r, bad ? 1u : 0u, got, t);
     }
     if (r >= nt) return;  // no token of this tile is ranked here; nothing is sent to this CTA
     // CTA r ranks token t0 + r once the eight groups' logits are in

@@ -78,44 +78,6 @@ __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x,
         : "memory");
 }
 
-// 16-byte / 4-byte asynchronous stores into CTA `rank` of the cluster (at
-// the offset of `dst` here), completing as transaction bytes on that CTA's
-// mbarrier at the offset of `bar`.
-__device__ __forceinline__ uint32_t cluster_addr(const void *p, int rank) {
-    uint32_t ra;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(p)), "r"(rank));
-    return ra;
-}
-__device__ __forceinline__ void st_async_v4_remote(float *dst, float a, float b, float c, float d,
-                                                   uint64_t *bar, int rank) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                     cluster_addr(dst, rank)),
-                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_addr(bar, rank))
-                 : "memory");
-}
-__device__ __forceinline__ void st_async_u32_remote(uint32_t *dst, uint32_t v, uint64_t *bar, int rank) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
-                     cluster_addr(dst, rank)),
-                 "r"(v), "r"(cluster_addr(bar, rank))
-                 : "memory");
-}
-// Bounded wait for a phase completed by other CTAs of the cluster (acquire
-// at cluster scope).
-__device__ __forceinline__ bool mbar_wait_cluster_acq(uint64_t *bar, uint32_t parity, uint64_t deadline) {
-    for (;;) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(smem_addr(bar)), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if (global_timer_ns() > deadline) return false;
-    }
-}
-
 // hi(v) (low 13 significand bits cleared) and lo(v) = v - hi(v), four at once.
 __device__ __forceinline__ void split4(const float4 v, float4 &hi, float4 &lo) {
     hi.x = __uint_as_float(__float_as_uint(v.x) & 0xFFFFE000u);
@@ -308,14 +270,14 @@ __global__ void __cluster_dims__(1, kSplit, 1) __launch_bounds__(kThreads, 1)
         float *dst = recv + (size_t(r) * kTok + lane) * kPS + (warp >> 2) * 64;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            st_async_v4_remote(dst + 4 * j, racc[4 * j], racc[4 * j + 1], racc[4 * j + 2], racc[4 * j + 3],
+            st_async_v4f(dst + 4 * j, racc[4 * j], racc[4 * j + 1], racc[4 * j + 2], racc[4 * j + 3],
                                pgot, owner);
     }
     if (tid == 0)
 #pragma unroll
-        for (int q = 0; q < kSplit; ++q) st_async_u32_remote(flags_in + r, uint32_t(*failed), pgot, q);
+        for (int q = 0; q < kSplit; ++q) st_async_u32(flags_in + r, uint32_t(*failed), pgot, q);
     if (warp >= kSplitWarps) return;
-    const bool got = mbar_wait_cluster_acq(pgot, 0u, deadline + p.wait_ns);
+    const bool got = mbar_wait_cluster(pgot, 0u, deadline + p.wait_ns);
     bool any_failed = !got;
 #pragma unroll
     for (int q = 0; q < kSplit; ++q) any_failed |= flags_in[q] != 0u;
