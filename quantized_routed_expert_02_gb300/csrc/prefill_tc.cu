@@ -68,7 +68,6 @@ constexpr int kBK = 64;    // K per stage
 constexpr int kTileA = kBM * kBK * 2;
 constexpr int kBoxRows = 32;                   // activation rows per TMA box
 constexpr int kBoxB = kBoxRows * kBK * 2;
-constexpr int kActSlot = kBM * kBK * 2;        // activation tile: 128 rows x 64 K fp16
 constexpr int kStageSlot = 2 * kTileA;         // stage ring slot: the two weight tiles
 constexpr int kHead = 2048;  // barriers, item info, token list
 constexpr int kDeq = 512;      // warps 4-19
@@ -103,8 +102,9 @@ struct Params {
                                 //   32q..32q+15 of lane quadrant q)
     int ns, s_off;              // stage ring: slots, byte offset (slot = kStageSlot bytes)
     int nb, b_off, b_slot;      // activation ring: slots, byte offset, bytes per slot (the
-                                //   chunk capacity x 128 B; kActSlot - b_slot bytes of
-                                //   padding follow the last slot)
+                                //   chunk capacity x 128 B; mrows x 128 - b_slot bytes of
+                                //   padding follow the last slot, since the MMA reads mrows
+                                //   rows from a slot's start)
     unsigned long long wait_ns;
     unsigned long long *timeline;  // profiling builds only: per-stage role stamps of CTA 0
     // Per-expert count of finished gate/up epilogue pieces (one per
