@@ -104,3 +104,33 @@ def test_down_readiness_timeout_is_reported(m):
     m.moe_workspace_init(ws)
     idx, w, y, _, _ = run_layer(m, case, ws=ws)
     check_layer(case, idx, w, y)
+
+
+def test_caller_routing_invalid_experts_tensor_path(m, oracle):
+    """A caller's routing on the tensor-core path (48 tokens x 8 slots) with a
+    few expert indices outside [0, E): those slots take no sorted row, count
+    toward no expert's readiness and add nothing to y; the call records
+    MOE_ERR_EXPERT_RANGE and y matches the oracle, which skips them too."""
+    import torch
+    from tests.cases import y_tolerance
+    from tests.test_gpu_parity import DEV, to_dev
+    shape = synth.custom_shape(48, 512, 16, 8, 256, cfg_id=94)
+    assert m.moe_layer_launch_count(48, 512, 16, 8, 256) == tensor_path_launches(48, 8)
+    case = layer_case(shape, 0, (0, 1, 47))
+    rng = np.random.default_rng(94)
+    idx_np = rng.integers(0, 16, (48, 8)).astype(np.int32)
+    idx_np[3, 2] = -1
+    idx_np[17, 7] = 16
+    idx_np[40, 0] = 1000
+    w_np = rng.uniform(-1.0, 1.0, (48, 8)).astype(np.float32)
+    yo, skipped = oracle.ffn(case["x"], idx_np, w_np.astype(np.float64), case["blobs"]["gate"],
+                             case["blobs"]["up"], case["blobs"]["down"], shape.E, shape.I)
+    assert skipped == 3
+    d = to_dev(case)
+    ws = m.alloc_workspace(48, shape.H, shape.E, shape.k, shape.I, device=DEV)
+    m.moe_ffn(d["x"], torch.from_numpy(idx_np).to(DEV), torch.from_numpy(w_np).to(DEV),
+              d["gate"], d["up"], d["down"], shape.E, shape.I, d["y"], ws)
+    code, _ = m.moe_read_device_status(ws)
+    assert m.status_str(code) == "MOE_ERR_EXPERT_RANGE"
+    y = d["y"].cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(y - yo)) <= y_tolerance(yo)
