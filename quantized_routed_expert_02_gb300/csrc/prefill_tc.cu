@@ -25,9 +25,11 @@
 //               of each of the tile's rows per raw stage, 2 x 128 rows;
 //   warps 4-19  dequantise each raw stage into four 64-K stages of fp16
 //               K-major tiles with the 128-byte swizzle (generic stores, then
-//               a proxy fence), thread = (row, half of the stage's codes);
-//               after the first stages of the next item they run the
-//               previous item's epilogue;
+//               a proxy fence) in two groups of eight warps, group g taking
+//               the stages c % 2 == g (two stages written at once), thread =
+//               (row, operand): all 32 code bytes of its row per stage;
+//               each group runs its share of the previous item's epilogue
+//               after its last stage below the tile ring's depth;
 //   warp 2      the chunk's activation rows of each stage by TMA (boxes of 32
 //               rows, 128-byte swizzle) into a ring of chunk-sized slots;
 //   warp 0      issues tcgen05.mma with the tokens as the M operand:
@@ -411,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             mbar_init(rempty + i, kDeq / 32);  // one arrival per dequant warp
         }
         for (int i = 0; i < NS; ++i) {
-            mbar_init(sfull + i, kDeq / 32);   // one arrival per dequant warp
+            mbar_init(sfull + i, kDeq / 64);   // one arrival per warp of the stage's group
             mbar_init(sempty + i, 1);          // MMA completion
         }
         for (int i = 0; i < NB; ++i) {
@@ -449,21 +451,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     if (warp >= 4) {
         // ---- dequantise weight rows into the A tiles; after the first stages
         // of the next item, run the previous item's epilogue
-        // thread -> (row r of A operand m, half hh of the stage's 32 code bytes:
-        // words 4hh..4hh+3, i.e. tile chunks 2hh, 2hh+1 (low nibbles) and
-        // 2hh+4, 2hh+5 (high nibbles))
+        // two groups of eight warps (warps 4-11: hh = 0, 12-19: hh = 1); group
+        // hh dequantises the stages c of each raw block with c % 2 == hh, so
+        // two stages are being written at once; thread -> (row r of A operand
+        // m): all 32 code bytes of its row per stage, tile chunks 0-7
         const int dq = tid - 128;
         const int r = dq & 127;
         const int m = (dq >> 7) & 1;  // A operand: gate / up, or the first / second 128 rows
         const int hh = dq >> 8;
         const uint32_t rbase = smem_addr(rring) + uint32_t(m * kRawMat) + uint32_t(kBlockBytes) * r;
         const uint32_t til0 = smem_addr(sring) + uint32_t(m * kTileA);
-        // this thread's four tile chunks: 2hh, 2hh+1 (low nibbles), 2hh+4, 2hh+5 (high)
-        uint32_t soff[4];
-        soff[0] = tc::sw128_offset(r, 8 * (2 * hh));
-        soff[1] = tc::sw128_offset(r, 8 * (2 * hh + 1));
-        soff[2] = tc::sw128_offset(r, 8 * (2 * hh + 4));
-        soff[3] = tc::sw128_offset(r, 8 * (2 * hh + 5));
+        // the row's eight tile chunks: 0-3 from the low nibbles of code words
+        // 0-7, 4-7 from the high nibbles
+        uint32_t soff[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) soff[j] = tc::sw128_offset(r, 8 * j);
         const int q = warp & 3, part = (warp - 4) >> 2;  // TMEM lane quadrant, column quarter
 
         uint32_t g = 0, gr = 0, li = 0;
@@ -485,48 +487,46 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const uint4 head = lds128(rsl);
 #pragma unroll
                 for (int c = 0; c < kSub; ++c) {
+                    // group hh (warps 4-11: 0, 12-19: 1) dequantises the sub-stages
+                    // with c % 2 == hh, all 32 code bytes of its row each
                     const int s = sr * kSub + c;
-                    const uint32_t as = ap.slot;
-                    if (tid == 128) GT_STAMP(p, 1, g);
-                    // code bytes 32c..32c+31 of the block: low nibbles = sub-block
-                    // 2c (K 0..31 of the stage), high = 2c+1 (K 32..63)
-                    const uint4 qv = lds128(rsl + 16u + 32u * c + 16u * hh);
-                    if (c == kSub - 1) {
-                        // The TMA that refills this raw slot writes through the async
-                        // proxy: without a proxy fence after the reads, a refill could
-                        // land before reads still in flight are performed.
+                    const uint32_t as = ap.slot, aph = ap.phase;
+                    ap.next(NS);
+                    const uint32_t gcur = g++;
+                    if ((c & 1) != hh) continue;
+                    const uint4 q0 = lds128(rsl + 16u + 32u * c), q1 = lds128(rsl + 16u + 32u * c + 16u);
+                    if (c + 2 >= kSub) {
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(rempty + rs);
                     }
-                    if (g >= uint32_t(NS) && !nap_wait(sempty + as, ap.phase ^ 1u, deadline, p.hdr, 11)) {
+                    if (gcur >= uint32_t(NS) && !nap_wait(sempty + as, aph ^ 1u, deadline, p.hdr, 11)) {
                         ok = false;
                         break;
                     }
-                    if (tid == 128) GT_STAMP(p, 2, g);
                     __half2 A, NB;
                     stage_scales_h2(head, c, A, NB);
                     const __half2 a0 = __low2half2(A), a1 = __high2half2(A);
                     const __half2 n0 = __low2half2(NB), n1 = __high2half2(NB);
                     const uint32_t tile = til0 + as * uint32_t(kStageSlot);
-                    sts128(tile + soff[0], chunk8<0>(qv.x, qv.y, a0, n0));
-                    sts128(tile + soff[1], chunk8<0>(qv.z, qv.w, a0, n0));
-                    sts128(tile + soff[2], chunk8<4>(qv.x, qv.y, a1, n1));
-                    sts128(tile + soff[3], chunk8<4>(qv.z, qv.w, a1, n1));
+                    sts128(tile + soff[0], chunk8<0>(q0.x, q0.y, a0, n0));
+                    sts128(tile + soff[1], chunk8<0>(q0.z, q0.w, a0, n0));
+                    sts128(tile + soff[2], chunk8<0>(q1.x, q1.y, a0, n0));
+                    sts128(tile + soff[3], chunk8<0>(q1.z, q1.w, a0, n0));
+                    sts128(tile + soff[4], chunk8<4>(q0.x, q0.y, a1, n1));
+                    sts128(tile + soff[5], chunk8<4>(q0.z, q0.w, a1, n1));
+                    sts128(tile + soff[6], chunk8<4>(q1.x, q1.y, a1, n1));
+                    sts128(tile + soff[7], chunk8<4>(q1.z, q1.w, a1, n1));
                     fence_proxy_async_smem();
                     __syncwarp();
-                    // one lane also waits for the stage's activation tile, so the
-                    // slot's "full" phase implies both operands are in place
                     if (lane == 0) mbar_arrive(sfull + as);
-                    if (tid == 128) GT_STAMP(p, 3, g);
-                    ++g;
-                    ap.next(NS);
-                    if (have_prev && s == epi_at) {
-                        if (tid == 128) GT_STAMP(p, 9, li - 1);
+                    // this group's share of the previous item's epilogue, after its last
+                    // stage below the ring depth: every wait before it depends only on the
+                    // previous item's MMAs, and the next item's first MMA needs it
+                    if (have_prev && s + 2 >= epi_at + 1) {
                         if (!item_epilogue(p, prev, li - 1, nbuf, taddr, accfull, accempty, deadline,
                                            q, part, lane))
                             ok = false;
-                        if (tid == 128) GT_STAMP(p, 10, li - 1);
                         have_prev = false;
                     }
                 }
