@@ -494,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     ap.next(NS);
                     const uint32_t gcur = g++;
                     if ((c & 1) != hh) continue;
+                    if (tid == 128) GT_STAMP(p, 1, gcur);  // profiling builds: group 0's stages
                     const uint4 q0 = lds128(rsl + 16u + 32u * c), q1 = lds128(rsl + 16u + 32u * c + 16u);
                     if (c + 2 >= kSub) {
                         fence_proxy_async_smem();
@@ -504,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         ok = false;
                         break;
                     }
+                    if (tid == 128) GT_STAMP(p, 2, gcur);
                     __half2 A, NB;
                     stage_scales_h2(head, c, A, NB);
                     const __half2 a0 = __low2half2(A), a1 = __high2half2(A);
@@ -520,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(sfull + as);
+                    if (tid == 128) GT_STAMP(p, 3, gcur);
                     // this group's share of the previous item's epilogue, after its last
                     // stage below the ring depth: every wait before it depends only on the
                     // previous item's MMAs, and the next item's first MMA needs it
