@@ -163,7 +163,7 @@ moe_status layer_enqueue(const float *x, const float *norm_w, float eps, const f
             static_cast<const uint8_t *>(down), H, E, k, I, y, W.u64(L.sync), W.f32(L.h), W.hdr(),
             g_withhold, g_wait_ns, W.u64(L.o), W.timeline_cap(), s));
     }
-    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(), sms, s)));
+    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(), sms, g_wait_ns, s)));
     if (decode_stream_supported(dev, T, H, E, k, I)) {
         return cuda_status(launch_decode_stream(
             x, idx, w, static_cast<const uint8_t *>(gate), static_cast<const uint8_t *>(up),
@@ -290,7 +290,7 @@ moe_status moe_router(const float *x, const float *Wr, const float *bias, int T,
     MOE_TRY(device_info(&sms, nullptr));
     Ws W{static_cast<uint8_t *>(ws), L};
     return cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(),
-                                     sms, static_cast<cudaStream_t>(stream)));
+                                     sms, g_wait_ns, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_permute(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offs,
@@ -496,7 +496,7 @@ moe_status moe_layer_q8k(const float *x, const float *Wr, const float *bias, con
     MOE_TRY(device_info(&sms, nullptr));
     Ws W{static_cast<uint8_t *>(ws), L};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(), sms, s)));
+    MOE_TRY(cuda_status(launch_router(x, Wr, bias, T, H, E, k, idx, w, W.f32(L.logits), W.hdr(), sms, g_wait_ns, s)));
     return q8k_ffn_enqueue(x, idx, w, gate, up, down, T, H, E, k, I, y, W, sms, s);
 }
 

@@ -17,7 +17,7 @@ cudaError_t init_router();
 // `hdr` carries the one- and two-token router's running CTA count.
 cudaError_t launch_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
                           int k, int32_t *idx, float *w, float *logits, WsHeader *hdr, int num_sms,
-                          cudaStream_t s);
+                          unsigned long long wait_ns, cudaStream_t s);
 
 // Three launches (count, scan, scatter); blockcnt holds ceil(T*k / kPermSlots)
 // x E ints of scratch, slotpos receives each slot's sorted position.

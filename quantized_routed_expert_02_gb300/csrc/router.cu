@@ -497,7 +497,7 @@ cudaError_t init_router() {
 // a few tens of GB/s, so the tile stays small enough to spread over 64 SMs
 // or more (measured at 64 tokens: 8 tiles of 8 beat 16 tiles of 4 by 3 %
 // of the layer call, at 32 A22B tokens by 1.5 %).
-int router_tile_tokens(int T) {
+static int router_tile_tokens(int T) {
     for (int tt = 8; tt > 1; tt >>= 1)
         if ((T + tt - 1) / tt >= 8) return tt;
     return 1;
@@ -516,11 +516,11 @@ static void launch_cluster(int tt, dim3 grid, size_t smem, cudaStream_t s, const
 
 cudaError_t launch_router(const float *x, const float *Wr, const float *bias, int T, int H, int E,
                           int k, int32_t *idx, float *w, float *logits, WsHeader *hdr, int num_sms,
-                          cudaStream_t s) {
+                          unsigned long long wait_ns, cudaStream_t s) {
     dim3 blk(256);
     // T >= 256, E <= 128: tensor cores (three-pass TF32, router_tc.cu)
     if (router_tc_supported(T, H, E))
-        return launch_router_tc(x, Wr, bias, T, H, E, k, idx, w, hdr, 1000000000ull, s);
+        return launch_router_tc(x, Wr, bias, T, H, E, k, idx, w, hdr, wait_ns, s);
     if (T >= 256) {
         launch_pdl(router_big_kernel, dim3((T + kRT - 1) / kRT), dim3(blk), size_t(kRouterBigSmem), s, x, Wr, bias, T, H, E, k, idx, w);
         return cudaGetLastError();
@@ -549,7 +549,7 @@ cudaError_t launch_router(const float *x, const float *Wr, const float *bias, in
     p.idx = idx;
     p.w = w;
     p.hdr = hdr;
-    p.wait_ns = 1000000000ull;
+    p.wait_ns = wait_ns;
     const size_t smem = size_t(1024 + kHead) + size_t(nslots) * slot_bytes;
     const dim3 grid(kCS, tiles);
     if (EG <= 16)
