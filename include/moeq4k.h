@@ -116,12 +116,20 @@ MOE_API int moe_layer_launch_count(int T, int H, int E, int k, int I);
 MOE_API moe_status moe_workspace_init(void *ws_dev, size_t ws_bytes, void *stream);
 
 /*
- * Router (logits, softmax, top-k, renormalise) for T tokens.
+ * Router (logits, softmax, top-k, renormalise) for T tokens
+ * (forward_qwen3_moe_cuda_traced.rs, aprender-serve 0.34.0, doc of
+ * forward_qwen3_moe_cuda_traced_with_plan: the router stage is the k
+ * post-softmax, renormalised top-k weights of a token).
  *  x_dev [T,H] fp32, Wr_dev [E,H] fp32, bias_dev [E] fp32 or NULL.
- *  Writes idx_dev [T,k] int32 (descending logit, ties -> lowest index) and
- *  w_dev [T,k] fp32 (sums to 1 per token).  The workspace must have been
- *  initialised (moe_workspace_init); calls that share a workspace must not
- *  overlap on the GPU (true of every call taking a workspace).
+ *  Writes idx_dev [T,k] int32 (descending logit, ties -> lowest index; a
+ *  NaN logit ranks below every number) and w_dev [T,k] fp32 (sums to 1 per
+ *  token).  The logits are fp32 sums; from 256 tokens with E <= 128 they
+ *  come from the tensor cores as a three-pass tf32 split product
+ *  (hi.hi + lo.hi + hi.lo of each operand's exact hi/lo split, fp32
+ *  accumulation), within about 1e-6 of sum |x_h Wr_eh| of the fp32 value.
+ *  One launch at every T.  The workspace must have been initialised
+ *  (moe_workspace_init); calls that share a workspace must not overlap on
+ *  the GPU (true of every call taking a workspace).
  */
 MOE_API moe_status moe_router(const float *x_dev, const float *Wr_dev, const float *bias_dev,
                       int T, int H, int E, int k,
