@@ -92,8 +92,9 @@ MOE_API int moe_version(void);
  * workspace holds the sticky status word, call and work counters and a
  * 2 KB region of tagged router logits that single-token calls keep between
  * calls (both at the same place for every shape), the permutation, the
- * expert activations h [T*k, I], the per-slot outputs [T*k, H] and the
- * fp16 activation rows of the tensor-core path.
+ * expert activations h [T*k, I], the per-slot outputs [T*k, H], and the
+ * fp16 activation rows, chunk plans and per-expert readiness counts of the
+ * tensor-core path.
  */
 MOE_API size_t moe_workspace_bytes(int T, int H, int E, int k, int I);
 
