@@ -223,7 +223,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, const uint4 &v) {
                  : "memory");
 }
 
-// A bounded wait by every lane of a warp, with one verdict for the warp (a
+// A bounded wait by every lane of a warp, with one outcome for the warp (a
 // lane that saw the phase complete just as another hit the deadline still
 // takes the abort path with it), so the warp never splits at a __syncwarp.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t deadline,
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if (!ok) *abort_flag = 1;
     } else if (warp == 0) {
         // ---- MMA issue: accumulators of item li in buffer li % nbuf.  The
-        // whole warp walks the loop (waits by all lanes with one verdict);
+        // whole warp walks the loop (waits by all lanes with one outcome);
         // the elected lane issues the MMAs and their commits.
         const bool leader = elect_one();
         uint32_t g = 0, li = 0;
