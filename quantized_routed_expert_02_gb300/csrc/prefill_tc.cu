@@ -353,7 +353,12 @@ __device__ __noinline__ bool item_epilogue(const Params &p, const Item &E, uint3
                 }
             }
             }
+            // every lane's tensor-memory loads have completed (each load waits for
+            // its values): the next item's MMAs may overwrite the accumulator
+            // while this warp's h rows are still being made visible below
             tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(accempty + buf);
             if (p.mode == 0 && p.ready != nullptr && !(p.withhold && blockIdx.x == 0)) {
                 // this warp's h rows of the item are stored: visible GPU-wide
                 // before the count that the down launch acquires
@@ -362,7 +367,6 @@ __device__ __noinline__ bool item_epilogue(const Params &p, const Item &E, uint3
                 if (lane == 0) red_release_add_u32(p.ready + E.ch.e, 1u);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(accempty + buf);
             return true;
         }
 
