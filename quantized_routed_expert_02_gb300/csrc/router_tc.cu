@@ -18,19 +18,22 @@
 //
 // A cluster of four CTAs per tile of 128 tokens, CTA r taking the K quarter
 // r.  Per 32-K stage: TMA brings the x and Wr tiles (128 rows x 128 bytes,
-// 128-byte swizzle) into a five-slot ring; every thread splits its share of
-// the two tiles in place (hi back into the tile, lo into one of two lo
-// buffers: the split is elementwise, so the swizzled layout carries over);
-// thread 0 issues twelve MMAs (M = 128 tokens, N = 128 experts, K = 8 each)
-// into the stage's own accumulator and commits.  Stage st's accumulator is
-// added into fp32 registers during stage st + 2 (three accumulators), so the
-// tensor pipe runs two stages behind the split.  The four partial tiles meet
-// through distributed shared memory: CTA r loads the quarters of its 32
-// tokens (every load issued before the first sum), adds them in rank order
-// with the bias and ranks each token with one warp, from registers.  Fixed
-// MMA and reduction order: deterministic.  Every wait is bounded by a
-// global-timer deadline; a timed-out wait records MOE_ERR_TIMEOUT and the
-// cluster writes no routing.
+// 128-byte swizzle) into a five-slot ring; eight split warps split the two
+// tiles in place (hi back into the tile, lo into one of two lo buffers: the
+// split is elementwise, so the swizzled layout carries over) and arrive on
+// the slot's barrier; a ninth warp, one elected lane issuing, waits for that
+// barrier and issues twelve MMAs (M = 128 tokens, N = 128 experts, K = 8
+// each) into the stage's own accumulator, then commits.  Stage st's
+// accumulator is added into fp32 registers by the split warps during stage
+// st + 2 (three accumulators), so the tensor pipe runs up to two stages
+// behind the split, and no CTA-wide barrier sits in the loop.  The four
+// partial tiles then meet in the owner's shared memory: each split warp
+// pushes its rows of another CTA's 32 tokens there with 16-byte
+// asynchronous stores that complete on the owner's barrier, and CTA r adds
+// the quarters of its tokens in rank order with the bias and ranks each
+// token with one warp, from registers.  Fixed MMA and reduction order:
+// deterministic.  Every wait is bounded by a global-timer deadline; a
+// timed-out wait records MOE_ERR_TIMEOUT and the cluster writes no routing.
 #include <cooperative_groups.h>
 #include <cuda.h>
 
