@@ -432,8 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         *abort_flag = 0;
         fence_mbar_init();
     }
-    // the activation ring starts as zeros: the MMA reads all 128 rows of a
-    // slot, and rows no copy has written must hold finite values
     // the activation ring (and the padding after it) starts as zeros: the MMA
     // reads 128 rows from a slot's start, and rows no copy has written must
     // hold finite values
