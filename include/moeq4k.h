@@ -169,7 +169,10 @@ MOE_API moe_status moe_ffn(const float *x_dev, const int32_t *idx_dev, const flo
 
 /*
  * The whole layer: moe_router then moe_ffn.  idx_dev / w_dev receive the
- * routing (the router stage), y_dev the output stage.
+ * routing (the router stage), y_dev the output stage.  One difference from
+ * moe_router, for a single token on the fused kernel: a NaN logit ranks
+ * with -inf (below every finite logit, ties to the lowest index) rather
+ * than below -inf.
  */
 MOE_API moe_status moe_layer(const float *x_dev, const float *Wr_dev, const float *bias_dev,
                      const void *gate_dev, const void *up_dev, const void *down_dev,
