@@ -282,7 +282,7 @@ def oracle_sample(name, seconds, rank=0, threads=0, max_tokens=64, inputs=None, 
         "kind": "oracle",
         "sample": (f"{calls} layer call(s) of {name}{' (Q8_K activations)' if q8k else ''} (T={T}"
                    + (f", FFN on {ntok} of {T} tokens, router on all" if tokens is not None else "")
-                   + f"), fp64 C oracle on {used} thread(s), {t_total:.1f} s"),
+                   + f"), fp64 C oracle on {used} thread(s), {t_total:.3g} s"),
     }
 
 
