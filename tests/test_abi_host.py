@@ -135,3 +135,107 @@ def test_layer_host_null(lib):
     r = f(P(None), P(ALIGNED), P(None), P(ALIGNED), P(ALIGNED), P(ALIGNED), 1, 2048, 128, 8, 768,
           P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), ctypes.c_size_t(1 << 40), P(None))
     assert r == 2
+
+
+def _fn(lib, name):
+    f = getattr(lib, name)
+    f.restype = ctypes.c_int
+    return f
+
+
+def test_layer_errors(lib):
+    """moe_layer: shape, null, alignment and workspace errors, in that order."""
+    P, S = ctypes.c_void_p, ctypes.c_size_t
+    f = _fn(lib, "moe_layer")
+
+    def call(x=ALIGNED, bias=None, y=ALIGNED, T=1, k=8, ws=ALIGNED, ws_bytes=1 << 40):
+        return f(P(x), P(ALIGNED), P(bias), P(ALIGNED), P(ALIGNED), P(ALIGNED), T, 2048, 128, k,
+                 768, P(ALIGNED), P(ALIGNED), P(y), P(ws), S(ws_bytes), P(None))
+    assert call(T=0) == 1
+    assert call(k=0) == 1
+    assert call(x=0) == 2
+    assert call(y=0) == 2
+    assert call(x=ALIGNED + 8) == 3
+    assert call(bias=ALIGNED + 4) == 3
+    assert call(ws=0) == 2
+    assert call(ws=ALIGNED + 16) == 3          # the workspace is 256-byte aligned
+    assert call(ws_bytes=1024) == 4
+
+
+def test_layer_block_errors(lib):
+    """moe_layer_block: eps must be finite and >= 0, capture_token in [-1, T),
+    the capture buffers aligned."""
+    P, S = ctypes.c_void_p, ctypes.c_size_t
+    f = _fn(lib, "moe_layer_block")
+
+    def call(eps=1e-6, cap=-1, cap_idx=None, cap_ffn=None, norm_w=None, T=2):
+        return f(P(ALIGNED), P(norm_w), ctypes.c_float(eps), P(ALIGNED), P(None), P(ALIGNED),
+                 P(ALIGNED), P(ALIGNED), T, 2048, 128, 8, 768, P(ALIGNED), P(ALIGNED), P(ALIGNED),
+                 1, cap, P(cap_idx), P(None), P(cap_ffn), P(ALIGNED), S(1024), P(None))
+    assert call(eps=-1.0) == 1
+    assert call(eps=float("nan")) == 1
+    assert call(eps=float("inf")) == 1
+    assert call(cap=-2) == 1
+    assert call(cap=2) == 1                     # T = 2: tokens 0 and 1
+    assert call(norm_w=ALIGNED + 4) == 3
+    assert call(cap=0, cap_idx=ALIGNED + 2) == 3
+    assert call(cap=0, cap_ffn=ALIGNED + 4) == 3
+    assert call(cap=1) == 4                     # valid so far; the 1 KB workspace is too small
+
+
+def test_permute_errors(lib):
+    P, S = ctypes.c_void_p, ctypes.c_size_t
+    f = _fn(lib, "moe_permute")
+
+    def call(idx=ALIGNED, T=5, k=4, E=16, perm=ALIGNED, ws_bytes=1 << 40):
+        return f(P(idx), T, k, E, P(ALIGNED), P(ALIGNED), P(perm), P(ALIGNED), S(ws_bytes), P(None))
+    assert call(T=0) == 1
+    assert call(k=17) == 1                      # k > E
+    assert call(idx=0) == 2
+    assert call(perm=ALIGNED + 4) == 3
+    assert call(ws_bytes=16) == 4
+
+
+def test_workspace_init_errors(lib):
+    P, S = ctypes.c_void_p, ctypes.c_size_t
+    f = _fn(lib, "moe_workspace_init")
+    assert f(P(None), S(1 << 20), P(None)) == 2
+    assert f(P(ALIGNED + 128), S(1 << 20), P(None)) == 3
+    assert f(P(ALIGNED), S(8), P(None)) == 4
+
+
+def test_q8k_errors(lib):
+    P, S = ctypes.c_void_p, ctypes.c_size_t
+    q = _fn(lib, "moe_quantize_q8k")
+    assert q(P(ALIGNED), 0, 256, P(ALIGNED), P(ALIGNED), P(ALIGNED), P(None)) == 1
+    assert q(P(ALIGNED), 2, 300, P(ALIGNED), P(ALIGNED), P(ALIGNED), P(None)) == 1  # n % 256
+    assert q(P(None), 2, 256, P(ALIGNED), P(ALIGNED), P(ALIGNED), P(None)) == 2
+    assert q(P(ALIGNED + 4), 2, 256, P(ALIGNED), P(ALIGNED), P(ALIGNED), P(None)) == 3
+    for name in ("moe_ffn_q8k", "moe_layer_q8k"):
+        f = _fn(lib, name)
+        if name == "moe_ffn_q8k":
+            call = lambda x=ALIGNED, T=1, ws_bytes=1 << 40: f(  # noqa: E731
+                P(x), P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), T, 2048, 128, 8,
+                768, P(ALIGNED), P(ALIGNED), S(ws_bytes), P(None))
+        else:
+            call = lambda x=ALIGNED, T=1, ws_bytes=1 << 40: f(  # noqa: E731
+                P(x), P(ALIGNED), P(None), P(ALIGNED), P(ALIGNED), P(ALIGNED), T, 2048, 128, 8,
+                768, P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), S(ws_bytes), P(None))
+        assert call(T=0) == 1, name
+        assert call(x=0) == 2, name
+        assert call(x=ALIGNED + 4) == 3, name
+        assert call(ws_bytes=1024) == 4, name
+
+
+def test_noalloc_errors(lib):
+    """moe_layer_noalloc: one token only, k*I within the fixed scratch."""
+    P = ctypes.c_void_p
+    f = _fn(lib, "moe_layer_noalloc")
+
+    def call(T=1, k=8, I=768, E=128, x=ALIGNED):
+        return f(P(x), P(ALIGNED), P(None), P(ALIGNED), P(ALIGNED), P(ALIGNED), T, 2048, E, k, I,
+                 P(ALIGNED), P(ALIGNED), P(ALIGNED), P(None))
+    assert call(T=2) == 1
+    assert call(k=32, I=4096) == 9               # k*I above the scratch limit
+    assert call(x=0) == 2
+    assert call(x=ALIGNED + 4) == 3
