@@ -17,7 +17,9 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "q4k_blocks.json")
 
 
 def _silu(z):
-    return z / (1.0 + np.exp(-z))
+    # exp(-z) overflows to inf for very negative z, and z / inf is the limit 0
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
 
 
 # ---------------------------------------------------------------- Q4_K decode
