@@ -45,8 +45,9 @@
 // the digits leave 6.1e-8 of the run's max|x|, the fp32 scalings add a few
 // ulps of x: below 2.5e-7 of the run's max|x| in all).  A 4-bit code times a
 // digit word is then one dp4a (four exact 8-bit products summed in int32),
-// and the fp32 scales of the block are applied once per sub-block.  Other
-// shapes, and all down rows, dot fp32 vectors in shared memory.
+// and the fp32 scales of the block are applied once per sub-block; with
+// I = 768 or 1024 h takes the same form for the down rows.  Other shapes dot
+// fp32 vectors in shared memory.
 #include <algorithm>
 
 #include "async_copy.cuh"
