@@ -138,7 +138,10 @@ MOE_API moe_status moe_router(const float *x_dev, const float *Wr_dev, const flo
                       void *ws_dev, size_t ws_bytes, void *stream);
 
 /*
- * Token->expert permutation of a routing: counts_dev [E], offs_dev [E+1]
+ * Token->expert permutation of a routing (the pages run the layer one
+ * position at a time, forward_qwen3_moe.rs, aprender-serve 0.35.0, step 2g
+ * of forward_qwen3_moe; grouping a batch's slots by expert lets each
+ * expert's bytes stream once per call): counts_dev [E], offs_dev [E+1]
  * (exclusive prefix sum of counts) and perm_dev [T*k] = slot ids p = t*k+j
  * grouped by expert, ascending p within an expert (stable).  Slots whose
  * expert index is outside [0,E) are left out (perm has offs[E] valid
@@ -168,8 +171,10 @@ MOE_API moe_status moe_ffn(const float *x_dev, const int32_t *idx_dev, const flo
                    void *ws_dev, size_t ws_bytes, void *stream);
 
 /*
- * The whole layer: moe_router then moe_ffn.  idx_dev / w_dev receive the
- * routing (the router stage), y_dev the output stage.  One difference from
+ * The whole layer: moe_router then moe_ffn (forward_qwen3_moe.rs,
+ * aprender-serve 0.35.0, step 2h of forward_single_qwen3_moe_with_cache and
+ * of forward_qwen3_moe: route, then the weighted SwiGLU experts).  idx_dev
+ * / w_dev receive the routing (the router stage), y_dev the output stage.  One difference from
  * moe_router, for a single token on the fused kernel: a NaN logit ranks
  * with -inf (below every finite logit, ties to the lowest index) rather
  * than below -inf.
